@@ -1,0 +1,88 @@
+/*
+ * msa_oracle.h -- plain fp64 CPU oracle for the block-sparse paged decode path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check
+ * and the benchmark's CPU-baseline leg may load this library.  It shares no
+ * code, header, table or helper with the CUDA library: it is written
+ * straight from the definitions on the MiniMax-M3 sparse-attention pages
+ * (vLLM PR 47287 "Add ROCm AITER sparse paged attention for MiniMax-M3",
+ * PR 54682 "Optimise MiniMax-M3 decode index and top-k on gfx950",
+ * PR 54404 "Attention sinks for ROCm AITER sparse MLA", PR 56170 "device
+ * zeroing of cu_seqlens_k[0]") and the OCP FP8 format definition.
+ *
+ * All arrays are host memory, row-major, owned by the caller.
+ *   bf16 tensors : uint16_t bit patterns
+ *   fp8 tensors  : uint8_t OCP e4m3fn codes
+ */
+#ifndef MSA_ORACLE_H
+#define MSA_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status bits (the same meaning as the library's device status word) */
+#define ORC_BAD_PAGE 1u    /* block-table page id outside [0, P) */
+#define ORC_BAD_LEN 2u     /* context_len + q_len != seq_len */
+#define ORC_MALFORMED 4u   /* malformed cu_seqlens / lengths beyond the table */
+#define ORC_BAD_TABLE 8u   /* sparse-table entry outside the page-16 pool */
+
+typedef struct {
+  int32_t num_reqs;             /* R */
+  int32_t num_rows;             /* N */
+  const int32_t* cu_seqlens_q;  /* [R+1] */
+  const int32_t* cu_seqlens_k;  /* [R+1] */
+  const int32_t* context_lens;  /* [R] */
+  const int32_t* block_table;   /* [R, bt_stride] page-128 ids */
+  int32_t bt_stride;
+  int32_t num_pages;            /* P */
+} orc_batch;
+
+/* Value of one OCP e4m3fn code (bias 7, no infinities, S.1111.111 = NaN). */
+double orc_fp8_e4m3_value(uint8_t code);
+/* Value of one bf16 bit pattern. */
+double orc_bf16_value(uint16_t bits);
+
+/* Per-row geometry.  req[r] = owning request or -1, pos[r] = absolute
+ * position, nb[r] = ceil((pos+1)/128), ok[r] = 1 unless the row is poisoned.
+ * Returns the status bits the batch raises. */
+uint32_t orc_row_geometry(const orc_batch* b, int32_t* req, int32_t* pos, int32_t* nb,
+                          int32_t* ok);
+
+/* Step 1: block scores.  scores[r, b] for b < nb[r] = max over index heads and
+ * over tokens t of block b with t <= pos[r] of sum_d qidx[r,h,d]*kidx[t,h,d],
+ * accumulated in fp64 and rounded to fp32; -inf for b >= nb[r], for blocks
+ * whose page id is out of range and for every block of a poisoned row. */
+uint32_t orc_index_score(const orc_batch* b, const uint16_t* idx_q, const uint16_t* idx_k,
+                         int32_t index_heads, int32_t index_dim, float* scores,
+                         int32_t score_stride, int32_t nthreads);
+
+/* Steps 2+3: top-k (ties to the lower block, output ascending by block) and
+ * page-16 table expansion with the context-length clamp. */
+uint32_t orc_topk_build_table(const orc_batch* b, const float* scores, int32_t score_stride,
+                              int32_t topk, int32_t* topk_idx, int32_t* sparse_tbl,
+                              int32_t tbl_stride, int32_t* sparse_len, int32_t nthreads);
+
+/* Step 4: GQA attention over the tokens the page-16 table addresses, with
+ * optional dequant scales and sink.  out [N,Hq,D] and lse [N,Hq] in fp64. */
+uint32_t orc_sparse_attn(int32_t num_rows, int32_t hq, int32_t hkv, int32_t head_dim,
+                         const uint16_t* q, const void* k_cache, const void* v_cache,
+                         int32_t kv_dtype, int32_t num_pages16, int32_t scale_mode,
+                         const float* k_scale, const float* v_scale, const int32_t* sparse_tbl,
+                         int32_t tbl_stride, const int32_t* sparse_len, const float* sinks,
+                         double softmax_scale, double* out, double* lse, int32_t nthreads);
+
+/* Dense attention over every visible token t < pos[r]+1 through the page-128
+ * block table (no index, no selection); the identity the sparse path reduces
+ * to when top-k covers every block. */
+uint32_t orc_dense_attn(const orc_batch* b, int32_t hq, int32_t hkv, int32_t head_dim,
+                        const uint16_t* q, const void* k_cache, const void* v_cache,
+                        int32_t kv_dtype, int32_t scale_mode, const float* k_scale,
+                        const float* v_scale, const float* sinks, double softmax_scale,
+                        double* out, double* lse, int32_t nthreads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

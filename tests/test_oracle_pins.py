@@ -1,0 +1,472 @@
+"""Pins for the CPU oracle: checks against facts that do not come from the
+oracle itself -- the FP8 format definition, hand-worked examples, closed
+forms, brute force on tiny inputs, library routines (numpy matmul, torch
+SDPA in float64) and invariances.  A plausible slip anywhere in the oracle
+(a dropped sink term, a wrong causal bound, a transposed operand, a wrong
+tie rule) fails at least one of these.
+
+Definitions cited (MiniMax-M3 sparse-attention pages): vLLM PR 47287 page
+"Implementation breakdown" items 2-3 (page-16 table, FP8 scales); PR 54682
+page "Implementation breakdown" item 1 (top-k fused with the page-16 table
+and context length); PR 54404 page "Features and motivation" / "Key source
+snippets" (sinks, natural-log LSE); PR 56170 page "Key source snippets"
+(128-token blocks, cu_seqlens).
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+NEG_INF = -np.inf
+
+
+# ---------------------------------------------------------------- formats
+
+def test_fp8_golden_values(orc):
+    with open(os.path.join(GOLDEN, "fp8_e4m3_values.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(rows) >= 20
+    for code, val in rows:
+        got = orc.fp8_e4m3_value(int(code, 16))
+        if val == "nan":
+            assert math.isnan(got), code
+        else:
+            assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val)), code
+
+
+def test_fp8_all_codes_match_torch(orc):
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([orc.fp8_e4m3_value(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+
+
+def test_bf16_values_match_torch(orc):
+    rng = np.random.default_rng(0)
+    bits = rng.integers(0, 1 << 16, size=2000, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([orc.bf16_value(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+
+
+# --------------------------------------------------------------- geometry
+
+def _batch(orc, q_lens, seq_lens, bt, num_pages, context=None):
+    q_lens = np.asarray(q_lens)
+    seq_lens = np.asarray(seq_lens)
+    cu_q = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(seq_lens)]).astype(np.int32)
+    ctx = (seq_lens - q_lens) if context is None else np.asarray(context)
+    return orc.Batch(cu_q, cu_k, ctx, np.asarray(bt, np.int32), num_pages)
+
+
+def test_geometry_speculative_rows(orc):
+    # 4 speculative rows of a request of length L sit at L-4 .. L-1
+    b = _batch(orc, [4, 1], [258, 128], [[0, 1, 2], [3, -1, -1]], 4)
+    g = orc.row_geometry(b)
+    assert g["status"] == 0
+    assert list(g["req"]) == [0, 0, 0, 0, 1]
+    assert list(g["pos"]) == [254, 255, 256, 257, 127]
+    assert list(g["nb"]) == [2, 2, 3, 3, 1]
+    assert list(g["ok"]) == [1, 1, 1, 1, 1]
+
+
+def test_geometry_errors(orc):
+    # length mismatch (context + q_len != seq_len)
+    b = _batch(orc, [1], [200], [[0, 1]], 2, context=[150])
+    g = orc.row_geometry(b)
+    assert g["status"] == orc.BAD_LEN and list(g["ok"]) == [0]
+    # page id out of range in a block the request covers
+    b = _batch(orc, [1], [200], [[0, 9]], 2)
+    g = orc.row_geometry(b)
+    assert g["status"] == orc.BAD_PAGE and list(g["ok"]) == [2]
+    # an out-of-range id beyond the request's blocks is never looked at
+    b = _batch(orc, [1], [100], [[0, 9]], 2)
+    assert orc.row_geometry(b)["status"] == 0
+    # sequence longer than the block table can address
+    b = _batch(orc, [1], [300], [[0, 1]], 4)
+    assert orc.row_geometry(b)["status"] == orc.MALFORMED
+    # cu_seqlens_q that does not tile the rows
+    b = orc.Batch(np.array([0, 2], np.int32), np.array([0, 10], np.int32),
+                  np.array([8], np.int32), np.zeros((1, 1), np.int32), 1)
+    b.s.num_rows = 3
+    b.num_rows = 3
+    assert orc.row_geometry(b)["status"] == orc.MALFORMED
+
+
+# ------------------------------------------------------------ index score
+
+def _planted_index_case():
+    """One request, L = 1000 (8 blocks, last 104 tokens), Di = 64, q = e_0.
+    Every index-K vector is 0 except dim 0 of a few planted tokens, so block
+    b's score is max(0, planted values of b that sit at t <= 999)."""
+    L, di = 1000, 64
+    perm = np.array([5, 2, 7, 0, 6, 1, 3, 4], np.int32)
+    kf = np.zeros((8, 128, 1, di), np.float32)
+    planted = {0: [(3, 4.0)], 1: [(127, 9.0), (5, 2.0)], 2: [(0, -5.0)],  # block 2: all <= 0 -> 0
+               3: [(64, 1.0)], 4: [], 5: [(100, 7.0)], 6: [(1, 3.0)],
+               7: [(103, 6.0), (104, 50.0), (127, 60.0)]}  # 104+ lie past the last token
+    for blk, items in planted.items():
+        for tl, v in items:
+            kf[perm[blk], tl, 0, 0] = v
+    expected = np.array([4, 9, 0, 1, 0, 7, 3, 6], np.float32)
+    qf = np.zeros((1, 1, di), np.float32)
+    qf[0, 0, 0] = 1.0
+    return L, perm, W.bf16_bits(qf), W.bf16_bits(kf), expected
+
+
+def test_index_score_planted(orc):
+    L, perm, q, k, expected = _planted_index_case()
+    b = _batch(orc, [1], [L], perm[None, :], 8)
+    scores, st = orc.index_score(b, q, k, score_stride=10)
+    assert st == 0
+    assert np.array_equal(scores[0, :8], expected)
+    assert np.all(scores[0, 8:] == NEG_INF)
+
+
+def test_index_score_planted_causal_rows(orc):
+    # three rows at positions 997..999: the token at 999 (block 7, slot 103)
+    # is visible only to the last row
+    L, perm, q, k, _ = _planted_index_case()
+    b = _batch(orc, [3], [L], perm[None, :], 8)
+    scores, _ = orc.index_score(b, np.repeat(q, 3, axis=0), k)
+    assert list(scores[:, 7]) == [0.0, 0.0, 6.0]
+
+
+def _dense_index_scores(w):
+    """numpy reference: gather each request's index-K through the block table,
+    matmul in float64, mask future tokens, max within each 128-token block."""
+    to_f = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).double().numpy()
+    qf, kf = to_f(w.idx_q), to_f(w.idx_k)
+    out = np.full((w.num_rows, w.bt_stride), NEG_INF)
+    for r in range(w.num_reqs):
+        L = int(w.seq_lens[r])
+        nb = -(-L // 128)
+        pages = w.block_table[r, :nb]
+        K = kf[pages].reshape(nb * 128, w.index_heads, w.index_dim)
+        for j in range(int(w.q_lens[r])):
+            row = int(w.cu_seqlens_q[r]) + j
+            pos = int(w.context_lens[r]) + j
+            s = np.einsum("hd,thd->th", qf[row], K).max(axis=1)  # max over index heads
+            s[pos + 1:] = NEG_INF
+            out[row, : -(-(pos + 1) // 128)] = s.reshape(nb, 128).max(axis=1)[: -(-(pos + 1) // 128)]
+    return out
+
+
+@pytest.mark.parametrize("hi,di", [(1, 64), (2, 64), (1, 128)])
+def test_index_score_matches_matmul(orc, hi, di):
+    w = W.custom(11, q_lens=[1, 4, 3], seq_lens=[700, 1029, 130], hq=4, di=di, hi=hi, topk=3)
+    b = orc.Batch.of(w)
+    scores, st = orc.index_score(b, w.idx_q, w.idx_k)
+    assert st == 0
+    ref = _dense_index_scores(w)
+    assert np.array_equal(scores.astype(np.float64), ref)
+
+
+def test_index_score_ignores_garbage(orc):
+    # NaN in unused slots and pages must not reach any score
+    w = W.custom(12, q_lens=[1, 2], seq_lens=[300, 513], hq=4, di=64, topk=2, fill_unused_nan=True)
+    scores, st = orc.index_score(orc.Batch.of(w), w.idx_q, w.idx_k)
+    g = orc.row_geometry(orc.Batch.of(w))
+    for r in range(w.num_rows):
+        assert np.all(np.isfinite(scores[r, : g["nb"][r]]))
+
+
+# ------------------------------------------------------------------ top-k
+
+def _one_row_batch(orc, L, nblocks, num_pages=None):
+    bt = np.arange(nblocks, dtype=np.int32)[None, :]
+    return _batch(orc, [1], [L], bt, num_pages or nblocks)
+
+
+def test_topk_brute_force_with_ties(orc):
+    """For tiny rows, enumerate every subset of size min(k, n) and keep the
+    ones where each selected block beats each unselected block under
+    (higher score, then lower index).  Exactly one subset qualifies; the
+    oracle must return it in ascending order."""
+    rng = np.random.default_rng(5)
+    for trial in range(150):
+        n = int(rng.integers(1, 9))
+        k = int(rng.integers(1, 7))
+        L = 128 * (n - 1) + int(rng.integers(1, 129))
+        sc = rng.integers(0, 3, size=n).astype(np.float32)  # heavy ties
+        b = _one_row_batch(orc, L, n)
+        sel, tbl, slen, st = orc.topk_build_table(b, sc[None, :], k)
+        m = min(k, n)
+        beats = lambda a, c: sc[a] > sc[c] or (sc[a] == sc[c] and a < c)
+        good = [S for S in itertools.combinations(range(n), m)
+                if all(beats(a, c) for a in S for c in set(range(n)) - set(S))]
+        assert len(good) == 1
+        assert list(sel[0, :m]) == list(good[0])
+        assert np.all(sel[0, m:] == -1)
+
+
+def test_topk_nan_ranks_last(orc):
+    sc = np.array([[np.nan, 1.0, np.nan, -np.inf, 0.5]], np.float32)
+    b = _one_row_batch(orc, 5 * 128, 5)
+    sel, *_ = orc.topk_build_table(b, sc, 3)
+    assert list(sel[0]) == [1, 3, 4]
+    sel, *_ = orc.topk_build_table(b, sc, 4)
+    assert list(sel[0]) == [0, 1, 3, 4]
+
+
+def test_table_golden_example(orc):
+    with open(os.path.join(GOLDEN, "table_example.txt")) as f:
+        kv = {ln.split()[0]: [int(x) for x in ln.split()[1:]]
+              for ln in f if ln.strip() and not ln.startswith("#")}
+    L = kv["L"][0]
+    bt = np.array(kv["block_table"], np.int32)[None, :]
+    b = _batch(orc, [1], [L], bt, 8)
+    sc = np.array([[5, 7, 3, 3, 3, 7, 5, 7]], np.float32)  # ties: 5 at blocks 0 and 6 -> 0 wins
+    sel, tbl, slen, st = orc.topk_build_table(b, sc, 4, tbl_stride=40)
+    assert st == 0
+    assert list(sel[0]) == kv["selected"]
+    assert list(tbl[0]) == kv["table"]
+    assert int(slen[0]) == kv["sparse_len"][0]
+
+
+def test_table_all_blocks_closed_form(orc):
+    # k >= number of blocks: every block is selected, the length is the whole
+    # visible length and the table is the block table expanded in order
+    w = W.custom(13, q_lens=[1, 4], seq_lens=[1000, 385], hq=4, di=64, topk=8)
+    b = orc.Batch.of(w)
+    scores, _ = orc.index_score(b, w.idx_q, w.idx_k)
+    sel, tbl, slen, st = orc.topk_build_table(b, scores, 8, tbl_stride=70)
+    g = orc.row_geometry(b)
+    for r in range(w.num_rows):
+        L = g["pos"][r] + 1
+        assert slen[r] == L
+        pages = w.block_table[g["req"][r]]
+        exp = []
+        for blk in range(-(-L // 128)):
+            sub = -(-min(128, L - 128 * blk) // 16)
+            exp += [8 * int(pages[blk]) + j for j in range(sub)] + [0] * (8 - sub)
+        exp += [0] * (70 - len(exp))
+        assert list(tbl[r]) == exp
+
+
+def test_poisoned_rows_get_empty_tables(orc):
+    bt = np.array([[0, 7]], np.int32)  # page 7 is outside a 2-page pool
+    b = _batch(orc, [1], [200], bt, 2)
+    sc = np.zeros((1, 2), np.float32)
+    sel, tbl, slen, st = orc.topk_build_table(b, sc, 2)
+    assert st == orc.BAD_PAGE
+    assert np.all(sel == -1) and np.all(tbl == 0) and slen[0] == 0
+
+
+# -------------------------------------------------------------- attention
+
+def _f64(a, kv_dtype):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if kv_dtype == W.KV_FP8:
+        return t.view(torch.float8_e4m3fn).double().numpy()
+    return t.view(torch.int16).view(torch.bfloat16).double().numpy()
+
+
+def _sdpa_reference(w):
+    """torch SDPA (float64) over the dense visible tokens of each row, with the
+    dequant scales applied to K and V and the sink as one extra key whose
+    logit is the sink and whose value is zero.  LSE via torch.logsumexp."""
+    qf = _f64(w.q, W.KV_BF16)
+    kf = _f64(w.k_cache, w.kv_dtype)
+    vf = _f64(w.v_cache, w.kv_dtype)
+    P = w.num_pages
+    if w.scale_mode == W.SCALE_SCALAR:
+        kf = kf * float(w.k_scale[0])
+        vf = vf * float(w.v_scale[0])
+    elif w.scale_mode == W.SCALE_PER_TOKEN_HEAD:
+        kf = kf * w.k_scale.reshape(P, 128, w.hkv, 1)
+        vf = vf * w.v_scale.reshape(P, 128, w.hkv, 1)
+    out = np.zeros((w.num_rows, w.hq, w.head_dim))
+    lse = np.zeros((w.num_rows, w.hq))
+    group = w.hq // w.hkv
+    for r in range(w.num_reqs):
+        for j in range(int(w.q_lens[r])):
+            row = int(w.cu_seqlens_q[r]) + j
+            L = int(w.context_lens[r]) + j + 1
+            pages = w.block_table[r, : -(-L // 128)]
+            K = torch.from_numpy(kf[pages].reshape(-1, w.hkv, w.head_dim)[:L])
+            V = torch.from_numpy(vf[pages].reshape(-1, w.hkv, w.head_dim)[:L])
+            for h in range(w.hq):
+                kvh = h // group
+                qv = torch.from_numpy(qf[row, h])
+                Kh, Vh = K[:, kvh], V[:, kvh]
+                logits = (Kh @ qv) * w.softmax_scale
+                if w.sinks is not None:
+                    # a key whose logit is exactly the sink, carrying a zero value
+                    sink = float(w.sinks[h])
+                    ks = qv * (sink / (w.softmax_scale * float(qv @ qv)))
+                    Kh = torch.cat([Kh, ks[None]])
+                    Vh = torch.cat([Vh, torch.zeros(1, w.head_dim, dtype=torch.float64)])
+                    logits = torch.cat([logits, torch.tensor([sink], dtype=torch.float64)])
+                o = torch.nn.functional.scaled_dot_product_attention(
+                    qv[None, None, None], Kh[None, None], Vh[None, None], scale=w.softmax_scale)
+                out[row, h] = o[0, 0, 0].numpy()
+                lse[row, h] = float(torch.logsumexp(logits, 0))
+    return out, lse
+
+
+@pytest.mark.parametrize("kv_dtype,scale_mode,sink", [
+    (W.KV_BF16, W.SCALE_NONE, False), (W.KV_BF16, W.SCALE_NONE, True),
+    (W.KV_FP8, W.SCALE_SCALAR, True), (W.KV_FP8, W.SCALE_PER_TOKEN_HEAD, False)])
+def test_dense_attention_matches_sdpa(orc, kv_dtype, scale_mode, sink):
+    w = W.custom(21, q_lens=[1, 2], seq_lens=[300, 170], hq=4, di=64, topk=2,
+                 kv_dtype=kv_dtype, scale_mode=scale_mode, with_sink=sink)
+    out, lse, st = orc.dense(w)
+    ref_o, ref_l = _sdpa_reference(w)
+    assert st == 0
+    np.testing.assert_allclose(out, ref_o, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(lse, ref_l, rtol=1e-11, atol=1e-11)
+
+
+def test_dense_attention_gqa_heads(orc):
+    # two KV heads, four query heads: head h reads KV head h // 2
+    w = W.custom(22, q_lens=[1], seq_lens=[200], hq=4, di=64, topk=2)
+    rng = np.random.default_rng(3)
+    w.k_cache = W.bf16_bits(rng.standard_normal((w.num_pages, 128, 2, 128)))
+    w.v_cache = W.bf16_bits(rng.standard_normal((w.num_pages, 128, 2, 128)))
+    out, lse, _ = orc.dense(w)
+    ref_o, ref_l = _sdpa_reference(w)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(lse, ref_l, rtol=1e-11)
+
+
+def test_sparse_equals_dense_when_k_covers_all(orc):
+    # spec identity: with k >= number of blocks the sparse path is dense attention
+    for kv, sm, sink in [(W.KV_BF16, W.SCALE_NONE, False), (W.KV_FP8, W.SCALE_PER_TOKEN_HEAD, True)]:
+        w = W.custom(23, q_lens=[1, 4, 2], seq_lens=[900, 385, 129], hq=8, di=64, topk=8,
+                     kv_dtype=kv, scale_mode=sm, with_sink=sink)
+        r = orc.decode(w)
+        out, lse, _ = orc.dense(w)
+        np.testing.assert_allclose(r["out"], out, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(r["lse"], lse, rtol=1e-12, atol=1e-13)
+
+
+def test_sink_to_minus_infinity_is_no_sink(orc):
+    w = W.custom(24, q_lens=[1, 1], seq_lens=[700, 1500], hq=8, di=64, topk=3, with_sink=True)
+    w.sinks = np.full(8, -1e30, np.float32)
+    r1 = orc.decode(w)
+    w.sinks = None
+    r0 = orc.decode(w)
+    np.testing.assert_array_equal(r1["out"], r0["out"])
+    np.testing.assert_array_equal(r1["lse"], r0["lse"])
+
+
+def test_page_permutation_invariance(orc):
+    w = W.custom(25, q_lens=[1, 3], seq_lens=[1200, 650], hq=8, di=64, topk=4,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_PER_TOKEN_HEAD, with_sink=True)
+    r0 = orc.decode(w)
+    perm = np.random.default_rng(9).permutation(w.num_pages)
+    inv = np.argsort(perm)  # new page p holds old page perm[p]
+    w.idx_k, w.k_cache, w.v_cache = w.idx_k[perm], w.k_cache[perm], w.v_cache[perm]
+    w.k_scale, w.v_scale = w.k_scale[perm], w.v_scale[perm]
+    bt = w.block_table.copy()
+    bt[bt >= 0] = inv[bt[bt >= 0]]
+    w.block_table = bt
+    r1 = orc.decode(w)
+    for key in ("topk_idx", "sparse_len", "out", "lse", "scores"):
+        np.testing.assert_array_equal(r0[key], r1[key])
+
+
+def _single_token_case(orc, sink):
+    """One row, one visible token: O = v * e^s / (e^s + e^sink)."""
+    w = W.custom(26, q_lens=[1], seq_lens=[1], hq=4, di=64, topk=1, with_sink=sink is not None)
+    if sink is not None:
+        w.sinks = np.array(sink, np.float32)
+    r = orc.decode(w)
+    qf = _f64(w.q, W.KV_BF16)[0]
+    page = w.block_table[0, 0]
+    k = _f64(w.k_cache, W.KV_BF16)[page, 0, 0]
+    v = _f64(w.v_cache, W.KV_BF16)[page, 0, 0]
+    return w, r, qf, k, v
+
+
+def test_single_token_closed_form(orc):
+    w, r, qf, k, v = _single_token_case(orc, [0.3, -1.0, 2.0, -4.0])
+    sinks = [float(x) for x in w.sinks]  # the fp32 values the oracle sees
+    for h in range(4):
+        s = float(w.softmax_scale) * float(qf[h] @ k)
+        sig = 1.0 / (1.0 + math.exp(sinks[h] - s))
+        np.testing.assert_allclose(r["out"][0, h], v * sig, rtol=1e-12, atol=1e-15)
+        assert abs(r["lse"][0, h] - math.log(math.exp(s) + math.exp(sinks[h]))) < 1e-12
+    w, r, qf, k, v = _single_token_case(orc, None)
+    np.testing.assert_allclose(r["out"][0], np.tile(v, (4, 1)), rtol=0, atol=0)
+
+
+def test_equal_scores_and_constant_values(orc):
+    # K = 0 -> every logit is 0: LSE = ln(n) (+ sink term), O = mean of V.
+    # V = c everywhere -> O = c * (1 - e^(sink - LSE)).
+    w = W.custom(27, q_lens=[1], seq_lens=[777], hq=4, di=64, topk=8, with_sink=True)
+    w.k_cache = np.zeros_like(w.k_cache)
+    r = orc.decode(w)
+    n = 777
+    vf = _f64(w.v_cache, W.KV_BF16)[w.block_table[0, :7]].reshape(-1, 128)[:n]
+    for h in range(4):
+        sink = float(w.sinks[h])
+        den = n + math.exp(sink)
+        assert abs(r["lse"][0, h] - math.log(den)) < 1e-12
+        np.testing.assert_allclose(r["out"][0, h], vf.sum(0) / den, rtol=1e-10, atol=1e-13)
+    w2 = W.custom(28, q_lens=[2], seq_lens=[500], hq=4, di=64, topk=2, with_sink=True)
+    w2.v_cache = np.full_like(w2.v_cache, W.bf16_bits(np.array([1.5], np.float32))[0])
+    r2 = orc.decode(w2)
+    for row in range(2):
+        for h in range(4):
+            c = 1.5 * (1 - math.exp(float(w2.sinks[h]) - r2["lse"][row, h]))
+            np.testing.assert_allclose(r2["out"][row, h], c, rtol=1e-12)
+
+
+def test_scalar_and_uniform_per_token_scales_agree(orc):
+    # per-token-head scales that are all equal to c behave like scalar c, and
+    # scalar (a, b) equals unscaled attention with softmax scale x a, times b
+    w = W.custom(29, q_lens=[1, 2], seq_lens=[640, 333], hq=8, di=64, topk=3,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_SCALAR, with_sink=True)
+    a, bsc = 0.75, 1.25
+    w.k_scale = np.array([a], np.float32)
+    w.v_scale = np.array([bsc], np.float32)
+    r_scalar = orc.decode(w)
+    w.scale_mode = W.SCALE_PER_TOKEN_HEAD
+    w.k_scale = np.full((w.num_pages, 128, 1), a, np.float32)
+    w.v_scale = np.full((w.num_pages, 128, 1), bsc, np.float32)
+    r_tok = orc.decode(w)
+    np.testing.assert_allclose(r_tok["out"], r_scalar["out"], rtol=1e-13, atol=1e-15)
+    w.scale_mode = W.SCALE_NONE
+    w.k_scale = w.v_scale = None
+    w.softmax_scale = w.softmax_scale * a
+    r_none = orc.decode(w)
+    np.testing.assert_allclose(r_scalar["out"], bsc * r_none["out"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(r_scalar["lse"], r_none["lse"], rtol=1e-13)
+
+
+def test_empty_and_poisoned_rows(orc):
+    w = W.custom(30, q_lens=[1], seq_lens=[300], hq=4, di=64, topk=2, with_sink=True)
+    tbl = np.zeros((3, 16), np.int32)
+    slen = np.array([0, 20, 16 * 16 + 1], np.int32)  # empty; bad id below; too long
+    tbl[1, 1] = 10 ** 6
+    q = np.repeat(w.q, 3, axis=0)
+    out, lse, st = orc.sparse_attn(q, w.k_cache, w.v_cache, w.kv_dtype, tbl, slen,
+                                   sinks=w.sinks, softmax_scale=w.softmax_scale)
+    assert st == orc.BAD_TABLE
+    assert np.all(out == 0)
+    np.testing.assert_array_equal(lse, np.tile(w.sinks.astype(np.float64), (3, 1)))
+    out, lse, st = orc.sparse_attn(q[:1], w.k_cache, w.v_cache, w.kv_dtype, tbl[:1], slen[:1],
+                                   softmax_scale=w.softmax_scale)
+    assert st == 0 and np.all(out == 0) and np.all(lse == NEG_INF)
+
+
+def test_threads_do_not_change_results(orc):
+    w = W.custom(31, q_lens=[2, 1, 3], seq_lens=[900, 1300, 260], hq=8, di=64, topk=3,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_PER_TOKEN_HEAD, with_sink=True)
+    r1 = orc.decode(w, nthreads=1)
+    r4 = orc.decode(w, nthreads=4)
+    for key in ("scores", "topk_idx", "tbl", "sparse_len", "out", "lse"):
+        np.testing.assert_array_equal(r1[key], r4[key])
