@@ -1,0 +1,376 @@
+"""Benchmark: query rows/s of the fused block-sparse paged decode on one GB300,
+and the HBM roofline fraction of its dominant kernel (the index-K scan).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+A step = one msa_decode call (index score -> top-k + page-16 table ->
+sparse paged attention) over the whole synthetic batch, inputs resident in
+HBM.  L2 is flushed (a 512 MiB write) between timed steps, outside the timed
+events.  Under torchrun each rank runs its own independent batch (requests
+are independent; no collective on the data path) and rank 0 prints one JSON
+line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "query rows/s for fused index-topk+sparse paged decode; % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------- bytes model
+
+def algorithmic_bytes(w, sparse_len: np.ndarray) -> dict:
+    """Bytes the method must move for one call, per kernel and in total:
+    index-K read once per request, queries, block tables, the selected K/V
+    (+ per-token scales), the tables, O and LSE.  Scores are intermediates."""
+    seq = w.seq_lens
+    nb_req = (seq + 127) // 128
+    N = w.num_rows
+    idx_k = int(seq.sum()) * w.index_heads * w.index_dim * 2
+    idx_q = N * w.index_heads * w.index_dim * 2
+    bt = int(nb_req.sum()) * 4
+    q = N * w.hq * w.head_dim * 2
+    kv_elem = 1 if w.kv_dtype == W.KV_FP8 else 2
+    toks = int(np.asarray(sparse_len, np.int64).sum())
+    kv = toks * w.hkv * w.head_dim * kv_elem * 2
+    if w.scale_mode == W.SCALE_PER_TOKEN_HEAD:
+        kv += toks * w.hkv * 4 * 2
+    k = w.topk
+    tables = N * (k * 4 + 8 * k * 4 + 4)
+    out = N * (w.hq * w.head_dim * 2 + w.hq * 4)
+    score = idx_k + idx_q + bt  # what the index-score kernel must read
+    total = score + q + kv + tables + out
+    return dict(score_kernel=score, attention=q + kv + out, total=total, index_k=idx_k, kv=kv)
+
+
+# ---------------------------------------------------------------- environment
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_sparse_paged_02_gb300", "csrc")
+    for name in ("index_score.cu", "msa_internal.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str):
+    """dram bytes per launch of the score kernel from the committed ncu
+    summary, or None if the kernel changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "score_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(workload)
+        if ent and ent.get("source_hash") == kernel_source_hash():
+            return int(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- arms
+
+def cpu_oracle_run(w, budget_s: float = 12.0, max_reps: int = 3):
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(w, nthreads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if reps >= max_reps or el >= budget_s:
+            break
+    return dict(value=w.num_rows * reps / el, unit="rows/s", cores=threads,
+                kind="oracle", sample=f"{reps} x full {w.name} batch ({w.num_rows} rows), "
+                f"fp64 C oracle, {threads} threads, {el:.2f} s")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = W.NAMED[args.workload](seed=rank_seed(args.workload, 0))
+    times = []
+    for _ in range(args.warmup):
+        cpu_oracle_run(w, budget_s=0.0, max_reps=1)
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        cpu_oracle_run(w, budget_s=0.0, max_reps=1)
+        times.append(time.perf_counter() - t0)
+    import oracle
+    total = sum(times)
+    value = w.num_rows * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.default_threads(),
+                             "kind": "oracle",
+                             "sample": f"full {w.name} batch per step ({w.num_rows} rows)"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+W_SEED = {"tiny_decode": 1, "batched_decode": 2, "speculative_decode": 3,
+          "large_batch_decode": 4, "chunked_prefill": 5}
+
+
+def rank_seed(workload: str, rank: int) -> int:
+    """Seed of a rank's batch: rank 0 draws the named workload itself, every
+    other rank an independent batch of the same shape."""
+    return W_SEED[workload] + 1000 * rank
+
+
+def workload_config(w):
+    seq = w.seq_lens
+    return {"workload": w.name, "requests": w.num_reqs, "rows": w.num_rows,
+            "query_heads": w.hq, "kv_heads": w.hkv, "head_dim": w.head_dim,
+            "index_dim": w.index_dim, "topk": w.topk,
+            "kv": "fp8_e4m3" if w.kv_dtype == W.KV_FP8 else "bf16",
+            "scales": ["none", "scalar", "per_token_head"][w.scale_mode],
+            "sinks": w.sinks is not None, "context_tokens": int(seq.sum()),
+            "median_context": float(np.median(seq)), "l2": "flushed between steps"}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_paged_02_gb300 as msa
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    # weak scaling: every rank owns its own batch of independent requests
+    w = W.NAMED[args.workload](seed=rank_seed(args.workload, rank))
+    case = msa.DeviceCase(w, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = None if args.profile else torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    if args.profile:
+        # plain run for profilers: warm-up + K steps, nothing else
+        for _ in range(args.warmup + args.steps):
+            case.decode(keep_tables=False)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_run": w.name, "status": int(case.status.item())}))
+        return 0
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        case.decode(keep_tables=False)
+    torch.cuda.synchronize()
+    if int(case.status.item()) != 0:
+        raise RuntimeError(f"device status {int(case.status.item())} on a clean workload")
+
+    # ---- timed: K steps, per-step events, L2 flushed between steps
+    marks = [(ev(), ev(), ev(), ev()) for _ in range(args.steps)]
+    traces = [msa.make_trace(m[1], m[2], m[3]) for m in marks]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            marks[i][0].record(stream)
+            case.decode(keep_tables=False, trace=traces[i])
+        torch.cuda.synchronize()
+    barrier()
+    step_ms = [m[0].elapsed_time(m[3]) for m in marks]
+    score_ms = [m[0].elapsed_time(m[1]) for m in marks]
+    topk_ms = [m[1].elapsed_time(m[2]) for m in marks]
+    attn_ms = [m[2].elapsed_time(m[3]) for m in marks]
+    total_ms = sum(step_ms)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end through the public API: host buffers, copies inside
+    case.decode()
+    torch.cuda.synchronize()
+    sparse_len = case.sparse_len[: w.num_rows].cpu().numpy()
+    host = {name: getattr(case, name).cpu().pin_memory()
+            for name in ("q", "idx_q", "cu_q", "cu_k", "ctx", "bt")}
+    out_h = torch.empty_like(case.out, device="cpu").pin_memory()
+    lse_h = torch.empty_like(case.lse, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    e2e_marks = [(ev(), ev()) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush.fill_(i & 0xff)
+        if i >= args.warmup:
+            e2e_marks[i - args.warmup][0].record(stream)
+        for name, t in host.items():
+            getattr(case, name).copy_(t, non_blocking=True)
+        case.decode(keep_tables=False)
+        out_h.copy_(case.out, non_blocking=True)
+        lse_h.copy_(case.lse, non_blocking=True)
+        if i >= args.warmup:
+            e2e_marks[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_marks)
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+    rows_total = w.num_rows * ws * args.steps
+    value = rows_total / (total_ms / 1e3)
+    peak, peak_kind = read_peaks()
+    nbytes = algorithmic_bytes(w, sparse_len)
+    score_avg = statistics.mean(score_ms)
+    achieved = nbytes["score_kernel"] / (score_avg / 1e3) / 1e9
+    step_avg = total_ms / args.steps
+    cpu = cpu_oracle_run(w)
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_avg, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 kv / bf16 q / fp32 acc"
+        if w.kv_dtype == W.KV_FP8 else "bf16 / fp32 acc", "data": "synthetic",
+        "config": workload_config(w),
+        "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": read_traffic(w.name),
+                     "algorithmic_bytes_per_launch": nbytes["score_kernel"],
+                     "avg_launch_ms": score_avg},
+        "step_roofline": {"algorithmic_bytes": nbytes["total"],
+                          "achieved_gbs": nbytes["total"] / (step_avg / 1e3) / 1e9,
+                          "frac": nbytes["total"] / (step_avg / 1e3) / 1e9 / peak},
+        "kernel_ms": {"index_score": score_avg, "topk_table": statistics.mean(topk_ms),
+                      "sparse_attn": statistics.mean(attn_ms)},
+        "e2e": {"value": rows_total / (e2e_ms / 1e3), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="large_batch_decode", choices=sorted(W.NAMED))
+    ap.add_argument("--profile", action="store_true",
+                    help="plain warm-up + K decode steps for a profiler (no timing)")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

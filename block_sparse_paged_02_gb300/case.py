@@ -1,0 +1,96 @@
+"""Device-resident copy of one batch (host arrays -> torch CUDA tensors) with
+the output buffers and workspace the C ABI needs.  Marshalling only."""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+
+def _dev(a: np.ndarray, device, dtype=None) -> torch.Tensor:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:  # bf16 bit patterns
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(a)
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(device)
+
+
+class DeviceCase:
+    """Inputs of one decode call resident on the GPU, plus outputs.
+
+    `w` is any object with the fields of `workloads.Workload` (host numpy
+    arrays).  The KV and index-K pools stay resident; `refresh_step_inputs`
+    re-uploads only what changes per step (queries and batch geometry)."""
+
+    def __init__(self, w, device: str = "cuda", topk: Optional[int] = None,
+                 tbl_stride: Optional[int] = None):
+        self.w = w
+        self.device = device
+        self.topk = int(topk or w.topk)
+        self.tbl_stride = int(tbl_stride or 8 * self.topk)
+        self.cu_q = _dev(w.cu_seqlens_q, device)
+        self.cu_k = _dev(w.cu_seqlens_k, device)
+        self.ctx = _dev(w.context_lens, device)
+        self.bt = _dev(w.block_table, device)
+        self.idx_q = _dev(w.idx_q, device)
+        self.idx_k = _dev(w.idx_k, device)
+        self.q = _dev(w.q, device)
+        self.k = _dev(w.k_cache, device)
+        self.v = _dev(w.v_cache, device)
+        self.k_scale = None if w.k_scale is None else _dev(w.k_scale, device)
+        self.v_scale = None if w.v_scale is None else _dev(w.v_scale, device)
+        self.sinks = None if w.sinks is None else _dev(w.sinks, device)
+        N, hq, d = (int(x) for x in w.q.shape)
+        self.num_rows = N
+        self.out = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((N, hq), dtype=torch.float32, device=device)
+        self.scores = torch.empty((max(N, 1), w.bt_stride), dtype=torch.float32, device=device)
+        self.topk_idx = torch.empty((max(N, 1), self.topk), dtype=torch.int32, device=device)
+        self.tbl = torch.empty((max(N, 1), self.tbl_stride), dtype=torch.int32, device=device)
+        self.sparse_len = torch.empty((max(N, 1),), dtype=torch.int32, device=device)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=device)
+        self.batch = B.make_batch(self.cu_q, self.cu_k, self.ctx, self.bt, w.num_pages, N)
+        self.attn = B.make_attn_args(self.q, self.k, self.v, w.kv_dtype, w.num_pages, self.out,
+                                     self.lse, scale_mode=w.scale_mode, k_scale=self.k_scale,
+                                     v_scale=self.v_scale, sinks=self.sinks,
+                                     softmax_scale=w.softmax_scale)
+        ws = B.msa_workspace_size(N, w.bt_stride, self.topk, hq, d, self.tbl_stride)
+        self.workspace = torch.zeros((ws,), dtype=torch.uint8, device=device)
+        ws_a = B.msa_workspace_size(N, 0, 0, hq, d, self.tbl_stride)
+        self.attn_workspace = torch.zeros((ws_a,), dtype=torch.uint8, device=device)
+
+    # -- the four entry points on this batch
+    def index_score(self, stream=None):
+        B.msa_index_score(self.batch, self.idx_q, self.idx_k, self.w.index_heads,
+                          self.w.index_dim, self.scores, self.w.bt_stride, self.status, stream)
+
+    def topk_build_table(self, stream=None):
+        B.msa_topk_build_table(self.batch, self.scores, self.w.bt_stride, self.topk,
+                               self.topk_idx, self.tbl, self.tbl_stride, self.sparse_len,
+                               self.status, stream)
+
+    def sparse_paged_attn(self, stream=None):
+        B.msa_sparse_paged_attn(self.attn, self.tbl, self.tbl_stride, self.sparse_len,
+                                self.attn_workspace, self.status, stream)
+
+    def decode(self, keep_tables: bool = True, trace=None, stream=None):
+        B.msa_decode(self.batch, self.idx_q, self.idx_k, self.w.index_heads, self.w.index_dim,
+                     self.topk, self.attn, self.topk_idx if keep_tables else None,
+                     self.tbl if keep_tables else None, self.tbl_stride,
+                     self.sparse_len if keep_tables else None, self.workspace, self.status,
+                     trace, stream)
+
+    def fetch(self):
+        torch.cuda.synchronize()
+        n = self.num_rows
+        return dict(scores=self.scores[:n].cpu().numpy(), topk_idx=self.topk_idx[:n].cpu().numpy(),
+                    tbl=self.tbl[:n].cpu().numpy(), sparse_len=self.sparse_len[:n].cpu().numpy(),
+                    out=self.out.float().cpu().numpy().astype(np.float64),
+                    lse=self.lse.cpu().numpy().astype(np.float64),
+                    status=int(self.status.item()))

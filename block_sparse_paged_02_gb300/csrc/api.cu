@@ -1,0 +1,287 @@
+// api.cu -- the C ABI of libmsa: argument validation, workspace layout and
+// kernel launches.  Nothing here touches device data or synchronises: every
+// check is on host-visible arguments, and data errors are left to the
+// kernels' device status word (see msa.h).
+#include <cstring>
+#include <mutex>
+
+#include "msa_internal.cuh"
+
+namespace msa {
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Attention work split: page-16 entries per split and the split count, from
+// the row count and the widest possible row (max_entries page-16 entries),
+// aiming at about two CTAs per SM.
+void attn_split(int num_rows, int max_entries, int* pps, int* splits) {
+  const int sms = device_sm_count();
+  const int target = num_rows > 0 ? (2 * sms + num_rows - 1) / num_rows : 1;
+  int per = (max_entries + target - 1) / target;
+  per = per < 4 ? 4 : (per + 3) / 4 * 4;
+  *pps = per;
+  *splits = max_entries > 0 ? (max_entries + per - 1) / per : 1;
+}
+
+struct DecodeWs {
+  size_t counters, scores, topk, tbl, len, partials, total;
+};
+
+DecodeWs decode_layout(int num_rows, int bt_stride, int topk, int splits) {
+  DecodeWs w;
+  const size_t n = (size_t)(num_rows > 0 ? num_rows : 1);
+  size_t off = 0;
+  w.counters = off;
+  off = round_up(off + n * 4, 256);
+  w.scores = off;
+  off = round_up(off + n * (size_t)bt_stride * 4, 256);
+  w.topk = off;
+  off = round_up(off + n * (size_t)topk * 4, 256);
+  w.tbl = off;
+  off = round_up(off + n * (size_t)topk * 8 * 4, 256);
+  w.len = off;
+  off = round_up(off + n * 4, 256);
+  w.partials = off;
+  off = round_up(off + n * (size_t)splits * kPartFloats * 4, 256);
+  w.total = off;
+  return w;
+}
+
+msa_status check_batch(const msa_batch* b) {
+  if (!b) return MSA_ERR_NULL;
+  if (b->num_reqs < 0 || b->num_rows < 0 || b->num_pages < 0 || b->bt_stride < 1)
+    return MSA_ERR_SHAPE;
+  if (b->num_reqs > 0 &&
+      (!b->cu_seqlens_q || !b->cu_seqlens_k || !b->context_lens || !b->block_table))
+    return MSA_ERR_NULL;
+  if (b->num_reqs == 0 && !b->cu_seqlens_q) return MSA_ERR_NULL;
+  if (b->num_reqs > kMaxReqs || b->bt_stride > kMaxBlocksPerRow) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+msa_status check_attn(const msa_attn_args* a) {
+  if (!a) return MSA_ERR_NULL;
+  if (a->kv_dtype != MSA_KV_BF16 && a->kv_dtype != MSA_KV_FP8_E4M3) return MSA_ERR_DTYPE;
+  if (a->scale_mode < MSA_SCALE_NONE || a->scale_mode > MSA_SCALE_PER_TOKEN_HEAD)
+    return MSA_ERR_DTYPE;
+  if (a->num_rows < 0 || a->num_heads < 1 || a->num_kv_heads < 1 || a->num_pages < 0)
+    return MSA_ERR_SHAPE;
+  if (a->num_heads % a->num_kv_heads != 0) return MSA_ERR_SHAPE;
+  if (a->num_kv_heads != 1 || a->head_dim != kHeadDim || a->num_heads > kMaxHeads)
+    return MSA_ERR_UNSUPPORTED;
+  if (a->num_rows > 0 && (!a->q || !a->k_cache || !a->v_cache || !a->out || !a->lse))
+    return MSA_ERR_NULL;
+  if (a->scale_mode != MSA_SCALE_NONE && (!a->k_scale || !a->v_scale)) return MSA_ERR_NULL;
+  if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache) ||
+      !aligned16(a->out) || !aligned16(a->lse))
+    return MSA_ERR_SHAPE;
+  if (a->scale_mode == MSA_SCALE_PER_TOKEN_HEAD && (!aligned16(a->k_scale) || !aligned16(a->v_scale)))
+    return MSA_ERR_SHAPE;
+  return MSA_OK;
+}
+
+AttnLaunch make_attn(const msa_attn_args* a, const int32_t* tbl, int tbl_stride,
+                     const int32_t* len, float* partials, uint32_t* counters, int pps,
+                     int splits, uint32_t* status) {
+  AttnLaunch L;
+  L.q = static_cast<const uint16_t*>(a->q);
+  L.num_rows = a->num_rows;
+  L.num_heads = a->num_heads;
+  L.k = static_cast<const uint8_t*>(a->k_cache);
+  L.v = static_cast<const uint8_t*>(a->v_cache);
+  L.kv_fp8 = a->kv_dtype == MSA_KV_FP8_E4M3;
+  L.num_pages16 = 8ll * a->num_pages;
+  L.scale_mode = a->scale_mode;
+  L.k_scale = a->k_scale;
+  L.v_scale = a->v_scale;
+  L.sinks = a->sinks;
+  L.softmax_scale = a->softmax_scale;
+  L.tbl = tbl;
+  L.tbl_stride = tbl_stride;
+  L.sparse_len = len;
+  L.out = static_cast<uint16_t*>(a->out);
+  L.lse = a->lse;
+  L.partials = partials;
+  L.counters = counters;
+  L.splits = splits;
+  L.pages_per_split = pps;
+  L.status = status;
+  return L;
+}
+
+msa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+const char* msa_status_string(msa_status s) {
+  switch (s) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_NULL: return "a required pointer is NULL";
+    case MSA_ERR_SHAPE: return "inconsistent sizes, strides or alignment";
+    case MSA_ERR_DTYPE: return "unknown kv dtype or scale mode";
+    case MSA_ERR_UNSUPPORTED: return "configuration not supported by this build";
+    case MSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MSA_ERR_CUDA: return "CUDA launch failed";
+  }
+  return "unknown status";
+}
+
+size_t msa_workspace_size(int32_t num_rows, int32_t bt_stride, int32_t topk, int32_t num_heads,
+                          int32_t head_dim, int32_t tbl_stride) {
+  (void)num_heads;
+  (void)head_dim;
+  if (num_rows < 0 || bt_stride < 0 || topk < 0 || tbl_stride < 0) return 0;
+  int pps, splits;
+  const int max_entries = topk > 0 ? 8 * topk : tbl_stride;
+  attn_split(num_rows, max_entries, &pps, &splits);
+  if (bt_stride == 0) {  // attention only: counters + partials
+    const size_t n = (size_t)(num_rows > 0 ? num_rows : 1);
+    return round_up(n * 4, 256) + round_up(n * (size_t)splits * kPartFloats * 4, 256);
+  }
+  return decode_layout(num_rows, bt_stride, topk, splits).total;
+}
+
+msa_status msa_index_score(const msa_batch* batch, const void* idx_q, const void* idx_k_cache,
+                           int32_t index_heads, int32_t index_dim, float* scores,
+                           int32_t score_stride, uint32_t* dev_status, cudaStream_t stream) {
+  msa_status st = check_batch(batch);
+  if (st != MSA_OK) return st;
+  if (!dev_status || (batch->num_rows > 0 && (!idx_q || !idx_k_cache || !scores)))
+    return MSA_ERR_NULL;
+  if (!((index_heads == 1 && (index_dim == 64 || index_dim == 128)) ||
+        (index_heads == 2 && index_dim == 64)))
+    return MSA_ERR_UNSUPPORTED;
+  if (score_stride < batch->bt_stride) return MSA_ERR_SHAPE;
+  if (!aligned16(idx_q) || !aligned16(idx_k_cache)) return MSA_ERR_SHAPE;
+  if (batch->num_rows == 0 || batch->num_reqs == 0) return MSA_OK;
+  ScoreLaunch p{*batch, static_cast<const uint16_t*>(idx_q),
+                static_cast<const uint8_t*>(idx_k_cache), index_heads, index_dim, scores,
+                score_stride, dev_status};
+  return cuda_status(launch_index_score(p, stream));
+}
+
+msa_status msa_topk_build_table(const msa_batch* batch, const float* scores,
+                                int32_t score_stride, int32_t topk, int32_t* topk_idx,
+                                int32_t* sparse_tbl, int32_t tbl_stride, int32_t* sparse_len,
+                                uint32_t* dev_status, cudaStream_t stream) {
+  msa_status st = check_batch(batch);
+  if (st != MSA_OK) return st;
+  if (!dev_status) return MSA_ERR_NULL;
+  if (topk < 1) return MSA_ERR_SHAPE;
+  if (tbl_stride < 8 * topk || score_stride < batch->bt_stride) return MSA_ERR_SHAPE;
+  if (batch->num_rows > 0 && (!scores || !topk_idx || !sparse_tbl || !sparse_len))
+    return MSA_ERR_NULL;
+  if (batch->num_rows == 0) return MSA_OK;
+  if (batch->num_reqs == 0) return MSA_ERR_SHAPE;  // rows without any request
+  TopkLaunch p{*batch, scores, score_stride, topk, topk_idx, sparse_tbl, tbl_stride, sparse_len,
+               nullptr, dev_status};
+  return cuda_status(launch_topk_table(p, stream));
+}
+
+msa_status msa_sparse_paged_attn(const msa_attn_args* attn, const int32_t* sparse_tbl,
+                                 int32_t tbl_stride, const int32_t* sparse_len, void* workspace,
+                                 size_t workspace_bytes, uint32_t* dev_status,
+                                 cudaStream_t stream) {
+  msa_status st = check_attn(attn);
+  if (st != MSA_OK) return st;
+  if (!dev_status) return MSA_ERR_NULL;
+  if (tbl_stride < 1) return MSA_ERR_SHAPE;
+  if (attn->num_rows == 0) return MSA_OK;
+  if (!sparse_tbl || !sparse_len) return MSA_ERR_NULL;
+  const size_t need = msa_workspace_size(attn->num_rows, 0, 0, attn->num_heads, attn->head_dim,
+                                         tbl_stride);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return MSA_ERR_WORKSPACE;
+  int pps, splits;
+  attn_split(attn->num_rows, tbl_stride, &pps, &splits);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws);
+  float* partials = reinterpret_cast<float*>(ws + round_up((size_t)attn->num_rows * 4, 256));
+  AttnLaunch p = make_attn(attn, sparse_tbl, tbl_stride, sparse_len, partials, counters, pps,
+                           splits, dev_status);
+  return cuda_status(launch_sparse_attn(p, stream));
+}
+
+msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx_k_cache,
+                      int32_t index_heads, int32_t index_dim, int32_t topk,
+                      const msa_attn_args* attn, int32_t* topk_idx, int32_t* sparse_tbl,
+                      int32_t tbl_stride, int32_t* sparse_len, void* workspace,
+                      size_t workspace_bytes, uint32_t* dev_status, const msa_trace* trace,
+                      cudaStream_t stream) {
+  msa_status st = check_batch(batch);
+  if (st != MSA_OK) return st;
+  st = check_attn(attn);
+  if (st != MSA_OK) return st;
+  if (!dev_status) return MSA_ERR_NULL;
+  if (topk < 1) return MSA_ERR_SHAPE;
+  if (attn->num_rows != batch->num_rows) return MSA_ERR_SHAPE;
+  if (attn->num_pages != batch->num_pages) return MSA_ERR_SHAPE;
+  if (!((index_heads == 1 && (index_dim == 64 || index_dim == 128)) ||
+        (index_heads == 2 && index_dim == 64)))
+    return MSA_ERR_UNSUPPORTED;
+  if (sparse_tbl && tbl_stride < 8 * topk) return MSA_ERR_SHAPE;
+  if (batch->num_rows == 0) return MSA_OK;
+  if (batch->num_reqs == 0) return MSA_ERR_SHAPE;
+  if (!idx_q || !idx_k_cache) return MSA_ERR_NULL;
+  if (!aligned16(idx_q) || !aligned16(idx_k_cache)) return MSA_ERR_SHAPE;
+  const size_t need = msa_workspace_size(batch->num_rows, batch->bt_stride, topk,
+                                         attn->num_heads, attn->head_dim, 8 * topk);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return MSA_ERR_WORKSPACE;
+
+  int pps, splits;
+  attn_split(batch->num_rows, 8 * topk, &pps, &splits);
+  const DecodeWs L = decode_layout(batch->num_rows, batch->bt_stride, topk, splits);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws + L.counters);
+  float* scores = reinterpret_cast<float*>(ws + L.scores);
+  int32_t* k_idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + L.topk);
+  int32_t* tbl = sparse_tbl ? sparse_tbl : reinterpret_cast<int32_t*>(ws + L.tbl);
+  const int tstride = sparse_tbl ? tbl_stride : 8 * topk;
+  int32_t* len = sparse_len ? sparse_len : reinterpret_cast<int32_t*>(ws + L.len);
+
+  ScoreLaunch sp{*batch, static_cast<const uint16_t*>(idx_q),
+                 static_cast<const uint8_t*>(idx_k_cache), index_heads, index_dim, scores,
+                 batch->bt_stride, dev_status};
+  cudaError_t e = launch_index_score(sp, stream);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  if (trace && trace->after_score) cudaEventRecord(trace->after_score, stream);
+
+  TopkLaunch tp{*batch, scores, batch->bt_stride, topk, k_idx, tbl, tstride, len, counters,
+                dev_status};
+  e = launch_topk_table(tp, stream);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  if (trace && trace->after_topk) cudaEventRecord(trace->after_topk, stream);
+
+  AttnLaunch ap = make_attn(attn, tbl, tstride, len, reinterpret_cast<float*>(ws + L.partials),
+                            counters, pps, splits, dev_status);
+  // the attention split depends only on the selected width (8*topk entries)
+  e = launch_sparse_attn(ap, stream);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  if (trace && trace->after_attn) cudaEventRecord(trace->after_attn, stream);
+  return MSA_OK;
+}
+
+}  // extern "C"

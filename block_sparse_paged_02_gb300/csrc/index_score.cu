@@ -1,0 +1,302 @@
+// index_score.cu -- step 1: block scores of the index query against the paged
+// index-K cache.
+//
+// Definition ("Optimise MiniMax-M3 decode index and top-k on gfx950", vLLM PR
+// 54682, "Implementation breakdown" item 1 and "Key files"): each cached
+// 128-token block of a request gets, for every query row of that request, the
+// maximum over the block's visible tokens (t <= the row's position) and over
+// index heads of the dot product idx_q[row] . idx_k[t].
+//
+// GB300 design.  The index-K scan is the dominant byte stream of the decode
+// path and is HBM-bound (~1 FMA per 2 bytes for one row), so the kernel is a
+// persistent, bandwidth-first streamer:
+//   * work = the flattened list of (request, block) items over all requests;
+//     each CTA takes an equal contiguous slice (balanced by actual block
+//     count, the lesson of the PR 54682 balanced scorer);
+//   * one producer thread issues one 1-D bulk async copy (TMA bulk engine)
+//     per 128-token index-K page (16 or 32 KB, contiguous in the page-128
+//     layout) into a ring of shared-memory stages guarded by mbarriers;
+//   * each consumer warp owns one stage and scores the whole page
+//     (warp-per-block): every lane holds 4*Hi token sub-rows, walks their
+//     16-byte chunks in a lane-rotated order (bank-conflict free), and keeps
+//     fp32 dot products for up to 4 query rows of the request at once, so a
+//     staged page is shared by all rows of the request;
+//   * a warp max-reduce produces the block score; integer-valued inputs give
+//     exact fp32 scores.
+#include <cfloat>
+
+#include "msa_internal.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kRowGroup = 4;
+
+template <int DI, int HI>
+struct ScoreCfg {
+  static constexpr int kSubRowBytes = DI * 2;
+  static constexpr int kChunks = DI / 8;  // 16-byte chunks per sub-row
+  static constexpr int kSubPerLane = kBlock * HI / 32;
+  static constexpr int kPageBytes = kBlock * HI * DI * 2;
+  static constexpr int kStages = kPageBytes >= 32768 ? 6 : 12;  // 192 KB of stages
+  static constexpr int kThreads = 32 * (1 + kStages);
+  static constexpr int kQBytes = kRowGroup * HI * DI * 2;  // per consumer warp
+};
+
+struct StageInfo {
+  int req;
+  int blk;
+  int valid;
+  int pad;
+};
+
+template <int DI, int HI>
+struct ScoreSmem {
+  using C = ScoreCfg<DI, HI>;
+  static constexpr size_t kPages = 0;
+  static constexpr size_t kQ = kPages + (size_t)C::kStages * C::kPageBytes;
+  static constexpr size_t kBars = kQ + (size_t)C::kStages * C::kQBytes;
+  static constexpr size_t kInfo = kBars + 2 * C::kStages * sizeof(uint64_t);
+  static constexpr size_t kMisc = kInfo + C::kStages * sizeof(StageInfo);
+  static constexpr size_t kPrefix = kMisc + 64;
+  static size_t bytes(int num_reqs) { return kPrefix + (size_t)(num_reqs + 1) * sizeof(int); }
+};
+
+// Scores of one staged page for NR (<= kRowGroup) query rows held in q_s.
+// Returns, in lane 0..NR-1 order via out[], the per-row block maxima.
+template <int DI, int HI, int NR>
+__device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q_s, int lane,
+                                           int blk, const int (&pos)[kRowGroup],
+                                           float (&out)[kRowGroup]) {
+  using C = ScoreCfg<DI, HI>;
+  float acc[C::kSubPerLane][NR];
+#pragma unroll
+  for (int j = 0; j < C::kSubPerLane; ++j)
+#pragma unroll
+    for (int r = 0; r < NR; ++r) acc[j][r] = 0.f;
+  const int head = lane % HI;  // sub-row lane+32j holds index head (lane % HI)
+#pragma unroll 2
+  for (int i = 0; i < C::kChunks; ++i) {
+    const int c = (i + lane) & (C::kChunks - 1);
+    float qf[NR][8];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const uint4 w = lds128(q_s + ((r * HI + head) * DI + c * 8) * 2);
+      qf[r][0] = bf16lo(w.x);
+      qf[r][1] = bf16hi(w.x);
+      qf[r][2] = bf16lo(w.y);
+      qf[r][3] = bf16hi(w.y);
+      qf[r][4] = bf16lo(w.z);
+      qf[r][5] = bf16hi(w.z);
+      qf[r][6] = bf16lo(w.w);
+      qf[r][7] = bf16hi(w.w);
+    }
+#pragma unroll
+    for (int j = 0; j < C::kSubPerLane; ++j) {
+      const int sr = lane + 32 * j;
+      const uint4 w = lds128(page + sr * C::kSubRowBytes + c * 16);
+      const float k0 = bf16lo(w.x), k1 = bf16hi(w.x), k2 = bf16lo(w.y), k3 = bf16hi(w.y);
+      const float k4 = bf16lo(w.z), k5 = bf16hi(w.z), k6 = bf16lo(w.w), k7 = bf16hi(w.w);
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        float a = acc[j][r];
+        a = fmaf(qf[r][0], k0, a);
+        a = fmaf(qf[r][1], k1, a);
+        a = fmaf(qf[r][2], k2, a);
+        a = fmaf(qf[r][3], k3, a);
+        a = fmaf(qf[r][4], k4, a);
+        a = fmaf(qf[r][5], k5, a);
+        a = fmaf(qf[r][6], k6, a);
+        a = fmaf(qf[r][7], k7, a);
+        acc[j][r] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < C::kSubPerLane; ++j) {
+      const int token = (lane + 32 * j) / HI;
+      if (blk * kBlock + token <= pos[r]) m = fmaxf(m, acc[j][r]);  // NaN never wins
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    out[r] = m;
+  }
+}
+
+template <int DI, int HI>
+__global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
+    index_score_kernel(const ScoreLaunch p) {
+  using C = ScoreCfg<DI, HI>;
+  using S = ScoreSmem<DI, HI>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
+  uint64_t* empty = full + C::kStages;
+  StageInfo* info = reinterpret_cast<StageInfo*>(smem + S::kInfo);
+  int* misc = reinterpret_cast<int*>(smem + S::kMisc);
+  int* prefix = reinterpret_cast<int*>(smem + S::kPrefix);
+
+  const msa_batch& b = p.batch;
+  const int R = b.num_reqs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // ---- setup: per-request block counts, batch checks, prefix sums
+  if (tid == 0) {
+    misc[0] = 0;  // per-request status bits seen by this CTA
+    // rows must be tiled by cu_seqlens_q, else no row maps to a request
+    misc[1] = !(b.cu_seqlens_q[0] == 0 && b.cu_seqlens_q[R] == b.num_rows);
+  }
+  if (tid < C::kStages) {
+    mbar_init(&full[tid], 1);
+    mbar_init(&empty[tid], 1);
+  }
+  fence_barrier_init();
+  __syncthreads();
+  for (int q = tid; q < R; q += blockDim.x) {
+    int q0, ql, ctx, nb;
+    const uint32_t bad = request_lengths(b, q, &q0, &ql, &ctx, &nb);
+    if (ql < 0) misc[1] = 1;
+    if (bad) {
+      atomicOr(reinterpret_cast<unsigned*>(&misc[0]), bad);
+      nb = 0;
+    }
+    prefix[q + 1] = nb;
+  }
+  __syncthreads();
+  if (misc[1]) {  // the batch cannot be mapped: score nothing
+    if (blockIdx.x == 0 && tid == 0) atomicOr(p.status, MSA_DEV_MALFORMED);
+    return;
+  }
+  if (warp == 0) {  // inclusive scan of block counts -> prefix[0..R]
+    int carry = 0;
+    if (lane == 0) prefix[0] = 0;
+    for (int base = 0; base < R; base += 32) {
+      const int q = base + lane;
+      int v = q < R ? prefix[q + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+      }
+      if (q < R) prefix[q + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && tid == 0 && misc[0]) atomicOr(p.status, (unsigned)misc[0]);
+
+  const long long total = prefix[R];
+  const int i0 = (int)(total * blockIdx.x / gridDim.x);
+  const int i1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+  const int n_items = i1 - i0;
+
+  if (warp == 0) {
+    // ---- producer: one elected thread streams index-K pages into the ring
+    if (lane == 0) {
+      for (int j = 0; j < n_items; ++j) {
+        const int s = j % C::kStages, use = j / C::kStages;
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+          atomicOr(p.status, MSA_DEV_TIMEOUT);
+          break;
+        }
+        const int it = i0 + j;
+        int lo = 0, hi = R;  // largest q with prefix[q] <= it
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (prefix[mid] <= it) lo = mid; else hi = mid;
+        }
+        const int blk = it - prefix[lo];
+        const int page = b.block_table[(long long)lo * b.bt_stride + blk];
+        const bool valid = page >= 0 && page < b.num_pages;
+        info[s] = StageInfo{lo, blk, valid ? 1 : 0, 0};
+        if (valid) {
+          mbar_arrive_expect_tx(&full[s], C::kPageBytes);
+          bulk_g2s(smem + S::kPages + (size_t)s * C::kPageBytes,
+                   p.idx_k + (long long)page * C::kPageBytes, C::kPageBytes, &full[s]);
+        } else {
+          atomicOr(p.status, MSA_DEV_BAD_PAGE);
+          mbar_arrive(&full[s]);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- consumers: warp w owns stage w
+  const int w = warp - 1;
+  const uint8_t* page = smem + S::kPages + (size_t)w * C::kPageBytes;
+  uint8_t* q_s = smem + S::kQ + (size_t)w * C::kQBytes;
+  int cur_req = -1, cur_g0 = -1;
+  for (int j = w, use = 0; j < n_items; j += C::kStages, ++use) {
+    if (!mbar_wait(&full[w], use & 1)) {
+      if (lane == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
+      break;
+    }
+    const StageInfo si = info[w];
+    const int q0 = b.cu_seqlens_q[si.req];
+    const int qlen = b.cu_seqlens_q[si.req + 1] - q0;
+    const int ctx = b.context_lens[si.req];
+    // rows j with ctx + j >= 128*blk can see this block
+    const int jstart = max(0, si.blk * kBlock - ctx);
+    for (int g0 = jstart; g0 < qlen; g0 += kRowGroup) {
+      const int nr = min(kRowGroup, qlen - g0);
+      int pos[kRowGroup];
+#pragma unroll
+      for (int r = 0; r < kRowGroup; ++r) pos[r] = ctx + g0 + min(r, nr - 1);
+      float best[kRowGroup];
+      if (si.valid) {
+        if (si.req != cur_req || g0 != cur_g0) {  // stage the query rows of this group
+          __syncwarp();
+          const int chunks = nr * HI * DI / 8;
+          const uint4* src = reinterpret_cast<const uint4*>(
+              p.idx_q + (long long)(q0 + g0) * HI * DI);
+          for (int c = lane; c < chunks; c += 32)
+            *reinterpret_cast<uint4*>(q_s + c * 16) = src[c];
+          __syncwarp();
+          cur_req = si.req;
+          cur_g0 = g0;
+        }
+        if (nr == 1)
+          score_page<DI, HI, 1>(page, q_s, lane, si.blk, pos, best);
+        else if (nr == 2)
+          score_page<DI, HI, 2>(page, q_s, lane, si.blk, pos, best);
+        else
+          score_page<DI, HI, 4>(page, q_s, lane, si.blk, pos, best);  // rows >= nr unused
+      } else {
+#pragma unroll
+        for (int r = 0; r < kRowGroup; ++r) best[r] = -INFINITY;
+      }
+#pragma unroll
+      for (int r = 0; r < kRowGroup; ++r)
+        if (lane == r && r < nr)
+          p.scores[(long long)(q0 + g0 + r) * p.score_stride + si.blk] = best[r];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[w]);
+  }
+}
+
+template <int DI, int HI>
+cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
+  using C = ScoreCfg<DI, HI>;
+  const size_t smem = ScoreSmem<DI, HI>::bytes(p.batch.num_reqs);
+  auto kern = index_score_kernel<DI, HI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<device_sm_count(), C::kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream) {
+  if (p.index_heads == 1 && p.index_dim == 128) return launch_cfg<128, 1>(p, stream);
+  if (p.index_heads == 1 && p.index_dim == 64) return launch_cfg<64, 1>(p, stream);
+  if (p.index_heads == 2 && p.index_dim == 64) return launch_cfg<64, 2>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace msa

@@ -1,0 +1,239 @@
+// msa_internal.cuh -- shared device helpers and launch interfaces of libmsa.
+//
+// Blackwell (sm_103a) building blocks written as inline PTX: mbarriers,
+// 1-D bulk async copies (the TMA bulk engine), bounded waits, warp MMA.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "msa.h"
+
+namespace msa {
+
+constexpr int kBlock = 128;  // tokens per index block == tokens per KV page
+constexpr int kPage16 = 16;  // tokens per page of the attention view
+constexpr int kHeadDim = 128;
+constexpr int kMaxHeads = 16;
+constexpr int kMaxReqs = 4096;
+constexpr int kMaxBlocksPerRow = 16384;
+// bounded waits: a wait that has not completed after this long gives up
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
+
+// partial (m, l, acc) record of one attention split: m[16], l[16], acc[16][128]
+constexpr int kPartFloats = 2 * kMaxHeads + kMaxHeads * kHeadDim;
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+// make mbarrier initialisation visible to the async (bulk-copy) proxy
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; gives up after
+// kWaitNs and returns false (the caller records MSA_DEV_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitNs) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared, completion signalled on `bar` (tx bytes).
+// src, dst 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
+
+// bf16 pair (lo, hi halves of a 32-bit word) -> two fp32 (exact)
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// two OCP e4m3 codes (lo byte -> lo half) -> f16x2 (exact conversion)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t out;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(v));
+  return out;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t out;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(hi), "f"(lo));
+  return out;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t out;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(hi), "f"(lo));
+  return out;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t out;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(out) : "r"(a), "r"(b), "r"(sel));
+  return out;
+}
+
+// D = A(16x16, row) * B(16x8, col) + D; bf16 or f16 operands, fp32 accumulate
+template <bool kF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (kF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+// Orderable unsigned key of an fp32 score: a larger score gives a larger
+// key; -0 and +0 share a key; NaN maps to 0, below every number.
+__device__ __forceinline__ uint32_t score_key(float s) {
+  if (s != s) return 0u;
+  const uint32_t u = __float_as_uint(s + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// --------------------------------------------------- batch geometry checks
+
+// Request q's lengths.  Returns 0 if usable, else MSA_DEV_BAD_LEN or
+// MSA_DEV_MALFORMED; *nb = ceil(seq_len/128) when usable.
+__device__ __forceinline__ uint32_t request_lengths(const msa_batch& b, int q, int* q_begin,
+                                                    int* q_len, int* ctx, int* nb) {
+  const int c0 = b.cu_seqlens_q[q], c1 = b.cu_seqlens_q[q + 1];
+  const int slen = b.cu_seqlens_k[q + 1] - b.cu_seqlens_k[q];
+  *q_begin = c0;
+  *q_len = c1 - c0;
+  *ctx = b.context_lens[q];
+  *nb = 0;
+  if (slen < *q_len || *ctx < 0 || (long long)slen > (long long)kBlock * b.bt_stride)
+    return MSA_DEV_MALFORMED;
+  if (*ctx + *q_len != slen) return MSA_DEV_BAD_LEN;
+  *nb = (slen + kBlock - 1) / kBlock;
+  return 0u;
+}
+
+// ------------------------------------------------------- launch interfaces
+
+struct ScoreLaunch {
+  msa_batch batch;
+  const uint16_t* idx_q;
+  const uint8_t* idx_k;
+  int index_heads, index_dim;
+  float* scores;
+  int score_stride;
+  uint32_t* status;
+};
+
+struct TopkLaunch {
+  msa_batch batch;
+  const float* scores;
+  int score_stride;
+  int topk;
+  int32_t* topk_idx;
+  int32_t* tbl;
+  int tbl_stride;
+  int32_t* sparse_len;
+  uint32_t* attn_counters;  // zeroed per row when non-null (fused path)
+  uint32_t* status;
+};
+
+struct AttnLaunch {
+  const uint16_t* q;
+  int num_rows, num_heads;
+  const uint8_t* k;
+  const uint8_t* v;
+  int kv_fp8;
+  long long num_pages16;
+  int scale_mode;
+  const float* k_scale;
+  const float* v_scale;
+  const float* sinks;
+  float softmax_scale;
+  const int32_t* tbl;
+  int tbl_stride;
+  const int32_t* sparse_len;
+  uint16_t* out;
+  float* lse;
+  float* partials;
+  uint32_t* counters;
+  int splits;
+  int pages_per_split;  // page-16 entries per split
+  uint32_t* status;
+};
+
+cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream);
+cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream);
+cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace msa

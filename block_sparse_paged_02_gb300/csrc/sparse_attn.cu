@@ -1,0 +1,432 @@
+// sparse_attn.cu -- step 4: GQA flash-decode over the tokens a page-16 sparse
+// table addresses, with FP8 dequant scales, an optional per-head sink and a
+// natural-log LSE.
+//
+// Definitions: "Add ROCm AITER sparse paged attention for MiniMax-M3" (vLLM PR
+// 47287), "Implementation breakdown" items 2-3 (k_scale / v_scale, scalar or
+// per_token_head; page-16 view of the page-128 cache); "Attention sinks for
+// ROCm AITER sparse MLA" (vLLM PR 54404), "Features and motivation" (learnable
+// sinks; empty rows must not produce NaN) and "Key source snippets" (split-KV
+// decode returning a natural-log LSE, which every split count must write).
+//
+// GB300 design.  One KV head serves up to 16 query heads, so a row's heads x
+// 8 tokens form a real m16n8k16 tensor-core tile: S = Q K^T and O += P V run
+// on warp MMA with fp32 accumulation (the M = heads = 16 tile is below the
+// 64/128-row minimum of tcgen05, and the path is HBM-bound).  The row's
+// tokens are split across CTAs (grid = splits x rows, sized from the SM
+// count); each warp streams its page-16 K and V slabs (2-4 KB each,
+// contiguous) with 1-D bulk async copies into a private 4-deep shared-memory
+// ring, converts FP8 to f16 in registers (exact), applies per-token k scales
+// to the fp32 logits and folds per-token v scales into P.  Warps merge in
+// shared memory; splits merge through (m, l, acc) partials in the workspace,
+// finished by whichever CTA of the row arrives last (atomic counter, reset
+// by that CTA: no spin-wait anywhere).  The sink joins the denominator only
+// in the final merge.
+#include "msa_internal.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kAccStride = 132;  // padded head stride of the shared-memory merge area
+constexpr int kAccWarpFloats = kMaxHeads * kAccStride;  // 2112
+
+template <bool FP8>
+struct AttnCfg {
+  static constexpr int kElem = FP8 ? 1 : 2;
+  static constexpr int kSlab = kPage16 * kHeadDim * kElem;  // one page-16 K (or V) slab
+  static constexpr int kStageBytes = 2 * kSlab + 2 * 64;    // K, V, k-scales, v-scales
+  static constexpr int kStages = FP8 ? 4 : 3;
+  static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+  static constexpr int kMergeBytes = kWarps * (kAccWarpFloats + 2 * kMaxHeads) * 4;
+  static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+  static constexpr int kSmemBytes = kDataBytes + kWarps * kStages * 8 + 64;
+};
+
+__device__ __forceinline__ int acc_index(int head, int dim) {
+  return head * kAccStride + dim + (dim >> 5);
+}
+
+template <bool FP8, int SCALE>
+__global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(const AttnLaunch p) {
+  using C = AttnCfg<FP8>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
+  int* flags = reinterpret_cast<int*>(smem + C::kDataBytes + kWarps * C::kStages * 8);
+
+  const int split = blockIdx.x, r = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const long long tbl_row = (long long)r * p.tbl_stride;
+
+  // ---- validate the whole row (every split decides the same way)
+  int len = p.sparse_len[r];
+  bool poisoned = len < 0 || (long long)len > (long long)kPage16 * p.tbl_stride;
+  int nent = poisoned ? 0 : (len + kPage16 - 1) / kPage16;
+  int bad = 0;
+  for (int i = tid; i < nent; i += kThreads) {
+    const int e = p.tbl[tbl_row + i];
+    bad |= (e < 0 || (long long)e >= p.num_pages16);
+  }
+  poisoned = __syncthreads_or(bad) || poisoned;
+  if (poisoned) {
+    len = 0;
+    nent = 0;
+  }
+  const int n_active = max(1, (nent + p.pages_per_split - 1) / p.pages_per_split);
+  if (split >= n_active) return;
+  if (poisoned && split == 0 && tid == 0) atomicOr(p.status, MSA_DEV_BAD_TABLE);
+
+  // ---- this warp's page-16 entries: split*pps + warp + 4*i
+  const int e_begin = split * p.pages_per_split;
+  const int e_end = min(nent, e_begin + p.pages_per_split);
+  const int n_my = e_end > e_begin + warp ? (e_end - (e_begin + warp) + kWarps - 1) / kWarps : 0;
+  uint8_t* ring = smem + (size_t)warp * C::kStages * C::kStageBytes;
+  uint64_t* wbar = bars + warp * C::kStages;
+
+  auto issue = [&](int i) {  // lane 0 only
+    const int st = i % C::kStages;
+    const long long e = p.tbl[tbl_row + e_begin + warp + kWarps * i];
+    uint8_t* dst = ring + st * C::kStageBytes;
+    const uint32_t bytes = 2 * C::kSlab + (SCALE == MSA_SCALE_PER_TOKEN_HEAD ? 128 : 0);
+    mbar_arrive_expect_tx(&wbar[st], bytes);
+    bulk_g2s(dst, p.k + e * C::kSlab, C::kSlab, &wbar[st]);
+    bulk_g2s(dst + C::kSlab, p.v + e * C::kSlab, C::kSlab, &wbar[st]);
+    if constexpr (SCALE == MSA_SCALE_PER_TOKEN_HEAD) {
+      bulk_g2s(dst + 2 * C::kSlab, p.k_scale + e * kPage16, 64, &wbar[st]);
+      bulk_g2s(dst + 2 * C::kSlab + 64, p.v_scale + e * kPage16, 64, &wbar[st]);
+    }
+  };
+  if (lane == 0) {
+    for (int s = 0; s < C::kStages; ++s) mbar_init(&wbar[s], 1);
+    fence_barrier_init();
+    for (int i = 0; i < min(n_my, C::kStages); ++i) issue(i);
+  }
+  __syncwarp();
+
+  // ---- query fragments (A operand of S = Q K^T), permuted k-slots:
+  // k-step kk, slots (2c, 2c+1) <-> dims 32c+4kk+{0,1}; (2c+8, 2c+9) <-> +{2,3}
+  uint32_t qa[8][4];
+  {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q + (long long)r * p.num_heads * kHeadDim);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int h = g + 8 * half;
+        uint32_t w01 = 0, w23 = 0;
+        if (h < p.num_heads) {
+          const int d = 32 * c + 4 * kk;
+          w01 = q32[(h * kHeadDim + d) >> 1];
+          w23 = q32[(h * kHeadDim + d + 2) >> 1];
+        }
+        if constexpr (FP8) {  // f16 operands for the fp8 path
+          w01 = pack_f16x2(bf16lo(w01), bf16hi(w01));
+          w23 = pack_f16x2(bf16lo(w23), bf16hi(w23));
+        }
+        qa[kk][half] = w01;      // a0a1 (row g) / a2a3 (row g+8)
+        qa[kk][2 + half] = w23;  // a4a5 (row g) / a6a7 (row g+8)
+      }
+    }
+  }
+  float scale2 = p.softmax_scale * kLog2e;  // logits in log2 units
+  if constexpr (SCALE == MSA_SCALE_SCALAR) scale2 *= __ldg(p.k_scale);
+
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float o[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+  bool timed_out = false;
+  for (int i = 0; i < n_my; ++i) {
+    const int st = i % C::kStages;
+    if (!mbar_wait(&wbar[st], (i / C::kStages) & 1)) {
+      timed_out = true;
+      break;
+    }
+    const uint8_t* ks_ = ring + st * C::kStageBytes;
+    const uint8_t* vs_ = ks_ + C::kSlab;
+    const float* ksc = reinterpret_cast<const float*>(ks_ + 2 * C::kSlab);
+    const float* vsc = ksc + kPage16;
+    const int tok0 = (e_begin + warp + kWarps * i) * kPage16;  // row token index of slot 0
+    const int nvalid = min(kPage16, len - tok0);              // >= 1
+
+    // ---- S = Q K^T for the 16 tokens: two n-tiles (tokens g and 8+g)
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      const uint8_t* krow = ks_ + (8 * nt + g) * kHeadDim * C::kElem + 32 * c * C::kElem;
+      if constexpr (FP8) {
+        const uint4 k0 = lds128(krow), k1 = lds128(krow + 16);
+        const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma16816<true>(s[nt], qa[kk], e4m3x2_to_f16x2((uint16_t)(kw[kk] & 0xffffu)),
+                         e4m3x2_to_f16x2((uint16_t)(kw[kk] >> 16)));
+      } else {
+        uint32_t kw[16];
+#pragma unroll
+        for (int h4 = 0; h4 < 4; ++h4) {
+          const uint4 v = lds128(krow + 16 * h4);
+          kw[4 * h4] = v.x;
+          kw[4 * h4 + 1] = v.y;
+          kw[4 * h4 + 2] = v.z;
+          kw[4 * h4 + 3] = v.w;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma16816<false>(s[nt], qa[kk], kw[2 * kk], kw[2 * kk + 1]);
+      }
+    }
+    // ---- scale, mask, online softmax (rows g and g+8)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = 8 * nt + 2 * c + (e & 1);
+        float v = s[nt][e] * scale2;
+        if constexpr (SCALE == MSA_SCALE_PER_TOKEN_HEAD) v *= ksc[t];
+        s[nt][e] = t < nvalid ? v : -INFINITY;
+      }
+    float mx[2];
+    mx[0] = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    mx[1] = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+    float alpha[2], base[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 1));
+      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
+      const float mn = fmaxf(m_run[hh], mx[hh]);
+      alpha[hh] = m_run[hh] == -INFINITY ? 0.f : exp2f(m_run[hh] - mn);
+      base[hh] = mn == -INFINITY ? 0.f : mn;
+      m_run[hh] = mn;
+    }
+    float pr[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pr[nt][e] = exp2f(s[nt][e] - base[e >> 1]);
+    l_run[0] = l_run[0] * alpha[0] + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
+    l_run[1] = l_run[1] * alpha[1] + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      o[j][0] *= alpha[0];
+      o[j][1] *= alpha[0];
+      o[j][2] *= alpha[1];
+      o[j][3] *= alpha[1];
+    }
+    if constexpr (SCALE == MSA_SCALE_PER_TOKEN_HEAD) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pr[nt][e] *= vsc[8 * nt + 2 * c + (e & 1)];
+    }
+    // P as the A operand of O += P V: tokens (2c, 2c+1) from n-tile 0, (2c+8, 2c+9) from 1
+    uint32_t pa[4];
+    if constexpr (FP8) {
+      pa[0] = pack_f16x2(pr[0][0], pr[0][1]);
+      pa[1] = pack_f16x2(pr[0][2], pr[0][3]);
+      pa[2] = pack_f16x2(pr[1][0], pr[1][1]);
+      pa[3] = pack_f16x2(pr[1][2], pr[1][3]);
+    } else {
+      pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+      pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+      pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+      pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+    }
+    // ---- V fragments: tokens {2c, 2c+1, 2c+8, 2c+9}, dims 16g + j for n-tile j
+    const int vt[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+    if constexpr (FP8) {
+      uint32_t vw[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const uint4 v = lds128(vs_ + vt[a] * kHeadDim + 16 * g);
+        const bool ok = vt[a] < nvalid;  // never let garbage past the end reach P V
+        vw[a][0] = ok ? v.x : 0u;
+        vw[a][1] = ok ? v.y : 0u;
+        vw[a][2] = ok ? v.z : 0u;
+        vw[a][3] = ok ? v.w : 0u;
+      }
+#pragma unroll
+      for (int j2 = 0; j2 < 8; ++j2) {  // n-tiles 2*j2, 2*j2+1
+        const int wi = j2 >> 1, by = 2 * (j2 & 1);
+        const uint32_t sel = (uint32_t)(by | ((4 + by) << 4) | ((by + 1) << 8) | ((5 + by) << 12));
+        const uint32_t lo = prmt(vw[0][wi], vw[1][wi], sel);  // tokens 2c, 2c+1
+        const uint32_t hi = prmt(vw[2][wi], vw[3][wi], sel);  // tokens 2c+8, 2c+9
+        mma16816<true>(o[2 * j2], pa, e4m3x2_to_f16x2((uint16_t)(lo & 0xffffu)),
+                       e4m3x2_to_f16x2((uint16_t)(hi & 0xffffu)));
+        mma16816<true>(o[2 * j2 + 1], pa, e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
+                       e4m3x2_to_f16x2((uint16_t)(hi >> 16)));
+      }
+    } else {
+      uint32_t vw[4][8];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const uint8_t* src = vs_ + (vt[a] * kHeadDim + 16 * g) * 2;
+        const uint4 v0 = lds128(src), v1 = lds128(src + 16);
+        const bool ok = vt[a] < nvalid;
+        vw[a][0] = ok ? v0.x : 0u;
+        vw[a][1] = ok ? v0.y : 0u;
+        vw[a][2] = ok ? v0.z : 0u;
+        vw[a][3] = ok ? v0.w : 0u;
+        vw[a][4] = ok ? v1.x : 0u;
+        vw[a][5] = ok ? v1.y : 0u;
+        vw[a][6] = ok ? v1.z : 0u;
+        vw[a][7] = ok ? v1.w : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+        const uint32_t b0 = prmt(vw[0][j >> 1], vw[1][j >> 1], sel);
+        const uint32_t b1 = prmt(vw[2][j >> 1], vw[3][j >> 1], sel);
+        mma16816<false>(o[j], pa, b0, b1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && i + C::kStages < n_my) {
+      fence_proxy_async_smem();
+      issue(i + C::kStages);
+    }
+  }
+  if (timed_out && lane == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 1);
+    l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 2);
+  }
+
+  // ---- merge the 4 warps in shared memory (reusing the ring)
+  __syncthreads();
+  float* acc_s = reinterpret_cast<float*>(smem);
+  float* ml_s = acc_s + kWarps * kAccWarpFloats;  // [warp][m 16 | l 16]
+  {
+    float* aw = acc_s + warp * kAccWarpFloats;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      aw[acc_index(g, 32 * c + j)] = o[j][0];
+      aw[acc_index(g, 32 * c + 16 + j)] = o[j][1];
+      aw[acc_index(g + 8, 32 * c + j)] = o[j][2];
+      aw[acc_index(g + 8, 32 * c + 16 + j)] = o[j][3];
+    }
+    if (c == 0) {
+      ml_s[warp * 32 + g] = m_run[0];
+      ml_s[warp * 32 + g + 8] = m_run[1];
+      ml_s[warp * 32 + 16 + g] = l_run[0];
+      ml_s[warp * 32 + 16 + g + 8] = l_run[1];
+    }
+  }
+  __syncthreads();
+  // thread t: head t/8, dims 16*(t%8) .. +16
+  const int head = tid >> 3, d0 = 16 * (tid & 7);
+  float mh = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) mh = fmaxf(mh, ml_s[w * 32 + head]);
+  float lh = 0.f, acc[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const float mw = ml_s[w * 32 + head];
+    const float f = mw == -INFINITY ? 0.f : exp2f(mw - mh);
+    lh += f * ml_s[w * 32 + 16 + head];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] += f * acc_s[w * kAccWarpFloats + acc_index(head, d0 + j)];
+  }
+
+  if (n_active > 1) {
+    // ---- publish this split's partial; the last CTA of the row merges all
+    float* part = p.partials + ((long long)r * p.splits + split) * kPartFloats;
+    if ((tid & 7) == 0) {
+      part[head] = mh;
+      part[kMaxHeads + head] = lh;
+    }
+    float4* pa4 = reinterpret_cast<float4*>(part + 2 * kMaxHeads + head * kHeadDim + d0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      pa4[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) flags[0] = (atomicAdd(&p.counters[r], 1u) == (unsigned)(n_active - 1));
+    __syncthreads();
+    if (!flags[0]) return;
+    __threadfence();
+    mh = -INFINITY;
+    for (int sp = 0; sp < n_active; ++sp)
+      mh = fmaxf(mh, __ldcg(p.partials + ((long long)r * p.splits + sp) * kPartFloats + head));
+    lh = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    for (int sp = 0; sp < n_active; ++sp) {
+      const float* ps = p.partials + ((long long)r * p.splits + sp) * kPartFloats;
+      const float ms = __ldcg(ps + head);
+      const float f = ms == -INFINITY ? 0.f : exp2f(ms - mh);
+      lh += f * __ldcg(ps + kMaxHeads + head);
+      const float4* a4 = reinterpret_cast<const float4*>(ps + 2 * kMaxHeads + head * kHeadDim + d0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 v = __ldcg(a4 + j);
+        acc[4 * j] += f * v.x;
+        acc[4 * j + 1] += f * v.y;
+        acc[4 * j + 2] += f * v.z;
+        acc[4 * j + 3] += f * v.w;
+      }
+    }
+    if (tid == 0) p.counters[r] = 0;  // ready for the next call / graph replay
+  }
+
+  // ---- finalize: sink in the denominator, natural-log LSE
+  if (head < p.num_heads) {
+    float M = mh, Lsum = lh;
+    if (p.sinks) {
+      const float sink2 = __ldg(p.sinks + head) * kLog2e;
+      const float Mn = fmaxf(M, sink2);
+      Lsum = (M == -INFINITY ? 0.f : Lsum * exp2f(M - Mn)) + exp2f(sink2 - Mn);
+      const float f = M == -INFINITY ? 0.f : exp2f(M - Mn);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] *= f;
+      M = Mn;
+    }
+    float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
+    if constexpr (SCALE == MSA_SCALE_SCALAR) inv *= __ldg(p.v_scale);
+    uint32_t packed[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) packed[j] = pack_bf16x2(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+    uint4* dst = reinterpret_cast<uint4*>(p.out + ((long long)r * p.num_heads + head) * kHeadDim + d0);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    if ((tid & 7) == 0)
+      p.lse[(long long)r * p.num_heads + head] =
+          (M == -INFINITY || Lsum <= 0.f) ? -INFINITY : (M + log2f(Lsum)) * kLn2;
+  }
+}
+
+template <bool FP8, int SCALE>
+cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t stream) {
+  using C = AttnCfg<FP8>;
+  auto kern = sparse_attn_kernel<FP8, SCALE>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.splits, p.num_rows);
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t stream) {
+  if (p.num_rows == 0) return cudaSuccess;
+  if (p.kv_fp8) {
+    if (p.scale_mode == MSA_SCALE_NONE) return launch_cfg<true, MSA_SCALE_NONE>(p, stream);
+    if (p.scale_mode == MSA_SCALE_SCALAR) return launch_cfg<true, MSA_SCALE_SCALAR>(p, stream);
+    return launch_cfg<true, MSA_SCALE_PER_TOKEN_HEAD>(p, stream);
+  }
+  if (p.scale_mode == MSA_SCALE_NONE) return launch_cfg<false, MSA_SCALE_NONE>(p, stream);
+  if (p.scale_mode == MSA_SCALE_SCALAR) return launch_cfg<false, MSA_SCALE_SCALAR>(p, stream);
+  return launch_cfg<false, MSA_SCALE_PER_TOKEN_HEAD>(p, stream);
+}
+
+}  // namespace msa

@@ -1,0 +1,238 @@
+/*
+ * msa.h -- C ABI of libmsa: block-sparse paged decode for MiniMax-M3-style
+ * sparse attention on one GB300 (sm_103a).
+ *
+ * Per query row the path scores every cached 128-token block with an index
+ * query, keeps the top-k blocks, expands them into a page-16 sparse block
+ * table, and runs GQA attention over only those tokens (bf16 or FP8-e4m3
+ * KV with optional dequant scales, optional per-head sink, natural-log LSE).
+ *
+ * Definitions come from the MiniMax-M3 sparse-attention pages:
+ *   [P47287] "Add ROCm AITER sparse paged attention for MiniMax-M3"
+ *            (vLLM PR 47287)
+ *   [P54682] "Optimise MiniMax-M3 decode index and top-k on gfx950"
+ *            (vLLM PR 54682)
+ *   [P54404] "Attention sinks for ROCm AITER sparse MLA" (vLLM PR 54404)
+ *   [P56170] "Device-side zeroing of cu_seqlens_k[0] for MiniMax M3"
+ *            (vLLM PR 56170)
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller; the library keeps no
+ *     reference after the call returns and never allocates, frees or copies
+ *     between host and device.
+ *   - Work is enqueued on `stream` and is asynchronous.  No entry point
+ *     synchronises the host (no blocking copy, no stream sync), so a
+ *     sequence of calls can be captured into a CUDA graph.
+ *   - Argument errors are detected on the host before anything is launched
+ *     and returned as an msa_status.  Errors in device-side data (page ids,
+ *     lengths) cannot be seen on the host without a sync; kernels set bits
+ *     in the caller's `dev_status` word (atomicOr, never cleared by the
+ *     library), give the affected rows defined "empty" outputs and never
+ *     trap.  Clear the word before a call if you want per-call bits.
+ *   - Arrays are row-major and densely packed unless a stride is given.
+ *     Device pointers must be 16-byte aligned.
+ */
+#ifndef MSA_H
+#define MSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum msa_status {
+  MSA_OK = 0,
+  MSA_ERR_NULL = 1,        /* a required pointer is NULL */
+  MSA_ERR_SHAPE = 2,       /* inconsistent sizes or strides, misaligned pointer */
+  MSA_ERR_DTYPE = 3,       /* unknown kv dtype or scale mode */
+  MSA_ERR_UNSUPPORTED = 4, /* valid but not built: see each entry point */
+  MSA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than msa_workspace_size() */
+  MSA_ERR_CUDA = 6         /* a CUDA launch failed (cudaGetLastError after launch) */
+} msa_status;
+
+/* KV cache element types */
+enum { MSA_KV_BF16 = 0, MSA_KV_FP8_E4M3 = 1 };
+/* KV dequant scale modes [P47287 "Implementation breakdown" item 2] */
+enum { MSA_SCALE_NONE = 0, MSA_SCALE_SCALAR = 1, MSA_SCALE_PER_TOKEN_HEAD = 2 };
+
+/* Device status bits (atomicOr into *dev_status).  A "poisoned" row gets
+ * the outputs of an empty row: scores not written, topk_idx = -1, table =
+ * 0, sparse_len = 0, O = 0, LSE = sink (or -inf without a sink). */
+#define MSA_DEV_BAD_PAGE 1u  /* a request's block table holds a page id outside [0, num_pages)
+                                for one of its ceil(seq_len/128) blocks: its rows are poisoned */
+#define MSA_DEV_BAD_LEN 2u   /* context_lens[q] + q_len != seq_len: the request is poisoned
+                                [P56170 "Implementation breakdown" item 3] */
+#define MSA_DEV_MALFORMED 4u /* cu_seqlens_q does not tile [0, num_rows), seq_len < q_len,
+                                context_len < 0, or seq_len > 128 * bt_stride */
+#define MSA_DEV_BAD_TABLE 8u /* sparse table entry outside the page-16 pool, or sparse_len
+                                < 0 or > 16 * tbl_stride: the row is poisoned */
+#define MSA_DEV_TIMEOUT 16u  /* a bounded wait inside a kernel gave up (hardware stall);
+                                outputs of that call are unspecified */
+
+/* Batch geometry: the attention-metadata inputs of [P56170 "Key source
+ * snippets"] (the prefill metadata record) and [P54682 "Implementation
+ * breakdown" item 2].  All arrays are device int32.
+ *   cu_seqlens_q [R+1]  rows of request q are [cu_q[q], cu_q[q+1]); must be
+ *                       non-decreasing with cu_q[0] = 0, cu_q[R] = num_rows
+ *   cu_seqlens_k [R+1]  seq_len of request q = cu_k[q+1] - cu_k[q] (the
+ *                       pages keep cu_k[0] = 0; only differences are used)
+ *   context_lens [R]    tokens cached before this step; row j of request q
+ *                       sits at absolute position context_lens[q] + j and
+ *                       sees tokens 0..position (causal)
+ *   block_table  [R, bt_stride]  page-128 physical page of each logical
+ *                       128-token block; only the first ceil(seq_len/128)
+ *                       entries of a row are read
+ *   num_pages    P, the number of page-128 pages in the pools (bounds check) */
+typedef struct msa_batch {
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  const int32_t* context_lens;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  int32_t num_reqs;
+  int32_t num_rows;
+  int32_t num_pages;
+} msa_batch;
+
+/* Attention operands [P47287 "Implementation breakdown" items 2-3],
+ * [P54404 "Key source snippets"].
+ *   q        [num_rows, num_heads, head_dim] bf16
+ *   k_cache, v_cache  page-128 pools [P, 128, num_kv_heads, head_dim] of
+ *            kv_dtype; the page-16 view [8P, 16, num_kv_heads, head_dim] is
+ *            the same bytes (page-16 id e = 8 * page128 + j)
+ *   scale_mode NONE: k_scale/v_scale ignored (may be NULL)
+ *            SCALAR: k_scale, v_scale each fp32 [1]
+ *            PER_TOKEN_HEAD: fp32 [P, 128, num_kv_heads], paged like K/V
+ *            The dequantised key is k_scale * k, the value v_scale * v.
+ *   sinks    fp32 [num_heads] learnable sink logits, or NULL for none; a
+ *            sink adds exp(sink_h) to head h's softmax denominator
+ *   softmax_scale  logit = softmax_scale * (q . k_dequantised)
+ *   out      [num_rows, num_heads, head_dim] bf16
+ *   lse      [num_rows, num_heads] fp32, natural log of the denominator
+ *            out was normalised by (sink term included)
+ * Supported: num_kv_heads == 1 (one KV head per rank, as on [P47287 "Risks
+ * and impact" item 4]), head_dim == 128, 1 <= num_heads <= 16.  Others
+ * return MSA_ERR_UNSUPPORTED.  With FP8 KV the query is converted to fp16
+ * for the tensor-core products, so |q| must stay below 65504. */
+typedef struct msa_attn_args {
+  const void* q;
+  int32_t num_rows;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  const void* k_cache;
+  const void* v_cache;
+  int32_t kv_dtype;
+  int32_t num_pages; /* P, page-128 pages in the pools */
+  int32_t scale_mode;
+  const float* k_scale;
+  const float* v_scale;
+  const float* sinks;
+  float softmax_scale;
+  void* out;
+  float* lse;
+} msa_attn_args;
+
+/* Optional CUDA events msa_decode records on `stream` after each stage (for
+ * timing; any may be NULL). */
+typedef struct msa_trace {
+  cudaEvent_t after_score;
+  cudaEvent_t after_topk;
+  cudaEvent_t after_attn;
+} msa_trace;
+
+/* Step 1, index scoring [P54682 "Implementation breakdown" item 1; the
+ * balanced scorer of "Key files" that maps work by each request's actual
+ * block count and shares index-K tiles across a request's query rows].
+ * For each row r (request q, position pos) and block b < nb_r =
+ * ceil((pos+1)/128):
+ *     scores[r*score_stride + b] = max over index heads h and tokens
+ *         t in [128b, min(128b+127, pos)] of  sum_d idx_q[r,h,d]*idx_k[t,h,d]
+ * with idx_k addressed through the block table (token t of the request
+ * lives at page block_table[q, t/128], slot t%128), accumulated in fp32.
+ *   idx_q       [num_rows, index_heads, index_dim] bf16
+ *   idx_k_cache [P, 128, index_heads, index_dim] bf16
+ *   scores      [num_rows, score_stride] fp32; score_stride >= bt_stride.
+ *               Entries b >= nb_r, and rows of poisoned requests, are not
+ *               written; a block whose page id is out of range scores -inf.
+ * Supported (index_heads, index_dim): (1, 64), (2, 64), (1, 128);
+ * num_reqs <= 4096. */
+msa_status msa_index_score(const msa_batch* batch, const void* idx_q, const void* idx_k_cache,
+                           int32_t index_heads, int32_t index_dim, float* scores,
+                           int32_t score_stride, uint32_t* dev_status, cudaStream_t stream);
+
+/* Steps 2+3, top-k selection fused with the page-16 table build and the
+ * context-length clamp [P54682 "Implementation breakdown" items 1 and 4;
+ * P47287 "Implementation breakdown" item 3 and "Review highlights"].
+ * For each row r with nb_r candidate blocks:
+ *   - select m = min(topk, nb_r) blocks with the highest scores; equal scores
+ *     go to the lower block index; NaN ranks below every number;
+ *   - topk_idx[r, 0..m) = the selected blocks in ASCENDING block order,
+ *     topk_idx[r, m..topk) = -1;
+ *   - for the i-th selected block b with page p = block_table[q, b] and
+ *     valid = min(128, pos+1 - 128b):
+ *       sparse_tbl[r, 8i + j] = 8p + j   for j < ceil(valid/16)
+ *     every other entry of the row up to tbl_stride is 0;
+ *   - sparse_len[r] = sum of valid over the selected blocks, so token n of
+ *     the row lives at page-16 sparse_tbl[r, n/16], slot n%16.
+ *   scores   [num_rows, score_stride] fp32 (only b < nb_r is read)
+ *   topk_idx [num_rows, topk] int32
+ *   sparse_tbl [num_rows, tbl_stride] int32, tbl_stride >= 8*topk
+ *   sparse_len [num_rows] int32
+ * Supported: bt_stride <= 16384. */
+msa_status msa_topk_build_table(const msa_batch* batch, const float* scores,
+                                int32_t score_stride, int32_t topk, int32_t* topk_idx,
+                                int32_t* sparse_tbl, int32_t tbl_stride, int32_t* sparse_len,
+                                uint32_t* dev_status, cudaStream_t stream);
+
+/* Step 4, sparse paged GQA attention [P47287 "Implementation breakdown"
+ * items 2-3; P54404 "Features and motivation", "Key source snippets"].
+ * For row r and head h (KV head h / (num_heads/num_kv_heads)) over the
+ * n = sparse_len[r] tokens the table addresses:
+ *   s_t = softmax_scale * k_scale_t * (q_h . k_t),  m = max(max_t s_t, sink_h)
+ *   den = sum_t exp(s_t - m) + exp(sink_h - m)
+ *   out = sum_t exp(s_t - m) * v_scale_t * v_t / den,  lse = m + ln(den)
+ * (no sink: the sink terms are absent).  An empty row gives out = 0 and
+ * lse = sink_h (or -inf).  The work is split along the tokens; partial
+ * results are merged through their LSE inside the call.
+ *   sparse_tbl [num_rows, tbl_stride] int32 page-16 ids, sparse_len [num_rows]
+ *   workspace  device scratch of msa_workspace_size(...) bytes; its first
+ *              use must find it zero-filled (cudaMemset once); every call
+ *              leaves the counters it uses back at zero.  Calls that share a
+ *              workspace must be ordered on one stream. */
+msa_status msa_sparse_paged_attn(const msa_attn_args* attn, const int32_t* sparse_tbl,
+                                 int32_t tbl_stride, const int32_t* sparse_len, void* workspace,
+                                 size_t workspace_bytes, uint32_t* dev_status,
+                                 cudaStream_t stream);
+
+/* The whole path: msa_index_score -> msa_topk_build_table ->
+ * msa_sparse_paged_attn in stream order, with the intermediates held in the
+ * workspace [P54682 "Implementation breakdown" items 2-3: the indexer writes
+ * the sparse table the attention consumes].  Results are bit-identical to
+ * the three separate calls.  topk_idx, sparse_tbl and sparse_len may be NULL
+ * (kept in the workspace) or device arrays that receive them; tbl_stride is
+ * the width of the caller's sparse_tbl (>= 8*topk, ignored when NULL).
+ * trace may be NULL. */
+msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx_k_cache,
+                      int32_t index_heads, int32_t index_dim, int32_t topk,
+                      const msa_attn_args* attn, int32_t* topk_idx, int32_t* sparse_tbl,
+                      int32_t tbl_stride, int32_t* sparse_len, void* workspace,
+                      size_t workspace_bytes, uint32_t* dev_status, const msa_trace* trace,
+                      cudaStream_t stream);
+
+/* Bytes of workspace msa_decode (bt_stride > 0) or msa_sparse_paged_attn
+ * (bt_stride = 0, topk = 0) needs for these sizes. */
+size_t msa_workspace_size(int32_t num_rows, int32_t bt_stride, int32_t topk, int32_t num_heads,
+                          int32_t head_dim, int32_t tbl_stride);
+
+/* Static description of a status code. */
+const char* msa_status_string(msa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MSA_H */

@@ -1,0 +1,58 @@
+"""Shared test helpers: tolerances, comparisons and sampled-row sub-batches."""
+import numpy as np
+
+import workloads as W
+
+# Attention tolerance for bf16/FP8 KV against the fp64 oracle:
+# |O - O_ref| <= 1e-2 * (1 + |O_ref|), |LSE - LSE_ref| <= 2e-3.
+O_RTOL = 1e-2
+LSE_ATOL = 2e-3
+
+
+def assert_attn_close(out, lse, ref_out, ref_lse, rows=None):
+    out = np.asarray(out, np.float64)
+    ref_out = np.asarray(ref_out, np.float64)
+    if rows is not None:
+        out, lse = out[rows], np.asarray(lse)[rows]
+    err = np.abs(out - ref_out)
+    bound = O_RTOL * (1.0 + np.abs(ref_out))
+    bad = ~(err <= bound)
+    assert not bad.any(), (f"O mismatch at {np.argwhere(bad)[:5].tolist()}: "
+                           f"max err/bound {float(np.max(err / bound)):.3f}")
+    lse = np.asarray(lse, np.float64)
+    ref_lse = np.asarray(ref_lse, np.float64)
+    both_inf = np.isneginf(lse) & np.isneginf(ref_lse)
+    lerr = np.where(both_inf, 0.0, np.abs(lse - ref_lse))
+    assert np.all(lerr <= LSE_ATOL), f"LSE max err {float(np.nanmax(lerr))}"
+
+
+def valid_score_mask(geom, score_stride):
+    """Entries the score kernel defines: rows that are scored, b < nb_r."""
+    n = len(geom["nb"])
+    mask = np.zeros((n, score_stride), bool)
+    for r in range(n):
+        if geom["ok"][r] != 0:
+            mask[r, : geom["nb"][r]] = True
+    return mask
+
+
+def sub_workload(w, rows):
+    """A batch holding only the given rows, each as its own one-row request at
+    the same position over the same pages and caches.  A row's result depends
+    only on its own position, query and its request's pages, so the oracle on
+    this batch reproduces those rows of the full batch."""
+    req_of = np.searchsorted(w.cu_seqlens_q, np.arange(w.num_rows), side="right") - 1
+    rows = np.asarray(rows)
+    pos = np.array([w.context_lens[req_of[r]] + (r - w.cu_seqlens_q[req_of[r]]) for r in rows])
+    seq = pos + 1
+    n = len(rows)
+    cu = np.arange(n + 1, dtype=np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(seq)]).astype(np.int32)
+    sub = W.Workload(name=w.name + "_rows", cu_seqlens_q=cu, cu_seqlens_k=cu_k,
+                     context_lens=pos.astype(np.int32),
+                     block_table=w.block_table[req_of[rows]].copy(), num_pages=w.num_pages,
+                     idx_q=w.idx_q[rows], idx_k=w.idx_k, topk=w.topk, q=w.q[rows],
+                     k_cache=w.k_cache, v_cache=w.v_cache, kv_dtype=w.kv_dtype,
+                     scale_mode=w.scale_mode, k_scale=w.k_scale, v_scale=w.v_scale,
+                     sinks=w.sinks, softmax_scale=w.softmax_scale, seed=w.seed)
+    return sub

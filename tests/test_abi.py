@@ -1,0 +1,104 @@
+"""The C ABI library builds for sm_103a, loads, and exports every entry point
+include/msa.h declares; host-side argument validation needs no GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "msa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_paged_02_gb300 import binding
+    return binding.lib()
+
+
+def test_header_declares_the_path(lib):
+    syms = declared_symbols()
+    for name in ("msa_index_score", "msa_topk_build_table", "msa_sparse_paged_attn",
+                 "msa_decode", "msa_workspace_size", "msa_status_string"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    from block_sparse_paged_02_gb300 import binding as B
+    for code in range(7):
+        assert B.msa_status_string(code)
+    assert "NULL" in B.msa_status_string(B.MSA_ERR_NULL)
+
+
+def test_workspace_size_grows_with_rows(lib):
+    from block_sparse_paged_02_gb300 import binding as B
+    a = B.msa_workspace_size(8, 256, 16, 16, 128, 128)
+    b = B.msa_workspace_size(64, 1024, 16, 16, 128, 128)
+    assert 0 < a < b
+    assert B.msa_workspace_size(64, 0, 0, 16, 128, 128) > 0
+    assert B.msa_workspace_size(-1, 0, 0, 16, 128, 128) == 0
+
+
+def test_host_validation_without_gpu(lib):
+    from block_sparse_paged_02_gb300 import binding as B
+    # NULL batch / NULL args are rejected before any launch
+    assert lib.msa_index_score(None, None, None, 1, 128, None, 1, None, None) == B.MSA_ERR_NULL
+    assert lib.msa_topk_build_table(None, None, 1, 4, None, None, 32, None, None, None) == \
+        B.MSA_ERR_NULL
+    assert lib.msa_sparse_paged_attn(None, None, 32, None, None, 0, None, None) == B.MSA_ERR_NULL
+    b = B.msa_batch(None, None, None, None, 4, 1, 1, 10)
+    assert lib.msa_index_score(ctypes.byref(b), None, None, 1, 128, None, 4, None, None) == \
+        B.MSA_ERR_NULL
+    fake = ctypes.c_void_p(0x10000)
+    b = B.msa_batch(fake, fake, fake, fake, 4, 1, 1, 10)
+    st = ctypes.c_void_p(0x20000)
+    # unsupported index geometry, score stride below the block-table width
+    assert lib.msa_index_score(ctypes.byref(b), fake, fake, 3, 128, fake, 4, st, None) == \
+        B.MSA_ERR_UNSUPPORTED
+    assert lib.msa_index_score(ctypes.byref(b), fake, fake, 1, 128, fake, 3, st, None) == \
+        B.MSA_ERR_SHAPE
+    # table narrower than 8*topk
+    assert lib.msa_topk_build_table(ctypes.byref(b), fake, 4, 4, fake, fake, 31, fake, st,
+                                    None) == B.MSA_ERR_SHAPE
+    # attention: 2 KV heads, head_dim 64, 17 heads, bad dtype -> rejected
+    def attn(**kw):
+        a = dict(q=fake, num_rows=1, num_heads=16, num_kv_heads=1, head_dim=128, k_cache=fake,
+                 v_cache=fake, kv_dtype=0, num_pages=1, scale_mode=0, k_scale=None,
+                 v_scale=None, sinks=None, softmax_scale=0.1, out=fake, lse=fake)
+        a.update(kw)
+        return B.msa_attn_args(**a)
+    ws = ctypes.c_void_p(0x30000)
+    call = lambda a, n=1 << 30: lib.msa_sparse_paged_attn(ctypes.byref(a), fake, 32, fake, ws, n,
+                                                          st, None)
+    assert call(attn(num_kv_heads=2, num_heads=16)) == B.MSA_ERR_UNSUPPORTED
+    assert call(attn(head_dim=64)) == B.MSA_ERR_UNSUPPORTED
+    assert call(attn(num_heads=17)) == B.MSA_ERR_UNSUPPORTED
+    assert call(attn(num_heads=16, num_kv_heads=3)) == B.MSA_ERR_SHAPE
+    assert call(attn(kv_dtype=7)) == B.MSA_ERR_DTYPE
+    assert call(attn(scale_mode=1)) == B.MSA_ERR_NULL  # scalar scales need pointers
+    assert call(attn(q=ctypes.c_void_p(0x10004))) == B.MSA_ERR_SHAPE  # misaligned
+    assert call(attn(), n=16) == B.MSA_ERR_WORKSPACE
+
+
+def test_sinks_contract_checked_in_binding():
+    import torch
+    from block_sparse_paged_02_gb300 import binding as B
+    B.check_sinks(None, 16)
+    B.check_sinks(torch.zeros(16), 16)
+    with pytest.raises(ValueError):
+        B.check_sinks(torch.zeros(16, dtype=torch.float16), 16)
+    with pytest.raises(ValueError):
+        B.check_sinks(torch.zeros(8), 16)
+    with pytest.raises(ValueError):
+        B.check_sinks(torch.zeros(32)[::2], 16)

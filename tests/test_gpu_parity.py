@@ -1,0 +1,308 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Block scores, top-k indices, page-16 tables and sparse lengths must be
+bit-exact (integer-valued index vectors make every fp32 score exact);
+attention must satisfy |O - O_ref| <= 1e-2 (1 + |O_ref|) and
+|LSE - LSE_ref| <= 2e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.helpers import assert_attn_close, sub_workload, valid_score_mask
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def msa():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import block_sparse_paged_02_gb300 as m
+    m.lib()
+    return m
+
+
+def run_steps(msa, w, **kw):
+    """Run the three entry points separately, then the fused call, and return
+    the separate results plus the fused ones."""
+    c = msa.DeviceCase(w, **kw)
+    c.index_score()
+    c.topk_build_table()
+    c.sparse_paged_attn()
+    sep = c.fetch()
+    # fused path into fresh outputs
+    c.out.zero_()
+    c.lse.zero_()
+    c.topk_idx.fill_(123)
+    c.tbl.fill_(123)
+    c.sparse_len.fill_(123)
+    c.decode()
+    fused = c.fetch()
+    return c, sep, fused
+
+
+def check_against_oracle(orc, w, sep, fused, topk=None):
+    k = int(topk or w.topk)
+    b = orc.Batch.of(w)
+    geom = orc.row_geometry(b)
+    ref = orc.decode(w, topk=k)
+    mask = valid_score_mask(geom, w.bt_stride)
+    assert np.array_equal(sep["scores"][mask], ref["scores"][mask]), "block scores differ"
+    assert np.array_equal(sep["topk_idx"], ref["topk_idx"]), "top-k indices differ"
+    assert np.array_equal(sep["sparse_len"], ref["sparse_len"]), "sparse lengths differ"
+    assert np.array_equal(sep["tbl"][:, : 8 * k], ref["tbl"][:, : 8 * k]), "sparse tables differ"
+    assert np.all(sep["tbl"][:, 8 * k:] == 0)
+    assert sep["status"] == ref["status"]
+    assert_attn_close(sep["out"], sep["lse"], ref["out"], ref["lse"])
+    # the fused call is bit-identical to the separate calls
+    for key in ("topk_idx", "tbl", "sparse_len", "out", "lse"):
+        assert np.array_equal(fused[key], sep[key], equal_nan=True), f"fused {key} differs"
+    return ref
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "batched_decode", "speculative_decode",
+                                  "large_batch_decode"])
+def test_named_workload_full_size(msa, orc, name):
+    w = W.NAMED[name]()
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+def test_chunked_prefill_full_size_sampled_rows(msa, orc):
+    w = W.chunked_prefill()
+    _, sep, fused = run_steps(msa, w)
+    for key in ("topk_idx", "tbl", "sparse_len", "out", "lse"):
+        assert np.array_equal(fused[key], sep[key], equal_nan=True)
+    rng = np.random.default_rng(0)
+    # first/last rows of each request, rows around block boundaries, random rows
+    rows = {0, 1, 127, 128, 2047, 2048, 2049, 4095}
+    rows |= set(int(x) for x in rng.choice(w.num_rows, 40, replace=False))
+    rows = np.array(sorted(rows))
+    sub = sub_workload(w, rows)
+    ref = orc.decode(sub)
+    assert ref["status"] == 0 and sep["status"] == 0
+    assert np.array_equal(sep["topk_idx"][rows], ref["topk_idx"])
+    assert np.array_equal(sep["tbl"][rows], ref["tbl"])
+    assert np.array_equal(sep["sparse_len"][rows], ref["sparse_len"])
+    nb = ref["tbl"].shape[1]
+    assert_attn_close(sep["out"][rows], sep["lse"][rows], ref["out"], ref["lse"])
+    # every row: the length is the clamp of the selected blocks, the table has
+    # exactly ceil(len/16) leading non-empty slots per selected block pattern
+    L = (w.context_lens[0] + np.arange(2048) + 1)
+    assert np.all(sep["sparse_len"][:2048] <= np.minimum(L, 16 * 128))
+
+
+def test_chunked_prefill_small_elementwise(msa, orc):
+    w = W.chunked_prefill(seed=15, context=1000, new_tokens=300, reqs=2)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8])
+@pytest.mark.parametrize("scale", [W.SCALE_NONE, W.SCALE_SCALAR, W.SCALE_PER_TOKEN_HEAD])
+@pytest.mark.parametrize("sink", [False, True])
+def test_dtype_scale_sink_matrix(msa, orc, kv, scale, sink):
+    w = W.custom(40 + 3 * kv + scale, q_lens=[1, 4, 2, 1, 3],
+                 seq_lens=[5000, 2100, 700, 130, 9000], hq=16, di=128, topk=8, kv_dtype=kv,
+                 scale_mode=scale, with_sink=sink)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+def test_edge_lengths_and_empty_requests(msa, orc):
+    seq = [1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 2000, 3, 640]
+    ql = [1, 1, 1, 2, 1, 0, 4, 1, 0, 3, 1, 2, 1]
+    w = W.custom(50, q_lens=ql, seq_lens=seq, hq=8, di=64, topk=3, kv_dtype=W.KV_FP8,
+                 scale_mode=W.SCALE_PER_TOKEN_HEAD, with_sink=True)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+@pytest.mark.parametrize("topk", [1, 2, 40])
+def test_topk_extremes(msa, orc, topk):
+    # k = 1, small k, and k larger than every row's block count (select all)
+    w = W.custom(51, q_lens=[1, 2, 1], seq_lens=[4000, 1100, 130], hq=16, di=128, topk=topk,
+                 with_sink=True)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+def test_heavy_ties(msa, orc):
+    # index values in {-1, 0, 1} with Di 64: many blocks tie at the same score
+    w = W.custom(52, q_lens=[1, 4], seq_lens=[30000, 20000], hq=16, di=64, idx_range=1,
+                 topk=16)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+def test_garbage_past_the_end_is_ignored(msa, orc):
+    for kv in (W.KV_BF16, W.KV_FP8):
+        w = W.custom(53, q_lens=[1, 3, 1], seq_lens=[1000, 517, 129], hq=16, di=128, topk=4,
+                     kv_dtype=kv, with_sink=True, fill_unused_nan=True)
+        _, sep, fused = run_steps(msa, w)
+        check_against_oracle(orc, w, sep, fused)
+        assert np.all(np.isfinite(sep["out"])) and np.all(np.isfinite(sep["lse"]))
+
+
+@pytest.mark.parametrize("hi,di", [(1, 64), (2, 64), (1, 128)])
+def test_index_head_variants(msa, orc, hi, di):
+    w = W.custom(54, q_lens=[1, 4, 2], seq_lens=[3000, 1500, 260], hq=16, di=di, hi=hi, topk=4)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+@pytest.mark.parametrize("hq", [1, 8, 12, 16])
+def test_query_head_counts(msa, orc, hq):
+    w = W.custom(55, q_lens=[1, 2], seq_lens=[2500, 900], hq=hq, di=128, topk=4, with_sink=True,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_SCALAR)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+def test_many_rows_single_split(msa, orc):
+    # enough rows that each row runs as a single split (no cross-CTA merge)
+    w = W.custom(56, q_lens=[300, 200], seq_lens=[2500, 1200], hq=16, di=128, topk=8)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+def test_poisoned_requests_match_oracle(msa, orc):
+    w = W.custom(57, q_lens=[1, 2, 1, 1], seq_lens=[900, 700, 400, 300], hq=16, di=128, topk=2,
+                 with_sink=True)
+    bt = w.block_table.copy()
+    bt[1, 2] = w.num_pages + 5  # request 1 addresses a page outside the pool
+    w.block_table = bt
+    ctx = w.context_lens.copy()
+    ctx[2] -= 1                 # request 2: context + q_len != seq_len
+    w.context_lens = ctx
+    _, sep, fused = run_steps(msa, w)
+    ref = orc.decode(w)
+    assert sep["status"] == ref["status"] == (msa.MSA_DEV_BAD_PAGE | msa.MSA_DEV_BAD_LEN)
+    for key in ("topk_idx", "tbl", "sparse_len"):
+        assert np.array_equal(sep[key], ref[key])
+    assert_attn_close(sep["out"], sep["lse"], ref["out"], ref["lse"])
+    for r in (1, 2, 3):  # poisoned rows are empty rows: O = 0, LSE = sink
+        assert np.all(sep["out"][r] == 0)
+        np.testing.assert_allclose(sep["lse"][r], w.sinks, atol=1e-6)
+
+
+def test_malformed_batch_sets_status(msa):
+    w = W.custom(58, q_lens=[1, 1], seq_lens=[300, 200], hq=16, di=128, topk=2)
+    cu = w.cu_seqlens_q.copy()
+    cu[2] = 1  # rows are not tiled: cu_seqlens_q decreases and stops short of num_rows
+    w.cu_seqlens_q = cu
+    c = msa.DeviceCase(w)
+    c.decode()
+    res = c.fetch()
+    assert res["status"] & msa.MSA_DEV_MALFORMED
+    assert np.all(res["sparse_len"] == 0) and np.all(res["out"] == 0)
+
+
+def test_standalone_attention_bad_table(msa, orc):
+    w = W.custom(59, q_lens=[1, 1, 1], seq_lens=[600, 600, 600], hq=16, di=128, topk=4,
+                 with_sink=True)
+    c = msa.DeviceCase(w)
+    c.index_score()
+    c.topk_build_table()
+    c.tbl[1, 3] = 8 * w.num_pages  # first id past the page-16 pool
+    c.sparse_len[2] = 16 * c.tbl_stride + 1
+    c.sparse_paged_attn()
+    res = c.fetch()
+    assert res["status"] == msa.MSA_DEV_BAD_TABLE
+    ref_o, ref_l, st = orc.sparse_attn(w.q, w.k_cache, w.v_cache, w.kv_dtype, res["tbl"],
+                                       res["sparse_len"], sinks=w.sinks,
+                                       softmax_scale=w.softmax_scale, num_pages16=8 * w.num_pages)
+    assert st == orc.BAD_TABLE
+    assert_attn_close(res["out"], res["lse"], ref_o, ref_l)
+    assert np.all(res["out"][1:] == 0)
+
+
+def test_page_permutation_invariance(msa):
+    w = W.custom(60, q_lens=[1, 4, 1], seq_lens=[6000, 3000, 900], hq=16, di=128, topk=8,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_PER_TOKEN_HEAD, with_sink=True)
+    _, a, _ = run_steps(msa, w)
+    perm = np.random.default_rng(1).permutation(w.num_pages)
+    inv = np.argsort(perm)
+    w.idx_k, w.k_cache, w.v_cache = w.idx_k[perm], w.k_cache[perm], w.v_cache[perm]
+    w.k_scale, w.v_scale = w.k_scale[perm], w.v_scale[perm]
+    bt = w.block_table.copy()
+    bt[bt >= 0] = inv[bt[bt >= 0]]
+    w.block_table = bt
+    _, b, _ = run_steps(msa, w)
+    for key in ("topk_idx", "sparse_len", "out", "lse"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_graph_capture_and_replay(msa):
+    w = W.custom(61, q_lens=[1, 4, 1, 1], seq_lens=[7000, 3000, 1200, 260], hq=16, di=128,
+                 topk=8, kv_dtype=W.KV_FP8, scale_mode=W.SCALE_SCALAR, with_sink=True)
+    c = msa.DeviceCase(w)
+    c.decode()
+    eager = c.fetch()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        c.decode(stream=s)  # capture fails if the call syncs or copies to/from the host
+    for _ in range(3):
+        c.out.zero_()
+        c.lse.zero_()
+        g.replay()
+        rep = c.fetch()
+        for key in ("topk_idx", "tbl", "sparse_len", "out", "lse"):
+            assert np.array_equal(rep[key], eager[key]), key
+
+
+def test_repeated_calls_are_identical(msa):
+    w = W.custom(62, q_lens=[1, 1], seq_lens=[20000, 9000], hq=16, di=128, topk=16,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_PER_TOKEN_HEAD, with_sink=True)
+    c = msa.DeviceCase(w)
+    c.decode()
+    a = c.fetch()
+    for _ in range(3):
+        c.sparse_paged_attn()  # separate workspace, counters must be back at 0
+        c.decode()
+    b = c.fetch()
+    for key in ("out", "lse", "tbl"):
+        assert np.array_equal(a[key], b[key])
+
+
+def test_outputs_stay_inside_their_rows(msa):
+    """Sentinel guard regions around every output stay untouched."""
+    w = W.custom(63, q_lens=[1, 3], seq_lens=[3000, 700], hq=16, di=128, topk=4, with_sink=True)
+    c = msa.DeviceCase(w)
+    G = 4096
+    N, k, ts = w.num_rows, c.topk, c.tbl_stride
+
+    def guarded(n, dtype, fill):
+        buf = torch.full((2 * G + n,), fill, dtype=dtype, device="cuda")
+        return buf, buf[G:G + n]
+
+    tb, tbl = guarded(N * ts, torch.int32, -7)
+    kb, kidx = guarded(N * k, torch.int32, -7)
+    lb, slen = guarded(N, torch.int32, -7)
+    ob, out = guarded(N * 16 * 128, torch.bfloat16, 3.0)
+    eb, lse = guarded(N * 16, torch.float32, 3.0)
+    c.attn = msa.make_attn_args(c.q, c.k, c.v, w.kv_dtype, w.num_pages, out.view(N, 16, 128),
+                                lse.view(N, 16), sinks=c.sinks, softmax_scale=w.softmax_scale)
+    msa.msa_decode(c.batch, c.idx_q, c.idx_k, 1, 128, k, c.attn, kidx, tbl, ts, slen,
+                   c.workspace, c.status)
+    torch.cuda.synchronize()
+    for buf, n, fill in ((tb, N * ts, -7), (kb, N * k, -7), (lb, N, -7), (ob, N * 2048, 3.0),
+                         (eb, N * 16, 3.0)):
+        assert torch.all(buf[:G] == fill) and torch.all(buf[G + n:] == fill)
+    assert int(c.status.item()) == 0
+
+
+def test_empty_batch_is_a_no_op(msa):
+    dev = "cuda"
+    z = torch.zeros(1, dtype=torch.int32, device=dev)
+    bt = torch.zeros((0, 1), dtype=torch.int32, device=dev)
+    b = msa.make_batch(z, z, torch.zeros(0, dtype=torch.int32, device=dev), bt, 0, 0)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    scores = torch.zeros((1, 1), dtype=torch.float32, device=dev)
+    q = torch.zeros((1, 1, 64), dtype=torch.bfloat16, device=dev)
+    msa.msa_index_score(b, q, q, 1, 64, scores, 1, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
