@@ -55,7 +55,10 @@ class DeviceCase:
         self.tbl = torch.empty((max(N, 1), self.tbl_stride), dtype=torch.int32, device=device)
         self.sparse_len = torch.empty((max(N, 1),), dtype=torch.int32, device=device)
         self.status = torch.zeros((1,), dtype=torch.int32, device=device)
-        self.batch = B.make_batch(self.cu_q, self.cu_k, self.ctx, self.bt, w.num_pages, N)
+        q_lens = np.diff(np.asarray(w.cu_seqlens_q, np.int64))
+        self.max_q_len = int(q_lens.max()) if q_lens.size else 0
+        self.batch = B.make_batch(self.cu_q, self.cu_k, self.ctx, self.bt, w.num_pages, N,
+                                  max_q_len=self.max_q_len)
         self.attn = B.make_attn_args(self.q, self.k, self.v, w.kv_dtype, w.num_pages, self.out,
                                      self.lse, scale_mode=w.scale_mode, k_scale=self.k_scale,
                                      v_scale=self.v_scale, sinks=self.sinks,

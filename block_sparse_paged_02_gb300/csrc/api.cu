@@ -130,6 +130,16 @@ AttnLaunch make_attn(const msa_attn_args* a, const int32_t* tbl, int tbl_stride,
 
 msa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
 
+// Step 1: the streaming CUDA-core kernel, plus the tensor-core kernel for
+// requests with many rows when the batch may hold any (max_q_len hint).
+cudaError_t launch_scores(ScoreLaunch p, cudaStream_t stream) {
+  const bool tc = p.batch.max_q_len >= kTcMinRows && tc_score_supported(p.index_heads, p.index_dim);
+  p.tc_min_rows = tc ? kTcMinRows : 0;
+  cudaError_t e = launch_index_score(p, stream);
+  if (e != cudaSuccess || !tc) return e;
+  return launch_index_score_tc(p, stream);
+}
+
 }  // namespace
 }  // namespace msa
 
@@ -180,8 +190,8 @@ msa_status msa_index_score(const msa_batch* batch, const void* idx_q, const void
   if (batch->num_rows == 0 || batch->num_reqs == 0) return MSA_OK;
   ScoreLaunch p{*batch, static_cast<const uint16_t*>(idx_q),
                 static_cast<const uint8_t*>(idx_k_cache), index_heads, index_dim, scores,
-                score_stride, dev_status};
-  return cuda_status(launch_index_score(p, stream));
+                score_stride, dev_status, 0};
+  return cuda_status(launch_scores(p, stream));
 }
 
 msa_status msa_topk_build_table(const msa_batch* batch, const float* scores,
@@ -264,8 +274,8 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
 
   ScoreLaunch sp{*batch, static_cast<const uint16_t*>(idx_q),
                  static_cast<const uint8_t*>(idx_k_cache), index_heads, index_dim, scores,
-                 batch->bt_stride, dev_status};
-  cudaError_t e = launch_index_score(sp, stream);
+                 batch->bt_stride, dev_status, 0};
+  cudaError_t e = launch_scores(sp, stream);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_score) cudaEventRecord(trace->after_score, stream);
 

@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
       atomicOr(reinterpret_cast<unsigned*>(&misc[0]), bad);
       nb = 0;
     }
+    if (p.tc_min_rows > 0 && ql >= p.tc_min_rows) nb = 0;  // scored on the tensor cores
     prefix[q + 1] = nb;
   }
   __syncthreads();

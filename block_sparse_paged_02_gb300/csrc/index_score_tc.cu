@@ -1,0 +1,453 @@
+// index_score_tc.cu -- step 1 for requests with many query rows (chunked
+// prefill): the block score as the row-wise masked max of a dense
+// contraction, on the 5th-generation tensor cores.
+//
+// Definition as in index_score.cu ("Optimise MiniMax-M3 decode index and
+// top-k on gfx950", vLLM PR 54682, "Implementation breakdown" item 1): for
+// each query row and 128-token block, the max over the block's visible
+// tokens of idx_q[row] . idx_k[token].
+//
+// When a request brings >= kTcMinRows query rows, 128 rows x 128 tokens x Di
+// is a real dense tile: D = Q_tile . K_block^T runs as tcgen05.mma
+// (kind::f16, bf16 in, fp32 accumulate in TMEM), and the epilogue reduces
+// each TMEM lane (= query row) to its causal-masked max.  Integer-valued
+// index vectors keep every partial sum an exact fp32 integer, so the scores
+// equal the CUDA-core kernel's and the oracle's bit for bit.
+//
+// CTA roles (persistent grid, one CTA per SM, work = the flat list of
+// (request, 128-row tile, block) items split evenly across CTAs):
+//   warp 0  TMA producer: Q tile (once per row tile) and K block per item,
+//           128-byte-swizzled tiles via cp.async.bulk.tensor into a 4-stage
+//           ring with mbarrier completion;
+//   warp 1  allocates 256 TMEM columns (two 128-column accumulators);
+//           one thread issues the MMAs and tcgen05.commit;
+//   warps 2-5 epilogue: tcgen05.ld of 32 rows x 128 columns each, masked
+//           max, score store; releases the accumulator.
+// Every wait is bounded; on expiry the kernel records MSA_DEV_TIMEOUT, stops
+// issuing work and still frees its TMEM.
+#include "msa_internal.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 192;
+constexpr int kTileRows = 128;
+constexpr uint32_t kTmemCols = 256;
+
+template <int DI>
+struct TcCfg {
+  static constexpr int kHalves = DI / 64;          // 128-byte swizzle atoms along K
+  static constexpr int kTileBytes = kTileRows * DI * 2;
+  static constexpr int kHalfBytes = kTileRows * 128;
+  static constexpr int kKSteps = DI / 16;
+  // smem: A tile, B ring, then barriers / bookkeeping, then request prefix
+  static constexpr int kA = 0;
+  static constexpr int kB = kTileBytes;
+  static constexpr int kBars = kB + kTcStages * kTileBytes;
+  static constexpr int kMisc = kBars + 16 * 8;
+  static constexpr int kPrefix = kMisc + 64;
+  static size_t bytes(int num_reqs) { return 1024 + kPrefix + (size_t)(num_reqs + 1) * 4; }
+};
+
+// ------------------------------------------------------------ tcgen05 PTX
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
+// 8-row core groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused when swizzled)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both
+// K-major, N = 128, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
+                            ((128u >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------------------------ work cursor
+
+// Walks the (request, row tile, block) items of the tensor-core requests in
+// order.  prefix[q] = items before request q (smem).
+struct Cursor {
+  int q, tile, blk, nb, ntiles, q0, qlen, ctx;
+
+  __device__ void load_request(const msa_batch& b) {
+    q0 = b.cu_seqlens_q[q];
+    qlen = b.cu_seqlens_q[q + 1] - q0;
+    ctx = b.context_lens[q];
+    ntiles = (qlen + kTileRows - 1) / kTileRows;
+  }
+  __device__ int tile_blocks(int t) const {
+    const int last_row = min(t * kTileRows + kTileRows - 1, qlen - 1);
+    return (ctx + last_row) / kBlock + 1;
+  }
+  __device__ void seek(const msa_batch& b, const int* prefix, int R, int item) {
+    int lo = 0, hi = R;  // largest q with prefix[q] <= item
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= item) lo = mid; else hi = mid;
+    }
+    while (lo < R - 1 && prefix[lo + 1] <= item) ++lo;
+    q = lo;
+    load_request(b);
+    int rem = item - prefix[q];
+    tile = 0;
+    nb = tile_blocks(0);
+    while (rem >= nb) {
+      rem -= nb;
+      ++tile;
+      nb = tile_blocks(tile);
+    }
+    blk = rem;
+  }
+  __device__ void next(const msa_batch& b, const int* prefix, int R) {
+    if (++blk < nb) return;
+    blk = 0;
+    if (++tile < ntiles) {
+      nb = tile_blocks(tile);
+      return;
+    }
+    do { ++q; } while (q < R - 1 && prefix[q + 1] == prefix[q]);  // skip item-less requests
+    if (q >= R) return;
+    load_request(b);
+    tile = 0;
+    nb = tile_blocks(0);
+  }
+};
+
+template <int DI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    index_score_tc_kernel(const ScoreLaunch p, const __grid_constant__ CUtensorMap qmap,
+                          const __grid_constant__ CUtensorMap kmap) {
+  using C = TcCfg<DI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBars);
+  uint64_t* b_full = bars;                   // [kTcStages]
+  uint64_t* b_empty = bars + kTcStages;      // [kTcStages]
+  uint64_t* a_full = bars + 2 * kTcStages;
+  uint64_t* a_empty = a_full + 1;
+  uint64_t* acc_full = a_full + 2;           // [2]
+  uint64_t* acc_empty = a_full + 4;          // [2]
+  int* misc = reinterpret_cast<int*>(smem + C::kMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 4);
+  int* prefix = reinterpret_cast<int*>(smem + C::kPrefix);
+
+  const msa_batch& b = p.batch;
+  const int R = b.num_reqs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // ---- setup (same request checks as the CUDA-core kernel)
+  if (tid == 0) {
+    misc[0] = !(b.cu_seqlens_q[0] == 0 && b.cu_seqlens_q[R] == b.num_rows);
+    misc[1] = 0;  // timeout seen
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    mbar_init(a_full, 1);
+    mbar_init(a_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  for (int q = tid; q < R; q += blockDim.x) {
+    int q0, ql, ctx, nb;
+    const uint32_t bad = request_lengths(b, q, &q0, &ql, &ctx, &nb);
+    if (ql < 0) misc[0] = 1;
+    int items = 0;
+    if (!bad && ql >= kTcMinRows) {
+      for (int t = 0; t * kTileRows < ql; ++t) {
+        const int last_row = min(t * kTileRows + kTileRows - 1, ql - 1);
+        items += (ctx + last_row) / kBlock + 1;
+      }
+    }
+    prefix[q + 1] = items;
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  __syncthreads();
+  const bool batch_ok = misc[0] == 0;  // the CUDA-core kernel reports the status bits
+  if (batch_ok && warp == 0) {
+    int carry = 0;
+    if (lane == 0) prefix[0] = 0;
+    for (int base = 0; base < R; base += 32) {
+      const int q = base + lane;
+      int v = q < R ? prefix[q + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+      }
+      if (q < R) prefix[q + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const long long total = batch_ok ? prefix[R] : 0;
+  const int i0 = (int)(total * blockIdx.x / gridDim.x);
+  const int i1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+  const int n_items = i1 - i0;
+
+  if (n_items > 0) {
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer
+      Cursor cur;
+      cur.seek(b, prefix, R, i0);
+      int a_key_q = -1, a_key_t = -1, a_loads = 0;
+      for (int j = 0; j < n_items; ++j) {
+        if (cur.q != a_key_q || cur.tile != a_key_t) {
+          if (a_loads > 0 && !mbar_wait(a_empty, (a_loads - 1) & 1)) {
+            misc[1] = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(a_full, C::kTileBytes);
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_2d(smem + C::kA + h * C::kHalfBytes, &qmap, 64 * h,
+                        cur.q0 + cur.tile * kTileRows, a_full);
+          a_key_q = cur.q;
+          a_key_t = cur.tile;
+          ++a_loads;
+        }
+        const int s = j % kTcStages;
+        if (j >= kTcStages && !mbar_wait(&b_empty[s], ((j / kTcStages) - 1) & 1)) {
+          misc[1] = 1;
+          break;
+        }
+        const int page = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
+        if (page >= 0 && page < b.num_pages) {
+          mbar_arrive_expect_tx(&b_full[s], C::kTileBytes);
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_2d(smem + C::kB + s * C::kTileBytes + h * C::kHalfBytes, &kmap, 64 * h,
+                        page * kBlock, &b_full[s]);
+        } else {
+          mbar_arrive(&b_full[s]);  // nothing to load; the epilogue writes -inf
+        }
+        cur.next(b, prefix, R);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- MMA issuer
+      Cursor cur;
+      cur.seek(b, prefix, R, i0);
+      int a_key_q = -1, a_key_t = -1, a_loads = 0;
+      for (int j = 0; j < n_items; ++j) {
+        if (cur.q != a_key_q || cur.tile != a_key_t) {
+          if (!mbar_wait(a_full, a_loads & 1)) {
+            misc[1] = 1;
+            break;
+          }
+          a_key_q = cur.q;
+          a_key_t = cur.tile;
+          ++a_loads;
+        }
+        const int s = j % kTcStages, buf = j & 1;
+        if (j >= 2 && !mbar_wait(&acc_empty[buf], ((j >> 1) - 1) & 1)) {
+          misc[1] = 1;
+          break;
+        }
+        if (!mbar_wait(&b_full[s], (j / kTcStages) & 1)) {
+          misc[1] = 1;
+          break;
+        }
+        tc_fence_after();
+        const int page = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
+        if (page >= 0 && page < b.num_pages) {
+          const uint32_t a_base = smem_u32(smem + C::kA);
+          const uint32_t b_base = smem_u32(smem + C::kB + s * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < C::kKSteps; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+            umma_bf16(tmem + buf * 128, sw128_desc(a_base + off), sw128_desc(b_base + off),
+                      kk > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&b_empty[s]);
+        umma_commit(&acc_full[buf]);
+        Cursor nx = cur;
+        nx.next(b, prefix, R);
+        if (j == n_items - 1 || nx.q != cur.q || nx.tile != cur.tile) umma_commit(a_empty);
+        cur = nx;
+      }
+    } else if (warp >= 2) {
+      // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
+      const int quarter = warp & 3;
+      Cursor cur;
+      cur.seek(b, prefix, R, i0);
+      for (int j = 0; j < n_items; ++j) {
+        const int buf = j & 1;
+        // warp-uniform decision: tcgen05.ld below needs the whole warp
+        if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (j >> 1) & 1))) {
+          misc[1] = 1;
+          break;
+        }
+        tc_fence_after();
+        const int m = quarter * 32 + lane;
+        const int row_in_req = cur.tile * kTileRows + m;
+        const int pos = cur.ctx + row_in_req;
+        const int page = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
+        const bool page_ok = page >= 0 && page < b.num_pages;
+        const int last = pos - cur.blk * kBlock;  // visible columns: c <= last
+        float best = -INFINITY;
+#pragma unroll
+        for (int chunk = 0; chunk < 4; ++chunk) {
+          float v[32];
+          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * 128 + chunk * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (chunk * 32 + i <= last) best = fmaxf(best, v[i]);
+        }
+        if (row_in_req < cur.qlen && last >= 0)
+          p.scores[(long long)(cur.q0 + row_in_req) * p.score_stride + cur.blk] =
+              page_ok ? best : -INFINITY;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        cur.next(b, prefix, R);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (misc[1] && tid == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, di] (row stride di*2 bytes), 64 x 128 boxes, 128-B swizzle
+bool make_map(CUtensorMap* map, const void* base, long long rows, int di) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)di, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)di * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kTileRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DI>
+cudaError_t launch_tc(const ScoreLaunch& p, cudaStream_t stream) {
+  CUtensorMap qmap, kmap;
+  if (!make_map(&qmap, p.idx_q, (long long)p.batch.num_rows, DI) ||
+      !make_map(&kmap, p.idx_k, (long long)p.batch.num_pages * kBlock, DI))
+    return cudaErrorInvalidValue;
+  const size_t smem = TcCfg<DI>::bytes(p.batch.num_reqs);
+  auto kern = index_score_tc_kernel<DI>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<device_sm_count(), kTcThreads, smem, stream>>>(p, qmap, kmap);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_score_supported(int index_heads, int index_dim) {
+  return index_heads == 1 && (index_dim == 64 || index_dim == 128) && encode_fn() != nullptr;
+}
+
+cudaError_t launch_index_score_tc(const ScoreLaunch& p, cudaStream_t stream) {
+  if (p.batch.num_rows == 0 || p.batch.num_reqs == 0) return cudaSuccess;
+  if (p.index_dim == 128) return launch_tc<128>(p, stream);
+  return launch_tc<64>(p, stream);
+}
+
+}  // namespace msa

@@ -4,6 +4,7 @@
 // 1-D bulk async copies (the TMA bulk engine), bounded waits, warp MMA.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -19,6 +20,8 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxHeads = 16;
 constexpr int kMaxReqs = 4096;
 constexpr int kMaxBlocksPerRow = 16384;
+// requests with at least this many query rows are scored on the tensor cores
+constexpr int kTcMinRows = 64;
 // bounded waits: a wait that has not completed after this long gives up
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
 
@@ -191,6 +194,7 @@ struct ScoreLaunch {
   float* scores;
   int score_stride;
   uint32_t* status;
+  int tc_min_rows;  // > 0: requests with q_len >= this are left to the tensor-core kernel
 };
 
 struct TopkLaunch {
@@ -231,6 +235,8 @@ struct AttnLaunch {
 };
 
 cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream);
+cudaError_t launch_index_score_tc(const ScoreLaunch& p, cudaStream_t stream);
+bool tc_score_supported(int index_heads, int index_dim);
 cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream);
 cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t stream);
 

@@ -86,7 +86,11 @@ enum { MSA_SCALE_NONE = 0, MSA_SCALE_SCALAR = 1, MSA_SCALE_PER_TOKEN_HEAD = 2 };
  *   block_table  [R, bt_stride]  page-128 physical page of each logical
  *                       128-token block; only the first ceil(seq_len/128)
  *                       entries of a row are read
- *   num_pages    P, the number of page-128 pages in the pools (bounds check) */
+ *   num_pages    P, the number of page-128 pages in the pools (bounds check)
+ *   max_q_len    host-side upper bound of any request's q_len (the metadata's
+ *                max_query_len); only a launch hint: when it is >= 64, requests
+ *                with >= 64 rows are scored by the tensor-core kernel.  Results
+ *                do not depend on it. */
 typedef struct msa_batch {
   const int32_t* cu_seqlens_q;
   const int32_t* cu_seqlens_k;
@@ -96,6 +100,7 @@ typedef struct msa_batch {
   int32_t num_reqs;
   int32_t num_rows;
   int32_t num_pages;
+  int32_t max_q_len;
 } msa_batch;
 
 /* Attention operands [P47287 "Implementation breakdown" items 2-3],
