@@ -214,6 +214,33 @@ msa_status msa_sparse_paged_attn(const msa_attn_args* attn, const int32_t* spars
                                  size_t workspace_bytes, uint32_t* dev_status,
                                  cudaStream_t stream);
 
+/* Size of the device array msa_sparse_paged_attn_static draws its scratch
+ * from (8 MiB per GPU that loads the library, held until the process exits). */
+#define MSA_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* msa_sparse_paged_attn without a workspace, for callers that cannot
+ * allocate device memory: code where cudaMalloc is off limits because it
+ * synchronises the device and would stall a serving loop, plug-ins whose
+ * host framework owns all device memory and offers no allocator, runtimes
+ * that forbid allocation after start-up.  (The pages have no counterpart;
+ * it is an addition of this library.)
+ * Same arguments, semantics and results as msa_sparse_paged_attn, minus the
+ * workspace: the split-merge scratch comes from one static device array of
+ * MSA_STATIC_SCRATCH_BYTES.  Returns MSA_ERR_WORKSPACE when the call would
+ * need more than that (msa_workspace_size(num_rows, 0, 0, num_heads,
+ * head_dim, tbl_stride) > MSA_STATIC_SCRATCH_BYTES).  Allocates nothing and
+ * calls no allocating routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Each call clears the array's counters on `stream` (cudaMemsetAsync)
+ *     before the kernel; the rest of the array keeps the last call's data.
+ *   - The array is shared by all calls in the process: calls whose kernels
+ *     overlap on the GPU race on it (order them on one stream). */
+msa_status msa_sparse_paged_attn_static(const msa_attn_args* attn, const int32_t* sparse_tbl,
+                                        int32_t tbl_stride, const int32_t* sparse_len,
+                                        uint32_t* dev_status, cudaStream_t stream);
+
 /* The whole path: msa_index_score -> msa_topk_build_table ->
  * msa_sparse_paged_attn in stream order, with the intermediates held in the
  * workspace [P54682 "Implementation breakdown" items 2-3: the indexer writes
