@@ -6,7 +6,7 @@ and the HBM roofline fraction of its dominant kernel (the index-K scan).
 
 A step = one msa_decode call (index score -> top-k + page-16 table ->
 sparse paged attention) over the whole synthetic batch, inputs resident in
-HBM.  L2 is flushed (a 512 MiB write) between timed steps, outside the timed
+HBM.  L2 is flushed (a 512 MiB write, then a 256 MiB read) between timed steps, outside the timed
 events.  Under torchrun each rank runs its own independent batch (requests
 are independent; no collective on the data path) and rank 0 prints one JSON
 line with the max-over-ranks time.
@@ -227,7 +227,7 @@ def workload_config(w):
             "kv": "fp8_e4m3" if w.kv_dtype == W.KV_FP8 else "bf16",
             "scales": ["none", "scalar", "per_token_head"][w.scale_mode],
             "sinks": w.sinks is not None, "context_tokens": int(seq.sum()),
-            "median_context": float(np.median(seq)), "l2": "flushed between steps"}
+            "median_context": float(np.median(seq)), "l2": "flushed between steps (512 MiB write, then 256 MiB read)"}
 
 
 def run_gpu(args):
@@ -259,34 +259,73 @@ def run_gpu(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile_run": w.name, "status": int(case.status.item())}))
         return 0
-    for _ in range(args.warmup):
-        flush.fill_(1)
+    rbuf = torch.ones(L2_FLUSH_BYTES // 2, dtype=torch.uint8, device=dev)
+
+    def flush_l2(i):
+        # write a buffer larger than L2, then read another one so that no dirty
+        # lines are left for the timed kernels to write back
+        flush.fill_(i & 0xff)
+        rbuf.sum(dtype=torch.int32)
+
+    for i in range(args.warmup):
+        flush_l2(i)
         case.decode(keep_tables=False)
     torch.cuda.synchronize()
     if int(case.status.item()) != 0:
         raise RuntimeError(f"device status {int(case.status.item())} on a clean workload")
 
-    # ---- timed: K steps, per-step events, L2 flushed between steps
-    marks = [(ev(), ev(), ev(), ev()) for _ in range(args.steps)]
-    traces = [msa.make_trace(m[1], m[2], m[3]) for m in marks]
+    def capture(fn):
+        """The decode call captured once into a CUDA graph (the library is
+        graph-capturable: no host sync, no allocation, no host copy)."""
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn(s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        return g
+
+    launch_mode = "cuda_graph"
+    try:
+        g_main = capture(lambda s: case.decode(keep_tables=False, stream=s))
+    except Exception as exc:  # graph capture unavailable: time eager launches
+        launch_mode, g_main = f"eager ({type(exc).__name__})", None
+    run_step = (lambda: g_main.replay()) if g_main is not None else \
+        (lambda: case.decode(keep_tables=False))
+
+    # ---- timed: K steps, per-step events on the launching stream
+    marks = [(ev(), ev()) for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
-            flush.fill_(i & 0xff)
+            flush_l2(i)
             marks[i][0].record(stream)
-            case.decode(keep_tables=False, trace=traces[i])
+            run_step()
+            marks[i][1].record(stream)
         torch.cuda.synchronize()
     barrier()
-    step_ms = [m[0].elapsed_time(m[3]) for m in marks]
-    score_ms = [m[0].elapsed_time(m[1]) for m in marks]
-    topk_ms = [m[1].elapsed_time(m[2]) for m in marks]
-    attn_ms = [m[2].elapsed_time(m[3]) for m in marks]
+    step_ms = [a.elapsed_time(b) for a, b in marks]
     total_ms = sum(step_ms)
     if ws > 1:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
+
+    # ---- per-kernel times: the same step with events after each stage
+    e = [ev() for _ in range(4)]
+    trace = msa.make_trace(e[1], e[2], e[3])
+    # (eager launches: events recorded inside a graph cannot be timed)
+    score_ms, topk_ms, attn_ms = [], [], []
+    for i in range(args.steps):
+        flush_l2(i)
+        e[0].record(stream)
+        case.decode(keep_tables=False, trace=trace)
+        torch.cuda.synchronize()
+        score_ms.append(e[0].elapsed_time(e[1]))
+        topk_ms.append(e[1].elapsed_time(e[2]))
+        attn_ms.append(e[2].elapsed_time(e[3]))
 
     # ---- end to end through the public API: host buffers, copies inside
     case.decode()
@@ -300,7 +339,7 @@ def run_gpu(args):
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
     e2e_marks = [(ev(), ev()) for _ in range(args.steps)]
     for i in range(args.warmup + args.steps):
-        flush.fill_(i & 0xff)
+        flush_l2(i)
         if i >= args.warmup:
             e2e_marks[i - args.warmup][0].record(stream)
         for name, t in host.items():
@@ -321,6 +360,8 @@ def run_gpu(args):
         dist.destroy_process_group()
         return 0
     rows_total = w.num_rows * ws * args.steps
+    q_lens = np.diff(w.cu_seqlens_q)
+    launches_per_step = 3 + int(q_lens.max() >= 64 and w.index_heads == 1)
     value = rows_total / (total_ms / 1e3)
     peak, peak_kind = read_peaks()
     nbytes = algorithmic_bytes(w, sparse_len)
@@ -346,7 +387,8 @@ def run_gpu(args):
                       "sparse_attn": statistics.mean(attn_ms)},
         "e2e": {"value": rows_total / (e2e_ms / 1e3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
+        "launch": launch_mode,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
     }

@@ -23,7 +23,7 @@ MSA_DEV_BAD_PAGE, MSA_DEV_BAD_LEN, MSA_DEV_MALFORMED, MSA_DEV_BAD_TABLE, MSA_DEV
     1, 2, 4, 8, 16
 
 EXPORTED = ("msa_index_score", "msa_topk_build_table", "msa_sparse_paged_attn", "msa_decode",
-            "msa_workspace_size", "msa_status_string")
+            "msa_kv_insert", "msa_workspace_size", "msa_status_string")
 
 
 class MsaError(RuntimeError):
@@ -86,6 +86,9 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.msa_decode.restype = ctypes.c_int
             L.msa_decode.argtypes = [P, P, P, i32, i32, i32, P, P, P, i32, P, P, ctypes.c_size_t,
                                      P, P, P]
+            L.msa_kv_insert.restype = ctypes.c_int
+            L.msa_kv_insert.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, i32, i32, P, P,
+                                        i32, P, P]
             L.msa_workspace_size.restype = ctypes.c_size_t
             L.msa_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
             L.msa_status_string.restype = ctypes.c_char_p
@@ -197,6 +200,16 @@ def msa_decode(batch: msa_batch, idx_q, idx_k_cache, index_heads, index_dim, top
         _p(sparse_len), _p(workspace),
         int(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
         _p(dev_status), ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def msa_kv_insert(batch: msa_batch, k_new, v_new, idx_new, num_kv_heads, head_dim, index_heads,
+                  index_dim, k_cache, v_cache, idx_k_cache, kv_dtype, scale_mode, k_scale,
+                  v_scale, skip_index, dev_status, stream=None):
+    _check("msa_kv_insert", lib().msa_kv_insert(
+        ctypes.byref(batch), _p(k_new), _p(v_new), _p(idx_new), int(num_kv_heads),
+        int(head_dim), int(index_heads), int(index_dim), _p(k_cache), _p(v_cache),
+        _p(idx_k_cache), int(kv_dtype), int(scale_mode), _p(k_scale), _p(v_scale),
+        int(bool(skip_index)), _p(dev_status), _stream(stream)))
 
 
 def make_trace(after_score=None, after_topk=None, after_attn=None) -> msa_trace:

@@ -89,6 +89,13 @@ class DeviceCase:
                      self.sparse_len if keep_tables else None, self.workspace, self.status,
                      trace, stream)
 
+    def kv_insert(self, k_new, v_new, idx_new, skip_index: bool = False, stream=None):
+        """Write the rows' new K/V/index-K (device bf16 tensors) into the pools."""
+        B.msa_kv_insert(self.batch, k_new, v_new, idx_new, self.w.hkv, self.w.head_dim,
+                        self.w.index_heads, self.w.index_dim, self.k, self.v, self.idx_k,
+                        self.w.kv_dtype, self.w.scale_mode, self.k_scale, self.v_scale,
+                        skip_index, self.status, stream)
+
     def fetch(self):
         torch.cuda.synchronize()
         n = self.num_rows

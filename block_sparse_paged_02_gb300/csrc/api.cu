@@ -30,16 +30,27 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Attention work split: page-16 entries per split and the split count, from
-// the row count and the widest possible row (max_entries page-16 entries),
-// aiming at about two CTAs per SM.
-void attn_split(int num_rows, int max_entries, int* pps, int* splits) {
-  const int sms = device_sm_count();
-  const int target = num_rows > 0 ? (2 * sms + num_rows - 1) / num_rows : 1;
+// Attention work split: page-16 entries per split and the split count.  The
+// grid (splits x rows) is sized to fill the GPU once: as many splits per row
+// as fit in ctas_per_sm resident CTAs on every SM, each split a multiple of 4
+// entries (one per warp) and at most kMaxSplitEntries.  Workspaces are sized
+// with the largest residency of any variant (3), launches use their own.
+constexpr int kMaxAttnCtasPerSm =
+    MSA_ATTN_CTAS_FP8 > MSA_ATTN_CTAS_BF16 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_CTAS_BF16;
+
+void attn_split(int num_rows, int max_entries, int ctas_per_sm, int* pps, int* splits) {
+  const int capacity = device_sm_count() * ctas_per_sm;
+  int target = num_rows > 0 ? capacity / num_rows : 1;
+  if (target < 1) target = 1;
   int per = (max_entries + target - 1) / target;
   per = per < 4 ? 4 : (per + 3) / 4 * 4;
+  if (per > kMaxSplitEntries) per = kMaxSplitEntries;
   *pps = per;
   *splits = max_entries > 0 ? (max_entries + per - 1) / per : 1;
+}
+
+int attn_ctas_per_sm(const msa_attn_args* a) {
+  return a->kv_dtype == MSA_KV_FP8_E4M3 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_CTAS_BF16;
 }
 
 struct DecodeWs {
@@ -167,7 +178,7 @@ size_t msa_workspace_size(int32_t num_rows, int32_t bt_stride, int32_t topk, int
   if (num_rows < 0 || bt_stride < 0 || topk < 0 || tbl_stride < 0) return 0;
   int pps, splits;
   const int max_entries = topk > 0 ? 8 * topk : tbl_stride;
-  attn_split(num_rows, max_entries, &pps, &splits);
+  attn_split(num_rows, max_entries, kMaxAttnCtasPerSm, &pps, &splits);
   if (bt_stride == 0) {  // attention only: counters + partials
     const size_t n = (size_t)(num_rows > 0 ? num_rows : 1);
     return round_up(n * 4, 256) + round_up(n * (size_t)splits * kPartFloats * 4, 256);
@@ -202,6 +213,7 @@ msa_status msa_topk_build_table(const msa_batch* batch, const float* scores,
   if (st != MSA_OK) return st;
   if (!dev_status) return MSA_ERR_NULL;
   if (topk < 1) return MSA_ERR_SHAPE;
+  if (topk > kMaxTopk) return MSA_ERR_UNSUPPORTED;
   if (tbl_stride < 8 * topk || score_stride < batch->bt_stride) return MSA_ERR_SHAPE;
   if (batch->num_rows > 0 && (!scores || !topk_idx || !sparse_tbl || !sparse_len))
     return MSA_ERR_NULL;
@@ -209,7 +221,7 @@ msa_status msa_topk_build_table(const msa_batch* batch, const float* scores,
   if (batch->num_reqs == 0) return MSA_ERR_SHAPE;  // rows without any request
   TopkLaunch p{*batch, scores, score_stride, topk, topk_idx, sparse_tbl, tbl_stride, sparse_len,
                nullptr, dev_status};
-  return cuda_status(launch_topk_table(p, stream));
+  return cuda_status(launch_topk_table(p, stream, false));
 }
 
 msa_status msa_sparse_paged_attn(const msa_attn_args* attn, const int32_t* sparse_tbl,
@@ -226,13 +238,13 @@ msa_status msa_sparse_paged_attn(const msa_attn_args* attn, const int32_t* spars
                                          tbl_stride);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return MSA_ERR_WORKSPACE;
   int pps, splits;
-  attn_split(attn->num_rows, tbl_stride, &pps, &splits);
+  attn_split(attn->num_rows, tbl_stride, attn_ctas_per_sm(attn), &pps, &splits);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* counters = reinterpret_cast<uint32_t*>(ws);
   float* partials = reinterpret_cast<float*>(ws + round_up((size_t)attn->num_rows * 4, 256));
   AttnLaunch p = make_attn(attn, sparse_tbl, tbl_stride, sparse_len, partials, counters, pps,
                            splits, dev_status);
-  return cuda_status(launch_sparse_attn(p, stream));
+  return cuda_status(launch_sparse_attn(p, stream, false));
 }
 
 msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx_k_cache,
@@ -247,6 +259,7 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
   if (st != MSA_OK) return st;
   if (!dev_status) return MSA_ERR_NULL;
   if (topk < 1) return MSA_ERR_SHAPE;
+  if (topk > kMaxTopk) return MSA_ERR_UNSUPPORTED;
   if (attn->num_rows != batch->num_rows) return MSA_ERR_SHAPE;
   if (attn->num_pages != batch->num_pages) return MSA_ERR_SHAPE;
   if (!((index_heads == 1 && (index_dim == 64 || index_dim == 128)) ||
@@ -261,9 +274,10 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
                                          attn->num_heads, attn->head_dim, 8 * topk);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return MSA_ERR_WORKSPACE;
 
-  int pps, splits;
-  attn_split(batch->num_rows, 8 * topk, &pps, &splits);
-  const DecodeWs L = decode_layout(batch->num_rows, batch->bt_stride, topk, splits);
+  int pps, splits, ws_pps, ws_splits;
+  attn_split(batch->num_rows, 8 * topk, attn_ctas_per_sm(attn), &pps, &splits);
+  attn_split(batch->num_rows, 8 * topk, kMaxAttnCtasPerSm, &ws_pps, &ws_splits);
+  const DecodeWs L = decode_layout(batch->num_rows, batch->bt_stride, topk, ws_splits);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* counters = reinterpret_cast<uint32_t*>(ws + L.counters);
   float* scores = reinterpret_cast<float*>(ws + L.scores);
@@ -281,17 +295,59 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
 
   TopkLaunch tp{*batch, scores, batch->bt_stride, topk, k_idx, tbl, tstride, len, counters,
                 dev_status};
-  e = launch_topk_table(tp, stream);
+  e = launch_topk_table(tp, stream, true);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_topk) cudaEventRecord(trace->after_topk, stream);
 
   AttnLaunch ap = make_attn(attn, tbl, tstride, len, reinterpret_cast<float*>(ws + L.partials),
                             counters, pps, splits, dev_status);
   // the attention split depends only on the selected width (8*topk entries)
-  e = launch_sparse_attn(ap, stream);
+  e = launch_sparse_attn(ap, stream, true);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_attn) cudaEventRecord(trace->after_attn, stream);
   return MSA_OK;
+}
+
+msa_status msa_kv_insert(const msa_batch* batch, const void* k_new, const void* v_new,
+                         const void* idx_new, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t index_heads, int32_t index_dim, void* k_cache, void* v_cache,
+                         void* idx_k_cache, int32_t kv_dtype, int32_t scale_mode, float* k_scale,
+                         float* v_scale, int32_t skip_index, uint32_t* dev_status,
+                         cudaStream_t stream) {
+  msa_status st = check_batch(batch);
+  if (st != MSA_OK) return st;
+  if (!dev_status) return MSA_ERR_NULL;
+  if (kv_dtype != MSA_KV_BF16 && kv_dtype != MSA_KV_FP8_E4M3) return MSA_ERR_DTYPE;
+  if (scale_mode < MSA_SCALE_NONE || scale_mode > MSA_SCALE_PER_TOKEN_HEAD) return MSA_ERR_DTYPE;
+  if (num_kv_heads < 1 || index_heads < 1 || index_dim < 1) return MSA_ERR_SHAPE;
+  if (head_dim != kHeadDim || (index_heads * index_dim) % 4 != 0) return MSA_ERR_UNSUPPORTED;
+  if (batch->num_rows == 0) return MSA_OK;
+  if (batch->num_reqs == 0) return MSA_ERR_SHAPE;
+  if (!k_new || !v_new || !k_cache || !v_cache) return MSA_ERR_NULL;
+  if (!skip_index && (!idx_new || !idx_k_cache)) return MSA_ERR_NULL;
+  const bool fp8 = kv_dtype == MSA_KV_FP8_E4M3;
+  if (fp8 && scale_mode != MSA_SCALE_NONE && (!k_scale || !v_scale)) return MSA_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return MSA_ERR_SHAPE;
+  if (!skip_index && (!aligned16(idx_new) || !aligned16(idx_k_cache))) return MSA_ERR_SHAPE;
+  KvInsertLaunch p;
+  p.batch = *batch;
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.idx_new = static_cast<const uint16_t*>(idx_new);
+  p.num_kv_heads = num_kv_heads;
+  p.index_heads = index_heads;
+  p.index_dim = index_dim;
+  p.k_cache = static_cast<uint8_t*>(k_cache);
+  p.v_cache = static_cast<uint8_t*>(v_cache);
+  p.idx_k_cache = static_cast<uint16_t*>(idx_k_cache);
+  p.kv_fp8 = fp8;
+  p.scale_mode = fp8 ? scale_mode : MSA_SCALE_NONE;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.skip_index = skip_index != 0;
+  p.status = dev_status;
+  return cuda_status(launch_kv_insert(p, stream));
 }
 
 }  // extern "C"

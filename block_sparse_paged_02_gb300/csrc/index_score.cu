@@ -36,18 +36,20 @@ template <int DI, int HI>
 struct ScoreCfg {
   static constexpr int kSubRowBytes = DI * 2;
   static constexpr int kChunks = DI / 8;  // 16-byte chunks per sub-row
-  static constexpr int kSubPerLane = kBlock * HI / 32;
   static constexpr int kPageBytes = kBlock * HI * DI * 2;
   static constexpr int kStages = kPageBytes >= 32768 ? 6 : 12;  // 192 KB of stages
-  static constexpr int kThreads = 32 * (1 + kStages);
+  // warps per stage; each takes an equal share of the page's sub-rows (one
+  // warp per page measured fastest: a pair split adds work without raising
+  // the bytes in flight enough to matter)
+  static constexpr int kParts = 1;
+  static constexpr int kConsumers = kStages * kParts;
+  static constexpr int kSubPerLane = kBlock * HI / 32 / kParts;
+  static constexpr int kThreads = 32 * (1 + kConsumers);
   static constexpr int kQBytes = kRowGroup * HI * DI * 2;  // per consumer warp
 };
 
-struct StageInfo {
-  int req;
-  int blk;
-  int valid;
-  int pad;
+struct StageInfo {  // written by the producer before it arms the stage
+  int req, blk, valid, q0, qlen, ctx, pad0, pad1;
 };
 
 template <int DI, int HI>
@@ -55,8 +57,9 @@ struct ScoreSmem {
   using C = ScoreCfg<DI, HI>;
   static constexpr size_t kPages = 0;
   static constexpr size_t kQ = kPages + (size_t)C::kStages * C::kPageBytes;
-  static constexpr size_t kBars = kQ + (size_t)C::kStages * C::kQBytes;
-  static constexpr size_t kInfo = kBars + 2 * C::kStages * sizeof(uint64_t);
+  static constexpr size_t kPair = kQ + (size_t)C::kConsumers * C::kQBytes;
+  static constexpr size_t kBars = kPair + (size_t)C::kStages * kRowGroup * sizeof(float);
+  static constexpr size_t kInfo = kBars + 3 * C::kStages * sizeof(uint64_t);
   static constexpr size_t kMisc = kInfo + C::kStages * sizeof(StageInfo);
   static constexpr size_t kPrefix = kMisc + 64;
   static size_t bytes(int num_reqs) { return kPrefix + (size_t)(num_reqs + 1) * sizeof(int); }
@@ -66,7 +69,7 @@ struct ScoreSmem {
 // Returns, in lane 0..NR-1 order via out[], the per-row block maxima.
 template <int DI, int HI, int NR>
 __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q_s, int lane,
-                                           int blk, const int (&pos)[kRowGroup],
+                                           int sub0, int blk, const int (&pos)[kRowGroup],
                                            float (&out)[kRowGroup]) {
   using C = ScoreCfg<DI, HI>;
   float acc[C::kSubPerLane][NR];
@@ -93,7 +96,7 @@ __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q
     }
 #pragma unroll
     for (int j = 0; j < C::kSubPerLane; ++j) {
-      const int sr = lane + 32 * j;
+      const int sr = sub0 + lane + 32 * j;
       const uint4 w = lds128(page + sr * C::kSubRowBytes + c * 16);
       const float k0 = bf16lo(w.x), k1 = bf16hi(w.x), k2 = bf16lo(w.y), k3 = bf16hi(w.y);
       const float k4 = bf16lo(w.z), k5 = bf16hi(w.z), k6 = bf16lo(w.w), k7 = bf16hi(w.w);
@@ -117,7 +120,7 @@ __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < C::kSubPerLane; ++j) {
-      const int token = (lane + 32 * j) / HI;
+      const int token = (sub0 + lane + 32 * j) / HI;
       if (blk * kBlock + token <= pos[r]) m = fmaxf(m, acc[j][r]);  // NaN never wins
     }
 #pragma unroll
@@ -134,6 +137,8 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
   uint64_t* empty = full + C::kStages;
+  uint64_t* pairbar = empty + C::kStages;  // part 1 -> part 0 of a page, per row group
+  float* pairmax = reinterpret_cast<float*>(smem + S::kPair);
   StageInfo* info = reinterpret_cast<StageInfo*>(smem + S::kInfo);
   int* misc = reinterpret_cast<int*>(smem + S::kMisc);
   int* prefix = reinterpret_cast<int*>(smem + S::kPrefix);
@@ -141,6 +146,9 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
   const msa_batch& b = p.batch;
   const int R = b.num_reqs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the next kernel on the stream may start its prologue now; it waits on the
+  // device for this grid's scores before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- setup: per-request block counts, batch checks, prefix sums
   if (tid == 0) {
@@ -150,7 +158,8 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
   }
   if (tid < C::kStages) {
     mbar_init(&full[tid], 1);
-    mbar_init(&empty[tid], 1);
+    mbar_init(&empty[tid], C::kParts);
+    mbar_init(&pairbar[tid], 1);
   }
   fence_barrier_init();
   __syncthreads();
@@ -194,51 +203,91 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
   const int n_items = i1 - i0;
 
   if (warp == 0) {
-    // ---- producer: one elected thread streams index-K pages into the ring
-    if (lane == 0) {
-      for (int j = 0; j < n_items; ++j) {
+    // ---- producer warp.  An item lookup (request by binary search over the
+    // prefix, its row range, and the page id from the block table) costs a
+    // global-memory round trip; the first ring's worth of items is looked up
+    // by one lane each in parallel, then the elected lane keeps one lookup in
+    // flight ahead of the copy it is about to issue.
+    auto lookup = [&](int j, StageInfo* si, int* page) {
+      const int it = i0 + j;
+      int lo = 0, hi = R;  // largest q with prefix[q] <= it
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= it) lo = mid; else hi = mid;
+      }
+      si->req = lo;
+      si->blk = it - prefix[lo];
+      si->q0 = b.cu_seqlens_q[lo];
+      si->qlen = b.cu_seqlens_q[lo + 1] - si->q0;
+      si->ctx = b.context_lens[lo];
+      si->pad0 = si->pad1 = 0;
+      *page = b.block_table[(long long)lo * b.bt_stride + si->blk];
+      si->valid = *page >= 0 && *page < b.num_pages;
+    };
+    auto issue = [&](int j, const StageInfo& si, int page) {  // elected lane only
+      const int s = j % C::kStages;
+      info[s] = si;
+      if (si.valid) {
+        mbar_arrive_expect_tx(&full[s], C::kPageBytes);
+        bulk_g2s(smem + S::kPages + (size_t)s * C::kPageBytes,
+                 p.idx_k + (long long)page * C::kPageBytes, C::kPageBytes, &full[s]);
+      } else {
+        atomicOr(p.status, MSA_DEV_BAD_PAGE);
+        mbar_arrive(&full[s]);
+      }
+    };
+    const int first = min(C::kStages, n_items);
+    StageInfo mine{0, 0, 0, 0, 0, 0, 0, 0};
+    int my_page = -1;
+    if (lane < first) lookup(lane, &mine, &my_page);
+    for (int j = 0; j < first; ++j) {  // the ring starts empty: no waits
+      StageInfo si;
+      si.req = __shfl_sync(0xffffffffu, mine.req, j);
+      si.blk = __shfl_sync(0xffffffffu, mine.blk, j);
+      si.valid = __shfl_sync(0xffffffffu, mine.valid, j);
+      si.q0 = __shfl_sync(0xffffffffu, mine.q0, j);
+      si.qlen = __shfl_sync(0xffffffffu, mine.qlen, j);
+      si.ctx = __shfl_sync(0xffffffffu, mine.ctx, j);
+      si.pad0 = si.pad1 = 0;
+      const int pg = __shfl_sync(0xffffffffu, my_page, j);
+      if (lane == 0) issue(j, si, pg);
+    }
+    if (lane == 0 && first < n_items) {
+      StageInfo next;
+      int next_page;
+      lookup(first, &next, &next_page);
+      for (int j = first; j < n_items; ++j) {
+        const StageInfo cur = next;
+        const int cur_page = next_page;
+        if (j + 1 < n_items) lookup(j + 1, &next, &next_page);  // in flight during the wait
         const int s = j % C::kStages, use = j / C::kStages;
-        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+        if (!mbar_wait(&empty[s], (use - 1) & 1)) {
           atomicOr(p.status, MSA_DEV_TIMEOUT);
           break;
         }
-        const int it = i0 + j;
-        int lo = 0, hi = R;  // largest q with prefix[q] <= it
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (prefix[mid] <= it) lo = mid; else hi = mid;
-        }
-        const int blk = it - prefix[lo];
-        const int page = b.block_table[(long long)lo * b.bt_stride + blk];
-        const bool valid = page >= 0 && page < b.num_pages;
-        info[s] = StageInfo{lo, blk, valid ? 1 : 0, 0};
-        if (valid) {
-          mbar_arrive_expect_tx(&full[s], C::kPageBytes);
-          bulk_g2s(smem + S::kPages + (size_t)s * C::kPageBytes,
-                   p.idx_k + (long long)page * C::kPageBytes, C::kPageBytes, &full[s]);
-        } else {
-          atomicOr(p.status, MSA_DEV_BAD_PAGE);
-          mbar_arrive(&full[s]);
-        }
+        issue(j, cur, cur_page);
       }
     }
     return;
   }
 
-  // ---- consumers: warp w owns stage w
+  // ---- consumers: warps (kParts*s .. kParts*s + kParts-1) share stage s
   const int w = warp - 1;
-  const uint8_t* page = smem + S::kPages + (size_t)w * C::kPageBytes;
+  const int st = w / C::kParts, part = w % C::kParts;
+  const int sub0 = part * (kBlock * HI / C::kParts);
+  const uint8_t* page = smem + S::kPages + (size_t)st * C::kPageBytes;
   uint8_t* q_s = smem + S::kQ + (size_t)w * C::kQBytes;
-  int cur_req = -1, cur_g0 = -1;
-  for (int j = w, use = 0; j < n_items; j += C::kStages, ++use) {
-    if (!mbar_wait(&full[w], use & 1)) {
+  float* pmax = pairmax + st * kRowGroup;
+  int cur_req = -1, cur_g0 = -1, pair_uses = 0;
+  bool failed = false;
+  for (int j = st, use = 0; j < n_items && !failed; j += C::kStages, ++use) {
+    // warp-uniform: the page is scored with warp shuffles
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], use & 1))) {
       if (lane == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
       break;
     }
-    const StageInfo si = info[w];
-    const int q0 = b.cu_seqlens_q[si.req];
-    const int qlen = b.cu_seqlens_q[si.req + 1] - q0;
-    const int ctx = b.context_lens[si.req];
+    const StageInfo si = info[st];
+    const int q0 = si.q0, qlen = si.qlen, ctx = si.ctx;
     // rows j with ctx + j >= 128*blk can see this block
     const int jstart = max(0, si.blk * kBlock - ctx);
     for (int g0 = jstart; g0 < qlen; g0 += kRowGroup) {
@@ -260,22 +309,43 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
           cur_g0 = g0;
         }
         if (nr == 1)
-          score_page<DI, HI, 1>(page, q_s, lane, si.blk, pos, best);
+          score_page<DI, HI, 1>(page, q_s, lane, sub0, si.blk, pos, best);
         else if (nr == 2)
-          score_page<DI, HI, 2>(page, q_s, lane, si.blk, pos, best);
+          score_page<DI, HI, 2>(page, q_s, lane, sub0, si.blk, pos, best);
         else
-          score_page<DI, HI, 4>(page, q_s, lane, si.blk, pos, best);  // rows >= nr unused
+          score_page<DI, HI, 4>(page, q_s, lane, sub0, si.blk, pos, best);  // rows >= nr unused
       } else {
 #pragma unroll
         for (int r = 0; r < kRowGroup; ++r) best[r] = -INFINITY;
       }
+      if constexpr (C::kParts == 2) {
+        // part 1 hands its half-page maxima to part 0, which writes the scores
+        if (part == 1) {
 #pragma unroll
-      for (int r = 0; r < kRowGroup; ++r)
-        if (lane == r && r < nr)
-          p.scores[(long long)(q0 + g0 + r) * p.score_stride + si.blk] = best[r];
+          for (int r = 0; r < kRowGroup; ++r)
+            if (lane == r) pmax[r] = best[r];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pairbar[st]);
+        } else {
+          if (!__all_sync(0xffffffffu, mbar_wait(&pairbar[st], pair_uses & 1))) {
+            if (lane == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
+            failed = true;
+            break;
+          }
+#pragma unroll
+          for (int r = 0; r < kRowGroup; ++r) best[r] = fmaxf(best[r], pmax[r]);
+        }
+        ++pair_uses;
+      }
+      if (part == 0) {
+#pragma unroll
+        for (int r = 0; r < kRowGroup; ++r)
+          if (lane == r && r < nr)
+            p.scores[(long long)(q0 + g0 + r) * p.score_stride + si.blk] = best[r];
+      }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[w]);
+    if (lane == 0) mbar_arrive(&empty[st]);
   }
 }
 

@@ -47,6 +47,7 @@ struct TcCfg {
   static constexpr int kBars = kB + kTcStages * kTileBytes;
   static constexpr int kMisc = kBars + 16 * 8;
   static constexpr int kPrefix = kMisc + 64;
+  static_assert(8 + kTcStages <= 16, "misc area holds 16 ints");
   static size_t bytes(int num_reqs) { return 1024 + kPrefix + (size_t)(num_reqs + 1) * 4; }
 };
 
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* acc_empty = a_full + 4;          // [2]
   int* misc = reinterpret_cast<int*>(smem + C::kMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 4);
+  int* stage_valid = misc + 8;  // [kTcStages], written by the producer before arming
   int* prefix = reinterpret_cast<int*>(smem + C::kPrefix);
 
   const msa_batch& b = p.batch;
@@ -265,40 +267,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_items = i1 - i0;
 
   if (n_items > 0) {
-    if (warp == 0 && lane == 0) {
-      // ---------------- TMA producer
-      Cursor cur;
-      cur.seek(b, prefix, R, i0);
+    if (warp == 0) {
+      // ---------------- TMA producer warp: lanes look up 32 items at a time
+      // (request, tile, block, page id); one elected lane then arms the
+      // stages and issues the tile copies in order
       int a_key_q = -1, a_key_t = -1, a_loads = 0;
-      for (int j = 0; j < n_items; ++j) {
-        if (cur.q != a_key_q || cur.tile != a_key_t) {
-          if (a_loads > 0 && !mbar_wait(a_empty, (a_loads - 1) & 1)) {
-            misc[1] = 1;
+      bool stop = false;
+      for (int j0 = 0; j0 < n_items && !stop; j0 += 32) {
+        int mq = 0, mt = 0, mq0 = 0, mpage = -1;
+        if (j0 + lane < n_items) {
+          Cursor cur;
+          cur.seek(b, prefix, R, i0 + j0 + lane);
+          mq = cur.q;
+          mt = cur.tile;
+          mq0 = cur.q0;
+          mpage = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
+        }
+        const int cnt = min(32, n_items - j0);
+        for (int jj = 0; jj < cnt; ++jj) {
+          const int j = j0 + jj;
+          const int q = __shfl_sync(0xffffffffu, mq, jj);
+          const int t = __shfl_sync(0xffffffffu, mt, jj);
+          const int q0 = __shfl_sync(0xffffffffu, mq0, jj);
+          const int page = __shfl_sync(0xffffffffu, mpage, jj);
+          int ok = 1;
+          if (lane == 0) {
+            if (q != a_key_q || t != a_key_t) {
+              if (a_loads > 0 && !mbar_wait(a_empty, (a_loads - 1) & 1)) {
+                ok = 0;
+              } else {
+                mbar_arrive_expect_tx(a_full, C::kTileBytes);
+                for (int h = 0; h < C::kHalves; ++h)
+                  tma_load_2d(smem + C::kA + h * C::kHalfBytes, &qmap, 64 * h, q0 + t * kTileRows,
+                              a_full);
+                a_key_q = q;
+                a_key_t = t;
+                ++a_loads;
+              }
+            }
+            const int s = j % kTcStages;
+            if (ok && j >= kTcStages && !mbar_wait(&b_empty[s], ((j / kTcStages) - 1) & 1))
+              ok = 0;
+            if (ok) {
+              const bool valid = page >= 0 && page < b.num_pages;
+              stage_valid[s] = valid;
+              if (valid) {
+                mbar_arrive_expect_tx(&b_full[s], C::kTileBytes);
+                for (int h = 0; h < C::kHalves; ++h)
+                  tma_load_2d(smem + C::kB + s * C::kTileBytes + h * C::kHalfBytes, &kmap, 64 * h,
+                              page * kBlock, &b_full[s]);
+              } else {
+                mbar_arrive(&b_full[s]);  // nothing to load; the epilogue writes -inf
+              }
+            } else {
+              misc[1] = 1;
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            stop = true;
             break;
           }
-          mbar_arrive_expect_tx(a_full, C::kTileBytes);
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_2d(smem + C::kA + h * C::kHalfBytes, &qmap, 64 * h,
-                        cur.q0 + cur.tile * kTileRows, a_full);
-          a_key_q = cur.q;
-          a_key_t = cur.tile;
-          ++a_loads;
         }
-        const int s = j % kTcStages;
-        if (j >= kTcStages && !mbar_wait(&b_empty[s], ((j / kTcStages) - 1) & 1)) {
-          misc[1] = 1;
-          break;
-        }
-        const int page = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
-        if (page >= 0 && page < b.num_pages) {
-          mbar_arrive_expect_tx(&b_full[s], C::kTileBytes);
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_2d(smem + C::kB + s * C::kTileBytes + h * C::kHalfBytes, &kmap, 64 * h,
-                        page * kBlock, &b_full[s]);
-        } else {
-          mbar_arrive(&b_full[s]);  // nothing to load; the epilogue writes -inf
-        }
-        cur.next(b, prefix, R);
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------- MMA issuer
@@ -325,8 +354,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const int page = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
-        if (page >= 0 && page < b.num_pages) {
+        if (stage_valid[s]) {
           const uint32_t a_base = smem_u32(smem + C::kA);
           const uint32_t b_base = smem_u32(smem + C::kB + s * C::kTileBytes);
 #pragma unroll

@@ -22,6 +22,25 @@ constexpr int kMaxReqs = 4096;
 constexpr int kMaxBlocksPerRow = 16384;
 // requests with at least this many query rows are scored on the tensor cores
 constexpr int kTcMinRows = 64;
+constexpr int kMaxTopk = 2048;
+// at most this many page-16 entries per attention split (<= 32 per warp)
+constexpr int kMaxSplitEntries = 128;
+
+// Attention launch shape: stages of each warp's copy ring and the CTAs per SM
+// the grid is sized for (compile-time, so that launch-shape sweeps can build
+// variants with -D; the defaults are the measured choice).
+#ifndef MSA_ATTN_STAGES_FP8
+#define MSA_ATTN_STAGES_FP8 4
+#endif
+#ifndef MSA_ATTN_STAGES_BF16
+#define MSA_ATTN_STAGES_BF16 3
+#endif
+#ifndef MSA_ATTN_CTAS_FP8
+#define MSA_ATTN_CTAS_FP8 2
+#endif
+#ifndef MSA_ATTN_CTAS_BF16
+#define MSA_ATTN_CTAS_BF16 2
+#endif
 // bounded waits: a wait that has not completed after this long gives up
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
 
@@ -64,14 +83,19 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One test of the phase; the thread may sleep in hardware for up to
+// kWaitSuspendNs while the phase is incomplete (instead of spinning and
+// taking issue slots from the warps that compute).
+constexpr uint32_t kWaitSuspendNs = 100000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -237,8 +261,29 @@ struct AttnLaunch {
 cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream);
 cudaError_t launch_index_score_tc(const ScoreLaunch& p, cudaStream_t stream);
 bool tc_score_supported(int index_heads, int index_dim);
-cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream);
-cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t stream);
+struct KvInsertLaunch {
+  msa_batch batch;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const uint16_t* idx_new;
+  int num_kv_heads, index_heads, index_dim;
+  uint8_t* k_cache;
+  uint8_t* v_cache;
+  uint16_t* idx_k_cache;
+  int kv_fp8, scale_mode;
+  float* k_scale;
+  float* v_scale;
+  int skip_index;
+  uint32_t* status;
+};
+
+cudaError_t launch_kv_insert(const KvInsertLaunch& p, cudaStream_t stream);
+
+// `programmatic`: the kernel may start while the previous kernel on the
+// stream finishes (programmatic dependent launch); it waits for that kernel's
+// results on the device before reading them.
+cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream, bool programmatic);
+cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t stream, bool programmatic);
 
 int device_sm_count();
 

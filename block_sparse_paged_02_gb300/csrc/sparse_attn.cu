@@ -31,6 +31,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleSlack = 8.f;  // log2 units: unnormalised weights stay <= 256
 constexpr int kAccStride = 132;  // padded head stride of the shared-memory merge area
 constexpr int kAccWarpFloats = kMaxHeads * kAccStride;  // 2112
 
@@ -39,11 +40,14 @@ struct AttnCfg {
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kSlab = kPage16 * kHeadDim * kElem;  // one page-16 K (or V) slab
   static constexpr int kStageBytes = 2 * kSlab + 2 * 64;    // K, V, k-scales, v-scales
-  static constexpr int kStages = FP8 ? 4 : 3;
+  static constexpr int kStages = FP8 ? MSA_ATTN_STAGES_FP8 : MSA_ATTN_STAGES_BF16;
   static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
   static constexpr int kMergeBytes = kWarps * (kAccWarpFloats + 2 * kMaxHeads) * 4;
   static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
-  static constexpr int kSmemBytes = kDataBytes + kWarps * kStages * 8 + 64;
+  static constexpr int kQBytes = kMaxHeads * kHeadDim * 2;  // the row's queries, bf16
+  static constexpr int kQ = kDataBytes;
+  static constexpr int kBarOff = kQ + kQBytes;
+  static constexpr int kSmemBytes = kBarOff + (kWarps * kStages + 1) * 8 + 64;
 };
 
 __device__ __forceinline__ int acc_index(int head, int dim) {
@@ -51,45 +55,64 @@ __device__ __forceinline__ int acc_index(int head, int dim) {
 }
 
 template <bool FP8, int SCALE>
-__global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(const AttnLaunch p) {
+__global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_CTAS_BF16)
+    sparse_attn_kernel(const AttnLaunch p) {
   using C = AttnCfg<FP8>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
-  int* flags = reinterpret_cast<int*>(smem + C::kDataBytes + kWarps * C::kStages * 8);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* qbar = bars + kWarps * C::kStages;
+  int* flags = reinterpret_cast<int*>(qbar + 1);
+  const uint8_t* q_s = smem + C::kQ;
 
   const int split = blockIdx.x, r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const long long tbl_row = (long long)r * p.tbl_stride;
+  const unsigned full = 0xffffffffu;
 
-  // ---- validate the whole row (every split decides the same way)
-  int len = p.sparse_len[r];
-  bool poisoned = len < 0 || (long long)len > (long long)kPage16 * p.tbl_stride;
-  int nent = poisoned ? 0 : (len + kPage16 - 1) / kPage16;
-  int bad = 0;
-  for (int i = tid; i < nent; i += kThreads) {
-    const int e = p.tbl[tbl_row + i];
-    bad |= (e < 0 || (long long)e >= p.num_pages16);
+  // ---- prologue independent of the previous kernel: the row's queries
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const uint32_t q_bytes = (uint32_t)p.num_heads * kHeadDim * 2;
+  if (tid == 0) {
+    mbar_init(qbar, 1);
+    for (int s = 0; s < kWarps * C::kStages; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(qbar, q_bytes);
+    bulk_g2s(smem + C::kQ, p.q + (long long)r * p.num_heads * kHeadDim, q_bytes, qbar);
   }
-  poisoned = __syncthreads_or(bad) || poisoned;
-  if (poisoned) {
-    len = 0;
-    nent = 0;
-  }
-  const int n_active = max(1, (nent + p.pages_per_split - 1) / p.pages_per_split);
-  if (split >= n_active) return;
-  if (poisoned && split == 0 && tid == 0) atomicOr(p.status, MSA_DEV_BAD_TABLE);
+  // sparse tables and lengths come from the previous kernel on the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- this warp's page-16 entries: split*pps + warp + 4*i
+  // this warp's page-16 entries are split*pps + warp + 4*i, one per lane; the
+  // table load does not depend on the length, so both are in flight together
   const int e_begin = split * p.pages_per_split;
+  const int e_lane = e_begin + warp + kWarps * lane;
+  const bool lane_in_split = kWarps * lane + warp < p.pages_per_split && e_lane < p.tbl_stride;
+  long long my_e = lane_in_split ? (long long)p.tbl[tbl_row + e_lane] : 0ll;
+  int len = p.sparse_len[r];
+  const bool len_bad = len < 0 || (long long)len > (long long)kPage16 * p.tbl_stride;
+  const int nent = len_bad ? 0 : (len + kPage16 - 1) / kPage16;
+  const int n_active = max(1, (nent + p.pages_per_split - 1) / p.pages_per_split);
+  const bool active = split < n_active;
   const int e_end = min(nent, e_begin + p.pages_per_split);
-  const int n_my = e_end > e_begin + warp ? (e_end - (e_begin + warp) + kWarps - 1) / kWarps : 0;
+  int n_my = active && e_end > e_begin + warp ? (e_end - (e_begin + warp) + kWarps - 1) / kWarps : 0;
+  bool entry_bad = false;
+  if (lane < n_my) entry_bad = my_e < 0 || my_e >= p.num_pages16;
+  __syncthreads();  // barrier inits visible to every warp
+  const bool cta_bad = __syncthreads_or(entry_bad) != 0;
+  if (!active) {
+    // still drain the query copy this CTA issued before leaving
+    if (tid == 0 && !mbar_wait(qbar, 0)) atomicOr(p.status, MSA_DEV_TIMEOUT);
+    return;
+  }
+  if (cta_bad) n_my = 0;  // never copy from an id outside the pool
+  const bool single = n_active == 1;
+  if (single && (len_bad || cta_bad) && tid == 0) atomicOr(p.status, MSA_DEV_BAD_TABLE);
   uint8_t* ring = smem + (size_t)warp * C::kStages * C::kStageBytes;
   uint64_t* wbar = bars + warp * C::kStages;
 
-  auto issue = [&](int i) {  // lane 0 only
+  auto issue = [&](int i, long long e) {  // lane 0 only
     const int st = i % C::kStages;
-    const long long e = p.tbl[tbl_row + e_begin + warp + kWarps * i];
     uint8_t* dst = ring + st * C::kStageBytes;
     const uint32_t bytes = 2 * C::kSlab + (SCALE == MSA_SCALE_PER_TOKEN_HEAD ? 128 : 0);
     mbar_arrive_expect_tx(&wbar[st], bytes);
@@ -100,36 +123,41 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
       bulk_g2s(dst + 2 * C::kSlab + 64, p.v_scale + e * kPage16, 64, &wbar[st]);
     }
   };
-  if (lane == 0) {
-    for (int s = 0; s < C::kStages; ++s) mbar_init(&wbar[s], 1);
-    fence_barrier_init();
-    for (int i = 0; i < min(n_my, C::kStages); ++i) issue(i);
+  for (int i = 0; i < min(n_my, C::kStages); ++i) {
+    const long long e = __shfl_sync(full, my_e, i);
+    if (lane == 0) issue(i, e);
   }
-  __syncwarp();
+  if (!__syncthreads_and(mbar_wait(qbar, 0))) {  // CTA-uniform decision
+    if (tid == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
+    n_my = 0;
+  }
 
   // ---- query fragments (A operand of S = Q K^T), permuted k-slots:
   // k-step kk, slots (2c, 2c+1) <-> dims 32c+4kk+{0,1}; (2c+8, 2c+9) <-> +{2,3}
   uint32_t qa[8][4];
-  {
-    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q + (long long)r * p.num_heads * kHeadDim);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    // head row h, dims [32c, 32c+32): four 16-byte loads, 16 bf16 pairs
+    const int h = g + 8 * half;
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (h < p.num_heads) v = lds128(q_s + h * kHeadDim * 2 + 64 * c + 16 * j);
+      w[4 * j] = v.x;
+      w[4 * j + 1] = v.y;
+      w[4 * j + 2] = v.z;
+      w[4 * j + 3] = v.w;
+    }
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int h = g + 8 * half;
-        uint32_t w01 = 0, w23 = 0;
-        if (h < p.num_heads) {
-          const int d = 32 * c + 4 * kk;
-          w01 = q32[(h * kHeadDim + d) >> 1];
-          w23 = q32[(h * kHeadDim + d + 2) >> 1];
-        }
-        if constexpr (FP8) {  // f16 operands for the fp8 path
-          w01 = pack_f16x2(bf16lo(w01), bf16hi(w01));
-          w23 = pack_f16x2(bf16lo(w23), bf16hi(w23));
-        }
-        qa[kk][half] = w01;      // a0a1 (row g) / a2a3 (row g+8)
-        qa[kk][2 + half] = w23;  // a4a5 (row g) / a6a7 (row g+8)
+      uint32_t w01 = w[2 * kk], w23 = w[2 * kk + 1];  // dims 32c+4kk+{0,1} and +{2,3}
+      if constexpr (FP8) {  // f16 operands for the fp8 path
+        w01 = pack_f16x2(bf16lo(w01), bf16hi(w01));
+        w23 = pack_f16x2(bf16lo(w23), bf16hi(w23));
       }
+      qa[kk][half] = w01;      // a0a1 (row g) / a2a3 (row g+8)
+      qa[kk][2 + half] = w23;  // a4a5 (row g) / a6a7 (row g+8)
     }
   }
   float scale2 = p.softmax_scale * kLog2e;  // logits in log2 units
@@ -143,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
   bool timed_out = false;
   for (int i = 0; i < n_my; ++i) {
     const int st = i % C::kStages;
-    if (!mbar_wait(&wbar[st], (i / C::kStages) & 1)) {
+    // warp-uniform: the MMAs below need the whole warp
+    if (!__all_sync(full, mbar_wait(&wbar[st], (i / C::kStages) & 1))) {
       timed_out = true;
       break;
     }
@@ -155,17 +184,21 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
     const int nvalid = min(kPage16, len - tok0);              // >= 1
 
     // ---- S = Q K^T for the 16 tokens: two n-tiles (tokens g and 8+g)
-    float s[2][4];
+    // two accumulators per n-tile (even / odd k-steps) halve the dependent
+    // MMA chain; they are summed below
+    float s[2][4], s_odd[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      s_odd[nt][0] = s_odd[nt][1] = s_odd[nt][2] = s_odd[nt][3] = 0.f;
       const uint8_t* krow = ks_ + (8 * nt + g) * kHeadDim * C::kElem + 32 * c * C::kElem;
       if constexpr (FP8) {
         const uint4 k0 = lds128(krow), k1 = lds128(krow + 16);
         const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma16816<true>(s[nt], qa[kk], e4m3x2_to_f16x2((uint16_t)(kw[kk] & 0xffffu)),
+          mma16816<true>((kk & 1) ? s_odd[nt] : s[nt], qa[kk],
+                         e4m3x2_to_f16x2((uint16_t)(kw[kk] & 0xffffu)),
                          e4m3x2_to_f16x2((uint16_t)(kw[kk] >> 16)));
       } else {
         uint32_t kw[16];
@@ -178,8 +211,11 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
           kw[4 * h4 + 3] = v.w;
         }
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma16816<false>(s[nt], qa[kk], kw[2 * kk], kw[2 * kk + 1]);
+        for (int kk = 0; kk < 8; ++kk)
+          mma16816<false>((kk & 1) ? s_odd[nt] : s[nt], qa[kk], kw[2 * kk], kw[2 * kk + 1]);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] += s_odd[nt][e];
     }
     // ---- scale, mask, online softmax (rows g and g+8)
 #pragma unroll
@@ -194,30 +230,44 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
     float mx[2];
     mx[0] = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
     mx[1] = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-    float alpha[2], base[2];
+    // Lazy rescaling: the reference max m_run only moves when a slab's max
+    // exceeds it by more than kRescaleSlack (log2 units), so p <= 2^slack and
+    // the accumulators are rescaled only on those (rare) slabs.
+    bool move[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 1));
       mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
-      const float mn = fmaxf(m_run[hh], mx[hh]);
-      alpha[hh] = m_run[hh] == -INFINITY ? 0.f : exp2f(m_run[hh] - mn);
-      base[hh] = mn == -INFINITY ? 0.f : mn;
-      m_run[hh] = mn;
+      move[hh] = mx[hh] > m_run[hh] + kRescaleSlack;
     }
+    if (__any_sync(0xffffffffu, move[0] || move[1])) {
+      float alpha[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        alpha[hh] = 1.f;
+        if (move[hh]) {
+          alpha[hh] = m_run[hh] == -INFINITY ? 0.f : exp2f(m_run[hh] - mx[hh]);
+          m_run[hh] = mx[hh];
+        }
+        l_run[hh] *= alpha[hh];
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        o[j][0] *= alpha[0];
+        o[j][1] *= alpha[0];
+        o[j][2] *= alpha[1];
+        o[j][3] *= alpha[1];
+      }
+    }
+    const float base[2] = {m_run[0] == -INFINITY ? 0.f : m_run[0],
+                           m_run[1] == -INFINITY ? 0.f : m_run[1]};
     float pr[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) pr[nt][e] = exp2f(s[nt][e] - base[e >> 1]);
-    l_run[0] = l_run[0] * alpha[0] + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
-    l_run[1] = l_run[1] * alpha[1] + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      o[j][0] *= alpha[0];
-      o[j][1] *= alpha[0];
-      o[j][2] *= alpha[1];
-      o[j][3] *= alpha[1];
-    }
+    l_run[0] += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
+    l_run[1] += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
     if constexpr (SCALE == MSA_SCALE_PER_TOKEN_HEAD) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
@@ -244,11 +294,15 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
         const uint4 v = lds128(vs_ + vt[a] * kHeadDim + 16 * g);
-        const bool ok = vt[a] < nvalid;  // never let garbage past the end reach P V
-        vw[a][0] = ok ? v.x : 0u;
-        vw[a][1] = ok ? v.y : 0u;
-        vw[a][2] = ok ? v.z : 0u;
-        vw[a][3] = ok ? v.w : 0u;
+        vw[a][0] = v.x;
+        vw[a][1] = v.y;
+        vw[a][2] = v.z;
+        vw[a][3] = v.w;
+      }
+      if (nvalid < kPage16) {  // never let garbage past the end reach P V
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+          if (vt[a] >= nvalid) vw[a][0] = vw[a][1] = vw[a][2] = vw[a][3] = 0u;
       }
 #pragma unroll
       for (int j2 = 0; j2 < 8; ++j2) {  // n-tiles 2*j2, 2*j2+1
@@ -267,15 +321,21 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
       for (int a = 0; a < 4; ++a) {
         const uint8_t* src = vs_ + (vt[a] * kHeadDim + 16 * g) * 2;
         const uint4 v0 = lds128(src), v1 = lds128(src + 16);
-        const bool ok = vt[a] < nvalid;
-        vw[a][0] = ok ? v0.x : 0u;
-        vw[a][1] = ok ? v0.y : 0u;
-        vw[a][2] = ok ? v0.z : 0u;
-        vw[a][3] = ok ? v0.w : 0u;
-        vw[a][4] = ok ? v1.x : 0u;
-        vw[a][5] = ok ? v1.y : 0u;
-        vw[a][6] = ok ? v1.z : 0u;
-        vw[a][7] = ok ? v1.w : 0u;
+        vw[a][0] = v0.x;
+        vw[a][1] = v0.y;
+        vw[a][2] = v0.z;
+        vw[a][3] = v0.w;
+        vw[a][4] = v1.x;
+        vw[a][5] = v1.y;
+        vw[a][6] = v1.z;
+        vw[a][7] = v1.w;
+      }
+      if (nvalid < kPage16) {  // never let garbage past the end reach P V
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+          if (vt[a] >= nvalid)
+#pragma unroll
+            for (int x = 0; x < 8; ++x) vw[a][x] = 0u;
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
@@ -286,9 +346,12 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
       }
     }
     __syncwarp();
-    if (lane == 0 && i + C::kStages < n_my) {
-      fence_proxy_async_smem();
-      issue(i + C::kStages);
+    if (i + C::kStages < n_my) {
+      const long long e = __shfl_sync(full, my_e, i + C::kStages);
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue(i + C::kStages, e);
+      }
     }
   }
   if (timed_out && lane == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
@@ -303,13 +366,14 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
   float* acc_s = reinterpret_cast<float*>(smem);
   float* ml_s = acc_s + kWarps * kAccWarpFloats;  // [warp][m 16 | l 16]
   {
-    float* aw = acc_s + warp * kAccWarpFloats;
+    // acc_index(g, 32c + j) = g*132 + 33c + j for j < 32: one base, immediate offsets
+    float* aw = acc_s + warp * kAccWarpFloats + acc_index(g, 32 * c);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      aw[acc_index(g, 32 * c + j)] = o[j][0];
-      aw[acc_index(g, 32 * c + 16 + j)] = o[j][1];
-      aw[acc_index(g + 8, 32 * c + j)] = o[j][2];
-      aw[acc_index(g + 8, 32 * c + 16 + j)] = o[j][3];
+      aw[j] = o[j][0];
+      aw[16 + j] = o[j][1];
+      aw[8 * kAccStride + j] = o[j][2];
+      aw[8 * kAccStride + 16 + j] = o[j][3];
     }
     if (c == 0) {
       ml_s[warp * 32 + g] = m_run[0];
@@ -332,12 +396,16 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
     const float mw = ml_s[w * 32 + head];
     const float f = mw == -INFINITY ? 0.f : exp2f(mw - mh);
     lh += f * ml_s[w * 32 + 16 + head];
+    const float* ar = acc_s + w * kAccWarpFloats + acc_index(head, d0);  // d0..d0+15: same 32-block
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] += f * acc_s[w * kAccWarpFloats + acc_index(head, d0 + j)];
+    for (int j = 0; j < 16; ++j) acc[j] += f * ar[j];
   }
 
-  if (n_active > 1) {
-    // ---- publish this split's partial; the last CTA of the row merges all
+  bool empty_row = single && (len_bad || cta_bad);
+  if (!single) {
+    // ---- publish this split's partial; the last CTA of the row merges all.
+    // A CTA that saw an id outside the pool flags the row in the counter's
+    // top bit before counting itself in.
     float* part = p.partials + ((long long)r * p.splits + split) * kPartFloats;
     if ((tid & 7) == 0) {
       part[head] = mh;
@@ -349,32 +417,52 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
       pa4[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
     __threadfence();
     __syncthreads();
-    if (tid == 0) flags[0] = (atomicAdd(&p.counters[r], 1u) == (unsigned)(n_active - 1));
+    if (tid == 0) {
+      if (cta_bad) atomicOr(&p.counters[r], 0x80000000u);
+      const unsigned old = atomicAdd(&p.counters[r], 1u);
+      flags[0] = ((old & 0x7fffffffu) == (unsigned)(n_active - 1));
+      flags[1] = ((old | (cta_bad ? 0x80000000u : 0u)) & 0x80000000u) != 0;
+    }
     __syncthreads();
     if (!flags[0]) return;
     __threadfence();
+    empty_row = flags[1] != 0;
     mh = -INFINITY;
-    for (int sp = 0; sp < n_active; ++sp)
-      mh = fmaxf(mh, __ldcg(p.partials + ((long long)r * p.splits + sp) * kPartFloats + head));
     lh = 0.f;
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-    for (int sp = 0; sp < n_active; ++sp) {
+#pragma unroll 4
+    for (int sp = 0; sp < n_active; ++sp) {  // online merge, one pass over the partials
       const float* ps = p.partials + ((long long)r * p.splits + sp) * kPartFloats;
       const float ms = __ldcg(ps + head);
-      const float f = ms == -INFINITY ? 0.f : exp2f(ms - mh);
-      lh += f * __ldcg(ps + kMaxHeads + head);
+      const float ls = __ldcg(ps + kMaxHeads + head);
       const float4* a4 = reinterpret_cast<const float4*>(ps + 2 * kMaxHeads + head * kHeadDim + d0);
+      float4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = __ldcg(a4 + j);
+      const float mn = fmaxf(mh, ms);
+      const float fo = mh == -INFINITY ? 0.f : exp2f(mh - mn);
+      const float fs = ms == -INFINITY ? 0.f : exp2f(ms - mn);
+      lh = lh * fo + ls * fs;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float4 v = __ldcg(a4 + j);
-        acc[4 * j] += f * v.x;
-        acc[4 * j + 1] += f * v.y;
-        acc[4 * j + 2] += f * v.z;
-        acc[4 * j + 3] += f * v.w;
+        acc[4 * j] = acc[4 * j] * fo + v[j].x * fs;
+        acc[4 * j + 1] = acc[4 * j + 1] * fo + v[j].y * fs;
+        acc[4 * j + 2] = acc[4 * j + 2] * fo + v[j].z * fs;
+        acc[4 * j + 3] = acc[4 * j + 3] * fo + v[j].w * fs;
       }
+      mh = mn;
     }
-    if (tid == 0) p.counters[r] = 0;  // ready for the next call / graph replay
+    if (tid == 0) {
+      p.counters[r] = 0;  // ready for the next call / graph replay
+      if (empty_row) atomicOr(p.status, MSA_DEV_BAD_TABLE);
+    }
+  }
+  if (empty_row) {  // a poisoned row is an empty row
+    mh = -INFINITY;
+    lh = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
   }
 
   // ---- finalize: sink in the denominator, natural-log LSE
@@ -404,29 +492,39 @@ __global__ void __launch_bounds__(kThreads, FP8 ? 3 : 2) sparse_attn_kernel(cons
 }
 
 template <bool FP8, int SCALE>
-cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t stream) {
+cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t stream, bool programmatic) {
   using C = AttnCfg<FP8>;
   auto kern = sparse_attn_kernel<FP8, SCALE>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.splits, p.num_rows);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits, p.num_rows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = programmatic ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
 
-cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t stream) {
+cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t stream, bool programmatic) {
   if (p.num_rows == 0) return cudaSuccess;
   if (p.kv_fp8) {
-    if (p.scale_mode == MSA_SCALE_NONE) return launch_cfg<true, MSA_SCALE_NONE>(p, stream);
-    if (p.scale_mode == MSA_SCALE_SCALAR) return launch_cfg<true, MSA_SCALE_SCALAR>(p, stream);
-    return launch_cfg<true, MSA_SCALE_PER_TOKEN_HEAD>(p, stream);
+    if (p.scale_mode == MSA_SCALE_NONE) return launch_cfg<true, MSA_SCALE_NONE>(p, stream, programmatic);
+    if (p.scale_mode == MSA_SCALE_SCALAR)
+      return launch_cfg<true, MSA_SCALE_SCALAR>(p, stream, programmatic);
+    return launch_cfg<true, MSA_SCALE_PER_TOKEN_HEAD>(p, stream, programmatic);
   }
-  if (p.scale_mode == MSA_SCALE_NONE) return launch_cfg<false, MSA_SCALE_NONE>(p, stream);
-  if (p.scale_mode == MSA_SCALE_SCALAR) return launch_cfg<false, MSA_SCALE_SCALAR>(p, stream);
-  return launch_cfg<false, MSA_SCALE_PER_TOKEN_HEAD>(p, stream);
+  if (p.scale_mode == MSA_SCALE_NONE) return launch_cfg<false, MSA_SCALE_NONE>(p, stream, programmatic);
+  if (p.scale_mode == MSA_SCALE_SCALAR)
+    return launch_cfg<false, MSA_SCALE_SCALAR>(p, stream, programmatic);
+  return launch_cfg<false, MSA_SCALE_PER_TOKEN_HEAD>(p, stream, programmatic);
 }
 
 }  // namespace msa

@@ -8,13 +8,14 @@
 // "Implementation breakdown" item 3 (page-16 view of the page-128 cache) and
 // "Review highlights" (the zero fill must stay inside the row width).
 //
-// One CTA per query row.  The row's nb (<= 16384) candidate scores become
-// orderable 32-bit keys in shared memory; a 4-pass 8-bit radix select finds
-// the k-th largest key T and how many keys equal to T are still needed; a
-// stable ballot/popc compaction in block order then emits exactly the
-// selected blocks in ascending order (keys > T, plus the lowest-indexed keys
-// == T), which is the unique result under the lower-index tie rule.  The
-// table expansion and length follow in the same CTA.
+// One CTA of 256 threads per row; each thread holds KPT consecutive block
+// scores as orderable 32-bit keys in registers.  The k-th largest key T is
+// found bit by bit from the top: T takes a bit whenever at least k keys are
+// >= the candidate, each count being a warp reduction plus one barrier
+// (double-buffered partial counts).  Block-wide exclusive scans then place,
+// in ascending block order, every key > T and the lowest-indexed keys == T
+// until k are taken -- the unique result under the lower-index tie rule.
+// The page-16 expansion and the length follow in the same CTA.
 #include "msa_internal.cuh"
 
 namespace msa {
@@ -23,13 +24,16 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-// Block-wide exclusive count of `flag` over the CTA in thread order, plus
-// the total.  Uses `scratch[kWarps]`.
-__device__ __forceinline__ int block_excl_count(bool flag, int* scratch, int* total) {
+// exclusive scan of one int per thread over the CTA (two barriers)
+__device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned bal = __ballot_sync(0xffffffffu, flag);
-  const int in_warp = __popc(bal & ((1u << lane) - 1u));
-  if (lane == 0) scratch[warp] = __popc(bal);
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) scratch[warp] = x;
   __syncthreads();
   int before = 0, all = 0;
 #pragma unroll
@@ -40,77 +44,79 @@ __device__ __forceinline__ int block_excl_count(bool flag, int* scratch, int* to
   }
   __syncthreads();
   *total = all;
-  return before + in_warp;
+  return before + x - v;
 }
 
-// Block-wide inclusive scan of one value per thread.
-__device__ __forceinline__ int block_incl_scan(int v, int* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  if (lane == 31) scratch[warp] = v;
-  __syncthreads();
-  int before = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) before += (w < warp) ? scratch[w] : 0;
-  __syncthreads();
-  return before + v;
-}
-
+template <int KPT>
 __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p) {
-  extern __shared__ uint32_t keys[];  // [bt_stride] keys, then [topk] selected blocks
-  __shared__ uint32_t hist[256];
-  __shared__ int scratch[kWarps];
-  __shared__ int s_req, s_digit, s_rem, s_bad;
+  extern __shared__ int sel[];  // [topk] selected blocks, ascending
+  __shared__ int s_cnt[2][kWarps];
+  __shared__ int s_scan[kWarps];
+  __shared__ int s_bad;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   const msa_batch& b = p.batch;
   const int r = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = b.num_reqs;
-  int* sel = reinterpret_cast<int*>(keys + b.bt_stride);
+  const int k = p.topk;
+  const unsigned full = 0xffffffffu;
 
-  // ---- which request owns the row, and is it usable?
-  if (tid == 0) {
-    s_bad = 0;
-    s_req = -1;
-    if (!(b.cu_seqlens_q[0] == 0 && b.cu_seqlens_q[R] == b.num_rows)) s_bad = MSA_DEV_MALFORMED;
+  // ---- tiling check and the row's request: count requests starting at or before r
+  if (tid == 0)
+    s_bad = (b.cu_seqlens_q[0] == 0 && b.cu_seqlens_q[R] == b.num_rows) ? 0 : MSA_DEV_MALFORMED;
+  int le = 0;
+  bool mono = true;
+  for (int q = tid; q < R; q += kThreads) {
+    const int c0 = b.cu_seqlens_q[q], c1 = b.cu_seqlens_q[q + 1];
+    mono &= c1 >= c0;
+    le += c0 <= r;
   }
+  le = __reduce_add_sync(full, le);
+  if (lane == 0) s_cnt[0][warp] = le;
+  const bool all_mono = __syncthreads_and(mono) != 0;
+  if (!all_mono && tid == 0) s_bad = MSA_DEV_MALFORMED;
   __syncthreads();
-  for (int q = tid; q < R; q += kThreads)
-    if (b.cu_seqlens_q[q + 1] < b.cu_seqlens_q[q]) s_bad = MSA_DEV_MALFORMED;
-  __syncthreads();
-  int q = -1, q0 = 0, qlen = 0, ctx = 0, nbq = 0;
   uint32_t bad = (uint32_t)s_bad;
+  int count_le = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) count_le += s_cnt[0][w];
+  __syncthreads();  // s_cnt is reused below
+
+  int q = -1, q0 = 0, qlen = 0, ctx = 0, nbq = 0, L = 0, n = 0;
+  uint32_t key[KPT];
+  const float* srow = p.scores + (long long)r * p.score_stride;
   if (!bad) {
-    if (tid == 0) {  // largest q with cu_q[q] <= r (rows are tiled, so r < cu_q[q+1])
-      int lo = 0, hi = R;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (b.cu_seqlens_q[mid] <= r) lo = mid; else hi = mid;
-      }
-      while (lo < R - 1 && b.cu_seqlens_q[lo + 1] <= r) ++lo;  // skip empty requests
-      s_req = lo;
-    }
-    __syncthreads();
-    q = s_req;
+    q = count_le - 1;  // cu_q is sorted and r < cu_q[R]
     bad = request_lengths(b, q, &q0, &qlen, &ctx, &nbq);
-    if (!bad) {
-      int page_bad = 0;
-      for (int blk = tid; blk < nbq; blk += kThreads) {
-        const int page = b.block_table[(long long)q * b.bt_stride + blk];
-        page_bad |= (page < 0 || page >= b.num_pages);
-      }
-      if (__syncthreads_or(page_bad)) bad = MSA_DEV_BAD_PAGE;
+  }
+  if (!bad) {
+    int page_bad = 0;
+    for (int blk = tid; blk < nbq; blk += kThreads) {
+      const int page = b.block_table[(long long)q * b.bt_stride + blk];
+      page_bad |= (page < 0 || page >= b.num_pages);
+    }
+    if (__syncthreads_or(page_bad)) bad = MSA_DEV_BAD_PAGE;
+  }
+  // everything above reads only the batch geometry; the scores come from the
+  // previous kernel on the stream, which may still be running until here
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!bad) {
+    L = ctx + (r - q0) + 1;  // visible tokens
+    n = (L + kBlock - 1) / kBlock;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      const int blk = KPT * tid + i;
+      key[i] = blk < n ? score_key(srow[blk]) : 0u;
     }
   }
-  const bool first_row_of_req = (q >= 0) && (r == q0);
+  int32_t* out_idx = p.topk_idx + (long long)r * k;
+  int32_t* out_tbl = p.tbl + (long long)r * p.tbl_stride;
   if (bad) {
-    if (tid == 0 && (first_row_of_req || (bad == MSA_DEV_MALFORMED && r == 0)))
-      atomicOr(p.status, bad);
-    for (int i = tid; i < p.topk; i += kThreads) p.topk_idx[(long long)r * p.topk + i] = -1;
-    for (int i = tid; i < p.tbl_stride; i += kThreads) p.tbl[(long long)r * p.tbl_stride + i] = 0;
+    const bool report = (q >= 0) ? (r == q0) : (r == 0);
+    if (tid == 0 && report) atomicOr(p.status, bad);
+    for (int i = tid; i < k; i += kThreads) out_idx[i] = -1;
+    for (int i = tid; i < p.tbl_stride; i += kThreads) out_tbl[i] = 0;
     if (tid == 0) {
       p.sparse_len[r] = 0;
       if (p.attn_counters) p.attn_counters[r] = 0;
@@ -118,69 +124,61 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
     return;
   }
 
-  const int pos = ctx + (r - q0);
-  const int L = pos + 1;
-  const int n = (L + kBlock - 1) / kBlock;
-  const int k = p.topk;
   const int m = min(k, n);
-  const float* srow = p.scores + (long long)r * p.score_stride;
-
-  // ---- threshold key T and the number of keys == T to take
-  uint32_t T = 0;
-  int need_eq = 0;
-  const bool take_all = n <= k;
-  if (!take_all) {
-    for (int i = tid; i < n; i += kThreads) keys[i] = score_key(srow[i]);
-    uint32_t prefix = 0, mask = 0;
-    int remaining = k;
-    __syncthreads();
+  if (n <= k) {  // every candidate is selected
+    for (int i = tid; i < n; i += kThreads) {
+      sel[i] = i;
+      out_idx[i] = i;
+    }
+  } else {
+    // ---- the k-th largest key T (keys of blocks >= n are 0 < any candidate)
+    uint32_t T = 0;
 #pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      hist[tid] = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = T | (1u << bit);
+      int c = 0;
+#pragma unroll
+      for (int i = 0; i < KPT; ++i) c += key[i] >= cand;
+      c = __reduce_add_sync(full, c);
+      if (lane == 0) s_cnt[bit & 1][warp] = c;
       __syncthreads();
-      for (int i = tid; i < n; i += kThreads) {
-        const uint32_t key = keys[i];
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      // suffix counts: thread t looks at digit 255 - t
-      const int v = (int)hist[255 - tid];
-      const int incl = block_incl_scan(v, scratch);  // keys with digit >= 255 - t
-      if (incl >= remaining && incl - v < remaining) {
-        s_digit = 255 - tid;
-        s_rem = remaining - (incl - v);
-      }
-      __syncthreads();
-      prefix |= (uint32_t)s_digit << shift;
-      mask |= 255u << shift;
-      remaining = s_rem;
-      __syncthreads();
+      int total = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) total += s_cnt[bit & 1][w];
+      if (total >= k) T = cand;
     }
-    T = prefix;
-    need_eq = remaining;
-  }
-
-  // ---- stable compaction in block order -> ascending selected blocks
-  int eq_carry = 0, sel_carry = 0;
-  for (int base = 0; base < n; base += kThreads) {
-    const int i = base + tid;
-    uint32_t key = 0;
-    if (!take_all && i < n) key = keys[i];
-    const bool is_eq = !take_all && i < n && key == T;
-    int eq_total;
-    const int eq_before = block_excl_count(is_eq, scratch, &eq_total);
-    const bool take =
-        i < n && (take_all || key > T || (is_eq && eq_carry + eq_before < need_eq));
-    int sel_total;
-    const int at = sel_carry + block_excl_count(take, scratch, &sel_total);
-    if (take) {
-      sel[at] = i;
-      p.topk_idx[(long long)r * k + at] = i;
+    // ---- keys > T, then the lowest-indexed keys == T until k are taken
+    int my_gt = 0, my_eq = 0;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      const bool live = KPT * tid + i < n;
+      my_gt += live && key[i] > T;
+      my_eq += live && key[i] == T;
     }
-    eq_carry += eq_total;
-    sel_carry += sel_total;
+    int gt_total, eq_total, sel_total;
+    block_excl_scan(my_gt, s_scan, &gt_total);
+    const int eq_before = block_excl_scan(my_eq, s_scan, &eq_total);
+    const int need_eq = k - gt_total;
+    const int take_eq = max(0, min(my_eq, need_eq - eq_before));
+    int at = block_excl_scan(my_gt + take_eq, s_scan, &sel_total);
+    int eq_taken = 0;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      const int blk = KPT * tid + i;
+      const bool live = blk < n;
+      bool take = live && key[i] > T;
+      if (live && key[i] == T && eq_taken < take_eq) {
+        take = true;
+        ++eq_taken;
+      }
+      if (take) {
+        sel[at] = blk;
+        out_idx[at] = blk;
+        ++at;
+      }
+    }
   }
-  for (int i = m + tid; i < k; i += kThreads) p.topk_idx[(long long)r * k + i] = -1;
+  for (int i = m + tid; i < k; i += kThreads) out_idx[i] = -1;
   __syncthreads();
 
   // ---- page-16 expansion, zero fill bounded by the row width
@@ -193,7 +191,7 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
       const int valid = min(kBlock, L - kBlock * blk);
       if (j < (valid + kPage16 - 1) / kPage16) v = 8 * bt_row[blk] + j;
     }
-    p.tbl[(long long)r * p.tbl_stride + i] = v;
+    out_tbl[i] = v;
   }
   if (tid == 0) {
     // only the block holding the row's last token can be partial, and it is
@@ -203,16 +201,29 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
   }
 }
 
+template <int KPT>
+cudaError_t launch_kpt(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.batch.num_rows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)p.topk * sizeof(int);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = programmatic ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, topk_table_kernel<KPT>, p);
+}
+
 }  // namespace
 
-cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream) {
+cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
   if (p.batch.num_rows == 0) return cudaSuccess;
-  const size_t smem = (size_t)(p.batch.bt_stride + p.topk) * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(topk_table_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  topk_table_kernel<<<p.batch.num_rows, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  // a row has at most bt_stride candidate blocks
+  if (p.batch.bt_stride <= kThreads * 4) return launch_kpt<4>(p, stream, programmatic);
+  if (p.batch.bt_stride <= kThreads * 16) return launch_kpt<16>(p, stream, programmatic);
+  return launch_kpt<64>(p, stream, programmatic);
 }
 
 }  // namespace msa

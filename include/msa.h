@@ -256,6 +256,31 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
                       size_t workspace_bytes, uint32_t* dev_status, const msa_trace* trace,
                       cudaStream_t stream);
 
+/* The step before the path: write the new tokens' K, V and index-K into
+ * the paged pools [P47287 "Implementation breakdown" item 1: the fused
+ * q/k-norm + RoPE + KV insert with skip_index, so index-reuse layers skip the
+ * index-cache write; item 5: separate K and V pools].  Every query row of the
+ * batch is a new token at its own position pos = context_lens[q] + j; its
+ * vectors go to page block_table[q, pos/128], slot pos%128 (the q/k norm and
+ * RoPE need model weights and stay with the caller).
+ *   k_new, v_new [num_rows, num_kv_heads, head_dim] bf16
+ *   idx_new      [num_rows, index_heads, index_dim] bf16 (unused if skip_index)
+ *   k_cache, v_cache  pools [P, 128, num_kv_heads, head_dim] of kv_dtype
+ *   idx_k_cache  [P, 128, index_heads, index_dim] bf16
+ * FP8 pools store OCP e4m3 codes of x / s (IEEE fp32 division, round to
+ * nearest even, saturating to +-448): SCALAR takes s = k_scale[0] (v_scale[0])
+ * as input; PER_TOKEN_HEAD sets s = max_d |x_d| / 448 per token and KV head
+ * (1 for an all-zero vector) and writes it to k_scale / v_scale [P, 128,
+ * num_kv_heads] at the slot; NONE takes s = 1.  bf16 pools take a copy.
+ * Rows of requests that fail the device checks (MSA_DEV_BAD_PAGE, _BAD_LEN,
+ * _MALFORMED) are not written.  Supported: head_dim == 128. */
+msa_status msa_kv_insert(const msa_batch* batch, const void* k_new, const void* v_new,
+                         const void* idx_new, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t index_heads, int32_t index_dim, void* k_cache, void* v_cache,
+                         void* idx_k_cache, int32_t kv_dtype, int32_t scale_mode, float* k_scale,
+                         float* v_scale, int32_t skip_index, uint32_t* dev_status,
+                         cudaStream_t stream);
+
 /* Bytes of workspace msa_decode (bt_stride > 0) or msa_sparse_paged_attn
  * (bt_stride = 0, topk = 0) needs for these sizes. */
 size_t msa_workspace_size(int32_t num_rows, int32_t bt_stride, int32_t topk, int32_t num_heads,

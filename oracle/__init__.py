@@ -67,6 +67,11 @@ def _load():
             lib.orc_sparse_attn.restype = ctypes.c_uint32
             lib.orc_sparse_attn.argtypes = [i32, i32, i32, i32, P, P, P, i32, i32, i32, P, P, P,
                                             i32, P, P, ctypes.c_double, P, P, i32]
+            lib.orc_fp8_e4m3_encode.restype = ctypes.c_uint8
+            lib.orc_fp8_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.orc_kv_insert.restype = ctypes.c_uint32
+            lib.orc_kv_insert.argtypes = [P, i32, i32, P, P, i32, i32, P, P, P, P, i32, i32, P, P,
+                                          i32]
             lib.orc_dense_attn.restype = ctypes.c_uint32
             lib.orc_dense_attn.argtypes = [P, i32, i32, i32, P, P, P, i32, i32, P, P, P,
                                            ctypes.c_double, P, P, i32]
@@ -214,3 +219,28 @@ def dense(w, nthreads: Optional[int] = None):
     return dense_attn(b, w.q, w.k_cache, w.v_cache, w.kv_dtype, scale_mode=w.scale_mode,
                       k_scale=w.k_scale, v_scale=w.v_scale, sinks=w.sinks,
                       softmax_scale=w.softmax_scale, nthreads=nthreads)
+
+
+def fp8_e4m3_encode(x: float) -> int:
+    return int(_load().orc_fp8_e4m3_encode(float(x)))
+
+
+def kv_insert(w, k_new, v_new, idx_new, skip_index: bool = False):
+    """Insert the rows' new K/V/index-K into copies of the workload's pools;
+    returns (k_cache, v_cache, idx_k, k_scale, v_scale, status)."""
+    b = Batch.of(w)
+    kdt = np.uint8 if w.kv_dtype == 1 else np.uint16
+    k_cache = np.array(w.k_cache, dtype=kdt, copy=True)
+    v_cache = np.array(w.v_cache, dtype=kdt, copy=True)
+    idx_k = np.array(w.idx_k, dtype=np.uint16, copy=True)
+    k_scale = None if w.k_scale is None else np.array(w.k_scale, np.float32, copy=True)
+    v_scale = None if w.v_scale is None else np.array(w.v_scale, np.float32, copy=True)
+    k_new = _c(k_new, np.uint16)
+    v_new = _c(v_new, np.uint16)
+    idx_new = _c(idx_new, np.uint16)
+    st = _load().orc_kv_insert(ctypes.byref(b.s), int(w.hkv), int(w.head_dim), _ptr(k_new),
+                               _ptr(v_new), int(w.index_heads), int(w.index_dim), _ptr(idx_new),
+                               _ptr(k_cache), _ptr(v_cache), _ptr(idx_k), int(w.kv_dtype),
+                               int(w.scale_mode), _ptr(k_scale), _ptr(v_scale),
+                               int(bool(skip_index)))
+    return k_cache, v_cache, idx_k, k_scale, v_scale, int(st)

@@ -23,6 +23,9 @@
  *   - learnable per-head sink, natural-log LSE, fp32 [num_heads] sinks:
  *       vLLM PR 54404 page, "Features and motivation", "Key source
  *       snippets" (LSE op docstring, sink validation).
+ *   - KV insert with skip_index (the step before the path): vLLM PR 47287
+ *       page, "Implementation breakdown" item 1 (index-reuse layers skip the
+ *       index-cache write) and item 5 (separate K/V page layout).
  *   - where the pages are silent (block score = max over the block's valid
  *       tokens of the raw index dot product, ties to the lower block index,
  *       ascending table order, sink in the denominator, empty row -> O = 0):
@@ -487,6 +490,88 @@ uint32_t orc_dense_attn(const orc_batch* b, int32_t hq, int32_t hkv, int32_t hea
   c.out = out;
   c.lse = lse;
   for_each_row(b->num_rows, nthreads, dense_row, &c);
+  geometry_free(&g);
+  return st;
+}
+
+/* ------------------------------------------------------------ KV insert */
+
+uint8_t orc_fp8_e4m3_encode(float x) {
+  /* Brute force over the 127 finite magnitudes of the format: the nearest
+   * value wins; on a tie the even code (mantissa LSB 0) wins; anything at or
+   * beyond the largest finite magnitude saturates to it. */
+  if (isnan(x)) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  uint8_t best = 0;
+  double best_diff = INFINITY;
+  for (int code = 0; code <= 0x7E; ++code) {
+    const double d = fabs(a - orc_fp8_e4m3_value((uint8_t)code));
+    if (d < best_diff || (d == best_diff && (code & 1) == 0)) {
+      best = (uint8_t)code;
+      best_diff = d;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+static void quantize_row(const uint16_t* src, int32_t d, uint8_t* dst, float* scale_out,
+                         int32_t scale_mode, float given_scale) {
+  float s = 1.0f;
+  if (scale_mode == 2) {
+    float amax = 0.0f;
+    for (int32_t i = 0; i < d; ++i) {
+      const float v = fabsf((float)orc_bf16_value(src[i]));
+      if (v > amax) amax = v;
+    }
+    s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    *scale_out = s;
+  } else if (scale_mode == 1) {
+    s = given_scale;
+  }
+  for (int32_t i = 0; i < d; ++i) {
+    const float q = (float)orc_bf16_value(src[i]) / s; /* fp32 division */
+    dst[i] = orc_fp8_e4m3_encode(q);
+  }
+}
+
+uint32_t orc_kv_insert(const orc_batch* b, int32_t hkv, int32_t head_dim, const uint16_t* k_new,
+                       const uint16_t* v_new, int32_t index_heads, int32_t index_dim,
+                       const uint16_t* idx_new, void* k_cache, void* v_cache,
+                       uint16_t* idx_k_cache, int32_t kv_dtype, int32_t scale_mode,
+                       float* k_scale, float* v_scale, int32_t skip_index) {
+  geom_t g;
+  const uint32_t st = geometry_alloc(b, &g);
+  for (int32_t r = 0; r < b->num_rows; ++r) {
+    if (g.ok[r] != 1) continue;
+    const int32_t q = g.req[r];
+    const int32_t pos = g.pos[r];
+    const int32_t page = b->block_table[(int64_t)q * b->bt_stride + pos / BLOCK];
+    const int64_t token = (int64_t)page * BLOCK + pos % BLOCK; /* flat slot in [P*128] */
+    for (int32_t h = 0; h < hkv; ++h) {
+      const int64_t src = ((int64_t)r * hkv + h) * head_dim;
+      const int64_t dst = (token * hkv + h) * head_dim;
+      if (kv_dtype == 1) {
+        float ks = 1.0f, vs = 1.0f;
+        quantize_row(k_new + src, head_dim, (uint8_t*)k_cache + dst, &ks, scale_mode,
+                     scale_mode == 1 ? k_scale[0] : 1.0f);
+        quantize_row(v_new + src, head_dim, (uint8_t*)v_cache + dst, &vs, scale_mode,
+                     scale_mode == 1 ? v_scale[0] : 1.0f);
+        if (scale_mode == 2) {
+          k_scale[token * hkv + h] = ks;
+          v_scale[token * hkv + h] = vs;
+        }
+      } else {
+        memcpy((uint16_t*)k_cache + dst, k_new + src, sizeof(uint16_t) * (size_t)head_dim);
+        memcpy((uint16_t*)v_cache + dst, v_new + src, sizeof(uint16_t) * (size_t)head_dim);
+      }
+    }
+    if (!skip_index) {
+      const int64_t n = (int64_t)index_heads * index_dim;
+      memcpy(idx_k_cache + token * n, idx_new + (int64_t)r * n, sizeof(uint16_t) * (size_t)n);
+    }
+  }
   geometry_free(&g);
   return st;
 }

@@ -82,6 +82,24 @@ uint32_t orc_dense_attn(const orc_batch* b, int32_t hq, int32_t hkv, int32_t hea
                         const float* v_scale, const float* sinks, double softmax_scale,
                         double* out, double* lse, int32_t nthreads);
 
+/* OCP e4m3fn code of a float: round to nearest, ties to the even code,
+ * saturating to +-448 (infinities included); NaN gives 0x7F. */
+uint8_t orc_fp8_e4m3_encode(float x);
+
+/* The step before the path: write every row's new K, V (and index-K unless
+ * skip_index) into the paged pools at the row's own position (page
+ * block_table[q, pos/128], slot pos%128).  FP8 caches: SCALAR divides by the
+ * given k_scale[0] / v_scale[0]; PER_TOKEN_HEAD computes s = max_d |x_d| / 448
+ * per token and KV head (s = 1 when all zero), stores it in k_scale/v_scale
+ * at the slot and divides by it.  The division is fp32 and the code is
+ * orc_fp8_e4m3_encode of the quotient.  Rows of requests that do not pass
+ * the geometry checks are not written. */
+uint32_t orc_kv_insert(const orc_batch* b, int32_t hkv, int32_t head_dim, const uint16_t* k_new,
+                       const uint16_t* v_new, int32_t index_heads, int32_t index_dim,
+                       const uint16_t* idx_new, void* k_cache, void* v_cache,
+                       uint16_t* idx_k_cache, int32_t kv_dtype, int32_t scale_mode,
+                       float* k_scale, float* v_scale, int32_t skip_index);
+
 #ifdef __cplusplus
 }
 #endif

@@ -470,3 +470,84 @@ def test_threads_do_not_change_results(orc):
     r4 = orc.decode(w, nthreads=4)
     for key in ("scores", "topk_idx", "tbl", "sparse_len", "out", "lse"):
         np.testing.assert_array_equal(r1[key], r4[key])
+
+
+# ------------------------------------------------------------- KV insert
+
+def test_fp8_encode_matches_torch_in_range(orc):
+    # torch's float -> float8_e4m3fn cast is round-to-nearest-even; inside the
+    # finite range the two must agree code for code
+    rng = np.random.default_rng(4)
+    xs = np.concatenate([rng.standard_normal(3000) * s for s in (0.01, 1.0, 30.0, 150.0)])
+    xs = np.clip(xs, -448, 448).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.fp8_e4m3_encode(x) for x in xs], np.uint8)
+    assert np.array_equal(ref, got)
+
+
+def test_fp8_encode_roundtrip_ties_and_saturation(orc):
+    for code in range(256):
+        if code & 0x7F == 0x7F:
+            continue
+        v = orc.fp8_e4m3_value(code)
+        assert orc.fp8_e4m3_encode(np.float32(v)) == code  # every value encodes to itself
+    # halfway cases go to the even code
+    assert orc.fp8_e4m3_encode(1.0625) == 0x38      # between 1.0 (0x38) and 1.125 (0x39)
+    assert orc.fp8_e4m3_encode(1.1875) == 0x3A      # between 1.125 (0x39) and 1.25 (0x3a)
+    assert orc.fp8_e4m3_encode(2.0 ** -10) == 0x00  # between 0 and the smallest subnormal
+    assert orc.fp8_e4m3_encode(1.5 * 2.0 ** -9) == 0x02
+    # beyond the largest finite value: saturate, keeping the sign
+    for x in (449.0, 480.0, 1e30, float("inf")):
+        assert orc.fp8_e4m3_encode(x) == 0x7E and orc.fp8_e4m3_encode(-x) == 0xFE
+    assert orc.fp8_e4m3_encode(float("nan")) == 0x7F
+
+
+def _new_rows(w, seed):
+    rng = np.random.default_rng(seed)
+    k_new = W.bf16_bits(rng.standard_normal((w.num_rows, w.hkv, w.head_dim)) * 3)
+    v_new = W.bf16_bits(rng.standard_normal((w.num_rows, w.hkv, w.head_dim)) * 3)
+    idx_new = W.bf16_bits(rng.integers(-3, 4, (w.num_rows, w.index_heads, w.index_dim)))
+    return k_new, v_new, idx_new
+
+
+def test_kv_insert_writes_each_row_at_its_slot(orc):
+    w = W.custom(90, q_lens=[1, 3, 2], seq_lens=[300, 129, 1000], hq=4, di=64, topk=2)
+    k_new, v_new, idx_new = _new_rows(w, 1)
+    k, v, ik, _, _, st = orc.kv_insert(w, k_new, v_new, idx_new)
+    assert st == 0
+    r = 0
+    for q in range(w.num_reqs):
+        for j in range(int(w.q_lens[q])):
+            pos = int(w.context_lens[q]) + j
+            page = w.block_table[q, pos // 128]
+            assert np.array_equal(k[page, pos % 128], k_new[r])
+            assert np.array_equal(v[page, pos % 128], v_new[r])
+            assert np.array_equal(ik[page, pos % 128], idx_new[r])
+            r += 1
+    # nothing else changed
+    changed = (k != w.k_cache).any(axis=(2, 3))
+    assert changed.sum() <= w.num_rows
+    _, _, ik2, _, _, _ = orc.kv_insert(w, k_new, v_new, idx_new, skip_index=True)
+    assert np.array_equal(ik2, w.idx_k)  # index-reuse layers leave the index cache alone
+
+
+def test_kv_insert_fp8_per_token_scale_definition(orc):
+    w = W.custom(91, q_lens=[2, 1], seq_lens=[500, 77], hq=4, di=64, topk=2,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_PER_TOKEN_HEAD)
+    k_new, v_new, idx_new = _new_rows(w, 2)
+    k, v, _, ks, vs, st = orc.kv_insert(w, k_new, v_new, idx_new)
+    assert st == 0
+    to_f = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).float().numpy()
+    r = 0
+    for q in range(w.num_reqs):
+        for j in range(int(w.q_lens[q])):
+            pos = int(w.context_lens[q]) + j
+            page, slot = w.block_table[q, pos // 128], pos % 128
+            x = to_f(k_new[r, 0])
+            s = np.float32(np.abs(x).max()) / np.float32(448)
+            assert ks[page, slot, 0] == s
+            codes = k[page, slot, 0]
+            vals = np.array([orc.fp8_e4m3_value(c) for c in codes])
+            assert np.abs(vals).max() == 448.0  # the largest element lands on the top code
+            np.testing.assert_allclose(vals * s, x, rtol=2 ** -4, atol=s * 2 ** -9)
+            r += 1
