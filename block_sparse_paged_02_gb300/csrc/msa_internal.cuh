@@ -83,19 +83,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// One test of the phase; the thread may sleep in hardware for up to
-// kWaitSuspendNs while the phase is incomplete (instead of spinning and
-// taking issue slots from the warps that compute).
-constexpr uint32_t kWaitSuspendNs = 100000;
-
+// One test of the phase (the hardware may briefly suspend the thread while
+// the phase is incomplete).  A longer suspend-time hint was measured: no gain
+// for the streaming kernels and a slower single-thread MMA issuer.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitSuspendNs)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
