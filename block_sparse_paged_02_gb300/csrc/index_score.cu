@@ -32,12 +32,14 @@ namespace {
 
 constexpr int kRowGroup = 4;
 
-template <int DI, int HI>
+template <int DI, int HI, bool OVERLAP>
 struct ScoreCfg {
   static constexpr int kSubRowBytes = DI * 2;
   static constexpr int kChunks = DI / 8;  // 16-byte chunks per sub-row
   static constexpr int kPageBytes = kBlock * HI * DI * 2;
-  static constexpr int kStages = kPageBytes >= 32768 ? 6 : 12;  // 192 KB of stages
+  // 192 KB of stages alone; a smaller ring when sharing the SM (overlapped decode)
+  static constexpr int kStages32 = OVERLAP ? MSA_SCORE_STAGES_OVERLAP : 6;
+  static constexpr int kStages = kPageBytes >= 32768 ? kStages32 : 2 * kStages32;
   // warps per stage; each takes an equal share of the page's sub-rows (one
   // warp per page measured fastest: a pair split adds work without raising
   // the bytes in flight enough to matter)
@@ -52,9 +54,9 @@ struct StageInfo {  // written by the producer before it arms the stage
   int req, blk, valid, q0, qlen, ctx, pad0, pad1;
 };
 
-template <int DI, int HI>
+template <int DI, int HI, bool OVERLAP>
 struct ScoreSmem {
-  using C = ScoreCfg<DI, HI>;
+  using C = ScoreCfg<DI, HI, OVERLAP>;
   static constexpr size_t kPages = 0;
   static constexpr size_t kQ = kPages + (size_t)C::kStages * C::kPageBytes;
   static constexpr size_t kPair = kQ + (size_t)C::kConsumers * C::kQBytes;
@@ -71,7 +73,7 @@ template <int DI, int HI, int NR>
 __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q_s, int lane,
                                            int sub0, int blk, const int (&pos)[kRowGroup],
                                            float (&out)[kRowGroup]) {
-  using C = ScoreCfg<DI, HI>;
+  using C = ScoreCfg<DI, HI, false>;  // the ring size plays no part here
   float acc[C::kSubPerLane][NR];
 #pragma unroll
   for (int j = 0; j < C::kSubPerLane; ++j)
@@ -129,11 +131,11 @@ __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q
   }
 }
 
-template <int DI, int HI>
-__global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
+template <int DI, int HI, bool OVERLAP>
+__global__ void __launch_bounds__(ScoreCfg<DI, HI, OVERLAP>::kThreads, 1)
     index_score_kernel(const ScoreLaunch p) {
-  using C = ScoreCfg<DI, HI>;
-  using S = ScoreSmem<DI, HI>;
+  using C = ScoreCfg<DI, HI, OVERLAP>;
+  using S = ScoreSmem<DI, HI, OVERLAP>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
   uint64_t* empty = full + C::kStages;
@@ -171,6 +173,7 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
       atomicOr(reinterpret_cast<unsigned*>(&misc[0]), bad);
       nb = 0;
     }
+    if (ql <= 0) nb = 0;  // no query row needs these blocks
     if (p.tc_min_rows > 0 && ql >= p.tc_min_rows) nb = 0;  // scored on the tensor cores
     prefix[q + 1] = nb;
   }
@@ -280,6 +283,18 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
   float* pmax = pairmax + st * kRowGroup;
   int cur_req = -1, cur_g0 = -1, pair_uses = 0;
   bool failed = false;
+  // Finished items are counted per request and published when the warp moves
+  // to another request (or leaves): by then the score stores are long issued,
+  // so the fence before the release costs little.
+  int pend_req = -1, pend_cnt = 0;
+  auto publish = [&]() {
+    if (pend_cnt > 0) {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(p.done + pend_req, pend_cnt);
+    }
+    pend_cnt = 0;
+  };
   for (int j = st, use = 0; j < n_items && !failed; j += C::kStages, ++use) {
     // warp-uniform: the page is scored with warp shuffles
     if (!__all_sync(0xffffffffu, mbar_wait(&full[st], use & 1))) {
@@ -288,6 +303,10 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
     }
     const StageInfo si = info[st];
     const int q0 = si.q0, qlen = si.qlen, ctx = si.ctx;
+    if (p.done && si.req != pend_req) {
+      publish();
+      pend_req = si.req;
+    }
     // rows j with ctx + j >= 128*blk can see this block
     const int jstart = max(0, si.blk * kBlock - ctx);
     for (int g0 = jstart; g0 < qlen; g0 += kRowGroup) {
@@ -344,16 +363,18 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
             p.scores[(long long)(q0 + g0 + r) * p.score_stride + si.blk] = best[r];
       }
     }
+    ++pend_cnt;
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
   }
+  if (p.done) publish();
 }
 
-template <int DI, int HI>
+template <int DI, int HI, bool OVERLAP>
 cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
-  using C = ScoreCfg<DI, HI>;
-  const size_t smem = ScoreSmem<DI, HI>::bytes(p.batch.num_reqs);
-  auto kern = index_score_kernel<DI, HI>;
+  using C = ScoreCfg<DI, HI, OVERLAP>;
+  const size_t smem = ScoreSmem<DI, HI, OVERLAP>::bytes(p.batch.num_reqs);
+  auto kern = index_score_kernel<DI, HI, OVERLAP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
@@ -361,13 +382,18 @@ cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <bool OVERLAP>
+cudaError_t launch_dims(const ScoreLaunch& p, cudaStream_t stream) {
+  if (p.index_heads == 1 && p.index_dim == 128) return launch_cfg<128, 1, OVERLAP>(p, stream);
+  if (p.index_heads == 1 && p.index_dim == 64) return launch_cfg<64, 1, OVERLAP>(p, stream);
+  if (p.index_heads == 2 && p.index_dim == 64) return launch_cfg<64, 2, OVERLAP>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream) {
-  if (p.index_heads == 1 && p.index_dim == 128) return launch_cfg<128, 1>(p, stream);
-  if (p.index_heads == 1 && p.index_dim == 64) return launch_cfg<64, 1>(p, stream);
-  if (p.index_heads == 2 && p.index_dim == 64) return launch_cfg<64, 2>(p, stream);
-  return cudaErrorInvalidValue;
+  return p.done ? launch_dims<true>(p, stream) : launch_dims<false>(p, stream);
 }
 
 }  // namespace msa
