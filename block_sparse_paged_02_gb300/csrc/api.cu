@@ -34,10 +34,9 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // grid (splits x rows) is sized to fill the GPU once: as many splits per row
 // as fit in ctas_per_sm resident CTAs on every SM, each split a multiple of 4
 // entries (one per warp) and at most kMaxSplitEntries.  Workspaces are sized
-// with the largest residency of any variant, launches use their own.
-constexpr int cmax(int a, int b) { return a > b ? a : b; }
+// with the largest residency of any variant (3), launches use their own.
 constexpr int kMaxAttnCtasPerSm =
-    cmax(cmax(MSA_ATTN_CTAS_FP8, MSA_ATTN_CTAS_BF16), MSA_ATTN_CTAS_OVERLAP);
+    MSA_ATTN_CTAS_FP8 > MSA_ATTN_CTAS_BF16 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_CTAS_BF16;
 
 void attn_split(int num_rows, int max_entries, int ctas_per_sm, int* pps, int* splits) {
   const int capacity = device_sm_count() * ctas_per_sm;
@@ -54,23 +53,14 @@ int attn_ctas_per_sm(const msa_attn_args* a) {
   return a->kv_dtype == MSA_KV_FP8_E4M3 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_CTAS_BF16;
 }
 
-// Decode workspace.  The first region (queue tail, attention item queue,
-// per-request finished-block counts) is the overlapped decode's hand-off
-// state; msa_decode zero-fills it on the stream before the score kernel.
 struct DecodeWs {
-  size_t queue_tail, queue, done, counters, scores, topk, tbl, len, partials, total;
+  size_t counters, scores, topk, tbl, len, partials, total;
 };
 
 DecodeWs decode_layout(int num_rows, int bt_stride, int topk, int splits) {
   DecodeWs w;
   const size_t n = (size_t)(num_rows > 0 ? num_rows : 1);
   size_t off = 0;
-  w.queue_tail = off;
-  off += 256;
-  w.queue = off;
-  off = round_up(off + n * (size_t)splits * 4, 256);
-  w.done = off;
-  off = round_up(off + (size_t)kMaxReqs * 4, 256);
   w.counters = off;
   off = round_up(off + n * 4, 256);
   w.scores = off;
@@ -146,7 +136,6 @@ AttnLaunch make_attn(const msa_attn_args* a, const int32_t* tbl, int tbl_stride,
   L.splits = splits;
   L.pages_per_split = pps;
   L.status = status;
-  L.queue = nullptr;
   return L;
 }
 
@@ -285,15 +274,8 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
                                          attn->num_heads, attn->head_dim, 8 * topk);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return MSA_ERR_WORKSPACE;
 
-  // Overlapped decode unless the tensor-core scorer runs: the top-k kernel
-  // starts on each row as soon as the score kernel has finished the row's
-  // request, and the attention kernel on each row as soon as its table is
-  // out, while the score kernel still streams the other requests.
-  const bool overlap =
-      !(batch->max_q_len >= kTcMinRows && tc_score_supported(index_heads, index_dim));
   int pps, splits, ws_pps, ws_splits;
-  attn_split(batch->num_rows, 8 * topk, overlap ? MSA_ATTN_CTAS_OVERLAP : attn_ctas_per_sm(attn),
-             &pps, &splits);
+  attn_split(batch->num_rows, 8 * topk, attn_ctas_per_sm(attn), &pps, &splits);
   attn_split(batch->num_rows, 8 * topk, kMaxAttnCtasPerSm, &ws_pps, &ws_splits);
   const DecodeWs L = decode_layout(batch->num_rows, batch->bt_stride, topk, ws_splits);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -304,37 +286,21 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
   const int tstride = sparse_tbl ? tbl_stride : 8 * topk;
   int32_t* len = sparse_len ? sparse_len : reinterpret_cast<int32_t*>(ws + L.len);
 
-  int* queue_tail = reinterpret_cast<int*>(ws + L.queue_tail);
-  int* queue = reinterpret_cast<int*>(ws + L.queue);
-  int* done = reinterpret_cast<int*>(ws + L.done);
-  cudaError_t e = cudaSuccess;
-  if (overlap) {
-    e = cudaMemsetAsync(ws, 0, L.done + (size_t)batch->num_reqs * 4, stream);
-    if (e != cudaSuccess) return MSA_ERR_CUDA;
-  }
-
   ScoreLaunch sp{*batch, static_cast<const uint16_t*>(idx_q),
                  static_cast<const uint8_t*>(idx_k_cache), index_heads, index_dim, scores,
-                 batch->bt_stride, dev_status, 0, overlap ? done : nullptr};
-  e = launch_scores(sp, stream);
+                 batch->bt_stride, dev_status, 0};
+  cudaError_t e = launch_scores(sp, stream);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_score) cudaEventRecord(trace->after_score, stream);
 
   TopkLaunch tp{*batch, scores, batch->bt_stride, topk, k_idx, tbl, tstride, len, counters,
                 dev_status};
-  if (overlap) {
-    tp.done = done;
-    tp.queue = queue;
-    tp.queue_tail = queue_tail;
-    tp.splits = splits;
-  }
   e = launch_topk_table(tp, stream, true);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_topk) cudaEventRecord(trace->after_topk, stream);
 
   AttnLaunch ap = make_attn(attn, tbl, tstride, len, reinterpret_cast<float*>(ws + L.partials),
                             counters, pps, splits, dev_status);
-  if (overlap) ap.queue = queue;
   // the attention split depends only on the selected width (8*topk entries)
   e = launch_sparse_attn(ap, stream, true);
   if (e != cudaSuccess) return MSA_ERR_CUDA;

@@ -12,10 +12,12 @@
 // persistent, bandwidth-first streamer:
 //   * work = the flattened list of (request, block) items over all requests;
 //     each CTA takes an equal contiguous slice (balanced by actual block
-//     count, the lesson of the PR 54682 balanced scorer);
+//     count, the lesson of the PR 54682 balanced scorer; consecutive items
+//     share block-table lines, so the producer's lookups stay cache hits);
 //   * one producer thread issues one 1-D bulk async copy (TMA bulk engine)
 //     per 128-token index-K page (16 or 32 KB, contiguous in the page-128
-//     layout) into a ring of shared-memory stages guarded by mbarriers;
+//     layout), plus one for the query rows that see it, into a ring of
+//     shared-memory stages guarded by mbarriers;
 //   * each consumer warp owns one stage and scores the whole page
 //     (warp-per-block): every lane holds 4*Hi token sub-rows, walks their
 //     16-byte chunks in a lane-rotated order (bank-conflict free), and keeps
@@ -32,36 +34,30 @@ namespace {
 
 constexpr int kRowGroup = 4;
 
-template <int DI, int HI, bool OVERLAP>
+template <int DI, int HI>
 struct ScoreCfg {
   static constexpr int kSubRowBytes = DI * 2;
   static constexpr int kChunks = DI / 8;  // 16-byte chunks per sub-row
   static constexpr int kPageBytes = kBlock * HI * DI * 2;
-  // 192 KB of stages alone; a smaller ring when sharing the SM (overlapped decode)
-  static constexpr int kStages32 = OVERLAP ? MSA_SCORE_STAGES_OVERLAP : 6;
-  static constexpr int kStages = kPageBytes >= 32768 ? kStages32 : 2 * kStages32;
-  // warps per stage; each takes an equal share of the page's sub-rows (one
-  // warp per page measured fastest: a pair split adds work without raising
-  // the bytes in flight enough to matter)
-  static constexpr int kParts = 1;
-  static constexpr int kConsumers = kStages * kParts;
-  static constexpr int kSubPerLane = kBlock * HI / 32 / kParts;
-  static constexpr int kThreads = 32 * (1 + kConsumers);
-  static constexpr int kQBytes = kRowGroup * HI * DI * 2;  // per consumer warp
+  static constexpr int kStages = kPageBytes >= 32768 ? 6 : 12;  // 192 KB of stages
+  // one consumer warp per stage (a pair of warps per page measured slower:
+  // more instructions without more bytes in flight)
+  static constexpr int kSubPerLane = kBlock * HI / 32;
+  static constexpr int kThreads = 32 * (1 + kStages);
+  static constexpr int kQBytes = kRowGroup * HI * DI * 2;  // query rows staged with a page
 };
 
 struct StageInfo {  // written by the producer before it arms the stage
-  int req, blk, valid, q0, qlen, ctx, pad0, pad1;
+  int req, blk, valid, q0, qlen, ctx, jstart, pad;
 };
 
-template <int DI, int HI, bool OVERLAP>
+template <int DI, int HI>
 struct ScoreSmem {
-  using C = ScoreCfg<DI, HI, OVERLAP>;
+  using C = ScoreCfg<DI, HI>;
   static constexpr size_t kPages = 0;
   static constexpr size_t kQ = kPages + (size_t)C::kStages * C::kPageBytes;
-  static constexpr size_t kPair = kQ + (size_t)C::kConsumers * C::kQBytes;
-  static constexpr size_t kBars = kPair + (size_t)C::kStages * kRowGroup * sizeof(float);
-  static constexpr size_t kInfo = kBars + 3 * C::kStages * sizeof(uint64_t);
+  static constexpr size_t kBars = kQ + (size_t)C::kStages * C::kQBytes;
+  static constexpr size_t kInfo = kBars + 2 * C::kStages * sizeof(uint64_t);
   static constexpr size_t kMisc = kInfo + C::kStages * sizeof(StageInfo);
   static constexpr size_t kPrefix = kMisc + 64;
   static size_t bytes(int num_reqs) { return kPrefix + (size_t)(num_reqs + 1) * sizeof(int); }
@@ -71,9 +67,9 @@ struct ScoreSmem {
 // Returns, in lane 0..NR-1 order via out[], the per-row block maxima.
 template <int DI, int HI, int NR>
 __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q_s, int lane,
-                                           int sub0, int blk, const int (&pos)[kRowGroup],
+                                           int blk, const int (&pos)[kRowGroup],
                                            float (&out)[kRowGroup]) {
-  using C = ScoreCfg<DI, HI, false>;  // the ring size plays no part here
+  using C = ScoreCfg<DI, HI>;
   float acc[C::kSubPerLane][NR];
 #pragma unroll
   for (int j = 0; j < C::kSubPerLane; ++j)
@@ -98,7 +94,7 @@ __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q
     }
 #pragma unroll
     for (int j = 0; j < C::kSubPerLane; ++j) {
-      const int sr = sub0 + lane + 32 * j;
+      const int sr = lane + 32 * j;
       const uint4 w = lds128(page + sr * C::kSubRowBytes + c * 16);
       const float k0 = bf16lo(w.x), k1 = bf16hi(w.x), k2 = bf16lo(w.y), k3 = bf16hi(w.y);
       const float k4 = bf16lo(w.z), k5 = bf16hi(w.z), k6 = bf16lo(w.w), k7 = bf16hi(w.w);
@@ -122,7 +118,7 @@ __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < C::kSubPerLane; ++j) {
-      const int token = (sub0 + lane + 32 * j) / HI;
+      const int token = (lane + 32 * j) / HI;
       if (blk * kBlock + token <= pos[r]) m = fmaxf(m, acc[j][r]);  // NaN never wins
     }
 #pragma unroll
@@ -131,16 +127,14 @@ __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q
   }
 }
 
-template <int DI, int HI, bool OVERLAP>
-__global__ void __launch_bounds__(ScoreCfg<DI, HI, OVERLAP>::kThreads, 1)
+template <int DI, int HI>
+__global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
     index_score_kernel(const ScoreLaunch p) {
-  using C = ScoreCfg<DI, HI, OVERLAP>;
-  using S = ScoreSmem<DI, HI, OVERLAP>;
+  using C = ScoreCfg<DI, HI>;
+  using S = ScoreSmem<DI, HI>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
   uint64_t* empty = full + C::kStages;
-  uint64_t* pairbar = empty + C::kStages;  // part 1 -> part 0 of a page, per row group
-  float* pairmax = reinterpret_cast<float*>(smem + S::kPair);
   StageInfo* info = reinterpret_cast<StageInfo*>(smem + S::kInfo);
   int* misc = reinterpret_cast<int*>(smem + S::kMisc);
   int* prefix = reinterpret_cast<int*>(smem + S::kPrefix);
@@ -160,8 +154,7 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, OVERLAP>::kThreads, 1)
   }
   if (tid < C::kStages) {
     mbar_init(&full[tid], 1);
-    mbar_init(&empty[tid], C::kParts);
-    mbar_init(&pairbar[tid], 1);
+    mbar_init(&empty[tid], 1);
   }
   fence_barrier_init();
   __syncthreads();
@@ -223,15 +216,22 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, OVERLAP>::kThreads, 1)
       si->q0 = b.cu_seqlens_q[lo];
       si->qlen = b.cu_seqlens_q[lo + 1] - si->q0;
       si->ctx = b.context_lens[lo];
-      si->pad0 = si->pad1 = 0;
+      si->jstart = max(0, si->blk * kBlock - si->ctx);  // first row that sees the block
+      si->pad = 0;
       *page = b.block_table[(long long)lo * b.bt_stride + si->blk];
       si->valid = *page >= 0 && *page < b.num_pages;
     };
+    // One stage = the index-K page plus the query rows of the first row
+    // group that sees it (up to 4 rows, contiguous), so that consumers need
+    // no global load in the common (decode) case.
     auto issue = [&](int j, const StageInfo& si, int page) {  // elected lane only
       const int s = j % C::kStages;
       info[s] = si;
       if (si.valid) {
-        mbar_arrive_expect_tx(&full[s], C::kPageBytes);
+        const uint32_t qb = (uint32_t)min(kRowGroup, si.qlen - si.jstart) * HI * DI * 2;
+        mbar_arrive_expect_tx(&full[s], C::kPageBytes + qb);
+        bulk_g2s(smem + S::kQ + (size_t)s * C::kQBytes,
+                 p.idx_q + (long long)(si.q0 + si.jstart) * HI * DI, qb, &full[s]);
         bulk_g2s(smem + S::kPages + (size_t)s * C::kPageBytes,
                  p.idx_k + (long long)page * C::kPageBytes, C::kPageBytes, &full[s]);
       } else {
@@ -251,7 +251,8 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, OVERLAP>::kThreads, 1)
       si.q0 = __shfl_sync(0xffffffffu, mine.q0, j);
       si.qlen = __shfl_sync(0xffffffffu, mine.qlen, j);
       si.ctx = __shfl_sync(0xffffffffu, mine.ctx, j);
-      si.pad0 = si.pad1 = 0;
+      si.jstart = __shfl_sync(0xffffffffu, mine.jstart, j);
+      si.pad = 0;
       const int pg = __shfl_sync(0xffffffffu, my_page, j);
       if (lane == 0) issue(j, si, pg);
     }
@@ -274,28 +275,11 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, OVERLAP>::kThreads, 1)
     return;
   }
 
-  // ---- consumers: warps (kParts*s .. kParts*s + kParts-1) share stage s
-  const int w = warp - 1;
-  const int st = w / C::kParts, part = w % C::kParts;
-  const int sub0 = part * (kBlock * HI / C::kParts);
+  // ---- consumers: warp s+1 owns stage s
+  const int st = warp - 1;
   const uint8_t* page = smem + S::kPages + (size_t)st * C::kPageBytes;
-  uint8_t* q_s = smem + S::kQ + (size_t)w * C::kQBytes;
-  float* pmax = pairmax + st * kRowGroup;
-  int cur_req = -1, cur_g0 = -1, pair_uses = 0;
-  bool failed = false;
-  // Finished items are counted per request and published when the warp moves
-  // to another request (or leaves): by then the score stores are long issued,
-  // so the fence before the release costs little.
-  int pend_req = -1, pend_cnt = 0;
-  auto publish = [&]() {
-    if (pend_cnt > 0) {
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) atomicAdd(p.done + pend_req, pend_cnt);
-    }
-    pend_cnt = 0;
-  };
-  for (int j = st, use = 0; j < n_items && !failed; j += C::kStages, ++use) {
+  uint8_t* q_s = smem + S::kQ + (size_t)st * C::kQBytes;
+  for (int j = st, use = 0; j < n_items; j += C::kStages, ++use) {
     // warp-uniform: the page is scored with warp shuffles
     if (!__all_sync(0xffffffffu, mbar_wait(&full[st], use & 1))) {
       if (lane == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
@@ -303,20 +287,16 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, OVERLAP>::kThreads, 1)
     }
     const StageInfo si = info[st];
     const int q0 = si.q0, qlen = si.qlen, ctx = si.ctx;
-    if (p.done && si.req != pend_req) {
-      publish();
-      pend_req = si.req;
-    }
-    // rows j with ctx + j >= 128*blk can see this block
-    const int jstart = max(0, si.blk * kBlock - ctx);
-    for (int g0 = jstart; g0 < qlen; g0 += kRowGroup) {
+    bool wrote_q = false;
+    // rows j >= jstart (ctx + j >= 128*blk) can see this block
+    for (int g0 = si.jstart; g0 < qlen; g0 += kRowGroup) {
       const int nr = min(kRowGroup, qlen - g0);
       int pos[kRowGroup];
 #pragma unroll
       for (int r = 0; r < kRowGroup; ++r) pos[r] = ctx + g0 + min(r, nr - 1);
       float best[kRowGroup];
       if (si.valid) {
-        if (si.req != cur_req || g0 != cur_g0) {  // stage the query rows of this group
+        if (g0 != si.jstart) {  // later row groups (requests with > 4 rows): from global
           __syncwarp();
           const int chunks = nr * HI * DI / 8;
           const uint4* src = reinterpret_cast<const uint4*>(
@@ -324,57 +304,35 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, OVERLAP>::kThreads, 1)
           for (int c = lane; c < chunks; c += 32)
             *reinterpret_cast<uint4*>(q_s + c * 16) = src[c];
           __syncwarp();
-          cur_req = si.req;
-          cur_g0 = g0;
+          wrote_q = true;
         }
         if (nr == 1)
-          score_page<DI, HI, 1>(page, q_s, lane, sub0, si.blk, pos, best);
+          score_page<DI, HI, 1>(page, q_s, lane, si.blk, pos, best);
         else if (nr == 2)
-          score_page<DI, HI, 2>(page, q_s, lane, sub0, si.blk, pos, best);
+          score_page<DI, HI, 2>(page, q_s, lane, si.blk, pos, best);
         else
-          score_page<DI, HI, 4>(page, q_s, lane, sub0, si.blk, pos, best);  // rows >= nr unused
+          score_page<DI, HI, 4>(page, q_s, lane, si.blk, pos, best);  // rows >= nr unused
       } else {
 #pragma unroll
         for (int r = 0; r < kRowGroup; ++r) best[r] = -INFINITY;
       }
-      if constexpr (C::kParts == 2) {
-        // part 1 hands its half-page maxima to part 0, which writes the scores
-        if (part == 1) {
 #pragma unroll
-          for (int r = 0; r < kRowGroup; ++r)
-            if (lane == r) pmax[r] = best[r];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&pairbar[st]);
-        } else {
-          if (!__all_sync(0xffffffffu, mbar_wait(&pairbar[st], pair_uses & 1))) {
-            if (lane == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
-            failed = true;
-            break;
-          }
-#pragma unroll
-          for (int r = 0; r < kRowGroup; ++r) best[r] = fmaxf(best[r], pmax[r]);
-        }
-        ++pair_uses;
-      }
-      if (part == 0) {
-#pragma unroll
-        for (int r = 0; r < kRowGroup; ++r)
-          if (lane == r && r < nr)
-            p.scores[(long long)(q0 + g0 + r) * p.score_stride + si.blk] = best[r];
-      }
+      for (int r = 0; r < kRowGroup; ++r)
+        if (lane == r && r < nr)
+          p.scores[(long long)(q0 + g0 + r) * p.score_stride + si.blk] = best[r];
     }
-    ++pend_cnt;
+    // the next bulk copy into q_s must follow this warp's own writes to it
+    if (wrote_q) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
   }
-  if (p.done) publish();
 }
 
-template <int DI, int HI, bool OVERLAP>
+template <int DI, int HI>
 cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
-  using C = ScoreCfg<DI, HI, OVERLAP>;
-  const size_t smem = ScoreSmem<DI, HI, OVERLAP>::bytes(p.batch.num_reqs);
-  auto kern = index_score_kernel<DI, HI, OVERLAP>;
+  using C = ScoreCfg<DI, HI>;
+  const size_t smem = ScoreSmem<DI, HI>::bytes(p.batch.num_reqs);
+  auto kern = index_score_kernel<DI, HI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
@@ -382,18 +340,13 @@ cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <bool OVERLAP>
-cudaError_t launch_dims(const ScoreLaunch& p, cudaStream_t stream) {
-  if (p.index_heads == 1 && p.index_dim == 128) return launch_cfg<128, 1, OVERLAP>(p, stream);
-  if (p.index_heads == 1 && p.index_dim == 64) return launch_cfg<64, 1, OVERLAP>(p, stream);
-  if (p.index_heads == 2 && p.index_dim == 64) return launch_cfg<64, 2, OVERLAP>(p, stream);
-  return cudaErrorInvalidValue;
-}
-
 }  // namespace
 
 cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream) {
-  return p.done ? launch_dims<true>(p, stream) : launch_dims<false>(p, stream);
+  if (p.index_heads == 1 && p.index_dim == 128) return launch_cfg<128, 1>(p, stream);
+  if (p.index_heads == 1 && p.index_dim == 64) return launch_cfg<64, 1>(p, stream);
+  if (p.index_heads == 2 && p.index_dim == 64) return launch_cfg<64, 2>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace msa

@@ -41,23 +41,6 @@ constexpr int kMaxSplitEntries = 128;
 #ifndef MSA_ATTN_CTAS_BF16
 #define MSA_ATTN_CTAS_BF16 2
 #endif
-// Overlapped decode (top-k and attention run while the score kernel still
-// streams): the score ring shrinks so that one attention CTA fits beside it on
-// every SM (5 stages of 32 KB pages, twice as many 16 KB ones), the attention
-// copy rings shrink to match, and the attention work is split for CTAS
-// resident CTAs per SM.
-#ifndef MSA_SCORE_STAGES_OVERLAP
-#define MSA_SCORE_STAGES_OVERLAP 5
-#endif
-#ifndef MSA_ATTN_STAGES_OVERLAP_FP8
-#define MSA_ATTN_STAGES_OVERLAP_FP8 2
-#endif
-#ifndef MSA_ATTN_STAGES_OVERLAP_BF16
-#define MSA_ATTN_STAGES_OVERLAP_BF16 1
-#endif
-#ifndef MSA_ATTN_CTAS_OVERLAP
-#define MSA_ATTN_CTAS_OVERLAP 2
-#endif
 // bounded waits: a wait that has not completed after this long gives up
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
 
@@ -124,28 +107,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitNs) return false;
-  }
-}
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release(int* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// One thread waits until *p >= target (a counter or flag another CTA of a
-// running kernel raises with release semantics); false after kWaitNs.
-__device__ __forceinline__ bool wait_at_least(const int* p, int target) {
-  if (ld_acquire(p) >= target) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  while (true) {
-    __nanosleep(64);
-    if (ld_acquire(p) >= target) return true;
     if (globaltimer_ns() - t0 > kWaitNs) return false;
   }
 }
@@ -256,9 +217,6 @@ struct ScoreLaunch {
   int score_stride;
   uint32_t* status;
   int tc_min_rows;  // > 0: requests with q_len >= this are left to the tensor-core kernel
-  // overlapped decode: per-request count of finished (request, block) items,
-  // raised with release semantics (null: not counted)
-  int* done;
 };
 
 struct TopkLaunch {
@@ -272,13 +230,6 @@ struct TopkLaunch {
   int32_t* sparse_len;
   uint32_t* attn_counters;  // zeroed per row when non-null (fused path)
   uint32_t* status;
-  // overlapped decode: wait for done[q] to reach the request's block count
-  // instead of for the previous kernel, then append the row's `splits`
-  // attention items (r * splits + s + 1) to queue (null: not overlapped)
-  const int* done;
-  int* queue;
-  int* queue_tail;
-  int splits;
 };
 
 struct AttnLaunch {
@@ -303,9 +254,6 @@ struct AttnLaunch {
   int splits;
   int pages_per_split;  // page-16 entries per split
   uint32_t* status;
-  // overlapped decode: CTA i takes item queue[i] - 1 = row * splits + split
-  // once the top-k kernel has published it (null: grid = splits x rows)
-  const int* queue;
 };
 
 cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream);

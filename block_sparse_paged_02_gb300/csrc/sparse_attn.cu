@@ -35,14 +35,12 @@ constexpr float kRescaleSlack = 8.f;  // log2 units: unnormalised weights stay <
 constexpr int kAccStride = 132;  // padded head stride of the shared-memory merge area
 constexpr int kAccWarpFloats = kMaxHeads * kAccStride;  // 2112
 
-template <bool FP8, bool QUEUE>
+template <bool FP8>
 struct AttnCfg {
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kSlab = kPage16 * kHeadDim * kElem;  // one page-16 K (or V) slab
   static constexpr int kStageBytes = 2 * kSlab + 2 * 64;    // K, V, k-scales, v-scales
-  static constexpr int kStages =
-      QUEUE ? (FP8 ? MSA_ATTN_STAGES_OVERLAP_FP8 : MSA_ATTN_STAGES_OVERLAP_BF16)
-            : (FP8 ? MSA_ATTN_STAGES_FP8 : MSA_ATTN_STAGES_BF16);
+  static constexpr int kStages = FP8 ? MSA_ATTN_STAGES_FP8 : MSA_ATTN_STAGES_BF16;
   static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
   static constexpr int kMergeBytes = kWarps * (kAccWarpFloats + 2 * kMaxHeads) * 4;
   static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
@@ -56,63 +54,42 @@ __device__ __forceinline__ int acc_index(int head, int dim) {
   return head * kAccStride + dim + (dim >> 5);
 }
 
-template <bool FP8, int SCALE, bool QUEUE>
+template <bool FP8, int SCALE>
 __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_CTAS_BF16)
     sparse_attn_kernel(const AttnLaunch p) {
-  using C = AttnCfg<FP8, QUEUE>;
+  using C = AttnCfg<FP8>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* qbar = bars + kWarps * C::kStages;
   int* flags = reinterpret_cast<int*>(qbar + 1);
   const uint8_t* q_s = smem + C::kQ;
 
+  const int split = blockIdx.x, r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
+  const long long tbl_row = (long long)r * p.tbl_stride;
   const unsigned full = 0xffffffffu;
 
+  // ---- prologue independent of the previous kernel: the row's queries
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const uint32_t q_bytes = (uint32_t)p.num_heads * kHeadDim * 2;
   if (tid == 0) {
     mbar_init(qbar, 1);
     for (int s = 0; s < kWarps * C::kStages; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
-  }
-  int split, r;
-  if constexpr (QUEUE) {
-    // overlapped decode: the top-k kernel, still running, publishes each
-    // row's items as it finishes the row; this CTA takes item blockIdx.x
-    if (tid == 0)
-      flags[2] = wait_at_least(p.queue + blockIdx.x, 1) ? ld_acquire(p.queue + blockIdx.x) - 1 : -1;
-    __syncthreads();
-    const int item = flags[2];
-    if (item < 0) {  // nothing issued yet: leave at once
-      if (tid == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
-      return;
-    }
-    r = item / p.splits;
-    split = item - r * p.splits;
-  } else {
-    split = blockIdx.x;
-    r = blockIdx.y;
-  }
-  const long long tbl_row = (long long)r * p.tbl_stride;
-
-  // ---- the row's queries (independent of the previous kernel)
-  const uint32_t q_bytes = (uint32_t)p.num_heads * kHeadDim * 2;
-  if (tid == 0) {
     mbar_arrive_expect_tx(qbar, q_bytes);
     bulk_g2s(smem + C::kQ, p.q + (long long)r * p.num_heads * kHeadDim, q_bytes, qbar);
   }
   // sparse tables and lengths come from the previous kernel on the stream
-  // (overlapped: from the published row, see above)
-  if constexpr (!QUEUE) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // this warp's page-16 entries are split*pps + warp + 4*i, one per lane; the
   // table load does not depend on the length, so both are in flight together
   const int e_begin = split * p.pages_per_split;
   const int e_lane = e_begin + warp + kWarps * lane;
   const bool lane_in_split = kWarps * lane + warp < p.pages_per_split && e_lane < p.tbl_stride;
-  long long my_e = lane_in_split ? (long long)__ldcg(p.tbl + tbl_row + e_lane) : 0ll;
-  int len = __ldcg(p.sparse_len + r);
+  long long my_e = lane_in_split ? (long long)p.tbl[tbl_row + e_lane] : 0ll;
+  int len = p.sparse_len[r];
   const bool len_bad = len < 0 || (long long)len > (long long)kPage16 * p.tbl_stride;
   const int nent = len_bad ? 0 : (len + kPage16 - 1) / kPage16;
   const int n_active = max(1, (nent + p.pages_per_split - 1) / p.pages_per_split);
@@ -514,19 +491,15 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
   }
 }
 
-template <bool FP8, int SCALE, bool QUEUE>
-cudaError_t launch_q(const AttnLaunch& p, cudaStream_t stream, bool programmatic) {
-  using C = AttnCfg<FP8, QUEUE>;
-  auto kern = sparse_attn_kernel<FP8, SCALE, QUEUE>;
+template <bool FP8, int SCALE>
+cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t stream, bool programmatic) {
+  using C = AttnCfg<FP8>;
+  auto kern = sparse_attn_kernel<FP8, SCALE>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  // overlapped: share SMs configured for the score kernel's large ring
-  if (e == cudaSuccess && QUEUE)
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = QUEUE ? dim3(p.splits * p.num_rows) : dim3(p.splits, p.num_rows);
+  cfg.gridDim = dim3(p.splits, p.num_rows);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
@@ -536,12 +509,6 @@ cudaError_t launch_q(const AttnLaunch& p, cudaStream_t stream, bool programmatic
   cfg.attrs = attr;
   cfg.numAttrs = programmatic ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
-template <bool FP8, int SCALE>
-cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t stream, bool programmatic) {
-  return p.queue ? launch_q<FP8, SCALE, true>(p, stream, programmatic)
-                 : launch_q<FP8, SCALE, false>(p, stream, programmatic);
 }
 
 }  // namespace

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
   extern __shared__ int sel[];  // [topk] selected blocks, ascending
   __shared__ int s_cnt[2][kWarps];
   __shared__ int s_scan[kWarps];
-  __shared__ int s_bad, s_wait;
+  __shared__ int s_bad;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const msa_batch& b = p.batch;
@@ -90,8 +90,6 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
     q = count_le - 1;  // cu_q is sorted and r < cu_q[R]
     bad = request_lengths(b, q, &q0, &qlen, &ctx, &nbq);
   }
-  // the score kernel streams every block of such a request, bad pages included
-  const bool scored = !bad;
   if (!bad) {
     int page_bad = 0;
     for (int blk = tid; blk < nbq; blk += kThreads) {
@@ -100,43 +98,22 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
     }
     if (__syncthreads_or(page_bad)) bad = MSA_DEV_BAD_PAGE;
   }
-  // Everything above reads only the batch geometry.  The scores come from
-  // the score kernel, which may still be running until here: in the
-  // overlapped decode this row waits only for its own request's blocks,
-  // otherwise for the whole previous kernel.
-  if (p.done) {
-    if (scored) {  // CTA-uniform
-      if (tid == 0) s_wait = wait_at_least(p.done + q, nbq);
-      __syncthreads();
-      if (!s_wait) bad |= MSA_DEV_TIMEOUT;
-    }
-  } else {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-  }
+  // everything above reads only the batch geometry; the scores come from the
+  // previous kernel on the stream, which may still be running until here
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!bad) {
     L = ctx + (r - q0) + 1;  // visible tokens
     n = (L + kBlock - 1) / kBlock;
 #pragma unroll
     for (int i = 0; i < KPT; ++i) {
       const int blk = KPT * tid + i;
-      key[i] = blk < n ? score_key(__ldcg(srow + blk)) : 0u;
+      key[i] = blk < n ? score_key(srow[blk]) : 0u;
     }
   }
-  // overlapped decode: make the row's outputs visible, then hand its
-  // attention items to the attention kernel (CTA-uniform call)
-  auto publish = [&]() {
-    if (!p.queue) return;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      const int base = atomicAdd(p.queue_tail, p.splits);
-      for (int s = 0; s < p.splits; ++s) st_release(p.queue + base + s, r * p.splits + s + 1);
-    }
-  };
   int32_t* out_idx = p.topk_idx + (long long)r * k;
   int32_t* out_tbl = p.tbl + (long long)r * p.tbl_stride;
   if (bad) {
-    const bool report = ((q >= 0) ? (r == q0) : (r == 0)) || (bad & MSA_DEV_TIMEOUT);
+    const bool report = (q >= 0) ? (r == q0) : (r == 0);
     if (tid == 0 && report) atomicOr(p.status, bad);
     for (int i = tid; i < k; i += kThreads) out_idx[i] = -1;
     for (int i = tid; i < p.tbl_stride; i += kThreads) out_tbl[i] = 0;
@@ -144,7 +121,6 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
       p.sparse_len[r] = 0;
       if (p.attn_counters) p.attn_counters[r] = 0;
     }
-    publish();
     return;
   }
 
@@ -223,17 +199,10 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
     p.sparse_len[r] = m > 0 ? kBlock * (m - 1) + min(kBlock, L - kBlock * sel[m - 1]) : 0;
     if (p.attn_counters) p.attn_counters[r] = 0;
   }
-  publish();
 }
 
 template <int KPT>
 cudaError_t launch_kpt(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
-  if (p.done) {  // overlapped: share SMs configured for the score kernel's large ring
-    cudaError_t e = cudaFuncSetAttribute(topk_table_kernel<KPT>,
-                                         cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.batch.num_rows);
   cfg.blockDim = dim3(kThreads);
