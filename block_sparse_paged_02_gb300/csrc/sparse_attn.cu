@@ -169,70 +169,79 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
   bool timed_out = false;
-  for (int i = 0; i < n_my; ++i) {
-    const int st = i % C::kStages;
+  // Two page-16 slabs (A = warp entry i, B = entry i+1) per iteration: four
+  // independent S chains, one softmax pass over 32 tokens and 32 P.V MMAs,
+  // which doubles the independent work the warp has in flight.  A missing B
+  // (odd count) reads A's stage and is masked to zero weight.
+  for (int i = 0; i < n_my; i += 2) {
+    const bool has_b = i + 1 < n_my;
+    const int st_a = i % C::kStages, st_b = has_b ? (i + 1) % C::kStages : st_a;
     // warp-uniform: the MMAs below need the whole warp
-    if (!__all_sync(full, mbar_wait(&wbar[st], (i / C::kStages) & 1))) {
+    bool ready = mbar_wait(&wbar[st_a], (i / C::kStages) & 1);
+    if (has_b) ready = ready && mbar_wait(&wbar[st_b], ((i + 1) / C::kStages) & 1);
+    if (!__all_sync(full, ready)) {
       timed_out = true;
       break;
     }
-    const uint8_t* ks_ = ring + st * C::kStageBytes;
-    const uint8_t* vs_ = ks_ + C::kSlab;
-    const float* ksc = reinterpret_cast<const float*>(ks_ + 2 * C::kSlab);
-    const float* vsc = ksc + kPage16;
-    const int tok0 = (e_begin + warp + kWarps * i) * kPage16;  // row token index of slot 0
-    const int nvalid = min(kPage16, len - tok0);              // >= 1
+    const uint8_t* stage[2] = {ring + st_a * C::kStageBytes, ring + st_b * C::kStageBytes};
+    const int tok_a = (e_begin + warp + kWarps * i) * kPage16;  // row token index of A's slot 0
+    const int nvalid[2] = {min(kPage16, len - tok_a),
+                           has_b ? min(kPage16, len - tok_a - kWarps * kPage16) : 0};
 
-    // ---- S = Q K^T for the 16 tokens: two n-tiles (tokens g and 8+g)
-    // two accumulators per n-tile (even / odd k-steps) halve the dependent
-    // MMA chain; they are summed below
-    float s[2][4], s_odd[2][4];
+    // ---- S = Q K^T: n-tile u = 2*slab + half holds tokens 8*half + g of the slab
+    float s[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-      s_odd[nt][0] = s_odd[nt][1] = s_odd[nt][2] = s_odd[nt][3] = 0.f;
-      const uint8_t* krow = ks_ + (8 * nt + g) * kHeadDim * C::kElem + 32 * c * C::kElem;
-      if constexpr (FP8) {
+    for (int u = 0; u < 4; ++u) s[u][0] = s[u][1] = s[u][2] = s[u][3] = 0.f;
+    if constexpr (FP8) {
+      uint32_t kw[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint8_t* krow = stage[u >> 1] + (8 * (u & 1) + g) * kHeadDim + 32 * c;
         const uint4 k0 = lds128(krow), k1 = lds128(krow + 16);
-        const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        kw[u][0] = k0.x; kw[u][1] = k0.y; kw[u][2] = k0.z; kw[u][3] = k0.w;
+        kw[u][4] = k1.x; kw[u][5] = k1.y; kw[u][6] = k1.z; kw[u][7] = k1.w;
+      }
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma16816<true>((kk & 1) ? s_odd[nt] : s[nt], qa[kk],
-                         e4m3x2_to_f16x2((uint16_t)(kw[kk] & 0xffffu)),
-                         e4m3x2_to_f16x2((uint16_t)(kw[kk] >> 16)));
-      } else {
-        uint32_t kw[16];
+      for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          mma16816<true>(s[u], qa[kk], e4m3x2_to_f16x2((uint16_t)(kw[u][kk] & 0xffffu)),
+                         e4m3x2_to_f16x2((uint16_t)(kw[u][kk] >> 16)));
+    } else {
+      uint32_t kw[4][16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint8_t* krow = stage[u >> 1] + ((8 * (u & 1) + g) * kHeadDim + 32 * c) * 2;
 #pragma unroll
         for (int h4 = 0; h4 < 4; ++h4) {
           const uint4 v = lds128(krow + 16 * h4);
-          kw[4 * h4] = v.x;
-          kw[4 * h4 + 1] = v.y;
-          kw[4 * h4 + 2] = v.z;
-          kw[4 * h4 + 3] = v.w;
+          kw[u][4 * h4] = v.x; kw[u][4 * h4 + 1] = v.y; kw[u][4 * h4 + 2] = v.z; kw[u][4 * h4 + 3] = v.w;
         }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma16816<false>((kk & 1) ? s_odd[nt] : s[nt], qa[kk], kw[2 * kk], kw[2 * kk + 1]);
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] += s_odd[nt][e];
-    }
-    // ---- scale, mask, online softmax (rows g and g+8)
+      for (int kk = 0; kk < 8; ++kk)
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+        for (int u = 0; u < 4; ++u) mma16816<false>(s[u], qa[kk], kw[u][2 * kk], kw[u][2 * kk + 1]);
+    }
+    // ---- scale, mask, online softmax over the 32 tokens (rows g and g+8)
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int t = 8 * nt + 2 * c + (e & 1);
-        float v = s[nt][e] * scale2;
-        if constexpr (SCALE == MSA_SCALE_PER_TOKEN_HEAD) v *= ksc[t];
-        s[nt][e] = t < nvalid ? v : -INFINITY;
+        const int t = 8 * (u & 1) + 2 * c + (e & 1);
+        float v = s[u][e] * scale2;
+        if constexpr (SCALE == MSA_SCALE_PER_TOKEN_HEAD)
+          v *= reinterpret_cast<const float*>(stage[u >> 1] + 2 * C::kSlab)[t];
+        s[u][e] = t < nvalid[u >> 1] ? v : -INFINITY;
       }
     float mx[2];
-    mx[0] = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-    mx[1] = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-    // Lazy rescaling: the reference max m_run only moves when a slab's max
+    mx[0] = fmaxf(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])),
+                  fmaxf(fmaxf(s[2][0], s[2][1]), fmaxf(s[3][0], s[3][1])));
+    mx[1] = fmaxf(fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3])),
+                  fmaxf(fmaxf(s[2][2], s[2][3]), fmaxf(s[3][2], s[3][3])));
+    // Lazy rescaling: the reference max m_run only moves when a pair's max
     // exceeds it by more than kRescaleSlack (log2 units), so p <= 2^slack and
-    // the accumulators are rescaled only on those (rare) slabs.
+    // the accumulators are rescaled only on those (rare) iterations.
     bool move[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -261,96 +270,110 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
     }
     const float base[2] = {m_run[0] == -INFINITY ? 0.f : m_run[0],
                            m_run[1] == -INFINITY ? 0.f : m_run[1]};
-    float pr[2][4];
+    float pr[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int u = 0; u < 4; ++u)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pr[nt][e] = exp2f(s[nt][e] - base[e >> 1]);
-    l_run[0] += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
-    l_run[1] += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
+      for (int e = 0; e < 4; ++e) pr[u][e] = exp2f(s[u][e] - base[e >> 1]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      l_run[0] += pr[u][0] + pr[u][1];
+      l_run[1] += pr[u][2] + pr[u][3];
+    }
     if constexpr (SCALE == MSA_SCALE_PER_TOKEN_HEAD) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pr[nt][e] *= vsc[8 * nt + 2 * c + (e & 1)];
+        for (int e = 0; e < 4; ++e)
+          pr[u][e] *= reinterpret_cast<const float*>(stage[u >> 1] + 2 * C::kSlab + 64)
+              [8 * (u & 1) + 2 * c + (e & 1)];
     }
-    // P as the A operand of O += P V: tokens (2c, 2c+1) from n-tile 0, (2c+8, 2c+9) from 1
-    uint32_t pa[4];
-    if constexpr (FP8) {
-      pa[0] = pack_f16x2(pr[0][0], pr[0][1]);
-      pa[1] = pack_f16x2(pr[0][2], pr[0][3]);
-      pa[2] = pack_f16x2(pr[1][0], pr[1][1]);
-      pa[3] = pack_f16x2(pr[1][2], pr[1][3]);
-    } else {
-      pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-      pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-      pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-      pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+    // P as the A operand of O += P V, per slab: tokens (2c, 2c+1) from its
+    // first n-tile, (2c+8, 2c+9) from its second
+    uint32_t pa[2][4];
+#pragma unroll
+    for (int sl = 0; sl < 2; ++sl) {
+      if constexpr (FP8) {
+        pa[sl][0] = pack_f16x2(pr[2 * sl][0], pr[2 * sl][1]);
+        pa[sl][1] = pack_f16x2(pr[2 * sl][2], pr[2 * sl][3]);
+        pa[sl][2] = pack_f16x2(pr[2 * sl + 1][0], pr[2 * sl + 1][1]);
+        pa[sl][3] = pack_f16x2(pr[2 * sl + 1][2], pr[2 * sl + 1][3]);
+      } else {
+        pa[sl][0] = pack_bf16x2(pr[2 * sl][0], pr[2 * sl][1]);
+        pa[sl][1] = pack_bf16x2(pr[2 * sl][2], pr[2 * sl][3]);
+        pa[sl][2] = pack_bf16x2(pr[2 * sl + 1][0], pr[2 * sl + 1][1]);
+        pa[sl][3] = pack_bf16x2(pr[2 * sl + 1][2], pr[2 * sl + 1][3]);
+      }
     }
     // ---- V fragments: tokens {2c, 2c+1, 2c+8, 2c+9}, dims 16g + j for n-tile j
     const int vt[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
     if constexpr (FP8) {
-      uint32_t vw[4][4];
+      uint32_t vw[2][4][4];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const uint4 v = lds128(vs_ + vt[a] * kHeadDim + 16 * g);
-        vw[a][0] = v.x;
-        vw[a][1] = v.y;
-        vw[a][2] = v.z;
-        vw[a][3] = v.w;
-      }
-      if (nvalid < kPage16) {  // never let garbage past the end reach P V
+      for (int sl = 0; sl < 2; ++sl) {
+        const uint8_t* vs_ = stage[sl] + C::kSlab;
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-          if (vt[a] >= nvalid) vw[a][0] = vw[a][1] = vw[a][2] = vw[a][3] = 0u;
+        for (int a = 0; a < 4; ++a) {
+          const uint4 v = lds128(vs_ + vt[a] * kHeadDim + 16 * g);
+          vw[sl][a][0] = v.x; vw[sl][a][1] = v.y; vw[sl][a][2] = v.z; vw[sl][a][3] = v.w;
+        }
+        if (nvalid[sl] < kPage16) {  // never let garbage past the end reach P V
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+            if (vt[a] >= nvalid[sl]) vw[sl][a][0] = vw[sl][a][1] = vw[sl][a][2] = vw[sl][a][3] = 0u;
+        }
       }
 #pragma unroll
       for (int j2 = 0; j2 < 8; ++j2) {  // n-tiles 2*j2, 2*j2+1
         const int wi = j2 >> 1, by = 2 * (j2 & 1);
         const uint32_t sel = (uint32_t)(by | ((4 + by) << 4) | ((by + 1) << 8) | ((5 + by) << 12));
-        const uint32_t lo = prmt(vw[0][wi], vw[1][wi], sel);  // tokens 2c, 2c+1
-        const uint32_t hi = prmt(vw[2][wi], vw[3][wi], sel);  // tokens 2c+8, 2c+9
-        mma16816<true>(o[2 * j2], pa, e4m3x2_to_f16x2((uint16_t)(lo & 0xffffu)),
-                       e4m3x2_to_f16x2((uint16_t)(hi & 0xffffu)));
-        mma16816<true>(o[2 * j2 + 1], pa, e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
-                       e4m3x2_to_f16x2((uint16_t)(hi >> 16)));
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl) {
+          const uint32_t lo = prmt(vw[sl][0][wi], vw[sl][1][wi], sel);  // tokens 2c, 2c+1
+          const uint32_t hi = prmt(vw[sl][2][wi], vw[sl][3][wi], sel);  // tokens 2c+8, 2c+9
+          mma16816<true>(o[2 * j2], pa[sl], e4m3x2_to_f16x2((uint16_t)(lo & 0xffffu)),
+                         e4m3x2_to_f16x2((uint16_t)(hi & 0xffffu)));
+          mma16816<true>(o[2 * j2 + 1], pa[sl], e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
+                         e4m3x2_to_f16x2((uint16_t)(hi >> 16)));
+        }
       }
     } else {
-      uint32_t vw[4][8];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const uint8_t* src = vs_ + (vt[a] * kHeadDim + 16 * g) * 2;
-        const uint4 v0 = lds128(src), v1 = lds128(src + 16);
-        vw[a][0] = v0.x;
-        vw[a][1] = v0.y;
-        vw[a][2] = v0.z;
-        vw[a][3] = v0.w;
-        vw[a][4] = v1.x;
-        vw[a][5] = v1.y;
-        vw[a][6] = v1.z;
-        vw[a][7] = v1.w;
-      }
-      if (nvalid < kPage16) {  // never let garbage past the end reach P V
+      for (int sl = 0; sl < 2; ++sl) {
+        uint32_t vw[4][8];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-          if (vt[a] >= nvalid)
+        for (int a = 0; a < 4; ++a) {
+          const uint8_t* src = stage[sl] + C::kSlab + (vt[a] * kHeadDim + 16 * g) * 2;
+          const uint4 v0 = lds128(src), v1 = lds128(src + 16);
+          vw[a][0] = v0.x; vw[a][1] = v0.y; vw[a][2] = v0.z; vw[a][3] = v0.w;
+          vw[a][4] = v1.x; vw[a][5] = v1.y; vw[a][6] = v1.z; vw[a][7] = v1.w;
+        }
+        if (nvalid[sl] < kPage16) {  // never let garbage past the end reach P V
 #pragma unroll
-            for (int x = 0; x < 8; ++x) vw[a][x] = 0u;
-      }
+          for (int a = 0; a < 4; ++a)
+            if (vt[a] >= nvalid[sl])
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
-        const uint32_t b0 = prmt(vw[0][j >> 1], vw[1][j >> 1], sel);
-        const uint32_t b1 = prmt(vw[2][j >> 1], vw[3][j >> 1], sel);
-        mma16816<false>(o[j], pa, b0, b1);
+              for (int x = 0; x < 8; ++x) vw[a][x] = 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+          const uint32_t b0 = prmt(vw[0][j >> 1], vw[1][j >> 1], sel);
+          const uint32_t b1 = prmt(vw[2][j >> 1], vw[3][j >> 1], sel);
+          mma16816<false>(o[j], pa[sl], b0, b1);
+        }
       }
     }
     __syncwarp();
-    if (i + C::kStages < n_my) {
-      const long long e = __shfl_sync(full, my_e, i + C::kStages);
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue(i + C::kStages, e);
+#pragma unroll
+    for (int d = 0; d < 2; ++d) {
+      const int nxt = i + d + C::kStages;
+      if (nxt < n_my) {
+        const long long e = __shfl_sync(full, my_e, nxt);
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(nxt, e);
+        }
       }
     }
   }
