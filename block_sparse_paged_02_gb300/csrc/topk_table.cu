@@ -8,24 +8,28 @@
 // "Implementation breakdown" item 3 (page-16 view of the page-128 cache) and
 // "Review highlights" (the zero fill must stay inside the row width).
 //
-// One CTA of 256 threads per row; each thread holds KPT consecutive block
-// scores as orderable 32-bit keys in registers.  The k-th largest key T is
-// found bit by bit from the top: T takes a bit whenever at least k keys are
-// >= the candidate, each count being a warp reduction plus one barrier
-// (double-buffered partial counts).  Block-wide exclusive scans then place,
-// in ascending block order, every key > T and the lowest-indexed keys == T
-// until k are taken -- the unique result under the lower-index tie rule.
-// The page-16 expansion and the length follow in the same CTA.
+// One CTA per row; each thread holds KPT consecutive block scores as
+// orderable 32-bit keys in registers (rows of up to 1024 blocks: 1024
+// threads, one key each).  The k-th largest key T is found bit by bit from
+// the top: T takes a bit whenever at least k keys are >= the candidate.  With
+// one key per thread each count is a single counting barrier
+// (bar.red.popc); with several, a warp reduction plus one barrier.  One
+// block-wide exclusive scan of the packed (== T, > T) counts then places, in
+// ascending block order, every key > T and the lowest-indexed keys == T until
+// k are taken -- the unique result under the lower-index tie rule.  The
+// row's block-table entries are read into shared memory while the score
+// kernel still runs (they are checked there anyway), so the page-16
+// expansion after the selection touches no global memory but its writes.
 #include "msa_internal.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-
-// exclusive scan of one int per thread over the CTA (two barriers)
+// Exclusive scan of one int per thread over a CTA of THREADS threads (two
+// barriers); *total receives the sum.  scratch holds THREADS/32 + 1 ints.
+template <int THREADS>
 __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) {
+  constexpr int kWarps = THREADS / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -35,23 +39,32 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
   }
   if (lane == 31) scratch[warp] = x;
   __syncthreads();
-  int before = 0, all = 0;
+  if (warp == 0) {  // scan of the warp totals
+    const int t = lane < kWarps ? scratch[lane] : 0;
+    int y = t;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const int c = scratch[w];
-    before += (w < warp) ? c : 0;
-    all += c;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += n;
+    }
+    if (lane < kWarps) scratch[lane] = y - t;
+    if (lane == 31) scratch[kWarps] = y;
   }
   __syncthreads();
-  *total = all;
+  const int before = scratch[warp];
+  *total = scratch[kWarps];
+  __syncthreads();  // scratch is reused by the next scan
   return before + x - v;
 }
 
-template <int KPT>
-__global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p) {
-  extern __shared__ int sel[];  // [topk] selected blocks, ascending
+template <int KPT, int THREADS>
+__global__ void __launch_bounds__(THREADS) topk_table_kernel(const TopkLaunch p) {
+  constexpr int kWarps = THREADS / 32;
+  // [topk] selected blocks (ascending), then the request's block-table row
+  extern __shared__ int sel[];
+  int* pages = sel + p.topk;
   __shared__ int s_cnt[2][kWarps];
-  __shared__ int s_scan[kWarps];
+  __shared__ int s_scan[kWarps + 1];
   __shared__ int s_bad;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -67,7 +80,7 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
     s_bad = (b.cu_seqlens_q[0] == 0 && b.cu_seqlens_q[R] == b.num_rows) ? 0 : MSA_DEV_MALFORMED;
   int le = 0;
   bool mono = true;
-  for (int q = tid; q < R; q += kThreads) {
+  for (int q = tid; q < R; q += THREADS) {
     const int c0 = b.cu_seqlens_q[q], c1 = b.cu_seqlens_q[q + 1];
     mono &= c1 >= c0;
     le += c0 <= r;
@@ -92,9 +105,10 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
   }
   if (!bad) {
     int page_bad = 0;
-    for (int blk = tid; blk < nbq; blk += kThreads) {
+    for (int blk = tid; blk < nbq; blk += THREADS) {
       const int page = b.block_table[(long long)q * b.bt_stride + blk];
       page_bad |= (page < 0 || page >= b.num_pages);
+      pages[blk] = page;
     }
     if (__syncthreads_or(page_bad)) bad = MSA_DEV_BAD_PAGE;
   }
@@ -115,8 +129,8 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
   if (bad) {
     const bool report = (q >= 0) ? (r == q0) : (r == 0);
     if (tid == 0 && report) atomicOr(p.status, bad);
-    for (int i = tid; i < k; i += kThreads) out_idx[i] = -1;
-    for (int i = tid; i < p.tbl_stride; i += kThreads) out_tbl[i] = 0;
+    for (int i = tid; i < k; i += THREADS) out_idx[i] = -1;
+    for (int i = tid; i < p.tbl_stride; i += THREADS) out_tbl[i] = 0;
     if (tid == 0) {
       p.sparse_len[r] = 0;
       if (p.attn_counters) p.attn_counters[r] = 0;
@@ -126,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
 
   const int m = min(k, n);
   if (n <= k) {  // every candidate is selected
-    for (int i = tid; i < n; i += kThreads) {
+    for (int i = tid; i < n; i += THREADS) {
       sel[i] = i;
       out_idx[i] = i;
     }
@@ -136,18 +150,24 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
 #pragma unroll 1
     for (int bit = 31; bit >= 0; --bit) {
       const uint32_t cand = T | (1u << bit);
-      int c = 0;
+      int total;
+      if constexpr (KPT == 1) {
+        total = __syncthreads_count(key[0] >= cand);
+      } else {
+        int c = 0;
 #pragma unroll
-      for (int i = 0; i < KPT; ++i) c += key[i] >= cand;
-      c = __reduce_add_sync(full, c);
-      if (lane == 0) s_cnt[bit & 1][warp] = c;
-      __syncthreads();
-      int total = 0;
+        for (int i = 0; i < KPT; ++i) c += key[i] >= cand;
+        c = __reduce_add_sync(full, c);
+        if (lane == 0) s_cnt[bit & 1][warp] = c;  // double-buffered: one barrier per bit
+        __syncthreads();
+        total = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) total += s_cnt[bit & 1][w];
+        for (int w = 0; w < kWarps; ++w) total += s_cnt[bit & 1][w];
+      }
       if (total >= k) T = cand;
     }
-    // ---- keys > T, then the lowest-indexed keys == T until k are taken
+    // ---- keys > T, then the lowest-indexed keys == T until k are taken:
+    // one scan of (count == T) << 16 | (count > T) (both < 2^16)
     int my_gt = 0, my_eq = 0;
 #pragma unroll
     for (int i = 0; i < KPT; ++i) {
@@ -155,41 +175,38 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
       my_gt += live && key[i] > T;
       my_eq += live && key[i] == T;
     }
-    int gt_total, eq_total, sel_total;
-    block_excl_scan(my_gt, s_scan, &gt_total);
-    const int eq_before = block_excl_scan(my_eq, s_scan, &eq_total);
-    const int need_eq = k - gt_total;
-    const int take_eq = max(0, min(my_eq, need_eq - eq_before));
-    int at = block_excl_scan(my_gt + take_eq, s_scan, &sel_total);
-    int eq_taken = 0;
+    int packed_total;
+    const int packed_before = block_excl_scan<THREADS>((my_eq << 16) | my_gt, s_scan, &packed_total);
+    const int gt_before = packed_before & 0xffff, eq_before = packed_before >> 16;
+    const int need_eq = k - (packed_total & 0xffff);  // the ties taken, lowest blocks first
+    int gt_seen = 0, eq_seen = 0;
 #pragma unroll
     for (int i = 0; i < KPT; ++i) {
       const int blk = KPT * tid + i;
-      const bool live = blk < n;
-      bool take = live && key[i] > T;
-      if (live && key[i] == T && eq_taken < take_eq) {
-        take = true;
-        ++eq_taken;
-      }
-      if (take) {
-        sel[at] = blk;
-        out_idx[at] = blk;
-        ++at;
+      if (blk < n) {
+        const bool gt = key[i] > T, eq = key[i] == T;
+        const int eq_rank = eq_before + eq_seen;
+        if (gt || (eq && eq_rank < need_eq)) {
+          const int at = gt_before + gt_seen + min(eq_rank, need_eq);
+          sel[at] = blk;
+          out_idx[at] = blk;
+        }
+        gt_seen += gt;
+        eq_seen += eq;
       }
     }
   }
-  for (int i = m + tid; i < k; i += kThreads) out_idx[i] = -1;
+  for (int i = m + tid; i < k; i += THREADS) out_idx[i] = -1;
   __syncthreads();
 
-  // ---- page-16 expansion, zero fill bounded by the row width
-  const int* bt_row = b.block_table + (long long)q * b.bt_stride;
-  for (int i = tid; i < p.tbl_stride; i += kThreads) {
+  // ---- page-16 expansion (pages from shared memory), zero fill bounded by the row width
+  for (int i = tid; i < p.tbl_stride; i += THREADS) {
     const int e = i >> 3, j = i & 7;
     int v = 0;
     if (e < m) {
       const int blk = sel[e];
       const int valid = min(kBlock, L - kBlock * blk);
-      if (j < (valid + kPage16 - 1) / kPage16) v = 8 * bt_row[blk] + j;
+      if (j < (valid + kPage16 - 1) / kPage16) v = 8 * pages[blk] + j;
     }
     out_tbl[i] = v;
   }
@@ -201,19 +218,26 @@ __global__ void __launch_bounds__(kThreads) topk_table_kernel(const TopkLaunch p
   }
 }
 
-template <int KPT>
+template <int KPT, int THREADS>
 cudaError_t launch_kpt(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
+  auto kern = topk_table_kernel<KPT, THREADS>;
+  const size_t smem = (size_t)(p.topk + p.batch.bt_stride) * sizeof(int);
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.batch.num_rows);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = (size_t)p.topk * sizeof(int);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = programmatic ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, topk_table_kernel<KPT>, p);
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
@@ -221,9 +245,9 @@ cudaError_t launch_kpt(const TopkLaunch& p, cudaStream_t stream, bool programmat
 cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
   if (p.batch.num_rows == 0) return cudaSuccess;
   // a row has at most bt_stride candidate blocks
-  if (p.batch.bt_stride <= kThreads * 4) return launch_kpt<4>(p, stream, programmatic);
-  if (p.batch.bt_stride <= kThreads * 16) return launch_kpt<16>(p, stream, programmatic);
-  return launch_kpt<64>(p, stream, programmatic);
+  if (p.batch.bt_stride <= 1024) return launch_kpt<1, 1024>(p, stream, programmatic);
+  if (p.batch.bt_stride <= 256 * 16) return launch_kpt<16, 256>(p, stream, programmatic);
+  return launch_kpt<64, 256>(p, stream, programmatic);
 }
 
 }  // namespace msa

@@ -137,6 +137,17 @@ def test_heavy_ties(msa, orc):
     check_against_oracle(orc, w, sep, fused)
 
 
+@pytest.mark.parametrize("seq,idx_range", [(200_000, 3), (200_000, 1), (1_000_000, 3)])
+def test_long_rows_wide_block_tables(msa, orc, seq, idx_range):
+    # rows with more than 1024 candidate blocks take the several-keys-per-thread
+    # top-k (bt_stride up to 16384); k = 64 and, with idx_range 1, many ties
+    w = W.custom(53, q_lens=[1, 2], seq_lens=[seq, seq // 3], hq=16, di=64, topk=64,
+                 idx_range=idx_range)
+    assert w.bt_stride > 1024
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
 def test_garbage_past_the_end_is_ignored(msa, orc):
     for kv in (W.KV_BF16, W.KV_FP8):
         w = W.custom(53, q_lens=[1, 3, 1], seq_lens=[1000, 517, 129], hq=16, di=128, topk=4,
