@@ -37,10 +37,12 @@ L2_FLUSH_BYTES = 512 << 20
 
 # ---------------------------------------------------------------- bytes model
 
-def algorithmic_bytes(w, sparse_len: np.ndarray) -> dict:
+def algorithmic_bytes(w, topk_idx: np.ndarray) -> dict:
     """Bytes the method must move for one call, per kernel and in total:
     index-K read once per request, queries, block tables, the selected K/V
-    (+ per-token scales), the tables, O and LSE.  Scores are intermediates."""
+    (+ per-token scales) counted once per request over the union of its
+    rows' selected blocks (a block selected by several rows of a request is
+    read from HBM once), the tables, O and LSE.  Scores are intermediates."""
     seq = w.seq_lens
     nb_req = (seq + 127) // 128
     N = w.num_rows
@@ -49,7 +51,16 @@ def algorithmic_bytes(w, sparse_len: np.ndarray) -> dict:
     bt = int(nb_req.sum()) * 4
     q = N * w.hq * w.head_dim * 2
     kv_elem = 1 if w.kv_dtype == W.KV_FP8 else 2
-    toks = int(np.asarray(sparse_len, np.int64).sum())
+    toks = 0
+    for rq in range(len(seq)):
+        r0, r1 = int(w.cu_seqlens_q[rq]), int(w.cu_seqlens_q[rq + 1])
+        seen = {}
+        for r in range(r0, r1):
+            L = int(w.context_lens[rq]) + (r - r0) + 1  # tokens row r sees
+            for b in topk_idx[r]:
+                if b >= 0:
+                    seen[int(b)] = max(seen.get(int(b), 0), min(128, L - 128 * int(b)))
+        toks += sum(seen.values())
     kv = toks * w.hkv * w.head_dim * kv_elem * 2
     if w.scale_mode == W.SCALE_PER_TOKEN_HEAD:
         kv += toks * w.hkv * 4 * 2
@@ -330,7 +341,7 @@ def run_gpu(args):
     # ---- end to end through the public API: host buffers, copies inside
     case.decode()
     torch.cuda.synchronize()
-    sparse_len = case.sparse_len[: w.num_rows].cpu().numpy()
+    topk_sel = case.topk_idx[: w.num_rows].cpu().numpy()
     host = {name: getattr(case, name).cpu().pin_memory()
             for name in ("q", "idx_q", "cu_q", "cu_k", "ctx", "bt")}
     out_h = torch.empty_like(case.out, device="cpu").pin_memory()
@@ -364,7 +375,7 @@ def run_gpu(args):
     launches_per_step = 3 + int(q_lens.max() >= 64 and w.index_heads == 1)
     value = rows_total / (total_ms / 1e3)
     peak, peak_kind = read_peaks()
-    nbytes = algorithmic_bytes(w, sparse_len)
+    nbytes = algorithmic_bytes(w, topk_sel)
     score_avg = statistics.mean(score_ms)
     achieved = nbytes["score_kernel"] / (score_avg / 1e3) / 1e9
     step_avg = total_ms / args.steps
