@@ -62,6 +62,8 @@ def _load():
             lib.orc_row_geometry.argtypes = [P, P, P, P, P]
             lib.orc_index_score.restype = ctypes.c_uint32
             lib.orc_index_score.argtypes = [P, P, P, i32, i32, P, i32, i32]
+            lib.orc_index_score_fp8.restype = ctypes.c_uint32
+            lib.orc_index_score_fp8.argtypes = [P, P, P, P, i32, i32, P, i32, i32]
             lib.orc_topk_build_table.restype = ctypes.c_uint32
             lib.orc_topk_build_table.argtypes = [P, P, i32, i32, P, P, i32, P, i32]
             lib.orc_sparse_attn.restype = ctypes.c_uint32
@@ -132,14 +134,23 @@ def row_geometry(batch: Batch):
 
 
 def index_score(batch: Batch, idx_q, idx_k, score_stride: Optional[int] = None,
-                nthreads: Optional[int] = None):
+                nthreads: Optional[int] = None, *, fp8: bool = False, k_scale=None):
+    """Block scores; idx_k holds bf16 bits, or e4m3 codes when fp8 (with
+    optional per-token scales k_scale [P,128,Hi])."""
     idx_q = _c(idx_q, np.uint16)
-    idx_k = _c(idx_k, np.uint16)
     hi, di = int(idx_q.shape[1]), int(idx_q.shape[2])
     stride = int(score_stride or batch.s.bt_stride)
     scores = np.empty((max(batch.num_rows, 1), stride), np.float32)
-    st = _load().orc_index_score(ctypes.byref(batch.s), _ptr(idx_q), _ptr(idx_k), hi, di,
-                                 _ptr(scores), stride, nthreads or default_threads())
+    n = nthreads or default_threads()
+    if fp8:
+        idx_k = _c(idx_k, np.uint8)
+        ks = None if k_scale is None else _c(k_scale, np.float32)
+        st = _load().orc_index_score_fp8(ctypes.byref(batch.s), _ptr(idx_q), _ptr(idx_k),
+                                         _ptr(ks), hi, di, _ptr(scores), stride, n)
+    else:
+        idx_k = _c(idx_k, np.uint16)
+        st = _load().orc_index_score(ctypes.byref(batch.s), _ptr(idx_q), _ptr(idx_k), hi, di,
+                                     _ptr(scores), stride, n)
     return scores[: batch.num_rows], int(st)
 
 
@@ -204,7 +215,8 @@ def decode(w, nthreads: Optional[int] = None, topk: Optional[int] = None):
     """The whole path on a workload: scores -> top-k/table -> sparse attention."""
     b = Batch.of(w)
     k = int(topk or w.topk)
-    scores, st1 = index_score(b, w.idx_q, w.idx_k, nthreads=nthreads)
+    scores, st1 = index_score(b, w.idx_q, w.idx_k, nthreads=nthreads,
+                              fp8=w.index_dtype == 1, k_scale=w.idx_k_scale)
     topk_idx, tbl, slen, st2 = topk_build_table(b, scores, k, nthreads=nthreads)
     out, lse, st3 = sparse_attn(w.q, w.k_cache, w.v_cache, w.kv_dtype, tbl, slen,
                                 scale_mode=w.scale_mode, k_scale=w.k_scale, v_scale=w.v_scale,

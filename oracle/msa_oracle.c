@@ -187,11 +187,20 @@ static void geometry_free(geom_t* g) {
 typedef struct {
   const orc_batch* b;
   const geom_t* g;
-  const uint16_t *idx_q, *idx_k;
+  const uint16_t* idx_q;
+  const void* idx_k;      /* bf16 bits, or e4m3 codes when fp8 */
+  const float* k_scale;   /* fp8 only: [P, 128, hi] per-token scale, or NULL (1) */
+  int32_t fp8;
   int32_t hi, di;
   float* scores;
   int32_t score_stride;
 } score_ctx;
+
+/* Value of index-K element d of (page, token tl, head h). */
+static double index_k_value(const score_ctx* c, int64_t base, int32_t d) {
+  if (c->fp8) return orc_fp8_e4m3_value(((const uint8_t*)c->idx_k)[base + d]);
+  return orc_bf16_value(((const uint16_t*)c->idx_k)[base + d]);
+}
 
 static void score_row(void* vctx, int32_t r) {
   const score_ctx* c = (const score_ctx*)vctx;
@@ -209,9 +218,11 @@ static void score_row(void* vctx, int32_t r) {
       if (t > pos) break; /* causal: only tokens at or before the row's position */
       for (int32_t h = 0; h < c->hi; ++h) {
         const uint16_t* qv = c->idx_q + ((int64_t)r * c->hi + h) * c->di;
-        const uint16_t* kv = c->idx_k + (((int64_t)page * BLOCK + tl) * c->hi + h) * c->di;
+        const int64_t slot = ((int64_t)page * BLOCK + tl) * c->hi + h;
         double dot = 0.0;
-        for (int32_t d = 0; d < c->di; ++d) dot += orc_bf16_value(qv[d]) * orc_bf16_value(kv[d]);
+        for (int32_t d = 0; d < c->di; ++d)
+          dot += orc_bf16_value(qv[d]) * index_k_value(c, slot * c->di, d);
+        if (c->fp8 && c->k_scale) dot *= (double)c->k_scale[slot]; /* dequantised key */
         if (dot > best) best = dot; /* NaN dots never win */
       }
     }
@@ -224,7 +235,18 @@ uint32_t orc_index_score(const orc_batch* b, const uint16_t* idx_q, const uint16
                          int32_t score_stride, int32_t nthreads) {
   geom_t g;
   uint32_t st = geometry_alloc(b, &g);
-  score_ctx c = {b, &g, idx_q, idx_k, index_heads, index_dim, scores, score_stride};
+  score_ctx c = {b, &g, idx_q, idx_k, NULL, 0, index_heads, index_dim, scores, score_stride};
+  for_each_row(b->num_rows, nthreads, score_row, &c);
+  geometry_free(&g);
+  return st;
+}
+
+uint32_t orc_index_score_fp8(const orc_batch* b, const uint16_t* idx_q, const uint8_t* idx_k,
+                             const float* k_scale, int32_t index_heads, int32_t index_dim,
+                             float* scores, int32_t score_stride, int32_t nthreads) {
+  geom_t g;
+  uint32_t st = geometry_alloc(b, &g);
+  score_ctx c = {b, &g, idx_q, idx_k, k_scale, 1, index_heads, index_dim, scores, score_stride};
   for_each_row(b->num_rows, nthreads, score_row, &c);
   geometry_free(&g);
   return st;

@@ -58,6 +58,14 @@ uint32_t orc_index_score(const orc_batch* b, const uint16_t* idx_q, const uint16
                          int32_t index_heads, int32_t index_dim, float* scores,
                          int32_t score_stride, int32_t nthreads);
 
+/* Step 1 with an FP8 index-K cache (OCP e4m3 codes [P,128,Hi,Di]; optional
+ * fp32 per-token scales k_scale [P,128,Hi], NULL meaning 1): the dot product
+ * with the decoded codes, times the token's scale, then the same maximum and
+ * fp32 rounding as orc_index_score. */
+uint32_t orc_index_score_fp8(const orc_batch* b, const uint16_t* idx_q, const uint8_t* idx_k,
+                             const float* k_scale, int32_t index_heads, int32_t index_dim,
+                             float* scores, int32_t score_stride, int32_t nthreads);
+
 /* Steps 2+3: top-k (ties to the lower block, output ascending by block) and
  * page-16 table expansion with the context-length clamp. */
 uint32_t orc_topk_build_table(const orc_batch* b, const float* scores, int32_t score_stride,

@@ -143,11 +143,13 @@ def test_index_score_planted_causal_rows(orc):
     assert list(scores[:, 7]) == [0.0, 0.0, 6.0]
 
 
-def _dense_index_scores(w):
+def _dense_index_scores(w, k_values=None):
     """numpy reference: gather each request's index-K through the block table,
-    matmul in float64, mask future tokens, max within each 128-token block."""
+    matmul in float64, mask future tokens, max within each 128-token block.
+    k_values: the keys as floats (default: w.idx_k as bf16 bits)."""
     to_f = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).double().numpy()
-    qf, kf = to_f(w.idx_q), to_f(w.idx_k)
+    qf = to_f(w.idx_q)
+    kf = to_f(w.idx_k) if k_values is None else k_values
     out = np.full((w.num_rows, w.bt_stride), NEG_INF)
     for r in range(w.num_reqs):
         L = int(w.seq_lens[r])
@@ -171,6 +173,43 @@ def test_index_score_matches_matmul(orc, hi, di):
     assert st == 0
     ref = _dense_index_scores(w)
     assert np.array_equal(scores.astype(np.float64), ref)
+
+
+def _fp8_float(codes):
+    # an e4m3 decoder independent of the oracle's: torch's float8_e4m3fn
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("hi,di", [(1, 64), (2, 64), (1, 128)])
+def test_fp8_index_score_matches_matmul(orc, hi, di):
+    # e4m3 index-K with per-token scales: s_t * (q . k_t), max over the block's
+    # visible tokens and heads, checked against a matmul over torch-decoded keys
+    w = W.fp8_index(W.custom(13, q_lens=[1, 4, 3], seq_lens=[700, 1029, 130], hq=4, di=di,
+                             hi=hi, topk=3), seed=14)
+    scores, st = orc.index_score(orc.Batch.of(w), w.idx_q, w.idx_k, fp8=True,
+                                 k_scale=w.idx_k_scale)
+    assert st == 0
+    deq = _fp8_float(w.idx_k) * w.idx_k_scale[..., None].astype(np.float64)
+    ref = _dense_index_scores(w, k_values=deq)
+    assert np.array_equal(scores.astype(np.float64), ref)
+
+
+def test_fp8_index_without_scales_equals_bf16_index(orc):
+    # the integer index values are exact in e4m3, so unscaled FP8 keys score
+    # exactly as the bf16 keys they were encoded from
+    w = W.custom(15, q_lens=[2, 1], seq_lens=[2000, 333], hq=4, di=128, topk=4)
+    w8 = W.fp8_index(w, seed=16, scaled=False)
+    b = orc.Batch.of(w)
+    s16, _ = orc.index_score(b, w.idx_q, w.idx_k)
+    s8, _ = orc.index_score(b, w8.idx_q, w8.idx_k, fp8=True, k_scale=None)
+    assert np.array_equal(s16, s8, equal_nan=True)
+    # doubling every scale doubles every finite score
+    w8s = W.fp8_index(w, seed=17)
+    a, _ = orc.index_score(b, w8s.idx_q, w8s.idx_k, fp8=True, k_scale=w8s.idx_k_scale)
+    d, _ = orc.index_score(b, w8s.idx_q, w8s.idx_k, fp8=True, k_scale=2 * w8s.idx_k_scale)
+    fin = np.isfinite(a)
+    assert np.array_equal(2 * a[fin], d[fin]) and np.array_equal(np.isfinite(d), fin)
 
 
 def test_index_score_ignores_garbage(orc):

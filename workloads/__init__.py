@@ -83,6 +83,10 @@ class Workload:
     sinks: Optional[np.ndarray]    # fp32 [Hq]
     softmax_scale: float
     seed: int = 0
+    # index-K cache format: KV_BF16 (idx_k holds bf16 bits) or KV_FP8 (idx_k
+    # holds OCP e4m3 codes, idx_k_scale optional fp32 [P, 128, Hi])
+    index_dtype: int = 0
+    idx_k_scale: Optional[np.ndarray] = None
 
     @property
     def num_reqs(self) -> int:
@@ -275,10 +279,32 @@ def custom(seed: int, q_lens, seq_lens, *, hq=16, di=128, idx_range=3, topk=16,
                   fill_unused_nan=fill_unused_nan)
 
 
+def fp8_index(w: Workload, seed: int, scaled: bool = True) -> Workload:
+    """The same workload with its index-K cache stored as OCP e4m3 codes (the
+    integer index values are exact in e4m3; NaN fill stays NaN) and, when
+    scaled, per-token scales drawn from {1/2, 1, 2} (powers of two keep every
+    score exact)."""
+    rng = np.random.default_rng(seed)
+    vals = (np.asarray(w.idx_k, np.uint16).astype(np.uint32) << 16).view(np.float32)
+    codes = fp8_codes(vals)
+    scale = None
+    if scaled:
+        shape = (w.num_pages, BLOCK, w.index_heads)
+        scale = rng.choice(np.array([0.5, 1.0, 2.0], np.float32), size=shape).astype(np.float32)
+    return dataclasses.replace(w, name=w.name + "_fp8_index", idx_k=codes, index_dtype=KV_FP8,
+                               idx_k_scale=scale)
+
+
+def large_batch_fp8_index(seed: int = 4) -> Workload:
+    """The 64-request decode with an FP8 (e4m3, per-token scaled) index-K cache."""
+    return fp8_index(large_batch(seed), seed + 100)
+
+
 NAMED = {
     "tiny_decode": tiny,
     "batched_decode": batched,
     "speculative_decode": speculative,
     "large_batch_decode": large_batch,
     "chunked_prefill": chunked_prefill,
+    "large_batch_decode_fp8_index": large_batch_fp8_index,
 }
