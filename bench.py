@@ -46,7 +46,11 @@ def algorithmic_bytes(w, topk_idx: np.ndarray) -> dict:
     seq = w.seq_lens
     nb_req = (seq + 127) // 128
     N = w.num_rows
-    idx_k = int(seq.sum()) * w.index_heads * w.index_dim * 2
+    if getattr(w, "index_dtype", 0) == W.KV_FP8:  # e4m3 codes (+ fp32 per-token scales)
+        idx_k = int(seq.sum()) * w.index_heads * (w.index_dim + (4 if w.idx_k_scale is not None
+                                                                   else 0))
+    else:
+        idx_k = int(seq.sum()) * w.index_heads * w.index_dim * 2
     idx_q = N * w.index_heads * w.index_dim * 2
     bt = int(nb_req.sum()) * 4
     q = N * w.hq * w.head_dim * 2
@@ -221,7 +225,7 @@ def run_reference(args):
 
 
 W_SEED = {"tiny_decode": 1, "batched_decode": 2, "speculative_decode": 3,
-          "large_batch_decode": 4, "chunked_prefill": 5}
+          "large_batch_decode": 4, "chunked_prefill": 5, "large_batch_decode_fp8_index": 6}
 
 
 def rank_seed(workload: str, rank: int) -> int:
@@ -235,6 +239,8 @@ def workload_config(w):
     return {"workload": w.name, "requests": w.num_reqs, "rows": w.num_rows,
             "query_heads": w.hq, "kv_heads": w.hkv, "head_dim": w.head_dim,
             "index_dim": w.index_dim, "topk": w.topk,
+            "index_k": ("fp8_e4m3" + (" + per-token scales" if w.idx_k_scale is not None else "")
+                        if getattr(w, "index_dtype", 0) == W.KV_FP8 else "bf16"),
             "kv": "fp8_e4m3" if w.kv_dtype == W.KV_FP8 else "bf16",
             "scales": ["none", "scalar", "per_token_head"][w.scale_mode],
             "sinks": w.sinks is not None, "context_tokens": int(seq.sum()),
@@ -372,7 +378,8 @@ def run_gpu(args):
         return 0
     rows_total = w.num_rows * ws * args.steps
     q_lens = np.diff(w.cu_seqlens_q)
-    launches_per_step = 3 + int(q_lens.max() >= 64 and w.index_heads == 1)
+    launches_per_step = 3 + int(q_lens.max() >= 64 and w.index_heads == 1
+                                and getattr(w, "index_dtype", 0) != W.KV_FP8)
     value = rows_total / (total_ms / 1e3)
     peak, peak_kind = read_peaks()
     nbytes = algorithmic_bytes(w, topk_sel)

@@ -51,6 +51,11 @@ class msa_attn_args(ctypes.Structure):
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
 
 
+class msa_index_cache(ctypes.Structure):
+    _fields_ = [("k_cache", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("dtype", ctypes.c_int32), ("heads", ctypes.c_int32), ("dim", ctypes.c_int32)]
+
+
 class msa_trace(ctypes.Structure):
     _fields_ = [("after_score", ctypes.c_void_p), ("after_topk", ctypes.c_void_p),
                 ("after_attn", ctypes.c_void_p)]
@@ -78,17 +83,16 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L = ctypes.CDLL(path)
             P, i32 = ctypes.c_void_p, ctypes.c_int32
             L.msa_index_score.restype = ctypes.c_int
-            L.msa_index_score.argtypes = [P, P, P, i32, i32, P, i32, P, P]
+            L.msa_index_score.argtypes = [P, P, P, P, i32, P, P]
             L.msa_topk_build_table.restype = ctypes.c_int
             L.msa_topk_build_table.argtypes = [P, P, i32, i32, P, P, i32, P, P, P]
             L.msa_sparse_paged_attn.restype = ctypes.c_int
             L.msa_sparse_paged_attn.argtypes = [P, P, i32, P, P, ctypes.c_size_t, P, P]
             L.msa_decode.restype = ctypes.c_int
-            L.msa_decode.argtypes = [P, P, P, i32, i32, i32, P, P, P, i32, P, P, ctypes.c_size_t,
-                                     P, P, P]
+            L.msa_decode.argtypes = [P, P, P, i32, P, P, P, i32, P, P, ctypes.c_size_t, P, P, P]
             L.msa_kv_insert.restype = ctypes.c_int
-            L.msa_kv_insert.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, i32, i32, P, P,
-                                        i32, P, P]
+            L.msa_kv_insert.argtypes = [P, P, P, i32, i32, P, P, i32, i32, P, P, P, P, i32, P,
+                                        P]
             L.msa_workspace_size.restype = ctypes.c_size_t
             L.msa_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
             L.msa_status_string.restype = ctypes.c_char_p
@@ -150,6 +154,15 @@ def check_sinks(sinks: Optional[torch.Tensor], num_heads: int):
         raise ValueError("sinks must be contiguous")
 
 
+def make_index_cache(k_cache, dtype: int = MSA_KV_BF16, k_scale=None) -> msa_index_cache:
+    """The paged index-K cache [P, 128, heads, dim] (bf16, or e4m3 codes with
+    optional fp32 per-token scales [P, 128, heads])."""
+    x = msa_index_cache(_p(k_cache), _p(k_scale), int(dtype), int(k_cache.shape[2]),
+                        int(k_cache.shape[3]))
+    x._keep = (k_cache, k_scale)
+    return x
+
+
 def make_attn_args(q, k_cache, v_cache, kv_dtype: int, num_pages: int, out, lse, *,
                    scale_mode: int = MSA_SCALE_NONE, k_scale=None, v_scale=None, sinks=None,
                    softmax_scale: float) -> msa_attn_args:
@@ -169,11 +182,11 @@ def msa_workspace_size(num_rows, bt_stride, topk, num_heads, head_dim, tbl_strid
                                         int(num_heads), int(head_dim), int(tbl_stride)))
 
 
-def msa_index_score(batch: msa_batch, idx_q, idx_k_cache, index_heads, index_dim, scores,
-                    score_stride, dev_status, stream=None):
+def msa_index_score(batch: msa_batch, idx_q, index: msa_index_cache, scores, score_stride,
+                    dev_status, stream=None):
     _check("msa_index_score", lib().msa_index_score(
-        ctypes.byref(batch), _p(idx_q), _p(idx_k_cache), int(index_heads), int(index_dim),
-        _p(scores), int(score_stride), _p(dev_status), _stream(stream)))
+        ctypes.byref(batch), _p(idx_q), ctypes.byref(index), _p(scores), int(score_stride),
+        _p(dev_status), _stream(stream)))
 
 
 def msa_topk_build_table(batch: msa_batch, scores, score_stride, topk, topk_idx, sparse_tbl,
@@ -191,24 +204,23 @@ def msa_sparse_paged_attn(attn: msa_attn_args, sparse_tbl, tbl_stride, sparse_le
         _p(dev_status), _stream(stream)))
 
 
-def msa_decode(batch: msa_batch, idx_q, idx_k_cache, index_heads, index_dim, topk,
-               attn: msa_attn_args, topk_idx, sparse_tbl, tbl_stride, sparse_len, workspace,
-               dev_status, trace: Optional[msa_trace] = None, stream=None):
+def msa_decode(batch: msa_batch, idx_q, index: msa_index_cache, topk, attn: msa_attn_args,
+               topk_idx, sparse_tbl, tbl_stride, sparse_len, workspace, dev_status,
+               trace: Optional[msa_trace] = None, stream=None):
     _check("msa_decode", lib().msa_decode(
-        ctypes.byref(batch), _p(idx_q), _p(idx_k_cache), int(index_heads), int(index_dim),
-        int(topk), ctypes.byref(attn), _p(topk_idx), _p(sparse_tbl), int(tbl_stride),
-        _p(sparse_len), _p(workspace),
+        ctypes.byref(batch), _p(idx_q), ctypes.byref(index), int(topk), ctypes.byref(attn),
+        _p(topk_idx), _p(sparse_tbl), int(tbl_stride), _p(sparse_len), _p(workspace),
         int(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
         _p(dev_status), ctypes.byref(trace) if trace is not None else None, _stream(stream)))
 
 
-def msa_kv_insert(batch: msa_batch, k_new, v_new, idx_new, num_kv_heads, head_dim, index_heads,
-                  index_dim, k_cache, v_cache, idx_k_cache, kv_dtype, scale_mode, k_scale,
-                  v_scale, skip_index, dev_status, stream=None):
+def msa_kv_insert(batch: msa_batch, k_new, v_new, num_kv_heads, head_dim, k_cache, v_cache,
+                  kv_dtype, scale_mode, k_scale, v_scale, idx_new,
+                  index: Optional[msa_index_cache], skip_index, dev_status, stream=None):
     _check("msa_kv_insert", lib().msa_kv_insert(
-        ctypes.byref(batch), _p(k_new), _p(v_new), _p(idx_new), int(num_kv_heads),
-        int(head_dim), int(index_heads), int(index_dim), _p(k_cache), _p(v_cache),
-        _p(idx_k_cache), int(kv_dtype), int(scale_mode), _p(k_scale), _p(v_scale),
+        ctypes.byref(batch), _p(k_new), _p(v_new), int(num_kv_heads), int(head_dim),
+        _p(k_cache), _p(v_cache), int(kv_dtype), int(scale_mode), _p(k_scale), _p(v_scale),
+        _p(idx_new), ctypes.byref(index) if index is not None else None,
         int(bool(skip_index)), _p(dev_status), _stream(stream)))
 
 

@@ -40,6 +40,10 @@ class DeviceCase:
         self.bt = _dev(w.block_table, device)
         self.idx_q = _dev(w.idx_q, device)
         self.idx_k = _dev(w.idx_k, device)
+        idx_scale = getattr(w, "idx_k_scale", None)
+        self.idx_k_scale = None if idx_scale is None else _dev(idx_scale, device)
+        self.index = B.make_index_cache(self.idx_k, getattr(w, "index_dtype", B.MSA_KV_BF16),
+                                        self.idx_k_scale)
         self.q = _dev(w.q, device)
         self.k = _dev(w.k_cache, device)
         self.v = _dev(w.v_cache, device)
@@ -70,8 +74,8 @@ class DeviceCase:
 
     # -- the four entry points on this batch
     def index_score(self, stream=None):
-        B.msa_index_score(self.batch, self.idx_q, self.idx_k, self.w.index_heads,
-                          self.w.index_dim, self.scores, self.w.bt_stride, self.status, stream)
+        B.msa_index_score(self.batch, self.idx_q, self.index, self.scores, self.w.bt_stride,
+                          self.status, stream)
 
     def topk_build_table(self, stream=None):
         B.msa_topk_build_table(self.batch, self.scores, self.w.bt_stride, self.topk,
@@ -83,18 +87,17 @@ class DeviceCase:
                                 self.attn_workspace, self.status, stream)
 
     def decode(self, keep_tables: bool = True, trace=None, stream=None):
-        B.msa_decode(self.batch, self.idx_q, self.idx_k, self.w.index_heads, self.w.index_dim,
-                     self.topk, self.attn, self.topk_idx if keep_tables else None,
+        B.msa_decode(self.batch, self.idx_q, self.index, self.topk, self.attn,
+                     self.topk_idx if keep_tables else None,
                      self.tbl if keep_tables else None, self.tbl_stride,
                      self.sparse_len if keep_tables else None, self.workspace, self.status,
                      trace, stream)
 
     def kv_insert(self, k_new, v_new, idx_new, skip_index: bool = False, stream=None):
         """Write the rows' new K/V/index-K (device bf16 tensors) into the pools."""
-        B.msa_kv_insert(self.batch, k_new, v_new, idx_new, self.w.hkv, self.w.head_dim,
-                        self.w.index_heads, self.w.index_dim, self.k, self.v, self.idx_k,
+        B.msa_kv_insert(self.batch, k_new, v_new, self.w.hkv, self.w.head_dim, self.k, self.v,
                         self.w.kv_dtype, self.w.scale_mode, self.k_scale, self.v_scale,
-                        skip_index, self.status, stream)
+                        idx_new, self.index, skip_index, self.status, stream)
 
     def fetch(self):
         torch.cuda.synchronize()

@@ -110,6 +110,14 @@ msa_status check_attn(const msa_attn_args* a) {
   return MSA_OK;
 }
 
+msa_status check_index(const msa_index_cache* x) {
+  if (!x) return MSA_ERR_NULL;
+  if (x->dtype != MSA_KV_BF16 && x->dtype != MSA_KV_FP8_E4M3) return MSA_ERR_DTYPE;
+  if (!((x->heads == 1 && (x->dim == 64 || x->dim == 128)) || (x->heads == 2 && x->dim == 64)))
+    return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
 AttnLaunch make_attn(const msa_attn_args* a, const int32_t* tbl, int tbl_stride,
                      const int32_t* len, float* partials, uint32_t* counters, int pps,
                      int splits, uint32_t* status) {
@@ -144,7 +152,9 @@ msa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_E
 // Step 1: the streaming CUDA-core kernel, plus the tensor-core kernel for
 // requests with many rows when the batch may hold any (max_q_len hint).
 cudaError_t launch_scores(ScoreLaunch p, cudaStream_t stream) {
-  const bool tc = p.batch.max_q_len >= kTcMinRows && tc_score_supported(p.index_heads, p.index_dim);
+  // (bf16 keys only: an FP8 cache would need FP8 queries for the f8 MMA kinds)
+  const bool tc = !p.idx_fp8 && p.batch.max_q_len >= kTcMinRows &&
+                  tc_score_supported(p.index_heads, p.index_dim);
   p.tc_min_rows = tc ? kTcMinRows : 0;
   cudaError_t e = launch_index_score(p, stream);
   if (e != cudaSuccess || !tc) return e;
@@ -186,22 +196,24 @@ size_t msa_workspace_size(int32_t num_rows, int32_t bt_stride, int32_t topk, int
   return decode_layout(num_rows, bt_stride, topk, splits).total;
 }
 
-msa_status msa_index_score(const msa_batch* batch, const void* idx_q, const void* idx_k_cache,
-                           int32_t index_heads, int32_t index_dim, float* scores,
-                           int32_t score_stride, uint32_t* dev_status, cudaStream_t stream) {
+msa_status msa_index_score(const msa_batch* batch, const void* idx_q,
+                           const msa_index_cache* index, float* scores, int32_t score_stride,
+                           uint32_t* dev_status, cudaStream_t stream) {
   msa_status st = check_batch(batch);
   if (st != MSA_OK) return st;
-  if (!dev_status || (batch->num_rows > 0 && (!idx_q || !idx_k_cache || !scores)))
+  st = check_index(index);
+  if (st != MSA_OK) return st;
+  if (!dev_status || (batch->num_rows > 0 && (!idx_q || !index->k_cache || !scores)))
     return MSA_ERR_NULL;
-  if (!((index_heads == 1 && (index_dim == 64 || index_dim == 128)) ||
-        (index_heads == 2 && index_dim == 64)))
-    return MSA_ERR_UNSUPPORTED;
   if (score_stride < batch->bt_stride) return MSA_ERR_SHAPE;
-  if (!aligned16(idx_q) || !aligned16(idx_k_cache)) return MSA_ERR_SHAPE;
+  if (!aligned16(idx_q) || !aligned16(index->k_cache) ||
+      (index->k_scale && !aligned16(index->k_scale)))
+    return MSA_ERR_SHAPE;
   if (batch->num_rows == 0 || batch->num_reqs == 0) return MSA_OK;
   ScoreLaunch p{*batch, static_cast<const uint16_t*>(idx_q),
-                static_cast<const uint8_t*>(idx_k_cache), index_heads, index_dim, scores,
-                score_stride, dev_status, 0};
+                static_cast<const uint8_t*>(index->k_cache), index->heads, index->dim, scores,
+                score_stride, dev_status, 0, index->dtype == MSA_KV_FP8_E4M3,
+                index->dtype == MSA_KV_FP8_E4M3 ? index->k_scale : nullptr};
   return cuda_status(launch_scores(p, stream));
 }
 
@@ -247,9 +259,8 @@ msa_status msa_sparse_paged_attn(const msa_attn_args* attn, const int32_t* spars
   return cuda_status(launch_sparse_attn(p, stream, false));
 }
 
-msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx_k_cache,
-                      int32_t index_heads, int32_t index_dim, int32_t topk,
-                      const msa_attn_args* attn, int32_t* topk_idx, int32_t* sparse_tbl,
+msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index_cache* index,
+                      int32_t topk, const msa_attn_args* attn, int32_t* topk_idx, int32_t* sparse_tbl,
                       int32_t tbl_stride, int32_t* sparse_len, void* workspace,
                       size_t workspace_bytes, uint32_t* dev_status, const msa_trace* trace,
                       cudaStream_t stream) {
@@ -262,14 +273,15 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
   if (topk > kMaxTopk) return MSA_ERR_UNSUPPORTED;
   if (attn->num_rows != batch->num_rows) return MSA_ERR_SHAPE;
   if (attn->num_pages != batch->num_pages) return MSA_ERR_SHAPE;
-  if (!((index_heads == 1 && (index_dim == 64 || index_dim == 128)) ||
-        (index_heads == 2 && index_dim == 64)))
-    return MSA_ERR_UNSUPPORTED;
+  st = check_index(index);
+  if (st != MSA_OK) return st;
   if (sparse_tbl && tbl_stride < 8 * topk) return MSA_ERR_SHAPE;
   if (batch->num_rows == 0) return MSA_OK;
   if (batch->num_reqs == 0) return MSA_ERR_SHAPE;
-  if (!idx_q || !idx_k_cache) return MSA_ERR_NULL;
-  if (!aligned16(idx_q) || !aligned16(idx_k_cache)) return MSA_ERR_SHAPE;
+  if (!idx_q || !index->k_cache) return MSA_ERR_NULL;
+  if (!aligned16(idx_q) || !aligned16(index->k_cache) ||
+      (index->k_scale && !aligned16(index->k_scale)))
+    return MSA_ERR_SHAPE;
   const size_t need = msa_workspace_size(batch->num_rows, batch->bt_stride, topk,
                                          attn->num_heads, attn->head_dim, 8 * topk);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return MSA_ERR_WORKSPACE;
@@ -287,8 +299,9 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
   int32_t* len = sparse_len ? sparse_len : reinterpret_cast<int32_t*>(ws + L.len);
 
   ScoreLaunch sp{*batch, static_cast<const uint16_t*>(idx_q),
-                 static_cast<const uint8_t*>(idx_k_cache), index_heads, index_dim, scores,
-                 batch->bt_stride, dev_status, 0};
+                 static_cast<const uint8_t*>(index->k_cache), index->heads, index->dim, scores,
+                 batch->bt_stride, dev_status, 0, index->dtype == MSA_KV_FP8_E4M3,
+                 index->dtype == MSA_KV_FP8_E4M3 ? index->k_scale : nullptr};
   cudaError_t e = launch_scores(sp, stream);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_score) cudaEventRecord(trace->after_score, stream);
@@ -309,43 +322,48 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
 }
 
 msa_status msa_kv_insert(const msa_batch* batch, const void* k_new, const void* v_new,
-                         const void* idx_new, int32_t num_kv_heads, int32_t head_dim,
-                         int32_t index_heads, int32_t index_dim, void* k_cache, void* v_cache,
-                         void* idx_k_cache, int32_t kv_dtype, int32_t scale_mode, float* k_scale,
-                         float* v_scale, int32_t skip_index, uint32_t* dev_status,
-                         cudaStream_t stream) {
+                         int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
+                         int32_t kv_dtype, int32_t scale_mode, float* k_scale, float* v_scale,
+                         const void* idx_new, const msa_index_cache* index, int32_t skip_index,
+                         uint32_t* dev_status, cudaStream_t stream) {
   msa_status st = check_batch(batch);
   if (st != MSA_OK) return st;
   if (!dev_status) return MSA_ERR_NULL;
   if (kv_dtype != MSA_KV_BF16 && kv_dtype != MSA_KV_FP8_E4M3) return MSA_ERR_DTYPE;
   if (scale_mode < MSA_SCALE_NONE || scale_mode > MSA_SCALE_PER_TOKEN_HEAD) return MSA_ERR_DTYPE;
-  if (num_kv_heads < 1 || index_heads < 1 || index_dim < 1) return MSA_ERR_SHAPE;
-  if (head_dim != kHeadDim || (index_heads * index_dim) % 4 != 0) return MSA_ERR_UNSUPPORTED;
+  if (num_kv_heads < 1) return MSA_ERR_SHAPE;
+  if (head_dim != kHeadDim) return MSA_ERR_UNSUPPORTED;
+  if (!skip_index) {
+    st = check_index(index);
+    if (st != MSA_OK) return st;
+  }
   if (batch->num_rows == 0) return MSA_OK;
   if (batch->num_reqs == 0) return MSA_ERR_SHAPE;
   if (!k_new || !v_new || !k_cache || !v_cache) return MSA_ERR_NULL;
-  if (!skip_index && (!idx_new || !idx_k_cache)) return MSA_ERR_NULL;
+  if (!skip_index && (!idx_new || !index->k_cache)) return MSA_ERR_NULL;
   const bool fp8 = kv_dtype == MSA_KV_FP8_E4M3;
   if (fp8 && scale_mode != MSA_SCALE_NONE && (!k_scale || !v_scale)) return MSA_ERR_NULL;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
     return MSA_ERR_SHAPE;
-  if (!skip_index && (!aligned16(idx_new) || !aligned16(idx_k_cache))) return MSA_ERR_SHAPE;
+  if (!skip_index && (!aligned16(idx_new) || !aligned16(index->k_cache))) return MSA_ERR_SHAPE;
   KvInsertLaunch p;
   p.batch = *batch;
   p.k_new = static_cast<const uint16_t*>(k_new);
   p.v_new = static_cast<const uint16_t*>(v_new);
   p.idx_new = static_cast<const uint16_t*>(idx_new);
   p.num_kv_heads = num_kv_heads;
-  p.index_heads = index_heads;
-  p.index_dim = index_dim;
+  p.index_heads = skip_index ? 0 : index->heads;
+  p.index_dim = skip_index ? 0 : index->dim;
   p.k_cache = static_cast<uint8_t*>(k_cache);
   p.v_cache = static_cast<uint8_t*>(v_cache);
-  p.idx_k_cache = static_cast<uint16_t*>(idx_k_cache);
+  p.idx_k_cache = skip_index ? nullptr : static_cast<uint16_t*>(index->k_cache);
   p.kv_fp8 = fp8;
   p.scale_mode = fp8 ? scale_mode : MSA_SCALE_NONE;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.skip_index = skip_index != 0;
+  p.idx_fp8 = !skip_index && index->dtype == MSA_KV_FP8_E4M3;
+  p.idx_scale = p.idx_fp8 ? index->k_scale : nullptr;
   p.status = dev_status;
   return cuda_status(launch_kv_insert(p, stream));
 }

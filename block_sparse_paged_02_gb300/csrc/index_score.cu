@@ -34,29 +34,41 @@ namespace {
 
 constexpr int kRowGroup = 4;
 
-template <int DI, int HI>
+// Scoring kinds: bf16 keys on CUDA-core FMAs, bf16 keys on warp MMA, OCP
+// e4m3 keys on warp MMA (fp16 operands).
+enum { kFmaBf16 = 0, kMmaBf16 = 1, kMmaFp8 = 2 };
+
+template <int DI, int HI, int KIND>
 struct ScoreCfg {
+  static constexpr int kElem = KIND == kMmaFp8 ? 1 : 2;
   static constexpr int kSubRowBytes = DI * 2;
-  static constexpr int kChunks = DI / 8;  // 16-byte chunks per sub-row
-  static constexpr int kPageBytes = kBlock * HI * DI * 2;
-  static constexpr int kStages = kPageBytes >= 32768 ? 6 : 12;  // 192 KB of stages
+  static constexpr int kChunks = DI / 8;  // 16-byte chunks per bf16 sub-row
+  static constexpr int kPageBytes = kBlock * HI * DI * kElem;
+  // query rows scored per pass: 4 on FMAs, 8 (index heads) columns on MMA
+  static constexpr int kRows = KIND == kFmaBf16 ? kRowGroup : 8 / HI;
+  static constexpr int kQBytes = kRows * HI * DI * 2;  // query rows staged with a page
+  static constexpr int kScaleBytes = KIND == kMmaFp8 ? kBlock * HI * 4 : 0;  // per-token scales
+  // stages within 200 KB (the rest holds barriers and the request prefix):
+  // 6 for 32 KB pages, 10-12 for 16 KB ones
+  static constexpr int kStageBytes = kPageBytes + kQBytes + kScaleBytes;
+  static constexpr int kStages = 204800 / kStageBytes < 12 ? 204800 / kStageBytes : 12;
   // one consumer warp per stage (a pair of warps per page measured slower:
   // more instructions without more bytes in flight)
   static constexpr int kSubPerLane = kBlock * HI / 32;
   static constexpr int kThreads = 32 * (1 + kStages);
-  static constexpr int kQBytes = kRowGroup * HI * DI * 2;  // query rows staged with a page
 };
 
 struct StageInfo {  // written by the producer before it arms the stage
   int req, blk, valid, q0, qlen, ctx, jstart, pad;
 };
 
-template <int DI, int HI>
+template <int DI, int HI, int KIND>
 struct ScoreSmem {
-  using C = ScoreCfg<DI, HI>;
+  using C = ScoreCfg<DI, HI, KIND>;
   static constexpr size_t kPages = 0;
   static constexpr size_t kQ = kPages + (size_t)C::kStages * C::kPageBytes;
-  static constexpr size_t kBars = kQ + (size_t)C::kStages * C::kQBytes;
+  static constexpr size_t kScale = kQ + (size_t)C::kStages * C::kQBytes;
+  static constexpr size_t kBars = kScale + (size_t)C::kStages * C::kScaleBytes;
   static constexpr size_t kInfo = kBars + 2 * C::kStages * sizeof(uint64_t);
   static constexpr size_t kMisc = kInfo + C::kStages * sizeof(StageInfo);
   static constexpr size_t kPrefix = kMisc + 64;
@@ -69,7 +81,7 @@ template <int DI, int HI, int NR>
 __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q_s, int lane,
                                            int blk, const int (&pos)[kRowGroup],
                                            float (&out)[kRowGroup]) {
-  using C = ScoreCfg<DI, HI>;
+  using C = ScoreCfg<DI, HI, kFmaBf16>;
   float acc[C::kSubPerLane][NR];
 #pragma unroll
   for (int j = 0; j < C::kSubPerLane; ++j)
@@ -127,11 +139,137 @@ __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q
   }
 }
 
-template <int DI, int HI>
-__global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
+__device__ __forceinline__ uint2 lds64(const void* p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
+
+// Scores of one staged page on warp MMA: S^T = K Q^T with m16n8k16 tiles of
+// 16 (token, head) sub-rows x 8 columns (query row, index head) x 16 dims,
+// fp32 accumulation; e4m3 keys enter as their exact fp16 images and the
+// queries as fp16, bf16 keys and queries as they are.  Lane (g, c) holds, for
+// k-step kk, the dims c*DI/4 + 4kk + {0..3} of its rows (the same k-slot
+// permutation on both operands), so each sub-row span is a contiguous read.
+// Then, per column, the masked maximum over the block's tokens of
+// scale_t * S (a column only sees sub-rows of its own head).  Returns in
+// best[0..8/HI) the block score of each query row (all lanes).
+template <int DI, int HI, bool F8>
+__device__ __forceinline__ void score_page_mma(const uint8_t* page, const float* tscale,
+                                               const uint8_t* q_s, int nr, int lane, int blk,
+                                               const int (&pos)[8], float (&best)[8]) {
+  constexpr int kK = DI / 16;                 // k-steps
+  constexpr int kD4 = DI / 4;                 // dims of a lane per sub-row
+  constexpr int kElem = F8 ? 1 : 2;
+  constexpr int kRowB = DI * kElem;           // bytes per sub-row
+  constexpr int kSpanW = kD4 * kElem / 4;     // 32-bit words of a lane's span
+  constexpr int kSpanC = kSpanW / 4;          // 16-byte chunks of a lane's span
+  constexpr int kMt = kBlock * HI / 16;       // m-tiles
+  const int g = lane >> 2, c = lane & 3;
+  // B: column g = (query row g / HI, index head g % HI)
+  uint32_t bq[kK][2];
+  {
+    const int r = g / HI, h = g % HI;
+    const uint8_t* qrow = q_s + ((r * HI + h) * DI + c * kD4) * 2;
+#pragma unroll
+    for (int kk = 0; kk < kK; ++kk) {
+      uint2 w = make_uint2(0u, 0u);
+      if (r < nr) w = lds64(qrow + 8 * kk);
+      if constexpr (F8) {
+        bq[kk][0] = pack_f16x2(bf16lo(w.x), bf16hi(w.x));
+        bq[kk][1] = pack_f16x2(bf16lo(w.y), bf16hi(w.y));
+      } else {
+        bq[kk][0] = w.x;
+        bq[kk][1] = w.y;
+      }
+    }
+  }
+  // the lane's two columns: their query row, head and last visible token
+  int lim[2], hcol[2];
+  bool live[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int col = 2 * c + k, r = col / HI;
+    int pr = pos[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+      if (i == r) pr = pos[i];
+    live[k] = r < nr;
+    lim[k] = pr - blk * kBlock;  // tokens t <= lim are visible
+    hcol[k] = col % HI;
+  }
+  float m[2] = {-INFINITY, -INFINITY};
+#pragma unroll 2
+  for (int mt = 0; mt < kMt; ++mt) {
+    uint32_t w[2][kSpanW];  // spans of sub-rows 16mt + g and 16mt + g + 8
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const uint8_t* row = page + (16 * mt + g + 8 * half) * kRowB + c * kD4 * kElem;
+#pragma unroll
+      for (int i = 0; i < kSpanC; ++i) {
+        const int ch = (i + g) % kSpanC;  // rotated: rows 128 B apart hit other banks
+        const uint4 v = lds128(row + 16 * ch);
+        // (a constant-index store after the loop keeps w in registers)
+#pragma unroll
+        for (int x = 0; x < kSpanC; ++x)
+          if (x == ch) {
+            w[half][4 * x] = v.x;
+            w[half][4 * x + 1] = v.y;
+            w[half][4 * x + 2] = v.z;
+            w[half][4 * x + 3] = v.w;
+          }
+      }
+    }
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < kK; ++kk) {
+      uint32_t a[4];
+      if constexpr (F8) {
+        a[0] = e4m3x2_to_f16x2((uint16_t)(w[0][kk] & 0xffffu));
+        a[1] = e4m3x2_to_f16x2((uint16_t)(w[1][kk] & 0xffffu));
+        a[2] = e4m3x2_to_f16x2((uint16_t)(w[0][kk] >> 16));
+        a[3] = e4m3x2_to_f16x2((uint16_t)(w[1][kk] >> 16));
+      } else {
+        a[0] = w[0][2 * kk];
+        a[1] = w[1][2 * kk];
+        a[2] = w[0][2 * kk + 1];
+        a[3] = w[1][2 * kk + 1];
+      }
+      mma16816<F8>(d, a, bq[kk][0], bq[kk][1]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int sr = 16 * mt + g + 8 * (e >> 1);  // sub-row = token * HI + head
+      const int k = e & 1;
+      float v = d[e];
+      if (tscale) v *= tscale[sr];
+      const bool ok = live[k] && (sr % HI) == hcol[k] && sr / HI <= lim[k];
+      if (ok) m[k] = fmaxf(m[k], v);  // NaN never wins
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) m[k] = fmaxf(m[k], __shfl_xor_sync(0xffffffffu, m[k], o));
+  // lane c now holds columns 2c, 2c+1; gather the rows
+#pragma unroll
+  for (int r = 0; r < 8 / HI; ++r) {
+    if constexpr (HI == 1) {
+      const float a0 = __shfl_sync(0xffffffffu, m[0], r >> 1);
+      const float a1 = __shfl_sync(0xffffffffu, m[1], r >> 1);
+      best[r] = (r & 1) ? a1 : a0;
+    } else {
+      best[r] = fmaxf(__shfl_sync(0xffffffffu, m[0], r), __shfl_sync(0xffffffffu, m[1], r));
+    }
+  }
+}
+
+template <int DI, int HI, int KIND>
+__global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
     index_score_kernel(const ScoreLaunch p) {
-  using C = ScoreCfg<DI, HI>;
-  using S = ScoreSmem<DI, HI>;
+  using C = ScoreCfg<DI, HI, KIND>;
+  using S = ScoreSmem<DI, HI, KIND>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
   uint64_t* empty = full + C::kStages;
@@ -228,8 +366,12 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
       const int s = j % C::kStages;
       info[s] = si;
       if (si.valid) {
-        const uint32_t qb = (uint32_t)min(kRowGroup, si.qlen - si.jstart) * HI * DI * 2;
-        mbar_arrive_expect_tx(&full[s], C::kPageBytes + qb);
+        const uint32_t qb = (uint32_t)min(C::kRows, si.qlen - si.jstart) * HI * DI * 2;
+        const uint32_t sb = (KIND == kMmaFp8 && p.idx_scale) ? (uint32_t)C::kScaleBytes : 0u;
+        mbar_arrive_expect_tx(&full[s], C::kPageBytes + qb + sb);
+        if (sb)
+          bulk_g2s(smem + S::kScale + (size_t)s * C::kScaleBytes,
+                   p.idx_scale + (long long)page * kBlock * HI, sb, &full[s]);
         bulk_g2s(smem + S::kQ + (size_t)s * C::kQBytes,
                  p.idx_q + (long long)(si.q0 + si.jstart) * HI * DI, qb, &full[s]);
         bulk_g2s(smem + S::kPages + (size_t)s * C::kPageBytes,
@@ -289,12 +431,12 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
     const int q0 = si.q0, qlen = si.qlen, ctx = si.ctx;
     bool wrote_q = false;
     // rows j >= jstart (ctx + j >= 128*blk) can see this block
-    for (int g0 = si.jstart; g0 < qlen; g0 += kRowGroup) {
-      const int nr = min(kRowGroup, qlen - g0);
-      int pos[kRowGroup];
+    for (int g0 = si.jstart; g0 < qlen; g0 += C::kRows) {
+      const int nr = min(C::kRows, qlen - g0);
+      int pos[8];
 #pragma unroll
-      for (int r = 0; r < kRowGroup; ++r) pos[r] = ctx + g0 + min(r, nr - 1);
-      float best[kRowGroup];
+      for (int r = 0; r < 8; ++r) pos[r] = ctx + g0 + min(r, nr - 1);
+      float best[8];
       if (si.valid) {
         if (g0 != si.jstart) {  // later row groups (requests with > 4 rows): from global
           __syncwarp();
@@ -306,18 +448,32 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
           __syncwarp();
           wrote_q = true;
         }
-        if (nr == 1)
-          score_page<DI, HI, 1>(page, q_s, lane, si.blk, pos, best);
-        else if (nr == 2)
-          score_page<DI, HI, 2>(page, q_s, lane, si.blk, pos, best);
-        else
-          score_page<DI, HI, 4>(page, q_s, lane, si.blk, pos, best);  // rows >= nr unused
+        if constexpr (KIND == kFmaBf16) {
+          int pos4[kRowGroup];
+          float best4[kRowGroup];
+#pragma unroll
+          for (int r = 0; r < kRowGroup; ++r) pos4[r] = pos[r];
+          if (nr == 1)
+            score_page<DI, HI, 1>(page, q_s, lane, si.blk, pos4, best4);
+          else if (nr == 2)
+            score_page<DI, HI, 2>(page, q_s, lane, si.blk, pos4, best4);
+          else
+            score_page<DI, HI, 4>(page, q_s, lane, si.blk, pos4, best4);  // rows >= nr unused
+#pragma unroll
+          for (int r = 0; r < kRowGroup; ++r) best[r] = best4[r];
+        } else {
+          const float* tscale = (KIND == kMmaFp8 && p.idx_scale)
+              ? reinterpret_cast<const float*>(smem + S::kScale + (size_t)st * C::kScaleBytes)
+              : nullptr;
+          score_page_mma<DI, HI, KIND == kMmaFp8>(page, tscale, q_s, nr, lane, si.blk, pos,
+                                                  best);
+        }
       } else {
 #pragma unroll
-        for (int r = 0; r < kRowGroup; ++r) best[r] = -INFINITY;
+        for (int r = 0; r < 8; ++r) best[r] = -INFINITY;
       }
 #pragma unroll
-      for (int r = 0; r < kRowGroup; ++r)
+      for (int r = 0; r < C::kRows; ++r)
         if (lane == r && r < nr)
           p.scores[(long long)(q0 + g0 + r) * p.score_stride + si.blk] = best[r];
     }
@@ -328,11 +484,11 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI>::kThreads, 1)
   }
 }
 
-template <int DI, int HI>
+template <int DI, int HI, int KIND>
 cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
-  using C = ScoreCfg<DI, HI>;
-  const size_t smem = ScoreSmem<DI, HI>::bytes(p.batch.num_reqs);
-  auto kern = index_score_kernel<DI, HI>;
+  using C = ScoreCfg<DI, HI, KIND>;
+  const size_t smem = ScoreSmem<DI, HI, KIND>::bytes(p.batch.num_reqs);
+  auto kern = index_score_kernel<DI, HI, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
@@ -340,13 +496,19 @@ cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int KIND>
+cudaError_t launch_kind(const ScoreLaunch& p, cudaStream_t stream) {
+  if (p.index_heads == 1 && p.index_dim == 128) return launch_cfg<128, 1, KIND>(p, stream);
+  if (p.index_heads == 1 && p.index_dim == 64) return launch_cfg<64, 1, KIND>(p, stream);
+  if (p.index_heads == 2 && p.index_dim == 64) return launch_cfg<64, 2, KIND>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream) {
-  if (p.index_heads == 1 && p.index_dim == 128) return launch_cfg<128, 1>(p, stream);
-  if (p.index_heads == 1 && p.index_dim == 64) return launch_cfg<64, 1>(p, stream);
-  if (p.index_heads == 2 && p.index_dim == 64) return launch_cfg<64, 2>(p, stream);
-  return cudaErrorInvalidValue;
+  if (p.idx_fp8) return launch_kind<kMmaFp8>(p, stream);
+  return launch_kind<MSA_SCORE_BF16_KIND>(p, stream);
 }
 
 }  // namespace msa

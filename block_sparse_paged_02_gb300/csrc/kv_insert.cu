@@ -14,7 +14,9 @@
 //
 // One warp per row: lanes own 4 consecutive head dims; the amax is a warp
 // max-reduce; division is IEEE fp32 and the codes come from the hardware
-// round-to-nearest-even, saturating e4m3 conversion.
+// round-to-nearest-even, saturating e4m3 conversion.  An FP8 index cache is
+// written the same way per token and index head (the per-token-head rule when
+// its scales are kept, scale 1 otherwise).
 #include "msa_internal.cuh"
 
 namespace msa {
@@ -106,7 +108,34 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) kv_insert_kernel(const KvIn
     insert_vector(p.v_new + src, p.v_cache, dst, p.kv_fp8, p.scale_mode, p.v_scale, p.v_scale,
                   sat, lane);
   }
-  if (!p.skip_index) {
+  if (!p.skip_index && p.idx_fp8) {
+    // e4m3 index keys per (token, index head); index_dim 64 or 128, so each
+    // lane owns 2 or 4 consecutive dims
+    for (int h = 0; h < p.index_heads; ++h) {
+      const long long sat = token * p.index_heads + h;
+      const uint16_t* src = p.idx_new + ((long long)r * p.index_heads + h) * p.index_dim;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.idx_k_cache) + sat * p.index_dim;
+      if (p.index_dim == 128) {
+        insert_vector(src, dst, 0, 1, p.idx_scale ? MSA_SCALE_PER_TOKEN_HEAD : MSA_SCALE_NONE,
+                      nullptr, p.idx_scale, sat, lane);
+      } else {
+        const uint32_t raw = *reinterpret_cast<const uint32_t*>(src + 2 * lane);
+        const float x0 = bf16lo(raw), x1 = bf16hi(raw);
+        float s = 1.f;
+        if (p.idx_scale) {
+          float amax = fmaxf(fabsf(x0), fabsf(x1));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+          if (lane == 0) p.idx_scale[sat] = s;
+        }
+        uint16_t code;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+            : "=h"(code) : "f"(__fdiv_rn(x1, s)), "f"(__fdiv_rn(x0, s)));
+        *reinterpret_cast<uint16_t*>(dst + 2 * lane) = code;
+      }
+    }
+  } else if (!p.skip_index) {
     const int n = p.index_heads * p.index_dim;  // bf16 elements, a multiple of 4
     const uint2* src = reinterpret_cast<const uint2*>(p.idx_new + (long long)r * n);
     uint2* dst = reinterpret_cast<uint2*>(p.idx_k_cache + token * n);

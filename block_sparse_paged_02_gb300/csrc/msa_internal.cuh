@@ -41,6 +41,10 @@ constexpr int kMaxSplitEntries = 128;
 #ifndef MSA_ATTN_CTAS_BF16
 #define MSA_ATTN_CTAS_BF16 2
 #endif
+// bf16 index keys: scored on CUDA-core FMAs (0) or on warp MMA (1)
+#ifndef MSA_SCORE_BF16_KIND
+#define MSA_SCORE_BF16_KIND 0
+#endif
 // bounded waits: a wait that has not completed after this long gives up
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
 
@@ -217,6 +221,8 @@ struct ScoreLaunch {
   int score_stride;
   uint32_t* status;
   int tc_min_rows;  // > 0: requests with q_len >= this are left to the tensor-core kernel
+  int idx_fp8;              // index keys are OCP e4m3 codes
+  const float* idx_scale;   // FP8: per-token scales [P, 128, Hi], or null (1)
 };
 
 struct TopkLaunch {
@@ -272,6 +278,8 @@ struct KvInsertLaunch {
   float* k_scale;
   float* v_scale;
   int skip_index;
+  int idx_fp8;        // index cache of e4m3 codes
+  float* idx_scale;   // FP8 index: per-token scales written here, or null (scale 1)
   uint32_t* status;
 };
 

@@ -150,25 +150,44 @@ typedef struct msa_trace {
   cudaEvent_t after_attn;
 } msa_trace;
 
+/* The paged index-K cache, the keys of step 1 [P54682 "Implementation
+ * breakdown" item 1; the optional FP8 index storage and FP8 index scoring of
+ * its "Related context"].
+ *   k_cache  [P, 128, heads, dim], paged like the KV pools (token t of a
+ *            request at page block_table[q, t/128], slot t%128):
+ *            dtype MSA_KV_BF16: bf16 values;
+ *            dtype MSA_KV_FP8_E4M3: OCP e4m3 codes, the key being
+ *            k_scale[page, slot, h] * code (k_scale may be NULL: scale 1)
+ *   k_scale  fp32 [P, 128, heads] (FP8 only)
+ *   heads, dim  supported: (1, 64), (2, 64), (1, 128)
+ * Score and decode only read the cache; msa_kv_insert writes it. */
+typedef struct msa_index_cache {
+  void* k_cache;
+  float* k_scale;
+  int32_t dtype;
+  int32_t heads;
+  int32_t dim;
+} msa_index_cache;
+
 /* Step 1, index scoring [P54682 "Implementation breakdown" item 1; the
  * balanced scorer of "Key files" that maps work by each request's actual
  * block count and shares index-K tiles across a request's query rows].
  * For each row r (request q, position pos) and block b < nb_r =
  * ceil((pos+1)/128):
  *     scores[r*score_stride + b] = max over index heads h and tokens
- *         t in [128b, min(128b+127, pos)] of  sum_d idx_q[r,h,d]*idx_k[t,h,d]
- * with idx_k addressed through the block table (token t of the request
- * lives at page block_table[q, t/128], slot t%128), accumulated in fp32.
- *   idx_q       [num_rows, index_heads, index_dim] bf16
- *   idx_k_cache [P, 128, index_heads, index_dim] bf16
- *   scores      [num_rows, score_stride] fp32; score_stride >= bt_stride.
- *               Entries b >= nb_r, and rows of poisoned requests, are not
- *               written; a block whose page id is out of range scores -inf.
- * Supported (index_heads, index_dim): (1, 64), (2, 64), (1, 128);
- * num_reqs <= 4096. */
-msa_status msa_index_score(const msa_batch* batch, const void* idx_q, const void* idx_k_cache,
-                           int32_t index_heads, int32_t index_dim, float* scores,
-                           int32_t score_stride, uint32_t* dev_status, cudaStream_t stream);
+ *         t in [128b, min(128b+127, pos)] of  sum_d idx_q[r,h,d]*key[t,h,d]
+ * with key[t,h,d] from the index cache (FP8: scale[t,h] * code), the sum in
+ * fp32 (FP8: the products of the exact fp16 images of q and the code, then
+ * times the scale).
+ *   idx_q    [num_rows, heads, dim] bf16 (FP8 cache: converted to fp16 for
+ *            the tensor-core products, so |idx_q| must stay below 65504)
+ *   scores   [num_rows, score_stride] fp32; score_stride >= bt_stride.
+ *            Entries b >= nb_r, and rows of poisoned requests, are not
+ *            written; a block whose page id is out of range scores -inf.
+ * Supported: the index shapes above; num_reqs <= 4096. */
+msa_status msa_index_score(const msa_batch* batch, const void* idx_q,
+                           const msa_index_cache* index, float* scores, int32_t score_stride,
+                           uint32_t* dev_status, cudaStream_t stream);
 
 /* Steps 2+3, top-k selection fused with the page-16 table build and the
  * context-length clamp [P54682 "Implementation breakdown" items 1 and 4;
@@ -249,9 +268,8 @@ msa_status msa_sparse_paged_attn_static(const msa_attn_args* attn, const int32_t
  * (kept in the workspace) or device arrays that receive them; tbl_stride is
  * the width of the caller's sparse_tbl (>= 8*topk, ignored when NULL).
  * trace may be NULL. */
-msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx_k_cache,
-                      int32_t index_heads, int32_t index_dim, int32_t topk,
-                      const msa_attn_args* attn, int32_t* topk_idx, int32_t* sparse_tbl,
+msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index_cache* index,
+                      int32_t topk, const msa_attn_args* attn, int32_t* topk_idx, int32_t* sparse_tbl,
                       int32_t tbl_stride, int32_t* sparse_len, void* workspace,
                       size_t workspace_bytes, uint32_t* dev_status, const msa_trace* trace,
                       cudaStream_t stream);
@@ -264,22 +282,23 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const void* idx
  * vectors go to page block_table[q, pos/128], slot pos%128 (the q/k norm and
  * RoPE need model weights and stay with the caller).
  *   k_new, v_new [num_rows, num_kv_heads, head_dim] bf16
- *   idx_new      [num_rows, index_heads, index_dim] bf16 (unused if skip_index)
  *   k_cache, v_cache  pools [P, 128, num_kv_heads, head_dim] of kv_dtype
- *   idx_k_cache  [P, 128, index_heads, index_dim] bf16
+ *   idx_new      [num_rows, index->heads, index->dim] bf16
+ *   index        the index cache (may be NULL when skip_index)
  * FP8 pools store OCP e4m3 codes of x / s (IEEE fp32 division, round to
  * nearest even, saturating to +-448): SCALAR takes s = k_scale[0] (v_scale[0])
  * as input; PER_TOKEN_HEAD sets s = max_d |x_d| / 448 per token and KV head
  * (1 for an all-zero vector) and writes it to k_scale / v_scale [P, 128,
- * num_kv_heads] at the slot; NONE takes s = 1.  bf16 pools take a copy.
- * Rows of requests that fail the device checks (MSA_DEV_BAD_PAGE, _BAD_LEN,
- * _MALFORMED) are not written.  Supported: head_dim == 128. */
+ * num_kv_heads] at the slot; NONE takes s = 1.  bf16 pools take a copy.  An
+ * FP8 index cache is written the same way, per token and index head, with
+ * the PER_TOKEN_HEAD rule when index->k_scale is given and s = 1 when it is
+ * NULL.  Rows of requests that fail the device checks (MSA_DEV_BAD_PAGE,
+ * _BAD_LEN, _MALFORMED) are not written.  Supported: head_dim == 128. */
 msa_status msa_kv_insert(const msa_batch* batch, const void* k_new, const void* v_new,
-                         const void* idx_new, int32_t num_kv_heads, int32_t head_dim,
-                         int32_t index_heads, int32_t index_dim, void* k_cache, void* v_cache,
-                         void* idx_k_cache, int32_t kv_dtype, int32_t scale_mode, float* k_scale,
-                         float* v_scale, int32_t skip_index, uint32_t* dev_status,
-                         cudaStream_t stream);
+                         int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
+                         int32_t kv_dtype, int32_t scale_mode, float* k_scale, float* v_scale,
+                         const void* idx_new, const msa_index_cache* index, int32_t skip_index,
+                         uint32_t* dev_status, cudaStream_t stream);
 
 /* Bytes of workspace msa_decode (bt_stride > 0) or msa_sparse_paged_attn
  * (bt_stride = 0, topk = 0) needs for these sizes. */

@@ -54,5 +54,6 @@ def sub_workload(w, rows):
                      idx_q=w.idx_q[rows], idx_k=w.idx_k, topk=w.topk, q=w.q[rows],
                      k_cache=w.k_cache, v_cache=w.v_cache, kv_dtype=w.kv_dtype,
                      scale_mode=w.scale_mode, k_scale=w.k_scale, v_scale=w.v_scale,
-                     sinks=w.sinks, softmax_scale=w.softmax_scale, seed=w.seed)
+                     sinks=w.sinks, softmax_scale=w.softmax_scale, seed=w.seed,
+                     index_dtype=w.index_dtype, idx_k_scale=w.idx_k_scale)
     return sub

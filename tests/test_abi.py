@@ -53,21 +53,28 @@ def test_workspace_size_grows_with_rows(lib):
 def test_host_validation_without_gpu(lib):
     from block_sparse_paged_02_gb300 import binding as B
     # NULL batch / NULL args are rejected before any launch
-    assert lib.msa_index_score(None, None, None, 1, 128, None, 1, None, None) == B.MSA_ERR_NULL
+    assert lib.msa_index_score(None, None, None, None, 1, None, None) == B.MSA_ERR_NULL
     assert lib.msa_topk_build_table(None, None, 1, 4, None, None, 32, None, None, None) == \
         B.MSA_ERR_NULL
     assert lib.msa_sparse_paged_attn(None, None, 32, None, None, 0, None, None) == B.MSA_ERR_NULL
-    b = B.msa_batch(None, None, None, None, 4, 1, 1, 10)
-    assert lib.msa_index_score(ctypes.byref(b), None, None, 1, 128, None, 4, None, None) == \
-        B.MSA_ERR_NULL
     fake = ctypes.c_void_p(0x10000)
+    idx = lambda **kw: B.msa_index_cache(**{**dict(k_cache=fake, k_scale=None, dtype=0, heads=1,
+                                                    dim=128), **kw})
+    b = B.msa_batch(None, None, None, None, 4, 1, 1, 10)
+    assert lib.msa_index_score(ctypes.byref(b), None, ctypes.byref(idx()), None, 4, None,
+                               None) == B.MSA_ERR_NULL
     b = B.msa_batch(fake, fake, fake, fake, 4, 1, 1, 10)
     st = ctypes.c_void_p(0x20000)
-    # unsupported index geometry, score stride below the block-table width
-    assert lib.msa_index_score(ctypes.byref(b), fake, fake, 3, 128, fake, 4, st, None) == \
-        B.MSA_ERR_UNSUPPORTED
-    assert lib.msa_index_score(ctypes.byref(b), fake, fake, 1, 128, fake, 3, st, None) == \
-        B.MSA_ERR_SHAPE
+    score = lambda x, stride=4: lib.msa_index_score(ctypes.byref(b), fake, ctypes.byref(x), fake,
+                                                    stride, st, None)
+    # no index cache; unsupported index geometry or dtype; score stride below
+    # the block-table width; a misaligned FP8 scale array
+    assert lib.msa_index_score(ctypes.byref(b), fake, None, fake, 4, st, None) == B.MSA_ERR_NULL
+    assert score(idx(heads=3)) == B.MSA_ERR_UNSUPPORTED
+    assert score(idx(dim=96)) == B.MSA_ERR_UNSUPPORTED
+    assert score(idx(dtype=5)) == B.MSA_ERR_DTYPE
+    assert score(idx(), stride=3) == B.MSA_ERR_SHAPE
+    assert score(idx(dtype=1, k_scale=ctypes.c_void_p(0x10008))) == B.MSA_ERR_SHAPE
     # table narrower than 8*topk
     assert lib.msa_topk_build_table(ctypes.byref(b), fake, 4, 4, fake, fake, 31, fake, st,
                                     None) == B.MSA_ERR_SHAPE

@@ -77,3 +77,34 @@ def test_kv_insert_skips_invalid_requests(msa, orc):
     assert st == orc.BAD_PAGE
     assert np.array_equal(c.k.view(torch.int16).cpu().numpy().view(np.uint16), k)
     assert (c.k != before).any()  # request 0 was written
+
+
+@pytest.mark.parametrize("hi,di", [(1, 64), (2, 64), (1, 128)])
+@pytest.mark.parametrize("scaled", [True, False])
+def test_kv_insert_fp8_index_cache(msa, orc, hi, di, scaled):
+    # e4m3 index keys (+ per-token scales) written byte for byte as the oracle
+    # writes them, then a decode that scores the new keys
+    base = W.custom(94, q_lens=[1, 3, 1], seq_lens=[2000, 300, 129], hq=8, di=di, hi=hi, topk=4)
+    w = W.fp8_index(base, seed=95, scaled=scaled)
+    rng = np.random.default_rng(6)
+    k_new = W.bf16_bits(rng.standard_normal((w.num_rows, 1, 128)))
+    v_new = W.bf16_bits(rng.standard_normal((w.num_rows, 1, 128)))
+    idx_new = W.bf16_bits(rng.integers(-3, 4, (w.num_rows, hi, di)).astype(np.float32))
+    c = msa.DeviceCase(w)
+    c.kv_insert(_dev(k_new), _dev(v_new), _dev(idx_new))
+    torch.cuda.synchronize()
+    assert int(c.status.item()) == 0
+    res = orc.kv_insert(w, k_new, v_new, idx_new)
+    ik, st, iscale = res[2], res[5], res[6]
+    assert st == 0
+    assert np.array_equal(c.idx_k.cpu().numpy(), ik)
+    if scaled:
+        assert np.array_equal(c.idx_k_scale.cpu().numpy(), iscale)
+    c.decode()
+    got = c.fetch()
+    w.k_cache, w.v_cache, w.idx_k = res[0], res[1], ik
+    w.idx_k_scale = iscale
+    ref = orc.decode(w)
+    for key in ("topk_idx", "tbl", "sparse_len"):
+        assert np.array_equal(got[key], ref[key])
+    assert_attn_close(got["out"], got["lse"], ref["out"], ref["lse"])

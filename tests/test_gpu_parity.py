@@ -63,7 +63,7 @@ def check_against_oracle(orc, w, sep, fused, topk=None):
 
 
 @pytest.mark.parametrize("name", ["tiny_decode", "batched_decode", "speculative_decode",
-                                  "large_batch_decode"])
+                                  "large_batch_decode", "large_batch_decode_fp8_index"])
 def test_named_workload_full_size(msa, orc, name):
     w = W.NAMED[name]()
     _, sep, fused = run_steps(msa, w)
@@ -144,6 +144,27 @@ def test_long_rows_wide_block_tables(msa, orc, seq, idx_range):
     w = W.custom(53, q_lens=[1, 2], seq_lens=[seq, seq // 3], hq=16, di=64, topk=64,
                  idx_range=idx_range)
     assert w.bt_stride > 1024
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+@pytest.mark.parametrize("hi,di", [(1, 64), (2, 64), (1, 128)])
+@pytest.mark.parametrize("scaled", [True, False])
+def test_fp8_index_cache(msa, orc, hi, di, scaled):
+    # e4m3 index keys (+ per-token scales): scores and tables bit-exact
+    w = W.fp8_index(W.custom(60 + hi + di, q_lens=[1, 4, 9, 2], seq_lens=[5000, 2100, 700, 9000],
+                             hq=16, di=di, hi=hi, topk=8, kv_dtype=W.KV_FP8,
+                             scale_mode=W.SCALE_SCALAR, with_sink=True),
+                    seed=61, scaled=scaled)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)  # scores included, bit for bit
+
+
+def test_fp8_index_many_rows_and_garbage(msa, orc):
+    # a request with >= 64 rows (no tensor-core scorer for e4m3 keys) and NaN
+    # codes in every slot no row may see
+    w = W.fp8_index(W.custom(62, q_lens=[70, 1], seq_lens=[3000, 300], hq=8, di=64, topk=4,
+                             fill_unused_nan=True), seed=63)
     _, sep, fused = run_steps(msa, w)
     check_against_oracle(orc, w, sep, fused)
 
@@ -297,8 +318,8 @@ def test_outputs_stay_inside_their_rows(msa):
     eb, lse = guarded(N * 16, torch.float32, 3.0)
     c.attn = msa.make_attn_args(c.q, c.k, c.v, w.kv_dtype, w.num_pages, out.view(N, 16, 128),
                                 lse.view(N, 16), sinks=c.sinks, softmax_scale=w.softmax_scale)
-    msa.msa_decode(c.batch, c.idx_q, c.idx_k, 1, 128, k, c.attn, kidx, tbl, ts, slen,
-                   c.workspace, c.status)
+    msa.msa_decode(c.batch, c.idx_q, c.index, k, c.attn, kidx, tbl, ts, slen, c.workspace,
+                   c.status)
     torch.cuda.synchronize()
     for buf, n, fill in ((tb, N * ts, -7), (kb, N * k, -7), (lb, N, -7), (ob, N * 2048, 3.0),
                          (eb, N * 16, 3.0)):
@@ -314,6 +335,7 @@ def test_empty_batch_is_a_no_op(msa):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     scores = torch.zeros((1, 1), dtype=torch.float32, device=dev)
     q = torch.zeros((1, 1, 64), dtype=torch.bfloat16, device=dev)
-    msa.msa_index_score(b, q, q, 1, 64, scores, 1, status)
+    kc = torch.zeros((1, 128, 1, 64), dtype=torch.bfloat16, device=dev)
+    msa.msa_index_score(b, q, msa.make_index_cache(kc), scores, 1, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0

@@ -590,3 +590,30 @@ def test_kv_insert_fp8_per_token_scale_definition(orc):
             assert np.abs(vals).max() == 448.0  # the largest element lands on the top code
             np.testing.assert_allclose(vals * s, x, rtol=2 ** -4, atol=s * 2 ** -9)
             r += 1
+
+
+@pytest.mark.parametrize("scaled", [True, False])
+def test_kv_insert_fp8_index_cache(orc, scaled):
+    # e4m3 index keys per token and index head: with scales kept, the
+    # per-token-head rule (s = max|x| / 448, codes of x / s, torch's float8
+    # cast as the independent encoder); without, the codes of x itself
+    w = W.fp8_index(W.custom(92, q_lens=[2, 1], seq_lens=[500, 77], hq=4, di=64, hi=2, topk=2),
+                    seed=93, scaled=scaled)
+    k_new, v_new, idx_new = _new_rows(w, 2)
+    *_, st, iscale = orc.kv_insert(w, k_new, v_new, idx_new)
+    assert st == 0
+    codes = orc.kv_insert(w, k_new, v_new, idx_new)[2]
+    to_f = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).float().numpy()
+    r = 0
+    for q in range(w.num_reqs):
+        for j in range(int(w.q_lens[q])):
+            pos = int(w.context_lens[q]) + j
+            page, slot = w.block_table[q, pos // 128], pos % 128
+            for h in range(w.index_heads):
+                x = to_f(idx_new[r, h])
+                s = np.float32(np.abs(x).max()) / np.float32(448) if scaled else np.float32(1)
+                if scaled:
+                    assert iscale[page, slot, h] == s
+                want = W.fp8_codes(x / s)
+                assert np.array_equal(codes[page, slot, h], want)
+            r += 1
