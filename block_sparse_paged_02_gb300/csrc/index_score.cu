@@ -199,29 +199,30 @@ __device__ __forceinline__ void score_page_mma(const uint8_t* page, const float*
     lim[k] = pr - blk * kBlock;  // tokens t <= lim are visible
     hcol[k] = col % HI;
   }
+  // every sub-row of the block visible to both columns: no per-token mask
+  const bool whole = (!live[0] || lim[0] >= kBlock - 1) && (!live[1] || lim[1] >= kBlock - 1);
   float m[2] = {-INFINITY, -INFINITY};
 #pragma unroll 2
   for (int mt = 0; mt < kMt; ++mt) {
-    uint32_t w[2][kSpanW];  // spans of sub-rows 16mt + g and 16mt + g + 8
+    // spans of sub-rows 16mt + g and 16mt + g + 8.  Lanes of one column
+    // group read the same bytes of rows a page row apart (bank conflicts);
+    // rotating the read order per lane would need run-time register
+    // indexing, which measured far more costly than the conflicts.
+    uint32_t w[2][kSpanW];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const uint8_t* row = page + (16 * mt + g + 8 * half) * kRowB + c * kD4 * kElem;
 #pragma unroll
       for (int i = 0; i < kSpanC; ++i) {
-        const int ch = (i + g) % kSpanC;  // rotated: rows 128 B apart hit other banks
-        const uint4 v = lds128(row + 16 * ch);
-        // (a constant-index store after the loop keeps w in registers)
-#pragma unroll
-        for (int x = 0; x < kSpanC; ++x)
-          if (x == ch) {
-            w[half][4 * x] = v.x;
-            w[half][4 * x + 1] = v.y;
-            w[half][4 * x + 2] = v.z;
-            w[half][4 * x + 3] = v.w;
-          }
+        const uint4 v = lds128(row + 16 * i);
+        w[half][4 * i] = v.x;
+        w[half][4 * i + 1] = v.y;
+        w[half][4 * i + 2] = v.z;
+        w[half][4 * i + 3] = v.w;
       }
     }
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    // two accumulators (even / odd k-steps) halve the dependent MMA chain
+    float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < kK; ++kk) {
       uint32_t a[4];
@@ -236,15 +237,20 @@ __device__ __forceinline__ void score_page_mma(const uint8_t* page, const float*
         a[2] = w[0][2 * kk + 1];
         a[3] = w[1][2 * kk + 1];
       }
-      mma16816<F8>(d, a, bq[kk][0], bq[kk][1]);
+      mma16816<F8>((kk & 1) ? d2 : d, a, bq[kk][0], bq[kk][1]);
+    }
+    float sc[2] = {1.f, 1.f};
+    if (tscale) {
+      sc[0] = tscale[16 * mt + g];
+      sc[1] = tscale[16 * mt + g + 8];
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int sr = 16 * mt + g + 8 * (e >> 1);  // sub-row = token * HI + head
       const int k = e & 1;
-      float v = d[e];
-      if (tscale) v *= tscale[sr];
-      const bool ok = live[k] && (sr % HI) == hcol[k] && sr / HI <= lim[k];
+      const float v = (d[e] + d2[e]) * sc[e >> 1];
+      const bool ok = whole ? (HI == 1 || (sr % HI) == hcol[k]) && live[k]
+                            : live[k] && (sr % HI) == hcol[k] && sr / HI <= lim[k];
       if (ok) m[k] = fmaxf(m[k], v);  // NaN never wins
     }
   }
@@ -342,18 +348,31 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
     // global-memory round trip; the first ring's worth of items is looked up
     // by one lane each in parallel, then the elected lane keeps one lookup in
     // flight ahead of the copy it is about to issue.
+    // consecutive items mostly share a request: its row range and context
+    // are kept from the previous lookup of this lane
+    int c_req = -1, c_q0 = 0, c_qlen = 0, c_ctx = 0;
     auto lookup = [&](int j, StageInfo* si, int* page) {
       const int it = i0 + j;
-      int lo = 0, hi = R;  // largest q with prefix[q] <= it
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= it) lo = mid; else hi = mid;
+      int lo;
+      if (c_req >= 0 && prefix[c_req] <= it && it < prefix[c_req + 1]) {
+        lo = c_req;
+      } else {
+        lo = 0;
+        int hi = R;  // largest q with prefix[q] <= it
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (prefix[mid] <= it) lo = mid; else hi = mid;
+        }
+        c_req = lo;
+        c_q0 = b.cu_seqlens_q[lo];
+        c_qlen = b.cu_seqlens_q[lo + 1] - c_q0;
+        c_ctx = b.context_lens[lo];
       }
       si->req = lo;
       si->blk = it - prefix[lo];
-      si->q0 = b.cu_seqlens_q[lo];
-      si->qlen = b.cu_seqlens_q[lo + 1] - si->q0;
-      si->ctx = b.context_lens[lo];
+      si->q0 = c_q0;
+      si->qlen = c_qlen;
+      si->ctx = c_ctx;
       si->jstart = max(0, si->blk * kBlock - si->ctx);  // first row that sees the block
       si->pad = 0;
       *page = b.block_table[(long long)lo * b.bt_stride + si->blk];
