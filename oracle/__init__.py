@@ -62,6 +62,9 @@ def _load():
             lib.orc_row_geometry.argtypes = [P, P, P, P, P]
             lib.orc_index_score.restype = ctypes.c_uint32
             lib.orc_index_score.argtypes = [P, P, P, i32, i32, P, i32, i32]
+            lib.orc_sparse_mla.restype = ctypes.c_uint32
+            lib.orc_sparse_mla.argtypes = [i32, i32, i32, i32, P, P, ctypes.c_int64, P, P, P,
+                                           ctypes.c_double, P, P, i32]
             lib.orc_index_score_fp8.restype = ctypes.c_uint32
             lib.orc_index_score_fp8.argtypes = [P, P, P, P, i32, i32, P, i32, i32]
             lib.orc_topk_build_table.restype = ctypes.c_uint32
@@ -73,7 +76,7 @@ def _load():
             lib.orc_fp8_e4m3_encode.argtypes = [ctypes.c_float]
             lib.orc_kv_insert.restype = ctypes.c_uint32
             lib.orc_kv_insert.argtypes = [P, i32, i32, P, P, i32, i32, P, P, P, P, i32, i32, P, P,
-                                          i32]
+                                          i32, i32, P]
             lib.orc_dense_attn.restype = ctypes.c_uint32
             lib.orc_dense_attn.argtypes = [P, i32, i32, i32, P, P, P, i32, i32, P, P, P,
                                            ctypes.c_double, P, P, i32]
@@ -239,12 +242,15 @@ def fp8_e4m3_encode(x: float) -> int:
 
 def kv_insert(w, k_new, v_new, idx_new, skip_index: bool = False):
     """Insert the rows' new K/V/index-K into copies of the workload's pools;
-    returns (k_cache, v_cache, idx_k, k_scale, v_scale, status)."""
+    returns (k_cache, v_cache, idx_k, k_scale, v_scale, status), plus the
+    index scales as a 7th item when the index cache is FP8."""
     b = Batch.of(w)
     kdt = np.uint8 if w.kv_dtype == 1 else np.uint16
     k_cache = np.array(w.k_cache, dtype=kdt, copy=True)
     v_cache = np.array(w.v_cache, dtype=kdt, copy=True)
-    idx_k = np.array(w.idx_k, dtype=np.uint16, copy=True)
+    idt = np.uint8 if w.index_dtype == 1 else np.uint16
+    idx_k = np.array(w.idx_k, dtype=idt, copy=True)
+    idx_scale = None if w.idx_k_scale is None else np.array(w.idx_k_scale, np.float32, copy=True)
     k_scale = None if w.k_scale is None else np.array(w.k_scale, np.float32, copy=True)
     v_scale = None if w.v_scale is None else np.array(w.v_scale, np.float32, copy=True)
     k_new = _c(k_new, np.uint16)
@@ -254,5 +260,26 @@ def kv_insert(w, k_new, v_new, idx_new, skip_index: bool = False):
                                _ptr(v_new), int(w.index_heads), int(w.index_dim), _ptr(idx_new),
                                _ptr(k_cache), _ptr(v_cache), _ptr(idx_k), int(w.kv_dtype),
                                int(w.scale_mode), _ptr(k_scale), _ptr(v_scale),
-                               int(bool(skip_index)))
+                               int(bool(skip_index)), int(w.index_dtype), _ptr(idx_scale))
+    if w.index_dtype == 1:
+        return k_cache, v_cache, idx_k, k_scale, v_scale, int(st), idx_scale
     return k_cache, v_cache, idx_k, k_scale, v_scale, int(st)
+
+
+def sparse_mla(q, kv_cache, kv_indptr, kv_indices, dv: int, *, sinks=None,
+               softmax_scale: float, nthreads: Optional[int] = None):
+    """Sparse MLA decode: q [N, H, Dqk] bf16 bits, kv_cache [T, Dqk] bf16 bits
+    (value = first dv columns), per-row token ids through kv_indptr [N+1] /
+    kv_indices; returns (out [N, H, dv] fp64, lse [N, H] fp64, status)."""
+    q = _c(q, np.uint16)
+    kv = _c(kv_cache, np.uint16)
+    ip = _c(kv_indptr, np.int32)
+    ix = _c(kv_indices if len(kv_indices) else np.zeros(1, np.int32), np.int32)
+    N, H, dqk = (int(x) for x in q.shape)
+    out = np.empty((max(N, 1), H, dv), np.float64)
+    lse = np.empty((max(N, 1), H), np.float64)
+    sk = None if sinks is None else _c(sinks, np.float32)
+    st = _load().orc_sparse_mla(N, H, dqk, int(dv), _ptr(q), _ptr(kv), int(kv.shape[0]), _ptr(ip),
+                                _ptr(ix), _ptr(sk), float(softmax_scale), _ptr(out), _ptr(lse),
+                                nthreads or default_threads())
+    return out[:N], lse[:N], int(st)

@@ -561,8 +561,9 @@ static void quantize_row(const uint16_t* src, int32_t d, uint8_t* dst, float* sc
 uint32_t orc_kv_insert(const orc_batch* b, int32_t hkv, int32_t head_dim, const uint16_t* k_new,
                        const uint16_t* v_new, int32_t index_heads, int32_t index_dim,
                        const uint16_t* idx_new, void* k_cache, void* v_cache,
-                       uint16_t* idx_k_cache, int32_t kv_dtype, int32_t scale_mode,
-                       float* k_scale, float* v_scale, int32_t skip_index) {
+                       void* idx_k_cache, int32_t kv_dtype, int32_t scale_mode,
+                       float* k_scale, float* v_scale, int32_t skip_index, int32_t idx_dtype,
+                       float* idx_scale) {
   geom_t g;
   const uint32_t st = geometry_alloc(b, &g);
   for (int32_t r = 0; r < b->num_rows; ++r) {
@@ -589,11 +590,98 @@ uint32_t orc_kv_insert(const orc_batch* b, int32_t hkv, int32_t head_dim, const 
         memcpy((uint16_t*)v_cache + dst, v_new + src, sizeof(uint16_t) * (size_t)head_dim);
       }
     }
-    if (!skip_index) {
+    if (!skip_index && idx_dtype == 1) {
+      /* e4m3 index keys, per token and index head: the per-token-head rule
+       * when scales are kept, else scale 1 */
+      for (int32_t h = 0; h < index_heads; ++h) {
+        const int64_t src = ((int64_t)r * index_heads + h) * index_dim;
+        const int64_t dst = (token * index_heads + h) * index_dim;
+        float s = 1.0f;
+        quantize_row(idx_new + src, index_dim, (uint8_t*)idx_k_cache + dst, &s,
+                     idx_scale ? 2 : 0, 1.0f);
+        if (idx_scale) idx_scale[token * index_heads + h] = s;
+      }
+    } else if (!skip_index) {
       const int64_t n = (int64_t)index_heads * index_dim;
-      memcpy(idx_k_cache + token * n, idx_new + (int64_t)r * n, sizeof(uint16_t) * (size_t)n);
+      memcpy((uint16_t*)idx_k_cache + token * n, idx_new + (int64_t)r * n,
+             sizeof(uint16_t) * (size_t)n);
     }
   }
   geometry_free(&g);
+  return st;
+}
+
+/* ------------------------------------------------------ sparse MLA decode */
+
+/* One latent KV row per token: kv[t, 0:dqk] is the key (latent part + rope
+ * part), kv[t, 0:dv] the value.  Row r attends over the token ids
+ * kv_indices[kv_indptr[r] .. kv_indptr[r+1]) with the same softmax, sink and
+ * natural-log LSE as attend_head (softmax_scale only, no dequant scales). */
+typedef struct {
+  int32_t heads, dqk, dv;
+  const uint16_t *q, *kv;
+  int64_t num_tokens;
+  const int32_t *indptr, *indices;
+  const float* sinks;
+  double scale;
+  double *out, *lse;
+  uint32_t* row_status;
+} mla_ctx;
+
+static void mla_row(void* vctx, int32_t r) {
+  const mla_ctx* c = (const mla_ctx*)vctx;
+  const int64_t b0 = c->indptr[r], b1 = c->indptr[r + 1];
+  int64_t n = b1 - b0;
+  int poisoned = n < 0;
+  for (int64_t i = 0; !poisoned && i < n; ++i) {
+    const int32_t t = c->indices[b0 + i];
+    if (t < 0 || (int64_t)t >= c->num_tokens) poisoned = 1;
+  }
+  c->row_status[r] = poisoned ? ORC_BAD_TABLE : 0u;
+  if (poisoned) n = 0; /* a poisoned row is computed as an empty row */
+  double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  for (int32_t h = 0; h < c->heads; ++h) {
+    const uint16_t* qh = c->q + ((int64_t)r * c->heads + h) * c->dqk;
+    double* o = c->out + ((int64_t)r * c->heads + h) * c->dv;
+    const int has_sink = c->sinks != NULL;
+    const double sink = has_sink ? (double)c->sinks[h] : -INFINITY;
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) {
+      const uint16_t* k = c->kv + (int64_t)c->indices[b0 + i] * c->dqk;
+      double dot = 0.0;
+      for (int32_t d = 0; d < c->dqk; ++d) dot += orc_bf16_value(qh[d]) * orc_bf16_value(k[d]);
+      s[i] = c->scale * dot;
+      if (s[i] > m) m = s[i];
+    }
+    if (has_sink && sink > m) m = sink;
+    for (int32_t d = 0; d < c->dv; ++d) o[d] = 0.0;
+    if (m == -INFINITY) {
+      c->lse[(int64_t)r * c->heads + h] = -INFINITY;
+      continue;
+    }
+    double den = has_sink ? exp(sink - m) : 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+      const double p = exp(s[i] - m);
+      den += p;
+      const uint16_t* v = c->kv + (int64_t)c->indices[b0 + i] * c->dqk; /* value = latent part */
+      for (int32_t d = 0; d < c->dv; ++d) o[d] += p * orc_bf16_value(v[d]);
+    }
+    for (int32_t d = 0; d < c->dv; ++d) o[d] /= den;
+    c->lse[(int64_t)r * c->heads + h] = m + log(den);
+  }
+  free(s);
+}
+
+uint32_t orc_sparse_mla(int32_t num_rows, int32_t heads, int32_t dqk, int32_t dv,
+                        const uint16_t* q, const uint16_t* kv_cache, int64_t num_tokens,
+                        const int32_t* kv_indptr, const int32_t* kv_indices, const float* sinks,
+                        double softmax_scale, double* out, double* lse, int32_t nthreads) {
+  mla_ctx c = {heads, dqk, dv, q, kv_cache, num_tokens, kv_indptr, kv_indices, sinks,
+               softmax_scale, out, lse, NULL};
+  c.row_status = (uint32_t*)calloc((size_t)(num_rows > 0 ? num_rows : 1), sizeof(uint32_t));
+  for_each_row(num_rows, nthreads, mla_row, &c);
+  uint32_t st = 0;
+  for (int32_t r = 0; r < num_rows; ++r) st |= c.row_status[r];
+  free(c.row_status);
   return st;
 }

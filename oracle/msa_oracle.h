@@ -100,13 +100,31 @@ uint8_t orc_fp8_e4m3_encode(float x);
  * given k_scale[0] / v_scale[0]; PER_TOKEN_HEAD computes s = max_d |x_d| / 448
  * per token and KV head (s = 1 when all zero), stores it in k_scale/v_scale
  * at the slot and divides by it.  The division is fp32 and the code is
- * orc_fp8_e4m3_encode of the quotient.  Rows of requests that do not pass
- * the geometry checks are not written. */
+ * orc_fp8_e4m3_encode of the quotient.  An FP8 index cache (idx_dtype 1:
+ * e4m3 codes) is written the same way per token and index head, with the
+ * PER_TOKEN_HEAD rule into idx_scale [P,128,Hi] when idx_scale is given and
+ * scale 1 when it is NULL; a bf16 one (idx_dtype 0) takes a copy.  Rows of
+ * requests that do not pass the geometry checks are not written. */
 uint32_t orc_kv_insert(const orc_batch* b, int32_t hkv, int32_t head_dim, const uint16_t* k_new,
                        const uint16_t* v_new, int32_t index_heads, int32_t index_dim,
                        const uint16_t* idx_new, void* k_cache, void* v_cache,
-                       uint16_t* idx_k_cache, int32_t kv_dtype, int32_t scale_mode,
-                       float* k_scale, float* v_scale, int32_t skip_index);
+                       void* idx_k_cache, int32_t kv_dtype, int32_t scale_mode,
+                       float* k_scale, float* v_scale, int32_t skip_index, int32_t idx_dtype,
+                       float* idx_scale);
+
+/* Sparse MLA decode (the sparse-MLA-with-sinks page): one latent KV head,
+ * kv_cache [num_tokens, dqk] bf16 whose first dv columns are the value; row r
+ * attends over token ids kv_indices[kv_indptr[r] .. kv_indptr[r+1]) with
+ *   s_t = softmax_scale * (q_h . kv_t[0:dqk]),  m = max(max_t s_t, sink_h),
+ *   den = sum_t exp(s_t - m) + exp(sink_h - m),
+ *   out = sum_t exp(s_t - m) kv_t[0:dv] / den,  lse = m + ln(den)
+ * in fp64 (no sink: its terms are absent).  A row with a negative count or a
+ * token id outside [0, num_tokens) is an empty row and raises ORC_BAD_TABLE.
+ * q [num_rows, heads, dqk] bf16; out [num_rows, heads, dv], lse [num_rows, heads]. */
+uint32_t orc_sparse_mla(int32_t num_rows, int32_t heads, int32_t dqk, int32_t dv,
+                        const uint16_t* q, const uint16_t* kv_cache, int64_t num_tokens,
+                        const int32_t* kv_indptr, const int32_t* kv_indices, const float* sinks,
+                        double softmax_scale, double* out, double* lse, int32_t nthreads);
 
 #ifdef __cplusplus
 }

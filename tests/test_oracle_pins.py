@@ -617,3 +617,62 @@ def test_kv_insert_fp8_index_cache(orc, scaled):
                 want = W.fp8_codes(x / s)
                 assert np.array_equal(codes[page, slot, h], want)
             r += 1
+
+
+# ----------------------------------------------------------- sparse MLA decode
+
+def _mla_reference(w):
+    """float64 torch reference: gather each row's latent rows, softmax over the
+    scaled logits with the sink as one more logit, value = first dv columns."""
+    to_f = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).double()
+    q, kv = to_f(w.q), to_f(w.kv_cache)
+    out = np.zeros((w.num_rows, w.heads, w.dv))
+    lse = np.full((w.num_rows, w.heads), NEG_INF)
+    for r in range(w.num_rows):
+        ids = torch.from_numpy(w.kv_indices[w.kv_indptr[r]:w.kv_indptr[r + 1]].astype(np.int64))
+        K = kv[ids]                                   # [n, dqk]
+        logits = w.softmax_scale * (q[r] @ K.T)       # [H, n]
+        if w.sinks is not None:
+            logits = torch.cat([logits, torch.from_numpy(w.sinks).double()[:, None]], dim=1)
+        if logits.shape[1] == 0:
+            continue
+        p = torch.softmax(logits, dim=1)[:, : len(ids)]
+        out[r] = (p @ K[:, : w.dv]).numpy()
+        lse[r] = torch.logsumexp(logits, dim=1).numpy()
+    return out, lse
+
+
+@pytest.mark.parametrize("sink,dup", [(True, False), (False, False), (True, True)])
+def test_sparse_mla_matches_softmax_reference(orc, sink, dup):
+    w = W.sparse_mla_custom(31, [37, 16, 1, 200, 0], heads=8, ctx=512, dqk=96, dv=64,
+                            with_sink=sink, duplicates=dup)
+    out, lse, st = orc.sparse_mla(w.q, w.kv_cache, w.kv_indptr, w.kv_indices, w.dv,
+                                  sinks=w.sinks, softmax_scale=w.softmax_scale)
+    assert st == 0
+    ref_o, ref_l = _mla_reference(w)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-10, atol=1e-12)
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(lse), fin)
+    np.testing.assert_allclose(lse[fin], ref_l[fin], rtol=1e-12, atol=1e-12)
+    # the empty row: O = 0 and LSE = the sink (or -inf)
+    assert np.all(out[4] == 0)
+    assert np.array_equal(lse[4], w.sinks.astype(np.float64) if sink else np.full(8, NEG_INF))
+
+
+def test_sparse_mla_order_invariance_and_bad_ids(orc):
+    w = W.sparse_mla_custom(32, [50, 9], heads=4, ctx=256, dqk=96, dv=64)
+    a = orc.sparse_mla(w.q, w.kv_cache, w.kv_indptr, w.kv_indices, w.dv, sinks=w.sinks,
+                       softmax_scale=w.softmax_scale)
+    perm = w.kv_indices.copy()
+    perm[:50] = perm[:50][::-1]
+    b = orc.sparse_mla(w.q, w.kv_cache, w.kv_indptr, perm, w.dv, sinks=w.sinks,
+                       softmax_scale=w.softmax_scale)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-12, atol=1e-14)
+    # an id outside the cache poisons its row only: empty row + status bit
+    bad = w.kv_indices.copy()
+    bad[52] = w.num_tokens
+    o, l, st = orc.sparse_mla(w.q, w.kv_cache, w.kv_indptr, bad, w.dv, sinks=w.sinks,
+                              softmax_scale=w.softmax_scale)
+    assert st == 8
+    assert np.all(o[1] == 0) and np.array_equal(l[1], w.sinks.astype(np.float64))
+    np.testing.assert_array_equal(o[0], a[0][0])

@@ -295,8 +295,9 @@ def fp8_index(w: Workload, seed: int, scaled: bool = True) -> Workload:
                                idx_k_scale=scale)
 
 
-def large_batch_fp8_index(seed: int = 4) -> Workload:
-    """The 64-request decode with an FP8 (e4m3, per-token scaled) index-K cache."""
+def large_batch_fp8_index(seed: int = 6) -> Workload:
+    """The 64-request decode recipe with an FP8 (e4m3, per-token scaled)
+    index-K cache."""
     return fp8_index(large_batch(seed), seed + 100)
 
 
@@ -308,3 +309,70 @@ NAMED = {
     "chunked_prefill": chunked_prefill,
     "large_batch_decode_fp8_index": large_batch_fp8_index,
 }
+
+
+# ------------------------------------------------------------ sparse MLA decode
+
+@dataclasses.dataclass
+class MlaWorkload:
+    """Sparse MLA decode inputs: one latent KV head, one row of dqk values per
+    cached token (the first dv of them are the value), and per query row the
+    list of selected token ids (kv_indptr / kv_indices)."""
+    name: str
+    q: np.ndarray            # bf16 bits [N, H, dqk]
+    kv_cache: np.ndarray     # bf16 bits [T, dqk]
+    kv_indptr: np.ndarray    # int32 [N + 1]
+    kv_indices: np.ndarray   # int32 [nnz] token ids (< 0 or >= T marks a bad row)
+    dv: int
+    sinks: Optional[np.ndarray]  # fp32 [H]
+    softmax_scale: float
+    seed: int = 0
+
+    @property
+    def num_rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def heads(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def dqk(self) -> int:
+        return int(self.q.shape[2])
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.kv_cache.shape[0])
+
+
+def sparse_mla_custom(seed: int, counts, *, heads=16, ctx=4096, dqk=576, dv=512,
+                      with_sink=True, duplicates=False, name="sparse_mla_custom") -> MlaWorkload:
+    """Row r selects counts[r] token ids from its own context of ctx tokens
+    (ascending and distinct unless duplicates); q and the latent cache are
+    N(0,1) in bf16; the scale is 1/sqrt(192) (a 128 + 64 query-key head)."""
+    rng = np.random.default_rng(seed)
+    N = len(counts)
+    T = max(1, N * ctx)
+    tg = torch.Generator().manual_seed(int(seed) * 7919 + 29)
+    q = torch.empty((N, heads, dqk)).normal_(generator=tg).to(torch.bfloat16)
+    kv = torch.empty((T, dqk)).normal_(generator=tg).to(torch.bfloat16)
+    idx = []
+    for r, n in enumerate(counts):
+        if duplicates:
+            sel = rng.integers(0, ctx, size=n)
+        else:
+            sel = np.sort(rng.choice(ctx, size=min(n, ctx), replace=False))
+        idx.append((r * ctx + sel).astype(np.int32))
+    indptr = np.concatenate([[0], np.cumsum([len(x) for x in idx])]).astype(np.int32)
+    indices = np.concatenate(idx).astype(np.int32) if idx else np.zeros(0, np.int32)
+    sinks = rng.standard_normal(heads).astype(np.float32) if with_sink else None
+    return MlaWorkload(name=name, q=q.view(torch.int16).numpy().view(np.uint16).copy(),
+                       kv_cache=kv.view(torch.int16).numpy().view(np.uint16).copy(),
+                       kv_indptr=indptr, kv_indices=indices, dv=dv, sinks=sinks,
+                       softmax_scale=float(np.float32(1.0 / np.sqrt(192.0))), seed=seed)
+
+
+def sparse_mla_decode(seed: int = 7) -> MlaWorkload:
+    """64 decode rows, 16 heads, 2048 selected tokens each out of an 8192-token
+    context per row: the sparse-MLA decode recipe."""
+    return sparse_mla_custom(seed, [2048] * 64, heads=16, ctx=8192, name="sparse_mla_decode")
