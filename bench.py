@@ -199,22 +199,29 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    w = W.NAMED[args.workload](seed=rank_seed(args.workload, 0))
+    if args.workload == "sparse_mla_decode":
+        w = W.sparse_mla_decode(seed=rank_seed(args.workload, 0))
+        run_once = lambda: mla_cpu_run(w, budget_s=0.0, rows=w.num_rows)
+        metric, config = MLA_METRIC, mla_config(w)
+    else:
+        w = W.NAMED[args.workload](seed=rank_seed(args.workload, 0))
+        run_once = lambda: cpu_oracle_run(w, budget_s=0.0, max_reps=1)
+        metric, config = METRIC, workload_config(w)
     times = []
     for _ in range(args.warmup):
-        cpu_oracle_run(w, budget_s=0.0, max_reps=1)
+        run_once()
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        cpu_oracle_run(w, budget_s=0.0, max_reps=1)
+        run_once()
         times.append(time.perf_counter() - t0)
     import oracle
     total = sum(times)
     value = w.num_rows * args.steps / total
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "rows/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w),
+            "config": config,
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.default_threads(),
                              "kind": "oracle",
                              "sample": f"full {w.name} batch per step ({w.num_rows} rows)"},
@@ -225,7 +232,171 @@ def run_reference(args):
 
 
 W_SEED = {"tiny_decode": 1, "batched_decode": 2, "speculative_decode": 3,
-          "large_batch_decode": 4, "chunked_prefill": 5, "large_batch_decode_fp8_index": 6}
+          "large_batch_decode": 4, "chunked_prefill": 5, "large_batch_decode_fp8_index": 6,
+          "sparse_mla_decode": 7}
+MLA_METRIC = "query rows/s for sparse MLA decode with sinks; % of HBM roofline"
+
+
+# ------------------------------------------------------------ sparse MLA arm
+
+def mla_bytes(w) -> dict:
+    """Bytes and FLOPs of one sparse-MLA call: each row's distinct latent rows
+    (1152 B: read once however often listed), queries, token lists, outputs."""
+    N, H = w.num_rows, w.heads
+    toks = 0
+    for r in range(N):
+        toks += len(np.unique(w.kv_indices[w.kv_indptr[r]:w.kv_indptr[r + 1]]))
+    counts = np.diff(w.kv_indptr).astype(np.int64)
+    total = (toks * w.dqk * 2 + N * H * w.dqk * 2 + N * H * (w.dv * 2 + 4)
+             + int(counts.sum()) * 4 + (N + 1) * 4)
+    flops = int(counts.sum()) * H * (w.dqk + w.dv) * 2
+    return dict(total=total, flops=flops)
+
+
+def mla_cpu_run(w, budget_s: float = 12.0, rows: int = 16):
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    sub = min(rows, w.num_rows)
+    ip = w.kv_indptr[: sub + 1]
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.sparse_mla(w.q[:sub], w.kv_cache, ip, w.kv_indices[: int(ip[-1])], w.dv,
+                          sinks=w.sinks, softmax_scale=w.softmax_scale, nthreads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 3:
+            break
+    return dict(value=sub * reps / el, unit="rows/s", cores=threads, kind="oracle",
+                sample=f"{reps} x the first {sub} rows of {w.name}, fp64 C oracle, "
+                f"{threads} threads, {el:.2f} s")
+
+
+def mla_config(w):
+    counts = np.diff(w.kv_indptr)
+    return {"workload": w.name, "rows": w.num_rows, "heads": w.heads, "dqk": w.dqk, "dv": w.dv,
+            "cache_tokens": w.num_tokens, "tokens_per_row": int(np.median(counts)),
+            "kv": "bf16", "sinks": w.sinks is not None,
+            "l2": "flushed between steps (512 MiB write, then 256 MiB read)"}
+
+
+def run_mla_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_paged_02_gb300 as msa
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    w = W.sparse_mla_decode(seed=rank_seed(args.workload, rank))
+    case = msa.MlaCase(w, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(L2_FLUSH_BYTES // 2, dtype=torch.uint8, device=dev)
+
+    def flush_l2(i):
+        flush.fill_(i & 0xff)
+        rbuf.sum(dtype=torch.int32)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    if args.profile:
+        for _ in range(args.warmup + args.steps):
+            case.decode()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_run": w.name, "status": int(case.status.item())}))
+        return 0
+    for i in range(args.warmup):
+        flush_l2(i)
+        case.decode()
+    torch.cuda.synchronize()
+    if int(case.status.item()) != 0:
+        raise RuntimeError(f"device status {int(case.status.item())} on a clean workload")
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        case.decode(stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    marks = [(ev(), ev()) for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush_l2(i)
+            marks[i][0].record(stream)
+            g.replay()
+            marks[i][1].record(stream)
+        torch.cuda.synchronize()
+    total_ms = sum(a.elapsed_time(b) for a, b in marks)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    # end to end: queries and token lists from pinned host memory, O/LSE back
+    host = {name: getattr(case, name).cpu().pin_memory() for name in ("q", "indptr", "indices")}
+    out_h = torch.empty_like(case.out, device="cpu").pin_memory()
+    lse_h = torch.empty_like(case.lse, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    e2e_marks = [(ev(), ev()) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush_l2(i)
+        if i >= args.warmup:
+            e2e_marks[i - args.warmup][0].record(stream)
+        for name, t in host.items():
+            getattr(case, name).copy_(t, non_blocking=True)
+        case.decode()
+        out_h.copy_(case.out, non_blocking=True)
+        lse_h.copy_(case.lse, non_blocking=True)
+        if i >= args.warmup:
+            e2e_marks[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_marks)
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+        if rank != 0:
+            dist.destroy_process_group()
+            return 0
+    rows_total = w.num_rows * ws * args.steps
+    step = total_ms / args.steps
+    peak, peak_kind = read_peaks()
+    nb = mla_bytes(w)
+    achieved = nb["total"] / (step / 1e3) / 1e9
+    tflops = nb["flops"] / (step / 1e3) / 1e12
+    bf16_peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16_peak = float(json.load(f).get("bf16_tflops"))
+    except Exception:
+        pass
+    line = {
+        "metric": MLA_METRIC, "value": rows_total / (total_ms / 1e3), "unit": "rows/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 / fp32 acc", "data": "synthetic", "config": mla_config(w),
+        "roofline": {"bound": "hbm", "kernel": "sparse_mla", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": None, "algorithmic_bytes_per_launch": nb["total"],
+                     "avg_launch_ms": step},
+        "tensor": {"achieved_tflops": tflops, "peak_bf16_tflops": bf16_peak,
+                   "frac": tflops / bf16_peak if bf16_peak else None,
+                   "note": "mma.sync m16n8k16 bf16"},
+        "e2e": {"value": rows_total / (e2e_ms / 1e3), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps, "launch": "cuda_graph", "clocks": clocks.summary(),
+        "cpu_baseline": mla_cpu_run(w),
+    }
+    print(json.dumps(line))
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
 
 
 def rank_seed(workload: str, rank: int) -> int:
@@ -422,13 +593,16 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="large_batch_decode", choices=sorted(W.NAMED))
+    ap.add_argument("--workload", default="large_batch_decode",
+                    choices=sorted(W.NAMED) + ["sparse_mla_decode"])
     ap.add_argument("--profile", action="store_true",
                     help="plain warm-up + K decode steps for a profiler (no timing)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "sparse_mla_decode":
+        return run_mla_gpu(args)
     return run_gpu(args)
 
 

@@ -23,7 +23,8 @@ MSA_DEV_BAD_PAGE, MSA_DEV_BAD_LEN, MSA_DEV_MALFORMED, MSA_DEV_BAD_TABLE, MSA_DEV
     1, 2, 4, 8, 16
 
 EXPORTED = ("msa_index_score", "msa_topk_build_table", "msa_sparse_paged_attn", "msa_decode",
-            "msa_kv_insert", "msa_workspace_size", "msa_status_string")
+            "msa_kv_insert", "msa_sparse_mla_decode", "msa_sparse_mla_workspace_size",
+            "msa_workspace_size", "msa_status_string")
 
 
 class MsaError(RuntimeError):
@@ -54,6 +55,16 @@ class msa_attn_args(ctypes.Structure):
 class msa_index_cache(ctypes.Structure):
     _fields_ = [("k_cache", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
                 ("dtype", ctypes.c_int32), ("heads", ctypes.c_int32), ("dim", ctypes.c_int32)]
+
+
+class msa_mla_args(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("num_rows", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("dqk", ctypes.c_int32), ("dv", ctypes.c_int32),
+                ("kv_cache", ctypes.c_void_p), ("num_tokens", ctypes.c_int64),
+                ("kv_indptr", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p),
+                ("max_tokens", ctypes.c_int32), ("sinks", ctypes.c_void_p),
+                ("softmax_scale", ctypes.c_float), ("out", ctypes.c_void_p),
+                ("lse", ctypes.c_void_p)]
 
 
 class msa_trace(ctypes.Structure):
@@ -93,6 +104,10 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.msa_kv_insert.restype = ctypes.c_int
             L.msa_kv_insert.argtypes = [P, P, P, i32, i32, P, P, i32, i32, P, P, P, P, i32, P,
                                         P]
+            L.msa_sparse_mla_workspace_size.restype = ctypes.c_size_t
+            L.msa_sparse_mla_workspace_size.argtypes = [i32, i32, i32]
+            L.msa_sparse_mla_decode.restype = ctypes.c_int
+            L.msa_sparse_mla_decode.argtypes = [P, P, ctypes.c_size_t, P, P]
             L.msa_workspace_size.restype = ctypes.c_size_t
             L.msa_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
             L.msa_status_string.restype = ctypes.c_char_p
@@ -222,6 +237,34 @@ def msa_kv_insert(batch: msa_batch, k_new, v_new, num_kv_heads, head_dim, k_cach
         _p(k_cache), _p(v_cache), int(kv_dtype), int(scale_mode), _p(k_scale), _p(v_scale),
         _p(idx_new), ctypes.byref(index) if index is not None else None,
         int(bool(skip_index)), _p(dev_status), _stream(stream)))
+
+
+def make_mla_args(q, kv_cache, kv_indptr, kv_indices, out, lse, *, max_tokens: int,
+                  sinks=None, softmax_scale: float) -> msa_mla_args:
+    """Sparse MLA operands: q [N, H, 576] bf16, kv_cache [T, 576] bf16, int32
+    kv_indptr [N+1] / kv_indices, out [N, H, 512] bf16, lse [N, H] fp32."""
+    check_sinks(sinks, int(q.shape[1]))
+    for t in (kv_indptr, kv_indices):
+        if t.dtype != torch.int32:
+            raise ValueError("kv_indptr / kv_indices are int32")
+    a = msa_mla_args(_p(q), int(q.shape[0]), int(q.shape[1]), int(q.shape[2]),
+                     int(out.shape[2]), _p(kv_cache), int(kv_cache.shape[0]), _p(kv_indptr),
+                     _p(kv_indices), int(max_tokens), _p(sinks), float(softmax_scale), _p(out),
+                     _p(lse))
+    a._keep = (q, kv_cache, kv_indptr, kv_indices, out, lse, sinks)
+    return a
+
+
+def msa_sparse_mla_workspace_size(num_rows, num_heads, max_tokens) -> int:
+    return int(lib().msa_sparse_mla_workspace_size(int(num_rows), int(num_heads),
+                                                   int(max_tokens)))
+
+
+def msa_sparse_mla_decode(mla: msa_mla_args, workspace, dev_status, stream=None):
+    _check("msa_sparse_mla_decode", lib().msa_sparse_mla_decode(
+        ctypes.byref(mla), _p(workspace),
+        int(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
+        _p(dev_status), _stream(stream)))
 
 
 def make_trace(after_score=None, after_topk=None, after_attn=None) -> msa_trace:

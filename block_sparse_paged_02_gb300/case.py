@@ -107,3 +107,37 @@ class DeviceCase:
                     out=self.out.float().cpu().numpy().astype(np.float64),
                     lse=self.lse.cpu().numpy().astype(np.float64),
                     status=int(self.status.item()))
+
+
+class MlaCase:
+    """A sparse-MLA workload (`workloads.MlaWorkload` fields) resident on the
+    GPU, with outputs and workspace."""
+
+    def __init__(self, w, device: str = "cuda", max_tokens: Optional[int] = None):
+        self.w = w
+        counts = np.diff(np.asarray(w.kv_indptr, np.int64))
+        self.max_tokens = int(max_tokens or max(1, int(counts.max()) if counts.size else 1))
+        self.q = _dev(w.q, device)
+        self.kv = _dev(w.kv_cache, device)
+        self.indptr = _dev(w.kv_indptr, device)
+        self.indices = _dev(w.kv_indices if len(w.kv_indices) else np.zeros(1, np.int32), device)
+        self.sinks = None if w.sinks is None else _dev(w.sinks, device)
+        N, H = int(w.q.shape[0]), int(w.q.shape[1])
+        self.out = torch.empty((max(N, 1), H, w.dv), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((max(N, 1), H), dtype=torch.float32, device=device)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=device)
+        self.args = B.make_mla_args(self.q, self.kv, self.indptr, self.indices, self.out,
+                                    self.lse, max_tokens=self.max_tokens, sinks=self.sinks,
+                                    softmax_scale=w.softmax_scale)
+        ws = B.msa_sparse_mla_workspace_size(N, H, self.max_tokens)
+        self.workspace = torch.zeros((max(ws, 1),), dtype=torch.uint8, device=device)
+
+    def decode(self, stream=None):
+        B.msa_sparse_mla_decode(self.args, self.workspace, self.status, stream)
+
+    def fetch(self):
+        torch.cuda.synchronize()
+        n = int(self.w.q.shape[0])
+        return dict(out=self.out[:n].float().cpu().numpy().astype(np.float64),
+                    lse=self.lse[:n].cpu().numpy().astype(np.float64),
+                    status=int(self.status.item()))

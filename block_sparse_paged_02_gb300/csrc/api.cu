@@ -149,6 +149,39 @@ AttnLaunch make_attn(const msa_attn_args* a, const int32_t* tbl, int tbl_stride,
 
 msa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
 
+// Sparse MLA work split: splits of each (row, 16-head group) so that the
+// grid fills two CTAs per SM, each split at least 64 and at most
+// mla_max_tokens_per_split() token ids, a multiple of 16.
+void mla_split(int num_rows, int num_heads, int max_tokens, int* splits, int* per) {
+  const int groups = (num_heads + 15) / 16;
+  const long long base = (long long)num_rows * groups;
+  const int capacity = device_sm_count() * 2;
+  int s = base > 0 ? (int)max(1ll, capacity / base) : 1;
+  const int lim = mla_max_tokens_per_split();
+  s = max(s, (max_tokens + lim - 1) / lim);
+  s = min(s, max(1, (max_tokens + 63) / 64));
+  int t = (max_tokens + s - 1) / s;
+  t = (t + 15) / 16 * 16;
+  if (t > lim) t = lim;
+  *per = t;
+  *splits = max(1, (max_tokens + t - 1) / t);
+}
+
+struct MlaWs {
+  size_t counters, partials, total;
+};
+
+MlaWs mla_layout(int num_rows, int num_heads, int max_tokens) {
+  int splits, per;
+  mla_split(num_rows, num_heads, max_tokens, &splits, &per);
+  const size_t rg = (size_t)(num_rows > 0 ? num_rows : 1) * (size_t)((num_heads + 15) / 16);
+  MlaWs w;
+  w.counters = 0;
+  w.partials = round_up(rg * 4, 256);
+  w.total = w.partials + (splits > 1 ? rg * (size_t)splits * 16 * 516 * 4 : 0);
+  return w;
+}
+
 // Step 1: the streaming CUDA-core kernel, plus the tensor-core kernel for
 // requests with many rows when the batch may hold any (max_q_len hint).
 cudaError_t launch_scores(ScoreLaunch p, cudaStream_t stream) {
@@ -319,6 +352,46 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_attn) cudaEventRecord(trace->after_attn, stream);
   return MSA_OK;
+}
+
+size_t msa_sparse_mla_workspace_size(int32_t num_rows, int32_t num_heads, int32_t max_tokens) {
+  if (num_rows < 0 || num_heads < 1 || max_tokens < 1) return 0;
+  return mla_layout(num_rows, num_heads, max_tokens).total;
+}
+
+msa_status msa_sparse_mla_decode(const msa_mla_args* a, void* workspace, size_t workspace_bytes,
+                                 uint32_t* dev_status, cudaStream_t stream) {
+  if (!a || !dev_status) return MSA_ERR_NULL;
+  if (a->num_rows < 0 || a->num_heads < 1 || a->num_tokens < 0 || a->max_tokens < 1)
+    return MSA_ERR_SHAPE;
+  if (a->dqk != 576 || a->dv != 512 || a->num_heads > 128 || a->num_rows > 65535)
+    return MSA_ERR_UNSUPPORTED;
+  if (a->num_rows == 0) return MSA_OK;
+  if (!a->q || !a->kv_cache || !a->kv_indptr || !a->kv_indices || !a->out || !a->lse)
+    return MSA_ERR_NULL;
+  if (!aligned16(a->q) || !aligned16(a->kv_cache) || !aligned16(a->out)) return MSA_ERR_SHAPE;
+  const MlaWs L = mla_layout(a->num_rows, a->num_heads, a->max_tokens);
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return MSA_ERR_WORKSPACE;
+  MlaLaunch p;
+  p.q = static_cast<const uint16_t*>(a->q);
+  p.kv = static_cast<const uint16_t*>(a->kv_cache);
+  p.num_tokens = a->num_tokens;
+  p.indptr = a->kv_indptr;
+  p.indices = a->kv_indices;
+  p.num_rows = a->num_rows;
+  p.num_heads = a->num_heads;
+  p.head_groups = (a->num_heads + 15) / 16;
+  p.max_tokens = a->max_tokens;
+  mla_split(a->num_rows, a->num_heads, a->max_tokens, &p.splits, &p.tokens_per_split);
+  p.sinks = a->sinks;
+  p.softmax_scale = a->softmax_scale;
+  p.out = static_cast<uint16_t*>(a->out);
+  p.lse = a->lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
+  p.partials = reinterpret_cast<float*>(ws + L.partials);
+  p.status = dev_status;
+  return cuda_status(launch_sparse_mla(p, stream));
 }
 
 msa_status msa_kv_insert(const msa_batch* batch, const void* k_new, const void* v_new,

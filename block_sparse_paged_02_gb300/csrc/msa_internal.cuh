@@ -285,6 +285,27 @@ struct KvInsertLaunch {
 
 cudaError_t launch_kv_insert(const KvInsertLaunch& p, cudaStream_t stream);
 
+struct MlaLaunch {
+  const uint16_t* q;        // [num_rows, num_heads, 576] bf16
+  const uint16_t* kv;       // [num_tokens, 576] bf16
+  long long num_tokens;
+  const int32_t* indptr;    // [num_rows + 1]
+  const int32_t* indices;
+  int num_rows, num_heads, head_groups;  // head_groups = ceil(num_heads / 16)
+  int max_tokens;           // bound on a row's count (longer rows are refused)
+  int splits, tokens_per_split;
+  const float* sinks;
+  float softmax_scale;
+  uint16_t* out;            // [num_rows, num_heads, 512] bf16
+  float* lse;
+  float* partials;          // [num_rows, head_groups, splits, 16, 516] fp32
+  uint32_t* counters;       // [num_rows, head_groups], zero between calls
+  uint32_t* status;
+};
+
+cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream);
+int mla_max_tokens_per_split();
+
 // `programmatic`: the kernel may start while the previous kernel on the
 // stream finishes (programmatic dependent launch); it waits for that kernel's
 // results on the device before reading them.

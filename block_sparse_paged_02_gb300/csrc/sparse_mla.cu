@@ -1,0 +1,393 @@
+// sparse_mla.cu -- sparse MLA decode with attention sinks and a natural-log
+// LSE.
+//
+// Definition ("Attention sinks for ROCm AITER sparse MLA", vLLM PR 54404,
+// "Implementation breakdown" items 1-2 and "Key source snippets"): one
+// latent KV head whose cached row per token holds dqk = 576 values (512
+// latent + 64 rope); the key is the whole row, the value its first dv = 512
+// values.  Query row r attends over the token ids
+// kv_indices[kv_indptr[r] .. kv_indptr[r+1]) (the indptr / indices
+// convention of the MLA decode op), with the sink in the softmax denominator
+// and the natural-log LSE of that denominator; sinks are fp32 [heads].
+//
+// GB300 design.  16 heads x 16 tokens is a real tensor-core tile: a CTA of 4
+// warps owns 16 heads of one row and a contiguous span of its token list.
+// Per step of 16 tokens the token rows are gathered by 16 bulk async copies
+// (1152 B each) into a 4-deep shared ring; warp w computes the partial logits
+// over dims [144w, 144w + 144) (mma.sync m16n8k16, bf16, fp32 accumulation),
+// the four partials are summed through shared memory (one named barrier per
+// step, double buffered), every warp runs the same online softmax, and warp
+// w accumulates O for value dims [128w, 128w + 128) (64 fp32 registers per
+// lane).  Splits of a row merge through (m, l, acc) partials, finished by the
+// last-arriving CTA (atomic counter; its top bit carries "an id was out of
+// range" from any split).
+#include "msa_internal.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kMlaDqk = 576, kMlaDv = 512;
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kStepTok = 16;                       // tokens per step
+constexpr int kRowBytes = kMlaDqk * 2;             // 1152 B per cached token
+constexpr int kStages = 4;
+constexpr int kStageBytes = kStepTok * kRowBytes;  // 18 KB
+constexpr int kKQuarter = kMlaDqk / kWarps;        // 144 dims of the logits per warp
+constexpr int kKSteps = kKQuarter / 16;            // 9
+constexpr int kVQuarter = kMlaDv / kWarps;         // 128 value dims per warp
+constexpr int kXchgFloats = kWarps * 32 * 8;       // one step's partial logits
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleSlack = 8.f;  // log2 units
+constexpr int kPartHeadFloats = 4 + kMlaDv;        // m, l, 2 pad, acc[512] (16-B aligned)
+
+struct MlaSmem {
+  static constexpr int kRing = 0;
+  static constexpr int kXchg = kRing + kStages * kStageBytes;
+  static constexpr int kIds = kXchg + 2 * kXchgFloats * 4;
+  static constexpr int kMaxIds = 2048;  // token ids of one split held in shared memory
+  static constexpr int kBars = kIds + kMaxIds * 4;
+  static constexpr int kFlags = kBars + kStages * 8;
+  static constexpr int kBytes = kFlags + 64;
+};
+
+__device__ __forceinline__ uint2 lds64(const void* p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* ring = smem + MlaSmem::kRing;
+  float* xchg = reinterpret_cast<float*>(smem + MlaSmem::kXchg);
+  int* ids = reinterpret_cast<int*>(smem + MlaSmem::kIds);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + MlaSmem::kBars);
+  int* flags = reinterpret_cast<int*>(smem + MlaSmem::kFlags);
+
+  const int split = blockIdx.x, hg = blockIdx.y, r = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const unsigned full = 0xffffffffu;
+
+  // ---- this split's span of the row's token list
+  const long long b0 = p.indptr[r], b1 = p.indptr[r + 1];
+  const long long n_row = b1 - b0;
+  const long long lo = (long long)split * p.tokens_per_split;
+  const long long hi = (split == p.splits - 1) ? n_row : min(n_row, lo + p.tokens_per_split);
+  const int n = n_row < 0 ? 0 : (int)max(0ll, min(hi - lo, (long long)MlaSmem::kMaxIds));
+  // rows longer than the caller's bound (which sized the splits) are refused
+  bool bad = n_row < 0 || n_row > p.max_tokens || hi - lo > MlaSmem::kMaxIds;
+  for (int i = tid; i < n; i += kThreads) {
+    const int t = p.indices[b0 + lo + i];
+    bad |= t < 0 || (long long)t >= p.num_tokens;
+    ids[i] = t;
+  }
+  if (tid < kStages) mbar_init(&bars[tid], 1);
+  fence_barrier_init();
+  const bool cta_bad = __syncthreads_or(bad) != 0;
+  const int n_steps = cta_bad ? 0 : (n + kStepTok - 1) / kStepTok;
+
+  // ---- gather: one bulk copy per token row, issued by lanes of warp 0
+  auto issue = [&](int step) {  // warp 0, all lanes
+    const int st = step % kStages;
+    const int t0 = step * kStepTok;
+    const int cnt = min(kStepTok, n - t0);
+    if (lane == 0) mbar_arrive_expect_tx(&bars[st], (uint32_t)cnt * kRowBytes);
+    __syncwarp();
+    if (lane < cnt)
+      bulk_g2s(ring + st * kStageBytes + lane * kRowBytes,
+               p.kv + (long long)ids[t0 + lane] * kMlaDqk, kRowBytes, &bars[st]);
+  };
+  if (warp == 0)
+    for (int s = 0; s < min(n_steps, kStages); ++s) issue(s);
+
+  // ---- query fragments: heads 16hg + {g, g+8}, dims [144 warp, +144) with
+  // the k-slot permutation of the keys: k-step kk, slots (2c, 2c+1) <-> dims
+  // 36c + 4kk + {0,1}, (2c+8, 2c+9) <-> 36c + 4kk + {2,3}
+  uint32_t qa[kKSteps][4];
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int h = 16 * hg + g + 8 * half;
+    const uint16_t* qrow = p.q + ((long long)r * p.num_heads + h) * kMlaDqk + kKQuarter * warp +
+                           36 * c;
+#pragma unroll
+    for (int kk = 0; kk < kKSteps; ++kk) {
+      uint2 w = make_uint2(0u, 0u);
+      if (h < p.num_heads) w = *reinterpret_cast<const uint2*>(qrow + 4 * kk);
+      qa[kk][half] = w.x;
+      qa[kk][2 + half] = w.y;
+    }
+  }
+  const float scale2 = p.softmax_scale * kLog2e;  // logits in log2 units
+
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float o[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  bool timed_out = false;
+  int issued = min(n_steps, kStages);  // steps whose copies have been issued
+  int stopped = n_steps;               // first step not consumed
+
+  for (int step = 0; step < n_steps; ++step) {
+    const int st = step % kStages;
+    const bool late = !__all_sync(full, mbar_wait(&bars[st], (step / kStages) & 1));
+    const uint8_t* stage = ring + st * kStageBytes;
+    const int nvalid = min(kStepTok, n - step * kStepTok);
+
+    // ---- partial logits over this warp's 144 dims: n-tile nt = tokens 8nt + g
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      const uint8_t* krow = stage + (8 * nt + g) * kRowBytes + (kKQuarter * warp + 36 * c) * 2;
+#pragma unroll
+      for (int kk = 0; kk < kKSteps; ++kk) {
+        const uint2 kw = lds64(krow + 8 * kk);
+        mma16816<false>(s[nt], qa[kk], kw.x, kw.y);
+      }
+    }
+    float* xw = xchg + (step & 1) * kXchgFloats;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) xw[(warp * 32 + lane) * 8 + 4 * nt + e] = s[nt][e];
+    // one barrier per step, which also makes a wait that gave up in any warp
+    // a CTA-wide decision
+    if (__syncthreads_or(late)) {
+      timed_out = true;
+      stopped = step;
+      break;
+    }
+    // the same sum, in the same order, in every warp
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += xw[(w * 32 + lane) * 8 + 4 * nt + e];
+        const int t = 8 * nt + 2 * c + (e & 1);
+        s[nt][e] = t < nvalid ? v * scale2 : -INFINITY;
+      }
+    // the stage of the previous step is free in every warp now
+    if (step >= 1 && step - 1 + kStages < n_steps) {
+      if (warp == 0) {
+        if (lane == 0) fence_proxy_async_smem();
+        issue(step - 1 + kStages);
+      }
+      issued = step - 1 + kStages + 1;
+    }
+
+    // ---- online softmax (rows g and g+8), lazy rescaling
+    float mx[2];
+    mx[0] = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    mx[1] = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+    bool move[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(full, mx[hh], 1));
+      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(full, mx[hh], 2));
+      move[hh] = mx[hh] > m_run[hh] + kRescaleSlack;
+    }
+    if (__any_sync(full, move[0] || move[1])) {
+      float alpha[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        alpha[hh] = 1.f;
+        if (move[hh]) {
+          alpha[hh] = m_run[hh] == -INFINITY ? 0.f : exp2f(m_run[hh] - mx[hh]);
+          m_run[hh] = mx[hh];
+        }
+        l_run[hh] *= alpha[hh];
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        o[j][0] *= alpha[0];
+        o[j][1] *= alpha[0];
+        o[j][2] *= alpha[1];
+        o[j][3] *= alpha[1];
+      }
+    }
+    const float base[2] = {m_run[0] == -INFINITY ? 0.f : m_run[0],
+                           m_run[1] == -INFINITY ? 0.f : m_run[1]};
+    float pr[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pr[nt][e] = exp2f(s[nt][e] - base[e >> 1]);
+    l_run[0] += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
+    l_run[1] += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
+    uint32_t pa[4];
+    pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+    pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+    pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+    pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+
+    // ---- O += P V over this warp's value dims: n-tile j, column g <-> dim
+    // 128 warp + 16g + j; tokens {2c, 2c+1, 2c+8, 2c+9}
+    const int vt[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+    uint32_t vw[4][8];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const uint8_t* src = stage + vt[a] * kRowBytes + (kVQuarter * warp + 16 * g) * 2;
+      const uint4 v0 = lds128(src), v1 = lds128(src + 16);
+      vw[a][0] = v0.x; vw[a][1] = v0.y; vw[a][2] = v0.z; vw[a][3] = v0.w;
+      vw[a][4] = v1.x; vw[a][5] = v1.y; vw[a][6] = v1.z; vw[a][7] = v1.w;
+    }
+    if (nvalid < kStepTok) {  // rows past the end hold stale data: zero weight, zero value
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+        if (vt[a] >= nvalid)
+#pragma unroll
+          for (int x = 0; x < 8; ++x) vw[a][x] = 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+      const uint32_t b0v = prmt(vw[0][j >> 1], vw[1][j >> 1], sel);
+      const uint32_t b1v = prmt(vw[2][j >> 1], vw[3][j >> 1], sel);
+      mma16816<false>(o[j], pa, b0v, b1v);
+    }
+  }
+  if (timed_out) {
+    // let every copy still in flight land (bounded) before the ring is reused
+    if (tid == 0) {
+      atomicOr(p.status, MSA_DEV_TIMEOUT);
+      for (int step = stopped; step < issued; ++step)  // one pending phase each
+        mbar_wait(&bars[step % kStages], (step / kStages) & 1);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    l_run[hh] += __shfl_xor_sync(full, l_run[hh], 1);
+    l_run[hh] += __shfl_xor_sync(full, l_run[hh], 2);
+  }
+
+  // ---- this split's partial: m, l per head; acc per head and value dim
+  float* part = p.partials + (((long long)r * p.head_groups + hg) * p.splits + split) * 16 *
+                                 kPartHeadFloats;
+  auto put = [&](float* dst, const float (&acc)[16][4], const float (&m)[2], const float (&l)[2]) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float* ph = dst + (g + 8 * half) * kPartHeadFloats;
+      if (warp == 0 && c == 0) {
+        ph[0] = m[half];
+        ph[1] = l[half];
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        // c0,c1 (half 0) / c2,c3 (half 1): columns 2c, 2c+1 of n-tile j
+        ph[4 + kVQuarter * warp + 16 * (2 * c) + j] = acc[j][2 * half];
+        ph[4 + kVQuarter * warp + 16 * (2 * c + 1) + j] = acc[j][2 * half + 1];
+      }
+    }
+  };
+  const bool single = p.splits == 1;
+  bool poisoned = cta_bad;
+  if (!single) {
+    put(part, o, m_run, l_run);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      unsigned* ctr = p.counters + (long long)r * p.head_groups + hg;
+      if (cta_bad) atomicOr(ctr, 0x80000000u);
+      const unsigned old = atomicAdd(ctr, 1u);
+      flags[0] = (old & 0x7fffffffu) == (unsigned)(p.splits - 1);
+      flags[1] = ((old | (cta_bad ? 0x80000000u : 0u)) & 0x80000000u) != 0;
+      if (flags[0]) *ctr = 0;  // ready for the next call
+    }
+    __syncthreads();
+    if (!flags[0]) return;
+    __threadfence();
+    poisoned = flags[1] != 0;
+  }
+
+  // ---- final: thread t owns head t/8 (of 16) and value dims 64*(t%8) .. +64
+  const int head = tid >> 3, d0 = 64 * (tid & 7);
+  const int h_abs = 16 * hg + head;
+  float M = -INFINITY, Lsum = 0.f, acc[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+  if (!single) {
+    for (int sp = 0; sp < p.splits; ++sp) {
+      const float* ph = p.partials +
+          ((((long long)r * p.head_groups + hg) * p.splits + sp) * 16 + head) * kPartHeadFloats;
+      const float ms = __ldcg(ph), ls = __ldcg(ph + 1);
+      const float mn = fmaxf(M, ms);
+      const float fo = M == -INFINITY ? 0.f : exp2f(M - mn);
+      const float fs = ms == -INFINITY ? 0.f : exp2f(ms - mn);
+      Lsum = Lsum * fo + ls * fs;
+      const float4* a4 = reinterpret_cast<const float4*>(ph + 4 + d0);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float4 v = __ldcg(a4 + j);
+        acc[4 * j] = acc[4 * j] * fo + v.x * fs;
+        acc[4 * j + 1] = acc[4 * j + 1] * fo + v.y * fs;
+        acc[4 * j + 2] = acc[4 * j + 2] * fo + v.z * fs;
+        acc[4 * j + 3] = acc[4 * j + 3] * fo + v.w * fs;
+      }
+      M = mn;
+    }
+  } else {
+    // one split: stage this CTA's accumulators through shared memory
+    __syncthreads();
+    float* stage_f = reinterpret_cast<float*>(smem);  // the ring is free now
+    put(stage_f, o, m_run, l_run);
+    __syncthreads();
+    const float* ph = stage_f + head * kPartHeadFloats;
+    M = ph[0];
+    Lsum = ph[1];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) acc[j] = ph[4 + d0 + j];
+  }
+  if (tid == 0 && poisoned) atomicOr(p.status, MSA_DEV_BAD_TABLE);
+  if (poisoned) {  // a poisoned row is an empty row
+    M = -INFINITY;
+    Lsum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+  }
+  if (h_abs < p.num_heads) {
+    if (p.sinks) {
+      const float sink2 = __ldg(p.sinks + h_abs) * kLog2e;
+      const float Mn = fmaxf(M, sink2);
+      const float f = M == -INFINITY ? 0.f : exp2f(M - Mn);
+      Lsum = Lsum * f + exp2f(sink2 - Mn);
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] *= f;
+      M = Mn;
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + ((long long)r * p.num_heads + h_abs) * kMlaDv + d0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      dst[j] = make_uint4(pack_bf16x2(acc[8 * j] * inv, acc[8 * j + 1] * inv),
+                          pack_bf16x2(acc[8 * j + 2] * inv, acc[8 * j + 3] * inv),
+                          pack_bf16x2(acc[8 * j + 4] * inv, acc[8 * j + 5] * inv),
+                          pack_bf16x2(acc[8 * j + 6] * inv, acc[8 * j + 7] * inv));
+    if ((tid & 7) == 0)
+      p.lse[(long long)r * p.num_heads + h_abs] =
+          (M == -INFINITY || Lsum <= 0.f) ? -INFINITY : (M + log2f(Lsum)) * kLn2;
+  }
+}
+
+}  // namespace
+
+int mla_max_tokens_per_split() { return MlaSmem::kMaxIds; }
+
+cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream) {
+  if (p.num_rows == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       MlaSmem::kBytes);
+  if (e != cudaSuccess) return e;
+  sparse_mla_kernel<<<dim3(p.splits, p.head_groups, p.num_rows), kThreads, MlaSmem::kBytes,
+                      stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -300,6 +300,51 @@ msa_status msa_kv_insert(const msa_batch* batch, const void* k_new, const void* 
                          const void* idx_new, const msa_index_cache* index, int32_t skip_index,
                          uint32_t* dev_status, cudaStream_t stream);
 
+/* Sparse MLA decode operands ["Attention sinks for ROCm AITER sparse MLA"
+ * (vLLM PR 54404), "Implementation breakdown" items 1-2, "Key source
+ * snippets": one latent KV head, the indptr / indices token convention].
+ *   q          [num_rows, num_heads, dqk] bf16
+ *   kv_cache   [num_tokens, dqk] bf16: one latent row per cached token; the
+ *              key is the whole row, the value its first dv values
+ *   kv_indptr  [num_rows + 1] int32, kv_indices [kv_indptr[num_rows]] int32:
+ *              row r attends over token ids kv_indices[kv_indptr[r] ..
+ *              kv_indptr[r+1]) (repeats count as often as they appear)
+ *   max_tokens bound on every row's count; it sizes the work split, and a
+ *              longer row (or an id outside [0, num_tokens)) makes that row
+ *              an empty row and raises MSA_DEV_BAD_TABLE
+ *   sinks      fp32 [num_heads] or NULL;  softmax_scale as for attention
+ *   out        [num_rows, num_heads, dv] bf16;  lse [num_rows, num_heads] fp32
+ * For head h: s_t = softmax_scale * (q_h . kv_t[0:dqk]),
+ * m = max(max_t s_t, sink_h), den = sum_t exp(s_t - m) + exp(sink_h - m),
+ * out = sum_t exp(s_t - m) kv_t[0:dv] / den, lse = m + ln(den).
+ * Supported: dqk == 576, dv == 512 (512 latent + 64 rope), 1 <= num_heads
+ * <= 128, num_rows <= 65535. */
+typedef struct msa_mla_args {
+  const void* q;
+  int32_t num_rows;
+  int32_t num_heads;
+  int32_t dqk;
+  int32_t dv;
+  const void* kv_cache;
+  int64_t num_tokens;
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  int32_t max_tokens;
+  const float* sinks;
+  float softmax_scale;
+  void* out;
+  float* lse;
+} msa_mla_args;
+
+/* Bytes of workspace msa_sparse_mla_decode needs (zero-filled before its
+ * first use; every call leaves its counters back at zero). */
+size_t msa_sparse_mla_workspace_size(int32_t num_rows, int32_t num_heads, int32_t max_tokens);
+
+/* Sparse MLA decode with sinks and a natural-log LSE, as defined above. */
+msa_status msa_sparse_mla_decode(const msa_mla_args* mla, void* workspace,
+                                 size_t workspace_bytes, uint32_t* dev_status,
+                                 cudaStream_t stream);
+
 /* Bytes of workspace msa_decode (bt_stride > 0) or msa_sparse_paged_attn
  * (bt_stride = 0, topk = 0) needs for these sizes. */
 size_t msa_workspace_size(int32_t num_rows, int32_t bt_stride, int32_t topk, int32_t num_heads,

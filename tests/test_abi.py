@@ -109,3 +109,25 @@ def test_sinks_contract_checked_in_binding():
         B.check_sinks(torch.zeros(8), 16)
     with pytest.raises(ValueError):
         B.check_sinks(torch.zeros(32)[::2], 16)
+
+
+def test_mla_host_validation_without_gpu(lib):
+    from block_sparse_paged_02_gb300 import binding as B
+    fake = ctypes.c_void_p(0x10000)
+    st = ctypes.c_void_p(0x20000)
+    def args(**kw):
+        a = dict(q=fake, num_rows=2, num_heads=16, dqk=576, dv=512, kv_cache=fake,
+                 num_tokens=100, kv_indptr=fake, kv_indices=fake, max_tokens=64, sinks=None,
+                 softmax_scale=0.1, out=fake, lse=fake)
+        a.update(kw)
+        return B.msa_mla_args(**a)
+    call = lambda a, n=1 << 30: lib.msa_sparse_mla_decode(ctypes.byref(a), fake, n, st, None)
+    assert lib.msa_sparse_mla_decode(None, fake, 0, st, None) == B.MSA_ERR_NULL
+    assert call(args(dqk=128)) == B.MSA_ERR_UNSUPPORTED
+    assert call(args(dv=448)) == B.MSA_ERR_UNSUPPORTED
+    assert call(args(num_heads=129)) == B.MSA_ERR_UNSUPPORTED
+    assert call(args(max_tokens=0)) == B.MSA_ERR_SHAPE
+    assert call(args(kv_indices=None)) == B.MSA_ERR_NULL
+    assert call(args(q=ctypes.c_void_p(0x10008))) == B.MSA_ERR_SHAPE
+    assert call(args(num_rows=64), n=16) == B.MSA_ERR_WORKSPACE
+    assert B.msa_sparse_mla_workspace_size(64, 16, 2048) > B.msa_sparse_mla_workspace_size(1, 16, 16)
