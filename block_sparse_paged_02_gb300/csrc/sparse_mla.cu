@@ -31,8 +31,11 @@ constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStepTok = 16;                       // tokens per step
 constexpr int kRowBytes = kMlaDqk * 2;             // 1152 B per cached token
+// staged rows are 1168 B apart (16 B more than a row): the 8 rows an
+// ldmatrix reads then start 4 banks apart, which makes every read conflict-free
+constexpr int kRowPitch = kRowBytes + 16;
 constexpr int kStages = 4;
-constexpr int kStageBytes = kStepTok * kRowBytes;  // 18 KB
+constexpr int kStageBytes = kStepTok * kRowPitch;  // 18.25 KB
 constexpr int kKQuarter = kMlaDqk / kWarps;        // 144 dims of the logits per warp
 constexpr int kKSteps = kKQuarter / 16;            // 9
 constexpr int kVQuarter = kMlaDv / kWarps;         // 128 value dims per warp
@@ -52,11 +55,20 @@ struct MlaSmem {
   static constexpr int kBytes = kFlags + 64;
 };
 
-__device__ __forceinline__ uint2 lds64(const void* p) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p))
+// four 8x8 b16 matrices; lane l gives the row address of matrix l/8, row l%8
+// and receives (row g, cols 2c, 2c+1) of each (transposed: (rows 2c, 2c+1, col g))
+__device__ __forceinline__ void ldsm_x4(const void* row, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(row))
                : "memory");
-  return v;
+}
+
+__device__ __forceinline__ void ldsm_x4_t(const void* row, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(row))
+               : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch p) {
@@ -98,29 +110,35 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
     if (lane == 0) mbar_arrive_expect_tx(&bars[st], (uint32_t)cnt * kRowBytes);
     __syncwarp();
     if (lane < cnt)
-      bulk_g2s(ring + st * kStageBytes + lane * kRowBytes,
+      bulk_g2s(ring + st * kStageBytes + lane * kRowPitch,
                p.kv + (long long)ids[t0 + lane] * kMlaDqk, kRowBytes, &bars[st]);
   };
   if (warp == 0)
     for (int s = 0; s < min(n_steps, kStages); ++s) issue(s);
 
-  // ---- query fragments: heads 16hg + {g, g+8}, dims [144 warp, +144) with
-  // the k-slot permutation of the keys: k-step kk, slots (2c, 2c+1) <-> dims
-  // 36c + 4kk + {0,1}, (2c+8, 2c+9) <-> 36c + 4kk + {2,3}
+  // ---- query fragments (A of S = Q K^T): heads 16hg + {g, g+8}, k-step kk
+  // of this warp's dims [144 warp, +144): columns 16kk + 2c (+1) and +8
   uint32_t qa[kKSteps][4];
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int h = 16 * hg + g + 8 * half;
-    const uint16_t* qrow = p.q + ((long long)r * p.num_heads + h) * kMlaDqk + kKQuarter * warp +
-                           36 * c;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        p.q + ((long long)r * p.num_heads + h) * kMlaDqk + kKQuarter * warp + 2 * c);
 #pragma unroll
     for (int kk = 0; kk < kKSteps; ++kk) {
-      uint2 w = make_uint2(0u, 0u);
-      if (h < p.num_heads) w = *reinterpret_cast<const uint2*>(qrow + 4 * kk);
-      qa[kk][half] = w.x;
-      qa[kk][2 + half] = w.y;
+      const bool live = h < p.num_heads;
+      qa[kk][half] = live ? __ldg(qrow + 8 * kk) : 0u;          // cols 16kk + 2c, +1
+      qa[kk][2 + half] = live ? __ldg(qrow + 8 * kk + 4) : 0u;  // cols 16kk + 8 + 2c, +1
     }
   }
+  // ldmatrix row addresses of this lane: matrix mi = lane / 8, row lane % 8
+  const int mi = lane >> 3, mrow = lane & 7;
+  // K (B of Q K^T, k = dims, n = tokens): matrices (tokens 0-7 | 8-15) x
+  // (dims 16kk + 0-7 | 8-15) give n-tile 0's and 1's two k-halves
+  const int k_off = ((mi >> 1) * 8 + mrow) * kRowPitch + (kKQuarter * warp + (mi & 1) * 8) * 2;
+  // V (B of P V, k = tokens, n = dims), transposed: matrices (tokens 0-7 |
+  // 8-15) x (dims 16jj + 0-7 | 8-15) give n-tiles 2jj and 2jj+1
+  const int v_off = ((mi & 1) * 8 + mrow) * kRowPitch + (kVQuarter * warp + (mi >> 1) * 8) * 2;
   const float scale2 = p.softmax_scale * kLog2e;  // logits in log2 units
 
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
@@ -140,14 +158,13 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
     // ---- partial logits over this warp's 144 dims: n-tile nt = tokens 8nt + g
     float s[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-      const uint8_t* krow = stage + (8 * nt + g) * kRowBytes + (kKQuarter * warp + 36 * c) * 2;
+    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < kKSteps; ++kk) {
-        const uint2 kw = lds64(krow + 8 * kk);
-        mma16816<false>(s[nt], qa[kk], kw.x, kw.y);
-      }
+    for (int kk = 0; kk < kKSteps; ++kk) {
+      uint32_t kb[4];
+      ldsm_x4(stage + k_off + 32 * kk, kb);
+      mma16816<false>(s[0], qa[kk], kb[0], kb[1]);
+      mma16816<false>(s[1], qa[kk], kb[2], kb[3]);
     }
     float* xw = xchg + (step & 1) * kXchgFloats;
 #pragma unroll
@@ -226,30 +243,22 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
     pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
     pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
 
-    // ---- O += P V over this warp's value dims: n-tile j, column g <-> dim
-    // 128 warp + 16g + j; tokens {2c, 2c+1, 2c+8, 2c+9}
-    const int vt[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
-    uint32_t vw[4][8];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const uint8_t* src = stage + vt[a] * kRowBytes + (kVQuarter * warp + 16 * g) * 2;
-      const uint4 v0 = lds128(src), v1 = lds128(src + 16);
-      vw[a][0] = v0.x; vw[a][1] = v0.y; vw[a][2] = v0.z; vw[a][3] = v0.w;
-      vw[a][4] = v1.x; vw[a][5] = v1.y; vw[a][6] = v1.z; vw[a][7] = v1.w;
-    }
-    if (nvalid < kStepTok) {  // rows past the end hold stale data: zero weight, zero value
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-        if (vt[a] >= nvalid)
-#pragma unroll
-          for (int x = 0; x < 8; ++x) vw[a][x] = 0u;
+    // ---- O += P V over this warp's value dims (n-tile j = dims 8j .. 8j+7);
+    // rows past the end of the list hold stale or unwritten data: their
+    // value halves are zeroed (their weight is already 0)
+    uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;  // tokens (2c, 2c+1), (2c+8, 2c+9)
+    if (nvalid < kStepTok) {
+      keep_lo = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
+      keep_hi = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
-      const uint32_t b0v = prmt(vw[0][j >> 1], vw[1][j >> 1], sel);
-      const uint32_t b1v = prmt(vw[2][j >> 1], vw[3][j >> 1], sel);
-      mma16816<false>(o[j], pa, b0v, b1v);
+    for (int jj = 0; jj < 8; ++jj) {
+      uint32_t vb[4];
+      ldsm_x4_t(stage + v_off + 32 * jj, vb);
+      const uint32_t b0[2] = {vb[0] & keep_lo, vb[2] & keep_lo};
+      const uint32_t b1[2] = {vb[1] & keep_hi, vb[3] & keep_hi};
+      mma16816<false>(o[2 * jj], pa, b0[0], b1[0]);
+      mma16816<false>(o[2 * jj + 1], pa, b0[1], b1[1]);
     }
   }
   if (timed_out) {
@@ -280,9 +289,9 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        // c0,c1 (half 0) / c2,c3 (half 1): columns 2c, 2c+1 of n-tile j
-        ph[4 + kVQuarter * warp + 16 * (2 * c) + j] = acc[j][2 * half];
-        ph[4 + kVQuarter * warp + 16 * (2 * c + 1) + j] = acc[j][2 * half + 1];
+        // c0,c1 (half 0) / c2,c3 (half 1): dims 8j + 2c, +1 of this warp's 128
+        ph[4 + kVQuarter * warp + 8 * j + 2 * c] = acc[j][2 * half];
+        ph[4 + kVQuarter * warp + 8 * j + 2 * c + 1] = acc[j][2 * half + 1];
       }
     }
   };
