@@ -150,12 +150,12 @@ AttnLaunch make_attn(const msa_attn_args* a, const int32_t* tbl, int tbl_stride,
 msa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
 
 // Sparse MLA work split: splits of each (row, 16-head group) so that the
-// grid fills two CTAs per SM, each split at least 64 and at most
+// grid fills MSA_MLA_CTAS CTAs per SM, each split at least 64 and at most
 // mla_max_tokens_per_split() token ids, a multiple of 16.
 void mla_split(int num_rows, int num_heads, int max_tokens, int* splits, int* per) {
   const int groups = (num_heads + 15) / 16;
   const long long base = (long long)num_rows * groups;
-  const int capacity = device_sm_count() * 2;
+  const int capacity = device_sm_count() * MSA_MLA_CTAS;
   int s = base > 0 ? (int)max(1ll, capacity / base) : 1;
   const int lim = mla_max_tokens_per_split();
   s = max(s, (max_tokens + lim - 1) / lim);

@@ -41,6 +41,10 @@ constexpr int kMaxSplitEntries = 128;
 #ifndef MSA_ATTN_CTAS_BF16
 #define MSA_ATTN_CTAS_BF16 2
 #endif
+// sparse MLA: the grid is sized for this many CTAs per SM (2 resident)
+#ifndef MSA_MLA_CTAS
+#define MSA_MLA_CTAS 2
+#endif
 // bf16 index keys: scored on CUDA-core FMAs (0) or on warp MMA (1)
 #ifndef MSA_SCORE_BF16_KIND
 #define MSA_SCORE_BF16_KIND 0

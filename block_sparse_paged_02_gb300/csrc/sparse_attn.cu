@@ -39,6 +39,8 @@ template <bool FP8>
 struct AttnCfg {
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kSlab = kPage16 * kHeadDim * kElem;  // one page-16 K (or V) slab
+  // (copying the 16 token rows one by one into bank-staggered rows removes
+  // the K fragments' bank conflicts but measured slower: 24.6 vs 20.0 us)
   static constexpr int kStageBytes = 2 * kSlab + 2 * 64;    // K, V, k-scales, v-scales
   static constexpr int kStages = FP8 ? MSA_ATTN_STAGES_FP8 : MSA_ATTN_STAGES_BF16;
   static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
@@ -169,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
   bool timed_out = false;
+  int issued = min(n_my, C::kStages);  // entries whose copies this warp has issued
+  int stopped = n_my;                  // first entry not consumed
   // Two page-16 slabs (A = warp entry i, B = entry i+1) per iteration: four
   // independent S chains, one softmax pass over 32 tokens and 32 P.V MMAs,
   // which doubles the independent work the warp has in flight.  A missing B
@@ -181,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
     if (has_b) ready = ready && mbar_wait(&wbar[st_b], ((i + 1) / C::kStages) & 1);
     if (!__all_sync(full, ready)) {
       timed_out = true;
+      stopped = i;
       break;
     }
     const uint8_t* stage[2] = {ring + st_a * C::kStageBytes, ring + st_b * C::kStageBytes};
@@ -374,10 +379,16 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
           fence_proxy_async_smem();
           issue(nxt, e);
         }
+        issued = nxt + 1;
       }
     }
   }
-  if (timed_out && lane == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
+  if (timed_out && lane == 0) {
+    atomicOr(p.status, MSA_DEV_TIMEOUT);
+    // let this warp's copies still in flight land (bounded) before the ring
+    // is reused for the merge
+    for (int j = stopped; j < issued; ++j) mbar_wait(&wbar[j % C::kStages], (j / C::kStages) & 1);
+  }
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 1);

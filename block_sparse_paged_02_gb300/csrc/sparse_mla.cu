@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) xw[(warp * 32 + lane) * 8 + 4 * nt + e] = s[nt][e];
+      for (int e = 0; e < 4; ++e) xw[(warp * 8 + 4 * nt + e) * 32 + lane] = s[nt][e];
     // one barrier per step, which also makes a wait that gave up in any warp
     // a CTA-wide decision
     if (__syncthreads_or(late)) {
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
       for (int e = 0; e < 4; ++e) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += xw[(w * 32 + lane) * 8 + 4 * nt + e];
+        for (int w = 0; w < kWarps; ++w) v += xw[(w * 8 + 4 * nt + e) * 32 + lane];
         const int t = 8 * nt + 2 * c + (e & 1);
         s[nt][e] = t < nvalid ? v * scale2 : -INFINITY;
       }
