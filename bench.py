@@ -172,7 +172,7 @@ class ClockSampler:
 
 # --------------------------------------------------------------------- arms
 
-def cpu_oracle_run(w, budget_s: float = 12.0, max_reps: int = 3):
+def cpu_oracle_run(w, budget_s: float = 12.0, max_reps: int = 1 << 20):
     import oracle
     oracle.build()
     threads = oracle.default_threads()
