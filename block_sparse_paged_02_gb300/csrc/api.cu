@@ -44,6 +44,10 @@ void attn_split(int num_rows, int max_entries, int ctas_per_sm, int* pps, int* s
   if (target < 1) target = 1;
   int per = (max_entries + target - 1) / target;
   per = per < 4 ? 4 : (per + 3) / 4 * 4;
+  // at most 8 splits (one thread-block cluster merges them) whenever the
+  // entries fit: the cluster merge is much cheaper than the workspace one
+  if ((max_entries + per - 1) / per > 8 && max_entries <= 8 * kMaxSplitEntries)
+    per = ((max_entries + 7) / 8 + 3) / 4 * 4;
   if (per > kMaxSplitEntries) per = kMaxSplitEntries;
   *pps = per;
   *splits = max_entries > 0 ? (max_entries + per - 1) / per : 1;

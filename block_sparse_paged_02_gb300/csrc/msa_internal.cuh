@@ -130,6 +130,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 2-D tiled tensor copy global -> shared (box of the map at x, y), completion
+// on `bar`.  x times the element size is a multiple of 16 bytes; the box
+// lies inside the tensor; dst is 1024-byte aligned for 128-byte swizzle.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(const void* p) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -267,6 +279,12 @@ struct AttnLaunch {
 };
 
 cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream);
+// Host: 2-D tensor map [rows][inner] (row pitch row_stride_bytes) with
+// box_inner x box_rows boxes and 128-byte swizzle; false if the driver entry
+// point is missing or the encoder rejects the shape.
+bool tensor_maps_available();
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, long long inner,
+                   long long rows, long long row_stride_bytes, int box_inner, int box_rows);
 cudaError_t launch_index_score_tc(const ScoreLaunch& p, cudaStream_t stream);
 bool tc_score_supported(int index_heads, int index_dim);
 struct KvInsertLaunch {

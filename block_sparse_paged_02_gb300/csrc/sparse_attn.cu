@@ -22,6 +22,8 @@
 // finished by whichever CTA of the row arrives last (atomic counter, reset
 // by that CTA: no spin-wait anywhere).  The sink joins the denominator only
 // in the final merge.
+#include <string.h>
+
 #include "msa_internal.cuh"
 
 namespace msa {
@@ -34,31 +36,115 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;  // log2 units: unnormalised weights stay <= 256
 constexpr int kAccStride = 132;  // padded head stride of the shared-memory merge area
 constexpr int kAccWarpFloats = kMaxHeads * kAccStride;  // 2112
+// a row's splits merge inside one thread-block cluster when there are at
+// most this many (the portable cluster size); more splits merge through the
+// workspace (last-arriving CTA)
+constexpr int kMaxClusterSplits = 8;
+// per-CTA partial for the cluster merge, after the warps' merge area:
+// acc [16][128], m [16], l [16], poison flag
+constexpr int kCPart = kWarps * (kAccWarpFloats + 2 * kMaxHeads) * 4;
+constexpr int kCpM = kMaxHeads * kHeadDim, kCpL = kCpM + kMaxHeads, kCpFlag = kCpL + kMaxHeads;
+constexpr int kCPartBytes = (kCpFlag + 4) * 4;
 
 template <bool FP8>
 struct AttnCfg {
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kSlab = kPage16 * kHeadDim * kElem;  // one page-16 K (or V) slab
-  // (copying the 16 token rows one by one into bank-staggered rows removes
-  // the K fragments' bank conflicts but measured slower: 24.6 vs 20.0 us)
-  static constexpr int kStageBytes = 2 * kSlab + 2 * 64;    // K, V, k-scales, v-scales
   static constexpr int kStages = FP8 ? MSA_ATTN_STAGES_FP8 : MSA_ATTN_STAGES_BF16;
-  static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+  // rings of the 4 warps: K slabs, then V slabs (each slab 1024-byte aligned,
+  // as the 128-byte swizzle of the FP8 tensor copies needs), then scales
+  static constexpr int kSlots = kWarps * kStages;
+  static constexpr int kRingK = 0;
+  static constexpr int kRingV = kSlots * kSlab;
+  static constexpr int kRingS = 2 * kSlots * kSlab;
+  static constexpr int kRingBytes = kRingS + kSlots * 128;
   static constexpr int kMergeBytes = kWarps * (kAccWarpFloats + 2 * kMaxHeads) * 4;
   static constexpr int kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
   static constexpr int kQBytes = kMaxHeads * kHeadDim * 2;  // the row's queries, bf16
   static constexpr int kQ = kDataBytes;
   static constexpr int kBarOff = kQ + kQBytes;
-  static constexpr int kSmemBytes = kBarOff + (kWarps * kStages + 1) * 8 + 64;
+  static constexpr int kSmemBytes = kBarOff + (kSlots + 1) * 8 + 64;
+  static_assert(kCPart + kCPartBytes <= kDataBytes, "cluster partial must fit the ring");
 };
+
+// four 8x8 b16 matrices from a shared-memory address; lane l gives the row
+// address of matrix l/8, row l%8 and receives (row g, cols 2c, 2c+1) of each
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
 
 __device__ __forceinline__ int acc_index(int head, int dim) {
   return head * kAccStride + dim + (dim >> 5);
 }
 
-template <bool FP8, int SCALE>
+// ---- the row's output: sink in the denominator, 1/L (and the scalar v
+// scale), bf16 O for dims d0..d0+N of `head`, natural-log LSE
+template <int N, int SCALE>
+__device__ __forceinline__ void finalize_out(const AttnLaunch& p, int r, int head, int d0,
+                                             float (&acc)[N], float M, float Lsum, bool write_lse) {
+  if (p.sinks) {
+    const float sink2 = __ldg(p.sinks + head) * kLog2e;
+    const float Mn = fmaxf(M, sink2);
+    Lsum = (M == -INFINITY ? 0.f : Lsum * exp2f(M - Mn)) + exp2f(sink2 - Mn);
+    const float f = M == -INFINITY ? 0.f : exp2f(M - Mn);
+#pragma unroll
+    for (int j = 0; j < N; ++j) acc[j] *= f;
+    M = Mn;
+  }
+  float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
+  if constexpr (SCALE == MSA_SCALE_SCALAR) inv *= __ldg(p.v_scale);
+  uint32_t packed[N / 2];
+#pragma unroll
+  for (int j = 0; j < N / 2; ++j) packed[j] = pack_bf16x2(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+  uint16_t* o = p.out + ((long long)r * p.num_heads + head) * kHeadDim + d0;
+  if constexpr (N == 16) {
+    reinterpret_cast<uint4*>(o)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    reinterpret_cast<uint4*>(o)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  } else {
+    *reinterpret_cast<uint2*>(o) = make_uint2(packed[0], packed[1]);
+  }
+  if (write_lse)
+    p.lse[(long long)r * p.num_heads + head] =
+        (M == -INFINITY || Lsum <= 0.f) ? -INFINITY : (M + log2f(Lsum)) * kLn2;
+}
+
+// ---- thread-block cluster helpers (the splits of one row)
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// the address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+template <bool FP8, int SCALE, bool CL>
 __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_CTAS_BF16)
-    sparse_attn_kernel(const AttnLaunch p) {
+    sparse_attn_kernel(const AttnLaunch p, const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap) {
   using C = AttnCfg<FP8>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
@@ -102,66 +188,79 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
   if (lane < n_my) entry_bad = my_e < 0 || my_e >= p.num_pages16;
   __syncthreads();  // barrier inits visible to every warp
   const bool cta_bad = __syncthreads_or(entry_bad) != 0;
-  if (!active) {
-    // still drain the query copy this CTA issued before leaving
+  if (!CL && !active) {
+    // still drain the query copy this CTA issued before leaving (a CTA of a
+    // cluster stays: it takes part in the merge with an empty partial)
     if (tid == 0 && !mbar_wait(qbar, 0)) atomicOr(p.status, MSA_DEV_TIMEOUT);
     return;
   }
   if (cta_bad) n_my = 0;  // never copy from an id outside the pool
   const bool single = n_active == 1;
   if (single && (len_bad || cta_bad) && tid == 0) atomicOr(p.status, MSA_DEV_BAD_TABLE);
-  uint8_t* ring = smem + (size_t)warp * C::kStages * C::kStageBytes;
-  uint64_t* wbar = bars + warp * C::kStages;
+  const int slot0 = warp * C::kStages;  // this warp's first ring slot
+  uint64_t* wbar = bars + slot0;
 
   auto issue = [&](int i, long long e) {  // lane 0 only
     const int st = i % C::kStages;
-    uint8_t* dst = ring + st * C::kStageBytes;
+    uint8_t* kd = smem + C::kRingK + (slot0 + st) * C::kSlab;
+    uint8_t* vd = smem + C::kRingV + (slot0 + st) * C::kSlab;
     const uint32_t bytes = 2 * C::kSlab + (SCALE == MSA_SCALE_PER_TOKEN_HEAD ? 128 : 0);
     mbar_arrive_expect_tx(&wbar[st], bytes);
-    bulk_g2s(dst, p.k + e * C::kSlab, C::kSlab, &wbar[st]);
-    bulk_g2s(dst + C::kSlab, p.v + e * C::kSlab, C::kSlab, &wbar[st]);
+    if constexpr (FP8) {
+      // 16 rows x 128 B boxes, 128-byte swizzled: the fragment reads below
+      // then hit 32 distinct banks per phase
+      tma_load_2d(kd, &kmap, 0, (int)(e * kPage16), &wbar[st]);
+      tma_load_2d(vd, &vmap, 0, (int)(e * kPage16), &wbar[st]);
+    } else {
+      bulk_g2s(kd, p.k + e * C::kSlab, C::kSlab, &wbar[st]);
+      bulk_g2s(vd, p.v + e * C::kSlab, C::kSlab, &wbar[st]);
+    }
     if constexpr (SCALE == MSA_SCALE_PER_TOKEN_HEAD) {
-      bulk_g2s(dst + 2 * C::kSlab, p.k_scale + e * kPage16, 64, &wbar[st]);
-      bulk_g2s(dst + 2 * C::kSlab + 64, p.v_scale + e * kPage16, 64, &wbar[st]);
+      uint8_t* sd = smem + C::kRingS + (slot0 + st) * 128;
+      bulk_g2s(sd, p.k_scale + e * kPage16, 64, &wbar[st]);
+      bulk_g2s(sd + 64, p.v_scale + e * kPage16, 64, &wbar[st]);
     }
   };
   for (int i = 0; i < min(n_my, C::kStages); ++i) {
     const long long e = __shfl_sync(full, my_e, i);
     if (lane == 0) issue(i, e);
   }
-  if (!__syncthreads_and(mbar_wait(qbar, 0))) {  // CTA-uniform decision
+  const bool q_ok = __syncthreads_and(mbar_wait(qbar, 0)) != 0;  // CTA-uniform decision
+  if (!q_ok) {
     if (tid == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
     n_my = 0;
   }
 
-  // ---- query fragments (A operand of S = Q K^T), permuted k-slots:
-  // k-step kk, slots (2c, 2c+1) <-> dims 32c+4kk+{0,1}; (2c+8, 2c+9) <-> +{2,3}
-  uint32_t qa[8][4];
+  // ---- queries into the A-operand order of S = Q K^T, in place: k-step kk,
+  // slots (2c, 2c+1) <-> dims 32c+4kk+{0,1} and (2c+8, 2c+9) <-> +{2,3}, so
+  // that one 16-byte read per lane covers four k-steps of a key row.  The
+  // shared copy is [kk][slot half][head][8 slots] (2-byte elements, f16 for
+  // FP8 keys), which makes every ldmatrix phase read 128 contiguous bytes.
+  if (q_ok) {
+    uint32_t qw[2][4];
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    // head row h, dims [32c, 32c+32): four 16-byte loads, 16 bf16 pairs
-    const int h = g + 8 * half;
-    uint32_t w[16];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int k2 = 0; k2 < 2; ++k2) {  // chunks tid and tid + 128: head t/16, dims 8(t%16)..+8
+      const int t = tid + kThreads * k2, h = t >> 4;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (h < p.num_heads) v = lds128(q_s + h * kHeadDim * 2 + 64 * c + 16 * j);
-      w[4 * j] = v.x;
-      w[4 * j + 1] = v.y;
-      w[4 * j + 2] = v.z;
-      w[4 * j + 3] = v.w;
+      if (h < p.num_heads) v = lds128(q_s + 16 * t);
+      qw[k2][0] = v.x; qw[k2][1] = v.y; qw[k2][2] = v.z; qw[k2][3] = v.w;
     }
+    __syncthreads();
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t w01 = w[2 * kk], w23 = w[2 * kk + 1];  // dims 32c+4kk+{0,1} and +{2,3}
-      if constexpr (FP8) {  // f16 operands for the fp8 path
-        w01 = pack_f16x2(bf16lo(w01), bf16hi(w01));
-        w23 = pack_f16x2(bf16lo(w23), bf16hi(w23));
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int t = tid + kThreads * k2, h = t >> 4, q = t & 15;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {  // dims 8q+2w, +1: c = q/4, kk = 2(q%4) + w/2, half w%2
+        uint32_t x = qw[k2][w];
+        if constexpr (FP8) x = pack_f16x2(bf16lo(x), bf16hi(x));  // f16 operands for FP8 keys
+        const int kk = 2 * (q & 3) + (w >> 1);
+        *reinterpret_cast<uint32_t*>(smem + C::kQ + kk * 512 + (w & 1) * 256 + h * 16 + 4 * (q >> 2)) = x;
       }
-      qa[kk][half] = w01;      // a0a1 (row g) / a2a3 (row g+8)
-      qa[kk][2 + half] = w23;  // a4a5 (row g) / a6a7 (row g+8)
     }
   }
+  __syncthreads();
+  // ldmatrix row address of this lane: matrix lane/8 = (half lane/16, heads 8*((lane/8)&1)..)
+  const uint32_t qa_addr = smem_u32(smem + C::kQ) + (lane >> 4) * 256 + (lane & 15) * 16;
   float scale2 = p.softmax_scale * kLog2e;  // logits in log2 units
   if constexpr (SCALE == MSA_SCALE_SCALAR) scale2 *= __ldg(p.k_scale);
 
@@ -170,6 +269,13 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
 #pragma unroll
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
+  // 128-byte swizzle of the FP8 slabs: 16-byte chunk j of row t sits at chunk
+  // j ^ (t % 8).  K rows of this lane are g (mod 8); V rows are vt[a].
+  const int koff0 = 16 * ((2 * c) ^ g), koff1 = 16 * ((2 * c + 1) ^ g);
+  const int vt[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+  int voff[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) voff[a] = vt[a] * kHeadDim + 16 * (g ^ (vt[a] & 7));
   bool timed_out = false;
   int issued = min(n_my, C::kStages);  // entries whose copies this warp has issued
   int stopped = n_my;                  // first entry not consumed
@@ -188,7 +294,11 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
       stopped = i;
       break;
     }
-    const uint8_t* stage[2] = {ring + st_a * C::kStageBytes, ring + st_b * C::kStageBytes};
+    const int sl_a = slot0 + st_a, sl_b = slot0 + st_b;
+    const uint8_t* kst[2] = {smem + C::kRingK + sl_a * C::kSlab, smem + C::kRingK + sl_b * C::kSlab};
+    const uint8_t* vst[2] = {smem + C::kRingV + sl_a * C::kSlab, smem + C::kRingV + sl_b * C::kSlab};
+    const float* sst[2] = {reinterpret_cast<const float*>(smem + C::kRingS + sl_a * 128),
+                           reinterpret_cast<const float*>(smem + C::kRingS + sl_b * 128)};
     const int tok_a = (e_begin + warp + kWarps * i) * kPage16;  // row token index of A's slot 0
     const int nvalid[2] = {min(kPage16, len - tok_a),
                            has_b ? min(kPage16, len - tok_a - kWarps * kPage16) : 0};
@@ -201,22 +311,26 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
       uint32_t kw[4][8];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const uint8_t* krow = stage[u >> 1] + (8 * (u & 1) + g) * kHeadDim + 32 * c;
-        const uint4 k0 = lds128(krow), k1 = lds128(krow + 16);
+        // row 8(u&1)+g, 16-byte chunks 2c and 2c+1 at their swizzled places
+        const uint8_t* krow = kst[u >> 1] + (8 * (u & 1) + g) * kHeadDim;
+        const uint4 k0 = lds128(krow + koff0), k1 = lds128(krow + koff1);
         kw[u][0] = k0.x; kw[u][1] = k0.y; kw[u][2] = k0.z; kw[u][3] = k0.w;
         kw[u][4] = k1.x; kw[u][5] = k1.y; kw[u][6] = k1.z; kw[u][7] = k1.w;
       }
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t qa[4];
+        ldsm_x4(qa_addr + kk * 512u, qa);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          mma16816<true>(s[u], qa[kk], e4m3x2_to_f16x2((uint16_t)(kw[u][kk] & 0xffffu)),
+          mma16816<true>(s[u], qa, e4m3x2_to_f16x2((uint16_t)(kw[u][kk] & 0xffffu)),
                          e4m3x2_to_f16x2((uint16_t)(kw[u][kk] >> 16)));
+      }
     } else {
       uint32_t kw[4][16];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const uint8_t* krow = stage[u >> 1] + ((8 * (u & 1) + g) * kHeadDim + 32 * c) * 2;
+        const uint8_t* krow = kst[u >> 1] + ((8 * (u & 1) + g) * kHeadDim + 32 * c) * 2;
 #pragma unroll
         for (int h4 = 0; h4 < 4; ++h4) {
           const uint4 v = lds128(krow + 16 * h4);
@@ -224,9 +338,12 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
         }
       }
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t qa[4];
+        ldsm_x4(qa_addr + kk * 512u, qa);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) mma16816<false>(s[u], qa[kk], kw[u][2 * kk], kw[u][2 * kk + 1]);
+        for (int u = 0; u < 4; ++u) mma16816<false>(s[u], qa, kw[u][2 * kk], kw[u][2 * kk + 1]);
+      }
     }
     // ---- scale, mask, online softmax over the 32 tokens (rows g and g+8)
 #pragma unroll
@@ -236,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
         const int t = 8 * (u & 1) + 2 * c + (e & 1);
         float v = s[u][e] * scale2;
         if constexpr (SCALE == MSA_SCALE_PER_TOKEN_HEAD)
-          v *= reinterpret_cast<const float*>(stage[u >> 1] + 2 * C::kSlab)[t];
+          v *= sst[u >> 1][t];
         s[u][e] = t < nvalid[u >> 1] ? v : -INFINITY;
       }
     float mx[2];
@@ -290,8 +407,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
       for (int u = 0; u < 4; ++u)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          pr[u][e] *= reinterpret_cast<const float*>(stage[u >> 1] + 2 * C::kSlab + 64)
-              [8 * (u & 1) + 2 * c + (e & 1)];
+          pr[u][e] *= sst[u >> 1][kPage16 + 8 * (u & 1) + 2 * c + (e & 1)];
     }
     // P as the A operand of O += P V, per slab: tokens (2c, 2c+1) from its
     // first n-tile, (2c+8, 2c+9) from its second
@@ -311,15 +427,13 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
       }
     }
     // ---- V fragments: tokens {2c, 2c+1, 2c+8, 2c+9}, dims 16g + j for n-tile j
-    const int vt[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
     if constexpr (FP8) {
       uint32_t vw[2][4][4];
 #pragma unroll
       for (int sl = 0; sl < 2; ++sl) {
-        const uint8_t* vs_ = stage[sl] + C::kSlab;
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-          const uint4 v = lds128(vs_ + vt[a] * kHeadDim + 16 * g);
+          const uint4 v = lds128(vst[sl] + voff[a]);
           vw[sl][a][0] = v.x; vw[sl][a][1] = v.y; vw[sl][a][2] = v.z; vw[sl][a][3] = v.w;
         }
         if (nvalid[sl] < kPage16) {  // never let garbage past the end reach P V
@@ -348,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
         uint32_t vw[4][8];
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-          const uint8_t* src = stage[sl] + C::kSlab + (vt[a] * kHeadDim + 16 * g) * 2;
+          const uint8_t* src = vst[sl] + (vt[a] * kHeadDim + 16 * g) * 2;
           const uint4 v0 = lds128(src), v1 = lds128(src + 16);
           vw[a][0] = v0.x; vw[a][1] = v0.y; vw[a][2] = v0.z; vw[a][3] = v0.w;
           vw[a][4] = v1.x; vw[a][5] = v1.y; vw[a][6] = v1.z; vw[a][7] = v1.w;
@@ -435,6 +549,61 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
     for (int j = 0; j < 16; ++j) acc[j] += f * ar[j];
   }
 
+  if constexpr (CL) {
+    // ---- the row's splits form one cluster: each CTA leaves its partial in
+    // its own shared memory, then every CTA merges a share of the (head,
+    // 4-dim) outputs over all partials through distributed shared memory.
+    float* cp = reinterpret_cast<float*>(smem + kCPart);
+    float4* c4 = reinterpret_cast<float4*>(cp + head * kHeadDim + d0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c4[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+    if ((tid & 7) == 0) {
+      cp[kCpM + head] = mh;
+      cp[kCpL + head] = lh;
+    }
+    if (tid == 0) reinterpret_cast<int*>(cp)[kCpFlag] = (len_bad || cta_bad) ? 1 : 0;
+    cluster_sync();  // every partial of the row is written and visible
+    const uint32_t cp_addr = smem_u32(cp);
+    int fl = 0;
+    if (lane < p.splits) fl = ld_dsmem_s32(mapa_shared(cp_addr + 4u * kCpFlag, (uint32_t)lane));
+    const bool poisoned = __any_sync(full, fl != 0);  // an id outside the pool empties the row
+    if (poisoned && split == 0 && tid == 0) atomicOr(p.status, MSA_DEV_BAD_TABLE);
+    for (int i4 = split * kThreads + tid; i4 < kMaxHeads * kHeadDim / 4; i4 += p.splits * kThreads) {
+      const int h = i4 >> 5, d = 4 * (i4 & 31);
+      if (h >= p.num_heads) break;
+      float M = -INFINITY, L = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!poisoned) {
+        float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
+        float4 v[kMaxClusterSplits];
+#pragma unroll
+        for (int j = 0; j < kMaxClusterSplits; ++j) {
+          if (j < p.splits) {
+            const uint32_t base = mapa_shared(cp_addr, (uint32_t)j);
+            ms[j] = ld_dsmem_f32(base + 4u * (kCpM + h));
+            ls[j] = ld_dsmem_f32(base + 4u * (kCpL + h));
+            v[j] = ld_dsmem_f4(base + 4u * (h * kHeadDim + d));
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxClusterSplits; ++j) M = j < p.splits ? fmaxf(M, ms[j]) : M;
+#pragma unroll
+        for (int j = 0; j < kMaxClusterSplits; ++j) {
+          if (j < p.splits && ms[j] != -INFINITY) {
+            const float f = exp2f(ms[j] - M);
+            L += f * ls[j];
+            a[0] += f * v[j].x;
+            a[1] += f * v[j].y;
+            a[2] += f * v[j].z;
+            a[3] += f * v[j].w;
+          }
+        }
+      }
+      finalize_out<4, SCALE>(p, r, h, d, a, M, L, (i4 & 31) == 0);
+    }
+    cluster_sync();  // no CTA leaves while another may still read its partial
+    return;
+  }
+
   bool empty_row = single && (len_bad || cta_bad);
   if (!single) {
     // ---- publish this split's partial; the last CTA of the row merges all.
@@ -498,37 +667,27 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
   }
-
-  // ---- finalize: sink in the denominator, natural-log LSE
-  if (head < p.num_heads) {
-    float M = mh, Lsum = lh;
-    if (p.sinks) {
-      const float sink2 = __ldg(p.sinks + head) * kLog2e;
-      const float Mn = fmaxf(M, sink2);
-      Lsum = (M == -INFINITY ? 0.f : Lsum * exp2f(M - Mn)) + exp2f(sink2 - Mn);
-      const float f = M == -INFINITY ? 0.f : exp2f(M - Mn);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) acc[j] *= f;
-      M = Mn;
-    }
-    float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
-    if constexpr (SCALE == MSA_SCALE_SCALAR) inv *= __ldg(p.v_scale);
-    uint32_t packed[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) packed[j] = pack_bf16x2(acc[2 * j] * inv, acc[2 * j + 1] * inv);
-    uint4* dst = reinterpret_cast<uint4*>(p.out + ((long long)r * p.num_heads + head) * kHeadDim + d0);
-    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-    if ((tid & 7) == 0)
-      p.lse[(long long)r * p.num_heads + head] =
-          (M == -INFINITY || Lsum <= 0.f) ? -INFINITY : (M + log2f(Lsum)) * kLn2;
-  }
+  if (head < p.num_heads) finalize_out<16, SCALE>(p, r, head, d0, acc, mh, lh, (tid & 7) == 0);
 }
 
 template <bool FP8, int SCALE>
 cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t stream, bool programmatic) {
   using C = AttnCfg<FP8>;
-  auto kern = sparse_attn_kernel<FP8, SCALE>;
+  const bool cl = p.splits <= kMaxClusterSplits;
+  auto kern = cl ? sparse_attn_kernel<FP8, SCALE, true> : sparse_attn_kernel<FP8, SCALE, false>;
+  CUtensorMap kmap, vmap;
+  memset(&kmap, 0, sizeof(kmap));
+  memset(&vmap, 0, sizeof(vmap));
+  if constexpr (FP8) {
+    // the pools as [8P * 16 rows][128 B]; row coordinates must fit an int
+    const long long rows = p.num_pages16 * kPage16;
+    if (rows > 0x7fffffffll ||
+        !encode_map_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.k, kHeadDim, rows, kHeadDim,
+                       kHeadDim, kPage16) ||
+        !encode_map_2d(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.v, kHeadDim, rows, kHeadDim,
+                       kHeadDim, kPage16))
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -537,12 +696,23 @@ cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t stream, bool programmat
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (cl) {  // one cluster per row: its splits
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)p.splits;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (programmatic) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = programmatic ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, p, kmap, vmap);
 }
 
 }  // namespace
