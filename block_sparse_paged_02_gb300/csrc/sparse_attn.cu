@@ -14,14 +14,19 @@
 // on warp MMA with fp32 accumulation (the M = heads = 16 tile is below the
 // 64/128-row minimum of tcgen05, and the path is HBM-bound).  The row's
 // tokens are split across CTAs (grid = splits x rows, sized from the SM
-// count); each warp streams its page-16 K and V slabs (2-4 KB each,
-// contiguous) with 1-D bulk async copies into a private 4-deep shared-memory
-// ring, converts FP8 to f16 in registers (exact), applies per-token k scales
-// to the fp32 logits and folds per-token v scales into P.  Warps merge in
-// shared memory; splits merge through (m, l, acc) partials in the workspace,
-// finished by whichever CTA of the row arrives last (atomic counter, reset
-// by that CTA: no spin-wait anywhere).  The sink joins the denominator only
-// in the final merge.
+// count); each warp streams its page-16 K and V slabs (2 KB each for FP8,
+// contiguous in the pools) into a private shared-memory ring -- FP8 slabs by
+// 2-D tensor copies with the 128-byte swizzle, so that the fragment reads of
+// every phase hit 32 distinct banks, bf16 slabs by 1-D bulk copies -- and
+// converts FP8 to f16 in registers (exact), applies per-token k scales to the
+// fp32 logits and folds per-token v scales into P.  The queries sit in
+// shared memory in the MMA's k-slot order and are read with ldmatrix.  Warps
+// merge in shared memory.  Up to 8 splits of a row form one thread-block
+// cluster and merge through distributed shared memory (two cluster barriers,
+// no global round trip); more splits merge through (m, l, acc) partials in
+// the workspace, finished by whichever CTA of the row arrives last (atomic
+// counter, reset by that CTA).  No spin-wait anywhere.  The sink joins the
+// denominator only in the final merge.
 #include <string.h>
 
 #include "msa_internal.cuh"
@@ -63,7 +68,10 @@ struct AttnCfg {
   static constexpr int kQBytes = kMaxHeads * kHeadDim * 2;  // the row's queries, bf16
   static constexpr int kQ = kDataBytes;
   static constexpr int kBarOff = kQ + kQBytes;
-  static constexpr int kSmemBytes = kBarOff + (kSlots + 1) * 8 + 64;
+  // after the barriers: 2 merge flags, then the sinks (log2 units) and the scalar v scale
+  static constexpr int kFlagsOff = kBarOff + (kSlots + 1) * 8;
+  static constexpr int kSinkOff = kFlagsOff + 16;
+  static constexpr int kSmemBytes = kSinkOff + (kMaxHeads + 1) * 4 + 64;
   static_assert(kCPart + kCPartBytes <= kDataBytes, "cluster partial must fit the ring");
 };
 
@@ -83,10 +91,13 @@ __device__ __forceinline__ int acc_index(int head, int dim) {
 // ---- the row's output: sink in the denominator, 1/L (and the scalar v
 // scale), bf16 O for dims d0..d0+N of `head`, natural-log LSE
 template <int N, int SCALE>
-__device__ __forceinline__ void finalize_out(const AttnLaunch& p, int r, int head, int d0,
-                                             float (&acc)[N], float M, float Lsum, bool write_lse) {
+// (sink_s: the sinks in log2 units, then the scalar v scale, staged in
+// shared memory at the kernel's start)
+__device__ __forceinline__ void finalize_out(const AttnLaunch& p, const float* sink_s, int r,
+                                             int head, int d0, float (&acc)[N], float M,
+                                             float Lsum, bool write_lse) {
   if (p.sinks) {
-    const float sink2 = __ldg(p.sinks + head) * kLog2e;
+    const float sink2 = sink_s[head];
     const float Mn = fmaxf(M, sink2);
     Lsum = (M == -INFINITY ? 0.f : Lsum * exp2f(M - Mn)) + exp2f(sink2 - Mn);
     const float f = M == -INFINITY ? 0.f : exp2f(M - Mn);
@@ -95,7 +106,7 @@ __device__ __forceinline__ void finalize_out(const AttnLaunch& p, int r, int hea
     M = Mn;
   }
   float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
-  if constexpr (SCALE == MSA_SCALE_SCALAR) inv *= __ldg(p.v_scale);
+  if constexpr (SCALE == MSA_SCALE_SCALAR) inv *= sink_s[kMaxHeads];
   uint32_t packed[N / 2];
 #pragma unroll
   for (int j = 0; j < N / 2; ++j) packed[j] = pack_bf16x2(acc[2 * j] * inv, acc[2 * j + 1] * inv);
@@ -149,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* qbar = bars + kWarps * C::kStages;
-  int* flags = reinterpret_cast<int*>(qbar + 1);
+  int* flags = reinterpret_cast<int*>(smem + C::kFlagsOff);
+  float* sink_s = reinterpret_cast<float*>(smem + C::kSinkOff);
   const uint8_t* q_s = smem + C::kQ;
 
   const int split = blockIdx.x, r = blockIdx.y;
@@ -168,6 +180,11 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
     mbar_arrive_expect_tx(qbar, q_bytes);
     bulk_g2s(smem + C::kQ, p.q + (long long)r * p.num_heads * kHeadDim, q_bytes, qbar);
   }
+  // the sinks and the scalar v scale are inputs of the call: read them now,
+  // so that no global load sits on the final merge's path
+  if (tid < kMaxHeads) sink_s[tid] = (p.sinks && tid < p.num_heads) ? __ldg(p.sinks + tid) * kLog2e : 0.f;
+  if (tid == kMaxHeads)
+    sink_s[kMaxHeads] = SCALE == MSA_SCALE_SCALAR ? __ldg(p.v_scale) : 1.f;
   // sparse tables and lengths come from the previous kernel on the stream
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -598,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
           }
         }
       }
-      finalize_out<4, SCALE>(p, r, h, d, a, M, L, (i4 & 31) == 0);
+      finalize_out<4, SCALE>(p, sink_s, r, h, d, a, M, L, (i4 & 31) == 0);
     }
     cluster_sync();  // no CTA leaves while another may still read its partial
     return;
@@ -667,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
   }
-  if (head < p.num_heads) finalize_out<16, SCALE>(p, r, head, d0, acc, mh, lh, (tid & 7) == 0);
+  if (head < p.num_heads) finalize_out<16, SCALE>(p, sink_s, r, head, d0, acc, mh, lh, (tid & 7) == 0);
 }
 
 template <bool FP8, int SCALE>
