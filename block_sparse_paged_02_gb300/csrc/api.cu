@@ -155,7 +155,8 @@ msa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_E
 
 // Sparse MLA work split: splits of each (row, 16-head group) so that the
 // grid fills MSA_MLA_CTAS CTAs per SM, each split at least 64 and at most
-// mla_max_tokens_per_split() token ids, a multiple of 16.
+// mla_max_tokens_per_split() token ids, a multiple of 16, and at most 8
+// splits (one cluster) when that bound allows.
 void mla_split(int num_rows, int num_heads, int max_tokens, int* splits, int* per) {
   const int groups = (num_heads + 15) / 16;
   const long long base = (long long)num_rows * groups;
@@ -164,6 +165,9 @@ void mla_split(int num_rows, int num_heads, int max_tokens, int* splits, int* pe
   const int lim = mla_max_tokens_per_split();
   s = max(s, (max_tokens + lim - 1) / lim);
   s = min(s, max(1, (max_tokens + 63) / 64));
+  // at most 8 splits (one thread-block cluster merges them) whenever a
+  // split can hold the rest
+  if (s > 8 && (max_tokens + 7) / 8 <= lim) s = 8;
   int t = (max_tokens + s - 1) / s;
   t = (t + 15) / 16 * 16;
   if (t > lim) t = lim;
@@ -182,7 +186,8 @@ MlaWs mla_layout(int num_rows, int num_heads, int max_tokens) {
   MlaWs w;
   w.counters = 0;
   w.partials = round_up(rg * 4, 256);
-  w.total = w.partials + (splits > 1 ? rg * (size_t)splits * 16 * 516 * 4 : 0);
+  // partials only for more splits than one cluster holds
+  w.total = w.partials + (splits > 8 ? rg * (size_t)splits * 16 * 516 * 4 : 0);
   return w;
 }
 

@@ -122,36 +122,6 @@ __device__ __forceinline__ void finalize_out(const AttnLaunch& p, const float* s
         (M == -INFINITY || Lsum <= 0.f) ? -INFINITY : (M + log2f(Lsum)) * kLn2;
 }
 
-// ---- thread-block cluster helpers (the splits of one row)
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-// the address of the same shared-memory location in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t out;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
-  return out;
-}
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
 template <bool FP8, int SCALE, bool CL>
 __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_CTAS_BF16)
     sparse_attn_kernel(const AttnLaunch p, const __grid_constant__ CUtensorMap kmap,

@@ -20,7 +20,9 @@
 // shared memory (one barrier per step, double buffered; the same barrier
 // publishes the next step's rows), every warp runs the same online softmax, and warp
 // w accumulates O for value dims [128w, 128w + 128) (64 fp32 registers per
-// lane).  Splits of a row merge through (m, l, acc) partials, finished by the
+// lane).  Up to 8 splits of a (row, head group) form one thread-block
+// cluster and merge their (m, l, acc) through distributed shared memory;
+// more splits merge through workspace partials, finished by the
 // last-arriving CTA (atomic counter; its top bit carries "an id was out of
 // range" from any split).
 #include "msa_internal.cuh"
@@ -46,6 +48,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;  // log2 units
 constexpr int kPartHeadFloats = 4 + kMlaDv;        // m, l, 2 pad, acc[512] (16-B aligned)
+// a (row, head group)'s splits merge inside one thread-block cluster when
+// there are at most this many (the portable cluster size)
+constexpr int kMaxClusterSplits = 8;
 
 struct MlaSmem {
   static constexpr int kRing = 0;
@@ -295,9 +300,79 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
       }
     }
   };
-  const bool single = p.splits == 1;
+  if (p.splits <= kMaxClusterSplits) {
+    // ---- the row's splits form one cluster (of 1..8 CTAs): each CTA leaves
+    // its (m, l, acc) in its own shared memory, one barrier publishes them,
+    // and every CTA merges a share of the 16 x 512 outputs over all partials
+    // through distributed shared memory; the second barrier keeps each CTA's
+    // memory alive until its readers are done.
+    cp_async_wait<0>();
+    __syncthreads();  // the ring is free now
+    float* mine = reinterpret_cast<float*>(smem);
+    put(mine, o, m_run, l_run);
+    if (tid == 0) flags[2] = cta_bad ? 1 : 0;
+    cluster_sync();
+    const uint32_t base = smem_u32(mine);
+    int fl = 0;
+    if (lane < p.splits) fl = ld_dsmem_s32(mapa_shared(smem_u32(&flags[2]), (uint32_t)lane));
+    const bool poisoned = __any_sync(full, fl != 0);
+    if (poisoned && split == 0 && tid == 0) atomicOr(p.status, MSA_DEV_BAD_TABLE);
+    for (int i4 = split * kThreads + tid; i4 < 16 * kMlaDv / 4; i4 += p.splits * kThreads) {
+      const int head = i4 / (kMlaDv / 4), d = 4 * (i4 % (kMlaDv / 4));
+      const int h_abs = 16 * hg + head;
+      if (h_abs >= p.num_heads) break;
+      float M = -INFINITY, Lsum = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!poisoned) {
+        float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
+        float4 v[kMaxClusterSplits];
+#pragma unroll
+        for (int j = 0; j < kMaxClusterSplits; ++j) {
+          if (j < p.splits) {
+            const uint32_t ph = mapa_shared(base, (uint32_t)j) + 4u * head * kPartHeadFloats;
+            ms[j] = ld_dsmem_f32(ph);
+            ls[j] = ld_dsmem_f32(ph + 4u);
+            v[j] = ld_dsmem_f4(ph + 4u * (4 + d));
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxClusterSplits; ++j) M = j < p.splits ? fmaxf(M, ms[j]) : M;
+#pragma unroll
+        for (int j = 0; j < kMaxClusterSplits; ++j) {
+          if (j < p.splits && ms[j] != -INFINITY) {
+            const float f = exp2f(ms[j] - M);
+            Lsum += f * ls[j];
+            a[0] += f * v[j].x;
+            a[1] += f * v[j].y;
+            a[2] += f * v[j].z;
+            a[3] += f * v[j].w;
+          }
+        }
+      }
+      if (p.sinks) {
+        const float sink2 = __ldg(p.sinks + h_abs) * kLog2e;
+        const float Mn = fmaxf(M, sink2);
+        const float f = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        Lsum = Lsum * f + exp2f(sink2 - Mn);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[j] *= f;
+        M = Mn;
+      }
+      const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+      *reinterpret_cast<uint2*>(p.out + ((long long)r * p.num_heads + h_abs) * kMlaDv + d) =
+          make_uint2(pack_bf16x2(a[0] * inv, a[1] * inv), pack_bf16x2(a[2] * inv, a[3] * inv));
+      if (d == 0)
+        p.lse[(long long)r * p.num_heads + h_abs] =
+            (M == -INFINITY || Lsum <= 0.f) ? -INFINITY : (M + log2f(Lsum)) * kLn2;
+    }
+    cluster_sync();
+    return;
+  }
+
+  // ---- more than 8 splits: publish this split's partial; the last CTA of
+  // the (row, head group) merges all.  A CTA that saw an id outside the
+  // pool flags the row in the counter's top bit before counting itself in.
   bool poisoned = cta_bad;
-  if (!single) {
+  {
     put(part, o, m_run, l_run);
     __threadfence();
     __syncthreads();
@@ -321,37 +396,24 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
   float M = -INFINITY, Lsum = 0.f, acc[64];
 #pragma unroll
   for (int j = 0; j < 64; ++j) acc[j] = 0.f;
-  if (!single) {
-    for (int sp = 0; sp < p.splits; ++sp) {
-      const float* ph = p.partials +
-          ((((long long)r * p.head_groups + hg) * p.splits + sp) * 16 + head) * kPartHeadFloats;
-      const float ms = __ldcg(ph), ls = __ldcg(ph + 1);
-      const float mn = fmaxf(M, ms);
-      const float fo = M == -INFINITY ? 0.f : exp2f(M - mn);
-      const float fs = ms == -INFINITY ? 0.f : exp2f(ms - mn);
-      Lsum = Lsum * fo + ls * fs;
-      const float4* a4 = reinterpret_cast<const float4*>(ph + 4 + d0);
+  for (int sp = 0; sp < p.splits; ++sp) {
+    const float* ph = p.partials +
+        ((((long long)r * p.head_groups + hg) * p.splits + sp) * 16 + head) * kPartHeadFloats;
+    const float ms = __ldcg(ph), ls = __ldcg(ph + 1);
+    const float mn = fmaxf(M, ms);
+    const float fo = M == -INFINITY ? 0.f : exp2f(M - mn);
+    const float fs = ms == -INFINITY ? 0.f : exp2f(ms - mn);
+    Lsum = Lsum * fo + ls * fs;
+    const float4* a4 = reinterpret_cast<const float4*>(ph + 4 + d0);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float4 v = __ldcg(a4 + j);
-        acc[4 * j] = acc[4 * j] * fo + v.x * fs;
-        acc[4 * j + 1] = acc[4 * j + 1] * fo + v.y * fs;
-        acc[4 * j + 2] = acc[4 * j + 2] * fo + v.z * fs;
-        acc[4 * j + 3] = acc[4 * j + 3] * fo + v.w * fs;
-      }
-      M = mn;
+    for (int j = 0; j < 16; ++j) {
+      const float4 v = __ldcg(a4 + j);
+      acc[4 * j] = acc[4 * j] * fo + v.x * fs;
+      acc[4 * j + 1] = acc[4 * j + 1] * fo + v.y * fs;
+      acc[4 * j + 2] = acc[4 * j + 2] * fo + v.z * fs;
+      acc[4 * j + 3] = acc[4 * j + 3] * fo + v.w * fs;
     }
-  } else {
-    // one split: stage this CTA's accumulators through shared memory
-    __syncthreads();
-    float* stage_f = reinterpret_cast<float*>(smem);  // the ring is free now
-    put(stage_f, o, m_run, l_run);
-    __syncthreads();
-    const float* ph = stage_f + head * kPartHeadFloats;
-    M = ph[0];
-    Lsum = ph[1];
-#pragma unroll
-    for (int j = 0; j < 64; ++j) acc[j] = ph[4 + d0 + j];
+    M = mn;
   }
   if (tid == 0 && poisoned) atomicOr(p.status, MSA_DEV_BAD_TABLE);
   if (poisoned) {  // a poisoned row is an empty row
@@ -394,8 +456,20 @@ cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        MlaSmem::kBytes);
   if (e != cudaSuccess) return e;
-  sparse_mla_kernel<<<dim3(p.splits, p.head_groups, p.num_rows), kThreads, MlaSmem::kBytes,
-                      stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits, p.head_groups, p.num_rows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = MlaSmem::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of a (row, head group)
+  attr[0].val.clusterDim.x = (unsigned)p.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.splits <= kMaxClusterSplits ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

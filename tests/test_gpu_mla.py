@@ -70,3 +70,19 @@ def test_sparse_mla_rows_longer_than_the_bound_are_refused(msa, orc):
     out, lse, _ = orc.sparse_mla(w.q, w.kv_cache, w.kv_indptr, w.kv_indices, w.dv,
                                  sinks=w.sinks, softmax_scale=w.softmax_scale)
     assert_attn_close(got["out"][1:], got["lse"][1:], out[1:], lse[1:])
+
+
+def test_sparse_mla_more_splits_than_a_cluster(msa, orc):
+    # 20000 ids in one row need more than 8 splits of <= 2048 ids: those
+    # splits merge through the workspace (last-arriving CTA), and an id past
+    # the cache in that row still empties it
+    w = W.sparse_mla_custom(77, [20000, 3, 700], heads=16, ctx=24000)
+    _, got, out, lse, st = run(msa, orc, w)
+    assert st == 0 and got["status"] == 0
+    assert_attn_close(got["out"], got["lse"], out, lse)
+    w.kv_indices = w.kv_indices.copy()
+    w.kv_indices[12345] = w.num_tokens
+    _, got, out, lse, st = run(msa, orc, w)
+    assert st == 8 and got["status"] & 8
+    assert np.all(got["out"][0] == 0)
+    assert_attn_close(got["out"], got["lse"], out, lse)

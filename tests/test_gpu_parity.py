@@ -129,6 +129,16 @@ def test_topk_extremes(msa, orc, topk):
     check_against_oracle(orc, w, sep, fused)
 
 
+def test_more_attention_splits_than_a_cluster(msa, orc):
+    # k = 160 blocks = 1280 page-16 entries per row: more than 8 splits of
+    # <= 128 entries, so the splits merge through the workspace instead of a
+    # thread-block cluster
+    w = W.custom(59, q_lens=[1, 2], seq_lens=[30000, 24000], hq=16, di=128, topk=160,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_SCALAR, with_sink=True)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
 def test_heavy_ties(msa, orc):
     # index values in {-1, 0, 1} with Di 64: many blocks tie at the same score
     w = W.custom(52, q_lens=[1, 4], seq_lens=[30000, 20000], hq=16, di=64, idx_range=1,
@@ -298,6 +308,30 @@ def test_repeated_calls_are_identical(msa):
     b = c.fetch()
     for key in ("out", "lse", "tbl"):
         assert np.array_equal(a[key], b[key])
+
+
+def test_every_call_rescores_every_block(msa, orc):
+    # New queries on later calls must change every block score of the fused
+    # path (stale workspace scores from the first call would show up as wrong
+    # selections), on 20 requests of different lengths.
+    import dataclasses
+    w = W.custom(63, q_lens=[1] * 20, seq_lens=[3000 + 700 * i for i in range(20)], hq=16,
+                 di=128, topk=8, kv_dtype=W.KV_FP8, scale_mode=W.SCALE_SCALAR, with_sink=True)
+    c = msa.DeviceCase(w)
+    c.decode()
+    ref = orc.decode(w, topk=w.topk)
+    assert np.array_equal(c.fetch()["topk_idx"], ref["topk_idx"])
+    rng = np.random.default_rng(64)
+    w2 = dataclasses.replace(w, idx_q=W._int_bf16(rng.integers(-3, 4, size=w.idx_q.shape,
+                                                               dtype=np.int8)))
+    c.idx_q.copy_(torch.from_numpy(w2.idx_q.view(np.int16)).to(c.idx_q.device).view(c.idx_q.dtype))
+    for _ in range(2):
+        c.decode()
+        got = c.fetch()
+        ref2 = orc.decode(w2, topk=w.topk)
+        assert np.array_equal(got["topk_idx"], ref2["topk_idx"])
+        assert np.array_equal(got["tbl"], ref2["tbl"])
+        assert_attn_close(got["out"], got["lse"], ref2["out"], ref2["lse"])
 
 
 def test_outputs_stay_inside_their_rows(msa):
