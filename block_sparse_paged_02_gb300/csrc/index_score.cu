@@ -27,6 +27,8 @@
 //     exact fp32 scores.
 #include <cfloat>
 
+#include <string.h>
+
 #include "msa_internal.cuh"
 
 namespace msa {
@@ -57,6 +59,15 @@ struct ScoreCfg {
   static constexpr int kSubPerLane = kBlock * HI / 32;
   static constexpr int kThreads = 32 * (1 + kStages);
 };
+
+// e4m3 keys with 128 dims and one head: a page is 128 rows of 128 B, which
+// arrives by one tensor copy with the 128-byte swizzle, so that the MMA
+// scorer's reads of rows 128 B apart fall in distinct banks
+#ifndef MSA_SCORE_FP8_SWIZZLE
+#define MSA_SCORE_FP8_SWIZZLE 1
+#endif
+template <int DI, int HI, int KIND>
+constexpr bool kSwizzledPages = MSA_SCORE_FP8_SWIZZLE && KIND == kMmaFp8 && DI == 128 && HI == 1;
 
 struct StageInfo {  // written by the producer before it arms the stage
   int req, blk, valid, q0, qlen, ctx, jstart, pad;
@@ -155,7 +166,7 @@ __device__ __forceinline__ uint2 lds64(const void* p) {
 // Then, per column, the masked maximum over the block's tokens of
 // scale_t * S (a column only sees sub-rows of its own head).  Returns in
 // best[0..8/HI) the block score of each query row (all lanes).
-template <int DI, int HI, bool F8>
+template <int DI, int HI, bool F8, bool SWZ>
 __device__ __forceinline__ void score_page_mma(const uint8_t* page, const float* tscale,
                                                const uint8_t* q_s, int nr, int lane, int blk,
                                                const int (&pos)[8], float (&best)[8]) {
@@ -211,10 +222,13 @@ __device__ __forceinline__ void score_page_mma(const uint8_t* page, const float*
     uint32_t w[2][kSpanW];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      const uint8_t* row = page + (16 * mt + g + 8 * half) * kRowB + c * kD4 * kElem;
+      const uint8_t* row = page + (16 * mt + g + 8 * half) * kRowB;
 #pragma unroll
       for (int i = 0; i < kSpanC; ++i) {
-        const uint4 v = lds128(row + 16 * i);
+        // 16-byte chunk j of sub-row t sits at chunk j ^ (t % 8) when the page
+        // came by a swizzled tensor copy (t % 8 == g here)
+        const int chunk = c * kSpanC + i;
+        const uint4 v = lds128(row + 16 * (SWZ ? (chunk ^ g) : chunk));
         w[half][4 * i] = v.x;
         w[half][4 * i + 1] = v.y;
         w[half][4 * i + 2] = v.z;
@@ -273,7 +287,7 @@ __device__ __forceinline__ void score_page_mma(const uint8_t* page, const float*
 
 template <int DI, int HI, int KIND>
 __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
-    index_score_kernel(const ScoreLaunch p) {
+    index_score_kernel(const ScoreLaunch p, const __grid_constant__ CUtensorMap kmap) {
   using C = ScoreCfg<DI, HI, KIND>;
   using S = ScoreSmem<DI, HI, KIND>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -393,8 +407,12 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
                    p.idx_scale + (long long)page * kBlock * HI, sb, &full[s]);
         bulk_g2s(smem + S::kQ + (size_t)s * C::kQBytes,
                  p.idx_q + (long long)(si.q0 + si.jstart) * HI * DI, qb, &full[s]);
-        bulk_g2s(smem + S::kPages + (size_t)s * C::kPageBytes,
-                 p.idx_k + (long long)page * C::kPageBytes, C::kPageBytes, &full[s]);
+        if constexpr (kSwizzledPages<DI, HI, KIND>)  // one 128 x 128 B box, 128-byte swizzle
+          tma_load_2d(smem + S::kPages + (size_t)s * C::kPageBytes, &kmap, 0, page * kBlock,
+                      &full[s]);
+        else
+          bulk_g2s(smem + S::kPages + (size_t)s * C::kPageBytes,
+                   p.idx_k + (long long)page * C::kPageBytes, C::kPageBytes, &full[s]);
       } else {
         atomicOr(p.status, MSA_DEV_BAD_PAGE);
         mbar_arrive(&full[s]);
@@ -484,7 +502,8 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
           const float* tscale = (KIND == kMmaFp8 && p.idx_scale)
               ? reinterpret_cast<const float*>(smem + S::kScale + (size_t)st * C::kScaleBytes)
               : nullptr;
-          score_page_mma<DI, HI, KIND == kMmaFp8>(page, tscale, q_s, nr, lane, si.blk, pos,
+          score_page_mma<DI, HI, KIND == kMmaFp8, kSwizzledPages<DI, HI, KIND>>(
+              page, tscale, q_s, nr, lane, si.blk, pos,
                                                   best);
         }
       } else {
@@ -508,10 +527,19 @@ cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
   using C = ScoreCfg<DI, HI, KIND>;
   const size_t smem = ScoreSmem<DI, HI, KIND>::bytes(p.batch.num_reqs);
   auto kern = index_score_kernel<DI, HI, KIND>;
+  CUtensorMap kmap;
+  memset(&kmap, 0, sizeof(kmap));
+  if constexpr (kSwizzledPages<DI, HI, KIND>) {
+    // the pool as [P * 128 rows][128 B]; row coordinates must fit an int
+    const long long rows = (long long)p.batch.num_pages * kBlock;
+    if (rows > 0x7fffffffll ||
+        !encode_map_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.idx_k, DI, rows, DI, DI, kBlock))
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<device_sm_count(), C::kThreads, smem, stream>>>(p);
+  kern<<<device_sm_count(), C::kThreads, smem, stream>>>(p, kmap);
   return cudaGetLastError();
 }
 
