@@ -215,10 +215,11 @@ __device__ __forceinline__ void score_page_mma(const uint8_t* page, const float*
   float m[2] = {-INFINITY, -INFINITY};
 #pragma unroll 2
   for (int mt = 0; mt < kMt; ++mt) {
-    // spans of sub-rows 16mt + g and 16mt + g + 8.  Lanes of one column
-    // group read the same bytes of rows a page row apart (bank conflicts);
-    // rotating the read order per lane would need run-time register
-    // indexing, which measured far more costly than the conflicts.
+    // spans of sub-rows 16mt + g and 16mt + g + 8.  Unswizzled, lanes of one
+    // column group read the same bytes of rows a page row apart (bank
+    // conflicts; rotating the read order per lane would need run-time
+    // register indexing, which measured far more costly); swizzled pages
+    // place those bytes in distinct banks.
     uint32_t w[2][kSpanW];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
