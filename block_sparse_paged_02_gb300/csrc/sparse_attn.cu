@@ -50,6 +50,14 @@ constexpr int kMaxClusterSplits = 8;
 constexpr int kCPart = kWarps * (kAccWarpFloats + 2 * kMaxHeads) * 4;
 constexpr int kCpM = kMaxHeads * kHeadDim, kCpL = kCpM + kMaxHeads, kCpFlag = kCpL + kMaxHeads;
 constexpr int kCPartBytes = (kCpFlag + 4) * 4;
+// push merge: the 16 heads' outputs form 4 chunks of 4 heads (128 float4);
+// chunk q belongs to CTA q % splits, which receives it from every split:
+// [slot = q / splits][source split][128 float4], then (m, l) per head, then
+// one poison flag per source.  At most 8 (slot, source) pairs for 1..8 splits.
+constexpr int kRecvPairs = 8;
+constexpr int kRecvF4Bytes = kRecvPairs * 128 * 16;
+constexpr int kRecvMlBytes = kRecvPairs * 8 * 4;
+constexpr int kRecvFlagBytes = kMaxClusterSplits * 4;
 
 template <bool FP8>
 struct AttnCfg {
@@ -71,7 +79,11 @@ struct AttnCfg {
   // after the barriers: 2 merge flags, then the sinks (log2 units) and the scalar v scale
   static constexpr int kFlagsOff = kBarOff + (kSlots + 1) * 8;
   static constexpr int kSinkOff = kFlagsOff + 16;
-  static constexpr int kSmemBytes = kSinkOff + (kMaxHeads + 1) * 4 + 64;
+  // FP8 cluster merge: the receive area other CTAs of the row push their
+  // partials into, never used by this CTA before the merge (outside the ring)
+  static constexpr int kRecvOff = (kSinkOff + (kMaxHeads + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kRecvBytes = FP8 ? kRecvF4Bytes + kRecvMlBytes + kRecvFlagBytes : 0;
+  static constexpr int kSmemBytes = kRecvOff + kRecvBytes + 64;
   static_assert(kCPart + kCPartBytes <= kDataBytes, "cluster partial must fit the ring");
 };
 
@@ -536,7 +548,60 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
     for (int j = 0; j < 16; ++j) acc[j] += f * ar[j];
   }
 
-  if constexpr (CL) {
+  if constexpr (CL && FP8) {
+    // ---- the row's splits form one cluster.  Each CTA pushes its partial
+    // of every 4-head chunk straight into the shared memory of the chunk's
+    // owner (asynchronous remote stores), one cluster barrier makes all of
+    // them visible, and each owner merges its chunks from its own memory:
+    // no remote load on the path and no second barrier.
+    const uint32_t recv = smem_u32(smem + C::kRecvOff);
+    const uint32_t recv_ml = recv + kRecvF4Bytes, recv_fl = recv_ml + kRecvMlBytes;
+    {
+      const int q = head >> 2, owner = q % p.splits, slot = q / p.splits;
+      const int pair = slot * p.splits + split;
+      const uint32_t dst = mapa_shared(recv, (uint32_t)owner) +
+                           16u * (pair * 128 + (head & 3) * 32 + (d0 >> 2));
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        st_dsmem_f4(dst + 16u * j, make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+      if ((tid & 7) == 0) {
+        const uint32_t ml = mapa_shared(recv_ml, (uint32_t)owner) + 4u * (pair * 8 + (head & 3) * 2);
+        st_dsmem_f32(ml, mh);
+        st_dsmem_f32(ml + 4u, lh);
+      }
+      if (tid < p.splits)  // this split's poison flag, to every CTA of the row
+        st_dsmem_s32(mapa_shared(recv_fl, (uint32_t)tid) + 4u * split, (len_bad || cta_bad) ? 1 : 0);
+    }
+    cluster_sync();  // every push of the row has landed
+    const int* fl = reinterpret_cast<const int*>(smem + C::kRecvOff + kRecvF4Bytes + kRecvMlBytes);
+    const bool poisoned = __any_sync(full, lane < p.splits && fl[lane] != 0);
+    if (poisoned && split == 0 && tid == 0) atomicOr(p.status, MSA_DEV_BAD_TABLE);
+    const float4* rf4 = reinterpret_cast<const float4*>(smem + C::kRecvOff);
+    const float* rml = reinterpret_cast<const float*>(smem + C::kRecvOff + kRecvF4Bytes);
+    for (int q = split; q < 4; q += p.splits) {
+      const int slot = q / p.splits;
+      const int h = 4 * q + (tid >> 5), d = 4 * (tid & 31);
+      if (h >= p.num_heads) continue;
+      float M = -INFINITY, L = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!poisoned) {
+        for (int j = 0; j < p.splits; ++j) M = fmaxf(M, rml[(slot * p.splits + j) * 8 + (h & 3) * 2]);
+        for (int j = 0; j < p.splits; ++j) {
+          const int pair = slot * p.splits + j;
+          const float ms = rml[pair * 8 + (h & 3) * 2];
+          if (ms == -INFINITY) continue;
+          const float f = exp2f(ms - M);
+          L += f * rml[pair * 8 + (h & 3) * 2 + 1];
+          const float4 v = rf4[pair * 128 + tid];
+          a[0] += f * v.x;
+          a[1] += f * v.y;
+          a[2] += f * v.z;
+          a[3] += f * v.w;
+        }
+      }
+      finalize_out<4, SCALE>(p, sink_s, r, h, d, a, M, L, (tid & 31) == 0);
+    }
+    return;
+  } else if constexpr (CL) {
     // ---- the row's splits form one cluster: each CTA leaves its partial in
     // its own shared memory, then every CTA merges a share of the (head,
     // 4-dim) outputs over all partials through distributed shared memory.
@@ -660,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
 template <bool FP8, int SCALE>
 cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t stream, bool programmatic) {
   using C = AttnCfg<FP8>;
-  const bool cl = p.splits <= kMaxClusterSplits;
+  // one split needs no merge at all (the single-split path finalises directly)
+  const bool cl = p.splits > 1 && p.splits <= kMaxClusterSplits;
   auto kern = cl ? sparse_attn_kernel<FP8, SCALE, true> : sparse_attn_kernel<FP8, SCALE, false>;
   CUtensorMap kmap, vmap;
   memset(&kmap, 0, sizeof(kmap));
