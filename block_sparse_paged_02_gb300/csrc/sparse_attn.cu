@@ -21,12 +21,14 @@
 // converts FP8 to f16 in registers (exact), applies per-token k scales to the
 // fp32 logits and folds per-token v scales into P.  The queries sit in
 // shared memory in the MMA's k-slot order and are read with ldmatrix.  Warps
-// merge in shared memory.  Up to 8 splits of a row form one thread-block
-// cluster and merge through distributed shared memory (two cluster barriers,
-// no global round trip); more splits merge through (m, l, acc) partials in
-// the workspace, finished by whichever CTA of the row arrives last (atomic
-// counter, reset by that CTA).  No spin-wait anywhere.  The sink joins the
-// denominator only in the final merge.
+// merge in shared memory.  2 to 8 splits of a row form one thread-block
+// cluster and merge through distributed shared memory, no global round
+// trip: with FP8 slabs each CTA pushes its partials into the owners of the
+// output chunks (one cluster barrier), with bf16 slabs each CTA pulls its
+// share of the outputs from all partials (two barriers); more splits merge
+// through (m, l, acc) partials in the workspace, finished by whichever CTA
+// of the row arrives last (atomic counter, reset by that CTA).  No spin-wait
+// anywhere.  The sink joins the denominator only in the final merge.
 #include <string.h>
 
 #include "msa_internal.cuh"
