@@ -14,10 +14,10 @@
 //     each CTA takes an equal contiguous slice (balanced by actual block
 //     count, the lesson of the PR 54682 balanced scorer; consecutive items
 //     share block-table lines, so the producer's lookups stay cache hits);
-//   * one producer thread issues one 1-D bulk async copy (TMA bulk engine)
-//     per 128-token index-K page (16 or 32 KB, contiguous in the page-128
-//     layout), plus one for the query rows that see it, into a ring of
-//     shared-memory stages guarded by mbarriers;
+//   * two producer threads (one per producer warp, alternate items) issue
+//     one async copy per 128-token index-K page (16 or 32 KB, contiguous in
+//     the page-128 layout), plus one for the query rows that see it, into a
+//     ring of shared-memory stages guarded by mbarriers;
 //   * each consumer warp owns one stage and scores the whole page
 //     (warp-per-block): every lane holds 4*Hi token sub-rows, walks their
 //     16-byte chunks in a lane-rotated order (bank-conflict free), and keeps
@@ -40,8 +40,17 @@ constexpr int kRowGroup = 4;
 // e4m3 keys on warp MMA (fp16 operands).
 enum { kFmaBf16 = 0, kMmaBf16 = 1, kMmaFp8 = 2 };
 
+// producer warps of the score kernel (each issues every kProducers-th item)
+#ifndef MSA_SCORE_PRODUCERS
+#define MSA_SCORE_PRODUCERS 2
+#endif
+#ifndef MSA_SCORE_PRODUCERS_FP8
+#define MSA_SCORE_PRODUCERS_FP8 2
+#endif
+
 template <int DI, int HI, int KIND>
 struct ScoreCfg {
+  static constexpr int kProducers = KIND == kMmaFp8 ? MSA_SCORE_PRODUCERS_FP8 : MSA_SCORE_PRODUCERS;
   static constexpr int kElem = KIND == kMmaFp8 ? 1 : 2;
   static constexpr int kSubRowBytes = DI * 2;
   static constexpr int kChunks = DI / 8;  // 16-byte chunks per bf16 sub-row
@@ -53,11 +62,13 @@ struct ScoreCfg {
   // stages within 200 KB (the rest holds barriers and the request prefix):
   // 6 for 32 KB pages, 10-12 for 16 KB ones
   static constexpr int kStageBytes = kPageBytes + kQBytes + kScaleBytes;
-  static constexpr int kStages = 204800 / kStageBytes < 12 ? 204800 / kStageBytes : 12;
+  static constexpr int kStages =
+      (204800 / kStageBytes < 12 ? 204800 / kStageBytes : 12) / kProducers * kProducers;
   // one consumer warp per stage (a pair of warps per page measured slower:
   // more instructions without more bytes in flight)
   static constexpr int kSubPerLane = kBlock * HI / 32;
-  static constexpr int kThreads = 32 * (1 + kStages);
+  static constexpr int kThreads = 32 * (kProducers + kStages);
+  static_assert(kStages % kProducers == 0, "every stage needs a single producer");
 };
 
 // e4m3 keys with 128 dims and one head: a page is 128 rows of 128 B, which
@@ -357,12 +368,16 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
   const int i1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
   const int n_items = i1 - i0;
 
-  if (warp == 0) {
-    // ---- producer warp.  An item lookup (request by binary search over the
-    // prefix, its row range, and the page id from the block table) costs a
-    // global-memory round trip; the first ring's worth of items is looked up
-    // by one lane each in parallel, then the elected lane keeps one lookup in
-    // flight ahead of the copy it is about to issue.
+  if (warp < C::kProducers) {
+    // ---- producer warps: warp pw issues the items j = pw (mod kProducers),
+    // so every stage has one producer (kStages is a multiple of kProducers).
+    // An item lookup (request by binary search over the prefix, its row
+    // range, and the page id from the block table) costs a global-memory
+    // round trip; a warp's share of the first ring is looked up by one lane
+    // each in parallel, then its elected lane keeps one lookup in flight
+    // ahead of the copy it is about to issue.  One producer paces the e4m3
+    // stream: its per-item lookup and three copy issues take longer than the
+    // consumers need for a 16 KB page.
     // consecutive items mostly share a request: its row range and context
     // are kept from the previous lookup of this lane
     int c_req = -1, c_q0 = 0, c_qlen = 0, c_ctx = 0;
@@ -419,31 +434,35 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
         mbar_arrive(&full[s]);
       }
     };
-    const int first = min(C::kStages, n_items);
+    const int pw = warp;
+    constexpr int kProducers = C::kProducers;
+    const int n_mine = n_items > pw ? (n_items - pw + kProducers - 1) / kProducers : 0;
+    const int first = min(C::kStages / kProducers, n_mine);  // this warp's share of the empty ring
     StageInfo mine{0, 0, 0, 0, 0, 0, 0, 0};
     int my_page = -1;
-    if (lane < first) lookup(lane, &mine, &my_page);
-    for (int j = 0; j < first; ++j) {  // the ring starts empty: no waits
+    if (lane < first) lookup(pw + kProducers * lane, &mine, &my_page);
+    for (int t = 0; t < first; ++t) {  // the ring starts empty: no waits
       StageInfo si;
-      si.req = __shfl_sync(0xffffffffu, mine.req, j);
-      si.blk = __shfl_sync(0xffffffffu, mine.blk, j);
-      si.valid = __shfl_sync(0xffffffffu, mine.valid, j);
-      si.q0 = __shfl_sync(0xffffffffu, mine.q0, j);
-      si.qlen = __shfl_sync(0xffffffffu, mine.qlen, j);
-      si.ctx = __shfl_sync(0xffffffffu, mine.ctx, j);
-      si.jstart = __shfl_sync(0xffffffffu, mine.jstart, j);
+      si.req = __shfl_sync(0xffffffffu, mine.req, t);
+      si.blk = __shfl_sync(0xffffffffu, mine.blk, t);
+      si.valid = __shfl_sync(0xffffffffu, mine.valid, t);
+      si.q0 = __shfl_sync(0xffffffffu, mine.q0, t);
+      si.qlen = __shfl_sync(0xffffffffu, mine.qlen, t);
+      si.ctx = __shfl_sync(0xffffffffu, mine.ctx, t);
+      si.jstart = __shfl_sync(0xffffffffu, mine.jstart, t);
       si.pad = 0;
-      const int pg = __shfl_sync(0xffffffffu, my_page, j);
-      if (lane == 0) issue(j, si, pg);
+      const int pg = __shfl_sync(0xffffffffu, my_page, t);
+      if (lane == 0) issue(pw + kProducers * t, si, pg);
     }
-    if (lane == 0 && first < n_items) {
+    if (lane == 0 && first < n_mine) {
       StageInfo next;
       int next_page;
-      lookup(first, &next, &next_page);
-      for (int j = first; j < n_items; ++j) {
+      lookup(pw + kProducers * first, &next, &next_page);
+      for (int t = first; t < n_mine; ++t) {
+        const int j = pw + kProducers * t;
         const StageInfo cur = next;
         const int cur_page = next_page;
-        if (j + 1 < n_items) lookup(j + 1, &next, &next_page);  // in flight during the wait
+        if (t + 1 < n_mine) lookup(j + kProducers, &next, &next_page);  // in flight during the wait
         const int s = j % C::kStages, use = j / C::kStages;
         if (!mbar_wait(&empty[s], (use - 1) & 1)) {
           atomicOr(p.status, MSA_DEV_TIMEOUT);
@@ -455,8 +474,8 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
     return;
   }
 
-  // ---- consumers: warp s+1 owns stage s
-  const int st = warp - 1;
+  // ---- consumers: warp kProducers + s owns stage s
+  const int st = warp - C::kProducers;
   const uint8_t* page = smem + S::kPages + (size_t)st * C::kPageBytes;
   uint8_t* q_s = smem + S::kQ + (size_t)st * C::kQBytes;
   for (int j = st, use = 0; j < n_items; j += C::kStages, ++use) {
