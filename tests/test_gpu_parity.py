@@ -139,6 +139,23 @@ def test_more_attention_splits_than_a_cluster(msa, orc):
     check_against_oracle(orc, w, sep, fused)
 
 
+@pytest.mark.parametrize("rows,kv", [(152, W.KV_FP8), (101, W.KV_FP8), (60, W.KV_FP8),
+                                     (50, W.KV_FP8), (43, W.KV_FP8), (101, W.KV_BF16),
+                                     (43, W.KV_BF16)])
+def test_cluster_merge_split_counts(msa, orc, rows, kv):
+    # k = 16 blocks = 128 entries per row; on 152 SMs x 2 CTAs these row
+    # counts give 2, 3, 5, 6 and 7 splits per row, so the cluster merge runs
+    # with every owner layout (two chunks per CTA at 2 and 3 splits, one at
+    # 5..7, CTAs that own nothing at 5..7); bf16 slabs take the pull merge
+    rng = np.random.default_rng(rows)
+    seq = [int(x) for x in rng.integers(2100, 2600, size=rows)]
+    w = W.custom(80 + rows, q_lens=[1] * rows, seq_lens=seq, hq=16, di=128, topk=16,
+                 kv_dtype=kv, scale_mode=W.SCALE_SCALAR if kv == W.KV_FP8 else W.SCALE_NONE,
+                 with_sink=True)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
 def test_heavy_ties(msa, orc):
     # index values in {-1, 0, 1} with Di 64: many blocks tie at the same score
     w = W.custom(52, q_lens=[1, 4], seq_lens=[30000, 20000], hq=16, di=64, idx_range=1,
