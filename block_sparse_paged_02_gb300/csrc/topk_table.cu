@@ -10,10 +10,12 @@
 //
 // One CTA per row; each thread holds KPT consecutive block scores as
 // orderable 32-bit keys in registers (rows of up to 1024 blocks: 1024
-// threads, one key each).  The k-th largest key T is found bit by bit from
-// the top: T takes a bit whenever at least k keys are >= the candidate.  With
-// one key per thread each count is a single counting barrier
-// (bar.red.popc); with several, a warp reduction plus one barrier.  One
+// threads, one key each).  The k-th largest key T is found from the top: with
+// one key per thread by a radix select over four 8-bit digits (a shared
+// 256-bin histogram per digit, one warp locating the bin that holds the k-th
+// largest); with several keys per thread bit by bit (T takes a bit whenever
+// at least k keys are >= the candidate: a warp reduction plus one barrier
+// per bit).  One
 // block-wide exclusive scan of the packed (== T, > T) counts then places, in
 // ascending block order, every key > T and the lowest-indexed keys == T until
 // k are taken -- the unique result under the lower-index tie rule.  The
@@ -24,6 +26,13 @@
 
 namespace msa {
 namespace {
+
+// one key per thread (rows of up to 1024 blocks): radix select (1) or the
+// counting-barrier bit search (0) for the threshold
+#ifndef MSA_TOPK_RADIX
+#define MSA_TOPK_RADIX 1
+#endif
+constexpr bool kRadixTopk = MSA_TOPK_RADIX != 0;
 
 // Exclusive scan of one int per thread over a CTA of THREADS threads (two
 // barriers); *total receives the sum.  scratch holds THREADS/32 + 1 ints.
@@ -66,6 +75,8 @@ __global__ void __launch_bounds__(THREADS) topk_table_kernel(const TopkLaunch p)
   __shared__ int s_cnt[2][kWarps];
   __shared__ int s_scan[kWarps + 1];
   __shared__ int s_bad;
+  __shared__ int s_hist[KPT == 1 ? 256 : 1];
+  __shared__ int s_sel[2];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const msa_batch& b = p.batch;
@@ -147,6 +158,60 @@ __global__ void __launch_bounds__(THREADS) topk_table_kernel(const TopkLaunch p)
   } else {
     // ---- the k-th largest key T (keys of blocks >= n are 0 < any candidate)
     uint32_t T = 0;
+    if constexpr (KPT == 1 && kRadixTopk) {
+      // Radix select, 8 bits per round from the top: a 256-bin histogram of
+      // the next digit over the keys that match the bits found so far
+      // (lanes with equal digits add once, through __match_any_sync), then
+      // one warp finds the bin holding the k-th largest from the top.  Four
+      // rounds of three barriers replace 32 counting barriers; the result is
+      // the same k-th largest key.
+      int kk = k;
+      uint32_t mask = 0;
+#pragma unroll 1
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        if (tid < 256) s_hist[tid] = 0;
+        __syncthreads();
+        const bool in = (key[0] & mask) == T;
+        const uint32_t dig = in ? (key[0] >> shift) & 255u : 256u;
+        const unsigned peers = __match_any_sync(full, dig);
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&s_hist[dig], __popc(peers));
+        __syncthreads();
+        if (warp == 0) {
+          // lane l holds bins 255-8l .. 248-8l (descending)
+          int h[8], sum = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            h[i] = s_hist[255 - 8 * lane - i];
+            sum += h[i];
+          }
+          int incl = sum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(full, incl, o);
+            if (lane >= o) incl += v;
+          }
+          const unsigned hit = __ballot_sync(full, incl >= kk);
+          if (lane == __ffs(hit) - 1) {
+            int cum = incl - sum;  // keys in higher bins
+            int b = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (cum + h[i] >= kk) {
+                b = 255 - 8 * lane - i;
+                break;
+              }
+              cum += h[i];
+            }
+            s_sel[0] = b;
+            s_sel[1] = kk - cum;
+          }
+        }
+        __syncthreads();
+        T |= (uint32_t)s_sel[0] << shift;
+        mask |= 255u << shift;
+        kk = s_sel[1];
+      }
+    } else {
 #pragma unroll 1
     for (int bit = 31; bit >= 0; --bit) {
       const uint32_t cand = T | (1u << bit);
@@ -165,6 +230,7 @@ __global__ void __launch_bounds__(THREADS) topk_table_kernel(const TopkLaunch p)
         for (int w = 0; w < kWarps; ++w) total += s_cnt[bit & 1][w];
       }
       if (total >= k) T = cand;
+    }
     }
     // ---- keys > T, then the lowest-indexed keys == T until k are taken:
     // one scan of (count == T) << 16 | (count > T) (both < 2^16)
