@@ -27,12 +27,14 @@
 namespace msa {
 namespace {
 
-// one key per thread (rows of up to 1024 blocks): radix select (1) or the
-// counting-barrier bit search (0) for the threshold
-#ifndef MSA_TOPK_RADIX
-#define MSA_TOPK_RADIX 1
+// One key per thread (rows of up to 1024 blocks): the radix select has the
+// shorter chain (a latency win when the rows fit one wave of CTAs), the
+// counting-barrier bit search fewer instructions (a throughput win for
+// thousands of rows, e.g. a chunked prefill: 106 against 139 us for 4096
+// rows).  Radix select up to this many rows per SM; 0 never.
+#ifndef MSA_TOPK_RADIX_ROWS_PER_SM
+#define MSA_TOPK_RADIX_ROWS_PER_SM 2
 #endif
-constexpr bool kRadixTopk = MSA_TOPK_RADIX != 0;
 
 // Exclusive scan of one int per thread over a CTA of THREADS threads (two
 // barriers); *total receives the sum.  scratch holds THREADS/32 + 1 ints.
@@ -66,8 +68,8 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
   return before + x - v;
 }
 
-template <int KPT, int THREADS>
-__global__ void __launch_bounds__(THREADS) topk_table_kernel(const TopkLaunch p) {
+template <int KPT, int THREADS, bool RADIX>
+__device__ __forceinline__ void topk_table_body(const TopkLaunch& p) {
   constexpr int kWarps = THREADS / 32;
   // [topk] selected blocks (ascending), then the request's block-table row
   extern __shared__ int sel[];
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(THREADS) topk_table_kernel(const TopkLaunch p)
   __shared__ int s_cnt[2][kWarps];
   __shared__ int s_scan[kWarps + 1];
   __shared__ int s_bad;
-  __shared__ int s_hist[KPT == 1 ? 256 : 1];
+  __shared__ int s_hist[KPT == 1 && RADIX ? 256 : 1];
   __shared__ int s_sel[2];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(THREADS) topk_table_kernel(const TopkLaunch p)
   } else {
     // ---- the k-th largest key T (keys of blocks >= n are 0 < any candidate)
     uint32_t T = 0;
-    if constexpr (KPT == 1 && kRadixTopk) {
+    if constexpr (KPT == 1 && RADIX) {
       // Radix select, 8 bits per round from the top: a 256-bin histogram of
       // the next digit over the keys that match the bits found so far
       // (lanes with equal digits add once, through __match_any_sync), then
@@ -284,9 +286,25 @@ __global__ void __launch_bounds__(THREADS) topk_table_kernel(const TopkLaunch p)
   }
 }
 
-template <int KPT, int THREADS>
+// One key per thread: at most 40 registers, so that a 1024-thread CTA still
+// fits beside an attention CTA (launched early by PDL) on one SM.
+template <bool RADIX>
+__global__ void __maxnreg__(40) topk_table_kernel(const TopkLaunch p) {
+  topk_table_body<1, 1024, RADIX>(p);
+}
+
+template <int KPT>
+__global__ void __launch_bounds__(256) topk_table_kernel_multi(const TopkLaunch p) {
+  topk_table_body<KPT, 256, false>(p);
+}
+
+template <int KPT, int THREADS, bool RADIX = false>
 cudaError_t launch_kpt(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
-  auto kern = topk_table_kernel<KPT, THREADS>;
+  void (*kern)(const TopkLaunch);
+  if constexpr (KPT == 1)
+    kern = topk_table_kernel<RADIX>;
+  else
+    kern = topk_table_kernel_multi<KPT>;
   const size_t smem = (size_t)(p.topk + p.batch.bt_stride) * sizeof(int);
   if (smem > 48 * 1024) {
     cudaError_t e =
@@ -311,7 +329,11 @@ cudaError_t launch_kpt(const TopkLaunch& p, cudaStream_t stream, bool programmat
 cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
   if (p.batch.num_rows == 0) return cudaSuccess;
   // a row has at most bt_stride candidate blocks
-  if (p.batch.bt_stride <= 1024) return launch_kpt<1, 1024>(p, stream, programmatic);
+  if (p.batch.bt_stride <= 1024) {
+    if ((long long)p.batch.num_rows <= (long long)MSA_TOPK_RADIX_ROWS_PER_SM * device_sm_count())
+      return launch_kpt<1, 1024, true>(p, stream, programmatic);
+    return launch_kpt<1, 1024, false>(p, stream, programmatic);
+  }
   if (p.batch.bt_stride <= 256 * 16) return launch_kpt<16, 256>(p, stream, programmatic);
   return launch_kpt<64, 256>(p, stream, programmatic);
 }
