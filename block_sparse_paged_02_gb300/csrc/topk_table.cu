@@ -286,11 +286,18 @@ __device__ __forceinline__ void topk_table_body(const TopkLaunch& p) {
   }
 }
 
-// One key per thread: at most 40 registers, so that a 1024-thread CTA still
-// fits beside an attention CTA (launched early by PDL) on one SM.
-template <bool RADIX>
-__global__ void __maxnreg__(40) topk_table_kernel(const TopkLaunch p) {
-  topk_table_body<1, 1024, RADIX>(p);
+// One key per thread, radix select (up to two rows per SM): at most 40
+// registers, so that a 1024-thread CTA still fits beside an attention CTA
+// (launched early by PDL) on one SM.
+__global__ void __maxnreg__(40) topk_table_kernel_radix(const TopkLaunch p) {
+  topk_table_body<1, 1024, true>(p);
+}
+
+// One key per thread, bit search (thousands of rows): it needs 32 registers,
+// so two 1024-thread CTAs share an SM (held to 40 it ran one per SM: 166
+// against 106 us for 4096 rows).
+__global__ void __launch_bounds__(1024) topk_table_kernel(const TopkLaunch p) {
+  topk_table_body<1, 1024, false>(p);
 }
 
 template <int KPT>
@@ -301,8 +308,10 @@ __global__ void __launch_bounds__(256) topk_table_kernel_multi(const TopkLaunch 
 template <int KPT, int THREADS, bool RADIX = false>
 cudaError_t launch_kpt(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
   void (*kern)(const TopkLaunch);
-  if constexpr (KPT == 1)
-    kern = topk_table_kernel<RADIX>;
+  if constexpr (KPT == 1 && RADIX)
+    kern = topk_table_kernel_radix;
+  else if constexpr (KPT == 1)
+    kern = topk_table_kernel;
   else
     kern = topk_table_kernel_multi<KPT>;
   const size_t smem = (size_t)(p.topk + p.batch.bt_stride) * sizeof(int);
