@@ -28,12 +28,16 @@ namespace msa {
 namespace {
 
 // One key per thread (rows of up to 1024 blocks): the radix select has the
-// shorter chain (a latency win when the rows fit one wave of CTAs), the
-// counting-barrier bit search fewer instructions (a throughput win for
-// thousands of rows, e.g. a chunked prefill: 106 against 139 us for 4096
-// rows).  Radix select up to this many rows per SM; 0 never.
-#ifndef MSA_TOPK_RADIX_ROWS_PER_SM
-#define MSA_TOPK_RADIX_ROWS_PER_SM 2
+// shorter chain, the counting-barrier bit search fewer instructions and 32
+// registers (two CTAs per SM, and room beside a score CTA while the PDL
+// prologue runs).  Measured steps (same box): 16 rows of up to 1024 blocks
+// 46.0-46.3 us radix against 49.2-50.4 us bit search; 64 rows of up to 1024
+// blocks 85.4-85.6 against 84.9-85.4 us; 8 rows of up to 256 blocks
+// 35.7-35.9 against 34.6-34.7 us; 4096 rows 139 against 106 us of top-k.
+// So the radix select runs for at most MSA_TOPK_RADIX_MAX_ROWS rows whose
+// table rows exceed 512 blocks.
+#ifndef MSA_TOPK_RADIX_MAX_ROWS
+#define MSA_TOPK_RADIX_MAX_ROWS 32
 #endif
 
 // Exclusive scan of one int per thread over a CTA of THREADS threads (two
@@ -286,7 +290,7 @@ __device__ __forceinline__ void topk_table_body(const TopkLaunch& p) {
   }
 }
 
-// One key per thread, radix select (up to two rows per SM): at most 40
+// One key per thread, radix select (few long rows): at most 40
 // registers, so that a 1024-thread CTA still fits beside an attention CTA
 // (launched early by PDL) on one SM.
 __global__ void __maxnreg__(40) topk_table_kernel_radix(const TopkLaunch p) {
@@ -339,7 +343,7 @@ cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream, bool pro
   if (p.batch.num_rows == 0) return cudaSuccess;
   // a row has at most bt_stride candidate blocks
   if (p.batch.bt_stride <= 1024) {
-    if ((long long)p.batch.num_rows <= (long long)MSA_TOPK_RADIX_ROWS_PER_SM * device_sm_count())
+    if (p.batch.num_rows <= MSA_TOPK_RADIX_MAX_ROWS && p.batch.bt_stride > 512)
       return launch_kpt<1, 1024, true>(p, stream, programmatic);
     return launch_kpt<1, 1024, false>(p, stream, programmatic);
   }

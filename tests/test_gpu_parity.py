@@ -156,6 +156,18 @@ def test_cluster_merge_split_counts(msa, orc, rows, kv):
     check_against_oracle(orc, w, sep, fused)
 
 
+@pytest.mark.parametrize("idx_range", [1, 3])
+def test_radix_select_few_long_rows(msa, orc, idx_range):
+    # few rows whose block tables exceed 512 entries take the radix-select
+    # top-k; idx_range 1 makes many blocks tie at the threshold
+    w = W.custom(90 + idx_range, q_lens=[1, 2, 1], seq_lens=[70000, 90000, 3000], hq=16,
+                 di=128, topk=16, idx_range=idx_range, kv_dtype=W.KV_FP8,
+                 scale_mode=W.SCALE_SCALAR, with_sink=True)
+    assert w.bt_stride > 512
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
 def test_heavy_ties(msa, orc):
     # index values in {-1, 0, 1} with Di 64: many blocks tie at the same score
     w = W.custom(52, q_lens=[1, 4], seq_lens=[30000, 20000], hq=16, di=64, idx_range=1,
