@@ -52,8 +52,6 @@ template <int DI, int HI, int KIND>
 struct ScoreCfg {
   static constexpr int kProducers = KIND == kMmaFp8 ? MSA_SCORE_PRODUCERS_FP8 : MSA_SCORE_PRODUCERS;
   static constexpr int kElem = KIND == kMmaFp8 ? 1 : 2;
-  static constexpr int kSubRowBytes = DI * 2;
-  static constexpr int kChunks = DI / 8;  // 16-byte chunks per bf16 sub-row
   static constexpr int kPageBytes = kBlock * HI * DI * kElem;
   // query rows scored per pass: 4 on FMAs, 8 (index heads) columns on MMA
   static constexpr int kRows = KIND == kFmaBf16 ? kRowGroup : 8 / HI;
@@ -66,7 +64,6 @@ struct ScoreCfg {
       (204800 / kStageBytes < 12 ? 204800 / kStageBytes : 12) / kProducers * kProducers;
   // one consumer warp per stage (a pair of warps per page measured slower:
   // more instructions without more bytes in flight)
-  static constexpr int kSubPerLane = kBlock * HI / 32;
   static constexpr int kThreads = 32 * (kProducers + kStages);
   static_assert(kStages % kProducers == 0, "every stage needs a single producer");
 };
@@ -103,16 +100,18 @@ template <int DI, int HI, int NR>
 __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q_s, int lane,
                                            int blk, const int (&pos)[kRowGroup],
                                            float (&out)[kRowGroup]) {
-  using C = ScoreCfg<DI, HI, kFmaBf16>;
-  float acc[C::kSubPerLane][NR];
+  constexpr int kSubPerLane = kBlock * HI / 32;  // token sub-rows of a lane
+  constexpr int kChunks = DI / 8;                 // 16-byte chunks per bf16 sub-row
+  constexpr int kSubRowBytes = DI * 2;
+  float acc[kSubPerLane][NR];
 #pragma unroll
-  for (int j = 0; j < C::kSubPerLane; ++j)
+  for (int j = 0; j < kSubPerLane; ++j)
 #pragma unroll
     for (int r = 0; r < NR; ++r) acc[j][r] = 0.f;
   const int head = lane % HI;  // sub-row lane+32j holds index head (lane % HI)
 #pragma unroll 2
-  for (int i = 0; i < C::kChunks; ++i) {
-    const int c = (i + lane) & (C::kChunks - 1);
+  for (int i = 0; i < kChunks; ++i) {
+    const int c = (i + lane) & (kChunks - 1);
     float qf[NR][8];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
@@ -127,9 +126,9 @@ __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q
       qf[r][7] = bf16hi(w.w);
     }
 #pragma unroll
-    for (int j = 0; j < C::kSubPerLane; ++j) {
+    for (int j = 0; j < kSubPerLane; ++j) {
       const int sr = lane + 32 * j;
-      const uint4 w = lds128(page + sr * C::kSubRowBytes + c * 16);
+      const uint4 w = lds128(page + sr * kSubRowBytes + c * 16);
       const float k0 = bf16lo(w.x), k1 = bf16hi(w.x), k2 = bf16lo(w.y), k3 = bf16hi(w.y);
       const float k4 = bf16lo(w.z), k5 = bf16hi(w.z), k6 = bf16lo(w.w), k7 = bf16hi(w.w);
 #pragma unroll
@@ -151,7 +150,7 @@ __device__ __forceinline__ void score_page(const uint8_t* page, const uint8_t* q
   for (int r = 0; r < NR; ++r) {
     float m = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < C::kSubPerLane; ++j) {
+    for (int j = 0; j < kSubPerLane; ++j) {
       const int token = (lane + 32 * j) / HI;
       if (blk * kBlock + token <= pos[r]) m = fmaxf(m, acc[j][r]);  // NaN never wins
     }
