@@ -6,10 +6,18 @@ and the HBM roofline fraction of its dominant kernel (the index-K scan).
 
 A step = one msa_decode call (index score -> top-k + page-16 table ->
 sparse paged attention) over the whole synthetic batch, inputs resident in
-HBM.  L2 is flushed (a 512 MiB write, then a 256 MiB read) between timed steps, outside the timed
-events.  Under torchrun each rank runs its own independent batch (requests
-are independent; no collective on the data path) and rank 0 prints one JSON
-line with the max-over-ranks time.
+HBM.  L2 is flushed (a 512 MiB write, then a 256 MiB read) between timed
+steps, outside the timed events.  Under torchrun each rank runs its own
+independent batch (requests are independent; no collective on the data
+path) and rank 0 prints one JSON line with the max-over-ranks time.
+
+The line's headline keys are the 64-request decode (the workload the 70 %
+roofline target names).  At N = 1 the same line also carries `per_workload`:
+every other synthetic workload (tiny, batched, speculative, chunked
+prefill, plus the FP8 index-K and sparse-MLA variants) timed the same way,
+each with the median and mean of >= 100 graph replays, per-kernel times
+and roofline fractions, an end-to-end figure and the oracle on the host
+cores.
 """
 from __future__ import annotations
 
@@ -31,18 +39,34 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "query rows/s for fused index-topk+sparse paged decode; % of HBM roofline"
+MLA_METRIC = "query rows/s for sparse MLA decode with sinks; % of HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# the GB300's nominal HBM3e bandwidth (the "~8 TB/s" roofline); fractions are
+# reported against it next to the measured copy rate
+NOMINAL_HBM_GBS = 7900.0
 L2_FLUSH_BYTES = 512 << 20
+MEDIAN_ITERS = 100  # graph replays behind every median
+EXTRA_E2E_ITERS = 20
+EXTRA_KERNEL_ITERS = 20
+EXTRA_CPU_BUDGET_S = 3.0
+W_SEED = {"tiny_decode": 1, "batched_decode": 2, "speculative_decode": 3,
+          "large_batch_decode": 4, "chunked_prefill": 5, "large_batch_decode_fp8_index": 6,
+          "sparse_mla_decode": 7}
+EXTRA_WORKLOADS = ("tiny_decode", "batched_decode", "speculative_decode", "chunked_prefill",
+                   "large_batch_decode_fp8_index", "sparse_mla_decode")
 
 
 # ---------------------------------------------------------------- bytes model
 
 def algorithmic_bytes(w, topk_idx: np.ndarray) -> dict:
-    """Bytes the method must move for one call, per kernel and in total:
-    index-K read once per request, queries, block tables, the selected K/V
-    (+ per-token scales) counted once per request over the union of its
-    rows' selected blocks (a block selected by several rows of a request is
-    read from HBM once), the tables, O and LSE.  Scores are intermediates."""
+    """Bytes (and FLOPs) the method must move for one call, per kernel and in
+    total: index-K read once per request, queries, block tables, the
+    selected K/V (+ per-token scales) counted once per request over the
+    union of its rows' selected blocks (a block selected by several rows of a
+    request is read from HBM once), the tables, O and LSE.  Scores are
+    intermediates.  FLOPs: the causal index dot products, and QK^T plus PV
+    over each row's selected tokens."""
     seq = w.seq_lens
     nb_req = (seq + 127) // 128
     N = w.num_rows
@@ -56,14 +80,21 @@ def algorithmic_bytes(w, topk_idx: np.ndarray) -> dict:
     q = N * w.hq * w.head_dim * 2
     kv_elem = 1 if w.kv_dtype == W.KV_FP8 else 2
     toks = 0
+    row_tokens = 0  # sum over rows of the tokens each row attends to
+    score_flops = 0
+    score_reads = 0  # the top-k's reads of each row's candidate scores
     for rq in range(len(seq)):
         r0, r1 = int(w.cu_seqlens_q[rq]), int(w.cu_seqlens_q[rq + 1])
         seen = {}
         for r in range(r0, r1):
             L = int(w.context_lens[rq]) + (r - r0) + 1  # tokens row r sees
+            score_flops += 2 * L * w.index_heads * w.index_dim
+            score_reads += 4 * ((L + 127) // 128)
             for b in topk_idx[r]:
                 if b >= 0:
-                    seen[int(b)] = max(seen.get(int(b), 0), min(128, L - 128 * int(b)))
+                    n = min(128, L - 128 * int(b))
+                    row_tokens += n
+                    seen[int(b)] = max(seen.get(int(b), 0), n)
         toks += sum(seen.values())
     kv = toks * w.hkv * w.head_dim * kv_elem * 2
     if w.scale_mode == W.SCALE_PER_TOKEN_HEAD:
@@ -73,19 +104,24 @@ def algorithmic_bytes(w, topk_idx: np.ndarray) -> dict:
     out = N * (w.hq * w.head_dim * 2 + w.hq * 4)
     score = idx_k + idx_q + bt  # what the index-score kernel must read
     total = score + q + kv + tables + out
-    return dict(score_kernel=score, attention=q + kv + out, total=total, index_k=idx_k, kv=kv)
+    return dict(score_kernel=score, attention=q + kv + out, topk=score_reads + bt + tables,
+                total=total, index_k=idx_k, kv=kv, score_flops=score_flops,
+                attn_flops=4 * row_tokens * w.hq * w.head_dim)
 
 
 # ---------------------------------------------------------------- environment
 
-def read_peaks():
+def read_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS,
+                    bf16_sustained=FALLBACK_BF16_TFLOPS, source="fallback")
 
 
 def kernel_source_hash() -> str:
@@ -175,24 +211,6 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# --------------------------------------------------------------------- arms
-
-def cpu_oracle_run(w, budget_s: float = 12.0, max_reps: int = 1 << 20):
-    import oracle
-    oracle.build()
-    threads = oracle.default_threads()
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.decode(w, nthreads=threads)
-        reps += 1
-        el = time.perf_counter() - t0
-        if reps >= max_reps or el >= budget_s:
-            break
-    return dict(value=w.num_rows * reps / el, unit="rows/s", cores=threads,
-                kind="oracle", sample=f"{reps} x full {w.name} batch ({w.num_rows} rows), "
-                f"fp64 C oracle, {threads} threads, {el:.2f} s")
-
-
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -200,49 +218,64 @@ def dist_env():
     return ws, rank, local
 
 
-def run_reference(args):
-    ws, rank, _ = dist_env()
-    if rank != 0:
-        return 0
-    if args.workload == "sparse_mla_decode":
-        w = W.sparse_mla_decode(seed=rank_seed(args.workload, 0))
-        run_once = lambda: mla_cpu_run(w, budget_s=0.0, rows=w.num_rows)
-        metric, config = MLA_METRIC, mla_config(w)
-    else:
-        w = W.NAMED[args.workload](seed=rank_seed(args.workload, 0))
-        run_once = lambda: cpu_oracle_run(w, budget_s=0.0, max_reps=1)
-        metric, config = METRIC, workload_config(w)
-    times = []
-    for _ in range(args.warmup):
-        run_once()
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        run_once()
-        times.append(time.perf_counter() - t0)
+def rank_seed(workload: str, rank: int) -> int:
+    """Seed of a rank's batch: rank 0 draws the named workload itself, every
+    other rank an independent batch of the same shape."""
+    return W_SEED[workload] + 1000 * rank
+
+
+def workload_config(w):
+    seq = w.seq_lens
+    return {"workload": w.name, "requests": w.num_reqs, "rows": w.num_rows,
+            "query_heads": w.hq, "kv_heads": w.hkv, "head_dim": w.head_dim,
+            "index_dim": w.index_dim, "topk": w.topk,
+            "index_k": ("fp8_e4m3" + (" + per-token scales" if w.idx_k_scale is not None else "")
+                        if getattr(w, "index_dtype", 0) == W.KV_FP8 else "bf16"),
+            "kv": "fp8_e4m3" if w.kv_dtype == W.KV_FP8 else "bf16",
+            "scales": ["none", "scalar", "per_token_head"][w.scale_mode],
+            "sinks": w.sinks is not None, "context_tokens": int(seq.sum()),
+            "median_context": float(np.median(seq)),
+            "l2": "flushed between steps (512 MiB write, then 256 MiB read)"}
+
+
+def mla_config(w):
+    counts = np.diff(w.kv_indptr)
+    return {"workload": w.name, "rows": w.num_rows, "heads": w.heads, "dqk": w.dqk, "dv": w.dv,
+            "cache_tokens": w.num_tokens, "tokens_per_row": int(np.median(counts)),
+            "kv": "bf16", "sinks": w.sinks is not None,
+            "l2": "flushed between steps (512 MiB write, then 256 MiB read)"}
+
+
+# ------------------------------------------------------------- oracle (CPU)
+
+def cpu_oracle_run(w, budget_s: float = 12.0, max_reps: int = 1 << 20, rows=None):
+    """The fp64 C oracle on the host cores over the workload (or a sample of
+    its rows, each as a one-row request at its own position), timed."""
     import oracle
-    total = sum(times)
-    value = w.num_rows * args.steps / total
-    line = {"impl": "reference", "metric": metric, "value": value, "unit": "rows/s",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config,
-            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.default_threads(),
-                             "kind": "oracle",
-                             "sample": f"full {w.name} batch per step ({w.num_rows} rows)"},
-            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0}}
-    print(json.dumps(line))
-    return 0
+    oracle.build()
+    threads = oracle.default_threads()
+    sub = w if rows is None else W.row_subset(w, rows)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(sub, nthreads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if reps >= max_reps or el >= budget_s:
+            break
+    what = (f"full {w.name} batch ({w.num_rows} rows)" if rows is None else
+            f"{sub.num_rows} of the {w.num_rows} rows of {w.name} (every "
+            f"{max(1, w.num_rows // sub.num_rows)}th)")
+    return dict(value=sub.num_rows * reps / el, unit="rows/s", cores=threads, kind="oracle",
+                sample=f"{reps} x {what}, fp64 C oracle, {threads} threads, {el:.2f} s")
 
 
-W_SEED = {"tiny_decode": 1, "batched_decode": 2, "speculative_decode": 3,
-          "large_batch_decode": 4, "chunked_prefill": 5, "large_batch_decode_fp8_index": 6,
-          "sparse_mla_decode": 7}
-MLA_METRIC = "query rows/s for sparse MLA decode with sinks; % of HBM roofline"
+def cpu_rows_sample(w):
+    """Rows the oracle times for a workload: all of them, except for batches
+    of thousands of rows, where an evenly spaced sample keeps it to seconds."""
+    if w.num_rows <= 64:
+        return None
+    return np.arange(0, w.num_rows, w.num_rows // 64)
 
-
-# ------------------------------------------------------------ sparse MLA arm
 
 def mla_bytes(w) -> dict:
     """Bytes and FLOPs of one sparse-MLA call: each row's distinct latent rows
@@ -277,150 +310,300 @@ def mla_cpu_run(w, budget_s: float = 12.0, rows: int = 16):
                 f"{threads} threads, {el:.2f} s")
 
 
-def mla_config(w):
-    counts = np.diff(w.kv_indptr)
-    return {"workload": w.name, "rows": w.num_rows, "heads": w.heads, "dqk": w.dqk, "dv": w.dv,
-            "cache_tokens": w.num_tokens, "tokens_per_row": int(np.median(counts)),
-            "kv": "bf16", "sinks": w.sinks is not None,
-            "l2": "flushed between steps (512 MiB write, then 256 MiB read)"}
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    if args.workload == "sparse_mla_decode":
+        w = W.sparse_mla_decode(seed=rank_seed(args.workload, 0))
+        run_once = lambda: mla_cpu_run(w, budget_s=0.0, rows=w.num_rows)
+        metric, config, rows = MLA_METRIC, mla_config(w), w.num_rows
+        sample = f"full {w.name} batch per step ({w.num_rows} rows)"
+    else:
+        w = W.NAMED[args.workload](seed=rank_seed(args.workload, 0))
+        pick = cpu_rows_sample(w)
+        run_once = lambda: cpu_oracle_run(w, budget_s=0.0, max_reps=1, rows=pick)
+        metric, config = METRIC, workload_config(w)
+        rows = w.num_rows if pick is None else len(pick)
+        sample = (f"full {w.name} batch per step ({w.num_rows} rows)" if pick is None else
+                  f"{rows} evenly spaced rows of {w.name} per step")
+    times = []
+    for _ in range(args.warmup):
+        run_once()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run_once()
+        times.append(time.perf_counter() - t0)
+    import oracle
+    total = sum(times)
+    value = rows * args.steps / total
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config,
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.default_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
 
+
+# ------------------------------------------------------------- GPU helpers
+
+class Gpu:
+    """The device, stream, L2 flush and event helpers of one rank."""
+
+    def __init__(self, local: int, flush: bool = True):
+        import torch
+        self.torch = torch
+        torch.cuda.set_device(local)
+        self.dev = f"cuda:{local}"
+        self.local = local
+        self.stream = torch.cuda.current_stream()
+        self.flush = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=self.dev)
+                      if flush else None)
+        self.rbuf = (torch.ones(L2_FLUSH_BYTES // 2, dtype=torch.uint8, device=self.dev)
+                     if flush else None)
+
+    def ev(self):
+        return self.torch.cuda.Event(enable_timing=True)
+
+    def flush_l2(self, i):
+        # write a buffer larger than L2, then read another one so that no dirty
+        # lines are left for the timed kernels to write back
+        self.flush.fill_(i & 0xff)
+        self.rbuf.sum(dtype=self.torch.int32)
+
+    def capture(self, fn):
+        """fn(stream) captured once into a CUDA graph (the library is
+        graph-capturable: no host sync, no allocation, no host copy)."""
+        torch = self.torch
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn(s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        return g
+
+    def time_steps(self, step, n):
+        """Per-step device times (ms) of n calls of step(), L2 flushed before
+        each, events on the launching stream."""
+        marks = [(self.ev(), self.ev()) for _ in range(n)]
+        for i in range(n):
+            self.flush_l2(i)
+            marks[i][0].record(self.stream)
+            step()
+            marks[i][1].record(self.stream)
+        self.torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in marks]
+
+    def e2e(self, case, host_names, step, steps, warmup):
+        """End to end through the public call: the per-step inputs copied in
+        from pinned host memory and O/LSE copied back, inside the events."""
+        torch = self.torch
+        host = {name: getattr(case, name).cpu().pin_memory() for name in host_names}
+        out_h = torch.empty_like(case.out, device="cpu").pin_memory()
+        lse_h = torch.empty_like(case.lse, device="cpu").pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        marks = [(self.ev(), self.ev()) for _ in range(steps)]
+        for i in range(warmup + steps):
+            self.flush_l2(i)
+            if i >= warmup:
+                marks[i - warmup][0].record(self.stream)
+            for name, t in host.items():
+                getattr(case, name).copy_(t, non_blocking=True)
+            step()
+            out_h.copy_(case.out, non_blocking=True)
+            lse_h.copy_(case.lse, non_blocking=True)
+            if i >= warmup:
+                marks[i - warmup][1].record(self.stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in marks), h2d, d2h
+
+
+DECODE_INPUTS = ("q", "idx_q", "cu_q", "cu_k", "ctx", "bt")
+
+
+def decode_kernel_times(gpu, case, msa, iters):
+    """The same step eagerly with events after each stage (events recorded
+    inside a graph cannot be timed)."""
+    e = [gpu.ev() for _ in range(4)]
+    trace = msa.make_trace(e[1], e[2], e[3])
+    score, topk, attn = [], [], []
+    for i in range(iters):
+        gpu.flush_l2(i)
+        # keep the GPU busy (a spin kernel, no memory traffic) while the host
+        # enqueues the call, so that host-side launch time never shows up as
+        # a gap inside the first kernel's interval
+        gpu.torch.cuda._sleep(GATE_CYCLES)
+        e[0].record(gpu.stream)
+        case.decode(keep_tables=False, trace=trace)
+        gpu.torch.cuda.synchronize()
+        score.append(e[0].elapsed_time(e[1]))
+        topk.append(e[1].elapsed_time(e[2]))
+        attn.append(e[2].elapsed_time(e[3]))
+    return {"index_score": score, "topk_table": topk, "sparse_attn": attn}
+
+
+def launches_per_step(w) -> int:
+    q_lens = np.diff(w.cu_seqlens_q)
+    return 3 + int(q_lens.max() >= 64 and w.index_heads == 1
+                   and getattr(w, "index_dtype", 0) != W.KV_FP8)
+
+
+def kernel_rooflines(nbytes, kernel_ms, peaks):
+    """Per kernel: mean time, algorithmic bytes and FLOPs, and the fraction
+    of the measured HBM copy rate and of the bf16 tensor peak (burst) they
+    reach; the kernel's bound is the larger fraction."""
+    work = {"index_score": (nbytes["score_kernel"], nbytes["score_flops"]),
+            "topk_table": (nbytes["topk"], 0),
+            "sparse_attn": (nbytes["attention"], nbytes["attn_flops"])}
+    out = {}
+    for name, (b, f) in work.items():
+        ms = statistics.mean(kernel_ms[name])
+        gbs = b / (ms / 1e3) / 1e9
+        tfs = f / (ms / 1e3) / 1e12
+        hf, tf = gbs / peaks["hbm"], tfs / peaks["bf16"]
+        out[name] = {"ms": ms, "algorithmic_bytes": b, "flops": f, "achieved_gbs": gbs,
+                     "achieved_tflops": tfs, "hbm_frac": hf, "tensor_frac": tf,
+                     "bound": "tensor" if tf > hf else "hbm"}
+    return out
+
+
+def step_roofline(total_bytes, step_ms, peaks):
+    gbs = total_bytes / (step_ms / 1e3) / 1e9
+    return {"algorithmic_bytes": total_bytes, "achieved_gbs": gbs, "frac": gbs / peaks["hbm"],
+            "frac_nominal": gbs / NOMINAL_HBM_GBS, "nominal_gbs": NOMINAL_HBM_GBS}
+
+
+def measure_extra_decode(gpu, msa, name):
+    """One more decode workload: >= 100 graph replays (median and mean),
+    per-kernel times, end to end, oracle on the host cores."""
+    w = W.NAMED[name](seed=rank_seed(name, 0))
+    case = msa.DeviceCase(w, device=gpu.dev)
+    for i in range(3):
+        gpu.flush_l2(i)
+        case.decode(keep_tables=False)
+    gpu.torch.cuda.synchronize()
+    if int(case.status.item()) != 0:
+        raise RuntimeError(f"{name}: device status {int(case.status.item())}")
+    g = gpu.capture(lambda s: case.decode(keep_tables=False, stream=s))
+    steps = gpu.time_steps(g.replay, MEDIAN_ITERS)
+    kern = decode_kernel_times(gpu, case, msa, EXTRA_KERNEL_ITERS)
+    case.decode()
+    gpu.torch.cuda.synchronize()
+    topk_sel = case.topk_idx[: w.num_rows].cpu().numpy()
+    e2e_ms, h2d, d2h = gpu.e2e(case, DECODE_INPUTS, lambda: case.decode(keep_tables=False),
+                               EXTRA_E2E_ITERS, 3)
+    peaks = read_peaks()
+    nb = algorithmic_bytes(w, topk_sel)
+    mean, med = statistics.mean(steps), statistics.median(steps)
+    kr = kernel_rooflines(nb, kern, peaks)
+    dom = max(kr, key=lambda k: kr[k]["ms"])
+    return {
+        "config": workload_config(w),
+        "ms_per_step": mean, "ms_per_step_median": med, "iters": len(steps),
+        "value": w.num_rows / (mean / 1e3), "value_median": w.num_rows / (med / 1e3),
+        "unit": "rows/s",
+        "step_roofline": step_roofline(nb["total"], med, peaks),
+        "kernels": kr, "dominant_kernel": dom,
+        "dominant_kernel_frac": max(kr[dom]["hbm_frac"], kr[dom]["tensor_frac"]),
+        "dominant_bound": kr[dom]["bound"],
+        "e2e": {"value": w.num_rows * EXTRA_E2E_ITERS / (e2e_ms / 1e3), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches_per_step": launches_per_step(w),
+        "cpu_baseline": cpu_oracle_run(w, budget_s=EXTRA_CPU_BUDGET_S, rows=cpu_rows_sample(w)),
+        "peak_source": peaks["source"],
+    }
+
+
+def measure_mla(gpu, msa, seed, steps_n, warmup, cpu_budget):
+    """Sparse MLA decode: graph replays, end to end, oracle on the host."""
+    w = W.sparse_mla_decode(seed=seed)
+    case = msa.MlaCase(w, device=gpu.dev)
+    for i in range(warmup):
+        gpu.flush_l2(i)
+        case.decode()
+    gpu.torch.cuda.synchronize()
+    if int(case.status.item()) != 0:
+        raise RuntimeError(f"device status {int(case.status.item())} on a clean workload")
+    g = gpu.capture(lambda s: case.decode(stream=s))
+    steps = gpu.time_steps(g.replay, steps_n)
+    e2e_ms, h2d, d2h = gpu.e2e(case, ("q", "indptr", "indices"), case.decode, steps_n, warmup)
+    peaks = read_peaks()
+    nb = mla_bytes(w)
+    mean, med = statistics.mean(steps), statistics.median(steps)
+    achieved = nb["total"] / (med / 1e3) / 1e9
+    tflops = nb["flops"] / (med / 1e3) / 1e12
+    return w, steps, {
+        "config": mla_config(w),
+        "ms_per_step": mean, "ms_per_step_median": med, "iters": len(steps),
+        "value": w.num_rows / (mean / 1e3), "value_median": w.num_rows / (med / 1e3),
+        "unit": "rows/s",
+        "roofline": {"bound": "hbm", "kernel": "sparse_mla", "achieved": achieved,
+                     "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"],
+                     "frac_nominal": achieved / NOMINAL_HBM_GBS, "peak_source": peaks["source"],
+                     "traffic": None, "algorithmic_bytes_per_launch": nb["total"],
+                     "avg_launch_ms": med},
+        "tensor": {"achieved_tflops": tflops, "peak_bf16_tflops": peaks["bf16"],
+                   "frac": tflops / peaks["bf16"], "note": "mma.sync m16n8k16 bf16"},
+        "dominant_kernel": "sparse_mla", "dominant_kernel_frac": achieved / peaks["hbm"],
+        "e2e": {"value": w.num_rows * steps_n / (e2e_ms / 1e3), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches_per_step": 1,
+        "cpu_baseline": mla_cpu_run(w, budget_s=cpu_budget),
+    }
+
+
+# ------------------------------------------------------------------- arms
 
 def run_mla_gpu(args):
-    import torch
     import torch.distributed as dist
 
     import block_sparse_paged_02_gb300 as msa
 
     ws, rank, local = dist_env()
     if ws > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = f"cuda:{local}"
-    w = W.sparse_mla_decode(seed=rank_seed(args.workload, rank))
-    case = msa.MlaCase(w, device=dev)
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    rbuf = torch.ones(L2_FLUSH_BYTES // 2, dtype=torch.uint8, device=dev)
-
-    def flush_l2(i):
-        flush.fill_(i & 0xff)
-        rbuf.sum(dtype=torch.int32)
-
-    ev = lambda: torch.cuda.Event(enable_timing=True)
+        dist.init_process_group("nccl")
+    gpu = Gpu(local, flush=not args.profile)
     if args.profile:
+        # plain run for profilers: warm-up + K steps, nothing else
+        w = W.sparse_mla_decode(seed=rank_seed(args.workload, rank))
+        case = msa.MlaCase(w, device=gpu.dev)
         for _ in range(args.warmup + args.steps):
             case.decode()
-        torch.cuda.synchronize()
+        gpu.torch.cuda.synchronize()
         print(json.dumps({"profile_run": w.name, "status": int(case.status.item())}))
         return 0
-    for i in range(args.warmup):
-        flush_l2(i)
-        case.decode()
-    torch.cuda.synchronize()
-    if int(case.status.item()) != 0:
-        raise RuntimeError(f"device status {int(case.status.item())} on a clean workload")
-    s = torch.cuda.Stream(device=dev)
-    s.wait_stream(torch.cuda.current_stream())
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        case.decode(stream=s)
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    marks = [(ev(), ev()) for _ in range(args.steps)]
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        for i in range(args.steps):
-            flush_l2(i)
-            marks[i][0].record(stream)
-            g.replay()
-            marks[i][1].record(stream)
-        torch.cuda.synchronize()
-    total_ms = sum(a.elapsed_time(b) for a, b in marks)
+        if ws > 1:
+            dist.barrier()
+        w, steps, rep = measure_mla(gpu, msa, rank_seed(args.workload, rank), args.steps,
+                                    args.warmup, 12.0 if rank == 0 else 0.0)
+    total_ms = sum(steps)
     if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
+        t = gpu.torch.tensor([total_ms], device=gpu.dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
-    # end to end: queries and token lists from pinned host memory, O/LSE back
-    host = {name: getattr(case, name).cpu().pin_memory() for name in ("q", "indptr", "indices")}
-    out_h = torch.empty_like(case.out, device="cpu").pin_memory()
-    lse_h = torch.empty_like(case.lse, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
-    e2e_marks = [(ev(), ev()) for _ in range(args.steps)]
-    for i in range(args.warmup + args.steps):
-        flush_l2(i)
-        if i >= args.warmup:
-            e2e_marks[i - args.warmup][0].record(stream)
-        for name, t in host.items():
-            getattr(case, name).copy_(t, non_blocking=True)
-        case.decode()
-        out_h.copy_(case.out, non_blocking=True)
-        lse_h.copy_(case.lse, non_blocking=True)
-        if i >= args.warmup:
-            e2e_marks[i - args.warmup][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_marks)
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
         if rank != 0:
             dist.destroy_process_group()
             return 0
-    rows_total = w.num_rows * ws * args.steps
-    step = total_ms / args.steps
-    peak, peak_kind = read_peaks()
-    nb = mla_bytes(w)
-    achieved = nb["total"] / (step / 1e3) / 1e9
-    tflops = nb["flops"] / (step / 1e3) / 1e12
-    bf16_peak = None
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            bf16_peak = float(json.load(f).get("bf16_tflops"))
-    except Exception:
-        pass
-    line = {
-        "metric": MLA_METRIC, "value": rows_total / (total_ms / 1e3), "unit": "rows/s",
-        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 / fp32 acc", "data": "synthetic", "config": mla_config(w),
-        "roofline": {"bound": "hbm", "kernel": "sparse_mla", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
-                     "traffic": None, "algorithmic_bytes_per_launch": nb["total"],
-                     "avg_launch_ms": step},
-        "tensor": {"achieved_tflops": tflops, "peak_bf16_tflops": bf16_peak,
-                   "frac": tflops / bf16_peak if bf16_peak else None,
-                   "note": "mma.sync m16n8k16 bf16"},
-        "e2e": {"value": rows_total / (e2e_ms / 1e3), "unit": "rows/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps, "launch": "cuda_graph", "clocks": clocks.summary(),
-        "cpu_baseline": mla_cpu_run(w),
-    }
+    line = {"metric": MLA_METRIC, "value": w.num_rows * ws * args.steps / (total_ms / 1e3),
+            "unit": "rows/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 / fp32 acc", "data": "synthetic",
+            "config": rep["config"], "roofline": rep["roofline"], "tensor": rep["tensor"],
+            "e2e": rep["e2e"], "gpu_launches": args.steps, "launch": "cuda_graph",
+            "clocks": clocks.summary(), "cpu_baseline": rep["cpu_baseline"]}
     print(json.dumps(line))
     if ws > 1:
         dist.destroy_process_group()
     return 0
-
-
-def rank_seed(workload: str, rank: int) -> int:
-    """Seed of a rank's batch: rank 0 draws the named workload itself, every
-    other rank an independent batch of the same shape."""
-    return W_SEED[workload] + 1000 * rank
-
-
-def workload_config(w):
-    seq = w.seq_lens
-    return {"workload": w.name, "requests": w.num_reqs, "rows": w.num_rows,
-            "query_heads": w.hq, "kv_heads": w.hkv, "head_dim": w.head_dim,
-            "index_dim": w.index_dim, "topk": w.topk,
-            "index_k": ("fp8_e4m3" + (" + per-token scales" if w.idx_k_scale is not None else "")
-                        if getattr(w, "index_dtype", 0) == W.KV_FP8 else "bf16"),
-            "kv": "fp8_e4m3" if w.kv_dtype == W.KV_FP8 else "bf16",
-            "scales": ["none", "scalar", "per_token_head"][w.scale_mode],
-            "sinks": w.sinks is not None, "context_tokens": int(seq.sum()),
-            "median_context": float(np.median(seq)), "l2": "flushed between steps (512 MiB write, then 256 MiB read)"}
 
 
 def run_gpu(args):
@@ -432,19 +615,15 @@ def run_gpu(args):
     ws, rank, local = dist_env()
     if ws > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = f"cuda:{local}"
+    gpu = Gpu(local, flush=not args.profile)
     # weak scaling: every rank owns its own batch of independent requests
     w = W.NAMED[args.workload](seed=rank_seed(args.workload, rank))
-    case = msa.DeviceCase(w, device=dev)
-    stream = torch.cuda.current_stream()
-    flush = None if args.profile else torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    case = msa.DeviceCase(w, device=gpu.dev)
 
     def barrier():
         if ws > 1:
             dist.barrier()
 
-    ev = lambda: torch.cuda.Event(enable_timing=True)
     if args.profile:
         # plain run for profilers: warm-up + K steps, nothing else
         for _ in range(args.warmup + args.steps):
@@ -452,144 +631,96 @@ def run_gpu(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile_run": w.name, "status": int(case.status.item())}))
         return 0
-    rbuf = torch.ones(L2_FLUSH_BYTES // 2, dtype=torch.uint8, device=dev)
-
-    def flush_l2(i):
-        # write a buffer larger than L2, then read another one so that no dirty
-        # lines are left for the timed kernels to write back
-        flush.fill_(i & 0xff)
-        rbuf.sum(dtype=torch.int32)
 
     for i in range(args.warmup):
-        flush_l2(i)
+        gpu.flush_l2(i)
         case.decode(keep_tables=False)
     torch.cuda.synchronize()
     if int(case.status.item()) != 0:
         raise RuntimeError(f"device status {int(case.status.item())} on a clean workload")
 
-    def capture(fn):
-        """The decode call captured once into a CUDA graph (the library is
-        graph-capturable: no host sync, no allocation, no host copy)."""
-        s = torch.cuda.Stream(device=dev)
-        s.wait_stream(torch.cuda.current_stream())
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            fn(s)
-        torch.cuda.current_stream().wait_stream(s)
-        torch.cuda.synchronize()
-        return g
-
     launch_mode = "cuda_graph"
     try:
-        g_main = capture(lambda s: case.decode(keep_tables=False, stream=s))
+        g_main = gpu.capture(lambda s: case.decode(keep_tables=False, stream=s))
+        run_step = g_main.replay
     except Exception as exc:  # graph capture unavailable: time eager launches
-        launch_mode, g_main = f"eager ({type(exc).__name__})", None
-    run_step = (lambda: g_main.replay()) if g_main is not None else \
-        (lambda: case.decode(keep_tables=False))
+        launch_mode = f"eager ({type(exc).__name__})"
+        run_step = lambda: case.decode(keep_tables=False)
 
     # ---- timed: K steps, per-step events on the launching stream
-    marks = [(ev(), ev()) for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        for i in range(args.steps):
-            flush_l2(i)
-            marks[i][0].record(stream)
-            run_step()
-            marks[i][1].record(stream)
-        torch.cuda.synchronize()
-    barrier()
-    step_ms = [a.elapsed_time(b) for a, b in marks]
+        step_ms = gpu.time_steps(run_step, args.steps)
+        barrier()
+        # the median behind the headline: >= 100 more replays, timed the same way
+        med_ms = gpu.time_steps(run_step, max(MEDIAN_ITERS, args.steps))
     total_ms = sum(step_ms)
     if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
+        t = torch.tensor([total_ms], device=gpu.dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
 
-    # ---- per-kernel times: the same step with events after each stage
-    e = [ev() for _ in range(4)]
-    trace = msa.make_trace(e[1], e[2], e[3])
-    # (eager launches: events recorded inside a graph cannot be timed)
-    score_ms, topk_ms, attn_ms = [], [], []
-    for i in range(args.steps):
-        flush_l2(i)
-        # keep the GPU busy (a spin kernel, no memory traffic) while the host
-        # enqueues the call, so that host-side launch time never shows up as
-        # a gap inside the first kernel's interval
-        torch.cuda._sleep(GATE_CYCLES)
-        e[0].record(stream)
-        case.decode(keep_tables=False, trace=trace)
-        torch.cuda.synchronize()
-        score_ms.append(e[0].elapsed_time(e[1]))
-        topk_ms.append(e[1].elapsed_time(e[2]))
-        attn_ms.append(e[2].elapsed_time(e[3]))
-
-    # ---- end to end through the public API: host buffers, copies inside
+    kern = decode_kernel_times(gpu, case, msa, args.steps)
     case.decode()
     torch.cuda.synchronize()
     topk_sel = case.topk_idx[: w.num_rows].cpu().numpy()
-    host = {name: getattr(case, name).cpu().pin_memory()
-            for name in ("q", "idx_q", "cu_q", "cu_k", "ctx", "bt")}
-    out_h = torch.empty_like(case.out, device="cpu").pin_memory()
-    lse_h = torch.empty_like(case.lse, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
-    e2e_marks = [(ev(), ev()) for _ in range(args.steps)]
-    for i in range(args.warmup + args.steps):
-        flush_l2(i)
-        if i >= args.warmup:
-            e2e_marks[i - args.warmup][0].record(stream)
-        for name, t in host.items():
-            getattr(case, name).copy_(t, non_blocking=True)
-        case.decode(keep_tables=False)
-        out_h.copy_(case.out, non_blocking=True)
-        lse_h.copy_(case.lse, non_blocking=True)
-        if i >= args.warmup:
-            e2e_marks[i - args.warmup][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_marks)
+    e2e_ms, h2d, d2h = gpu.e2e(case, DECODE_INPUTS, lambda: case.decode(keep_tables=False),
+                               args.steps, args.warmup)
     if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
+        t = torch.tensor([e2e_ms], device=gpu.dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
+        if rank != 0:
+            dist.destroy_process_group()
+            return 0
 
-    if rank != 0:
-        dist.destroy_process_group()
-        return 0
     rows_total = w.num_rows * ws * args.steps
-    q_lens = np.diff(w.cu_seqlens_q)
-    launches_per_step = 3 + int(q_lens.max() >= 64 and w.index_heads == 1
-                                and getattr(w, "index_dtype", 0) != W.KV_FP8)
     value = rows_total / (total_ms / 1e3)
-    peak, peak_kind = read_peaks()
+    peaks = read_peaks()
     nbytes = algorithmic_bytes(w, topk_sel)
-    score_avg = statistics.mean(score_ms)
+    kr = kernel_rooflines(nbytes, kern, peaks)
+    score_avg = kr["index_score"]["ms"]
     achieved = nbytes["score_kernel"] / (score_avg / 1e3) / 1e9
     step_avg = total_ms / args.steps
-    cpu = cpu_oracle_run(w)
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_avg, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 kv / bf16 q / fp32 acc"
         if w.kv_dtype == W.KV_FP8 else "bf16 / fp32 acc", "data": "synthetic",
         "config": workload_config(w),
-        "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
-                     "traffic": read_traffic(w.name),
+        "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": achieved,
+                     "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"],
+                     "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                     "peak_source": peaks["source"], "traffic": read_traffic(w.name),
                      "algorithmic_bytes_per_launch": nbytes["score_kernel"],
                      "avg_launch_ms": score_avg},
-        "step_roofline": {"algorithmic_bytes": nbytes["total"],
-                          "achieved_gbs": nbytes["total"] / (step_avg / 1e3) / 1e9,
-                          "frac": nbytes["total"] / (step_avg / 1e3) / 1e9 / peak},
-        "kernel_ms": {"index_score": score_avg, "topk_table": statistics.mean(topk_ms),
-                      "sparse_attn": statistics.mean(attn_ms)},
-        "e2e": {"value": rows_total / (e2e_ms / 1e3), "unit": "rows/s",
+        "step_roofline": step_roofline(nbytes["total"], step_avg, peaks),
+        "ms_per_step_median": statistics.median(med_ms), "median_iters": len(med_ms),
+        "kernel_ms": {k: v["ms"] for k, v in kr.items()},
+        "kernels": kr,
+        "e2e": {"value": w.num_rows * ws * args.steps / (e2e_ms / 1e3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step(w) * args.steps,
         "launch": launch_mode,
         "clocks": clocks.summary(),
-        "cpu_baseline": cpu,
+        "cpu_baseline": cpu_oracle_run(w),
     }
+    if ws == 1 and not args.headline_only:
+        # every other workload, measured the same way (one GPU only: under
+        # torchrun the ranks time the headline batch alone)
+        per = {}
+        with ClockSampler(local) as extra_clocks:
+            for name in EXTRA_WORKLOADS:
+                if name == w.name:
+                    continue
+                if name == "sparse_mla_decode":
+                    per[name] = measure_mla(gpu, msa, rank_seed(name, 0), MEDIAN_ITERS, 3,
+                                            EXTRA_CPU_BUDGET_S)[2]
+                else:
+                    per[name] = measure_extra_decode(gpu, msa, name)
+        line["per_workload"] = per
+        line["per_workload_clocks"] = extra_clocks.summary()
     print(json.dumps(line))
     if ws > 1:
         dist.destroy_process_group()
@@ -604,6 +735,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="large_batch_decode",
                     choices=sorted(W.NAMED) + ["sparse_mla_decode"])
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time the named workload only (no per_workload section)")
     ap.add_argument("--profile", action="store_true",
                     help="plain warm-up + K decode steps for a profiler (no timing)")
     args = ap.parse_args(argv)

@@ -204,6 +204,43 @@ cudaError_t launch_scores(ScoreLaunch p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+msa_status attn_prepare(const msa_attn_args* attn, const int32_t* sparse_tbl, int tbl_stride,
+                        const int32_t* sparse_len, const uint32_t* dev_status, int* pps,
+                        int* splits) {
+  msa_status st = check_attn(attn);
+  if (st != MSA_OK) return st;
+  if (!dev_status) return MSA_ERR_NULL;
+  if (tbl_stride < 1) return MSA_ERR_SHAPE;
+  *pps = 0;
+  *splits = 0;
+  if (attn->num_rows == 0) return MSA_OK;
+  if (!sparse_tbl || !sparse_len) return MSA_ERR_NULL;
+  attn_split(attn->num_rows, tbl_stride, attn_ctas_per_sm(attn), pps, splits);
+  return MSA_OK;
+}
+
+size_t attn_scratch_offset_partials(int num_rows) {
+  return round_up((size_t)(num_rows > 0 ? num_rows : 1) * 4, 256);
+}
+
+size_t attn_scratch_need(int num_rows, int splits) {
+  const size_t counters = attn_scratch_offset_partials(num_rows);
+  if (splits <= kMaxClusterSplits) return counters;
+  return counters + round_up((size_t)num_rows * (size_t)splits * kPartFloats * 4, 256);
+}
+
+msa_status attn_run(const msa_attn_args* attn, const int32_t* sparse_tbl, int tbl_stride,
+                    const int32_t* sparse_len, void* scratch, int pps, int splits,
+                    uint32_t* dev_status, cudaStream_t stream) {
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws);
+  float* partials = reinterpret_cast<float*>(ws + attn_scratch_offset_partials(attn->num_rows));
+  AttnLaunch p = make_attn(attn, sparse_tbl, tbl_stride, sparse_len, partials, counters, pps,
+                           splits, dev_status);
+  return cuda_status(launch_sparse_attn(p, stream, false));
+}
+
 }  // namespace msa
 
 using namespace msa;
@@ -282,23 +319,15 @@ msa_status msa_sparse_paged_attn(const msa_attn_args* attn, const int32_t* spars
                                  int32_t tbl_stride, const int32_t* sparse_len, void* workspace,
                                  size_t workspace_bytes, uint32_t* dev_status,
                                  cudaStream_t stream) {
-  msa_status st = check_attn(attn);
-  if (st != MSA_OK) return st;
-  if (!dev_status) return MSA_ERR_NULL;
-  if (tbl_stride < 1) return MSA_ERR_SHAPE;
-  if (attn->num_rows == 0) return MSA_OK;
-  if (!sparse_tbl || !sparse_len) return MSA_ERR_NULL;
+  int pps, splits;
+  const msa_status st =
+      attn_prepare(attn, sparse_tbl, tbl_stride, sparse_len, dev_status, &pps, &splits);
+  if (st != MSA_OK || attn->num_rows == 0) return st;
   const size_t need = msa_workspace_size(attn->num_rows, 0, 0, attn->num_heads, attn->head_dim,
                                          tbl_stride);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return MSA_ERR_WORKSPACE;
-  int pps, splits;
-  attn_split(attn->num_rows, tbl_stride, attn_ctas_per_sm(attn), &pps, &splits);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint32_t* counters = reinterpret_cast<uint32_t*>(ws);
-  float* partials = reinterpret_cast<float*>(ws + round_up((size_t)attn->num_rows * 4, 256));
-  AttnLaunch p = make_attn(attn, sparse_tbl, tbl_stride, sparse_len, partials, counters, pps,
-                           splits, dev_status);
-  return cuda_status(launch_sparse_attn(p, stream, false));
+  return attn_run(attn, sparse_tbl, tbl_stride, sparse_len, workspace, pps, splits, dev_status,
+                  stream);
 }
 
 msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index_cache* index,

@@ -11,10 +11,13 @@
 // device array of fixed size.  Every GPU that loads the library reserves
 // that array until the process exits.
 //
-// The array is shared by every call in the process: the counters are
-// cleared on the stream at the start of each call, and two calls whose
-// kernels overlap on the GPU (different streams, no ordering between them)
-// race on it and give undefined results.
+// The array is shared by every call in the process.  Rows of 2 to 8 splits
+// merge inside their thread-block cluster and rows of one split need no
+// merge, so those calls use only the array's first bytes; rows of more
+// splits (top-k above 128 blocks) merge through the counters and partials,
+// and the counters are cleared on the stream before such a call.  Two calls
+// whose kernels overlap on the GPU (different streams, no ordering between
+// them) race on the array and give undefined results.
 #include <mutex>
 
 #include "msa_internal.cuh"
@@ -52,16 +55,25 @@ extern "C" msa_status msa_sparse_paged_attn_static(const msa_attn_args* attn,
                                                    const int32_t* sparse_tbl, int32_t tbl_stride,
                                                    const int32_t* sparse_len,
                                                    uint32_t* dev_status, cudaStream_t stream) {
-  if (!attn) return MSA_ERR_NULL;
-  if (attn->num_rows < 0 || tbl_stride < 1) return MSA_ERR_SHAPE;
-  const size_t need =
-      msa_workspace_size(attn->num_rows, 0, 0, attn->num_heads, attn->head_dim, tbl_stride);
-  if (need == 0 || need > (size_t)MSA_STATIC_SCRATCH_BYTES) return MSA_ERR_WORKSPACE;
+  // every argument check first: a refused call touches neither the array nor
+  // the stream
+  int pps = 0, splits = 0;
+  const msa_status st =
+      msa::attn_prepare(attn, sparse_tbl, tbl_stride, sparse_len, dev_status, &pps, &splits);
+  if (st != MSA_OK || attn->num_rows == 0) return st;
+  // only what this launch's split uses: the per-row counters, plus the
+  // (m, l, acc) partials when a row has more splits than one cluster merges
+  if (msa::attn_scratch_need(attn->num_rows, splits) > (size_t)MSA_STATIC_SCRATCH_BYTES)
+    return MSA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MSA_ERR_CUDA;
-  // the split counters must start at zero; the array keeps the last call's contents
-  const size_t counter_bytes = (size_t)(attn->num_rows > 0 ? attn->num_rows : 1) * sizeof(uint32_t);
-  if (cudaMemsetAsync(scratch, 0, counter_bytes, stream) != cudaSuccess) return MSA_ERR_CUDA;
-  return msa_sparse_paged_attn(attn, sparse_tbl, tbl_stride, sparse_len, scratch,
-                               (size_t)MSA_STATIC_SCRATCH_BYTES, dev_status, stream);
+  if (splits > msa::kMaxClusterSplits) {
+    // the last-arriver counters must start at zero; the array keeps whatever
+    // the last call (or an interrupted one) left there
+    if (cudaMemsetAsync(scratch, 0, (size_t)attn->num_rows * sizeof(uint32_t), stream) !=
+        cudaSuccess)
+      return MSA_ERR_CUDA;
+  }
+  return msa::attn_run(attn, sparse_tbl, tbl_stride, sparse_len, scratch, pps, splits,
+                       dev_status, stream);
 }

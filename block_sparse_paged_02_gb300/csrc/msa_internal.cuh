@@ -25,6 +25,10 @@ constexpr int kTcMinRows = 64;
 constexpr int kMaxTopk = 2048;
 // at most this many page-16 entries per attention split (<= 32 per warp)
 constexpr int kMaxSplitEntries = 128;
+// the splits of a row merge inside one thread-block cluster when there are at
+// most this many (the portable cluster size); more merge through scratch
+// partials finished by the last-arriving CTA
+constexpr int kMaxClusterSplits = 8;
 
 // Attention launch shape: stages of each warp's copy ring and the CTAs per SM
 // the grid is sized for (compile-time, so that launch-shape sweeps can build
@@ -375,6 +379,20 @@ int mla_max_tokens_per_split();
 // results on the device before reading them.
 cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream, bool programmatic);
 cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t stream, bool programmatic);
+
+// Step 4 behind its entry points (api.cu).  attn_prepare validates the
+// arguments (nothing is launched; *splits = 0 when there are no rows) and
+// picks the work split; attn_scratch_need is the scratch that split uses:
+// per-row merge counters, plus (m, l, acc) partials when a row has more
+// splits than one cluster merges; attn_run launches on that scratch (the
+// counters must be zero, and the kernel leaves them zero).
+msa_status attn_prepare(const msa_attn_args* attn, const int32_t* sparse_tbl, int tbl_stride,
+                        const int32_t* sparse_len, const uint32_t* dev_status, int* pps,
+                        int* splits);
+size_t attn_scratch_need(int num_rows, int splits);
+msa_status attn_run(const msa_attn_args* attn, const int32_t* sparse_tbl, int tbl_stride,
+                    const int32_t* sparse_len, void* scratch, int pps, int splits,
+                    uint32_t* dev_status, cudaStream_t stream);
 
 int device_sm_count();
 

@@ -43,10 +43,6 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;  // log2 units: unnormalised weights stay <= 256
 constexpr int kAccStride = 132;  // padded head stride of the shared-memory merge area
 constexpr int kAccWarpFloats = kMaxHeads * kAccStride;  // 2112
-// a row's splits merge inside one thread-block cluster when there are at
-// most this many (the portable cluster size); more splits merge through the
-// workspace (last-arriving CTA)
-constexpr int kMaxClusterSplits = 8;
 // per-CTA partial for the cluster merge, after the warps' merge area:
 // acc [16][128], m [16], l [16], poison flag
 constexpr int kCPart = kWarps * (kAccWarpFloats + 2 * kMaxHeads) * 4;

@@ -48,9 +48,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;  // log2 units
 constexpr int kPartHeadFloats = 4 + kMlaDv;        // m, l, 2 pad, acc[512] (16-B aligned)
-// a (row, head group)'s splits merge inside one thread-block cluster when
-// there are at most this many (the portable cluster size)
-constexpr int kMaxClusterSplits = 8;
 
 struct MlaSmem {
   static constexpr int kRing = 0;

@@ -243,17 +243,25 @@ msa_status msa_sparse_paged_attn(const msa_attn_args* attn, const int32_t* spars
  * host framework owns all device memory and offers no allocator, runtimes
  * that forbid allocation after start-up.  (The pages have no counterpart;
  * it is an addition of this library.)
- * Same arguments, semantics and results as msa_sparse_paged_attn, minus the
- * workspace: the split-merge scratch comes from one static device array of
- * MSA_STATIC_SCRATCH_BYTES.  Returns MSA_ERR_WORKSPACE when the call would
- * need more than that (msa_workspace_size(num_rows, 0, 0, num_heads,
- * head_dim, tbl_stride) > MSA_STATIC_SCRATCH_BYTES).  Allocates nothing and
- * calls no allocating routine.
+ * Same arguments, semantics, argument checks and results as
+ * msa_sparse_paged_attn, minus the workspace: the split-merge scratch comes
+ * from one static device array of MSA_STATIC_SCRATCH_BYTES.  Argument errors
+ * are returned before anything touches the array or the stream.
+ *   - Scratch use: rows are split along their tokens (at most 128 page-16
+ *     entries per split).  Rows of 1 to 8 splits (tbl_stride <= 1024, i.e.
+ *     top-k <= 128 blocks) merge inside a thread-block cluster and use only
+ *     4 bytes per row (rounded up to 256).  Rows of more splits merge
+ *     through partials: 4 + 8320 * splits bytes per row, splits =
+ *     ceil(tbl_stride / 128).  A call needing more than
+ *     MSA_STATIC_SCRATCH_BYTES returns MSA_ERR_WORKSPACE (e.g. more than
+ *     ~100 rows at tbl_stride 1280).
+ *   - Allocates nothing and calls no allocating routine.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
- *   - Each call clears the array's counters on `stream` (cudaMemsetAsync)
- *     before the kernel; the rest of the array keeps the last call's data.
+ *   - A call of more than 8 splits clears the array's counters on `stream`
+ *     (cudaMemsetAsync) before the kernel; the rest of the array keeps the
+ *     last call's data.
  *   - The array is shared by all calls in the process: calls whose kernels
  *     overlap on the GPU race on it (order them on one stream). */
 msa_status msa_sparse_paged_attn_static(const msa_attn_args* attn, const int32_t* sparse_tbl,

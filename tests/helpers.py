@@ -37,24 +37,6 @@ def valid_score_mask(geom, score_stride):
     return mask
 
 
-def sub_workload(w, rows):
-    """A batch holding only the given rows, each as its own one-row request at
-    the same position over the same pages and caches.  A row's result depends
-    only on its own position, query and its request's pages, so the oracle on
-    this batch reproduces those rows of the full batch."""
-    req_of = np.searchsorted(w.cu_seqlens_q, np.arange(w.num_rows), side="right") - 1
-    rows = np.asarray(rows)
-    pos = np.array([w.context_lens[req_of[r]] + (r - w.cu_seqlens_q[req_of[r]]) for r in rows])
-    seq = pos + 1
-    n = len(rows)
-    cu = np.arange(n + 1, dtype=np.int32)
-    cu_k = np.concatenate([[0], np.cumsum(seq)]).astype(np.int32)
-    sub = W.Workload(name=w.name + "_rows", cu_seqlens_q=cu, cu_seqlens_k=cu_k,
-                     context_lens=pos.astype(np.int32),
-                     block_table=w.block_table[req_of[rows]].copy(), num_pages=w.num_pages,
-                     idx_q=w.idx_q[rows], idx_k=w.idx_k, topk=w.topk, q=w.q[rows],
-                     k_cache=w.k_cache, v_cache=w.v_cache, kv_dtype=w.kv_dtype,
-                     scale_mode=w.scale_mode, k_scale=w.k_scale, v_scale=w.v_scale,
-                     sinks=w.sinks, softmax_scale=w.softmax_scale, seed=w.seed,
-                     index_dtype=w.index_dtype, idx_k_scale=w.idx_k_scale)
-    return sub
+# A batch holding only the given rows (each its own one-row request at the
+# same position over the same pages); see workloads.row_subset.
+sub_workload = W.row_subset

@@ -12,6 +12,7 @@ and context length); PR 54404 page "Features and motivation" / "Key source
 snippets" (sinks, natural-log LSE); PR 56170 page "Key source snippets"
 (128-token blocks, cu_seqlens).
 """
+import dataclasses
 import itertools
 import math
 import os
@@ -590,6 +591,94 @@ def test_kv_insert_fp8_per_token_scale_definition(orc):
             assert np.abs(vals).max() == 448.0  # the largest element lands on the top code
             np.testing.assert_allclose(vals * s, x, rtol=2 ** -4, atol=s * 2 ** -9)
             r += 1
+
+
+# Hand-worked codes of the SCALAR and NONE insert rules (code = e4m3 of x / s):
+# (x, s, code) from the OCP e4m3fn definition -- bias 7, 3 mantissa bits,
+# value = 2^(e-7) * (1 + m/8), largest finite 448 = 0x7E.  Each pair is chosen
+# so that a plausible slip changes the code: x * s instead of x / s, no
+# saturation, round-half-up instead of half-to-even, a dropped sign.
+_SCALAR_INSERT_CASES = [
+    (1.0, 0.5, 0x40),       # 1 / 0.5 = 2 = 2^1 -> e = 8, m = 0   (x * s = 0.5 would give 0x30)
+    (-3.0, 2.0, 0xBC),      # -1.5 -> e = 7, m = 4, sign bit
+    (2.125, 2.0, 0x38),     # 1.0625: halfway 1.0 (0x38) / 1.125 (0x39) -> even 0x38
+    (2.375, 2.0, 0x3A),     # 1.1875: halfway 1.125 (0x39) / 1.25 (0x3A) -> even 0x3A
+    (300.0, 0.5, 0x7E),     # 600 is beyond 448: saturate
+    (-300.0, 0.5, 0xFE),    # ... keeping the sign
+    (0.0, 4.0, 0x00),
+    (0.0078125, 4.0, 0x01),  # 2^-7 / 4 = 2^-9, the smallest subnormal
+    (96.0, 0.25, 0x7C),     # 384 = 2^8 * 1.5 -> e = 15, m = 4
+]
+_NONE_INSERT_CASES = [      # s = 1: the codes of x itself
+    (1.0, 0x38), (-0.5, 0xB0), (1000.0, 0x7E), (1.0625, 0x38), (0.001953125, 0x01),
+    (240.0, 0x77),          # 240 = 2^7 * 1.875 -> e = 14, m = 7
+]
+
+
+def _fp8_insert_workload(scale_mode, k_s, v_s, seed):
+    w = W.custom(seed, q_lens=[2, 1], seq_lens=[500, 77], hq=4, di=64, topk=2,
+                 kv_dtype=W.KV_FP8, scale_mode=scale_mode)
+    if scale_mode == W.SCALE_SCALAR:
+        w = dataclasses.replace(w, k_scale=np.array([k_s], np.float32),
+                                v_scale=np.array([v_s], np.float32))
+    return w
+
+
+def _slot(w, r):
+    q = int(np.searchsorted(w.cu_seqlens_q, r, side="right") - 1)
+    pos = int(w.context_lens[q]) + r - int(w.cu_seqlens_q[q])
+    return w.block_table[q, pos // 128], pos % 128
+
+
+@pytest.mark.parametrize("mode", ["scalar", "none"])
+def test_kv_insert_fp8_fixed_scale_hand_worked_codes(orc, mode):
+    # one hand-worked element at dim i of row 0's K and dim 5 + i of row 1's V,
+    # the rest zero; every case brings its own scale, so one workload each
+    cases = (_SCALAR_INSERT_CASES if mode == "scalar"
+             else [(x, 1.0, c) for x, c in _NONE_INSERT_CASES])
+    for i, (x, s, code) in enumerate(cases):
+        w = _fp8_insert_workload(W.SCALE_SCALAR if mode == "scalar" else W.SCALE_NONE, s, s,
+                                 seed=94)
+        k_new = np.zeros((w.num_rows, w.hkv, w.head_dim), np.float32)
+        v_new = np.zeros_like(k_new)
+        k_new[0, 0, i] = x
+        v_new[1, 0, 5 + i] = x
+        idx_new = W.bf16_bits(np.zeros((w.num_rows, w.index_heads, w.index_dim)))
+        k, v, _, ks, vs, st = orc.kv_insert(w, W.bf16_bits(k_new), W.bf16_bits(v_new), idx_new)
+        assert st == 0
+        pk, sk = _slot(w, 0)
+        pv, sv = _slot(w, 1)
+        assert k[pk, sk, 0, i] == code, (x, s, hex(int(k[pk, sk, 0, i])), hex(code))
+        assert v[pv, sv, 0, 5 + i] == code, (x, s)
+        assert np.count_nonzero(k[pk, sk, 0]) == (code & 0x7F != 0)
+        if mode == "scalar":  # the given scales are inputs, never rewritten
+            assert ks[0] == np.float32(s) and vs[0] == np.float32(s)
+
+
+@pytest.mark.parametrize("mode", [W.SCALE_SCALAR, W.SCALE_NONE])
+def test_kv_insert_fp8_fixed_scale_matches_torch_cast(orc, mode):
+    # a sweep over normal, large and tiny values: code = torch's float8_e4m3fn
+    # cast (round to nearest even) of the fp32 quotient x / s, saturated
+    w = _fp8_insert_workload(mode, 0.37109375, 2.75, seed=95)
+    rng = np.random.default_rng(96)
+    mag = np.exp(rng.uniform(np.log(1e-4), np.log(2e3), (w.num_rows, w.hkv, w.head_dim)))
+    sign = rng.choice([-1.0, 1.0], size=mag.shape)
+    k_new = W.bf16_bits(mag * sign)
+    v_new = W.bf16_bits(-mag[::-1] * sign)
+    idx_new = W.bf16_bits(rng.integers(-3, 4, (w.num_rows, w.index_heads, w.index_dim)))
+    k, v, _, _, _, st = orc.kv_insert(w, k_new, v_new, idx_new)
+    assert st == 0
+    to_f = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).float().numpy()
+    sk_ = np.float32(w.k_scale[0]) if mode == W.SCALE_SCALAR else np.float32(1)
+    sv_ = np.float32(w.v_scale[0]) if mode == W.SCALE_SCALAR else np.float32(1)
+    for r in range(w.num_rows):
+        page, slot = _slot(w, r)
+        want_k = W.fp8_codes(to_f(k_new[r, 0]) / sk_)
+        want_v = W.fp8_codes(to_f(v_new[r, 0]) / sv_)
+        assert np.array_equal(k[page, slot, 0], want_k)
+        assert np.array_equal(v[page, slot, 0], want_v)
+    # the sweep reaches both the saturating and the subnormal range
+    assert (np.abs(to_f(k_new)) / sk_ > 448).any() and (np.abs(to_f(k_new)) / sk_ < 2 ** -6).any()
 
 
 @pytest.mark.parametrize("scaled", [True, False])

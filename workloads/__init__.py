@@ -279,6 +279,28 @@ def custom(seed: int, q_lens, seq_lens, *, hq=16, di=128, idx_range=3, topk=16,
                   fill_unused_nan=fill_unused_nan)
 
 
+def row_subset(w: Workload, rows) -> Workload:
+    """A batch holding only the given rows, each as its own one-row request at
+    the same position over the same pages and caches.  A row's result depends
+    only on its own position, query and its request's pages, so the oracle on
+    this batch reproduces those rows of the full batch."""
+    req_of = np.searchsorted(w.cu_seqlens_q, np.arange(w.num_rows), side="right") - 1
+    rows = np.asarray(rows)
+    pos = np.array([w.context_lens[req_of[r]] + (r - w.cu_seqlens_q[req_of[r]]) for r in rows])
+    seq = pos + 1
+    n = len(rows)
+    cu = np.arange(n + 1, dtype=np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(seq)]).astype(np.int32)
+    return Workload(name=w.name + "_rows", cu_seqlens_q=cu, cu_seqlens_k=cu_k,
+                    context_lens=pos.astype(np.int32),
+                    block_table=w.block_table[req_of[rows]].copy(), num_pages=w.num_pages,
+                    idx_q=w.idx_q[rows], idx_k=w.idx_k, topk=w.topk, q=w.q[rows],
+                    k_cache=w.k_cache, v_cache=w.v_cache, kv_dtype=w.kv_dtype,
+                    scale_mode=w.scale_mode, k_scale=w.k_scale, v_scale=w.v_scale,
+                    sinks=w.sinks, softmax_scale=w.softmax_scale, seed=w.seed,
+                    index_dtype=w.index_dtype, idx_k_scale=w.idx_k_scale)
+
+
 def fp8_index(w: Workload, seed: int, scaled: bool = True) -> Workload:
     """The same workload with its index-K cache stored as OCP e4m3 codes (the
     integer index values are exact in e4m3; NaN fill stays NaN) and, when
