@@ -39,6 +39,11 @@ namespace {
 #ifndef MSA_TOPK_RADIX_MAX_ROWS
 #define MSA_TOPK_RADIX_MAX_ROWS 32
 #endif
+// batches of at least this many rows (with at most 1024 blocks and top-k <=
+// 128) run one warp per row
+#ifndef MSA_TOPK_WARP_MIN_ROWS
+#define MSA_TOPK_WARP_MIN_ROWS 512
+#endif
 
 // Exclusive scan of one int per thread over a CTA of THREADS threads (two
 // barriers); *total receives the sum.  scratch holds THREADS/32 + 1 ints.
@@ -309,6 +314,192 @@ __global__ void __launch_bounds__(256) topk_table_kernel_multi(const TopkLaunch 
   topk_table_body<KPT, 256, false>(p);
 }
 
+// ------------------------------------------------- one warp per row
+//
+// Thousands of rows with at most 1024 candidate blocks each (a prefill
+// chunk: every new token is a row): a 1024-thread CTA per row spends most of
+// its time on CTA-wide barriers and per-row set-up, so here one warp owns a
+// row and a CTA of 8 warps shares the batch checks.  Lane l holds the KPL
+// consecutive blocks l*KPL .. l*KPL+KPL-1, so lane order is block order; the
+// k-th largest key comes from the same bit-by-bit search (one warp
+// reduction per bit, no barrier) and one warp scan of the packed (== T, > T)
+// counts places the selection, as in the CTA form above.
+constexpr int kWarpRows = 8;            // rows (warps) per CTA
+constexpr int kWarpTopkMax = 128;       // largest k of the warp form
+
+template <int KPL>
+__global__ void __launch_bounds__(kWarpRows * 32) topk_table_kernel_warp(const TopkLaunch p) {
+  extern __shared__ int wsm[];
+  int* cuq = wsm;                             // [R + 1] cu_seqlens_q
+  int* sel_all = wsm + p.batch.num_reqs + 1;  // [kWarpRows][topk] selected blocks
+  __shared__ int s_bad;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  const msa_batch& b = p.batch;
+  const int R = b.num_reqs;
+  const int k = p.topk;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned full = 0xffffffffu;
+
+  // ---- batch checks shared by the CTA's rows: cu_seqlens_q tiles the rows
+  if (tid == 0)
+    s_bad = (b.cu_seqlens_q[0] == 0 && b.cu_seqlens_q[R] == b.num_rows) ? 0 : MSA_DEV_MALFORMED;
+  bool mono = true;
+  for (int q = tid; q <= R; q += blockDim.x) {
+    const int c = b.cu_seqlens_q[q];
+    cuq[q] = c;
+    if (q < R) mono &= b.cu_seqlens_q[q + 1] >= c;
+  }
+  const bool all_mono = __syncthreads_and(mono) != 0;
+  if (!all_mono && tid == 0) s_bad = MSA_DEV_MALFORMED;
+  __syncthreads();
+
+  const int r = blockIdx.x * kWarpRows + warp;
+  if (r >= b.num_rows) return;
+  int* sel = sel_all + warp * k;
+  uint32_t bad = (uint32_t)s_bad;
+  int q = -1, q0 = 0, qlen = 0, ctx = 0, nbq = 0;
+  if (!bad) {
+    // the row's request: the last q with cu_q[q] <= r (cu_q sorted, r < cu_q[R])
+    int lo = 0, hi = R;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cuq[mid] <= r) lo = mid; else hi = mid;
+    }
+    q = lo;
+    bad = request_lengths(b, q, &q0, &qlen, &ctx, &nbq);
+  }
+  if (!bad) {
+    int page_bad = 0;
+    for (int blk = lane; blk < nbq; blk += 32) {
+      const int page = b.block_table[(long long)q * b.bt_stride + blk];
+      page_bad |= (page < 0 || page >= b.num_pages);
+    }
+    if (__any_sync(full, page_bad)) bad = MSA_DEV_BAD_PAGE;
+  }
+  // everything above reads only the batch geometry; the scores come from the
+  // previous kernel on the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  int32_t* out_idx = p.topk_idx + (long long)r * k;
+  int32_t* out_tbl = p.tbl + (long long)r * p.tbl_stride;
+  if (bad) {
+    const bool report = (q >= 0) ? (r == q0) : (r == 0);
+    if (lane == 0 && report) atomicOr(p.status, bad);
+    for (int i = lane; i < k; i += 32) out_idx[i] = -1;
+    for (int i = lane; i < p.tbl_stride; i += 32) out_tbl[i] = 0;
+    if (lane == 0) {
+      p.sparse_len[r] = 0;
+      if (p.attn_counters) p.attn_counters[r] = 0;
+    }
+    return;
+  }
+  const int L = ctx + (r - q0) + 1;  // visible tokens
+  const int n = (L + kBlock - 1) / kBlock;
+  const float* srow = p.scores + (long long)r * p.score_stride;
+  const int m = min(k, n);
+  if (n <= k) {  // every candidate is selected
+    for (int i = lane; i < n; i += 32) {
+      sel[i] = i;
+      out_idx[i] = i;
+    }
+  } else {
+    uint32_t key[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int blk = KPL * lane + i;
+      key[i] = blk < n ? score_key(srow[blk]) : 0u;  // 0 ranks below every candidate
+    }
+    // ---- the k-th largest key T, bit by bit from the top
+    uint32_t T = 0;
+#pragma unroll 1
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = T | (1u << bit);
+      int c = 0;
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) c += key[i] >= cand;
+      if (__reduce_add_sync(full, c) >= k) T = cand;
+    }
+    // ---- keys > T, then the lowest-indexed keys == T until k are taken
+    int my_gt = 0, my_eq = 0;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const bool live = KPL * lane + i < n;
+      my_gt += live && key[i] > T;
+      my_eq += live && key[i] == T;
+    }
+    const int packed = (my_eq << 16) | my_gt;
+    int incl = packed;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(full, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int total = __shfl_sync(full, incl, 31);
+    const int before = incl - packed;
+    const int gt_before = before & 0xffff, eq_before = before >> 16;
+    const int need_eq = k - (total & 0xffff);
+    int gt_seen = 0, eq_seen = 0;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int blk = KPL * lane + i;
+      if (blk < n) {
+        const bool gt = key[i] > T, eq = key[i] == T;
+        const int eq_rank = eq_before + eq_seen;
+        if (gt || (eq && eq_rank < need_eq)) {
+          const int at = gt_before + gt_seen + min(eq_rank, need_eq);
+          sel[at] = blk;
+          out_idx[at] = blk;
+        }
+        gt_seen += gt;
+        eq_seen += eq;
+      }
+    }
+  }
+  for (int i = m + lane; i < k; i += 32) out_idx[i] = -1;
+  __syncwarp();
+
+  // ---- page-16 expansion, zero fill bounded by the row width
+  const int32_t* bt_row = b.block_table + (long long)q * b.bt_stride;
+  for (int i = lane; i < p.tbl_stride; i += 32) {
+    const int e = i >> 3, j = i & 7;
+    int v = 0;
+    if (e < m) {
+      const int blk = sel[e];
+      const int valid = min(kBlock, L - kBlock * blk);
+      if (j < (valid + kPage16 - 1) / kPage16) v = 8 * __ldg(bt_row + blk) + j;
+    }
+    out_tbl[i] = v;
+  }
+  if (lane == 0) {
+    // only the block holding the row's last token can be partial, and it is
+    // the highest selected block when selected
+    p.sparse_len[r] = m > 0 ? kBlock * (m - 1) + min(kBlock, L - kBlock * sel[m - 1]) : 0;
+    if (p.attn_counters) p.attn_counters[r] = 0;
+  }
+}
+
+template <int KPL>
+cudaError_t launch_warp(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
+  auto kern = topk_table_kernel_warp<KPL>;
+  const size_t smem = (size_t)(p.batch.num_reqs + 1 + kWarpRows * p.topk) * sizeof(int);
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.batch.num_rows + kWarpRows - 1) / kWarpRows);
+  cfg.blockDim = dim3(kWarpRows * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = programmatic ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <int KPT, int THREADS, bool RADIX = false>
 cudaError_t launch_kpt(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
   void (*kern)(const TopkLaunch);
@@ -342,6 +533,12 @@ cudaError_t launch_kpt(const TopkLaunch& p, cudaStream_t stream, bool programmat
 cudaError_t launch_topk_table(const TopkLaunch& p, cudaStream_t stream, bool programmatic) {
   if (p.batch.num_rows == 0) return cudaSuccess;
   // a row has at most bt_stride candidate blocks
+  if (p.batch.num_rows >= MSA_TOPK_WARP_MIN_ROWS && p.topk <= kWarpTopkMax &&
+      p.batch.bt_stride <= 1024) {
+    if (p.batch.bt_stride <= 256) return launch_warp<8>(p, stream, programmatic);
+    if (p.batch.bt_stride <= 512) return launch_warp<16>(p, stream, programmatic);
+    return launch_warp<32>(p, stream, programmatic);
+  }
   if (p.batch.bt_stride <= 1024) {
     if (p.batch.num_rows <= MSA_TOPK_RADIX_MAX_ROWS && p.batch.bt_stride > 512)
       return launch_kpt<1, 1024, true>(p, stream, programmatic);

@@ -239,6 +239,29 @@ def test_many_rows_single_split(msa, orc):
     check_against_oracle(orc, w, sep, fused)
 
 
+@pytest.mark.parametrize("long_seq", [20_000, 60_000, 120_000])
+def test_many_rows_warp_topk(msa, orc, long_seq):
+    # >= 512 rows take the warp-per-row top-k; the longest request sets the
+    # block-table width (157 / 469 / 938 blocks: 8, 16 or 32 keys per lane).
+    # Index values in {-1, 0, 1} make many blocks tie at the threshold; an
+    # empty request, a request with a page outside the pool and rows that
+    # see fewer blocks than k are in the same batch.
+    q_lens = [400, 0, 100, 6, 10, 3]
+    seq = [2600, 50, 1500, long_seq, 9000, 300]
+    w = W.custom(61, q_lens=q_lens, seq_lens=seq, hq=8, di=64, idx_range=1, topk=8,
+                 kv_dtype=W.KV_BF16, with_sink=True)
+    bt = w.block_table.copy()
+    bt[2, 3] = w.num_pages + 1
+    w.block_table = bt
+    c, sep, fused = run_steps(msa, w)
+    ref = orc.decode(w)
+    assert sep["status"] == ref["status"] == msa.MSA_DEV_BAD_PAGE
+    for key in ("topk_idx", "tbl", "sparse_len"):
+        assert np.array_equal(sep[key], ref[key]), key
+        assert np.array_equal(fused[key], sep[key]), key
+    assert_attn_close(sep["out"], sep["lse"], ref["out"], ref["lse"])
+
+
 def test_poisoned_requests_match_oracle(msa, orc):
     w = W.custom(57, q_lens=[1, 2, 1, 1], seq_lens=[900, 700, 400, 300], hq=16, di=128, topk=2,
                  with_sink=True)
