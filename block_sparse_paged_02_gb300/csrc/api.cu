@@ -58,25 +58,51 @@ int attn_ctas_per_sm(const msa_attn_args* a) {
 }
 
 struct DecodeWs {
-  size_t counters, scores, topk, tbl, len, partials, total;
+  size_t counters, scores, topk, tbl, len, partials;
+  // prefill path (present when topk <= kPrefillMaxTopk): route [N], list
+  // counts and lists, the plan, the per-(row, slot) partials
+  bool prefill;
+  size_t route, pf_counts, pf_lists, plan_hdr, plan_req_q, plan_req_item, item_q, item_b,
+      item_cnt, item_chunk, part_o, part_lse;
+  long long max_routed_reqs, max_items;
+  size_t total;
 };
 
 DecodeWs decode_layout(int num_rows, int bt_stride, int topk, int splits) {
   DecodeWs w;
   const size_t n = (size_t)(num_rows > 0 ? num_rows : 1);
   size_t off = 0;
-  w.counters = off;
-  off = round_up(off + n * 4, 256);
-  w.scores = off;
-  off = round_up(off + n * (size_t)bt_stride * 4, 256);
-  w.topk = off;
-  off = round_up(off + n * (size_t)topk * 4, 256);
-  w.tbl = off;
-  off = round_up(off + n * (size_t)topk * 8 * 4, 256);
-  w.len = off;
-  off = round_up(off + n * 4, 256);
-  w.partials = off;
-  off = round_up(off + n * (size_t)splits * kPartFloats * 4, 256);
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  };
+  w.counters = take(n * 4);
+  w.scores = take(n * (size_t)bt_stride * 4);
+  w.topk = take(n * (size_t)topk * 4);
+  w.tbl = take(n * (size_t)topk * 8 * 4);
+  w.len = take(n * 4);
+  w.partials = take(n * (size_t)splits * kPartFloats * 4);
+  w.prefill = topk >= 1 && topk <= kPrefillMaxTopk;
+  if (w.prefill) {
+    // a routed request has >= kPrefillMinRows rows, so at most n / 64 of them,
+    // each with at most bt_stride blocks; list counts sit at q0 * bt / 64
+    const size_t bt = (size_t)bt_stride;
+    w.max_routed_reqs = (long long)(n / kPrefillMinRows + 1);
+    w.max_items = (long long)(n * bt / kPrefillMinRows + bt);
+    w.route = take(n * 4);
+    w.pf_counts = take((size_t)w.max_items * 4);
+    w.pf_lists = take(n * bt * 4);
+    w.plan_hdr = take(64);
+    w.plan_req_q = take((size_t)w.max_routed_reqs * 4);
+    w.plan_req_item = take((size_t)w.max_routed_reqs * 4);
+    w.item_q = take((size_t)w.max_items * 4);
+    w.item_b = take((size_t)w.max_items * 4);
+    w.item_cnt = take((size_t)w.max_items * 4);
+    w.item_chunk = take((size_t)w.max_items * 4);
+    w.part_o = take(n * (size_t)topk * 16 * kHeadDim * 2);
+    w.part_lse = take(n * (size_t)topk * 16 * 4);
+  }
   w.total = off;
   return w;
 }
@@ -148,6 +174,7 @@ AttnLaunch make_attn(const msa_attn_args* a, const int32_t* tbl, int tbl_stride,
   L.splits = splits;
   L.pages_per_split = pps;
   L.status = status;
+  L.route = nullptr;
   return L;
 }
 
@@ -310,8 +337,8 @@ msa_status msa_topk_build_table(const msa_batch* batch, const float* scores,
     return MSA_ERR_NULL;
   if (batch->num_rows == 0) return MSA_OK;
   if (batch->num_reqs == 0) return MSA_ERR_SHAPE;  // rows without any request
-  TopkLaunch p{*batch, scores, score_stride, topk, topk_idx, sparse_tbl, tbl_stride, sparse_len,
-               nullptr, dev_status};
+  TopkLaunch p{*batch,     scores,     score_stride, topk,    topk_idx, sparse_tbl, tbl_stride,
+               sparse_len, nullptr,    dev_status,   nullptr, nullptr,  nullptr};
   return cuda_status(launch_topk_table(p, stream, false));
 }
 
@@ -369,6 +396,18 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
   const int tstride = sparse_tbl ? tbl_stride : 8 * topk;
   int32_t* len = sparse_len ? sparse_len : reinterpret_cast<int32_t*>(ws + L.len);
 
+  // Rows of requests with >= kPrefillMinRows rows take the block-major
+  // tensor-core attention when the batch may hold any (the max_q_len hint),
+  // the KV is bf16 without per-token scales and the selection fits a list
+  // entry; every other row takes the split-K decode attention.
+  const bool prefill = L.prefill && batch->max_q_len >= kPrefillMinRows &&
+                       attn->kv_dtype == MSA_KV_BF16 &&
+                       attn->scale_mode != MSA_SCALE_PER_TOKEN_HEAD &&
+                       batch->num_rows < (1 << 23) && prefill_attn_available();
+  int32_t* route = prefill ? reinterpret_cast<int32_t*>(ws + L.route) : nullptr;
+  int32_t* pf_counts = prefill ? reinterpret_cast<int32_t*>(ws + L.pf_counts) : nullptr;
+  int32_t* pf_lists = prefill ? reinterpret_cast<int32_t*>(ws + L.pf_lists) : nullptr;
+
   ScoreLaunch sp{*batch, static_cast<const uint16_t*>(idx_q),
                  static_cast<const uint8_t*>(index->k_cache), index->heads, index->dim, scores,
                  batch->bt_stride, dev_status, 0, index->dtype == MSA_KV_FP8_E4M3,
@@ -377,14 +416,55 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_score) cudaEventRecord(trace->after_score, stream);
 
-  TopkLaunch tp{*batch, scores, batch->bt_stride, topk, k_idx, tbl, tstride, len, counters,
-                dev_status};
+  if (prefill) {
+    // the list counters start at zero on every call, whatever another call
+    // (of another shape) left in this workspace
+    if (cudaMemsetAsync(pf_counts, 0, (size_t)L.max_items * 4, stream) != cudaSuccess)
+      return MSA_ERR_CUDA;
+  }
+  TopkLaunch tp{*batch, scores,     batch->bt_stride, topk,  k_idx,   tbl, tstride,
+                len,    counters,   dev_status,       route, pf_counts, pf_lists};
   e = launch_topk_table(tp, stream, true);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_topk) cudaEventRecord(trace->after_topk, stream);
 
+  if (prefill) {
+    PrefillLaunch pl;
+    pl.batch = *batch;
+    pl.q = static_cast<const uint16_t*>(attn->q);
+    pl.num_heads = attn->num_heads;
+    pl.k = static_cast<const uint16_t*>(attn->k_cache);
+    pl.v = static_cast<const uint16_t*>(attn->v_cache);
+    pl.k_scale = attn->scale_mode == MSA_SCALE_SCALAR ? attn->k_scale : nullptr;
+    pl.v_scale = attn->scale_mode == MSA_SCALE_SCALAR ? attn->v_scale : nullptr;
+    pl.sinks = attn->sinks;
+    pl.softmax_scale = attn->softmax_scale;
+    pl.topk = topk;
+    pl.topk_idx = k_idx;
+    pl.route = route;
+    pl.pf_counts = pf_counts;
+    pl.pf_lists = pf_lists;
+    pl.plan_hdr = reinterpret_cast<int32_t*>(ws + L.plan_hdr);
+    pl.plan_req_q = reinterpret_cast<int32_t*>(ws + L.plan_req_q);
+    pl.plan_req_item = reinterpret_cast<int32_t*>(ws + L.plan_req_item);
+    pl.item_q = reinterpret_cast<int32_t*>(ws + L.item_q);
+    pl.item_b = reinterpret_cast<int32_t*>(ws + L.item_b);
+    pl.item_cnt = reinterpret_cast<int32_t*>(ws + L.item_cnt);
+    pl.item_chunk = reinterpret_cast<int32_t*>(ws + L.item_chunk);
+    pl.max_routed_reqs = (int)L.max_routed_reqs;
+    pl.max_items = (int)L.max_items;
+    pl.part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
+    pl.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+    pl.out = static_cast<uint16_t*>(attn->out);
+    pl.lse = attn->lse;
+    pl.status = dev_status;
+    e = launch_prefill_attn(pl, stream);
+    if (e != cudaSuccess) return MSA_ERR_CUDA;
+  }
+
   AttnLaunch ap = make_attn(attn, tbl, tstride, len, reinterpret_cast<float*>(ws + L.partials),
                             counters, pps, splits, dev_status);
+  ap.route = route;  // rows of the prefill path leave at once
   // the attention split depends only on the selected width (8*topk entries)
   e = launch_sparse_attn(ap, stream, true);
   if (e != cudaSuccess) return MSA_ERR_CUDA;

@@ -25,7 +25,7 @@
 //           max, score store; releases the accumulator.
 // Every wait is bounded; on expiry the kernel records MSA_DEV_TIMEOUT, stops
 // issuing work and still frees its TMEM.
-#include "msa_internal.cuh"
+#include "tcgen05.cuh"
 
 namespace msa {
 namespace {
@@ -51,79 +51,13 @@ struct TcCfg {
   static size_t bytes(int num_reqs) { return 1024 + kPrefix + (size_t)(num_reqs + 1) * 4; }
 };
 
-// ------------------------------------------------------------ tcgen05 PTX
+using tc::commit;
+using tc::fence_after;
+using tc::fence_before;
+using tc::tmem_ld32;
 
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(dst)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
-// 8-row core groups 1024 B apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
-  d |= (uint64_t)1 << 16;                    // leading byte offset (unused when swizzled)
-  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
-  d |= (uint64_t)1 << 46;                    // descriptor version
-  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both
-// K-major, N = 128, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
-                            ((128u >> 4) << 24);
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
+// Instruction descriptor of the score tile: M = 128 rows, N = 128 tokens.
+constexpr uint32_t kIdesc = tc::idesc_bf16(128, 128, 0);
 
 // ------------------------------------------------------------ work cursor
 
@@ -230,7 +164,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     prefix[q + 1] = items;
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
   __syncthreads();
   const bool batch_ok = misc[0] == 0;  // the CUDA-core kernel reports the status bits
   if (batch_ok && warp == 0) {
@@ -248,9 +182,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
   }
-  tc_fence_before();
+  fence_before();
   __syncthreads();
-  tc_fence_after();
+  fence_after();
   const uint32_t tmem = *tmem_slot;
   const long long total = batch_ok ? prefix[R] : 0;
   const int i0 = (int)(total * blockIdx.x / gridDim.x);
@@ -344,22 +278,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           misc[1] = 1;
           break;
         }
-        tc_fence_after();
+        fence_after();
         if (stage_valid[s]) {
           const uint32_t a_base = smem_u32(smem + C::kA);
           const uint32_t b_base = smem_u32(smem + C::kB + s * C::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < C::kKSteps; ++kk) {
             const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-            umma_bf16(tmem + buf * 128, sw128_desc(a_base + off), sw128_desc(b_base + off),
-                      kk > 0 ? 1u : 0u);
+            tc::mma_ss(tmem + buf * 128, tc::desc_kmajor_sw128(a_base + off),
+                       tc::desc_kmajor_sw128(b_base + off), kIdesc, kk > 0 ? 1u : 0u);
           }
         }
-        umma_commit(&b_empty[s]);
-        umma_commit(&acc_full[buf]);
+        commit(&b_empty[s]);
+        commit(&acc_full[buf]);
         Cursor nx = cur;
         nx.next(b, prefix, R);
-        if (j == n_items - 1 || nx.q != cur.q || nx.tile != cur.tile) umma_commit(a_empty);
+        if (j == n_items - 1 || nx.q != cur.q || nx.tile != cur.tile) commit(a_empty);
         cur = nx;
       }
     } else if (warp >= 2) {
@@ -374,7 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           misc[1] = 1;
           break;
         }
-        tc_fence_after();
+        fence_after();
         const int m = quarter * 32 + lane;
         const int row_in_req = cur.tile * kTileRows + m;
         const int pos = cur.ctx + row_in_req;
@@ -393,19 +327,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (row_in_req < cur.qlen && last >= 0)
           p.scores[(long long)(cur.q0 + row_in_req) * p.score_stride + cur.blk] =
               page_ok ? best : -INFINITY;
-        tc_fence_before();
+        fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
         cur.next(b, prefix, R);
       }
     }
   }
-  tc_fence_before();
+  fence_before();
   __syncthreads();
   if (misc[1] && tid == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
   if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
   }
 }
 

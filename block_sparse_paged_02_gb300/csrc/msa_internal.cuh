@@ -22,6 +22,10 @@ constexpr int kMaxReqs = 4096;
 constexpr int kMaxBlocksPerRow = 16384;
 // requests with at least this many query rows are scored on the tensor cores
 constexpr int kTcMinRows = 64;
+// ... and, in the fused decode with bf16 KV, attend on the tensor cores too
+// (block-major prefill attention); list entries pack a row and a slot < 256
+constexpr int kPrefillMinRows = 64;
+constexpr int kPrefillMaxTopk = 128;
 constexpr int kMaxTopk = 2048;
 // at most this many page-16 entries per attention split (<= 32 per warp)
 constexpr int kMaxSplitEntries = 128;
@@ -298,6 +302,16 @@ struct TopkLaunch {
   int32_t* sparse_len;
   uint32_t* attn_counters;  // zeroed per row when non-null (fused path)
   uint32_t* status;
+  // Prefill routing (fused path only; null pointers when off).  Rows of
+  // requests with at least kPrefillMinRows rows get route[r] = q + 1 (others
+  // 0), and each selected (row, slot i, block b) is appended as r << 8 | i to
+  // the request's list of block b: pf_counts[q0 * bt_stride / 64 + b] counts
+  // the entries of pf_lists[q0 * bt_stride + b * q_len ...] (q0 = the
+  // request's first row).  The counts start at zero (msa_decode clears them
+  // on the stream before the top-k kernel).
+  int32_t* route;
+  int32_t* pf_counts;
+  int32_t* pf_lists;
 };
 
 struct AttnLaunch {
@@ -322,6 +336,7 @@ struct AttnLaunch {
   int splits;
   int pages_per_split;  // page-16 entries per split
   uint32_t* status;
+  const int32_t* route;  // fused path: rows with route[r] != 0 belong to the prefill path
 };
 
 cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream);
@@ -372,6 +387,45 @@ struct MlaLaunch {
 };
 
 cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream);
+
+// Block-major attention for the rows of prefill requests (fused decode,
+// bf16 KV, no per-token scales): plan -> attention -> merge.  Uses the lists
+// the top-k kernel appended (see TopkLaunch) and scratch in the workspace.
+struct PrefillLaunch {
+  msa_batch batch;
+  const uint16_t* q;      // [N, hq, 128] bf16
+  int num_heads;
+  const uint16_t* k;      // K / V pools [P, 128, 1, 128] bf16
+  const uint16_t* v;
+  const float* k_scale;   // SCALAR mode: fp32 [1] each, else null
+  const float* v_scale;
+  const float* sinks;
+  float softmax_scale;
+  int topk;
+  const int32_t* topk_idx;  // [N, topk]
+  const int32_t* route;     // [N]
+  const int32_t* pf_counts; // list counts (msa_decode clears them before the top-k)
+  const int32_t* pf_lists;
+  // plan: header [0] = items, [1] = chunks; routed requests (q, first item);
+  // items (request, block, rows, first chunk)
+  int32_t* plan_hdr;
+  int32_t* plan_req_q;
+  int32_t* plan_req_item;
+  int32_t* item_q;
+  int32_t* item_b;
+  int32_t* item_cnt;
+  int32_t* item_chunk;
+  int max_routed_reqs;      // capacity of plan_req_*
+  int max_items;            // capacity of item_*
+  uint16_t* part_o;         // [N, topk, 16, 128] bf16, each O / l
+  float* part_lse;          // [N, topk, 16] log2 units
+  uint16_t* out;            // [N, hq, 128] bf16
+  float* lse;               // [N, hq]
+  uint32_t* status;
+};
+
+cudaError_t launch_prefill_attn(const PrefillLaunch& p, cudaStream_t stream);
+bool prefill_attn_available();
 int mla_max_tokens_per_split();
 
 // `programmatic`: the kernel may start while the previous kernel on the

@@ -1,0 +1,628 @@
+// prefill_attn.cu -- step 4 for the rows of prefill requests (a chunk of new
+// tokens, every token a query row with its own causal top-k), block-major on
+// the 5th-generation tensor cores.
+//
+// Definitions as in sparse_attn.cu: "Add ROCm AITER sparse paged attention
+// for MiniMax-M3" (vLLM PR 47287), "Implementation breakdown" items 2-3 (a
+// separate prefill attention path over the same page-16 sparse selection,
+// k_scale / v_scale) and "Attention sinks for ROCm AITER sparse MLA" (vLLM PR
+// 54404), "Features and motivation" / "Key source snippets" (sinks in the
+// denominator, natural-log LSE, empty rows without NaN).
+//
+// Why block-major.  Each row of a prefill request picks its own k blocks;
+// with independent index queries two rows share few of them (8 consecutive
+// rows of the 2 x 2048-token chunk select ~102 distinct blocks out of 128
+// picks), so a tile of rows against the union of their blocks would waste
+// most of its MMA work, while a row-at-a-time kernel re-reads every block
+// from L2 once per row and stalls on shared-memory operand reads.  Turned
+// around, every block of a request is picked by ~k * q_len / nb rows (~130
+// here).  So the top-k kernel appends each (row, slot) to its block's list;
+// this file then
+//   plan:      one CTA compacts the non-empty (request, block) lists into
+//              items of 8-row chunks with a chunk prefix;
+//   attention: a persistent CTA per SM takes an equal range of chunks; per
+//              item it loads the block's K and V once (two 32 KB tensor
+//              copies, 128-byte swizzle), per chunk it gathers the 8 rows'
+//              queries (16 head slots each: M = 128) and computes
+//                S = Q K^T     tcgen05.mma M128 N128 K128, fp32 in TMEM
+//                P = exp2(S' - max)  per TMEM lane (= row, head), written
+//                              back into TMEM as bf16 over S
+//                O = P V       tcgen05.mma with A = P from TMEM, B = V
+//                              (MN-major), fp32 in TMEM
+//              and stores the chunk's per-(row, slot) partial O / l (bf16)
+//              and log2-sum-exp;
+//   merge:     per row, the k partials are combined through their LSEs,
+//              the sink joins the denominator, O and the natural-log LSE
+//              are written.
+// CTA roles in the attention kernel: warp 0 issues the tensor copies (all
+// lanes gather query rows), warp 1 allocates TMEM and one of its threads
+// issues the MMAs, warps 2-5 and 6-9 are two softmax / epilogue groups that
+// take alternate chunks (S, P and O are double-buffered in TMEM: 512
+// columns).  Every wait is bounded; on expiry the kernel records
+// MSA_DEV_TIMEOUT, stops and still frees its TMEM.
+#include <string.h>
+
+#include "tcgen05.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kChunkRows = 8;  // query rows per chunk (x 16 head slots = the MMA's M = 128)
+constexpr int kHeadSlots = 16;
+constexpr int kPaThreads = 320;
+constexpr int kQStages = 3;
+constexpr int kKvStages = 2;
+constexpr int kHalf = 128 * 128;     // 128 rows x 128 B: one swizzle-atom column of a tile
+constexpr int kTile = 2 * kHalf;     // a 128 x 128 bf16 tile
+constexpr int kSmK = 0;
+constexpr int kSmV = kSmK + kKvStages * kTile;
+constexpr int kSmQ = kSmV + kKvStages * kTile;
+constexpr int kSmBars = kSmQ + kQStages * kTile;
+// kv_full[2] kv_empty[2] q_full[3] q_empty[3] s_full[2] p_full[2] o_full[2] o_empty[2] kv_fill
+constexpr int kNumBars = 2 * kKvStages + 2 * kQStages + 8 + 1;
+constexpr int kSmMisc = kSmBars + kNumBars * 8;
+constexpr int kPaSmem = kSmMisc + 64 + 1024;  // + slack for the 1024-byte alignment
+constexpr uint32_t kTmemCols = 512;           // S[2] at 0 / 128, O[2] at 256 / 384
+constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, 0);
+constexpr uint32_t kIdescO = tc::idesc_bf16(128, 128, 1);
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kPlanThreads = 1024;
+constexpr int kMergeThreads = 128;
+
+// ------------------------------------------------------------------ plan
+
+// Exclusive scan over the CTA; *total gets the sum.  scratch: 33 ints.
+__device__ __forceinline__ int cta_excl_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const int t = lane < nw ? scratch[lane] : 0;
+    int y = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += n;
+    }
+    if (lane < nw) scratch[lane] = y - t;
+    if (lane == 31) scratch[32] = y;
+  }
+  __syncthreads();
+  const int before = scratch[warp];
+  *total = scratch[32];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PrefillLaunch p) {
+  __shared__ int scratch[33];
+  __shared__ int s_ok;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const msa_batch& b = p.batch;
+  const int R = b.num_reqs, tid = threadIdx.x;
+  const long long bt = b.bt_stride;
+
+  // ---- routed requests (geometry only): q_len >= kPrefillMinRows and sane
+  if (tid == 0) s_ok = b.cu_seqlens_q[0] == 0 && b.cu_seqlens_q[R] == b.num_rows;
+  bool mono = true;
+  for (int q = tid; q < R; q += kPlanThreads) mono &= b.cu_seqlens_q[q + 1] >= b.cu_seqlens_q[q];
+  if (!__syncthreads_and(mono)) s_ok = 0;
+  __syncthreads();
+  const bool ok = s_ok != 0;
+  int n_req = 0, n_cand = 0;
+  for (int base = 0; ok && base < R; base += kPlanThreads) {
+    const int q = base + tid;
+    int nb = 0, q0 = 0, ql = 0, ctx = 0;
+    const bool routed_q =
+        q < R && request_lengths(b, q, &q0, &ql, &ctx, &nb) == 0 && ql >= kPrefillMinRows;
+    if (!routed_q) nb = 0;
+    const int routed = nb > 0;
+    int t_req, t_cand;
+    const int at = n_req + cta_excl_scan(routed, scratch, &t_req);
+    const int cand = n_cand + cta_excl_scan(nb, scratch, &t_cand);
+    if (routed && at < p.max_routed_reqs) {
+      p.plan_req_q[at] = q;
+      p.plan_req_item[at] = cand;  // first candidate (request, block) of q
+    }
+    n_req += t_req;
+    n_cand += t_cand;
+  }
+  if (n_req > p.max_routed_reqs || n_cand > p.max_items) {  // cannot happen by construction
+    n_req = 0;
+    n_cand = 0;
+  }
+  __syncthreads();  // the request list is visible to the whole CTA
+
+  // wait for the top-k kernel's lists
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ---- candidates (request, block) -> non-empty items with a chunk prefix
+  int n_items = 0, n_chunks = 0;
+  for (int base = 0; base < n_cand; base += kPlanThreads) {
+    const int c = base + tid;
+    int q = 0, blk = 0, cnt = 0;
+    long long cidx = 0;
+    if (c < n_cand) {
+      int lo = 0, hi = n_req;  // last routed request with first candidate <= c
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.plan_req_item[mid] <= c) lo = mid; else hi = mid;
+      }
+      q = p.plan_req_q[lo];
+      blk = c - p.plan_req_item[lo];
+      cidx = (long long)b.cu_seqlens_q[q] * bt / kPrefillMinRows + blk;
+      // a list never holds more entries than the request has rows
+      cnt = min(p.pf_counts[cidx], b.cu_seqlens_q[q + 1] - b.cu_seqlens_q[q]);
+    }
+    const int live = cnt > 0;
+    const int chunks = (cnt + kChunkRows - 1) / kChunkRows;
+    int t_items, t_chunks;
+    const int at = n_items + cta_excl_scan(live, scratch, &t_items);
+    const int first = n_chunks + cta_excl_scan(chunks, scratch, &t_chunks);
+    if (live) {
+      p.item_q[at] = q;
+      p.item_b[at] = blk;
+      p.item_cnt[at] = cnt;
+      p.item_chunk[at] = first;
+    }
+    n_items += t_items;
+    n_chunks += t_chunks;
+  }
+  if (tid == 0) {
+    p.plan_hdr[0] = n_items;
+    p.plan_hdr[1] = n_chunks;
+  }
+}
+
+// --------------------------------------------------------------- attention
+
+// Walks the chunks of the plan in order: item `it`, chunk `ci` of it.
+struct Cursor {
+  int it, ci, n_items;
+  int q, blk, cnt, q0, qlen, ctx, seq;
+
+  __device__ void load(const PrefillLaunch& p) {
+    q = p.item_q[it];
+    blk = p.item_b[it];
+    cnt = p.item_cnt[it];
+    q0 = p.batch.cu_seqlens_q[q];
+    qlen = p.batch.cu_seqlens_q[q + 1] - q0;
+    ctx = p.batch.context_lens[q];
+    seq = ctx + qlen;
+  }
+  __device__ void seek(const PrefillLaunch& p, int chunk) {
+    int lo = 0, hi = n_items;  // last item whose first chunk <= chunk (items are non-empty)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.item_chunk[mid] <= chunk) lo = mid; else hi = mid;
+    }
+    it = lo;
+    load(p);
+    ci = chunk - p.item_chunk[it];
+  }
+  __device__ void next(const PrefillLaunch& p) {
+    if (kChunkRows * (++ci) < cnt) return;
+    ci = 0;
+    if (++it < n_items) load(p);
+  }
+  __device__ int rows() const { return min(kChunkRows, cnt - kChunkRows * ci); }
+  __device__ long long list_base(const PrefillLaunch& p) const {
+    return (long long)q0 * p.batch.bt_stride + (long long)blk * qlen + kChunkRows * ci;
+  }
+  // tokens of the block that exist (the request's last block may be partial)
+  __device__ int block_tokens() const { return min(kBlock, seq - kBlock * blk); }
+};
+
+// all lanes wait; the result is the same on every lane
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
+}
+
+template <bool SCALAR>
+__global__ void __launch_bounds__(kPaThreads, 1)
+    prefill_attn_kernel(const PrefillLaunch p, const __grid_constant__ CUtensorMap qmap,
+                        const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmBars);
+  uint64_t* kv_full = bars;
+  uint64_t* kv_empty = kv_full + kKvStages;
+  uint64_t* q_full = kv_empty + kKvStages;
+  uint64_t* q_empty = q_full + kQStages;
+  uint64_t* s_full = q_empty + kQStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_full = p_full + 2;
+  uint64_t* o_empty = o_full + 2;
+  uint64_t* kv_fill = o_empty + 2;
+  int* misc = reinterpret_cast<int*>(smem + kSmMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 4);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int hq = p.num_heads;
+
+  if (tid == 0) {
+    misc[1] = 0;  // timeout seen
+    for (int s = 0; s < kKvStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 4);  // the four warps of a softmax group
+      mbar_init(&o_full[s], 1);
+      mbar_init(&o_empty[s], 4);
+    }
+    mbar_init(kv_fill, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the plan (and the top-k lists)
+
+  const int n_items = p.plan_hdr[0];
+  const long long total = p.plan_hdr[1];
+  const int c0 = (int)(total * blockIdx.x / gridDim.x);
+  const int c1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+  const int nj = c1 - c0;
+
+  if (nj > 0) {
+    if (warp == 0) {
+      // ---------------- copies: K / V once per item, the chunk's query rows
+      Cursor cur;
+      cur.n_items = n_items;
+      cur.seek(p, c0);
+      int e_cur = lane < cur.rows() ? p.pf_lists[cur.list_base(p) + lane] : 0;
+      int kv_seq = 0, fills = 0;
+      for (int j = 0; j < nj; ++j) {
+        Cursor nxt = cur;
+        int e_nxt = 0;
+        if (j + 1 < nj) {  // the next chunk's list entries, in flight during this one
+          nxt.next(p);
+          e_nxt = lane < nxt.rows() ? p.pf_lists[nxt.list_base(p) + lane] : 0;
+        }
+        if (j == 0 || cur.ci == 0) {
+          const int kvs = kv_seq & 1;
+          if (kv_seq >= 2 && !warp_wait(&kv_empty[kvs], ((kv_seq >> 1) - 1) & 1)) {
+            misc[1] = 1;
+            break;
+          }
+          const int page =
+              p.batch.block_table[(long long)cur.q * p.batch.bt_stride + cur.blk];
+          const int ntok = cur.block_tokens();
+          // a partial last block: the tokens past the request's end are not
+          // data (never written); they are zeroed before P V reads them
+          uint64_t* land = ntok < kBlock ? kv_fill : &kv_full[kvs];
+          if (lane == 0) {
+            mbar_arrive_expect_tx(land, 2 * kTile);
+            uint8_t* kd = smem + kSmK + kvs * kTile;
+            uint8_t* vd = smem + kSmV + kvs * kTile;
+            for (int h = 0; h < 2; ++h) {
+              tma_load_2d(kd + h * kHalf, &kmap, 64 * h, page * kBlock, land);
+              tma_load_2d(vd + h * kHalf, &vmap, 64 * h, page * kBlock, land);
+            }
+          }
+          if (ntok < kBlock) {
+            if (!warp_wait(kv_fill, fills & 1)) {
+              misc[1] = 1;
+              break;
+            }
+            ++fills;
+            uint4* vd = reinterpret_cast<uint4*>(smem + kSmV + kvs * kTile);
+            // rows ntok..127 of both halves (each row 128 B; the swizzle
+            // only permutes 16-byte chunks inside a row)
+            for (int i = ntok * 8 + lane; i < kBlock * 8; i += 32) {
+              vd[i] = make_uint4(0u, 0u, 0u, 0u);
+              vd[kHalf / 16 + i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // generic writes before the MMA's async reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&kv_full[kvs]);
+          }
+          ++kv_seq;
+        }
+        const int qs = j % kQStages;
+        if (j >= kQStages && !warp_wait(&q_empty[qs], ((j / kQStages) - 1) & 1)) {
+          misc[1] = 1;
+          break;
+        }
+        const int n = cur.rows();
+        if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], (uint32_t)(n * hq * 256));
+        __syncwarp();
+        if (lane < n) {
+          // (an entry outside the request, impossible from the top-k kernel,
+          // is read from the request's first row and never written back)
+          const int er = e_cur >> 8;
+          const int r = (er >= cur.q0 && er < cur.q0 + cur.qlen) ? er : cur.q0;
+          uint8_t* qd = smem + kSmQ + qs * kTile + lane * (kHeadSlots * 128);
+          tma_load_2d(qd, &qmap, 0, r * hq, &q_full[qs]);
+          tma_load_2d(qd + kHalf, &qmap, 64, r * hq, &q_full[qs]);
+        }
+        cur = nxt;
+        e_cur = e_nxt;
+      }
+    } else if (warp == 1) {
+      // ---------------- MMA issue (one thread)
+      if (lane == 0) {
+        Cursor cur;
+        cur.n_items = n_items;
+        cur.seek(p, c0);
+        int kv_seq = 0, cur_kvs = 0, prev_kvs = 0;
+        bool prev_last = false;
+        for (int j = 0; j <= nj; ++j) {
+          bool last = false;
+          if (j < nj) {
+            const int buf = j & 1, qs = j % kQStages;
+            if (j == 0 || cur.ci == 0) {
+              cur_kvs = kv_seq & 1;
+              if (!mbar_wait(&kv_full[cur_kvs], (kv_seq >> 1) & 1)) {
+                misc[1] = 1;
+                break;
+              }
+              ++kv_seq;
+            }
+            if (!mbar_wait(&q_full[qs], (j / kQStages) & 1) ||
+                (j >= 2 && !mbar_wait(&o_empty[buf], ((j >> 1) - 1) & 1))) {
+              misc[1] = 1;
+              break;
+            }
+            tc::fence_after();
+            const uint32_t qa = smem_u32(smem + kSmQ + qs * kTile);
+            const uint32_t ka = smem_u32(smem + kSmK + cur_kvs * kTile);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+              tc::mma_ss(tmem + buf * 128, tc::desc_kmajor_sw128(qa + off),
+                         tc::desc_kmajor_sw128(ka + off), kIdescS, kk > 0 ? 1u : 0u);
+            }
+            tc::commit(&q_empty[qs]);
+            tc::commit(&s_full[buf]);
+            Cursor nx = cur;
+            nx.next(p);
+            last = j == nj - 1 || nx.ci == 0;
+            cur = nx;
+          }
+          if (j >= 1) {  // O = P V of the previous chunk
+            const int i = j - 1, pb = i & 1;
+            if (!mbar_wait(&p_full[pb], (i >> 1) & 1)) {
+              misc[1] = 1;
+              break;
+            }
+            tc::fence_after();
+            const uint32_t va = smem_u32(smem + kSmV + prev_kvs * kTile);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tc::mma_ts(tmem + 256 + pb * 128, tmem + pb * 128 + kk * 8,
+                         tc::desc_mnmajor_sw128(va + kk * 2048, kHalf), kIdescO,
+                         kk > 0 ? 1u : 0u);
+            tc::commit(&o_full[pb]);
+            if (prev_last) tc::commit(&kv_empty[prev_kvs]);
+          }
+          prev_kvs = cur_kvs;
+          prev_last = last;
+        }
+      }
+    } else {
+      // ---------------- softmax + epilogue, chunks j = grp, grp + 2, ...
+      const int grp = (warp - 2) >> 2, quarter = warp & 3;
+      const int m = quarter * 32 + lane, slot = m >> 4, head = m & 15;
+      const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+      float scale2 = p.softmax_scale * kLog2e;
+      if constexpr (SCALAR) scale2 *= __ldg(p.k_scale);
+      Cursor cur;
+      cur.n_items = n_items;
+      cur.seek(p, c0);
+      if (grp == 1 && nj > 1) cur.next(p);
+      int e = (slot < cur.rows()) ? p.pf_lists[cur.list_base(p) + slot] : 0;
+      for (int j = grp; j < nj; j += 2) {
+        const int buf = j & 1;
+        const int r = e >> 8, si = e & 255;
+        const bool live = slot < cur.rows() && head < hq && r >= cur.q0 &&
+                          r < cur.q0 + cur.qlen && si < p.topk;
+        const int pos = cur.ctx + (r - cur.q0);
+        const int valid = live ? min(kBlock, pos + 1 - kBlock * cur.blk) : 0;
+        if (!warp_wait(&s_full[buf], (j >> 1) & 1)) {
+          misc[1] = 1;
+          break;
+        }
+        tc::fence_after();
+        const uint32_t sa = tmem + lanes + buf * 128;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tc::tmem_ld32(sa + 32 * c, v);
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (32 * c + t < valid) mx = fmaxf(mx, v[t] * scale2);
+        }
+        if (!live) mx = 0.f;
+        float l = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tc::tmem_ld32(sa + 32 * c, v);  // P overwrites S columns already consumed
+          uint32_t w[16];
+#pragma unroll
+          for (int t = 0; t < 32; t += 2) {
+            const float p0 = 32 * c + t < valid ? exp2f(fmaf(v[t], scale2, -mx)) : 0.f;
+            const float p1 = 32 * c + t + 1 < valid ? exp2f(fmaf(v[t + 1], scale2, -mx)) : 0.f;
+            l += p0 + p1;
+            w[t >> 1] = pack_bf16x2(p0, p1);
+          }
+          tc::tmem_st16(sa + 16 * c, w);
+        }
+        tc::tmem_wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[buf]);
+        // the next chunk of this group: its list entry is in flight during the epilogue
+        Cursor nx = cur;
+        int e_nx = 0;
+        if (j + 2 < nj) {
+          nx.next(p);
+          nx.next(p);
+          e_nx = (slot < nx.rows()) ? p.pf_lists[nx.list_base(p) + slot] : 0;
+        }
+        if (!warp_wait(&o_full[buf], (j >> 1) & 1)) {
+          misc[1] = 1;
+          break;
+        }
+        tc::fence_after();
+        const float inv = (live && l > 0.f) ? 1.f / l : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.part_o + (((long long)r * p.topk + si) * kHeadSlots + head) * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tc::tmem_ld32(tmem + lanes + 256 + buf * 128 + 32 * c, v);
+          if (live) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              dst[4 * c + x] = make_uint4(
+                  pack_bf16x2(v[8 * x] * inv, v[8 * x + 1] * inv),
+                  pack_bf16x2(v[8 * x + 2] * inv, v[8 * x + 3] * inv),
+                  pack_bf16x2(v[8 * x + 4] * inv, v[8 * x + 5] * inv),
+                  pack_bf16x2(v[8 * x + 6] * inv, v[8 * x + 7] * inv));
+          }
+        }
+        if (live)
+          p.part_lse[((long long)r * p.topk + si) * kHeadSlots + head] = mx + log2f(l);
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_empty[buf]);
+        cur = nx;
+        e = e_nx;
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (misc[1] && tid == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ merge
+
+// One CTA per row: thread t owns head t / 8, dims 16 (t % 8) .. +16.  Rows
+// not routed to the prefill path leave at once.
+template <bool SCALAR>
+__global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(const PrefillLaunch p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const int head = tid >> 3, d0 = 16 * (tid & 7);
+  float sink2 = -INFINITY, vs = 1.f;
+  if (p.sinks && head < p.num_heads) sink2 = __ldg(p.sinks + head) * kLog2e;
+  if constexpr (SCALAR) vs = __ldg(p.v_scale);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (p.route[r] == 0) return;
+  // the row's selections (ascending blocks, then -1; topk <= kMergeThreads):
+  // one partial per selected block
+  const bool has = tid < p.topk && p.topk_idx[(long long)r * p.topk + tid] >= 0;
+  const int nsel = __syncthreads_count(has);
+  if (head >= p.num_heads) return;
+  const long long pbase = (long long)r * p.topk;
+  float M = sink2;
+  for (int i = 0; i < nsel; ++i) M = fmaxf(M, p.part_lse[(pbase + i) * kHeadSlots + head]);
+  float L = p.sinks ? exp2f(sink2 - M) : 0.f;
+  float acc[16];
+#pragma unroll
+  for (int x = 0; x < 16; ++x) acc[x] = 0.f;
+  for (int i = 0; i < nsel; ++i) {
+    const float w = exp2f(p.part_lse[(pbase + i) * kHeadSlots + head] - M);
+    L += w;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.part_o + ((pbase + i) * kHeadSlots + head) * kHeadDim + d0);
+    const uint4 a = src[0], b2 = src[1];
+    const uint32_t u[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      acc[2 * x] += w * bf16lo(u[x]);
+      acc[2 * x + 1] += w * bf16hi(u[x]);
+    }
+  }
+  const float inv = L > 0.f ? vs / L : 0.f;
+  uint32_t packed[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) packed[x] = pack_bf16x2(acc[2 * x] * inv, acc[2 * x + 1] * inv);
+  uint4* o = reinterpret_cast<uint4*>(p.out + ((long long)r * p.num_heads + head) * kHeadDim + d0);
+  o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  if ((tid & 7) == 0)
+    p.lse[(long long)r * p.num_heads + head] =
+        (M == -INFINITY || L <= 0.f) ? -INFINITY : (M + log2f(L)) * kLn2;
+}
+
+cudaError_t launch_pdl(const void* kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
+template <bool SCALAR>
+cudaError_t launch_all(const PrefillLaunch& p, cudaStream_t stream) {
+  CUtensorMap qmap, kmap, vmap;
+  memset(&qmap, 0, sizeof(qmap));
+  if (!encode_map_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, kHeadDim,
+                     (long long)p.batch.num_rows * p.num_heads, kHeadDim * 2, 64, p.num_heads) ||
+      !encode_map_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, kHeadDim,
+                     (long long)p.batch.num_pages * kBlock, kHeadDim * 2, 64, kBlock) ||
+      !encode_map_2d(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, kHeadDim,
+                     (long long)p.batch.num_pages * kBlock, kHeadDim * 2, 64, kBlock))
+    return cudaErrorInvalidValue;
+  PrefillLaunch pp = p;
+  void* plan_args[] = {&pp};
+  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(prefill_plan_kernel), dim3(1),
+                             dim3(kPlanThreads), 0, stream, plan_args);
+  if (e != cudaSuccess) return e;
+  auto attn = prefill_attn_kernel<SCALAR>;
+  e = cudaFuncSetAttribute(attn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPaSmem);
+  if (e != cudaSuccess) return e;
+  void* attn_args[] = {&pp, &qmap, &kmap, &vmap};
+  e = launch_pdl(reinterpret_cast<const void*>(attn), dim3(device_sm_count()), dim3(kPaThreads),
+                 kPaSmem, stream, attn_args);
+  if (e != cudaSuccess) return e;
+  void* merge_args[] = {&pp};
+  return launch_pdl(reinterpret_cast<const void*>(prefill_merge_kernel<SCALAR>),
+                    dim3(p.batch.num_rows), dim3(kMergeThreads), 0, stream, merge_args);
+}
+
+}  // namespace
+
+bool prefill_attn_available() { return tensor_maps_available(); }
+
+cudaError_t launch_prefill_attn(const PrefillLaunch& p, cudaStream_t stream) {
+  if (p.batch.num_rows == 0 || p.batch.num_reqs == 0) return cudaSuccess;
+  if (p.k_scale) return launch_all<true>(p, stream);
+  return launch_all<false>(p, stream);
+}
+
+}  // namespace msa

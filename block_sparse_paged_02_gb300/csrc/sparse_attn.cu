@@ -167,6 +167,13 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
     sink_s[kMaxHeads] = SCALE == MSA_SCALE_SCALAR ? __ldg(p.v_scale) : 1.f;
   // sparse tables and lengths come from the previous kernel on the stream
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (p.route && p.route[r] != 0) {
+    // a row of a prefill request: the block-major prefill attention writes
+    // it (uniform over the CTA and over the row's cluster); drain the query
+    // copy this CTA issued before leaving
+    if (tid == 0 && !mbar_wait(qbar, 0)) atomicOr(p.status, MSA_DEV_TIMEOUT);
+    return;
+  }
 
   // this warp's page-16 entries are split*pps + warp + 4*i, one per lane; the
   // table load does not depend on the length, so both are in flight together

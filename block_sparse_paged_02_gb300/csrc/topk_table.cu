@@ -77,6 +77,17 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
   return before + x - v;
 }
 
+// Fused decode with a prefill path: the row's selected block `blk` (its
+// slot-th selection) joins the request's list for that block (see
+// TopkLaunch).  A block is selected at most once per row, so a list never
+// holds more than q_len entries.
+__device__ __forceinline__ void prefill_append(const TopkLaunch& p, int q0, int qlen, int r,
+                                               int slot, int blk) {
+  const long long bt = p.batch.bt_stride;
+  const int pos = atomicAdd(p.pf_counts + (long long)q0 * bt / kPrefillMinRows + blk, 1);
+  p.pf_lists[(long long)q0 * bt + (long long)blk * qlen + pos] = (r << 8) | slot;
+}
+
 template <int KPT, int THREADS, bool RADIX>
 __device__ __forceinline__ void topk_table_body(const TopkLaunch& p) {
   constexpr int kWarps = THREADS / 32;
@@ -156,6 +167,7 @@ __device__ __forceinline__ void topk_table_body(const TopkLaunch& p) {
     if (tid == 0) {
       p.sparse_len[r] = 0;
       if (p.attn_counters) p.attn_counters[r] = 0;
+      if (p.route) p.route[r] = 0;  // an empty row, left to the decode attention
     }
     return;
   }
@@ -293,6 +305,12 @@ __device__ __forceinline__ void topk_table_body(const TopkLaunch& p) {
     p.sparse_len[r] = m > 0 ? kBlock * (m - 1) + min(kBlock, L - kBlock * sel[m - 1]) : 0;
     if (p.attn_counters) p.attn_counters[r] = 0;
   }
+  if (p.route) {
+    const bool routed = qlen >= kPrefillMinRows;
+    if (tid == 0) p.route[r] = routed ? q + 1 : 0;
+    if (routed)
+      for (int i = tid; i < m; i += THREADS) prefill_append(p, q0, qlen, r, i, sel[i]);
+  }
 }
 
 // One key per thread, radix select (few long rows): at most 40
@@ -390,6 +408,7 @@ __global__ void __launch_bounds__(kWarpRows * 32) topk_table_kernel_warp(const T
     if (lane == 0) {
       p.sparse_len[r] = 0;
       if (p.attn_counters) p.attn_counters[r] = 0;
+      if (p.route) p.route[r] = 0;  // an empty row, left to the decode attention
     }
     return;
   }
@@ -475,6 +494,12 @@ __global__ void __launch_bounds__(kWarpRows * 32) topk_table_kernel_warp(const T
     // the highest selected block when selected
     p.sparse_len[r] = m > 0 ? kBlock * (m - 1) + min(kBlock, L - kBlock * sel[m - 1]) : 0;
     if (p.attn_counters) p.attn_counters[r] = 0;
+  }
+  if (p.route) {
+    const bool routed = qlen >= kPrefillMinRows;
+    if (lane == 0) p.route[r] = routed ? q + 1 : 0;
+    if (routed)
+      for (int i = lane; i < m; i += 32) prefill_append(p, q0, qlen, r, i, sel[i]);
   }
 }
 

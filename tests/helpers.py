@@ -40,3 +40,27 @@ def valid_score_mask(geom, score_stride):
 # A batch holding only the given rows (each its own one-row request at the
 # same position over the same pages); see workloads.row_subset.
 sub_workload = W.row_subset
+
+
+# Rows msa_decode sends through the block-major prefill attention (requests
+# of >= 64 rows, bf16 KV without per-token scales, top-k <= 128): the fused
+# call's attention there differs from the stand-alone attention entry point
+# in rounding only, so those rows are checked against the oracle instead of
+# bit for bit against the separate calls.
+PREFILL_MIN_ROWS = 64
+PREFILL_MAX_TOPK = 128
+
+
+def prefill_rows(w, topk=None):
+    k = int(topk or w.topk)
+    mask = np.zeros(w.num_rows, bool)
+    if w.kv_dtype != W.KV_BF16 or w.scale_mode == W.SCALE_PER_TOKEN_HEAD or k > PREFILL_MAX_TOPK:
+        return mask
+    q_lens = np.diff(np.asarray(w.cu_seqlens_q, np.int64))
+    if q_lens.size == 0 or q_lens.max() < PREFILL_MIN_ROWS:
+        return mask
+    for q, ql in enumerate(q_lens):
+        if ql >= PREFILL_MIN_ROWS:
+            mask[int(w.cu_seqlens_q[q]): int(w.cu_seqlens_q[q + 1])] = True
+    return mask
+

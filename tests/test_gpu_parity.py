@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import workloads as W
-from tests.helpers import assert_attn_close, sub_workload, valid_score_mask
+from tests.helpers import assert_attn_close, prefill_rows, sub_workload, valid_score_mask
 
 pytestmark = pytest.mark.gpu
 
@@ -56,10 +56,24 @@ def check_against_oracle(orc, w, sep, fused, topk=None):
     assert np.all(sep["tbl"][:, 8 * k:] == 0)
     assert sep["status"] == ref["status"]
     assert_attn_close(sep["out"], sep["lse"], ref["out"], ref["lse"])
-    # the fused call is bit-identical to the separate calls
-    for key in ("topk_idx", "tbl", "sparse_len", "out", "lse"):
-        assert np.array_equal(fused[key], sep[key], equal_nan=True), f"fused {key} differs"
+    check_fused(w, sep, fused, ref, topk=k)
     return ref
+
+
+def check_fused(w, sep, fused, ref, topk=None):
+    """The fused call's tables equal the separate calls' bit for bit; so do
+    its outputs on rows of the split-K decode attention, while rows of the
+    prefill path are held to the oracle (ref: the oracle's decode, or None
+    to skip that check)."""
+    for key in ("topk_idx", "tbl", "sparse_len"):
+        assert np.array_equal(fused[key], sep[key]), f"fused {key} differs"
+    pre = prefill_rows(w, topk)
+    dec = ~pre
+    for key in ("out", "lse"):
+        assert np.array_equal(fused[key][dec], sep[key][dec], equal_nan=True), f"fused {key} differs"
+    if ref is not None and pre.any():
+        assert fused["status"] == ref["status"]
+        assert_attn_close(fused["out"][pre], fused["lse"][pre], ref["out"][pre], ref["lse"][pre])
 
 
 @pytest.mark.parametrize("name", ["tiny_decode", "batched_decode", "speculative_decode",
@@ -73,8 +87,8 @@ def test_named_workload_full_size(msa, orc, name):
 def test_chunked_prefill_full_size_sampled_rows(msa, orc):
     w = W.chunked_prefill()
     _, sep, fused = run_steps(msa, w)
-    for key in ("topk_idx", "tbl", "sparse_len", "out", "lse"):
-        assert np.array_equal(fused[key], sep[key], equal_nan=True)
+    check_fused(w, sep, fused, None)
+    assert prefill_rows(w).all()  # every row takes the prefill path in the fused call
     rng = np.random.default_rng(0)
     # first/last rows of each request, rows around block boundaries, random rows
     rows = {0, 1, 127, 128, 2047, 2048, 2049, 4095}
@@ -88,6 +102,9 @@ def test_chunked_prefill_full_size_sampled_rows(msa, orc):
     assert np.array_equal(sep["sparse_len"][rows], ref["sparse_len"])
     nb = ref["tbl"].shape[1]
     assert_attn_close(sep["out"][rows], sep["lse"][rows], ref["out"], ref["lse"])
+    assert_attn_close(fused["out"][rows], fused["lse"][rows], ref["out"], ref["lse"])
+    assert fused["status"] == 0
+    assert np.all(np.isfinite(fused["out"])) and np.all(np.isfinite(fused["lse"]))
     # every row: the length is the clamp of the selected blocks, the table has
     # exactly ceil(len/16) leading non-empty slots per selected block pattern
     L = (w.context_lens[0] + np.arange(2048) + 1)
@@ -258,8 +275,71 @@ def test_many_rows_warp_topk(msa, orc, long_seq):
     assert sep["status"] == ref["status"] == msa.MSA_DEV_BAD_PAGE
     for key in ("topk_idx", "tbl", "sparse_len"):
         assert np.array_equal(sep[key], ref[key]), key
-        assert np.array_equal(fused[key], sep[key]), key
     assert_attn_close(sep["out"], sep["lse"], ref["out"], ref["lse"])
+    check_fused(w, sep, fused, ref)
+
+
+# ------------------------------------------------ block-major prefill path
+
+@pytest.mark.parametrize("hq,scale,sink", [(16, W.SCALE_NONE, False), (16, W.SCALE_SCALAR, True),
+                                           (8, W.SCALE_NONE, True), (12, W.SCALE_SCALAR, False)])
+def test_prefill_path_mixed_batch(msa, orc, hq, scale, sink):
+    # requests of 100 and 64 rows take the prefill attention in the fused
+    # call, those of 1, 3 and 63 rows the split-K decode attention; contexts
+    # end inside a block (partial last blocks) and on a block boundary
+    q_lens = [100, 1, 3, 64, 63, 130]
+    seq = [5000, 3000, 700, 64 + 256, 2000, 9000 + 77]
+    w = W.custom(63 + hq, q_lens=q_lens, seq_lens=seq, hq=hq, di=128, topk=8,
+                 kv_dtype=W.KV_BF16, scale_mode=scale, with_sink=sink)
+    assert prefill_rows(w).sum() == 100 + 64 + 130
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+def test_prefill_path_all_blocks_and_garbage(msa, orc):
+    # top-k covering every block (short contexts), a request of a single
+    # partial block, NaN in every slot past each request's end
+    w = W.custom(70, q_lens=[90, 70, 65], seq_lens=[700, 70, 1000], hq=16, di=128, topk=16,
+                 kv_dtype=W.KV_BF16, with_sink=True, fill_unused_nan=True)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+    assert np.all(np.isfinite(fused["out"])) and np.all(np.isfinite(fused["lse"]))
+
+
+def test_prefill_path_poisoned_request(msa, orc):
+    # a request of the prefill path with a page outside the pool: its rows
+    # are empty rows (O = 0, LSE = sink); the other requests are unaffected
+    w = W.custom(71, q_lens=[80, 120, 2], seq_lens=[3000, 4000, 900], hq=16, di=128, topk=8,
+                 kv_dtype=W.KV_BF16, with_sink=True)
+    bt = w.block_table.copy()
+    bt[0, 5] = w.num_pages + 3
+    w.block_table = bt
+    _, sep, fused = run_steps(msa, w)
+    ref = check_against_oracle(orc, w, sep, fused)
+    assert ref["status"] == msa.MSA_DEV_BAD_PAGE
+    assert np.all(fused["out"][:80] == 0)
+    np.testing.assert_allclose(fused["lse"][:80], np.tile(w.sinks, (80, 1)), atol=1e-6)
+
+
+def test_prefill_path_repeated_calls(msa):
+    # the list counters and plan are rebuilt on every call: the same inputs
+    # give bit-identical results call after call (and across a call with
+    # another batch shape on the same workspace in between)
+    w = W.chunked_prefill(seed=16, context=3000, new_tokens=500, reqs=3)
+    c = msa.DeviceCase(w)
+    c.decode()
+    a = c.fetch()
+    other = W.custom(72, q_lens=[200, 1], seq_lens=[900, 400], hq=16, di=128, topk=16)
+    c2 = msa.DeviceCase(other)
+    c2.workspace = c.workspace[: c2.workspace.numel()] if c.workspace.numel() >= c2.workspace.numel() \
+        else c2.workspace
+    c2.decode()
+    for _ in range(2):
+        c.decode()
+        b = c.fetch()
+        for key in ("topk_idx", "tbl", "sparse_len", "out", "lse"):
+            assert np.array_equal(a[key], b[key], equal_nan=True), key
+        assert b["status"] == 0
 
 
 def test_poisoned_requests_match_oracle(msa, orc):
