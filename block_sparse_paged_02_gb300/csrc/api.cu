@@ -62,8 +62,8 @@ struct DecodeWs {
   // prefill path (present when topk <= kPrefillMaxTopk): route [N], list
   // counts and lists, the plan, the per-(row, slot) partials
   bool prefill;
-  size_t route, pf_counts, pf_lists, plan_hdr, plan_req_q, plan_req_item, item_q, item_b,
-      item_cnt, item_chunk, part_o, part_lse;
+  size_t route, pf_counts, pf_lists, plan_hdr, plan_req_q, plan_req_item, item_rec, item_kv,
+      item_chunk, part_o, part_ml;
   long long max_routed_reqs, max_items;
   size_t total;
 };
@@ -96,12 +96,11 @@ DecodeWs decode_layout(int num_rows, int bt_stride, int topk, int splits) {
     w.plan_hdr = take(64);
     w.plan_req_q = take((size_t)w.max_routed_reqs * 4);
     w.plan_req_item = take((size_t)w.max_routed_reqs * 4);
-    w.item_q = take((size_t)w.max_items * 4);
-    w.item_b = take((size_t)w.max_items * 4);
-    w.item_cnt = take((size_t)w.max_items * 4);
+    w.item_rec = take((size_t)w.max_items * 16);
+    w.item_kv = take((size_t)w.max_items * 8);
     w.item_chunk = take((size_t)w.max_items * 4);
     w.part_o = take(n * (size_t)topk * 16 * kHeadDim * 2);
-    w.part_lse = take(n * (size_t)topk * 16 * 4);
+    w.part_ml = take(n * (size_t)topk * 16 * 8);
   }
   w.total = off;
   return w;
@@ -403,7 +402,9 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
   const bool prefill = L.prefill && batch->max_q_len >= kPrefillMinRows &&
                        attn->kv_dtype == MSA_KV_BF16 &&
                        attn->scale_mode != MSA_SCALE_PER_TOKEN_HEAD &&
-                       batch->num_rows < (1 << 23) && prefill_attn_available();
+                       batch->num_rows < (1 << 23) &&
+                       (long long)batch->num_rows * batch->bt_stride < (1ll << 31) &&
+                       prefill_attn_available();
   int32_t* route = prefill ? reinterpret_cast<int32_t*>(ws + L.route) : nullptr;
   int32_t* pf_counts = prefill ? reinterpret_cast<int32_t*>(ws + L.pf_counts) : nullptr;
   int32_t* pf_lists = prefill ? reinterpret_cast<int32_t*>(ws + L.pf_lists) : nullptr;
@@ -447,14 +448,13 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
     pl.plan_hdr = reinterpret_cast<int32_t*>(ws + L.plan_hdr);
     pl.plan_req_q = reinterpret_cast<int32_t*>(ws + L.plan_req_q);
     pl.plan_req_item = reinterpret_cast<int32_t*>(ws + L.plan_req_item);
-    pl.item_q = reinterpret_cast<int32_t*>(ws + L.item_q);
-    pl.item_b = reinterpret_cast<int32_t*>(ws + L.item_b);
-    pl.item_cnt = reinterpret_cast<int32_t*>(ws + L.item_cnt);
+    pl.item_rec = reinterpret_cast<int4*>(ws + L.item_rec);
+    pl.item_kv = reinterpret_cast<int2*>(ws + L.item_kv);
     pl.item_chunk = reinterpret_cast<int32_t*>(ws + L.item_chunk);
     pl.max_routed_reqs = (int)L.max_routed_reqs;
     pl.max_items = (int)L.max_items;
     pl.part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
-    pl.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+    pl.part_ml = reinterpret_cast<float2*>(ws + L.part_ml);
     pl.out = static_cast<uint16_t*>(attn->out);
     pl.lse = attn->lse;
     pl.status = dev_status;

@@ -406,19 +406,18 @@ struct PrefillLaunch {
   const int32_t* route;     // [N]
   const int32_t* pf_counts; // list counts (msa_decode clears them before the top-k)
   const int32_t* pf_lists;
-  // plan: header [0] = items, [1] = chunks; routed requests (q, first item);
-  // items (request, block, rows, first chunk)
+  // plan: header [0] = items, [1] = chunks; routed requests (q, first
+  // candidate); items and their first chunks
   int32_t* plan_hdr;
   int32_t* plan_req_q;
   int32_t* plan_req_item;
-  int32_t* item_q;
-  int32_t* item_b;
-  int32_t* item_cnt;
+  int4* item_rec;       // per item: list base, rows, position of row 0 (pos = r + z), block
+  int2* item_kv;        // per item: page, tokens of the block that exist
   int32_t* item_chunk;
   int max_routed_reqs;      // capacity of plan_req_*
   int max_items;            // capacity of item_*
-  uint16_t* part_o;         // [N, topk, 16, 128] bf16, each O / l
-  float* part_lse;          // [N, topk, 16] log2 units
+  uint16_t* part_o;         // [N, topk, 16 dim chunks, 16 heads, 8 dims] bf16, sum p v
+  float2* part_ml;          // [N, topk, 16] (max, sum of p), log2 units
   uint16_t* out;            // [N, hq, 128] bf16
   float* lse;               // [N, hq]
   uint32_t* status;

@@ -29,8 +29,8 @@
 //                              back into TMEM as bf16 over S
 //                O = P V       tcgen05.mma with A = P from TMEM, B = V
 //                              (MN-major), fp32 in TMEM
-//              and stores the chunk's per-(row, slot) partial O / l (bf16)
-//              and log2-sum-exp;
+//              and stores the chunk's per-(row, slot) partial: the sum of
+//              p v (bf16) and the max and sum of p;
 //   merge:     per row, the k partials are combined through their LSEs,
 //              the sink joins the denominator, O and the natural-log LSE
 //              are written.
@@ -167,9 +167,11 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Prefil
     const int at = n_items + cta_excl_scan(live, scratch, &t_items);
     const int first = n_chunks + cta_excl_scan(chunks, scratch, &t_chunks);
     if (live) {
-      p.item_q[at] = q;
-      p.item_b[at] = blk;
-      p.item_cnt[at] = cnt;
+      const int q0 = b.cu_seqlens_q[q], ql = b.cu_seqlens_q[q + 1] - q0;
+      const int ctx = b.context_lens[q];
+      p.item_rec[at] = make_int4((int)((long long)q0 * bt + (long long)blk * ql), cnt, ctx - q0, blk);
+      p.item_kv[at] = make_int2(b.block_table[(long long)q * bt + blk],
+                                min(kBlock, ctx + ql - kBlock * blk));
       p.item_chunk[at] = first;
     }
     n_items += t_items;
@@ -183,48 +185,172 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Prefil
 
 // --------------------------------------------------------------- attention
 
-// Walks the chunks of the plan in order: item `it`, chunk `ci` of it.
+// Walks the chunks of the plan in order: item `it`, chunk `ci` of it, with
+// the item's record (list base, rows, position of row 0, block).
 struct Cursor {
   int it, ci, n_items;
-  int q, blk, cnt, q0, qlen, ctx, seq;
+  int4 rec;
 
-  __device__ void load(const PrefillLaunch& p) {
-    q = p.item_q[it];
-    blk = p.item_b[it];
-    cnt = p.item_cnt[it];
-    q0 = p.batch.cu_seqlens_q[q];
-    qlen = p.batch.cu_seqlens_q[q + 1] - q0;
-    ctx = p.batch.context_lens[q];
-    seq = ctx + qlen;
-  }
-  __device__ void seek(const PrefillLaunch& p, int chunk) {
+  __device__ __forceinline__ void seek(const PrefillLaunch& p, int chunk) {
     int lo = 0, hi = n_items;  // last item whose first chunk <= chunk (items are non-empty)
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (p.item_chunk[mid] <= chunk) lo = mid; else hi = mid;
     }
     it = lo;
-    load(p);
+    rec = p.item_rec[it];
     ci = chunk - p.item_chunk[it];
   }
-  __device__ void next(const PrefillLaunch& p) {
-    if (kChunkRows * (++ci) < cnt) return;
+  __device__ __forceinline__ void next(const PrefillLaunch& p) {
+    if (kChunkRows * (++ci) < rec.y) return;
     ci = 0;
-    if (++it < n_items) load(p);
+    if (++it < n_items) rec = p.item_rec[it];
   }
-  __device__ int rows() const { return min(kChunkRows, cnt - kChunkRows * ci); }
-  __device__ long long list_base(const PrefillLaunch& p) const {
-    return (long long)q0 * p.batch.bt_stride + (long long)blk * qlen + kChunkRows * ci;
-  }
-  // tokens of the block that exist (the request's last block may be partial)
-  __device__ int block_tokens() const { return min(kBlock, seq - kBlock * blk); }
+  __device__ __forceinline__ int rows() const { return min(kChunkRows, rec.y - kChunkRows * ci); }
+  __device__ __forceinline__ long long list_base() const { return (long long)rec.x + kChunkRows * ci; }
+  __device__ __forceinline__ int blk() const { return rec.w; }
 };
+
+// 2^x on the multi-function unit (x <= 0 here; tiny results flush to zero)
+__device__ __forceinline__ float ex2_mufu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^x for x <= 0 on the FMA pipe, to share the softmax's exponentials with
+// the multi-function unit (Cody-Waite range reduction): x = j + f with j =
+// round(x) -- adding 1.5 * 2^23 leaves round(x) in the low mantissa bits --
+// and f in [-1/2, 1/2]; 2^f from a degree-3 polynomial fitted for minimal
+// relative error on that interval (7.5e-5, below half a bf16 ulp); 2^j goes
+// into the exponent field (the shift drops the constant's bits).  x is
+// clamped to -125 so that the exponent stays normal.
+__device__ __forceinline__ float ex2_poly(float x) {
+  x = fmaxf(x, -125.f);
+  const float t = x + 12582912.f;
+  const float f = x - (t - 12582912.f);
+  const float p = fmaf(fmaf(fmaf(0.0551716685f, f, 0.2426111400f), f, 0.6932609677f), f,
+                       0.9999280572f);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
 
 // all lanes wait; the result is the same on every lane
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
 }
 
+// ---- the softmax of one TMEM lane (128 logits from column sa), warp-collective
+
+// 32 fp32 O columns of a lane as bf16, to dims chunks 0..3 of dst (chunk
+// stride: the 16 heads)
+__device__ __forceinline__ void store_o32(uint4* dst, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+    dst[kHeadSlots * x] =
+        make_uint4(pack_bf16x2(__uint_as_float(r[8 * x]), __uint_as_float(r[8 * x + 1])),
+                   pack_bf16x2(__uint_as_float(r[8 * x + 2]), __uint_as_float(r[8 * x + 3])),
+                   pack_bf16x2(__uint_as_float(r[8 * x + 4]), __uint_as_float(r[8 * x + 5])),
+                   pack_bf16x2(__uint_as_float(r[8 * x + 6]), __uint_as_float(r[8 * x + 7])));
+}
+
+// The softmax of one TMEM lane: 128 logits from column sa, warp-collective.
+// A block that holds some row's own position counts only its first `valid`
+// tokens (MASKED); the masked code performs exactly the same arithmetic
+// with the masked tokens' terms replaced by -inf / 0, so a row's result never
+// depends on which path its warp took.
+
+// running max over 32 raw scores (negated when NEG)
+template <bool NEG, bool MASKED>
+__device__ __forceinline__ float max32(const uint32_t (&r)[32], float acc, int base, int valid) {
+  float g8[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) g8[x] = acc;
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    float v = NEG ? -__uint_as_float(r[t]) : __uint_as_float(r[t]);
+    if (MASKED && base + t >= valid) v = -INFINITY;
+    g8[t & 7] = fmaxf(g8[t & 7], v);
+  }
+  return fmaxf(fmaxf(fmaxf(g8[0], g8[1]), fmaxf(g8[2], g8[3])),
+               fmaxf(fmaxf(g8[4], g8[5]), fmaxf(g8[6], g8[7])));
+}
+
+// max over the 128 raw scores (of their negations when NEG), loads in flight
+template <bool NEG, bool MASKED>
+__device__ __forceinline__ float row_max(uint32_t sa, int valid) {
+  uint32_t ra[32], rb[32];
+  float g = -INFINITY;
+  tc::tmem_ld32_issue(sa, ra);
+#pragma unroll 1
+  for (int c = 0; c < 4; c += 2) {
+    tc::tmem_wait_ld(ra);
+    tc::tmem_ld32_issue(sa + 32 * (c + 1), rb);
+    g = max32<NEG, MASKED>(ra, g, 32 * c, valid);
+    tc::tmem_wait_ld(rb);
+    if (c + 2 < 4) tc::tmem_ld32_issue(sa + 32 * (c + 2), ra);
+    g = max32<NEG, MASKED>(rb, g, 32 * c + 32, valid);
+  }
+  return g;
+}
+
+// p = 2^(s * scale2 - m) of 32 columns -- three of every four on the
+// multi-function unit, the fourth on the FMA pipe -- packed as bf16 pairs
+// into w; returns their sum
+template <bool MASKED>
+__device__ __forceinline__ float exp32(const uint32_t (&r)[32], float scale2, float m,
+                                       uint32_t (&w)[16], int base, int valid) {
+  float l8[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) l8[x] = 0.f;
+#pragma unroll
+  for (int t = 0; t < 32; t += 2) {
+    float p0 = ex2_mufu(fmaf(__uint_as_float(r[t]), scale2, -m));
+    const float x1 = fmaf(__uint_as_float(r[t + 1]), scale2, -m);
+    float p1 = (t & 2) ? ex2_poly(x1) : ex2_mufu(x1);
+    if (MASKED) {
+      p0 = base + t < valid ? p0 : 0.f;
+      p1 = base + t + 1 < valid ? p1 : 0.f;
+    }
+    l8[t & 7] += p0;
+    l8[(t + 1) & 7] += p1;
+    w[t >> 1] = pack_bf16x2(p0, p1);
+  }
+  return ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+}
+
+// P of the 128 columns written back over S (P group c takes columns 16c ..
+// 16c + 15, all read already), loads in flight; returns the sum of p
+template <bool MASKED>
+__device__ __forceinline__ float row_exp(uint32_t sa, float scale2, float m, int valid) {
+  uint32_t ra[32], rb[32], w[16];
+  float l = 0.f;
+  tc::tmem_ld32_issue(sa, ra);
+#pragma unroll 1
+  for (int c = 0; c < 4; c += 2) {
+    tc::tmem_wait_ld(ra);
+    tc::tmem_ld32_issue(sa + 32 * (c + 1), rb);
+    l += exp32<MASKED>(ra, scale2, m, w, 32 * c, valid);
+    tc::tmem_st16(sa + 16 * c, w);
+    tc::tmem_wait_ld(rb);
+    if (c + 2 < 4) tc::tmem_ld32_issue(sa + 32 * (c + 2), ra);
+    l += exp32<MASKED>(rb, scale2, m, w, 32 * c + 32, valid);
+    tc::tmem_st16(sa + 16 * (c + 1), w);
+  }
+  return l;
+}
+
+// (max of s * scale2, sum of p) of one lane
+template <bool MASKED>
+__device__ __forceinline__ float2 row_softmax(uint32_t sa, float scale2, int valid, bool live) {
+  // max of s * scale2 = |scale2| * max(sign(scale2) * s)
+  float m = scale2 >= 0.f ? row_max<false, MASKED>(sa, valid) * scale2
+                          : row_max<true, MASKED>(sa, valid) * -scale2;
+  if (!live) m = 0.f;
+  return make_float2(m, row_exp<MASKED>(sa, scale2, m, valid));
+}
+
+// (10 warps: three share a sub-partition's 16K registers, so at most 168
+// registers a thread)
 template <bool SCALAR>
 __global__ void __launch_bounds__(kPaThreads, 1)
     prefill_attn_kernel(const PrefillLaunch p, const __grid_constant__ CUtensorMap qmap,
@@ -288,14 +414,14 @@ __global__ void __launch_bounds__(kPaThreads, 1)
       Cursor cur;
       cur.n_items = n_items;
       cur.seek(p, c0);
-      int e_cur = lane < cur.rows() ? p.pf_lists[cur.list_base(p) + lane] : 0;
+      int e_cur = lane < cur.rows() ? p.pf_lists[cur.list_base() + lane] : 0;
       int kv_seq = 0, fills = 0;
       for (int j = 0; j < nj; ++j) {
         Cursor nxt = cur;
         int e_nxt = 0;
         if (j + 1 < nj) {  // the next chunk's list entries, in flight during this one
           nxt.next(p);
-          e_nxt = lane < nxt.rows() ? p.pf_lists[nxt.list_base(p) + lane] : 0;
+          e_nxt = lane < nxt.rows() ? p.pf_lists[nxt.list_base() + lane] : 0;
         }
         if (j == 0 || cur.ci == 0) {
           const int kvs = kv_seq & 1;
@@ -303,9 +429,8 @@ __global__ void __launch_bounds__(kPaThreads, 1)
             misc[1] = 1;
             break;
           }
-          const int page =
-              p.batch.block_table[(long long)cur.q * p.batch.bt_stride + cur.blk];
-          const int ntok = cur.block_tokens();
+          const int2 kv = p.item_kv[cur.it];
+          const int page = kv.x, ntok = kv.y;
           // a partial last block: the tokens past the request's end are not
           // data (never written); they are zeroed before P V reads them
           uint64_t* land = ntok < kBlock ? kv_fill : &kv_full[kvs];
@@ -346,10 +471,10 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], (uint32_t)(n * hq * 256));
         __syncwarp();
         if (lane < n) {
-          // (an entry outside the request, impossible from the top-k kernel,
-          // is read from the request's first row and never written back)
+          // (an entry outside the batch, impossible from the top-k kernel,
+          // reads row 0 and is never written back)
           const int er = e_cur >> 8;
-          const int r = (er >= cur.q0 && er < cur.q0 + cur.qlen) ? er : cur.q0;
+          const int r = er < p.batch.num_rows ? er : 0;
           uint8_t* qd = smem + kSmQ + qs * kTile + lane * (kHeadSlots * 128);
           tma_load_2d(qd, &qmap, 0, r * hq, &q_full[qs]);
           tma_load_2d(qd + kHalf, &qmap, 64, r * hq, &q_full[qs]);
@@ -358,30 +483,32 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         e_cur = e_nxt;
       }
     } else if (warp == 1) {
-      // ---------------- MMA issue (one thread)
+      // ---------------- MMA issue (one thread).  Buffers: S / P of chunk j
+      // in TMEM columns 128 (j & 1), O in 256 + 128 (j & 1).  S(j) may
+      // overwrite its buffer once P V of chunk j - 2 has completed (o_full);
+      // P V of chunk j may overwrite O once the epilogue of chunk j - 2 has
+      // read it (o_empty).  Issue order: S(j), then P V(j - 1), so that the
+      // tensor pipe computes the next scores while a softmax group works
+      // (issuing P V first whenever its P is ready measured slower: the
+      // other group then waits for its scores).
       if (lane == 0) {
         Cursor cur;
         cur.n_items = n_items;
         cur.seek(p, c0);
         int kv_seq = 0, cur_kvs = 0, prev_kvs = 0;
-        bool prev_last = false;
-        for (int j = 0; j <= nj; ++j) {
+        bool prev_last = false, ok = true;
+        for (int j = 0; j <= nj && ok; ++j) {
           bool last = false;
           if (j < nj) {
             const int buf = j & 1, qs = j % kQStages;
             if (j == 0 || cur.ci == 0) {
               cur_kvs = kv_seq & 1;
-              if (!mbar_wait(&kv_full[cur_kvs], (kv_seq >> 1) & 1)) {
-                misc[1] = 1;
-                break;
-              }
+              ok = mbar_wait(&kv_full[cur_kvs], (kv_seq >> 1) & 1);
               ++kv_seq;
             }
-            if (!mbar_wait(&q_full[qs], (j / kQStages) & 1) ||
-                (j >= 2 && !mbar_wait(&o_empty[buf], ((j >> 1) - 1) & 1))) {
-              misc[1] = 1;
-              break;
-            }
+            ok = ok && mbar_wait(&q_full[qs], (j / kQStages) & 1);
+            ok = ok && (j < 2 || mbar_wait(&o_full[buf], ((j >> 1) - 1) & 1));
+            if (!ok) break;
             tc::fence_after();
             const uint32_t qa = smem_u32(smem + kSmQ + qs * kTile);
             const uint32_t ka = smem_u32(smem + kSmK + cur_kvs * kTile);
@@ -393,17 +520,15 @@ __global__ void __launch_bounds__(kPaThreads, 1)
             }
             tc::commit(&q_empty[qs]);
             tc::commit(&s_full[buf]);
-            Cursor nx = cur;
-            nx.next(p);
-            last = j == nj - 1 || nx.ci == 0;
-            cur = nx;
+            const int before = cur.it;
+            cur.next(p);
+            last = j == nj - 1 || cur.it != before;
           }
           if (j >= 1) {  // O = P V of the previous chunk
             const int i = j - 1, pb = i & 1;
-            if (!mbar_wait(&p_full[pb], (i >> 1) & 1)) {
-              misc[1] = 1;
-              break;
-            }
+            ok = mbar_wait(&p_full[pb], (i >> 1) & 1) &&
+                 (i < 2 || mbar_wait(&o_empty[pb], ((i >> 1) - 1) & 1));
+            if (!ok) break;
             tc::fence_after();
             const uint32_t va = smem_u32(smem + kSmV + prev_kvs * kTile);
 #pragma unroll
@@ -417,9 +542,14 @@ __global__ void __launch_bounds__(kPaThreads, 1)
           prev_kvs = cur_kvs;
           prev_last = last;
         }
+        if (!ok) misc[1] = 1;
       }
     } else {
       // ---------------- softmax + epilogue, chunks j = grp, grp + 2, ...
+      // Thread = TMEM lane = (row slot, head) of the chunk; 128 logits each.
+      // The max and the sum run on 8 independent accumulators (the warp has
+      // little else to overlap with); rows whose block is entirely visible
+      // skip the per-token mask.
       const int grp = (warp - 2) >> 2, quarter = warp & 3;
       const int m = quarter * 32 + lane, slot = m >> 4, head = m & 15;
       const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
@@ -429,84 +559,74 @@ __global__ void __launch_bounds__(kPaThreads, 1)
       cur.n_items = n_items;
       cur.seek(p, c0);
       if (grp == 1 && nj > 1) cur.next(p);
-      int e = (slot < cur.rows()) ? p.pf_lists[cur.list_base(p) + slot] : 0;
+      int e = (slot < cur.rows()) ? p.pf_lists[cur.list_base() + slot] : 0;
       for (int j = grp; j < nj; j += 2) {
         const int buf = j & 1;
         const int r = e >> 8, si = e & 255;
-        const bool live = slot < cur.rows() && head < hq && r >= cur.q0 &&
-                          r < cur.q0 + cur.qlen && si < p.topk;
-        const int pos = cur.ctx + (r - cur.q0);
-        const int valid = live ? min(kBlock, pos + 1 - kBlock * cur.blk) : 0;
+        const bool live = slot < cur.rows() && head < hq && r < p.batch.num_rows && si < p.topk;
+        const int pos = r + cur.rec.z;
+        const int valid = live ? max(1, min(kBlock, pos + 1 - kBlock * cur.blk())) : 0;
+        const bool whole = __all_sync(0xffffffffu, valid == kBlock || !live);
+        // the next chunk of this group: its list entry is in flight meanwhile
+        Cursor nx = cur;
+        int e_nx = 0;
+        if (j + 2 < nj) {
+          nx.next(p);
+          nx.next(p);
+          e_nx = (slot < nx.rows()) ? p.pf_lists[nx.list_base() + slot] : 0;
+        }
         if (!warp_wait(&s_full[buf], (j >> 1) & 1)) {
           misc[1] = 1;
           break;
         }
         tc::fence_after();
         const uint32_t sa = tmem + lanes + buf * 128;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tc::tmem_ld32(sa + 32 * c, v);
-#pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (32 * c + t < valid) mx = fmaxf(mx, v[t] * scale2);
-        }
-        if (!live) mx = 0.f;
-        float l = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tc::tmem_ld32(sa + 32 * c, v);  // P overwrites S columns already consumed
-          uint32_t w[16];
-#pragma unroll
-          for (int t = 0; t < 32; t += 2) {
-            const float p0 = 32 * c + t < valid ? exp2f(fmaf(v[t], scale2, -mx)) : 0.f;
-            const float p1 = 32 * c + t + 1 < valid ? exp2f(fmaf(v[t + 1], scale2, -mx)) : 0.f;
-            l += p0 + p1;
-            w[t >> 1] = pack_bf16x2(p0, p1);
-          }
-          tc::tmem_st16(sa + 16 * c, w);
-        }
+        // Two passes over the 128 logits, 32 columns per load with the next
+        // load in flight: the max, then p = 2^(x - max) written back over S
+        // as bf16 and summed.  Whole blocks (every lane of the warp sees all
+        // 128 tokens) take the unrolled path; a block holding some row's own
+        // position takes a compact masked loop.
+        const float2 ml = whole ? row_softmax<false>(sa, scale2, kBlock, live)
+                                : row_softmax<true>(sa, scale2, valid, live);
+        const float m = ml.x, l = ml.y;
+        const float mx = m;
         tc::tmem_wait_st();
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[buf]);
-        // the next chunk of this group: its list entry is in flight during the epilogue
-        Cursor nx = cur;
-        int e_nx = 0;
-        if (j + 2 < nj) {
-          nx.next(p);
-          nx.next(p);
-          e_nx = (slot < nx.rows()) ? p.pf_lists[nx.list_base(p) + slot] : 0;
-        }
         if (!warp_wait(&o_full[buf], (j >> 1) & 1)) {
           misc[1] = 1;
           break;
         }
         tc::fence_after();
-        const float inv = (live && l > 0.f) ? 1.f / l : 0.f;
+        // partial per (row, slot): the unnormalised sum of p v as bf16 in
+        // [16 dim chunks][16 heads][8 dims], so the 16 head lanes of a slot
+        // store 256 contiguous bytes, and (max, sum of p) per head
         uint4* dst = reinterpret_cast<uint4*>(
-            p.part_o + (((long long)r * p.topk + si) * kHeadSlots + head) * kHeadDim);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tc::tmem_ld32(tmem + lanes + 256 + buf * 128 + 32 * c, v);
-          if (live) {
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-              dst[4 * c + x] = make_uint4(
-                  pack_bf16x2(v[8 * x] * inv, v[8 * x + 1] * inv),
-                  pack_bf16x2(v[8 * x + 2] * inv, v[8 * x + 3] * inv),
-                  pack_bf16x2(v[8 * x + 4] * inv, v[8 * x + 5] * inv),
-                  pack_bf16x2(v[8 * x + 6] * inv, v[8 * x + 7] * inv));
+                         p.part_o + ((long long)r * p.topk + si) * kHeadSlots * kHeadDim) +
+                     head;
+        {
+          const uint32_t oa = tmem + lanes + 256 + buf * 128;
+          uint32_t ra[32], rb[32];
+          tc::tmem_ld32_issue(oa, ra);
+#pragma unroll 1
+          for (int c = 0; c < 4; c += 2) {
+            tc::tmem_wait_ld(ra);
+            tc::tmem_ld32_issue(oa + 32 * (c + 1), rb);
+            if (live) store_o32(dst + kHeadSlots * 4 * c, ra);
+            tc::tmem_wait_ld(rb);
+            if (c + 2 < 4) {
+              tc::tmem_ld32_issue(oa + 32 * (c + 2), ra);
+            } else {
+              // every column is in registers: the O buffer is free
+              tc::fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&o_empty[buf]);
+            }
+            if (live) store_o32(dst + kHeadSlots * 4 * (c + 1), rb);
           }
         }
-        if (live)
-          p.part_lse[((long long)r * p.topk + si) * kHeadSlots + head] = mx + log2f(l);
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&o_empty[buf]);
+        if (live) p.part_ml[((long long)r * p.topk + si) * kHeadSlots + head] = make_float2(mx, l);
         cur = nx;
         e = e_nx;
       }
@@ -542,17 +662,19 @@ __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(const Pref
   if (head >= p.num_heads) return;
   const long long pbase = (long long)r * p.topk;
   float M = sink2;
-  for (int i = 0; i < nsel; ++i) M = fmaxf(M, p.part_lse[(pbase + i) * kHeadSlots + head]);
+  for (int i = 0; i < nsel; ++i) M = fmaxf(M, p.part_ml[(pbase + i) * kHeadSlots + head].x);
   float L = p.sinks ? exp2f(sink2 - M) : 0.f;
   float acc[16];
 #pragma unroll
   for (int x = 0; x < 16; ++x) acc[x] = 0.f;
   for (int i = 0; i < nsel; ++i) {
-    const float w = exp2f(p.part_lse[(pbase + i) * kHeadSlots + head] - M);
-    L += w;
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.part_o + ((pbase + i) * kHeadSlots + head) * kHeadDim + d0);
-    const uint4 a = src[0], b2 = src[1];
+    const float2 ml = p.part_ml[(pbase + i) * kHeadSlots + head];
+    const float w = exp2f(ml.x - M);
+    L += w * ml.y;
+    // [16 dim chunks][16 heads][8 dims]: dims d0.. are chunks d0 / 8, d0 / 8 + 1
+    const uint4* src = reinterpret_cast<const uint4*>(p.part_o + (pbase + i) * kHeadSlots * kHeadDim) +
+                       (d0 / 8) * kHeadSlots + head;
+    const uint4 a = src[0], b2 = src[kHeadSlots];
     const uint32_t u[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
 #pragma unroll
     for (int x = 0; x < 8; ++x) {

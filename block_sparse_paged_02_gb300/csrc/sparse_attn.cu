@@ -157,8 +157,10 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
     mbar_init(qbar, 1);
     for (int s = 0; s < kWarps * C::kStages; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(qbar, q_bytes);
-    bulk_g2s(smem + C::kQ, p.q + (long long)r * p.num_heads * kHeadDim, q_bytes, qbar);
+    if (!p.route) {  // (with a prefill path the row may not be ours: copy after the wait)
+      mbar_arrive_expect_tx(qbar, q_bytes);
+      bulk_g2s(smem + C::kQ, p.q + (long long)r * p.num_heads * kHeadDim, q_bytes, qbar);
+    }
   }
   // the sinks and the scalar v scale are inputs of the call: read them now,
   // so that no global load sits on the final merge's path
@@ -167,12 +169,14 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
     sink_s[kMaxHeads] = SCALE == MSA_SCALE_SCALAR ? __ldg(p.v_scale) : 1.f;
   // sparse tables and lengths come from the previous kernel on the stream
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (p.route && p.route[r] != 0) {
-    // a row of a prefill request: the block-major prefill attention writes
-    // it (uniform over the CTA and over the row's cluster); drain the query
-    // copy this CTA issued before leaving
-    if (tid == 0 && !mbar_wait(qbar, 0)) atomicOr(p.status, MSA_DEV_TIMEOUT);
-    return;
+  if (p.route) {
+    // a row of a prefill request is written by the block-major prefill
+    // attention: leave (uniform over the CTA and over the row's cluster)
+    if (p.route[r] != 0) return;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(qbar, q_bytes);
+      bulk_g2s(smem + C::kQ, p.q + (long long)r * p.num_heads * kHeadDim, q_bytes, qbar);
+    }
   }
 
   // this warp's page-16 entries are split*pps + warp + 4*i, one per lane; the
