@@ -11,6 +11,7 @@ from .binding import (MSA_DEV_BAD_LEN, MSA_DEV_BAD_PAGE, MSA_DEV_BAD_TABLE, MSA_
                       msa_sparse_paged_attn, msa_status_string, msa_topk_build_table,
                       msa_workspace_size)
 from .binding import make_mla_args, msa_sparse_mla_decode, msa_sparse_mla_workspace_size
+from .binding import MSA_CHECK_WAIT_COPY, MSA_CHECK_WAIT_TMEM, msa_check_bounded_wait
 from .case import DeviceCase, MlaCase
 
 __all__ = [
@@ -21,4 +22,5 @@ __all__ = [
     "msa_sparse_mla_decode", "msa_sparse_mla_workspace_size", "MSA_KV_BF16", "MSA_KV_FP8_E4M3",
     "MSA_SCALE_NONE", "MSA_SCALE_SCALAR", "MSA_SCALE_PER_TOKEN_HEAD", "MSA_DEV_BAD_PAGE",
     "MSA_DEV_BAD_LEN", "MSA_DEV_MALFORMED", "MSA_DEV_BAD_TABLE", "MSA_DEV_TIMEOUT",
+    "msa_check_bounded_wait", "MSA_CHECK_WAIT_TMEM", "MSA_CHECK_WAIT_COPY",
 ]

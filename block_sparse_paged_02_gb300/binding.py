@@ -24,7 +24,8 @@ MSA_DEV_BAD_PAGE, MSA_DEV_BAD_LEN, MSA_DEV_MALFORMED, MSA_DEV_BAD_TABLE, MSA_DEV
 
 EXPORTED = ("msa_index_score", "msa_topk_build_table", "msa_sparse_paged_attn", "msa_decode",
             "msa_kv_insert", "msa_sparse_mla_decode", "msa_sparse_mla_workspace_size",
-            "msa_workspace_size", "msa_status_string")
+            "msa_workspace_size", "msa_status_string", "msa_check_bounded_wait")
+MSA_CHECK_WAIT_TMEM, MSA_CHECK_WAIT_COPY = 1, 2
 
 
 class MsaError(RuntimeError):
@@ -110,6 +111,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.msa_sparse_mla_decode.argtypes = [P, P, ctypes.c_size_t, P, P]
             L.msa_workspace_size.restype = ctypes.c_size_t
             L.msa_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+            L.msa_check_bounded_wait.restype = ctypes.c_int
+            L.msa_check_bounded_wait.argtypes = [P, ctypes.c_uint32, i32, P, P]
             L.msa_status_string.restype = ctypes.c_char_p
             L.msa_status_string.argtypes = [ctypes.c_int]
             _lib = L
@@ -265,6 +268,14 @@ def msa_sparse_mla_decode(mla: msa_mla_args, workspace, dev_status, stream=None)
         ctypes.byref(mla), _p(workspace),
         int(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
         _p(dev_status), _stream(stream)))
+
+
+def msa_check_bounded_wait(dev_status, limit_us: int, flags: int = 0, copy_src=None,
+                           stream=None):
+    """Run the bounded-wait check (see msa.h): a wait that nothing satisfies
+    gives up after limit_us and sets MSA_DEV_TIMEOUT in dev_status."""
+    _check("msa_check_bounded_wait", lib().msa_check_bounded_wait(
+        _p(dev_status), int(limit_us), int(flags), _p(copy_src), _stream(stream)))
 
 
 def make_trace(after_score=None, after_topk=None, after_attn=None) -> msa_trace:

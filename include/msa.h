@@ -358,6 +358,29 @@ msa_status msa_sparse_mla_decode(const msa_mla_args* mla, void* workspace,
 size_t msa_workspace_size(int32_t num_rows, int32_t bt_stride, int32_t topk, int32_t num_heads,
                           int32_t head_dim, int32_t tbl_stride);
 
+/* Check of the bounded waits (failure detection without a GPU fault).
+ * Every kernel of the library gives up a wait that has not completed after
+ * a time limit (2 s), records MSA_DEV_TIMEOUT and returns, freeing what it
+ * holds, instead of hanging [P54404 "Key source snippets": a missing result
+ * must raise, not hang].  This entry point exercises that machinery on
+ * purpose: one CTA waits, with the library's own bounded wait and a limit
+ * of limit_us microseconds (1 .. 1e6), on an mbarrier armed for transaction
+ * bytes that nothing delivers, and on expiry sets MSA_DEV_TIMEOUT in
+ * *dev_status.  flags:
+ *   MSA_CHECK_WAIT_TMEM  the CTA holds tensor memory during the wait and
+ *                        frees it on the way out;
+ *   MSA_CHECK_WAIT_COPY  a real 16-byte bulk copy from copy_src (device,
+ *                        16-byte aligned) is in flight and is drained
+ *                        before the CTA leaves (a drain that itself gave up
+ *                        would set MSA_DEV_TIMEOUT << 1).
+ * The context stays usable: later calls on the stream run normally.
+ * Argument errors: dev_status NULL or a copy without copy_src -> NULL;
+ * limit_us out of range -> SHAPE; unknown flags -> UNSUPPORTED. */
+#define MSA_CHECK_WAIT_TMEM 1
+#define MSA_CHECK_WAIT_COPY 2
+msa_status msa_check_bounded_wait(uint32_t* dev_status, uint32_t limit_us, int32_t flags,
+                                  const void* copy_src, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* msa_status_string(msa_status status);
 

@@ -133,3 +133,17 @@ def test_mla_host_validation_without_gpu(lib):
     # up to 8 splits merge inside a cluster (no partials); more need partials
     assert B.msa_sparse_mla_workspace_size(64, 16, 2048) >= B.msa_sparse_mla_workspace_size(1, 16, 16)
     assert B.msa_sparse_mla_workspace_size(1, 16, 20000) > B.msa_sparse_mla_workspace_size(1, 16, 2048)
+
+
+def test_bounded_wait_check_validation_without_gpu(lib):
+    from block_sparse_paged_02_gb300 import binding as B
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: every case fails before a launch
+    assert lib.msa_check_bounded_wait(None, 1000, 0, None, None) == B.MSA_ERR_NULL
+    assert lib.msa_check_bounded_wait(fake, 0, 0, None, None) == B.MSA_ERR_SHAPE
+    assert lib.msa_check_bounded_wait(fake, 2_000_000, 0, None, None) == B.MSA_ERR_SHAPE
+    assert lib.msa_check_bounded_wait(fake, 1000, 8, None, None) == B.MSA_ERR_UNSUPPORTED
+    assert lib.msa_check_bounded_wait(fake, 1000, B.MSA_CHECK_WAIT_COPY, None, None) == \
+        B.MSA_ERR_NULL
+    assert lib.msa_check_bounded_wait(fake, 1000, B.MSA_CHECK_WAIT_COPY, ctypes.c_void_p(0x10008),
+                                      None) == B.MSA_ERR_NULL  # misaligned source
+
