@@ -16,13 +16,19 @@
 //
 // CTA roles (persistent grid, one CTA per SM, work = the flat list of
 // (request, 128-row tile, block) items split evenly across CTAs):
-//   warp 0  TMA producer: Q tile (once per row tile) and K block per item,
-//           128-byte-swizzled tiles via cp.async.bulk.tensor into a 4-stage
-//           ring with mbarrier completion;
-//   warp 1  allocates 256 TMEM columns (two 128-column accumulators);
-//           one thread issues the MMAs and tcgen05.commit;
-//   warps 2-5 epilogue: tcgen05.ld of 32 rows x 128 columns each, masked
-//           max, score store; releases the accumulator.
+//   warp 0  TMA producer: the K block of each item, 128-byte-swizzled
+//           tiles via cp.async.bulk.tensor into a 4-stage ring with
+//           mbarrier completion;
+//   warps 10-13 load each row tile's 128 index queries into TMEM (two
+//           buffers): the A operand, reused by every block of the tile,
+//           so the MMAs read only the K tile from shared memory (with both
+//           operands there, M128 N128 MMAs plus the tile copies saturate
+//           the shared-memory port);
+//   warp 1  allocates 512 TMEM columns (three 128-column accumulators,
+//           two query tiles); one thread issues the MMAs and commits;
+//   warps 2-9 epilogue, two groups of four on alternate items: tcgen05.ld
+//           of 32 rows x 128 columns each, masked max, score store;
+//           releases the accumulator.
 // Every wait is bounded; on expiry the kernel records MSA_DEV_TIMEOUT, stops
 // issuing work and still frees its TMEM.
 #include "tcgen05.cuh"
@@ -31,9 +37,11 @@ namespace msa {
 namespace {
 
 constexpr int kTcStages = 4;
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 448;  // 14 warps: copies, MMA, 2 x 4 epilogue, 4 query loaders
 constexpr int kTileRows = 128;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kAccBufs = 3;      // 128-column fp32 accumulators in TMEM (columns 0 .. 383)
+constexpr uint32_t kTmemA = 384; // then two query tiles (A operands), 64 columns each
+constexpr uint32_t kTmemCols = 512;
 
 template <int DI>
 struct TcCfg {
@@ -41,11 +49,13 @@ struct TcCfg {
   static constexpr int kTileBytes = kTileRows * DI * 2;
   static constexpr int kHalfBytes = kTileRows * 128;
   static constexpr int kKSteps = DI / 16;
-  // smem: A tile, B ring, then barriers / bookkeeping, then request prefix
-  static constexpr int kA = 0;
-  static constexpr int kB = kTileBytes;
+  static constexpr int kACols = DI / 2;            // a query row in TMEM: bf16 pairs
+  // smem: B ring, then barriers / bookkeeping, then request prefix
+  static constexpr int kB = 0;
   static constexpr int kBars = kB + kTcStages * kTileBytes;
-  static constexpr int kMisc = kBars + 16 * 8;
+  // b_full / b_empty [kTcStages], a_full / a_empty [2], acc_full / acc_empty [kAccBufs]
+  static constexpr int kNumBars = 2 * kTcStages + 4 + 2 * kAccBufs;
+  static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kPrefix = kMisc + 64;
   static_assert(8 + kTcStages <= 16, "misc area holds 16 ints");
   static size_t bytes(int num_reqs) { return 1024 + kPrefix + (size_t)(num_reqs + 1) * 4; }
@@ -58,6 +68,33 @@ using tc::tmem_ld32;
 
 // Instruction descriptor of the score tile: M = 128 rows, N = 128 tokens.
 constexpr uint32_t kIdesc = tc::idesc_bf16(128, 128, 0);
+
+// Max over the 128 accumulator columns of this thread's lane at ta, columns
+// c <= last only when MASKED (a block holding some row's own position);
+// 32 columns per load with the next load in flight (warp-collective).
+template <bool MASKED>
+__device__ __forceinline__ float row_max128(uint32_t ta, int last) {
+  uint32_t ra[32], rb[32];
+  float g8[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) g8[x] = -INFINITY;
+  tc::tmem_ld32_issue(ta, ra);
+#pragma unroll 1
+  for (int c = 0; c < 4; c += 2) {
+    tc::tmem_wait_ld(ra);
+    tc::tmem_ld32_issue(ta + 32 * (c + 1), rb);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (!MASKED || 32 * c + i <= last) g8[i & 7] = fmaxf(g8[i & 7], __uint_as_float(ra[i]));
+    tc::tmem_wait_ld(rb);
+    if (c + 2 < 4) tc::tmem_ld32_issue(ta + 32 * (c + 2), ra);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (!MASKED || 32 * c + 32 + i <= last) g8[i & 7] = fmaxf(g8[i & 7], __uint_as_float(rb[i]));
+  }
+  return fmaxf(fmaxf(fmaxf(g8[0], g8[1]), fmaxf(g8[2], g8[3])),
+               fmaxf(fmaxf(g8[4], g8[5]), fmaxf(g8[6], g8[7])));
+}
 
 // ------------------------------------------------------------ work cursor
 
@@ -110,10 +147,11 @@ struct Cursor {
   }
 };
 
+// (14 warps: four share a sub-partition's 16K registers, so at most 128
+// registers a thread; one CTA per SM)
 template <int DI>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    index_score_tc_kernel(const ScoreLaunch p, const __grid_constant__ CUtensorMap qmap,
-                          const __grid_constant__ CUtensorMap kmap) {
+__global__ void __maxnreg__(128)
+    index_score_tc_kernel(const ScoreLaunch p, const __grid_constant__ CUtensorMap kmap) {
   using C = TcCfg<DI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -121,10 +159,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBars);
   uint64_t* b_full = bars;                   // [kTcStages]
   uint64_t* b_empty = bars + kTcStages;      // [kTcStages]
-  uint64_t* a_full = bars + 2 * kTcStages;
-  uint64_t* a_empty = a_full + 1;
-  uint64_t* acc_full = a_full + 2;           // [2]
-  uint64_t* acc_empty = a_full + 4;          // [2]
+  uint64_t* a_full = bars + 2 * kTcStages;   // [2]
+  uint64_t* a_empty = a_full + 2;            // [2]
+  uint64_t* acc_full = a_empty + 2;          // [kAccBufs]
+  uint64_t* acc_empty = acc_full + kAccBufs; // [kAccBufs]
   int* misc = reinterpret_cast<int*>(smem + C::kMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 4);
   int* stage_valid = misc + 8;  // [kTcStages], written by the producer before arming
@@ -142,11 +180,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
     }
-    mbar_init(a_full, 1);
-    mbar_init(a_empty, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&a_full[i], 4);  // the four query-loader warps
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i], 4);  // the four warps of an epilogue group
     }
     fence_barrier_init();
   }
@@ -196,40 +236,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ---------------- TMA producer warp: lanes look up 32 items at a time
       // (request, tile, block, page id); one elected lane then arms the
       // stages and issues the tile copies in order
-      int a_key_q = -1, a_key_t = -1, a_loads = 0;
       bool stop = false;
       for (int j0 = 0; j0 < n_items && !stop; j0 += 32) {
-        int mq = 0, mt = 0, mq0 = 0, mpage = -1;
+        int mpage = -1;
         if (j0 + lane < n_items) {
           Cursor cur;
           cur.seek(b, prefix, R, i0 + j0 + lane);
-          mq = cur.q;
-          mt = cur.tile;
-          mq0 = cur.q0;
           mpage = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
         }
         const int cnt = min(32, n_items - j0);
         for (int jj = 0; jj < cnt; ++jj) {
           const int j = j0 + jj;
-          const int q = __shfl_sync(0xffffffffu, mq, jj);
-          const int t = __shfl_sync(0xffffffffu, mt, jj);
-          const int q0 = __shfl_sync(0xffffffffu, mq0, jj);
           const int page = __shfl_sync(0xffffffffu, mpage, jj);
           int ok = 1;
           if (lane == 0) {
-            if (q != a_key_q || t != a_key_t) {
-              if (a_loads > 0 && !mbar_wait(a_empty, (a_loads - 1) & 1)) {
-                ok = 0;
-              } else {
-                mbar_arrive_expect_tx(a_full, C::kTileBytes);
-                for (int h = 0; h < C::kHalves; ++h)
-                  tma_load_2d(smem + C::kA + h * C::kHalfBytes, &qmap, 64 * h, q0 + t * kTileRows,
-                              a_full);
-                a_key_q = q;
-                a_key_t = t;
-                ++a_loads;
-              }
-            }
             const int s = j % kTcStages;
             if (ok && j >= kTcStages && !mbar_wait(&b_empty[s], ((j / kTcStages) - 1) & 1))
               ok = 0;
@@ -255,22 +275,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     } else if (warp == 1 && lane == 0) {
-      // ---------------- MMA issuer
+      // ---------------- MMA issuer: D = Q_tile (TMEM) x K_block^T (shared)
       Cursor cur;
       cur.seek(b, prefix, R, i0);
-      int a_key_q = -1, a_key_t = -1, a_loads = 0;
+      int a_key_q = -1, a_key_t = -1, a_seq = 0, abuf = 0;
       for (int j = 0; j < n_items; ++j) {
-        if (cur.q != a_key_q || cur.tile != a_key_t) {
-          if (!mbar_wait(a_full, a_loads & 1)) {
+        if (cur.q != a_key_q || cur.tile != a_key_t) {  // the next row tile's queries
+          abuf = a_seq & 1;
+          if (!mbar_wait(&a_full[abuf], (a_seq >> 1) & 1)) {
             misc[1] = 1;
             break;
           }
           a_key_q = cur.q;
           a_key_t = cur.tile;
-          ++a_loads;
+          ++a_seq;
         }
-        const int s = j % kTcStages, buf = j & 1;
-        if (j >= 2 && !mbar_wait(&acc_empty[buf], ((j >> 1) - 1) & 1)) {
+        const int s = j % kTcStages, buf = j % kAccBufs;
+        if (j >= kAccBufs && !mbar_wait(&acc_empty[buf], ((j / kAccBufs) - 1) & 1)) {
           misc[1] = 1;
           break;
         }
@@ -280,31 +301,87 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         fence_after();
         if (stage_valid[s]) {
-          const uint32_t a_base = smem_u32(smem + C::kA);
           const uint32_t b_base = smem_u32(smem + C::kB + s * C::kTileBytes);
+          const uint32_t a_tm = tmem + kTmemA + abuf * 64u;
 #pragma unroll
           for (int kk = 0; kk < C::kKSteps; ++kk) {
             const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-            tc::mma_ss(tmem + buf * 128, tc::desc_kmajor_sw128(a_base + off),
-                       tc::desc_kmajor_sw128(b_base + off), kIdesc, kk > 0 ? 1u : 0u);
+            tc::mma_ts(tmem + buf * 128u, a_tm + kk * 8, tc::desc_kmajor_sw128(b_base + off),
+                       kIdesc, kk > 0 ? 1u : 0u);
           }
         }
         commit(&b_empty[s]);
         commit(&acc_full[buf]);
         Cursor nx = cur;
         nx.next(b, prefix, R);
-        if (j == n_items - 1 || nx.q != cur.q || nx.tile != cur.tile) commit(a_empty);
+        if (j == n_items - 1 || nx.q != cur.q || nx.tile != cur.tile) commit(&a_empty[abuf]);
         cur = nx;
       }
-    } else if (warp >= 2) {
-      // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
+    } else if (warp >= 10) {
+      // ---------------- query loaders: each row tile of the CTA's items into
+      // TMEM (lane = query row, column c = dims 2c, 2c+1), double-buffered;
+      // rows past the request's end are zero
       const int quarter = warp & 3;
+      const int m = quarter * 32 + lane;
+      const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
       Cursor cur;
       cur.seek(b, prefix, R, i0);
+      int a_seq = 0;
       for (int j = 0; j < n_items; ++j) {
-        const int buf = j & 1;
+        const bool new_tile = j == 0 || cur.blk == 0;  // a tile's items start at block 0
+        if (new_tile) {
+          const int ab = a_seq & 1;
+          if (a_seq >= 2 && !__all_sync(0xffffffffu, mbar_wait(&a_empty[ab], ((a_seq >> 1) - 1) & 1))) {
+            misc[1] = 1;
+            break;
+          }
+          const int row = cur.tile * kTileRows + m;
+          const uint4* src = reinterpret_cast<const uint4*>(p.idx_q + (long long)(cur.q0 + row) * DI);
+          const bool have = row < cur.qlen;
+#pragma unroll
+          for (int c = 0; c < C::kACols / 16; ++c) {
+            uint32_t w[16];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const uint4 v = have ? __ldg(src + 4 * c + x) : make_uint4(0u, 0u, 0u, 0u);
+              w[4 * x] = v.x;
+              w[4 * x + 1] = v.y;
+              w[4 * x + 2] = v.z;
+              w[4 * x + 3] = v.w;
+            }
+            tc::tmem_st16(tmem + lanes + kTmemA + ab * 64u + 16 * c, w);
+          }
+          tc::tmem_wait_st();
+          fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[ab]);
+          ++a_seq;
+        }
+        cur.next(b, prefix, R);
+      }
+    } else if (warp >= 2) {
+      // ---------------- epilogue: two groups of four warps take alternate
+      // items (accumulator j % 4); warp w reads TMEM lanes 32 (w % 4) .. +31
+      // = 32 query rows, each reduced to its causal-masked max over the 128
+      // token columns.  Blocks every row of the warp sees in full skip the
+      // mask; the next item's page id is loaded while this one is reduced.
+      const int grp = (warp - 2) >> 2, quarter = warp & 3;
+      const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+      Cursor cur;
+      cur.seek(b, prefix, R, i0);
+      if (grp == 1 && n_items > 1) cur.next(b, prefix, R);
+      int page = grp < n_items ? b.block_table[(long long)cur.q * b.bt_stride + cur.blk] : 0;
+      for (int j = grp; j < n_items; j += 2) {
+        const int buf = j % kAccBufs;
+        Cursor nx = cur;
+        int page_nx = 0;
+        if (j + 2 < n_items) {
+          nx.next(b, prefix, R);
+          nx.next(b, prefix, R);
+          page_nx = b.block_table[(long long)nx.q * b.bt_stride + nx.blk];
+        }
         // warp-uniform decision: tcgen05.ld below needs the whole warp
-        if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (j >> 1) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (j / kAccBufs) & 1))) {
           misc[1] = 1;
           break;
         }
@@ -312,25 +389,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int m = quarter * 32 + lane;
         const int row_in_req = cur.tile * kTileRows + m;
         const int pos = cur.ctx + row_in_req;
-        const int page = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
         const bool page_ok = page >= 0 && page < b.num_pages;
         const int last = pos - cur.blk * kBlock;  // visible columns: c <= last
-        float best = -INFINITY;
-#pragma unroll
-        for (int chunk = 0; chunk < 4; ++chunk) {
-          float v[32];
-          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * 128 + chunk * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (chunk * 32 + i <= last) best = fmaxf(best, v[i]);
-        }
-        if (row_in_req < cur.qlen && last >= 0)
-          p.scores[(long long)(cur.q0 + row_in_req) * p.score_stride + cur.blk] =
-              page_ok ? best : -INFINITY;
+        const uint32_t ta = tmem + lanes + buf * 128u;
+        const float best = __all_sync(0xffffffffu, last >= kBlock - 1)
+                               ? row_max128<false>(ta, last)
+                               : row_max128<true>(ta, last);
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        cur.next(b, prefix, R);
+        if (row_in_req < cur.qlen && last >= 0)
+          p.scores[(long long)(cur.q0 + row_in_req) * p.score_stride + cur.blk] =
+              page_ok ? best : -INFINITY;
+        cur = nx;
+        page = page_nx;
       }
     }
   }
@@ -351,16 +423,15 @@ bool make_map(CUtensorMap* map, const void* base, long long rows, int di) {
 
 template <int DI>
 cudaError_t launch_tc(const ScoreLaunch& p, cudaStream_t stream) {
-  CUtensorMap qmap, kmap;
-  if (!make_map(&qmap, p.idx_q, (long long)p.batch.num_rows, DI) ||
-      !make_map(&kmap, p.idx_k, (long long)p.batch.num_pages * kBlock, DI))
+  CUtensorMap kmap;
+  if (!make_map(&kmap, p.idx_k, (long long)p.batch.num_pages * kBlock, DI))
     return cudaErrorInvalidValue;
   const size_t smem = TcCfg<DI>::bytes(p.batch.num_reqs);
   auto kern = index_score_tc_kernel<DI>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<device_sm_count(), kTcThreads, smem, stream>>>(p, qmap, kmap);
+  kern<<<device_sm_count(), kTcThreads, smem, stream>>>(p, kmap);
   return cudaGetLastError();
 }
 
