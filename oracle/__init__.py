@@ -65,6 +65,10 @@ def _load():
             lib.orc_sparse_mla.restype = ctypes.c_uint32
             lib.orc_sparse_mla.argtypes = [i32, i32, i32, i32, P, P, ctypes.c_int64, P, P, P,
                                            ctypes.c_double, P, P, i32]
+            lib.orc_sparse_mla_ex.restype = ctypes.c_uint32
+            lib.orc_sparse_mla_ex.argtypes = [i32, i32, i32, i32, P, i32, ctypes.c_double, P,
+                                              i32, ctypes.c_double, ctypes.c_int64, P, P, P,
+                                              ctypes.c_double, P, P, i32]
             lib.orc_index_score_fp8.restype = ctypes.c_uint32
             lib.orc_index_score_fp8.argtypes = [P, P, P, P, i32, i32, P, i32, i32]
             lib.orc_topk_build_table.restype = ctypes.c_uint32
@@ -267,19 +271,28 @@ def kv_insert(w, k_new, v_new, idx_new, skip_index: bool = False):
 
 
 def sparse_mla(q, kv_cache, kv_indptr, kv_indices, dv: int, *, sinks=None,
-               softmax_scale: float, nthreads: Optional[int] = None):
-    """Sparse MLA decode: q [N, H, Dqk] bf16 bits, kv_cache [T, Dqk] bf16 bits
-    (value = first dv columns), per-row token ids through kv_indptr [N+1] /
-    kv_indices; returns (out [N, H, dv] fp64, lse [N, H] fp64, status)."""
-    q = _c(q, np.uint16)
-    kv = _c(kv_cache, np.uint16)
+               softmax_scale: float, nthreads: Optional[int] = None, q_scale=None,
+               kv_scale=None):
+    """Sparse MLA decode: q [N, H, Dqk] bf16 bits (or e4m3 codes, uint8, with
+    q_scale), kv_cache [T, Dqk] bf16 bits (or e4m3 codes, uint8, with
+    kv_scale; value = first dv columns), per-row token ids through kv_indptr
+    [N+1] / kv_indices; returns (out [N, H, dv] fp64, lse [N, H] fp64, status)."""
+    q = np.ascontiguousarray(q)
+    kv = np.ascontiguousarray(kv_cache)
+    q_fp8 = q.dtype == np.uint8
+    kv_fp8 = kv.dtype == np.uint8
+    q = _c(q, np.uint8 if q_fp8 else np.uint16)
+    kv = _c(kv, np.uint8 if kv_fp8 else np.uint16)
     ip = _c(kv_indptr, np.int32)
     ix = _c(kv_indices if len(kv_indices) else np.zeros(1, np.int32), np.int32)
     N, H, dqk = (int(x) for x in q.shape)
     out = np.empty((max(N, 1), H, dv), np.float64)
     lse = np.empty((max(N, 1), H), np.float64)
     sk = None if sinks is None else _c(sinks, np.float32)
-    st = _load().orc_sparse_mla(N, H, dqk, int(dv), _ptr(q), _ptr(kv), int(kv.shape[0]), _ptr(ip),
-                                _ptr(ix), _ptr(sk), float(softmax_scale), _ptr(out), _ptr(lse),
-                                nthreads or default_threads())
+    qs = 1.0 if q_scale is None else float(np.asarray(q_scale, np.float32).reshape(-1)[0])
+    ks = 1.0 if kv_scale is None else float(np.asarray(kv_scale, np.float32).reshape(-1)[0])
+    st = _load().orc_sparse_mla_ex(N, H, dqk, int(dv), _ptr(q), int(q_fp8), qs, _ptr(kv),
+                                   int(kv_fp8), ks, int(kv.shape[0]), _ptr(ip), _ptr(ix), _ptr(sk),
+                                   float(softmax_scale), _ptr(out), _ptr(lse),
+                                   nthreads or default_threads())
     return out[:N], lse[:N], int(st)

@@ -616,10 +616,15 @@ uint32_t orc_kv_insert(const orc_batch* b, int32_t hkv, int32_t head_dim, const 
 /* One latent KV row per token: kv[t, 0:dqk] is the key (latent part + rope
  * part), kv[t, 0:dv] the value.  Row r attends over the token ids
  * kv_indices[kv_indptr[r] .. kv_indptr[r+1]) with the same softmax, sink and
- * natural-log LSE as attend_head (softmax_scale only, no dequant scales). */
+ * natural-log LSE as attend_head.  FP8 operands ("Attention sinks for ROCm
+ * AITER sparse MLA", "Key source snippets": the decode op's q_scale and
+ * kv_scale): an e4m3 query element is q_scale * code, an e4m3 cache element
+ * kv_scale * code, for the key and the value alike. */
 typedef struct {
   int32_t heads, dqk, dv;
-  const uint16_t *q, *kv;
+  const void *q, *kv;
+  int32_t q_fp8, kv_fp8;
+  double q_scale, kv_scale;
   int64_t num_tokens;
   const int32_t *indptr, *indices;
   const float* sinks;
@@ -627,6 +632,16 @@ typedef struct {
   double *out, *lse;
   uint32_t* row_status;
 } mla_ctx;
+
+static double mla_q(const mla_ctx* c, int64_t index) {
+  if (c->q_fp8) return c->q_scale * orc_fp8_e4m3_value(((const uint8_t*)c->q)[index]);
+  return orc_bf16_value(((const uint16_t*)c->q)[index]);
+}
+
+static double mla_kv(const mla_ctx* c, int64_t index) {
+  if (c->kv_fp8) return c->kv_scale * orc_fp8_e4m3_value(((const uint8_t*)c->kv)[index]);
+  return orc_bf16_value(((const uint16_t*)c->kv)[index]);
+}
 
 static void mla_row(void* vctx, int32_t r) {
   const mla_ctx* c = (const mla_ctx*)vctx;
@@ -641,15 +656,15 @@ static void mla_row(void* vctx, int32_t r) {
   if (poisoned) n = 0; /* a poisoned row is computed as an empty row */
   double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
   for (int32_t h = 0; h < c->heads; ++h) {
-    const uint16_t* qh = c->q + ((int64_t)r * c->heads + h) * c->dqk;
+    const int64_t qh = ((int64_t)r * c->heads + h) * c->dqk;
     double* o = c->out + ((int64_t)r * c->heads + h) * c->dv;
     const int has_sink = c->sinks != NULL;
     const double sink = has_sink ? (double)c->sinks[h] : -INFINITY;
     double m = -INFINITY;
     for (int64_t i = 0; i < n; ++i) {
-      const uint16_t* k = c->kv + (int64_t)c->indices[b0 + i] * c->dqk;
+      const int64_t k = (int64_t)c->indices[b0 + i] * c->dqk;
       double dot = 0.0;
-      for (int32_t d = 0; d < c->dqk; ++d) dot += orc_bf16_value(qh[d]) * orc_bf16_value(k[d]);
+      for (int32_t d = 0; d < c->dqk; ++d) dot += mla_q(c, qh + d) * mla_kv(c, k + d);
       s[i] = c->scale * dot;
       if (s[i] > m) m = s[i];
     }
@@ -663,8 +678,8 @@ static void mla_row(void* vctx, int32_t r) {
     for (int64_t i = 0; i < n; ++i) {
       const double p = exp(s[i] - m);
       den += p;
-      const uint16_t* v = c->kv + (int64_t)c->indices[b0 + i] * c->dqk; /* value = latent part */
-      for (int32_t d = 0; d < c->dv; ++d) o[d] += p * orc_bf16_value(v[d]);
+      const int64_t v = (int64_t)c->indices[b0 + i] * c->dqk; /* value = latent part */
+      for (int32_t d = 0; d < c->dv; ++d) o[d] += p * mla_kv(c, v + d);
     }
     for (int32_t d = 0; d < c->dv; ++d) o[d] /= den;
     c->lse[(int64_t)r * c->heads + h] = m + log(den);
@@ -672,16 +687,27 @@ static void mla_row(void* vctx, int32_t r) {
   free(s);
 }
 
-uint32_t orc_sparse_mla(int32_t num_rows, int32_t heads, int32_t dqk, int32_t dv,
-                        const uint16_t* q, const uint16_t* kv_cache, int64_t num_tokens,
-                        const int32_t* kv_indptr, const int32_t* kv_indices, const float* sinks,
-                        double softmax_scale, double* out, double* lse, int32_t nthreads) {
-  mla_ctx c = {heads, dqk, dv, q, kv_cache, num_tokens, kv_indptr, kv_indices, sinks,
-               softmax_scale, out, lse, NULL};
+uint32_t orc_sparse_mla_ex(int32_t num_rows, int32_t heads, int32_t dqk, int32_t dv,
+                           const void* q, int32_t q_fp8, double q_scale, const void* kv_cache,
+                           int32_t kv_fp8, double kv_scale, int64_t num_tokens,
+                           const int32_t* kv_indptr, const int32_t* kv_indices,
+                           const float* sinks, double softmax_scale, double* out, double* lse,
+                           int32_t nthreads) {
+  mla_ctx c = {heads,    dqk,        dv,         q,          kv_cache, q_fp8, kv_fp8,
+               q_scale,  kv_scale,   num_tokens, kv_indptr,  kv_indices, sinks,
+               softmax_scale, out,   lse,        NULL};
   c.row_status = (uint32_t*)calloc((size_t)(num_rows > 0 ? num_rows : 1), sizeof(uint32_t));
   for_each_row(num_rows, nthreads, mla_row, &c);
   uint32_t st = 0;
   for (int32_t r = 0; r < num_rows; ++r) st |= c.row_status[r];
   free(c.row_status);
   return st;
+}
+
+uint32_t orc_sparse_mla(int32_t num_rows, int32_t heads, int32_t dqk, int32_t dv,
+                        const uint16_t* q, const uint16_t* kv_cache, int64_t num_tokens,
+                        const int32_t* kv_indptr, const int32_t* kv_indices, const float* sinks,
+                        double softmax_scale, double* out, double* lse, int32_t nthreads) {
+  return orc_sparse_mla_ex(num_rows, heads, dqk, dv, q, 0, 1.0, kv_cache, 0, 1.0, num_tokens,
+                           kv_indptr, kv_indices, sinks, softmax_scale, out, lse, nthreads);
 }

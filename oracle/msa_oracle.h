@@ -126,6 +126,18 @@ uint32_t orc_sparse_mla(int32_t num_rows, int32_t heads, int32_t dqk, int32_t dv
                         const int32_t* kv_indptr, const int32_t* kv_indices, const float* sinks,
                         double softmax_scale, double* out, double* lse, int32_t nthreads);
 
+/* The same with FP8 operands ("Attention sinks for ROCm AITER sparse MLA",
+ * "Key source snippets": q_scale, kv_scale of the decode op): q (q_fp8 = 1)
+ * holds e4m3 codes, an element being q_scale * code; kv_cache (kv_fp8 = 1)
+ * holds e4m3 codes, an element of the key and of the value being
+ * kv_scale * code; a bf16 operand ignores its scale. */
+uint32_t orc_sparse_mla_ex(int32_t num_rows, int32_t heads, int32_t dqk, int32_t dv,
+                           const void* q, int32_t q_fp8, double q_scale, const void* kv_cache,
+                           int32_t kv_fp8, double kv_scale, int64_t num_tokens,
+                           const int32_t* kv_indptr, const int32_t* kv_indices,
+                           const float* sinks, double softmax_scale, double* out, double* lse,
+                           int32_t nthreads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -765,3 +765,83 @@ def test_sparse_mla_order_invariance_and_bad_ids(orc):
     assert st == 8
     assert np.all(o[1] == 0) and np.array_equal(l[1], w.sinks.astype(np.float64))
     np.testing.assert_array_equal(o[0], a[0][0])
+
+
+# ------------------------------------------------------------ FP8 sparse MLA
+
+def _mla_fp8_reference(w):
+    """float64 torch reference for FP8 operands: e4m3 codes decoded by
+    torch's float8_e4m3fn (an independent decoder), times the per-tensor
+    scale (q_scale for the query, kv_scale for the key and the value), then
+    the same softmax with the sink as one more logit."""
+    def dec(a, scale):
+        if a.dtype == np.uint8:
+            return torch.from_numpy(a).view(torch.float8_e4m3fn).double() * float(scale[0])
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).double()
+    q, kv = dec(w.q, w.q_scale), dec(w.kv_cache, w.kv_scale)
+    out = np.zeros((w.num_rows, w.heads, w.dv))
+    lse = np.full((w.num_rows, w.heads), NEG_INF)
+    for r in range(w.num_rows):
+        ids = torch.from_numpy(w.kv_indices[w.kv_indptr[r]:w.kv_indptr[r + 1]].astype(np.int64))
+        K = kv[ids]
+        logits = w.softmax_scale * (q[r] @ K.T)
+        if w.sinks is not None:
+            logits = torch.cat([logits, torch.from_numpy(w.sinks).double()[:, None]], dim=1)
+        if logits.shape[1] == 0:
+            continue
+        p = torch.softmax(logits, dim=1)[:, : len(ids)]
+        out[r] = (p @ K[:, : w.dv]).numpy()
+        lse[r] = torch.logsumexp(logits, dim=1).numpy()
+    return out, lse
+
+
+@pytest.mark.parametrize("fp8_q,sink", [(True, True), (False, True), (True, False)])
+def test_fp8_sparse_mla_matches_torch_reference(orc, fp8_q, sink):
+    w = W.mla_fp8(W.sparse_mla_custom(33, [37, 16, 1, 200, 0], heads=8, ctx=512, dqk=96, dv=64,
+                                      with_sink=sink), seed=34, fp8_q=fp8_q)
+    out, lse, st = orc.sparse_mla(w.q, w.kv_cache, w.kv_indptr, w.kv_indices, w.dv,
+                                  sinks=w.sinks, softmax_scale=w.softmax_scale,
+                                  q_scale=w.q_scale, kv_scale=w.kv_scale)
+    assert st == 0
+    ref_o, ref_l = _mla_fp8_reference(w)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-10, atol=1e-12)
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(lse), fin)
+    np.testing.assert_allclose(lse[fin], ref_l[fin], rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_sparse_mla_unit_scales_equal_bf16(orc):
+    # e4m3 values are exact in bf16: with unit scales the FP8 oracle must
+    # equal the bf16 oracle on the decoded values bit for bit
+    w8 = W.mla_fp8(W.sparse_mla_custom(35, [20, 3, 64], heads=4, ctx=256, dqk=96, dv=64), 36)
+    w8 = dataclasses.replace(w8, q_scale=np.ones(1, np.float32), kv_scale=np.ones(1, np.float32))
+    to_bf16 = lambda codes: W.bf16_bits(torch.from_numpy(codes).view(torch.float8_e4m3fn)
+                                        .float().numpy())
+    a = orc.sparse_mla(w8.q, w8.kv_cache, w8.kv_indptr, w8.kv_indices, w8.dv, sinks=w8.sinks,
+                       softmax_scale=w8.softmax_scale, q_scale=w8.q_scale,
+                       kv_scale=w8.kv_scale)
+    b = orc.sparse_mla(to_bf16(w8.q), to_bf16(w8.kv_cache), w8.kv_indptr, w8.kv_indices, w8.dv,
+                       sinks=w8.sinks, softmax_scale=w8.softmax_scale)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[2] == b[2] == 0
+
+
+def test_fp8_sparse_mla_scale_placement(orc):
+    # kv_scale multiplies keys and values, q_scale the query: doubling
+    # kv_scale doubles every logit (so halving softmax_scale undoes it for
+    # the weights) and doubles every output value
+    w = W.mla_fp8(W.sparse_mla_custom(37, [40, 9], heads=4, ctx=256, dqk=96, dv=64,
+                                      with_sink=False), 38)
+    o1, l1, _ = orc.sparse_mla(w.q, w.kv_cache, w.kv_indptr, w.kv_indices, w.dv,
+                               softmax_scale=w.softmax_scale, q_scale=w.q_scale,
+                               kv_scale=w.kv_scale)
+    o2, l2, _ = orc.sparse_mla(w.q, w.kv_cache, w.kv_indptr, w.kv_indices, w.dv,
+                               softmax_scale=w.softmax_scale / 2, q_scale=w.q_scale,
+                               kv_scale=w.kv_scale * 2)
+    np.testing.assert_allclose(o2, 2 * o1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, rtol=1e-12, atol=1e-12)
+    o3, l3, _ = orc.sparse_mla(w.q, w.kv_cache, w.kv_indptr, w.kv_indices, w.dv,
+                               softmax_scale=w.softmax_scale * 2, q_scale=w.q_scale / 2,
+                               kv_scale=w.kv_scale)
+    np.testing.assert_allclose(o3, o1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l3, l1, rtol=1e-12, atol=1e-12)
+

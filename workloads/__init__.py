@@ -349,6 +349,10 @@ class MlaWorkload:
     sinks: Optional[np.ndarray]  # fp32 [H]
     softmax_scale: float
     seed: int = 0
+    # FP8 operands: q / kv_cache hold OCP e4m3 codes (uint8) and the element
+    # is scale * code; None for bf16 operands
+    q_scale: Optional[np.ndarray] = None   # fp32 [1]
+    kv_scale: Optional[np.ndarray] = None  # fp32 [1]
 
     @property
     def num_rows(self) -> int:
@@ -398,3 +402,27 @@ def sparse_mla_decode(seed: int = 7) -> MlaWorkload:
     """64 decode rows, 16 heads, 2048 selected tokens each out of an 8192-token
     context per row: the sparse-MLA decode recipe."""
     return sparse_mla_custom(seed, [2048] * 64, heads=16, ctx=8192, name="sparse_mla_decode")
+
+
+def mla_fp8(w: MlaWorkload, seed: int, fp8_q: bool = True) -> MlaWorkload:
+    """The same recipe with an FP8 latent cache (and query, if fp8_q): the
+    N(0,1) values encoded as e4m3 (RNE, saturating) with unit scale, then one
+    scale per tensor drawn from lognormal(0, 0.5) -- the element is scale *
+    code, as in the decode op's q_scale / kv_scale."""
+    rng = np.random.default_rng(seed)
+    as_f32 = lambda bits: (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+    kv = fp8_codes(as_f32(w.kv_cache))
+    kv_scale = np.array([rng.lognormal(0.0, 0.5)], np.float32)
+    q, q_scale = w.q, None
+    if fp8_q:
+        q = fp8_codes(as_f32(w.q))
+        q_scale = np.array([rng.lognormal(0.0, 0.5)], np.float32)
+    return dataclasses.replace(w, name=w.name + "_fp8", q=q, kv_cache=kv, q_scale=q_scale,
+                               kv_scale=kv_scale)
+
+
+def sparse_mla_decode_fp8(seed: int = 8) -> MlaWorkload:
+    """The sparse-MLA decode recipe with e4m3 query and latent cache, scalar
+    q_scale / kv_scale."""
+    return mla_fp8(sparse_mla_decode(seed), seed + 100)
+
