@@ -52,9 +52,11 @@ EXTRA_KERNEL_ITERS = 20
 EXTRA_CPU_BUDGET_S = 3.0
 W_SEED = {"tiny_decode": 1, "batched_decode": 2, "speculative_decode": 3,
           "large_batch_decode": 4, "chunked_prefill": 5, "large_batch_decode_fp8_index": 6,
-          "sparse_mla_decode": 7}
+          "sparse_mla_decode": 7, "sparse_mla_decode_fp8": 8}
+MLA_WORKLOADS = {"sparse_mla_decode": W.sparse_mla_decode,
+                 "sparse_mla_decode_fp8": W.sparse_mla_decode_fp8}
 EXTRA_WORKLOADS = ("tiny_decode", "batched_decode", "speculative_decode", "chunked_prefill",
-                   "large_batch_decode_fp8_index", "sparse_mla_decode")
+                   "large_batch_decode_fp8_index", "sparse_mla_decode", "sparse_mla_decode_fp8")
 
 
 # ---------------------------------------------------------------- bytes model
@@ -240,9 +242,10 @@ def workload_config(w):
 
 def mla_config(w):
     counts = np.diff(w.kv_indptr)
+    dt = lambda a: "fp8_e4m3 + scalar scale" if a.dtype == np.uint8 else "bf16"
     return {"workload": w.name, "rows": w.num_rows, "heads": w.heads, "dqk": w.dqk, "dv": w.dv,
             "cache_tokens": w.num_tokens, "tokens_per_row": int(np.median(counts)),
-            "kv": "bf16", "sinks": w.sinks is not None,
+            "kv": dt(w.kv_cache), "q": dt(w.q), "sinks": w.sinks is not None,
             "l2": "flushed between steps (512 MiB write, then 256 MiB read)"}
 
 
@@ -279,13 +282,16 @@ def cpu_rows_sample(w):
 
 def mla_bytes(w) -> dict:
     """Bytes and FLOPs of one sparse-MLA call: each row's distinct latent rows
-    (1152 B: read once however often listed), queries, token lists, outputs."""
+    (1152 B bf16 / 576 B e4m3: read once however often listed), queries,
+    token lists, outputs."""
     N, H = w.num_rows, w.heads
     toks = 0
     for r in range(N):
         toks += len(np.unique(w.kv_indices[w.kv_indptr[r]:w.kv_indptr[r + 1]]))
     counts = np.diff(w.kv_indptr).astype(np.int64)
-    total = (toks * w.dqk * 2 + N * H * w.dqk * 2 + N * H * (w.dv * 2 + 4)
+    kv_b = 1 if w.kv_cache.dtype == np.uint8 else 2
+    q_b = 1 if w.q.dtype == np.uint8 else 2
+    total = (toks * w.dqk * kv_b + N * H * w.dqk * q_b + N * H * (w.dv * 2 + 4)
              + int(counts.sum()) * 4 + (N + 1) * 4)
     flops = int(counts.sum()) * H * (w.dqk + w.dv) * 2
     return dict(total=total, flops=flops)
@@ -300,7 +306,8 @@ def mla_cpu_run(w, budget_s: float = 12.0, rows: int = 16):
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle.sparse_mla(w.q[:sub], w.kv_cache, ip, w.kv_indices[: int(ip[-1])], w.dv,
-                          sinks=w.sinks, softmax_scale=w.softmax_scale, nthreads=threads)
+                          sinks=w.sinks, softmax_scale=w.softmax_scale, nthreads=threads,
+                          q_scale=w.q_scale, kv_scale=w.kv_scale)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -314,8 +321,8 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    if args.workload == "sparse_mla_decode":
-        w = W.sparse_mla_decode(seed=rank_seed(args.workload, 0))
+    if args.workload in MLA_WORKLOADS:
+        w = MLA_WORKLOADS[args.workload](seed=rank_seed(args.workload, 0))
         run_once = lambda: mla_cpu_run(w, budget_s=0.0, rows=w.num_rows)
         metric, config, rows = MLA_METRIC, mla_config(w), w.num_rows
         sample = f"full {w.name} batch per step ({w.num_rows} rows)"
@@ -522,9 +529,9 @@ def measure_extra_decode(gpu, msa, name):
     }
 
 
-def measure_mla(gpu, msa, seed, steps_n, warmup, cpu_budget):
+def measure_mla(gpu, msa, name, seed, steps_n, warmup, cpu_budget):
     """Sparse MLA decode: graph replays, end to end, oracle on the host."""
-    w = W.sparse_mla_decode(seed=seed)
+    w = MLA_WORKLOADS[name](seed=seed)
     case = msa.MlaCase(w, device=gpu.dev)
     for i in range(warmup):
         gpu.flush_l2(i)
@@ -551,7 +558,9 @@ def measure_mla(gpu, msa, seed, steps_n, warmup, cpu_budget):
                      "traffic": None, "algorithmic_bytes_per_launch": nb["total"],
                      "avg_launch_ms": med},
         "tensor": {"achieved_tflops": tflops, "peak_bf16_tflops": peaks["bf16"],
-                   "frac": tflops / peaks["bf16"], "note": "mma.sync m16n8k16 bf16"},
+                   "frac": tflops / peaks["bf16"],
+                   "note": "mma.sync m16n8k16 " + ("f16 (e4m3 converted exactly)"
+                                                   if w.kv_cache.dtype == np.uint8 else "bf16")},
         "dominant_kernel": "sparse_mla", "dominant_kernel_frac": achieved / peaks["hbm"],
         "e2e": {"value": w.num_rows * steps_n / (e2e_ms / 1e3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -573,7 +582,7 @@ def run_mla_gpu(args):
     gpu = Gpu(local, flush=not args.profile)
     if args.profile:
         # plain run for profilers: warm-up + K steps, nothing else
-        w = W.sparse_mla_decode(seed=rank_seed(args.workload, rank))
+        w = MLA_WORKLOADS[args.workload](seed=rank_seed(args.workload, rank))
         case = msa.MlaCase(w, device=gpu.dev)
         for _ in range(args.warmup + args.steps):
             case.decode()
@@ -583,8 +592,8 @@ def run_mla_gpu(args):
     with ClockSampler(local) as clocks:
         if ws > 1:
             dist.barrier()
-        w, steps, rep = measure_mla(gpu, msa, rank_seed(args.workload, rank), args.steps,
-                                    args.warmup, 12.0 if rank == 0 else 0.0)
+        w, steps, rep = measure_mla(gpu, msa, args.workload, rank_seed(args.workload, rank),
+                                    args.steps, args.warmup, 12.0 if rank == 0 else 0.0)
     total_ms = sum(steps)
     if ws > 1:
         t = gpu.torch.tensor([total_ms], device=gpu.dev)
@@ -714,8 +723,8 @@ def run_gpu(args):
             for name in EXTRA_WORKLOADS:
                 if name == w.name:
                     continue
-                if name == "sparse_mla_decode":
-                    per[name] = measure_mla(gpu, msa, rank_seed(name, 0), MEDIAN_ITERS, 3,
+                if name in MLA_WORKLOADS:
+                    per[name] = measure_mla(gpu, msa, name, rank_seed(name, 0), MEDIAN_ITERS, 3,
                                             EXTRA_CPU_BUDGET_S)[2]
                 else:
                     per[name] = measure_extra_decode(gpu, msa, name)
@@ -734,7 +743,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="large_batch_decode",
-                    choices=sorted(W.NAMED) + ["sparse_mla_decode"])
+                    choices=sorted(W.NAMED) + sorted(MLA_WORKLOADS))
     ap.add_argument("--headline-only", action="store_true",
                     help="time the named workload only (no per_workload section)")
     ap.add_argument("--profile", action="store_true",
@@ -743,7 +752,7 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
-    if args.workload == "sparse_mla_decode":
+    if args.workload in MLA_WORKLOADS:
         return run_mla_gpu(args)
     return run_gpu(args)
 

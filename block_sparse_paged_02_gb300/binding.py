@@ -65,7 +65,9 @@ class msa_mla_args(ctypes.Structure):
                 ("kv_indptr", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p),
                 ("max_tokens", ctypes.c_int32), ("sinks", ctypes.c_void_p),
                 ("softmax_scale", ctypes.c_float), ("out", ctypes.c_void_p),
-                ("lse", ctypes.c_void_p)]
+                ("lse", ctypes.c_void_p), ("q_dtype", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("q_scale", ctypes.c_void_p),
+                ("kv_scale", ctypes.c_void_p)]
 
 
 class msa_trace(ctypes.Structure):
@@ -243,18 +245,24 @@ def msa_kv_insert(batch: msa_batch, k_new, v_new, num_kv_heads, head_dim, k_cach
 
 
 def make_mla_args(q, kv_cache, kv_indptr, kv_indices, out, lse, *, max_tokens: int,
-                  sinks=None, softmax_scale: float) -> msa_mla_args:
-    """Sparse MLA operands: q [N, H, 576] bf16, kv_cache [T, 576] bf16, int32
-    kv_indptr [N+1] / kv_indices, out [N, H, 512] bf16, lse [N, H] fp32."""
+                  sinks=None, softmax_scale: float, q_scale=None,
+                  kv_scale=None) -> msa_mla_args:
+    """Sparse MLA operands: q [N, H, 576] bf16 (or uint8 e4m3 codes with
+    q_scale), kv_cache [T, 576] bf16 (or uint8 e4m3 codes with kv_scale),
+    int32 kv_indptr [N+1] / kv_indices, out [N, H, 512] bf16, lse [N, H]
+    fp32; scales are device fp32 [1]."""
     check_sinks(sinks, int(q.shape[1]))
     for t in (kv_indptr, kv_indices):
         if t.dtype != torch.int32:
             raise ValueError("kv_indptr / kv_indices are int32")
+    q8 = q.dtype == torch.uint8
+    kv8 = kv_cache.dtype == torch.uint8
     a = msa_mla_args(_p(q), int(q.shape[0]), int(q.shape[1]), int(q.shape[2]),
                      int(out.shape[2]), _p(kv_cache), int(kv_cache.shape[0]), _p(kv_indptr),
                      _p(kv_indices), int(max_tokens), _p(sinks), float(softmax_scale), _p(out),
-                     _p(lse))
-    a._keep = (q, kv_cache, kv_indptr, kv_indices, out, lse, sinks)
+                     _p(lse), MSA_KV_FP8_E4M3 if q8 else MSA_KV_BF16,
+                     MSA_KV_FP8_E4M3 if kv8 else MSA_KV_BF16, _p(q_scale), _p(kv_scale))
+    a._keep = (q, kv_cache, kv_indptr, kv_indices, out, lse, sinks, q_scale, kv_scale)
     return a
 
 

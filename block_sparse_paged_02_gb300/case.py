@@ -122,13 +122,18 @@ class MlaCase:
         self.indptr = _dev(w.kv_indptr, device)
         self.indices = _dev(w.kv_indices if len(w.kv_indices) else np.zeros(1, np.int32), device)
         self.sinks = None if w.sinks is None else _dev(w.sinks, device)
+        q_scale = getattr(w, "q_scale", None)
+        kv_scale = getattr(w, "kv_scale", None)
+        self.q_scale = None if q_scale is None else _dev(q_scale, device)
+        self.kv_scale = None if kv_scale is None else _dev(kv_scale, device)
         N, H = int(w.q.shape[0]), int(w.q.shape[1])
         self.out = torch.empty((max(N, 1), H, w.dv), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((max(N, 1), H), dtype=torch.float32, device=device)
         self.status = torch.zeros((1,), dtype=torch.int32, device=device)
         self.args = B.make_mla_args(self.q, self.kv, self.indptr, self.indices, self.out,
                                     self.lse, max_tokens=self.max_tokens, sinks=self.sinks,
-                                    softmax_scale=w.softmax_scale)
+                                    softmax_scale=w.softmax_scale, q_scale=self.q_scale,
+                                    kv_scale=self.kv_scale)
         ws = B.msa_sparse_mla_workspace_size(N, H, self.max_tokens)
         self.workspace = torch.zeros((max(ws, 1),), dtype=torch.uint8, device=device)
 

@@ -484,8 +484,16 @@ msa_status msa_sparse_mla_decode(const msa_mla_args* a, void* workspace, size_t 
     return MSA_ERR_SHAPE;
   if (a->dqk != 576 || a->dv != 512 || a->num_heads > 128 || a->num_rows > 65535)
     return MSA_ERR_UNSUPPORTED;
+  if ((a->q_dtype != MSA_KV_BF16 && a->q_dtype != MSA_KV_FP8_E4M3) ||
+      (a->kv_dtype != MSA_KV_BF16 && a->kv_dtype != MSA_KV_FP8_E4M3))
+    return MSA_ERR_DTYPE;
+  if (a->q_dtype == MSA_KV_FP8_E4M3 && a->kv_dtype != MSA_KV_FP8_E4M3)
+    return MSA_ERR_UNSUPPORTED;
   if (a->num_rows == 0) return MSA_OK;
   if (!a->q || !a->kv_cache || !a->kv_indptr || !a->kv_indices || !a->out || !a->lse)
+    return MSA_ERR_NULL;
+  if ((a->kv_dtype == MSA_KV_FP8_E4M3 && !a->kv_scale) ||
+      (a->q_dtype == MSA_KV_FP8_E4M3 && !a->q_scale))
     return MSA_ERR_NULL;
   if (!aligned16(a->q) || !aligned16(a->kv_cache) || !aligned16(a->out)) return MSA_ERR_SHAPE;
   const MlaWs L = mla_layout(a->num_rows, a->num_heads, a->max_tokens);
@@ -509,6 +517,10 @@ msa_status msa_sparse_mla_decode(const msa_mla_args* a, void* workspace, size_t 
   p.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
   p.partials = reinterpret_cast<float*>(ws + L.partials);
   p.status = dev_status;
+  p.kv_fp8 = a->kv_dtype == MSA_KV_FP8_E4M3;
+  p.q_fp8 = a->q_dtype == MSA_KV_FP8_E4M3;
+  p.q_scale = p.q_fp8 ? a->q_scale : nullptr;
+  p.kv_scale = p.kv_fp8 ? a->kv_scale : nullptr;
   return cuda_status(launch_sparse_mla(p, stream));
 }
 

@@ -386,6 +386,9 @@ struct MlaLaunch {
   float* partials;          // [num_rows, head_groups, splits, 16, 516] fp32
   uint32_t* counters;       // [num_rows, head_groups], zero between calls
   uint32_t* status;
+  int kv_fp8, q_fp8;        // e4m3 codes in kv (then q may be e4m3 or bf16)
+  const float* q_scale;     // fp32 [1] when q_fp8
+  const float* kv_scale;    // fp32 [1] when kv_fp8
 };
 
 cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream);

@@ -58,6 +58,24 @@ struct MlaSmem {
   static constexpr int kBytes = kFlags + 64;
 };
 
+// FP8 latent cache: e4m3 rows (576 B) land by 16-byte asynchronous copies in
+// a 4-deep staging ring; during each step every thread converts its share
+// of the next step's rows to f16 (exact) into a 3-deep ring of the bf16
+// layout (the stage being read and the one the previous step's P V may still
+// be reading are never written), and the MMAs run on f16.
+constexpr int kRowBytes8 = kMlaDqk;                 // 576 B per cached token
+constexpr int kStageBytes8 = kStepTok * kRowBytes8; // 9 KB
+constexpr int kRing16 = 3;
+struct MlaSmem8 {
+  static constexpr int kStaging = 0;
+  static constexpr int kRing = kStaging + kStages * kStageBytes8;
+  static constexpr int kXchg = kRing + kRing16 * kStageBytes;
+  static constexpr int kIds = kXchg + 2 * kXchgFloats * 4;
+  static constexpr int kFlags = kIds + MlaSmem::kMaxIds * 4;
+  static constexpr int kBytes = kFlags + 64;
+  static_assert(16 * kPartHeadFloats * 4 <= kXchg, "partials fit before the exchange area");
+};
+
 // four 8x8 b16 matrices; lane l gives the row address of matrix l/8, row l%8
 // and receives (row g, cols 2c, 2c+1) of each (transposed: (rows 2c, 2c+1, col g))
 __device__ __forceinline__ void ldsm_x4(const void* row, uint32_t (&r)[4]) {
@@ -86,12 +104,14 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+template <bool FP8KV>
 __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* ring = smem + MlaSmem::kRing;
-  float* xchg = reinterpret_cast<float*>(smem + MlaSmem::kXchg);
-  int* ids = reinterpret_cast<int*>(smem + MlaSmem::kIds);
-  int* flags = reinterpret_cast<int*>(smem + MlaSmem::kFlags);
+  uint8_t* ring = smem + (FP8KV ? MlaSmem8::kRing : MlaSmem::kRing);
+  uint8_t* staging = smem + MlaSmem8::kStaging;  // (FP8 only)
+  float* xchg = reinterpret_cast<float*>(smem + (FP8KV ? MlaSmem8::kXchg : MlaSmem::kXchg));
+  int* ids = reinterpret_cast<int*>(smem + (FP8KV ? MlaSmem8::kIds : MlaSmem::kIds));
+  int* flags = reinterpret_cast<int*>(smem + (FP8KV ? MlaSmem8::kFlags : MlaSmem::kFlags));
 
   const int split = blockIdx.x, hg = blockIdx.y, r = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -122,26 +142,70 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
       const int st = step % kStages;
       const int t0 = step * kStepTok;
       const int cnt = min(kStepTok, n - t0);
-      uint8_t* dst = ring + st * kStageBytes;
-      constexpr int kChunksPerRow = kRowBytes / 16;  // 72
+      if constexpr (FP8KV) {
+        uint8_t* dst = staging + st * kStageBytes8;
+        const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+        constexpr int kChunksPerRow = kRowBytes8 / 16;  // 36
 #pragma unroll
-      for (int k = 0; k < kStepTok * kChunksPerRow / kThreads; ++k) {
-        const int q = tid + kThreads * k;
-        const int row = q / kChunksPerRow, col = q - row * kChunksPerRow;
-        if (row < cnt)
-          cp_async16(dst + row * kRowPitch + 16 * col,
-                     p.kv + (long long)ids[t0 + row] * kMlaDqk + 8 * col);
+        for (int k = 0; k < (kStepTok * kChunksPerRow + kThreads - 1) / kThreads; ++k) {
+          const int q = tid + kThreads * k;
+          const int row = q / kChunksPerRow, col = q - row * kChunksPerRow;
+          if (row < cnt)
+            cp_async16(dst + row * kRowBytes8 + 16 * col,
+                       kv8 + (long long)ids[t0 + row] * kMlaDqk + 16 * col);
+        }
+      } else {
+        uint8_t* dst = ring + st * kStageBytes;
+        constexpr int kChunksPerRow = kRowBytes / 16;  // 72
+#pragma unroll
+        for (int k = 0; k < kStepTok * kChunksPerRow / kThreads; ++k) {
+          const int q = tid + kThreads * k;
+          const int row = q / kChunksPerRow, col = q - row * kChunksPerRow;
+          if (row < cnt)
+            cp_async16(dst + row * kRowPitch + 16 * col,
+                       p.kv + (long long)ids[t0 + row] * kMlaDqk + 8 * col);
+        }
       }
     }
     cp_async_commit();
   };
+  // FP8: this thread's share of a landed step -- the same chunks its gather
+  // copied -- e4m3 -> f16, into the f16 ring (rows past the end convert
+  // stale bytes; their logits and values are masked below)
+  auto convert = [&](int step) {
+    const uint8_t* src = staging + (step % kStages) * kStageBytes8;
+    uint8_t* dst = ring + (step % kRing16) * kStageBytes;
+    constexpr int kChunksPerRow = kRowBytes8 / 16;  // 36
+#pragma unroll
+    for (int k = 0; k < (kStepTok * kChunksPerRow + kThreads - 1) / kThreads; ++k) {
+      const int q = tid + kThreads * k;
+      if (q < kStepTok * kChunksPerRow) {
+        const int row = q / kChunksPerRow, col = q - row * kChunksPerRow;
+        const uint4 v = lds128(src + row * kRowBytes8 + 16 * col);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t h[8];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          h[2 * x] = e4m3x2_to_f16x2((uint16_t)(w[x] & 0xffffu));
+          h[2 * x + 1] = e4m3x2_to_f16x2((uint16_t)(w[x] >> 16));
+        }
+        uint4* o = reinterpret_cast<uint4*>(dst + row * kRowPitch + 32 * col);
+        o[0] = make_uint4(h[0], h[1], h[2], h[3]);
+        o[1] = make_uint4(h[4], h[5], h[6], h[7]);
+      }
+    }
+  };
   for (int s = 0; s < kStages; ++s) gather(s);
   cp_async_wait<kStages - 1>();  // step 0 has landed (this thread's part)
+  if constexpr (FP8KV) {
+    if (n_steps > 0) convert(0);  // this thread's own copies: no barrier needed
+  }
   __syncthreads();               // ... everyone's
 
   // ---- query fragments (A of S = Q K^T): heads 16hg + {g, g+8}, k-step kk
   // of this warp's dims [144 warp, +144): columns 16kk + 2c (+1) and +8
   uint32_t qa[kKSteps][4];
+  const bool q_bf16 = !FP8KV || !p.q_fp8;  // (e4m3 queries load below)
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int h = 16 * hg + g + 8 * half;
@@ -149,9 +213,31 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
         p.q + ((long long)r * p.num_heads + h) * kMlaDqk + kKQuarter * warp + 2 * c);
 #pragma unroll
     for (int kk = 0; kk < kKSteps; ++kk) {
-      const bool live = h < p.num_heads;
+      const bool live = q_bf16 && h < p.num_heads;
       qa[kk][half] = live ? __ldg(qrow + 8 * kk) : 0u;          // cols 16kk + 2c, +1
       qa[kk][2 + half] = live ? __ldg(qrow + 8 * kk + 4) : 0u;  // cols 16kk + 8 + 2c, +1
+    }
+  }
+  if constexpr (FP8KV) {
+    // f16 operands: bf16 queries convert (|q| < 65504), e4m3 codes decode exactly
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int h = 16 * hg + g + 8 * half;
+      const uint16_t* q8 = reinterpret_cast<const uint16_t*>(
+          reinterpret_cast<const uint8_t*>(p.q) +
+          ((long long)r * p.num_heads + h) * kMlaDqk + kKQuarter * warp + 2 * c);
+#pragma unroll
+      for (int kk = 0; kk < kKSteps; ++kk) {
+        const bool live = h < p.num_heads;
+        if (p.q_fp8) {
+          qa[kk][half] = live ? e4m3x2_to_f16x2(__ldg(q8 + 8 * kk)) : 0u;
+          qa[kk][2 + half] = live ? e4m3x2_to_f16x2(__ldg(q8 + 8 * kk + 4)) : 0u;
+        } else {
+          const uint32_t a = qa[kk][half], b2 = qa[kk][2 + half];
+          qa[kk][half] = pack_f16x2(bf16lo(a), bf16hi(a));
+          qa[kk][2 + half] = pack_f16x2(bf16lo(b2), bf16hi(b2));
+        }
+      }
     }
   }
   // ldmatrix row addresses of this lane: matrix mi = lane / 8, row lane % 8
@@ -162,7 +248,11 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
   // V (B of P V, k = tokens, n = dims), transposed: matrices (tokens 0-7 |
   // 8-15) x (dims 16jj + 0-7 | 8-15) give n-tiles 2jj and 2jj+1
   const int v_off = ((mi & 1) * 8 + mrow) * kRowPitch + (kVQuarter * warp + (mi >> 1) * 8) * 2;
-  const float scale2 = p.softmax_scale * kLog2e;  // logits in log2 units
+  float scale2 = p.softmax_scale * kLog2e;  // logits in log2 units
+  if constexpr (FP8KV) {
+    scale2 *= __ldg(p.kv_scale);
+    if (p.q_fp8) scale2 *= __ldg(p.q_scale);
+  }
 
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   float o[16][4];
@@ -170,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
   for (int step = 0; step < n_steps; ++step) {
-    const int st = step % kStages;
+    const int st = step % (FP8KV ? kRing16 : kStages);
     const uint8_t* stage = ring + st * kStageBytes;
     const int nvalid = min(kStepTok, n - step * kStepTok);
 
@@ -182,17 +272,25 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
     for (int kk = 0; kk < kKSteps; ++kk) {
       uint32_t kb[4];
       ldsm_x4(stage + k_off + 32 * kk, kb);
-      mma16816<false>(s[0], qa[kk], kb[0], kb[1]);
-      mma16816<false>(s[1], qa[kk], kb[2], kb[3]);
+      mma16816<FP8KV>(s[0], qa[kk], kb[0], kb[1]);
+      mma16816<FP8KV>(s[1], qa[kk], kb[2], kb[3]);
     }
     float* xw = xchg + (step & 1) * kXchgFloats;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) xw[(warp * 8 + 4 * nt + e) * 32 + lane] = s[nt][e];
-    // the next step's rows have landed (this thread's part; steps complete
-    // in order), and the one barrier of the step makes them everyone's
-    cp_async_wait<kStages - 3>();
+    if constexpr (FP8KV) {
+      // the next step's rows have landed in the staging ring (this thread's
+      // part; steps complete in order); each thread converts exactly the
+      // chunks it copied, and the barrier below publishes them
+      cp_async_wait<kStages - 2>();
+      if (step + 1 < n_steps) convert(step + 1);
+    } else {
+      // the next step's rows have landed (this thread's part; steps complete
+      // in order), and the one barrier of the step makes them everyone's
+      cp_async_wait<kStages - 3>();
+    }
     __syncthreads();
     // the same sum, in the same order, in every warp
 #pragma unroll
@@ -205,8 +303,13 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
         const int t = 8 * nt + 2 * c + (e & 1);
         s[nt][e] = t < nvalid ? v * scale2 : -INFINITY;
       }
-    // the stage of the previous step is free in every warp now
-    if (step >= 1) gather(step - 1 + kStages);
+    // the stage of the previous step is free in every warp now (FP8: the
+    // staging of this step was converted before the previous barrier)
+    if constexpr (FP8KV) {
+      gather(step + kStages);
+    } else {
+      if (step >= 1) gather(step - 1 + kStages);
+    }
 
     // ---- online softmax (rows g and g+8), lazy rescaling
     float mx[2];
@@ -248,10 +351,17 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
     l_run[0] += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
     l_run[1] += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
     uint32_t pa[4];
-    pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-    pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-    pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-    pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+    if constexpr (FP8KV) {
+      pa[0] = pack_f16x2(pr[0][0], pr[0][1]);
+      pa[1] = pack_f16x2(pr[0][2], pr[0][3]);
+      pa[2] = pack_f16x2(pr[1][0], pr[1][1]);
+      pa[3] = pack_f16x2(pr[1][2], pr[1][3]);
+    } else {
+      pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+      pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+      pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+      pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+    }
 
     // ---- O += P V over this warp's value dims (n-tile j = dims 8j .. 8j+7);
     // rows past the end of the list hold stale or unwritten data: their
@@ -267,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
       ldsm_x4_t(stage + v_off + 32 * jj, vb);
       const uint32_t b0[2] = {vb[0] & keep_lo, vb[2] & keep_lo};
       const uint32_t b1[2] = {vb[1] & keep_hi, vb[3] & keep_hi};
-      mma16816<false>(o[2 * jj], pa, b0[0], b1[0]);
-      mma16816<false>(o[2 * jj + 1], pa, b0[1], b1[1]);
+      mma16816<FP8KV>(o[2 * jj], pa, b0[0], b1[0]);
+      mma16816<FP8KV>(o[2 * jj + 1], pa, b0[1], b1[1]);
     }
   }
 
@@ -354,7 +464,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
         for (int j = 0; j < 4; ++j) a[j] *= f;
         M = Mn;
       }
-      const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+      float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+      if constexpr (FP8KV) inv *= __ldg(p.kv_scale);  // values are kv_scale * code
       *reinterpret_cast<uint2*>(p.out + ((long long)r * p.num_heads + h_abs) * kMlaDv + d) =
           make_uint2(pack_bf16x2(a[0] * inv, a[1] * inv), pack_bf16x2(a[2] * inv, a[3] * inv));
       if (d == 0)
@@ -429,7 +540,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
       for (int j = 0; j < 64; ++j) acc[j] *= f;
       M = Mn;
     }
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    if constexpr (FP8KV) inv *= __ldg(p.kv_scale);  // values are kv_scale * code
     uint4* dst = reinterpret_cast<uint4*>(p.out + ((long long)r * p.num_heads + h_abs) * kMlaDv + d0);
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -449,14 +561,15 @@ int mla_max_tokens_per_split() { return MlaSmem::kMaxIds; }
 
 cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream) {
   if (p.num_rows == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       MlaSmem::kBytes);
+  auto kern = p.kv_fp8 ? sparse_mla_kernel<true> : sparse_mla_kernel<false>;
+  const int smem_bytes = p.kv_fp8 ? MlaSmem8::kBytes : MlaSmem::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, p.head_groups, p.num_rows);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = MlaSmem::kBytes;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of a (row, head group)
@@ -465,7 +578,7 @@ cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.splits <= kMaxClusterSplits ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -322,11 +322,20 @@ msa_status msa_kv_insert(const msa_batch* batch, const void* k_new, const void* 
  *              an empty row and raises MSA_DEV_BAD_TABLE
  *   sinks      fp32 [num_heads] or NULL;  softmax_scale as for attention
  *   out        [num_rows, num_heads, dv] bf16;  lse [num_rows, num_heads] fp32
+ *   kv_dtype   MSA_KV_BF16, or MSA_KV_FP8_E4M3: kv_cache holds OCP e4m3
+ *              codes [num_tokens, dqk] and an element (of the key and of the
+ *              value) is kv_scale[0] * code (kv_scale: device fp32 [1])
+ *   q_dtype    MSA_KV_BF16, or MSA_KV_FP8_E4M3 (only with an FP8 cache): q
+ *              holds e4m3 codes and an element is q_scale[0] * code
+ *              [the decode op's q_scale / kv_scale, "Key source snippets"]
  * For head h: s_t = softmax_scale * (q_h . kv_t[0:dqk]),
  * m = max(max_t s_t, sink_h), den = sum_t exp(s_t - m) + exp(sink_h - m),
  * out = sum_t exp(s_t - m) kv_t[0:dv] / den, lse = m + ln(den).
- * Supported: dqk == 576, dv == 512 (512 latent + 64 rope), 1 <= num_heads
- * <= 128, num_rows <= 65535. */
+ * With an FP8 cache the products run in f16 on the tensor cores (e4m3 codes
+ * convert exactly; a bf16 query converts to f16, so |q| must stay below
+ * 65504).  Supported: dqk == 576, dv == 512 (512 latent + 64 rope),
+ * 1 <= num_heads <= 128, num_rows <= 65535; an FP8 query with a bf16 cache
+ * returns MSA_ERR_UNSUPPORTED. */
 typedef struct msa_mla_args {
   const void* q;
   int32_t num_rows;
@@ -342,6 +351,10 @@ typedef struct msa_mla_args {
   float softmax_scale;
   void* out;
   float* lse;
+  int32_t q_dtype;
+  int32_t kv_dtype;
+  const float* q_scale;
+  const float* kv_scale;
 } msa_mla_args;
 
 /* Bytes of workspace msa_sparse_mla_decode needs (zero-filled before its
