@@ -438,7 +438,10 @@ DECODE_INPUTS = ("q", "idx_q", "cu_q", "cu_k", "ctx", "bt")
 
 def decode_kernel_times(gpu, case, msa, iters):
     """The same step eagerly with events after each stage (events recorded
-    inside a graph cannot be timed)."""
+    inside a graph cannot be timed), and the number of kernels the call
+    launches (the library's own count).  When the score kernel selects the
+    blocks there is no top-k kernel: its interval is empty and the score
+    kernel's includes the selection."""
     e = [gpu.ev() for _ in range(4)]
     trace = msa.make_trace(e[1], e[2], e[3])
     score, topk, attn = [], [], []
@@ -454,13 +457,7 @@ def decode_kernel_times(gpu, case, msa, iters):
         score.append(e[0].elapsed_time(e[1]))
         topk.append(e[1].elapsed_time(e[2]))
         attn.append(e[2].elapsed_time(e[3]))
-    return {"index_score": score, "topk_table": topk, "sparse_attn": attn}
-
-
-def launches_per_step(w) -> int:
-    q_lens = np.diff(w.cu_seqlens_q)
-    return 3 + int(q_lens.max() >= 64 and w.index_heads == 1
-                   and getattr(w, "index_dtype", 0) != W.KV_FP8)
+    return {"index_score": score, "topk_table": topk, "sparse_attn": attn}, int(trace.kernels)
 
 
 def kernel_rooflines(nbytes, kernel_ms, peaks):
@@ -473,6 +470,9 @@ def kernel_rooflines(nbytes, kernel_ms, peaks):
     out = {}
     for name, (b, f) in work.items():
         ms = statistics.mean(kernel_ms[name])
+        if ms < 1e-4:  # no such kernel (the selection ran inside the score kernel)
+            out[name] = {"ms": ms, "algorithmic_bytes": b, "flops": f, "fused": True}
+            continue
         gbs = b / (ms / 1e3) / 1e9
         tfs = f / (ms / 1e3) / 1e12
         hf, tf = gbs / peaks["hbm"], tfs / peaks["bf16"]
@@ -501,7 +501,7 @@ def measure_extra_decode(gpu, msa, name):
         raise RuntimeError(f"{name}: device status {int(case.status.item())}")
     g = gpu.capture(lambda s: case.decode(keep_tables=False, stream=s))
     steps = gpu.time_steps(g.replay, MEDIAN_ITERS)
-    kern = decode_kernel_times(gpu, case, msa, EXTRA_KERNEL_ITERS)
+    kern, nk = decode_kernel_times(gpu, case, msa, EXTRA_KERNEL_ITERS)
     case.decode()
     gpu.torch.cuda.synchronize()
     topk_sel = case.topk_idx[: w.num_rows].cpu().numpy()
@@ -523,7 +523,7 @@ def measure_extra_decode(gpu, msa, name):
         "dominant_bound": kr[dom]["bound"],
         "e2e": {"value": w.num_rows * EXTRA_E2E_ITERS / (e2e_ms / 1e3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches_per_step": launches_per_step(w),
+        "gpu_launches_per_step": nk,
         "cpu_baseline": cpu_oracle_run(w, budget_s=EXTRA_CPU_BUDGET_S, rows=cpu_rows_sample(w)),
         "peak_source": peaks["source"],
     }
@@ -670,7 +670,7 @@ def run_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
 
-    kern = decode_kernel_times(gpu, case, msa, args.steps)
+    kern, nk = decode_kernel_times(gpu, case, msa, args.steps)
     case.decode()
     torch.cuda.synchronize()
     topk_sel = case.topk_idx[: w.num_rows].cpu().numpy()
@@ -710,7 +710,7 @@ def run_gpu(args):
         "kernels": kr,
         "e2e": {"value": w.num_rows * ws * args.steps / (e2e_ms / 1e3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step(w) * args.steps,
+        "gpu_launches": nk * args.steps,
         "launch": launch_mode,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu_oracle_run(w),

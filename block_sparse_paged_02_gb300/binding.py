@@ -72,7 +72,7 @@ class msa_mla_args(ctypes.Structure):
 
 class msa_trace(ctypes.Structure):
     _fields_ = [("after_score", ctypes.c_void_p), ("after_topk", ctypes.c_void_p),
-                ("after_attn", ctypes.c_void_p)]
+                ("after_attn", ctypes.c_void_p), ("kernels", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -294,6 +294,6 @@ def make_trace(after_score=None, after_topk=None, after_attn=None) -> msa_trace:
         if e is not None and not e.cuda_event:
             e.record()
     h = lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else None
-    t = msa_trace(h(after_score), h(after_topk), h(after_attn))
+    t = msa_trace(h(after_score), h(after_topk), h(after_attn), 0)
     t._keep = (after_score, after_topk, after_attn)
     return t

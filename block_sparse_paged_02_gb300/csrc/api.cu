@@ -219,11 +219,12 @@ MlaWs mla_layout(int num_rows, int num_heads, int max_tokens) {
 
 // Step 1: the streaming CUDA-core kernel, plus the tensor-core kernel for
 // requests with many rows when the batch may hold any (max_q_len hint).
-cudaError_t launch_scores(ScoreLaunch p, cudaStream_t stream) {
+cudaError_t launch_scores(ScoreLaunch p, cudaStream_t stream, int* kernels = nullptr) {
   // (bf16 keys only: an FP8 cache would need FP8 queries for the f8 MMA kinds)
   const bool tc = !p.idx_fp8 && p.batch.max_q_len >= kTcMinRows &&
                   tc_score_supported(p.index_heads, p.index_dim);
   p.tc_min_rows = tc ? kTcMinRows : 0;
+  if (kernels) *kernels = tc ? 2 : 1;
   cudaError_t e = launch_index_score(p, stream);
   if (e != cudaSuccess || !tc) return e;
   return launch_index_score_tc(p, stream);
@@ -359,7 +360,7 @@ msa_status msa_sparse_paged_attn(const msa_attn_args* attn, const int32_t* spars
 msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index_cache* index,
                       int32_t topk, const msa_attn_args* attn, int32_t* topk_idx, int32_t* sparse_tbl,
                       int32_t tbl_stride, int32_t* sparse_len, void* workspace,
-                      size_t workspace_bytes, uint32_t* dev_status, const msa_trace* trace,
+                      size_t workspace_bytes, uint32_t* dev_status, msa_trace* trace,
                       cudaStream_t stream) {
   msa_status st = check_batch(batch);
   if (st != MSA_OK) return st;
@@ -413,7 +414,8 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
                  static_cast<const uint8_t*>(index->k_cache), index->heads, index->dim, scores,
                  batch->bt_stride, dev_status, 0, index->dtype == MSA_KV_FP8_E4M3,
                  index->dtype == MSA_KV_FP8_E4M3 ? index->k_scale : nullptr};
-  cudaError_t e = launch_scores(sp, stream);
+  int score_kernels = 0;
+  cudaError_t e = launch_scores(sp, stream, &score_kernels);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_score) cudaEventRecord(trace->after_score, stream);
 
@@ -469,6 +471,7 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
   e = launch_sparse_attn(ap, stream, true);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   if (trace && trace->after_attn) cudaEventRecord(trace->after_attn, stream);
+  if (trace) trace->kernels = score_kernels + 2 + (prefill ? 3 : 0);
   return MSA_OK;
 }
 

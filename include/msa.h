@@ -143,11 +143,13 @@ typedef struct msa_attn_args {
 } msa_attn_args;
 
 /* Optional CUDA events msa_decode records on `stream` after each stage (for
- * timing; any may be NULL). */
+ * timing; any may be NULL).  msa_decode writes `kernels`: the number of
+ * kernels the call launched. */
 typedef struct msa_trace {
   cudaEvent_t after_score;
   cudaEvent_t after_topk;
   cudaEvent_t after_attn;
+  int32_t kernels;
 } msa_trace;
 
 /* The paged index-K cache, the keys of step 1 [P54682 "Implementation
@@ -270,16 +272,22 @@ msa_status msa_sparse_paged_attn_static(const msa_attn_args* attn, const int32_t
 
 /* The whole path: msa_index_score -> msa_topk_build_table ->
  * msa_sparse_paged_attn in stream order, with the intermediates held in the
- * workspace [P54682 "Implementation breakdown" items 2-3: the indexer writes
- * the sparse table the attention consumes].  Results are bit-identical to
- * the three separate calls.  topk_idx, sparse_tbl and sparse_len may be NULL
- * (kept in the workspace) or device arrays that receive them; tbl_stride is
+ * workspace [P54682 "Implementation breakdown" items 1-3: the decode index
+ * scoring fused with the top-k, the indexer writing the sparse table the
+ * attention consumes].  topk_idx, sparse_tbl and sparse_len may be NULL
+ * (held in the workspace) or device arrays that receive them; tbl_stride is
  * the width of the caller's sparse_tbl (>= 8*topk, ignored when NULL).
- * trace may be NULL. */
+ * trace may be NULL.  Calls sharing a workspace must be ordered on one
+ * stream.  Selection, table and lengths are bit-identical to the three
+ * separate calls, and so are O / LSE except on the rows of requests with
+ * >= 64 rows when max_q_len >= 64, the KV is bf16 without per-token scales
+ * and topk <= 128: those rows take a block-major tensor-core attention,
+ * whose O / LSE agree with the other path within the attention tolerance,
+ * not bit for bit. */
 msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index_cache* index,
                       int32_t topk, const msa_attn_args* attn, int32_t* topk_idx, int32_t* sparse_tbl,
                       int32_t tbl_stride, int32_t* sparse_len, void* workspace,
-                      size_t workspace_bytes, uint32_t* dev_status, const msa_trace* trace,
+                      size_t workspace_bytes, uint32_t* dev_status, msa_trace* trace,
                       cudaStream_t stream);
 
 /* The step before the path: write the new tokens' K, V and index-K into
