@@ -661,25 +661,51 @@ __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(const Pref
   const int nsel = __syncthreads_count(has);
   if (head >= p.num_heads) return;
   const long long pbase = (long long)r * p.topk;
+  // one pass over the partials, four at a time with all their loads in
+  // flight together; the running max moves once per group of four
   float M = sink2;
-  for (int i = 0; i < nsel; ++i) M = fmaxf(M, p.part_ml[(pbase + i) * kHeadSlots + head].x);
-  float L = p.sinks ? exp2f(sink2 - M) : 0.f;
+  float L = p.sinks ? 1.f : 0.f;  // the sink's term, relative to M
   float acc[16];
 #pragma unroll
   for (int x = 0; x < 16; ++x) acc[x] = 0.f;
-  for (int i = 0; i < nsel; ++i) {
-    const float2 ml = p.part_ml[(pbase + i) * kHeadSlots + head];
-    const float w = exp2f(ml.x - M);
-    L += w * ml.y;
-    // [16 dim chunks][16 heads][8 dims]: dims d0.. are chunks d0 / 8, d0 / 8 + 1
-    const uint4* src = reinterpret_cast<const uint4*>(p.part_o + (pbase + i) * kHeadSlots * kHeadDim) +
-                       (d0 / 8) * kHeadSlots + head;
-    const uint4 a = src[0], b2 = src[kHeadSlots];
-    const uint32_t u[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+  for (int i0 = 0; i0 < nsel; i0 += 4) {
+    float2 ml[4];
+    uint4 va[4], vb[4];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) {
-      acc[2 * x] += w * bf16lo(u[x]);
-      acc[2 * x + 1] += w * bf16hi(u[x]);
+    for (int u = 0; u < 4; ++u) {
+      ml[u] = make_float2(-INFINITY, 0.f);
+      va[u] = vb[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (i0 + u < nsel) {
+        // [16 dim chunks][16 heads][8 dims]: dims d0.. are chunks d0 / 8, d0 / 8 + 1
+        const long long slot = pbase + i0 + u;
+        ml[u] = p.part_ml[slot * kHeadSlots + head];
+        const uint4* src = reinterpret_cast<const uint4*>(p.part_o + slot * kHeadSlots * kHeadDim) +
+                           (d0 / 8) * kHeadSlots + head;
+        va[u] = src[0];
+        vb[u] = src[kHeadSlots];
+      }
+    }
+    float mb = M;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) mb = fmaxf(mb, ml[u].x);
+    if (mb > M) {  // rescale what was gathered so far to the new max
+      const float f = M == -INFINITY ? 0.f : exp2f(M - mb);
+      L *= f;
+#pragma unroll
+      for (int x = 0; x < 16; ++x) acc[x] *= f;
+      M = mb;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (ml[u].x == -INFINITY) continue;  // (a missing or empty partial adds nothing)
+      const float w = exp2f(ml[u].x - M);
+      L += w * ml[u].y;
+      const uint32_t uu[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        acc[2 * x] += w * bf16lo(uu[x]);
+        acc[2 * x + 1] += w * bf16hi(uu[x]);
+      }
     }
   }
   const float inv = L > 0.f ? vs / L : 0.f;
