@@ -209,7 +209,7 @@ msa_status msa_index_score(const msa_batch* batch, const void* idx_q,
  *   topk_idx [num_rows, topk] int32
  *   sparse_tbl [num_rows, tbl_stride] int32, tbl_stride >= 8*topk
  *   sparse_len [num_rows] int32
- * Supported: bt_stride <= 16384. */
+ * Supported: bt_stride <= 16384, topk <= 2048. */
 msa_status msa_topk_build_table(const msa_batch* batch, const float* scores,
                                 int32_t score_stride, int32_t topk, int32_t* topk_idx,
                                 int32_t* sparse_tbl, int32_t tbl_stride, int32_t* sparse_len,

@@ -78,6 +78,16 @@ def test_host_validation_without_gpu(lib):
     # table narrower than 8*topk
     assert lib.msa_topk_build_table(ctypes.byref(b), fake, 4, 4, fake, fake, 31, fake, st,
                                     None) == B.MSA_ERR_SHAPE
+    # the largest sizes: topk 2048, bt_stride 16384, 4096 requests; one past
+    # each is refused before any launch
+    big = B.msa_batch(fake, fake, fake, fake, 16385, 1, 1, 10)
+    assert lib.msa_topk_build_table(ctypes.byref(big), fake, 16385, 4, fake, fake, 32, fake, st,
+                                    None) == B.MSA_ERR_UNSUPPORTED
+    many = B.msa_batch(fake, fake, fake, fake, 4, 4097, 4097, 10)
+    assert lib.msa_topk_build_table(ctypes.byref(many), fake, 4, 4, fake, fake, 32, fake, st,
+                                    None) == B.MSA_ERR_UNSUPPORTED
+    assert lib.msa_topk_build_table(ctypes.byref(b), fake, 4, 2049, fake, fake, 8 * 2049, fake,
+                                    st, None) == B.MSA_ERR_UNSUPPORTED
     # attention: 2 KV heads, head_dim 64, 17 heads, bad dtype -> rejected
     def attn(**kw):
         a = dict(q=fake, num_rows=1, num_heads=16, num_kv_heads=1, head_dim=128, k_cache=fake,

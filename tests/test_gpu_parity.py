@@ -156,6 +156,32 @@ def test_more_attention_splits_than_a_cluster(msa, orc):
     check_against_oracle(orc, w, sep, fused)
 
 
+def test_largest_block_table_and_topk(msa, orc):
+    # the largest sizes the ABI accepts: a row with bt_stride = 16384 blocks
+    # (2^21 tokens) selecting topk = 2048 blocks (16384 page-16 entries, 128
+    # attention splits merged through the workspace), beside a row whose
+    # blocks are fewer than k (all selected)
+    w = W.custom(71, q_lens=[1, 1], seq_lens=[16384 * 128, 5000], hq=8, di=64, topk=2048,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_SCALAR, with_sink=True)
+    assert w.bt_stride == 16384
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
+def test_largest_request_count(msa, orc):
+    # num_reqs = 4096 (the most a batch may hold): one-row requests and a few
+    # empty ones, contexts of 1..400 tokens; thousands of rows take the
+    # one-warp-per-row top-k
+    rng = np.random.default_rng(72)
+    ql = [0 if i % 97 == 5 else 1 for i in range(4096)]
+    seq = [int(x) for x in rng.integers(1, 401, size=4096)]
+    w = W.custom(72, q_lens=ql, seq_lens=seq, hq=8, di=64, topk=3, kv_dtype=W.KV_FP8,
+                 scale_mode=W.SCALE_PER_TOKEN_HEAD, with_sink=True)
+    assert len(w.cu_seqlens_q) - 1 == 4096
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
 @pytest.mark.parametrize("rows,kv", [(152, W.KV_FP8), (101, W.KV_FP8), (60, W.KV_FP8),
                                      (50, W.KV_FP8), (43, W.KV_FP8), (101, W.KV_BF16),
                                      (43, W.KV_BF16)])
