@@ -25,8 +25,10 @@ class DeviceCase:
     """Inputs of one decode call resident on the GPU, plus outputs.
 
     `w` is any object with the fields of `workloads.Workload` (host numpy
-    arrays).  The KV and index-K pools stay resident; `refresh_step_inputs`
-    re-uploads only what changes per step (queries and batch geometry)."""
+    arrays).  The KV and index-K pools stay resident; after
+    `pack_step_inputs()` what changes per step (queries and batch geometry)
+    sits in one device buffer, `step_inputs`, that one copy refreshes, and
+    O / LSE in another, `step_outputs`."""
 
     def __init__(self, w, device: str = "cuda", topk: Optional[int] = None,
                  tbl_stride: Optional[int] = None):
@@ -61,16 +63,49 @@ class DeviceCase:
         self.status = torch.zeros((1,), dtype=torch.int32, device=device)
         q_lens = np.diff(np.asarray(w.cu_seqlens_q, np.int64))
         self.max_q_len = int(q_lens.max()) if q_lens.size else 0
-        self.batch = B.make_batch(self.cu_q, self.cu_k, self.ctx, self.bt, w.num_pages, N,
-                                  max_q_len=self.max_q_len)
-        self.attn = B.make_attn_args(self.q, self.k, self.v, w.kv_dtype, w.num_pages, self.out,
-                                     self.lse, scale_mode=w.scale_mode, k_scale=self.k_scale,
-                                     v_scale=self.v_scale, sinks=self.sinks,
-                                     softmax_scale=w.softmax_scale)
         ws = B.msa_workspace_size(N, w.bt_stride, self.topk, hq, d, self.tbl_stride)
         self.workspace = torch.zeros((ws,), dtype=torch.uint8, device=device)
         ws_a = B.msa_workspace_size(N, 0, 0, hq, d, self.tbl_stride)
         self.attn_workspace = torch.zeros((ws_a,), dtype=torch.uint8, device=device)
+        self.step_inputs = None
+        self.step_outputs = None
+        self._args()
+
+    def _args(self):
+        w = self.w
+        self.batch = B.make_batch(self.cu_q, self.cu_k, self.ctx, self.bt, w.num_pages,
+                                  self.num_rows, max_q_len=self.max_q_len)
+        self.attn = B.make_attn_args(self.q, self.k, self.v, w.kv_dtype, w.num_pages, self.out,
+                                     self.lse, scale_mode=w.scale_mode, k_scale=self.k_scale,
+                                     v_scale=self.v_scale, sinks=self.sinks,
+                                     softmax_scale=w.softmax_scale)
+
+    @staticmethod
+    def _pack(tensors, device):
+        """One byte buffer holding the tensors (256-byte aligned each) and
+        views of it with their shapes and dtypes, contents copied."""
+        offs, total = [], 0
+        for t in tensors:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty((max(total, 256),), dtype=torch.uint8, device=device)
+        views = []
+        for t, o in zip(tensors, offs):
+            n = t.numel() * t.element_size()
+            v = buf[o:o + n].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            views.append(v)
+        return buf, views
+
+    def pack_step_inputs(self):
+        """Move the per-step inputs into one device buffer and O / LSE into
+        another (the argument structs are rebuilt on the new addresses)."""
+        buf, (self.q, self.idx_q, self.cu_q, self.cu_k, self.ctx, self.bt) = self._pack(
+            [self.q, self.idx_q, self.cu_q, self.cu_k, self.ctx, self.bt], self.device)
+        self.step_inputs = buf
+        obuf, (self.out, self.lse) = self._pack([self.out, self.lse], self.device)
+        self.step_outputs = obuf
+        self._args()
 
     # -- the four entry points on this batch
     def index_score(self, stream=None):

@@ -468,6 +468,26 @@ def test_repeated_calls_are_identical(msa):
         assert np.array_equal(a[key], b[key])
 
 
+def test_packed_step_inputs(msa):
+    # per-step inputs and outputs moved into one buffer each (one copy per
+    # step each way): the same results, and a refreshed input buffer is used
+    w = W.custom(63, q_lens=[1, 3, 2], seq_lens=[7000, 3000, 900], hq=16, di=128, topk=8,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_SCALAR, with_sink=True)
+    c = msa.DeviceCase(w)
+    c.decode()
+    a = c.fetch()
+    assert c.step_inputs is None
+    c.pack_step_inputs()
+    host = c.step_inputs.cpu()
+    c.step_inputs.zero_()
+    c.step_inputs.copy_(host)
+    c.decode()
+    b = c.fetch()
+    for key in ("out", "lse", "tbl", "topk_idx", "sparse_len"):
+        assert np.array_equal(a[key], b[key]), key
+    assert b["status"] == 0
+
+
 def test_every_call_rescores_every_block(msa, orc):
     # New queries on later calls must change every block score of the fused
     # path (stale workspace scores from the first call would show up as wrong
