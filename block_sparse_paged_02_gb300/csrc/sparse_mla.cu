@@ -58,18 +58,21 @@ struct MlaSmem {
   static constexpr int kBytes = kFlags + 64;
 };
 
-// FP8 latent cache: e4m3 rows (576 B) land by 16-byte asynchronous copies in
-// a 4-deep staging ring; during each step every thread converts its share
-// of the next step's rows to f16 (exact) into a 3-deep ring of the bf16
-// layout (the stage being read and the one the previous step's P V may still
-// be reading are never written), and the MMAs run on f16.
-constexpr int kRowBytes8 = kMlaDqk;                 // 576 B per cached token
-constexpr int kStageBytes8 = kStepTok * kRowBytes8; // 9 KB
-constexpr int kRing16 = 3;
+// FP8 latent cache: e4m3 rows (576 B, 592 B apart) land by 16-byte
+// asynchronous copies in a 4-deep ring, the same pipeline as bf16 rows; the
+// MMA fragments are read straight from the e4m3 bytes and converted to f16
+// (exact) in registers.  Logits: lane (g, c) takes the 4 consecutive dims
+// 16kk + 4c .. + 3 of token g as its k-slots (2c, 2c+1, 2c+8, 2c+9) -- one
+// 32-bit read; the queries use the same slot order.  Values: lane (g, c)
+// reads dims 16g .. 16g + 15 of tokens 2c, 2c+1, 2c+8, 2c+9 (16 bytes each)
+// and pairs the tokens' bytes with byte permutes, so n-tile j's column g is
+// value dim 16g + j of the warp's 128.  (A converted f16 copy of each step
+// in shared memory measured 12.5 us slower on the 64-row workload.)
+constexpr int kRowPitch8 = kMlaDqk + 16;            // 592 B: rows 4 banks apart
+constexpr int kStageBytes8 = kStepTok * kRowPitch8; // 9.25 KB
 struct MlaSmem8 {
-  static constexpr int kStaging = 0;
-  static constexpr int kRing = kStaging + kStages * kStageBytes8;
-  static constexpr int kXchg = kRing + kRing16 * kStageBytes;
+  static constexpr int kRing = 0;
+  static constexpr int kXchg = kRing + kStages * kStageBytes8;
   static constexpr int kIds = kXchg + 2 * kXchgFloats * 4;
   static constexpr int kFlags = kIds + MlaSmem::kMaxIds * 4;
   static constexpr int kBytes = kFlags + 64;
@@ -108,7 +111,6 @@ template <bool FP8KV>
 __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem + (FP8KV ? MlaSmem8::kRing : MlaSmem::kRing);
-  uint8_t* staging = smem + MlaSmem8::kStaging;  // (FP8 only)
   float* xchg = reinterpret_cast<float*>(smem + (FP8KV ? MlaSmem8::kXchg : MlaSmem::kXchg));
   int* ids = reinterpret_cast<int*>(smem + (FP8KV ? MlaSmem8::kIds : MlaSmem::kIds));
   int* flags = reinterpret_cast<int*>(smem + (FP8KV ? MlaSmem8::kFlags : MlaSmem::kFlags));
@@ -143,15 +145,15 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
       const int t0 = step * kStepTok;
       const int cnt = min(kStepTok, n - t0);
       if constexpr (FP8KV) {
-        uint8_t* dst = staging + st * kStageBytes8;
+        uint8_t* dst = ring + st * kStageBytes8;
         const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-        constexpr int kChunksPerRow = kRowBytes8 / 16;  // 36
+        constexpr int kChunksPerRow = kMlaDqk / 16;  // 36
 #pragma unroll
         for (int k = 0; k < (kStepTok * kChunksPerRow + kThreads - 1) / kThreads; ++k) {
           const int q = tid + kThreads * k;
           const int row = q / kChunksPerRow, col = q - row * kChunksPerRow;
           if (row < cnt)
-            cp_async16(dst + row * kRowBytes8 + 16 * col,
+            cp_async16(dst + row * kRowPitch8 + 16 * col,
                        kv8 + (long long)ids[t0 + row] * kMlaDqk + 16 * col);
         }
       } else {
@@ -169,43 +171,14 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
     }
     cp_async_commit();
   };
-  // FP8: this thread's share of a landed step -- the same chunks its gather
-  // copied -- e4m3 -> f16, into the f16 ring (rows past the end convert
-  // stale bytes; their logits and values are masked below)
-  auto convert = [&](int step) {
-    const uint8_t* src = staging + (step % kStages) * kStageBytes8;
-    uint8_t* dst = ring + (step % kRing16) * kStageBytes;
-    constexpr int kChunksPerRow = kRowBytes8 / 16;  // 36
-#pragma unroll
-    for (int k = 0; k < (kStepTok * kChunksPerRow + kThreads - 1) / kThreads; ++k) {
-      const int q = tid + kThreads * k;
-      if (q < kStepTok * kChunksPerRow) {
-        const int row = q / kChunksPerRow, col = q - row * kChunksPerRow;
-        const uint4 v = lds128(src + row * kRowBytes8 + 16 * col);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t h[8];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          h[2 * x] = e4m3x2_to_f16x2((uint16_t)(w[x] & 0xffffu));
-          h[2 * x + 1] = e4m3x2_to_f16x2((uint16_t)(w[x] >> 16));
-        }
-        uint4* o = reinterpret_cast<uint4*>(dst + row * kRowPitch + 32 * col);
-        o[0] = make_uint4(h[0], h[1], h[2], h[3]);
-        o[1] = make_uint4(h[4], h[5], h[6], h[7]);
-      }
-    }
-  };
   for (int s = 0; s < kStages; ++s) gather(s);
   cp_async_wait<kStages - 1>();  // step 0 has landed (this thread's part)
-  if constexpr (FP8KV) {
-    if (n_steps > 0) convert(0);  // this thread's own copies: no barrier needed
-  }
   __syncthreads();               // ... everyone's
 
   // ---- query fragments (A of S = Q K^T): heads 16hg + {g, g+8}, k-step kk
   // of this warp's dims [144 warp, +144): columns 16kk + 2c (+1) and +8
   uint32_t qa[kKSteps][4];
-  const bool q_bf16 = !FP8KV || !p.q_fp8;  // (e4m3 queries load below)
+  const bool q_bf16 = !FP8KV;  // (with an e4m3 cache the queries load below)
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int h = 16 * hg + g + 8 * half;
@@ -219,24 +192,31 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
     }
   }
   if constexpr (FP8KV) {
-    // f16 operands: bf16 queries convert (|q| < 65504), e4m3 codes decode exactly
+    // f16 operands in the key spans' slot order: k-slots (2c, 2c+1) and
+    // (2c+8, 2c+9) of k-step kk are dims 16kk + 4c, +1 and +2, +3 of the
+    // warp's 144; bf16 queries convert (|q| < 65504), e4m3 codes exactly
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int h = 16 * hg + g + 8 * half;
-      const uint16_t* q8 = reinterpret_cast<const uint16_t*>(
-          reinterpret_cast<const uint8_t*>(p.q) +
-          ((long long)r * p.num_heads + h) * kMlaDqk + kKQuarter * warp + 2 * c);
+      const bool live = h < p.num_heads;
+      const long long qoff = ((long long)r * p.num_heads + (live ? h : 0)) * kMlaDqk +
+                             kKQuarter * warp + 4 * c;
 #pragma unroll
       for (int kk = 0; kk < kKSteps; ++kk) {
-        const bool live = h < p.num_heads;
+        uint32_t lo = 0u, hi = 0u;
         if (p.q_fp8) {
-          qa[kk][half] = live ? e4m3x2_to_f16x2(__ldg(q8 + 8 * kk)) : 0u;
-          qa[kk][2 + half] = live ? e4m3x2_to_f16x2(__ldg(q8 + 8 * kk + 4)) : 0u;
-        } else {
-          const uint32_t a = qa[kk][half], b2 = qa[kk][2 + half];
-          qa[kk][half] = pack_f16x2(bf16lo(a), bf16hi(a));
-          qa[kk][2 + half] = pack_f16x2(bf16lo(b2), bf16hi(b2));
+          const uint32_t w = live ? __ldg(reinterpret_cast<const uint32_t*>(
+                                          reinterpret_cast<const uint8_t*>(p.q) + qoff + 16 * kk))
+                                  : 0u;
+          lo = e4m3x2_to_f16x2((uint16_t)(w & 0xffffu));
+          hi = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+        } else if (live) {
+          const uint2 w = __ldg(reinterpret_cast<const uint2*>(p.q + qoff + 16 * kk));
+          lo = pack_f16x2(bf16lo(w.x), bf16hi(w.x));
+          hi = pack_f16x2(bf16lo(w.y), bf16hi(w.y));
         }
+        qa[kk][half] = lo;
+        qa[kk][2 + half] = hi;
       }
     }
   }
@@ -260,37 +240,43 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
   for (int step = 0; step < n_steps; ++step) {
-    const int st = step % (FP8KV ? kRing16 : kStages);
-    const uint8_t* stage = ring + st * kStageBytes;
+    const int st = step % kStages;
+    const uint8_t* stage = ring + st * (FP8KV ? kStageBytes8 : kStageBytes);
     const int nvalid = min(kStepTok, n - step * kStepTok);
 
     // ---- partial logits over this warp's 144 dims: n-tile nt = tokens 8nt + g
     float s[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    if constexpr (FP8KV) {
+      // token 8nt + g, dims 16kk + 4c .. + 3 of the warp's 144: one word
 #pragma unroll
-    for (int kk = 0; kk < kKSteps; ++kk) {
-      uint32_t kb[4];
-      ldsm_x4(stage + k_off + 32 * kk, kb);
-      mma16816<FP8KV>(s[0], qa[kk], kb[0], kb[1]);
-      mma16816<FP8KV>(s[1], qa[kk], kb[2], kb[3]);
+      for (int nt = 0; nt < 2; ++nt) {
+        const uint8_t* krow = stage + (8 * nt + g) * kRowPitch8 + kKQuarter * warp + 4 * c;
+#pragma unroll
+        for (int kk = 0; kk < kKSteps; ++kk) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(krow + 16 * kk);
+          mma16816<true>(s[nt], qa[kk], e4m3x2_to_f16x2((uint16_t)(w & 0xffffu)),
+                         e4m3x2_to_f16x2((uint16_t)(w >> 16)));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < kKSteps; ++kk) {
+        uint32_t kb[4];
+        ldsm_x4(stage + k_off + 32 * kk, kb);
+        mma16816<false>(s[0], qa[kk], kb[0], kb[1]);
+        mma16816<false>(s[1], qa[kk], kb[2], kb[3]);
+      }
     }
     float* xw = xchg + (step & 1) * kXchgFloats;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) xw[(warp * 8 + 4 * nt + e) * 32 + lane] = s[nt][e];
-    if constexpr (FP8KV) {
-      // the next step's rows have landed in the staging ring (this thread's
-      // part; steps complete in order); each thread converts exactly the
-      // chunks it copied, and the barrier below publishes them
-      cp_async_wait<kStages - 2>();
-      if (step + 1 < n_steps) convert(step + 1);
-    } else {
-      // the next step's rows have landed (this thread's part; steps complete
-      // in order), and the one barrier of the step makes them everyone's
-      cp_async_wait<kStages - 3>();
-    }
+    // the next step's rows have landed (this thread's part; steps complete
+    // in order), and the one barrier of the step makes them everyone's
+    cp_async_wait<kStages - 3>();
     __syncthreads();
     // the same sum, in the same order, in every warp
 #pragma unroll
@@ -303,13 +289,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
         const int t = 8 * nt + 2 * c + (e & 1);
         s[nt][e] = t < nvalid ? v * scale2 : -INFINITY;
       }
-    // the stage of the previous step is free in every warp now (FP8: the
-    // staging of this step was converted before the previous barrier)
-    if constexpr (FP8KV) {
-      gather(step + kStages);
-    } else {
-      if (step >= 1) gather(step - 1 + kStages);
-    }
+    // the stage of the previous step is free in every warp now
+    if (step >= 1) gather(step - 1 + kStages);
 
     // ---- online softmax (rows g and g+8), lazy rescaling
     float mx[2];
@@ -371,14 +352,39 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
       keep_lo = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
       keep_hi = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
     }
+    if constexpr (FP8KV) {
+      // tokens 2c, 2c+1, 2c+8, 2c+9: value dims 16g .. 16g + 15 of the
+      // warp's 128, 16 bytes each; n-tile j takes byte j of each (column g
+      // of n-tile j = value dim 16g + j), the two tokens of a k-slot pair
+      // joined by a byte permute
+      uint32_t vw[4][4];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      uint32_t vb[4];
-      ldsm_x4_t(stage + v_off + 32 * jj, vb);
-      const uint32_t b0[2] = {vb[0] & keep_lo, vb[2] & keep_lo};
-      const uint32_t b1[2] = {vb[1] & keep_hi, vb[3] & keep_hi};
-      mma16816<FP8KV>(o[2 * jj], pa, b0[0], b1[0]);
-      mma16816<FP8KV>(o[2 * jj + 1], pa, b0[1], b1[1]);
+      for (int a = 0; a < 4; ++a) {
+        const int t = 2 * c + (a & 1) + 8 * (a >> 1);
+        const uint4 v = lds128(stage + t * kRowPitch8 + kVQuarter * warp + 16 * g);
+        vw[a][0] = v.x; vw[a][1] = v.y; vw[a][2] = v.z; vw[a][3] = v.w;
+      }
+#pragma unroll
+      for (int j2 = 0; j2 < 8; ++j2) {  // n-tiles 2 j2, 2 j2 + 1
+        const int wi = j2 >> 1, by = 2 * (j2 & 1);
+        const uint32_t sel = (uint32_t)(by | ((4 + by) << 4) | ((by + 1) << 8) | ((5 + by) << 12));
+        const uint32_t lo = prmt(vw[0][wi], vw[1][wi], sel);  // tokens 2c, 2c+1
+        const uint32_t hi = prmt(vw[2][wi], vw[3][wi], sel);  // tokens 2c+8, 2c+9
+        mma16816<true>(o[2 * j2], pa, e4m3x2_to_f16x2((uint16_t)(lo & 0xffffu)) & keep_lo,
+                       e4m3x2_to_f16x2((uint16_t)(hi & 0xffffu)) & keep_hi);
+        mma16816<true>(o[2 * j2 + 1], pa, e4m3x2_to_f16x2((uint16_t)(lo >> 16)) & keep_lo,
+                       e4m3x2_to_f16x2((uint16_t)(hi >> 16)) & keep_hi);
+      }
+    } else {
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        uint32_t vb[4];
+        ldsm_x4_t(stage + v_off + 32 * jj, vb);
+        const uint32_t b0[2] = {vb[0] & keep_lo, vb[2] & keep_lo};
+        const uint32_t b1[2] = {vb[1] & keep_hi, vb[3] & keep_hi};
+        mma16816<false>(o[2 * jj], pa, b0[0], b1[0]);
+        mma16816<false>(o[2 * jj + 1], pa, b0[1], b1[1]);
+      }
     }
   }
 
@@ -401,9 +407,16 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_kernel(const MlaLaunch
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        // c0,c1 (half 0) / c2,c3 (half 1): dims 8j + 2c, +1 of this warp's 128
-        ph[4 + kVQuarter * warp + 8 * j + 2 * c] = acc[j][2 * half];
-        ph[4 + kVQuarter * warp + 8 * j + 2 * c + 1] = acc[j][2 * half + 1];
+        // c0,c1 (half 0) / c2,c3 (half 1): columns 2c, 2c+1 of n-tile j, i.e.
+        // dims 8j + 2c, +1 of this warp's 128 (bf16 cache) or 16 (2c) + j,
+        // 16 (2c + 1) + j (e4m3 cache)
+        if constexpr (FP8KV) {
+          ph[4 + kVQuarter * warp + 32 * c + j] = acc[j][2 * half];
+          ph[4 + kVQuarter * warp + 32 * c + 16 + j] = acc[j][2 * half + 1];
+        } else {
+          ph[4 + kVQuarter * warp + 8 * j + 2 * c] = acc[j][2 * half];
+          ph[4 + kVQuarter * warp + 8 * j + 2 * c + 1] = acc[j][2 * half + 1];
+        }
       }
     }
   };
