@@ -643,13 +643,15 @@ __global__ void __launch_bounds__(kPaThreads, 1)
 
 // ------------------------------------------------------------------ merge
 
-// One CTA per row: thread t owns head t / 8, dims 16 (t % 8) .. +16.  Rows
-// not routed to the prefill path leave at once.
+// One CTA per row: thread t owns head t % 16 and the 8-dim chunks t / 16
+// and t / 16 + 8, so that a warp reads 512 contiguous bytes of a partial
+// ([16 dim chunks][16 heads][8 dims]) per load.  Rows not routed to the
+// prefill path leave at once.
 template <bool SCALAR>
 __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(const PrefillLaunch p) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int r = blockIdx.x, tid = threadIdx.x;
-  const int head = tid >> 3, d0 = 16 * (tid & 7);
+  const int head = tid & 15, ca = tid >> 4;  // chunks ca and ca + 8
   float sink2 = -INFINITY, vs = 1.f;
   if (p.sinks && head < p.num_heads) sink2 = __ldg(p.sinks + head) * kLog2e;
   if constexpr (SCALAR) vs = __ldg(p.v_scale);
@@ -676,13 +678,12 @@ __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(const Pref
       ml[u] = make_float2(-INFINITY, 0.f);
       va[u] = vb[u] = make_uint4(0u, 0u, 0u, 0u);
       if (i0 + u < nsel) {
-        // [16 dim chunks][16 heads][8 dims]: dims d0.. are chunks d0 / 8, d0 / 8 + 1
         const long long slot = pbase + i0 + u;
         ml[u] = p.part_ml[slot * kHeadSlots + head];
         const uint4* src = reinterpret_cast<const uint4*>(p.part_o + slot * kHeadSlots * kHeadDim) +
-                           (d0 / 8) * kHeadSlots + head;
+                           ca * kHeadSlots + head;
         va[u] = src[0];
-        vb[u] = src[kHeadSlots];
+        vb[u] = src[8 * kHeadSlots];
       }
     }
     float mb = M;
@@ -712,10 +713,10 @@ __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(const Pref
   uint32_t packed[8];
 #pragma unroll
   for (int x = 0; x < 8; ++x) packed[x] = pack_bf16x2(acc[2 * x] * inv, acc[2 * x + 1] * inv);
-  uint4* o = reinterpret_cast<uint4*>(p.out + ((long long)r * p.num_heads + head) * kHeadDim + d0);
-  o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  if ((tid & 7) == 0)
+  uint4* o = reinterpret_cast<uint4*>(p.out + ((long long)r * p.num_heads + head) * kHeadDim);
+  o[ca] = make_uint4(packed[0], packed[1], packed[2], packed[3]);      // dims 8 ca ..
+  o[ca + 8] = make_uint4(packed[4], packed[5], packed[6], packed[7]);  // dims 64 + 8 ca ..
+  if (ca == 0)
     p.lse[(long long)r * p.num_heads + head] =
         (M == -INFINITY || L <= 0.f) ? -INFINITY : (M + log2f(L)) * kLn2;
 }
