@@ -24,11 +24,15 @@
 //           so the MMAs read only the K tile from shared memory (with both
 //           operands there, M128 N128 MMAs plus the tile copies saturate
 //           the shared-memory port);
-//   warp 1  allocates 512 TMEM columns (three 128-column accumulators,
-//           two query tiles); one thread issues the MMAs and commits;
-//   warps 2-9 epilogue, two groups of four on alternate items: tcgen05.ld
-//           of 32 rows x 128 columns each, masked max, score store;
-//           releases the accumulator.
+//   warp 1  allocates 512 TMEM columns (two 128-column accumulators, two
+//           query tiles); one thread of warp 1 and one of warp 14 issue the
+//           MMAs of alternate items and commit (one issuing thread left the
+//           tensor pipe idle while it waited and did its per-item
+//           bookkeeping);
+//   warps 2-9 epilogue, two groups of four on alternate items (group g
+//           drains the accumulator issuer g fills): tcgen05.ld of 32 rows x
+//           128 columns each, masked max, score store; releases the
+//           accumulator.
 // Every wait is bounded; on expiry the kernel records MSA_DEV_TIMEOUT, stops
 // issuing work and still frees its TMEM.
 #include "tcgen05.cuh"
@@ -37,10 +41,23 @@ namespace msa {
 namespace {
 
 constexpr int kTcStages = 4;
-constexpr int kTcThreads = 448;  // 14 warps: copies, MMA, 2 x 4 epilogue, 4 query loaders
+// threads issuing the MMAs: with two, items alternate between them, so one
+// issues while the other waits and does its per-item bookkeeping
+#ifndef MSA_TC_ISSUERS
+#define MSA_TC_ISSUERS 2
+#endif
+constexpr int kIssuers = MSA_TC_ISSUERS;
+static_assert(kIssuers == 1 || kIssuers == 2, "one or two MMA issuers");
+// warps: copies, MMA, 2 x 4 epilogue, 4 query loaders, the second MMA issuer
+constexpr int kTcThreads = 32 * (13 + kIssuers);
+constexpr int kIssuerWarp2 = 14;
 constexpr int kTileRows = 128;
-constexpr int kAccBufs = 3;      // 128-column fp32 accumulators in TMEM (columns 0 .. 383)
-constexpr uint32_t kTmemA = 384; // then two query tiles (A operands), 64 columns each
+// 128-column fp32 accumulators in TMEM: with two issuers each issuer and its
+// epilogue group own one (an issuer never waits on a buffer the other fills)
+constexpr int kAccBufs = kIssuers == 2 ? 2 : 3;
+constexpr uint32_t kTmemA = 128 * kAccBufs;  // then two query tiles (A operands), 64 columns each
+static_assert(kTcStages % kIssuers == 0 && kAccBufs % kIssuers == 0,
+              "each ring stage and accumulator belongs to one issuer");
 constexpr uint32_t kTmemCols = 512;
 
 template <int DI>
@@ -147,7 +164,7 @@ struct Cursor {
   }
 };
 
-// (14 warps: four share a sub-partition's 16K registers, so at most 128
+// (15 warps: at most four share a sub-partition's 16K registers, so at most 128
 // registers a thread; one CTA per SM)
 template <int DI>
 __global__ void __maxnreg__(128)
@@ -182,7 +199,7 @@ __global__ void __maxnreg__(128)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&a_full[i], 4);  // the four query-loader warps
-      mbar_init(&a_empty[i], 1);
+      mbar_init(&a_empty[i], kIssuers);  // each issuer commits once per row tile
     }
     for (int i = 0; i < kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -274,8 +291,13 @@ __global__ void __maxnreg__(128)
           }
         }
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------- MMA issuer: D = Q_tile (TMEM) x K_block^T (shared)
+    } else if ((warp == 1 || (kIssuers == 2 && warp == kIssuerWarp2)) && lane == 0) {
+      // ---------------- MMA issuer(s): D = Q_tile (TMEM) x K_block^T (shared).
+      // Issuer ii takes items j = ii mod kIssuers: ring stages and
+      // accumulators are then each used by one issuer, in order.  Both walk
+      // every row tile: each waits for its queries and commits once to its
+      // release (after its own MMAs of the tile, if any).
+      const int ii = warp == 1 ? 0 : 1;
       Cursor cur;
       cur.seek(b, prefix, R, i0);
       int a_key_q = -1, a_key_t = -1, a_seq = 0, abuf = 0;
@@ -290,34 +312,36 @@ __global__ void __maxnreg__(128)
           a_key_t = cur.tile;
           ++a_seq;
         }
-        const int s = j % kTcStages, buf = j % kAccBufs;
-        if (j >= kAccBufs && !mbar_wait(&acc_empty[buf], ((j / kAccBufs) - 1) & 1)) {
-          misc[1] = 1;
-          break;
-        }
-        if (!mbar_wait(&b_full[s], (j / kTcStages) & 1)) {
-          misc[1] = 1;
-          break;
-        }
-        fence_after();
-        if (stage_valid[s]) {
-          const uint32_t b_base = smem_u32(smem + C::kB + s * C::kTileBytes);
-          const uint32_t a_tm = tmem + kTmemA + abuf * 64u;
-#pragma unroll
-          for (int kk = 0; kk < C::kKSteps; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-            tc::mma_ts(tmem + buf * 128u, a_tm + kk * 8, tc::desc_kmajor_sw128(b_base + off),
-                       kIdesc, kk > 0 ? 1u : 0u);
+        if (j % kIssuers == ii) {
+          const int s = j % kTcStages, buf = j % kAccBufs;
+          if (j >= kAccBufs && !mbar_wait(&acc_empty[buf], ((j / kAccBufs) - 1) & 1)) {
+            misc[1] = 1;
+            break;
           }
+          if (!mbar_wait(&b_full[s], (j / kTcStages) & 1)) {
+            misc[1] = 1;
+            break;
+          }
+          fence_after();
+          if (stage_valid[s]) {
+            const uint32_t b_base = smem_u32(smem + C::kB + s * C::kTileBytes);
+            const uint32_t a_tm = tmem + kTmemA + abuf * 64u;
+#pragma unroll
+            for (int kk = 0; kk < C::kKSteps; ++kk) {
+              const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+              tc::mma_ts(tmem + buf * 128u, a_tm + kk * 8, tc::desc_kmajor_sw128(b_base + off),
+                         kIdesc, kk > 0 ? 1u : 0u);
+            }
+          }
+          commit(&b_empty[s]);
+          commit(&acc_full[buf]);
         }
-        commit(&b_empty[s]);
-        commit(&acc_full[buf]);
         Cursor nx = cur;
         nx.next(b, prefix, R);
         if (j == n_items - 1 || nx.q != cur.q || nx.tile != cur.tile) commit(&a_empty[abuf]);
         cur = nx;
       }
-    } else if (warp >= 10) {
+    } else if (warp >= 10 && warp < 14) {
       // ---------------- query loaders: each row tile of the CTA's items into
       // TMEM (lane = query row, column c = dims 2c, 2c+1), double-buffered;
       // rows past the request's end are zero
@@ -359,7 +383,7 @@ __global__ void __maxnreg__(128)
         }
         cur.next(b, prefix, R);
       }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < 10) {
       // ---------------- epilogue: two groups of four warps take alternate
       // items (accumulator j % 4); warp w reads TMEM lanes 32 (w % 4) .. +31
       // = 32 query rows, each reduced to its causal-masked max over the 128
