@@ -29,10 +29,10 @@
 //           MMAs of alternate items and commit (one issuing thread left the
 //           tensor pipe idle while it waited and did its per-item
 //           bookkeeping);
-//   warps 2-9 epilogue, two groups of four on alternate items (group g
-//           drains the accumulator issuer g fills): tcgen05.ld of 32 rows x
-//           128 columns each, masked max, score store; releases the
-//           accumulator.
+//   warps 2-9 epilogue: every item by all eight, the two warps of a TMEM
+//           lane quarter taking 64 columns each (tcgen05.ld, masked max),
+//           one of them storing the 32 rows' scores; each releases the
+//           accumulator once it holds its columns in registers.
 // Every wait is bounded; on expiry the kernel records MSA_DEV_TIMEOUT, stops
 // issuing work and still frees its TMEM.
 #include "tcgen05.cuh"
@@ -52,8 +52,14 @@ static_assert(kIssuers == 1 || kIssuers == 2, "one or two MMA issuers");
 constexpr int kTcThreads = 32 * (13 + kIssuers);
 constexpr int kIssuerWarp2 = 14;
 constexpr int kTileRows = 128;
-// 128-column fp32 accumulators in TMEM: with two issuers each issuer and its
-// epilogue group own one (an issuer never waits on a buffer the other fills)
+// epilogue: every item drained by all eight warps, two per TMEM lane quarter
+// taking 64 columns each (1), or by one group of four on alternate items (0)
+#ifndef MSA_TC_EPI_SPLIT
+#define MSA_TC_EPI_SPLIT 1
+#endif
+constexpr bool kEpiSplit = MSA_TC_EPI_SPLIT != 0;
+// 128-column fp32 accumulators in TMEM: with two issuers each owns one
+// (three shared ones, safe with the in-order epilogue, measured slower)
 constexpr int kAccBufs = kIssuers == 2 ? 2 : 3;
 constexpr uint32_t kTmemA = 128 * kAccBufs;  // then two query tiles (A operands), 64 columns each
 static_assert(kTcStages % kIssuers == 0 && kAccBufs % kIssuers == 0,
@@ -73,10 +79,48 @@ struct TcCfg {
   // b_full / b_empty [kTcStages], a_full / a_empty [2], acc_full / acc_empty [kAccBufs]
   static constexpr int kNumBars = 2 * kTcStages + 4 + 2 * kAccBufs;
   static constexpr int kMisc = kBars + kNumBars * 8;
-  static constexpr int kPrefix = kMisc + 64;
+  static constexpr int kRed = kMisc + 64;  // [2][128] floats: the split epilogue's hand-off
+  static constexpr int kPrefix = kRed + 2 * kTileRows * 4;
   static_assert(8 + kTcStages <= 16, "misc area holds 16 ints");
   static size_t bytes(int num_reqs) { return 1024 + kPrefix + (size_t)(num_reqs + 1) * 4; }
 };
+
+// Max over 64 accumulator columns at ta (two loads in flight), columns
+// c <= last only when MASKED.
+template <bool MASKED>
+__device__ __forceinline__ float row_max64(uint32_t ta, int last) {
+  uint32_t ra[32], rb[32];
+  tc::tmem_ld32_issue(ta, ra);
+  tc::tmem_ld32_issue(ta + 32, rb);
+  tc::tmem_wait_ld(ra);
+  tc::tmem_wait_ld(rb);
+  float g8[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) g8[x] = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (!MASKED || i <= last) g8[i & 7] = fmaxf(g8[i & 7], __uint_as_float(ra[i]));
+    if (!MASKED || 32 + i <= last) g8[i & 7] = fmaxf(g8[i & 7], __uint_as_float(rb[i]));
+  }
+  return fmaxf(fmaxf(fmaxf(g8[0], g8[1]), fmaxf(g8[2], g8[3])),
+               fmaxf(fmaxf(g8[4], g8[5]), fmaxf(g8[6], g8[7])));
+}
+
+// The two epilogue warps of one TMEM lane quarter (named barrier 1 + quarter,
+// 64 threads): AND of a predicate over both, and a plain rendezvous.
+__device__ __forceinline__ bool pair_and(bool v, int id) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, 64, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
 
 using tc::commit;
 using tc::fence_after;
@@ -203,7 +247,7 @@ __global__ void __maxnreg__(128)
     }
     for (int i = 0; i < kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);  // the four warps of an epilogue group
+      mbar_init(&acc_empty[i], kEpiSplit ? 8 : 4);  // the epilogue warps draining it
     }
     fence_barrier_init();
   }
@@ -383,7 +427,56 @@ __global__ void __maxnreg__(128)
         }
         cur.next(b, prefix, R);
       }
-    } else if (warp >= 2 && warp < 10) {
+    } else if (kEpiSplit && warp >= 2 && warp < 10) {
+      // ---------------- epilogue: every item by all eight warps.  The two
+      // warps of lane quarter w % 4 (= 32 query rows) take columns 0..63 and
+      // 64..127 of the accumulator; the second hands its 32 maxima to the
+      // first through shared memory, which stores the scores.  Both decide
+      // together whether to go on (a timed-out wait ends both), so neither
+      // is left at their barrier.
+      const int half = (warp - 2) >> 2, quarter = warp & 3, bar_id = 1 + quarter;
+      const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+      float* red = reinterpret_cast<float*>(smem + C::kRed);  // maxima of the second half
+      Cursor cur;
+      cur.seek(b, prefix, R, i0);
+      int page = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
+      for (int j = 0; j < n_items; ++j) {
+        const int buf = j % kAccBufs;
+        Cursor nx = cur;
+        int page_nx = 0;
+        if (j + 1 < n_items) {
+          nx.next(b, prefix, R);
+          page_nx = b.block_table[(long long)nx.q * b.bt_stride + nx.blk];
+        }
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (j / kAccBufs) & 1));
+        if (!pair_and(ok, bar_id)) {
+          misc[1] = 1;
+          break;
+        }
+        fence_after();
+        const int m = quarter * 32 + lane;
+        const int row_in_req = cur.tile * kTileRows + m;
+        const int pos = cur.ctx + row_in_req;
+        const bool page_ok = page >= 0 && page < b.num_pages;
+        const int last = pos - cur.blk * kBlock - 64 * half;  // visible columns of this half
+        const uint32_t ta = tmem + lanes + buf * 128u + 64u * half;
+        float best = __all_sync(0xffffffffu, last >= 63) ? row_max64<false>(ta, last)
+                                                         : row_max64<true>(ta, last);
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        if (half == 1) red[(j & 1) * kTileRows + m] = best;
+        pair_sync(bar_id);
+        if (half == 0) {
+          best = fmaxf(best, red[(j & 1) * kTileRows + m]);
+          if (row_in_req < cur.qlen && last >= 0)
+            p.scores[(long long)(cur.q0 + row_in_req) * p.score_stride + cur.blk] =
+                page_ok ? best : -INFINITY;
+        }
+        cur = nx;
+        page = page_nx;
+      }
+    } else if (!kEpiSplit && warp >= 2 && warp < 10) {
       // ---------------- epilogue: two groups of four warps take alternate
       // items (accumulator j % 4); warp w reads TMEM lanes 32 (w % 4) .. +31
       // = 32 query rows, each reduced to its causal-masked max over the 128
