@@ -85,15 +85,11 @@ struct TcCfg {
   static size_t bytes(int num_reqs) { return 1024 + kPrefix + (size_t)(num_reqs + 1) * 4; }
 };
 
-// Max over 64 accumulator columns at ta (two loads in flight), columns
-// c <= last only when MASKED.
+// Max over 64 accumulator columns loaded into ra (0..31) and rb (32..63),
+// columns c <= last only when MASKED.
 template <bool MASKED>
-__device__ __forceinline__ float row_max64(uint32_t ta, int last) {
-  uint32_t ra[32], rb[32];
-  tc::tmem_ld32_issue(ta, ra);
-  tc::tmem_ld32_issue(ta + 32, rb);
-  tc::tmem_wait_ld(ra);
-  tc::tmem_wait_ld(rb);
+__device__ __forceinline__ float row_max64(const uint32_t (&ra)[32], const uint32_t (&rb)[32],
+                                           int last) {
   float g8[8];
 #pragma unroll
   for (int x = 0; x < 8; ++x) g8[x] = -INFINITY;
@@ -460,11 +456,17 @@ __global__ void __maxnreg__(128)
         const bool page_ok = page >= 0 && page < b.num_pages;
         const int last = pos - cur.blk * kBlock - 64 * half;  // visible columns of this half
         const uint32_t ta = tmem + lanes + buf * 128u + 64u * half;
-        float best = __all_sync(0xffffffffu, last >= 63) ? row_max64<false>(ta, last)
-                                                         : row_max64<true>(ta, last);
+        uint32_t ra[32], rb[32];
+        tc::tmem_ld32_issue(ta, ra);
+        tc::tmem_ld32_issue(ta + 32, rb);
+        tc::tmem_wait_ld(ra);
+        tc::tmem_wait_ld(rb);
+        // the columns are in registers: the accumulator is free again
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        float best = __all_sync(0xffffffffu, last >= 63) ? row_max64<false>(ra, rb, last)
+                                                         : row_max64<true>(ra, rb, last);
         if (half == 1) red[(j & 1) * kTileRows + m] = best;
         pair_sync(bar_id);
         if (half == 0) {

@@ -34,11 +34,11 @@
 //   merge:     per row, the k partials are combined through their LSEs,
 //              the sink joins the denominator, O and the natural-log LSE
 //              are written.
-// CTA roles in the attention kernel: warp 0 issues the tensor copies (all
-// lanes gather query rows), warp 1 allocates TMEM and one of its threads
-// issues the MMAs, warps 2-5 and 6-9 are two softmax / epilogue groups that
-// take alternate chunks (S, P and O are double-buffered in TMEM: 512
-// columns).  Every wait is bounded; on expiry the kernel records
+// CTA roles in the attention kernel: warp 0 issues the tensor copies (its
+// lanes and warp 15's gather the chunks' query rows), warp 1 allocates TMEM and one of its threads
+// issues the S MMAs, one thread of warp 14 the P V MMAs, warps 2-5 and 6-9
+// are two softmax groups that take alternate chunks, warps 10-13 store every
+// chunk's O (S, P and O are double-buffered in TMEM: 512 columns).  Every wait is bounded; on expiry the kernel records
 // MSA_DEV_TIMEOUT, stops and still frees its TMEM.
 #include <string.h>
 
@@ -49,7 +49,15 @@ namespace {
 
 constexpr int kChunkRows = 8;  // query rows per chunk (x 16 head slots = the MMA's M = 128)
 constexpr int kHeadSlots = 16;
-constexpr int kPaThreads = 320;
+// warps: copies, S issue, two softmax groups of four, four O-epilogue
+// warps, P V issue, query gathers
+constexpr int kPaThreads = 512;
+constexpr int kPvWarp = 14;
+// A chunk's query rows are gathered by two warps, rows 0-3 by warp 0 and
+// rows 4-7 by warp 15: each tensor copy costs its warp ~100 cycles to issue,
+// and sixteen per chunk from one warp bounded the kernel.
+constexpr int kGatherWarp2 = 15;
+constexpr int kGatherRowsA = 4;
 constexpr int kQStages = 3;
 constexpr int kKvStages = 2;
 constexpr int kHalf = 128 * 128;     // 128 rows x 128 B: one swizzle-atom column of a tile
@@ -211,27 +219,25 @@ struct Cursor {
   __device__ __forceinline__ int blk() const { return rec.w; }
 };
 
-// 2^x on the multi-function unit (x <= 0 here; tiny results flush to zero)
-__device__ __forceinline__ float ex2_mufu(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+// p = 2^x of two logits at once on the multi-function unit: x rounded to
+// f16 (x <= 0; the rounding moves p by at most ~2^-11 relative per unit of
+// |x|, so a term's absolute error stays below 2e-4 of the row's largest),
+// 2^x in f16, widened back for the sum and the bf16 pack
+__device__ __forceinline__ void ex2_pair_f16(float x0, float x1, float& p0, float& p1) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
+  asm("ex2.approx.f16x2 %0, %0;" : "+r"(h));
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+      : "=f"(p0), "=f"(p1)
+      : "r"(h));
 }
 
-// 2^x for x <= 0 on the FMA pipe, to share the softmax's exponentials with
-// the multi-function unit (Cody-Waite range reduction): x = j + f with j =
-// round(x) -- adding 1.5 * 2^23 leaves round(x) in the low mantissa bits --
-// and f in [-1/2, 1/2]; 2^f from a degree-3 polynomial fitted for minimal
-// relative error on that interval (7.5e-5, below half a bf16 ulp); 2^j goes
-// into the exponent field (the shift drops the constant's bits).  x is
-// clamped to -125 so that the exponent stays normal.
-__device__ __forceinline__ float ex2_poly(float x) {
-  x = fmaxf(x, -125.f);
-  const float t = x + 12582912.f;
-  const float f = x - (t - 12582912.f);
-  const float p = fmaf(fmaf(fmaf(0.0551716685f, f, 0.2426111400f), f, 0.6932609677f), f,
-                       0.9999280572f);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+// max of three (one instruction)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // all lanes wait; the result is the same on every lane
@@ -266,13 +272,14 @@ __device__ __forceinline__ float max32(const uint32_t (&r)[32], float acc, int b
 #pragma unroll
   for (int x = 0; x < 8; ++x) g8[x] = acc;
 #pragma unroll
-  for (int t = 0; t < 32; ++t) {
-    float v = NEG ? -__uint_as_float(r[t]) : __uint_as_float(r[t]);
-    if (MASKED && base + t >= valid) v = -INFINITY;
-    g8[t & 7] = fmaxf(g8[t & 7], v);
+  for (int t = 0; t < 32; t += 2) {
+    float v0 = NEG ? -__uint_as_float(r[t]) : __uint_as_float(r[t]);
+    float v1 = NEG ? -__uint_as_float(r[t + 1]) : __uint_as_float(r[t + 1]);
+    if (MASKED && base + t >= valid) v0 = -INFINITY;
+    if (MASKED && base + t + 1 >= valid) v1 = -INFINITY;
+    g8[(t >> 1) & 7] = fmax3(g8[(t >> 1) & 7], v0, v1);
   }
-  return fmaxf(fmaxf(fmaxf(g8[0], g8[1]), fmaxf(g8[2], g8[3])),
-               fmaxf(fmaxf(g8[4], g8[5]), fmaxf(g8[6], g8[7])));
+  return fmaxf(fmax3(g8[0], g8[1], g8[2]), fmax3(g8[3], g8[4], fmax3(g8[5], g8[6], g8[7])));
 }
 
 // max over the 128 raw scores (of their negations when NEG), loads in flight
@@ -293,9 +300,8 @@ __device__ __forceinline__ float row_max(uint32_t sa, int valid) {
   return g;
 }
 
-// p = 2^(s * scale2 - m) of 32 columns -- three of every four on the
-// multi-function unit, the fourth on the FMA pipe -- packed as bf16 pairs
-// into w; returns their sum
+// p = 2^(s * scale2 - m) of 32 columns, two at a time in f16 on the
+// multi-function unit, packed as bf16 pairs into w; returns their sum
 template <bool MASKED>
 __device__ __forceinline__ float exp32(const uint32_t (&r)[32], float scale2, float m,
                                        uint32_t (&w)[16], int base, int valid) {
@@ -304,9 +310,9 @@ __device__ __forceinline__ float exp32(const uint32_t (&r)[32], float scale2, fl
   for (int x = 0; x < 8; ++x) l8[x] = 0.f;
 #pragma unroll
   for (int t = 0; t < 32; t += 2) {
-    float p0 = ex2_mufu(fmaf(__uint_as_float(r[t]), scale2, -m));
-    const float x1 = fmaf(__uint_as_float(r[t + 1]), scale2, -m);
-    float p1 = (t & 2) ? ex2_poly(x1) : ex2_mufu(x1);
+    float p0, p1;
+    ex2_pair_f16(fmaf(__uint_as_float(r[t]), scale2, -m), fmaf(__uint_as_float(r[t + 1]), scale2, -m),
+                 p0, p1);
     if (MASKED) {
       p0 = base + t < valid ? p0 : 0.f;
       p1 = base + t + 1 < valid ? p1 : 0.f;
@@ -349,10 +355,10 @@ __device__ __forceinline__ float2 row_softmax(uint32_t sa, float scale2, int val
   return make_float2(m, row_exp<MASKED>(sa, scale2, m, valid));
 }
 
-// (10 warps: three share a sub-partition's 16K registers, so at most 168
-// registers a thread)
+// (16 warps: four share a sub-partition's 16K registers, so at most 128
+// registers a thread; one CTA per SM by its shared memory)
 template <bool SCALAR>
-__global__ void __launch_bounds__(kPaThreads, 1)
+__global__ void __maxnreg__(128)
     prefill_attn_kernel(const PrefillLaunch p, const __grid_constant__ CUtensorMap qmap,
                         const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
@@ -382,14 +388,14 @@ __global__ void __launch_bounds__(kPaThreads, 1)
       mbar_init(&kv_empty[s], 1);
     }
     for (int s = 0; s < kQStages; ++s) {
-      mbar_init(&q_full[s], 1);
+      mbar_init(&q_full[s], 2);  // the two gathering warps
       mbar_init(&q_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 4);  // the four warps of a softmax group
       mbar_init(&o_full[s], 1);
-      mbar_init(&o_empty[s], 4);
+      mbar_init(&o_empty[s], 4);  // the four O-epilogue warps
     }
     mbar_init(kv_fill, 1);
     fence_barrier_init();
@@ -468,9 +474,10 @@ __global__ void __launch_bounds__(kPaThreads, 1)
           break;
         }
         const int n = cur.rows();
-        if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], (uint32_t)(n * hq * 256));
+        const int na = min(n, kGatherRowsA);  // this warp's rows 0 .. na - 1
+        if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], (uint32_t)(na * hq * 256));
         __syncwarp();
-        if (lane < n) {
+        if (lane < na) {
           // (an entry outside the batch, impossible from the top-k kernel,
           // reads row 0 and is never written back)
           const int er = e_cur >> 8;
@@ -482,74 +489,115 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         cur = nxt;
         e_cur = e_nxt;
       }
+    } else if (warp == kGatherWarp2) {
+      // ---------------- query rows kGatherRowsA .. 7 of every chunk
+      Cursor cur;
+      cur.n_items = n_items;
+      cur.seek(p, c0);
+      const int slot = kGatherRowsA + lane;
+      int e_cur = slot < cur.rows() ? p.pf_lists[cur.list_base() + slot] : 0;
+      for (int j = 0; j < nj; ++j) {
+        Cursor nxt = cur;
+        int e_nxt = 0;
+        if (j + 1 < nj) {
+          nxt.next(p);
+          e_nxt = slot < nxt.rows() ? p.pf_lists[nxt.list_base() + slot] : 0;
+        }
+        const int qs = j % kQStages;
+        if (j >= kQStages && !warp_wait(&q_empty[qs], ((j / kQStages) - 1) & 1)) {
+          misc[1] = 1;
+          break;
+        }
+        const int nb = max(cur.rows() - kGatherRowsA, 0);
+        if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], (uint32_t)(nb * hq * 256));
+        __syncwarp();
+        if (lane < nb) {
+          const int er = e_cur >> 8;
+          const int r = er < p.batch.num_rows ? er : 0;
+          uint8_t* qd = smem + kSmQ + qs * kTile + slot * (kHeadSlots * 128);
+          tma_load_2d(qd, &qmap, 0, r * hq, &q_full[qs]);
+          tma_load_2d(qd + kHalf, &qmap, 64, r * hq, &q_full[qs]);
+        }
+        cur = nxt;
+        e_cur = e_nxt;
+      }
     } else if (warp == 1) {
-      // ---------------- MMA issue (one thread).  Buffers: S / P of chunk j
-      // in TMEM columns 128 (j & 1), O in 256 + 128 (j & 1).  S(j) may
-      // overwrite its buffer once P V of chunk j - 2 has completed (o_full);
-      // P V of chunk j may overwrite O once the epilogue of chunk j - 2 has
-      // read it (o_empty).  Issue order: S(j), then P V(j - 1), so that the
-      // tensor pipe computes the next scores while a softmax group works
-      // (issuing P V first whenever its P is ready measured slower: the
-      // other group then waits for its scores).
+      // ---------------- S = Q K^T issue (one thread).  S / P of chunk j live
+      // in TMEM columns 128 (j & 1); S(j) may overwrite its buffer once P V
+      // of chunk j - 2 has completed (o_full).  (One thread issuing both
+      // products was the kernel's bound: ~100 cycles per MMA instruction.)
       if (lane == 0) {
         Cursor cur;
         cur.n_items = n_items;
         cur.seek(p, c0);
-        int kv_seq = 0, cur_kvs = 0, prev_kvs = 0;
-        bool prev_last = false, ok = true;
-        for (int j = 0; j <= nj && ok; ++j) {
-          bool last = false;
-          if (j < nj) {
-            const int buf = j & 1, qs = j % kQStages;
-            if (j == 0 || cur.ci == 0) {
-              cur_kvs = kv_seq & 1;
-              ok = mbar_wait(&kv_full[cur_kvs], (kv_seq >> 1) & 1);
-              ++kv_seq;
-            }
-            ok = ok && mbar_wait(&q_full[qs], (j / kQStages) & 1);
-            ok = ok && (j < 2 || mbar_wait(&o_full[buf], ((j >> 1) - 1) & 1));
-            if (!ok) break;
-            tc::fence_after();
-            const uint32_t qa = smem_u32(smem + kSmQ + qs * kTile);
-            const uint32_t ka = smem_u32(smem + kSmK + cur_kvs * kTile);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-              tc::mma_ss(tmem + buf * 128, tc::desc_kmajor_sw128(qa + off),
-                         tc::desc_kmajor_sw128(ka + off), kIdescS, kk > 0 ? 1u : 0u);
-            }
-            tc::commit(&q_empty[qs]);
-            tc::commit(&s_full[buf]);
-            const int before = cur.it;
-            cur.next(p);
-            last = j == nj - 1 || cur.it != before;
+        int kv_seq = 0, cur_kvs = 0;
+        bool ok = true;
+        for (int j = 0; j < nj; ++j) {
+          const int buf = j & 1, qs = j % kQStages;
+          if (j == 0 || cur.ci == 0) {
+            cur_kvs = kv_seq & 1;
+            ok = mbar_wait(&kv_full[cur_kvs], (kv_seq >> 1) & 1);
+            ++kv_seq;
           }
-          if (j >= 1) {  // O = P V of the previous chunk
-            const int i = j - 1, pb = i & 1;
-            ok = mbar_wait(&p_full[pb], (i >> 1) & 1) &&
-                 (i < 2 || mbar_wait(&o_empty[pb], ((i >> 1) - 1) & 1));
-            if (!ok) break;
-            tc::fence_after();
-            const uint32_t va = smem_u32(smem + kSmV + prev_kvs * kTile);
+          ok = ok && mbar_wait(&q_full[qs], (j / kQStages) & 1);
+          ok = ok && (j < 2 || mbar_wait(&o_full[buf], ((j >> 1) - 1) & 1));
+          if (!ok) break;
+          tc::fence_after();
+          const uint32_t qa = smem_u32(smem + kSmQ + qs * kTile);
+          const uint32_t ka = smem_u32(smem + kSmK + cur_kvs * kTile);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              tc::mma_ts(tmem + 256 + pb * 128, tmem + pb * 128 + kk * 8,
-                         tc::desc_mnmajor_sw128(va + kk * 2048, kHalf), kIdescO,
-                         kk > 0 ? 1u : 0u);
-            tc::commit(&o_full[pb]);
-            if (prev_last) tc::commit(&kv_empty[prev_kvs]);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            tc::mma_ss(tmem + buf * 128, tc::desc_kmajor_sw128(qa + off),
+                       tc::desc_kmajor_sw128(ka + off), kIdescS, kk > 0 ? 1u : 0u);
           }
-          prev_kvs = cur_kvs;
-          prev_last = last;
+          tc::commit(&q_empty[qs]);
+          tc::commit(&s_full[buf]);
+          cur.next(p);
         }
         if (!ok) misc[1] = 1;
       }
-    } else {
-      // ---------------- softmax + epilogue, chunks j = grp, grp + 2, ...
+    } else if (warp == kPvWarp) {
+      // ---------------- O = P V issue (one thread): O of chunk i in TMEM
+      // columns 256 + 128 (i & 1), once the epilogue has read O of chunk
+      // i - 2 (o_empty); after the last chunk of an item its K / V stage is
+      // released (its scores were read before that chunk's P was written).
+      if (lane == 0) {
+        Cursor cur;
+        cur.n_items = n_items;
+        cur.seek(p, c0);
+        int kv_seq = 0, cur_kvs = 0;
+        bool ok = true;
+        for (int i = 0; i < nj; ++i) {
+          const int pb = i & 1;
+          if (i == 0 || cur.ci == 0) {
+            cur_kvs = kv_seq & 1;
+            ok = mbar_wait(&kv_full[cur_kvs], (kv_seq >> 1) & 1);
+            ++kv_seq;
+          }
+          ok = ok && mbar_wait(&p_full[pb], (i >> 1) & 1) &&
+               (i < 2 || mbar_wait(&o_empty[pb], ((i >> 1) - 1) & 1));
+          if (!ok) break;
+          tc::fence_after();
+          const uint32_t va = smem_u32(smem + kSmV + cur_kvs * kTile);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc::mma_ts(tmem + 256 + pb * 128, tmem + pb * 128 + kk * 8,
+                       tc::desc_mnmajor_sw128(va + kk * 2048, kHalf), kIdescO, kk > 0 ? 1u : 0u);
+          tc::commit(&o_full[pb]);
+          const int before = cur.it;
+          cur.next(p);
+          if (i == nj - 1 || cur.it != before) tc::commit(&kv_empty[cur_kvs]);
+        }
+        if (!ok) misc[1] = 1;
+      }
+    } else if (warp >= 2 && warp < 10) {
+      // ---------------- softmax, chunks j = grp, grp + 2, ...
       // Thread = TMEM lane = (row slot, head) of the chunk; 128 logits each.
       // The max and the sum run on 8 independent accumulators (the warp has
       // little else to overlap with); rows whose block is entirely visible
-      // skip the per-token mask.
+      // skip the per-token mask.  The group stores the chunk's (max, sum)
+      // and goes on; its O is drained by the epilogue warps.
       const int grp = (warp - 2) >> 2, quarter = warp & 3;
       const int m = quarter * 32 + lane, slot = m >> 4, head = m & 15;
       const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
@@ -594,14 +642,37 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[buf]);
+        if (live) p.part_ml[((long long)r * p.topk + si) * kHeadSlots + head] = make_float2(mx, l);
+        cur = nx;
+        e = e_nx;
+      }
+    } else if (warp >= 10 && warp < 14) {
+      // ---------------- O epilogue, every chunk in order: warp w drains TMEM
+      // lanes 32 (w % 4) .. +31 of the chunk's O.  Partial per (row, slot):
+      // the unnormalised sum of p v as bf16 in [16 dim chunks][16 heads][8
+      // dims], so the 16 head lanes of a slot store 256 contiguous bytes.
+      const int quarter = warp & 3;
+      const int m = quarter * 32 + lane, slot = m >> 4, head = m & 15;
+      const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+      Cursor cur;
+      cur.n_items = n_items;
+      cur.seek(p, c0);
+      int e = (slot < cur.rows()) ? p.pf_lists[cur.list_base() + slot] : 0;
+      for (int j = 0; j < nj; ++j) {
+        const int buf = j & 1;
+        const int r = e >> 8, si = e & 255;
+        const bool live = slot < cur.rows() && head < hq && r < p.batch.num_rows && si < p.topk;
+        Cursor nx = cur;
+        int e_nx = 0;
+        if (j + 1 < nj) {
+          nx.next(p);
+          e_nx = (slot < nx.rows()) ? p.pf_lists[nx.list_base() + slot] : 0;
+        }
         if (!warp_wait(&o_full[buf], (j >> 1) & 1)) {
           misc[1] = 1;
           break;
         }
         tc::fence_after();
-        // partial per (row, slot): the unnormalised sum of p v as bf16 in
-        // [16 dim chunks][16 heads][8 dims], so the 16 head lanes of a slot
-        // store 256 contiguous bytes, and (max, sum of p) per head
         uint4* dst = reinterpret_cast<uint4*>(
                          p.part_o + ((long long)r * p.topk + si) * kHeadSlots * kHeadDim) +
                      head;
@@ -626,7 +697,6 @@ __global__ void __launch_bounds__(kPaThreads, 1)
             if (live) store_o32(dst + kHeadSlots * 4 * (c + 1), rb);
           }
         }
-        if (live) p.part_ml[((long long)r * p.topk + si) * kHeadSlots + head] = make_float2(mx, l);
         cur = nx;
         e = e_nx;
       }
