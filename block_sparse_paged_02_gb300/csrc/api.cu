@@ -63,7 +63,7 @@ struct DecodeWs {
   // counts and lists, the plan, the per-(row, slot) partials
   bool prefill;
   size_t route, pf_counts, pf_lists, plan_hdr, plan_req_q, plan_req_item, item_rec, item_kv,
-      item_chunk, part_o, part_ml;
+      item_chunk, item_cost, part_o, part_ml;
   long long max_routed_reqs, max_items;
   size_t total;
 };
@@ -98,7 +98,8 @@ DecodeWs decode_layout(int num_rows, int bt_stride, int topk, int splits) {
     w.plan_req_item = take((size_t)w.max_routed_reqs * 4);
     w.item_rec = take((size_t)w.max_items * 16);
     w.item_kv = take((size_t)w.max_items * 8);
-    w.item_chunk = take((size_t)w.max_items * 4);
+    w.item_chunk = take((size_t)w.max_items * 4);  // (max_items > items: room for the totals)
+    w.item_cost = take((size_t)w.max_items * 4);
     w.part_o = take(n * (size_t)topk * 16 * kHeadDim * 2);
     w.part_ml = take(n * (size_t)topk * 16 * 8);
   }
@@ -453,6 +454,7 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
     pl.item_rec = reinterpret_cast<int4*>(ws + L.item_rec);
     pl.item_kv = reinterpret_cast<int2*>(ws + L.item_kv);
     pl.item_chunk = reinterpret_cast<int32_t*>(ws + L.item_chunk);
+    pl.item_cost = reinterpret_cast<int32_t*>(ws + L.item_cost);
     pl.max_routed_reqs = (int)L.max_routed_reqs;
     pl.max_items = (int)L.max_items;
     pl.part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);

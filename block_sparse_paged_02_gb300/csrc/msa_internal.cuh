@@ -411,14 +411,16 @@ struct PrefillLaunch {
   const int32_t* route;     // [N]
   const int32_t* pf_counts; // list counts (msa_decode clears them before the top-k)
   const int32_t* pf_lists;
-  // plan: header [0] = items, [1] = chunks; routed requests (q, first
-  // candidate); items and their first chunks
+  // plan: header [0] = items, [1] = chunks, [2] = estimated cost; routed
+  // requests (q, first candidate); items, their first chunks and the
+  // exclusive prefix of their costs (entry [items] = the totals)
   int32_t* plan_hdr;
   int32_t* plan_req_q;
   int32_t* plan_req_item;
   int4* item_rec;       // per item: list base, rows, position of row 0 (pos = r + z), block
   int2* item_kv;        // per item: page, tokens of the block that exist
   int32_t* item_chunk;
+  int32_t* item_cost;
   int max_routed_reqs;      // capacity of plan_req_*
   int max_items;            // capacity of item_*
   uint16_t* part_o;         // [N, topk, 16 dim chunks, 16 heads, 8 dims] bf16, sum p v

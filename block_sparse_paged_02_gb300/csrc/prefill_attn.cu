@@ -76,6 +76,14 @@ constexpr uint32_t kIdescO = tc::idesc_bf16(128, 128, 1);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kPlanThreads = 1024;
+// Estimated cost of the attention's work, to split it evenly across CTAs:
+// per item its K / V load, per chunk its products and softmax, more for a
+// block that holds some row's own position (the masked softmax).  Items of
+// such blocks have few rows each, so a range of them loads many blocks: an
+// equal split by chunks left the CTAs that got them ~20 % behind.
+constexpr int kCostItem = 4;
+constexpr int kCostChunk = 4;
+constexpr int kCostDiagChunk = 6;
 constexpr int kMergeThreads = 128;
 
 // ------------------------------------------------------------------ plan
@@ -152,7 +160,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Prefil
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- candidates (request, block) -> non-empty items with a chunk prefix
-  int n_items = 0, n_chunks = 0;
+  int n_items = 0, n_chunks = 0, n_cost = 0;
   for (int base = 0; base < n_cand; base += kPlanThreads) {
     const int c = base + tid;
     int q = 0, blk = 0, cnt = 0;
@@ -171,9 +179,13 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Prefil
     }
     const int live = cnt > 0;
     const int chunks = (cnt + kChunkRows - 1) / kChunkRows;
-    int t_items, t_chunks;
+    // a block reaching past the request's first row position is diagonal
+    const bool diag = live && (long long)kBlock * blk + kBlock - 1 >= b.context_lens[q];
+    const int cost = live ? kCostItem + chunks * (diag ? kCostDiagChunk : kCostChunk) : 0;
+    int t_items, t_chunks, t_cost;
     const int at = n_items + cta_excl_scan(live, scratch, &t_items);
     const int first = n_chunks + cta_excl_scan(chunks, scratch, &t_chunks);
+    const int first_cost = n_cost + cta_excl_scan(cost, scratch, &t_cost);
     if (live) {
       const int q0 = b.cu_seqlens_q[q], ql = b.cu_seqlens_q[q + 1] - q0;
       const int ctx = b.context_lens[q];
@@ -181,13 +193,18 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Prefil
       p.item_kv[at] = make_int2(b.block_table[(long long)q * bt + blk],
                                 min(kBlock, ctx + ql - kBlock * blk));
       p.item_chunk[at] = first;
+      p.item_cost[at] = first_cost;
     }
     n_items += t_items;
     n_chunks += t_chunks;
+    n_cost += t_cost;
   }
   if (tid == 0) {
     p.plan_hdr[0] = n_items;
     p.plan_hdr[1] = n_chunks;
+    p.plan_hdr[2] = n_cost;
+    p.item_chunk[n_items] = n_chunks;
+    p.item_cost[n_items] = n_cost;
   }
 }
 
@@ -409,9 +426,35 @@ __global__ void __maxnreg__(128)
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the plan (and the top-k lists)
 
   const int n_items = p.plan_hdr[0];
-  const long long total = p.plan_hdr[1];
-  const int c0 = (int)(total * blockIdx.x / gridDim.x);
-  const int c1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+  // this CTA's chunks [c0, c1): an equal share of the estimated cost.  The
+  // boundary at cost x is the number of chunks that start below x (chunk 0
+  // of an item starts with the item's K / V load, chunk i > 0 at kCostItem +
+  // i chunk costs into the item); the item holding x is found by all threads
+  // at once.
+  {
+    const long long cost = p.plan_hdr[2];
+    const long long x0 = cost * blockIdx.x / gridDim.x, x1 = cost * (blockIdx.x + 1) / gridDim.x;
+    if (tid == 0) {
+      misc[8] = 0;
+      misc[9] = p.plan_hdr[1];
+    }
+    __syncthreads();
+    for (int it = tid; it < n_items; it += kPaThreads) {
+      const int s0 = p.item_cost[it], s1 = p.item_cost[it + 1];
+      const int f0 = p.item_chunk[it], n = p.item_chunk[it + 1] - f0;
+      const int cw = (s1 - s0 - kCostItem) / max(n, 1);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const long long x = k ? x1 : x0;
+        if (s0 < x && x <= s1) {
+          const long long v = x - s0 - kCostItem;
+          misc[8 + k] = f0 + (v <= 0 ? 1 : 1 + min(n - 1, (int)((v + cw - 1) / cw) - 1));
+        }
+      }
+    }
+    __syncthreads();
+  }
+  const int c0 = misc[8], c1 = misc[9];
   const int nj = c1 - c0;
 
   if (nj > 0) {
