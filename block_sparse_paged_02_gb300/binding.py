@@ -39,7 +39,8 @@ class msa_batch(ctypes.Structure):
                 ("context_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
                 ("bt_stride", ctypes.c_int32), ("num_reqs", ctypes.c_int32),
                 ("num_rows", ctypes.c_int32), ("num_pages", ctypes.c_int32),
-                ("max_q_len", ctypes.c_int32)]
+                ("max_q_len", ctypes.c_int32),
+                ("min_q_len", ctypes.c_int32)]
 
 
 class msa_attn_args(ctypes.Structure):
@@ -150,13 +151,15 @@ def _check(fn: str, code: int):
 
 
 def make_batch(cu_seqlens_q, cu_seqlens_k, context_lens, block_table, num_pages: int,
-               num_rows: Optional[int] = None, max_q_len: int = 0) -> msa_batch:
+               num_rows: Optional[int] = None, max_q_len: int = 0,
+               min_q_len: int = 0) -> msa_batch:
     for t in (cu_seqlens_q, cu_seqlens_k, context_lens, block_table):
         if t.dtype != torch.int32:
             raise ValueError("batch geometry arrays are int32")
     b = msa_batch(_p(cu_seqlens_q), _p(cu_seqlens_k), _p(context_lens), _p(block_table),
                   int(block_table.shape[1]), int(context_lens.shape[0]),
-                  int(num_rows if num_rows is not None else 0), int(num_pages), int(max_q_len))
+                  int(num_rows if num_rows is not None else 0), int(num_pages), int(max_q_len),
+                  int(min_q_len))
     b._keep = (cu_seqlens_q, cu_seqlens_k, context_lens, block_table)
     return b
 

@@ -28,10 +28,12 @@ class DeviceCase:
     arrays).  The KV and index-K pools stay resident; after
     `pack_step_inputs()` what changes per step (queries and batch geometry)
     sits in one device buffer, `step_inputs`, that one copy refreshes, and
-    O / LSE in another, `step_outputs`."""
+    O / LSE in another, `step_outputs`.  The batch carries the request
+    length bounds as host hints (max_q_len, and min_q_len unless
+    `min_q_len_hint` is False; an int overrides it)."""
 
     def __init__(self, w, device: str = "cuda", topk: Optional[int] = None,
-                 tbl_stride: Optional[int] = None):
+                 tbl_stride: Optional[int] = None, min_q_len_hint=True):
         self.w = w
         self.device = device
         self.topk = int(topk or w.topk)
@@ -63,6 +65,10 @@ class DeviceCase:
         self.status = torch.zeros((1,), dtype=torch.int32, device=device)
         q_lens = np.diff(np.asarray(w.cu_seqlens_q, np.int64))
         self.max_q_len = int(q_lens.max()) if q_lens.size else 0
+        if min_q_len_hint is True:
+            self.min_q_len = int(q_lens.min()) if q_lens.size else 0
+        else:
+            self.min_q_len = int(min_q_len_hint or 0)
         ws = B.msa_workspace_size(N, w.bt_stride, self.topk, hq, d, self.tbl_stride)
         self.workspace = torch.zeros((ws,), dtype=torch.uint8, device=device)
         ws_a = B.msa_workspace_size(N, 0, 0, hq, d, self.tbl_stride)
@@ -74,7 +80,8 @@ class DeviceCase:
     def _args(self):
         w = self.w
         self.batch = B.make_batch(self.cu_q, self.cu_k, self.ctx, self.bt, w.num_pages,
-                                  self.num_rows, max_q_len=self.max_q_len)
+                                  self.num_rows, max_q_len=self.max_q_len,
+                                  min_q_len=self.min_q_len)
         self.attn = B.make_attn_args(self.q, self.k, self.v, w.kv_dtype, w.num_pages, self.out,
                                      self.lse, scale_mode=w.scale_mode, k_scale=self.k_scale,
                                      v_scale=self.v_scale, sinks=self.sinks,

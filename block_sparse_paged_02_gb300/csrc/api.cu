@@ -407,6 +407,8 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
                        batch->num_rows < (1 << 23) &&
                        (long long)batch->num_rows * batch->bt_stride < (1ll << 31) &&
                        prefill_attn_available();
+  // every request known to bring >= kPrefillMinRows rows: no decode attention
+  const bool prefill_only = prefill && batch->min_q_len >= kPrefillMinRows;
   int32_t* route = prefill ? reinterpret_cast<int32_t*>(ws + L.route) : nullptr;
   int32_t* pf_counts = prefill ? reinterpret_cast<int32_t*>(ws + L.pf_counts) : nullptr;
   int32_t* pf_lists = prefill ? reinterpret_cast<int32_t*>(ws + L.pf_lists) : nullptr;
@@ -457,6 +459,7 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
     pl.item_cost = reinterpret_cast<int32_t*>(ws + L.item_cost);
     pl.max_routed_reqs = (int)L.max_routed_reqs;
     pl.max_items = (int)L.max_items;
+    pl.finish_unrouted = prefill_only ? 1 : 0;
     pl.part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
     pl.part_ml = reinterpret_cast<float2*>(ws + L.part_ml);
     pl.out = static_cast<uint16_t*>(attn->out);
@@ -466,14 +469,16 @@ msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index
     if (e != cudaSuccess) return MSA_ERR_CUDA;
   }
 
-  AttnLaunch ap = make_attn(attn, tbl, tstride, len, reinterpret_cast<float*>(ws + L.partials),
-                            counters, pps, splits, dev_status);
-  ap.route = route;  // rows of the prefill path leave at once
-  // the attention split depends only on the selected width (8*topk entries)
-  e = launch_sparse_attn(ap, stream, true);
-  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  if (!prefill_only) {
+    AttnLaunch ap = make_attn(attn, tbl, tstride, len, reinterpret_cast<float*>(ws + L.partials),
+                              counters, pps, splits, dev_status);
+    ap.route = route;  // rows of the prefill path leave at once
+    // the attention split depends only on the selected width (8*topk entries)
+    e = launch_sparse_attn(ap, stream, true);
+    if (e != cudaSuccess) return MSA_ERR_CUDA;
+  }
   if (trace && trace->after_attn) cudaEventRecord(trace->after_attn, stream);
-  if (trace) trace->kernels = score_kernels + 2 + (prefill ? 3 : 0);
+  if (trace) trace->kernels = score_kernels + 1 + (prefill ? 3 : 0) + (prefill_only ? 0 : 1);
   return MSA_OK;
 }
 

@@ -271,7 +271,8 @@ __device__ __forceinline__ uint32_t request_lengths(const msa_batch& b, int q, i
   *q_len = c1 - c0;
   *ctx = b.context_lens[q];
   *nb = 0;
-  if (slen < *q_len || *ctx < 0 || (long long)slen > (long long)kBlock * b.bt_stride)
+  if (slen < *q_len || *ctx < 0 || (long long)slen > (long long)kBlock * b.bt_stride ||
+      *q_len < b.min_q_len)
     return MSA_DEV_MALFORMED;
   if (*ctx + *q_len != slen) return MSA_DEV_BAD_LEN;
   *nb = (slen + kBlock - 1) / kBlock;
@@ -422,6 +423,8 @@ struct PrefillLaunch {
   int32_t* item_chunk;
   int32_t* item_cost;
   int max_routed_reqs;      // capacity of plan_req_*
+  int finish_unrouted;      // no decode attention runs: the merge writes unrouted rows
+                            // (all poisoned) as empty rows
   int max_items;            // capacity of item_*
   uint16_t* part_o;         // [N, topk, 16 dim chunks, 16 heads, 8 dims] bf16, sum p v
   float2* part_ml;          // [N, topk, 16] (max, sum of p), log2 units

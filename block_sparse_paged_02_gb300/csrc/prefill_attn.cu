@@ -759,7 +759,8 @@ __global__ void __maxnreg__(128)
 // One CTA per row: thread t owns head t % 16 and the 8-dim chunks t / 16
 // and t / 16 + 8, so that a warp reads 512 contiguous bytes of a partial
 // ([16 dim chunks][16 heads][8 dims]) per load.  Rows not routed to the
-// prefill path leave at once.
+// prefill path leave at once, or, when no decode attention runs, are
+// written as empty rows.
 template <bool SCALAR>
 __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(const PrefillLaunch p) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -769,10 +770,14 @@ __global__ void __launch_bounds__(kMergeThreads) prefill_merge_kernel(const Pref
   if (p.sinks && head < p.num_heads) sink2 = __ldg(p.sinks + head) * kLog2e;
   if constexpr (SCALAR) vs = __ldg(p.v_scale);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (p.route[r] == 0) return;
+  // a row left to the decode attention; with none launched (every request
+  // known to be a prefill request) such a row is poisoned: written here as
+  // an empty row (O = 0, LSE = sink or -inf)
+  const bool routed = p.route[r] != 0;
+  if (!routed && !p.finish_unrouted) return;
   // the row's selections (ascending blocks, then -1; topk <= kMergeThreads):
   // one partial per selected block
-  const bool has = tid < p.topk && p.topk_idx[(long long)r * p.topk + tid] >= 0;
+  const bool has = routed && tid < p.topk && p.topk_idx[(long long)r * p.topk + tid] >= 0;
   const int nsel = __syncthreads_count(has);
   if (head >= p.num_heads) return;
   const long long pbase = (long long)r * p.topk;

@@ -67,7 +67,8 @@ enum { MSA_SCALE_NONE = 0, MSA_SCALE_SCALAR = 1, MSA_SCALE_PER_TOKEN_HEAD = 2 };
 #define MSA_DEV_BAD_LEN 2u   /* context_lens[q] + q_len != seq_len: the request is poisoned
                                 [P56170 "Implementation breakdown" item 3] */
 #define MSA_DEV_MALFORMED 4u /* cu_seqlens_q does not tile [0, num_rows), seq_len < q_len,
-                                context_len < 0, or seq_len > 128 * bt_stride */
+                                context_len < 0, seq_len > 128 * bt_stride, or q_len below
+                                a non-zero min_q_len: the request is poisoned */
 #define MSA_DEV_BAD_TABLE 8u /* sparse table entry outside the page-16 pool, or sparse_len
                                 < 0 or > 16 * tbl_stride: the row is poisoned */
 #define MSA_DEV_TIMEOUT 16u  /* a bounded wait inside a kernel gave up (hardware stall);
@@ -90,7 +91,12 @@ enum { MSA_SCALE_NONE = 0, MSA_SCALE_SCALAR = 1, MSA_SCALE_PER_TOKEN_HEAD = 2 };
  *   max_q_len    host-side upper bound of any request's q_len (the metadata's
  *                max_query_len); only a launch hint: when it is >= 64, requests
  *                with >= 64 rows are scored by the tensor-core kernel.  Results
- *                do not depend on it. */
+ *                do not depend on it.
+ *   min_q_len    host-side lower bound of every request's q_len, 0 when not
+ *                known.  When it is >= 64 (and the block-major prefill
+ *                attention serves the call, see msa_decode) msa_decode
+ *                launches no split-K decode attention.  A request with fewer
+ *                rows than a non-zero bound is poisoned (MSA_DEV_MALFORMED). */
 typedef struct msa_batch {
   const int32_t* cu_seqlens_q;
   const int32_t* cu_seqlens_k;
@@ -101,6 +107,7 @@ typedef struct msa_batch {
   int32_t num_rows;
   int32_t num_pages;
   int32_t max_q_len;
+  int32_t min_q_len;
 } msa_batch;
 
 /* Attention operands [P47287 "Implementation breakdown" items 2-3],
@@ -283,7 +290,9 @@ msa_status msa_sparse_paged_attn_static(const msa_attn_args* attn, const int32_t
  * >= 64 rows when max_q_len >= 64, the KV is bf16 without per-token scales
  * and topk <= 128: those rows take a block-major tensor-core attention,
  * whose O / LSE agree with the other path within the attention tolerance,
- * not bit for bit. */
+ * not bit for bit.  When min_q_len >= 64 as well, every row takes that path
+ * and the split-K decode attention is not launched (a poisoned row is then
+ * written as an empty row by the block-major path's merge). */
 msa_status msa_decode(const msa_batch* batch, const void* idx_q, const msa_index_cache* index,
                       int32_t topk, const msa_attn_args* attn, int32_t* topk_idx, int32_t* sparse_tbl,
                       int32_t tbl_stride, int32_t* sparse_len, void* workspace,

@@ -368,6 +368,49 @@ def test_prefill_path_repeated_calls(msa):
         assert b["status"] == 0
 
 
+def test_prefill_only_batch_skips_decode_attention(msa, orc):
+    # every request brings >= 64 rows and the batch says so (min_q_len):
+    # msa_decode launches no split-K decode attention, and its results equal
+    # those of the call without the hint bit for bit, and the oracle's
+    w = W.chunked_prefill(seed=17, context=1500, new_tokens=200, reqs=2)
+    runs = {}
+    for hint in (True, False):
+        c = msa.DeviceCase(w, min_q_len_hint=hint)
+        tr = msa.make_trace()
+        c.decode(trace=tr)
+        runs[hint] = (c.fetch(), tr.kernels)
+    (got, k_hint), (plain, k_plain) = runs[True], runs[False]
+    assert k_hint == k_plain - 1
+    for key in ("topk_idx", "tbl", "sparse_len", "out", "lse"):
+        assert np.array_equal(got[key], plain[key], equal_nan=True), key
+    ref = orc.decode(w)
+    assert got["status"] == ref["status"] == 0
+    for key in ("topk_idx", "tbl", "sparse_len"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert_attn_close(got["out"], got["lse"], ref["out"], ref["lse"])
+
+
+def test_min_q_len_hint_violated(msa, orc):
+    # a bound of 64 rows per request on a batch that also holds a 3-row
+    # request: that request is poisoned (MSA_DEV_MALFORMED, empty rows,
+    # written by the prefill merge since no decode attention runs); the
+    # prefill request is unaffected
+    w = W.custom(73, q_lens=[100, 3], seq_lens=[3000, 900], hq=16, di=128, topk=8,
+                 kv_dtype=W.KV_BF16, with_sink=True)
+    c = msa.DeviceCase(w, min_q_len_hint=64)
+    c.decode()
+    got = c.fetch()
+    ref = orc.decode(w)
+    assert ref["status"] == 0 and got["status"] == msa.MSA_DEV_MALFORMED
+    pre = slice(0, 100)
+    for key in ("topk_idx", "tbl", "sparse_len"):
+        assert np.array_equal(got[key][pre], ref[key][pre]), key
+    assert_attn_close(got["out"][pre], got["lse"][pre], ref["out"][pre], ref["lse"][pre])
+    assert np.all(got["topk_idx"][100:] == -1) and np.all(got["sparse_len"][100:] == 0)
+    assert np.all(got["out"][100:] == 0)
+    np.testing.assert_allclose(got["lse"][100:], np.tile(w.sinks, (3, 1)), atol=1e-6)
+
+
 def test_poisoned_requests_match_oracle(msa, orc):
     w = W.custom(57, q_lens=[1, 2, 1, 1], seq_lens=[900, 700, 400, 300], hq=16, di=128, topk=2,
                  with_sink=True)
