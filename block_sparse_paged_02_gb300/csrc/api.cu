@@ -225,9 +225,16 @@ cudaError_t launch_scores(ScoreLaunch p, cudaStream_t stream, int* kernels = nul
   const bool tc = !p.idx_fp8 && p.batch.max_q_len >= kTcMinRows &&
                   tc_score_supported(p.index_heads, p.index_dim);
   p.tc_min_rows = tc ? kTcMinRows : 0;
-  if (kernels) *kernels = tc ? 2 : 1;
-  cudaError_t e = launch_index_score(p, stream);
-  if (e != cudaSuccess || !tc) return e;
+  // every request known to have tensor-core rows (min_q_len hint): the
+  // CUDA-core kernel would score nothing; the tensor-core one then reports
+  // the batch's status bits
+  const bool cuda_core = !(tc && p.batch.min_q_len >= kTcMinRows);
+  p.report_status = cuda_core ? 0 : 1;
+  if (kernels) *kernels = (cuda_core ? 1 : 0) + (tc ? 1 : 0);
+  if (cuda_core) {
+    cudaError_t e = launch_index_score(p, stream);
+    if (e != cudaSuccess || !tc) return e;
+  }
   return launch_index_score_tc(p, stream);
 }
 

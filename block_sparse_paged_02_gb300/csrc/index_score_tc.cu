@@ -233,6 +233,7 @@ __global__ void __maxnreg__(128)
   if (tid == 0) {
     misc[0] = !(b.cu_seqlens_q[0] == 0 && b.cu_seqlens_q[R] == b.num_rows);
     misc[1] = 0;  // timeout seen
+    misc[2] = 0;  // per-request status bits
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
@@ -252,6 +253,7 @@ __global__ void __maxnreg__(128)
     int q0, ql, ctx, nb;
     const uint32_t bad = request_lengths(b, q, &q0, &ql, &ctx, &nb);
     if (ql < 0) misc[0] = 1;
+    if (bad) atomicOr(reinterpret_cast<unsigned*>(&misc[2]), bad);
     int items = 0;
     if (!bad && ql >= kTcMinRows) {
       for (int t = 0; t * kTileRows < ql; ++t) {
@@ -263,7 +265,11 @@ __global__ void __maxnreg__(128)
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
   __syncthreads();
-  const bool batch_ok = misc[0] == 0;  // the CUDA-core kernel reports the status bits
+  const bool batch_ok = misc[0] == 0;
+  // the same status bits as the CUDA-core kernel (which msa_decode does not
+  // launch when every request has tensor-core rows)
+  if (blockIdx.x == 0 && tid == 0 && p.report_status)
+    atomicOr(p.status, batch_ok ? (unsigned)misc[2] : MSA_DEV_MALFORMED);
   if (batch_ok && warp == 0) {
     int carry = 0;
     if (lane == 0) prefix[0] = 0;

@@ -292,6 +292,8 @@ struct ScoreLaunch {
   int tc_min_rows;  // > 0: requests with q_len >= this are left to the tensor-core kernel
   int idx_fp8;              // index keys are OCP e4m3 codes
   const float* idx_scale;   // FP8: per-token scales [P, 128, Hi], or null (1)
+  int report_status;        // tensor-core kernel: report the batch's status bits (the
+                            // CUDA-core kernel, which otherwise does, is not launched)
 };
 
 struct TopkLaunch {

@@ -370,8 +370,9 @@ def test_prefill_path_repeated_calls(msa):
 
 def test_prefill_only_batch_skips_decode_attention(msa, orc):
     # every request brings >= 64 rows and the batch says so (min_q_len):
-    # msa_decode launches no split-K decode attention, and its results equal
-    # those of the call without the hint bit for bit, and the oracle's
+    # msa_decode launches neither the CUDA-core scorer nor the split-K decode
+    # attention, and its results equal those of the call without the hint
+    # bit for bit, and the oracle's
     w = W.chunked_prefill(seed=17, context=1500, new_tokens=200, reqs=2)
     runs = {}
     for hint in (True, False):
@@ -380,7 +381,7 @@ def test_prefill_only_batch_skips_decode_attention(msa, orc):
         c.decode(trace=tr)
         runs[hint] = (c.fetch(), tr.kernels)
     (got, k_hint), (plain, k_plain) = runs[True], runs[False]
-    assert k_hint == k_plain - 1
+    assert k_hint == k_plain - 2
     for key in ("topk_idx", "tbl", "sparse_len", "out", "lse"):
         assert np.array_equal(got[key], plain[key], equal_nan=True), key
     ref = orc.decode(w)
@@ -391,11 +392,11 @@ def test_prefill_only_batch_skips_decode_attention(msa, orc):
 
 
 def test_min_q_len_hint_violated(msa, orc):
-    # a bound of 64 rows per request on a batch that also holds a 3-row
-    # request: that request is poisoned (MSA_DEV_MALFORMED, empty rows,
-    # written by the prefill merge since no decode attention runs); the
-    # prefill request is unaffected
-    w = W.custom(73, q_lens=[100, 3], seq_lens=[3000, 900], hq=16, di=128, topk=8,
+    # a bound of 64 rows per request on a batch that also holds a 3-row and a
+    # 0-row request: both are poisoned (MSA_DEV_MALFORMED; the 3 rows are
+    # empty rows, written by the prefill merge since no decode attention
+    # runs); the prefill request is unaffected
+    w = W.custom(73, q_lens=[100, 3, 0], seq_lens=[3000, 900, 500], hq=16, di=128, topk=8,
                  kv_dtype=W.KV_BF16, with_sink=True)
     c = msa.DeviceCase(w, min_q_len_hint=64)
     c.decode()
@@ -409,6 +410,28 @@ def test_min_q_len_hint_violated(msa, orc):
     assert np.all(got["topk_idx"][100:] == -1) and np.all(got["sparse_len"][100:] == 0)
     assert np.all(got["out"][100:] == 0)
     np.testing.assert_allclose(got["lse"][100:], np.tile(w.sinks, (3, 1)), atol=1e-6)
+
+
+def test_prefill_only_batch_poisoned_request(msa, orc):
+    # the prefill-only launch (min_q_len hint) with a page outside the pool
+    # in request 0: its rows are empty rows, the status bit is reported
+    # without the CUDA-core scorer, request 1 is unaffected
+    w = W.custom(74, q_lens=[80, 120], seq_lens=[3000, 4000], hq=16, di=128, topk=8,
+                 kv_dtype=W.KV_BF16, with_sink=True)
+    bt = w.block_table.copy()
+    bt[0, 5] = w.num_pages + 3
+    w.block_table = bt
+    c = msa.DeviceCase(w)
+    assert c.min_q_len == 80
+    c.decode()
+    got = c.fetch()
+    ref = orc.decode(w)
+    assert got["status"] == ref["status"] == msa.MSA_DEV_BAD_PAGE
+    for key in ("topk_idx", "tbl", "sparse_len"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert_attn_close(got["out"], got["lse"], ref["out"], ref["lse"])
+    assert np.all(got["out"][:80] == 0)
+    np.testing.assert_allclose(got["lse"][:80], np.tile(w.sinks, (80, 1)), atol=1e-6)
 
 
 def test_poisoned_requests_match_oracle(msa, orc):
