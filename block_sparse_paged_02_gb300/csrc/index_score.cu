@@ -35,6 +35,8 @@ namespace msa {
 namespace {
 
 constexpr int kRowGroup = 4;
+// bf16 keys: requests of at least this many rows (max_q_len hint) -> MMA scorer
+constexpr int kMmaMinRows = 2;
 
 // Scoring kinds: bf16 keys on CUDA-core FMAs, bf16 keys on warp MMA, OCP
 // e4m3 keys on warp MMA (fp16 operands).
@@ -53,8 +55,10 @@ struct ScoreCfg {
   static constexpr int kProducers = KIND == kMmaFp8 ? MSA_SCORE_PRODUCERS_FP8 : MSA_SCORE_PRODUCERS;
   static constexpr int kElem = KIND == kMmaFp8 ? 1 : 2;
   static constexpr int kPageBytes = kBlock * HI * DI * kElem;
-  // query rows scored per pass: 4 on FMAs, 8 (index heads) columns on MMA
-  static constexpr int kRows = KIND == kFmaBf16 ? kRowGroup : 8 / HI;
+  // query rows scored per pass: 4 for bf16 keys (FMA or MMA: the stage's
+  // query copy stays small, so the ring keeps 6 stages), 8 / HI for e4m3
+  // keys (the MMA's 8 columns)
+  static constexpr int kRows = KIND == kMmaFp8 ? 8 / HI : kRowGroup;
   static constexpr int kQBytes = kRows * HI * DI * 2;  // query rows staged with a page
   static constexpr int kScaleBytes = KIND == kMmaFp8 ? kBlock * HI * 4 : 0;  // per-token scales
   // stages within 200 KB (the rest holds barriers and the request prefix):
@@ -68,14 +72,15 @@ struct ScoreCfg {
   static_assert(kStages % kProducers == 0, "every stage needs a single producer");
 };
 
-// e4m3 keys with 128 dims and one head: a page is 128 rows of 128 B, which
-// arrives by one tensor copy with the 128-byte swizzle, so that the MMA
-// scorer's reads of rows 128 B apart fall in distinct banks
+// Pages for the MMA scorer with 128 dims and one head arrive by tensor
+// copies with the 128-byte swizzle: e4m3 keys as one box of 128 rows x 128 B,
+// bf16 keys as two (dims 0-63, then 64-127, 16 KB apart), so that the
+// scorer's reads of rows a page row apart fall in distinct banks
 #ifndef MSA_SCORE_FP8_SWIZZLE
 #define MSA_SCORE_FP8_SWIZZLE 1
 #endif
 template <int DI, int HI, int KIND>
-constexpr bool kSwizzledPages = MSA_SCORE_FP8_SWIZZLE && KIND == kMmaFp8 && DI == 128 && HI == 1;
+constexpr bool kSwizzledPages = MSA_SCORE_FP8_SWIZZLE && KIND != kFmaBf16 && DI == 128 && HI == 1;
 
 struct StageInfo {  // written by the producer before it arms the stage
   int req, blk, valid, q0, qlen, ctx, jstart, pad;
@@ -236,10 +241,13 @@ __device__ __forceinline__ void score_page_mma(const uint8_t* page, const float*
       const uint8_t* row = page + (16 * mt + g + 8 * half) * kRowB;
 #pragma unroll
       for (int i = 0; i < kSpanC; ++i) {
-        // 16-byte chunk j of sub-row t sits at chunk j ^ (t % 8) when the page
-        // came by a swizzled tensor copy (t % 8 == g here)
+        // swizzled pages: 16-byte chunk j of sub-row t sits in box j / 8
+        // (128 rows x 128 B each) at chunk (j % 8) ^ (t % 8) (t % 8 == g here)
         const int chunk = c * kSpanC + i;
-        const uint4 v = lds128(row + 16 * (SWZ ? (chunk ^ g) : chunk));
+        const uint4 v =
+            SWZ ? lds128(page + (chunk >> 3) * (kBlock * 128) + (16 * mt + g + 8 * half) * 128 +
+                         16 * ((chunk & 7) ^ g))
+                : lds128(row + 16 * chunk);
         w[half][4 * i] = v.x;
         w[half][4 * i + 1] = v.y;
         w[half][4 * i + 2] = v.z;
@@ -422,10 +430,12 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
                    p.idx_scale + (long long)page * kBlock * HI, sb, &full[s]);
         bulk_g2s(smem + S::kQ + (size_t)s * C::kQBytes,
                  p.idx_q + (long long)(si.q0 + si.jstart) * HI * DI, qb, &full[s]);
-        if constexpr (kSwizzledPages<DI, HI, KIND>)  // one 128 x 128 B box, 128-byte swizzle
-          tma_load_2d(smem + S::kPages + (size_t)s * C::kPageBytes, &kmap, 0, page * kBlock,
-                      &full[s]);
-        else
+        if constexpr (kSwizzledPages<DI, HI, KIND>) {  // 128 x 128 B boxes, 128-byte swizzle
+#pragma unroll
+          for (int h = 0; h < C::kPageBytes / (kBlock * 128); ++h)
+            tma_load_2d(smem + S::kPages + (size_t)s * C::kPageBytes + h * (kBlock * 128), &kmap,
+                        64 * h, page * kBlock, &full[s]);
+        } else
           bulk_g2s(smem + S::kPages + (size_t)s * C::kPageBytes,
                    p.idx_k + (long long)page * C::kPageBytes, C::kPageBytes, &full[s]);
       } else {
@@ -549,11 +559,14 @@ cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
   CUtensorMap kmap;
   memset(&kmap, 0, sizeof(kmap));
   if constexpr (kSwizzledPages<DI, HI, KIND>) {
-    // the pool as [P * 128 rows][128 B]; row coordinates must fit an int
+    // the pool as [P * 128 rows][DI keys]; boxes of 128 B x 128 rows;
+    // row coordinates must fit an int
     const long long rows = (long long)p.batch.num_pages * kBlock;
-    if (rows > 0x7fffffffll ||
-        !encode_map_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.idx_k, DI, rows, DI, DI, kBlock))
-      return cudaErrorInvalidValue;
+    const bool ok = KIND == kMmaFp8
+        ? encode_map_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.idx_k, DI, rows, DI, DI, kBlock)
+        : encode_map_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.idx_k, DI, rows, DI * 2, 64,
+                        kBlock);
+    if (rows > 0x7fffffffll || !ok) return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -574,7 +587,12 @@ cudaError_t launch_kind(const ScoreLaunch& p, cudaStream_t stream) {
 
 cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream) {
   if (p.idx_fp8) return launch_kind<kMmaFp8>(p, stream);
-  return launch_kind<MSA_SCORE_BF16_KIND>(p, stream);
+  // bf16 keys: one query row per request streams at the copy rate on FMAs;
+  // several rows (speculative decode) multiply the FMA work per byte, and
+  // the warp MMA scorer takes them
+  if (MSA_SCORE_BF16_KIND == 1 || p.batch.max_q_len >= kMmaMinRows)
+    return launch_kind<kMmaBf16>(p, stream);
+  return launch_kind<kFmaBf16>(p, stream);
 }
 
 }  // namespace msa
