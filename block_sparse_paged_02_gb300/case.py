@@ -104,15 +104,32 @@ class DeviceCase:
             views.append(v)
         return buf, views
 
-    def pack_step_inputs(self):
+    _STEP_FIELDS = ("q", "idx_q", "cu_q", "cu_k", "ctx", "bt", "out", "lse", "batch", "attn",
+                    "step_inputs", "step_outputs")
+
+    def pack_step_inputs(self, sets: int = 1):
         """Move the per-step inputs into one device buffer and O / LSE into
-        another (the argument structs are rebuilt on the new addresses)."""
-        buf, (self.q, self.idx_q, self.cu_q, self.cu_k, self.ctx, self.bt) = self._pack(
-            [self.q, self.idx_q, self.cu_q, self.cu_k, self.ctx, self.bt], self.device)
-        self.step_inputs = buf
-        obuf, (self.out, self.lse) = self._pack([self.out, self.lse], self.device)
-        self.step_outputs = obuf
-        self._args()
+        another (the argument structs are rebuilt on the new addresses).
+        With sets > 1, that many independent buffer pairs with their own
+        argument structs (same pools and workspace), for a pipeline that
+        copies one step's inputs in while another step runs;
+        `use_step_set(i)` selects set i (the first is selected)."""
+        src_in = [self.q, self.idx_q, self.cu_q, self.cu_k, self.ctx, self.bt]
+        src_out = [self.out, self.lse]
+        self._sets = []
+        for _ in range(sets):
+            buf, (self.q, self.idx_q, self.cu_q, self.cu_k, self.ctx, self.bt) = self._pack(
+                src_in, self.device)
+            self.step_inputs = buf
+            obuf, (self.out, self.lse) = self._pack(src_out, self.device)
+            self.step_outputs = obuf
+            self._args()
+            self._sets.append({k: getattr(self, k) for k in self._STEP_FIELDS})
+        self.use_step_set(0)
+
+    def use_step_set(self, i: int):
+        for k, v in self._sets[i].items():
+            setattr(self, k, v)
 
     # -- the four entry points on this batch
     def index_score(self, stream=None):

@@ -554,6 +554,27 @@ def test_packed_step_inputs(msa):
     assert b["status"] == 0
 
 
+def test_two_step_buffer_sets(msa):
+    # two sets of step buffers with their own argument structs over the same
+    # pools and workspace (the pipelined end-to-end loop): each set gives the
+    # results of the plain call, and steps alternating sets on two streams'
+    # copies stay intact
+    w = W.custom(64, q_lens=[1, 3, 2], seq_lens=[7000, 3000, 900], hq=16, di=128, topk=8,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_SCALAR, with_sink=True)
+    c = msa.DeviceCase(w)
+    c.decode()
+    a = c.fetch()
+    c.pack_step_inputs(sets=2)
+    for b in (1, 0, 1):
+        c.use_step_set(b)
+        c.step_outputs.zero_()
+        c.decode()
+        got = c.fetch()
+        for key in ("out", "lse", "tbl", "topk_idx", "sparse_len"):
+            assert np.array_equal(a[key], got[key]), (b, key)
+    assert c._sets[0]["step_inputs"].data_ptr() != c._sets[1]["step_inputs"].data_ptr()
+
+
 def test_every_call_rescores_every_block(msa, orc):
     # New queries on later calls must change every block score of the fused
     # path (stale workspace scores from the first call would show up as wrong
