@@ -391,6 +391,26 @@ def test_prefill_only_batch_skips_decode_attention(msa, orc):
     assert_attn_close(got["out"], got["lse"], ref["out"], ref["lse"])
 
 
+def test_min_q_len_hint_with_fp8_kv(msa, orc):
+    # every request has >= 64 rows (hint given) but the KV is FP8, which the
+    # block-major path does not take: the tensor-core scorer alone scores
+    # (the CUDA-core one is not launched) and the split-K decode attention
+    # still serves every row
+    w = W.custom(75, q_lens=[96, 70], seq_lens=[2500, 1800], hq=16, di=128, topk=8,
+                 kv_dtype=W.KV_FP8, scale_mode=W.SCALE_PER_TOKEN_HEAD, with_sink=True)
+    c = msa.DeviceCase(w)
+    assert c.min_q_len == 70
+    tr = msa.make_trace()
+    c.decode(trace=tr)
+    got = c.fetch()
+    assert tr.kernels == 3  # tensor-core scorer, top-k, decode attention
+    ref = orc.decode(w)
+    assert got["status"] == ref["status"] == 0
+    for key in ("topk_idx", "tbl", "sparse_len"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert_attn_close(got["out"], got["lse"], ref["out"], ref["lse"])
+
+
 def test_min_q_len_hint_violated(msa, orc):
     # a bound of 64 rows per request on a batch that also holds a 3-row and a
     # 0-row request: both are poisoned (MSA_DEV_MALFORMED; the 3 rows are
