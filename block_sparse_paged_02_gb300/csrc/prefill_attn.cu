@@ -19,8 +19,10 @@
 // here).  So the top-k kernel appends each (row, slot) to its block's list;
 // this file then
 //   plan:      one CTA compacts the non-empty (request, block) lists into
-//              items of 8-row chunks with a chunk prefix;
-//   attention: a persistent CTA per SM takes an equal range of chunks; per
+//              items of 8-row chunks with prefixes of their chunks and of
+//              their estimated costs;
+//   attention: a persistent CTA per SM takes the chunks of an equal share
+//              of the estimated cost; per
 //              item it loads the block's K and V once (two 32 KB tensor
 //              copies, 128-byte swizzle), per chunk it gathers the 8 rows'
 //              queries (16 head slots each: M = 128) and computes
@@ -35,11 +37,12 @@
 //              the sink joins the denominator, O and the natural-log LSE
 //              are written.
 // CTA roles in the attention kernel: warp 0 issues the tensor copies (its
-// lanes and warp 15's gather the chunks' query rows), warp 1 allocates TMEM and one of its threads
-// issues the S MMAs, one thread of warp 14 the P V MMAs, warps 2-5 and 6-9
-// are two softmax groups that take alternate chunks, warps 10-13 store every
-// chunk's O (S, P and O are double-buffered in TMEM: 512 columns).  Every wait is bounded; on expiry the kernel records
-// MSA_DEV_TIMEOUT, stops and still frees its TMEM.
+// lanes and warp 15's gather the chunks' query rows), warp 1 allocates TMEM
+// and one of its threads issues the S MMAs, one thread of warp 14 the P V
+// MMAs, warps 2-5 and 6-9 are two softmax groups that take alternate
+// chunks, warps 10-13 store every chunk's O (S, P and O are double-buffered
+// in TMEM: 512 columns).  Every wait is bounded; on expiry the kernel
+// records MSA_DEV_TIMEOUT, stops and still frees its TMEM.
 #include <string.h>
 
 #include "tcgen05.cuh"
