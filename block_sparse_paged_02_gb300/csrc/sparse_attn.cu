@@ -57,7 +57,9 @@ constexpr int kRecvF4Bytes = kRecvPairs * 128 * 16;
 constexpr int kRecvMlBytes = kRecvPairs * 8 * 4;
 constexpr int kRecvFlagBytes = kMaxClusterSplits * 4;
 
-template <bool FP8>
+// PUSH: the push merge (a receive area outside the ring) for bf16 K/V too;
+// FP8 always pushes
+template <bool FP8, bool PUSH = false>
 struct AttnCfg {
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kSlab = kPage16 * kHeadDim * kElem;  // one page-16 K (or V) slab
@@ -80,7 +82,8 @@ struct AttnCfg {
   // FP8 cluster merge: the receive area other CTAs of the row push their
   // partials into, never used by this CTA before the merge (outside the ring)
   static constexpr int kRecvOff = (kSinkOff + (kMaxHeads + 1) * 4 + 15) / 16 * 16;
-  static constexpr int kRecvBytes = FP8 ? kRecvF4Bytes + kRecvMlBytes + kRecvFlagBytes : 0;
+  static constexpr int kRecvBytes =
+      (FP8 || PUSH) ? kRecvF4Bytes + kRecvMlBytes + kRecvFlagBytes : 0;
   static constexpr int kSmemBytes = kRecvOff + kRecvBytes + 64;
   static_assert(kCPart + kCPartBytes <= kDataBytes, "cluster partial must fit the ring");
 };
@@ -132,11 +135,11 @@ __device__ __forceinline__ void finalize_out(const AttnLaunch& p, const float* s
         (M == -INFINITY || Lsum <= 0.f) ? -INFINITY : (M + log2f(Lsum)) * kLn2;
 }
 
-template <bool FP8, int SCALE, bool CL>
-__global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_CTAS_BF16)
+template <bool FP8, int SCALE, bool CL, bool PUSH = false>
+__global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : (PUSH ? 1 : MSA_ATTN_CTAS_BF16))
     sparse_attn_kernel(const AttnLaunch p, const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap) {
-  using C = AttnCfg<FP8>;
+  using C = AttnCfg<FP8, PUSH>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* qbar = bars + kWarps * C::kStages;
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
     for (int j = 0; j < 16; ++j) acc[j] += f * ar[j];
   }
 
-  if constexpr (CL && FP8) {
+  if constexpr (CL && (FP8 || PUSH)) {
     // ---- the row's splits form one cluster.  Each CTA pushes its partial
     // of every 4-head chunk straight into the shared memory of the chunk's
     // owner (asynchronous remote stores), one cluster barrier makes all of
@@ -733,10 +736,14 @@ __global__ void __launch_bounds__(kThreads, FP8 ? MSA_ATTN_CTAS_FP8 : MSA_ATTN_C
 
 template <bool FP8, int SCALE>
 cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t stream, bool programmatic) {
-  using C = AttnCfg<FP8>;
   // one split needs no merge at all (the single-split path finalises directly)
   const bool cl = p.splits > 1 && p.splits <= kMaxClusterSplits;
-  auto kern = cl ? sparse_attn_kernel<FP8, SCALE, true> : sparse_attn_kernel<FP8, SCALE, false>;
+  // bf16 K/V: the push merge's receive area fits only at one CTA per SM,
+  // which a grid of no more CTAs than SMs leaves anyway
+  const bool push = !FP8 && cl && (long long)p.num_rows * p.splits <= device_sm_count();
+  auto kern = push ? sparse_attn_kernel<FP8, SCALE, true, true>
+                   : cl ? sparse_attn_kernel<FP8, SCALE, true> : sparse_attn_kernel<FP8, SCALE, false>;
+  const int smem_bytes = push ? AttnCfg<FP8, true>::kSmemBytes : AttnCfg<FP8>::kSmemBytes;
   CUtensorMap kmap, vmap;
   memset(&kmap, 0, sizeof(kmap));
   memset(&vmap, 0, sizeof(vmap));
@@ -751,12 +758,12 @@ cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t stream, bool programmat
       return cudaErrorInvalidValue;
   }
   cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, p.num_rows);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int n = 0;
