@@ -34,6 +34,45 @@ def test_every_declared_symbol_is_exported(lib):
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
 
 
+def header_structs():
+    """Field names and C types of every struct typedef in include/msa.h, in order."""
+    src = open(os.path.join(ROOT, "include", "msa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for name, body in re.findall(r"typedef struct (\w+) \{(.*?)\} \1;", src, flags=re.S):
+        fields = []
+        for decl in body.split(";"):
+            decl = " ".join(decl.split())
+            if decl:
+                m = re.match(r"(.*?)(\w+)$", decl)
+                fields.append((m.group(2), m.group(1).replace(" ", "")))
+        out[name] = fields
+    return out
+
+
+def test_struct_layouts_match_header():
+    # the ctypes mirrors in the binding follow the header field by field:
+    # same names, same order, and a pointer / 64-bit / 32-bit / float kind
+    # per field, so a field added to one side alone fails here
+    from block_sparse_paged_02_gb300 import binding as B
+    structs = header_structs()
+    assert set(structs) == {"msa_batch", "msa_attn_args", "msa_trace", "msa_index_cache",
+                            "msa_mla_args"}
+    for name, fields in structs.items():
+        py = getattr(B, name)._fields_
+        assert [f for f, _ in fields] == [f for f, _ in py], name
+        for (f, ctype), (_, pytype) in zip(fields, py):
+            if "*" in ctype or ctype in ("cudaEvent_t", "cudaStream_t"):
+                assert pytype is ctypes.c_void_p, (name, f)
+            elif ctype == "float":
+                assert pytype is ctypes.c_float, (name, f)
+            elif ctype in ("int64_t", "size_t"):
+                assert ctypes.sizeof(pytype) == 8, (name, f)
+            else:
+                assert ctype in ("int32_t", "uint32_t", "int"), (name, f, ctype)
+                assert ctypes.sizeof(pytype) == 4, (name, f)
+
+
 def test_status_strings(lib):
     from block_sparse_paged_02_gb300 import binding as B
     for code in range(7):
