@@ -370,13 +370,13 @@ __global__ void __maxnreg__(128)
           }
           fence_after();
           if (stage_valid[s]) {
-            const uint32_t b_base = smem_u32(smem + C::kB + s * C::kTileBytes);
+            const uint64_t bd = tc::desc_kmajor_sw128(smem_u32(smem + C::kB + s * C::kTileBytes));
             const uint32_t a_tm = tmem + kTmemA + abuf * 64u;
 #pragma unroll
             for (int kk = 0; kk < C::kKSteps; ++kk) {
               const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-              tc::mma_ts(tmem + buf * 128u, a_tm + kk * 8, tc::desc_kmajor_sw128(b_base + off),
-                         kIdesc, kk > 0 ? 1u : 0u);
+              tc::mma_ts(tmem + buf * 128u, a_tm + kk * 8, tc::desc_advance(bd, off), kIdesc,
+                         kk > 0 ? 1u : 0u);
             }
           }
           commit(&b_empty[s]);

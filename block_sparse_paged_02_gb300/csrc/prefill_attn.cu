@@ -589,13 +589,13 @@ __global__ void __maxnreg__(128)
           ok = ok && (j < 2 || mbar_wait(&o_full[buf], ((j >> 1) - 1) & 1));
           if (!ok) break;
           tc::fence_after();
-          const uint32_t qa = smem_u32(smem + kSmQ + qs * kTile);
-          const uint32_t ka = smem_u32(smem + kSmK + cur_kvs * kTile);
+          const uint64_t qd = tc::desc_kmajor_sw128(smem_u32(smem + kSmQ + qs * kTile));
+          const uint64_t kd = tc::desc_kmajor_sw128(smem_u32(smem + kSmK + cur_kvs * kTile));
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            tc::mma_ss(tmem + buf * 128, tc::desc_kmajor_sw128(qa + off),
-                       tc::desc_kmajor_sw128(ka + off), kIdescS, kk > 0 ? 1u : 0u);
+            tc::mma_ss(tmem + buf * 128, tc::desc_advance(qd, off), tc::desc_advance(kd, off),
+                       kIdescS, kk > 0 ? 1u : 0u);
           }
           tc::commit(&q_empty[qs]);
           tc::commit(&s_full[buf]);
@@ -625,11 +625,11 @@ __global__ void __maxnreg__(128)
                (i < 2 || mbar_wait(&o_empty[pb], ((i >> 1) - 1) & 1));
           if (!ok) break;
           tc::fence_after();
-          const uint32_t va = smem_u32(smem + kSmV + cur_kvs * kTile);
+          const uint64_t vd = tc::desc_mnmajor_sw128(smem_u32(smem + kSmV + cur_kvs * kTile), kHalf);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             tc::mma_ts(tmem + 256 + pb * 128, tmem + pb * 128 + kk * 8,
-                       tc::desc_mnmajor_sw128(va + kk * 2048, kHalf), kIdescO, kk > 0 ? 1u : 0u);
+                       tc::desc_advance(vd, kk * 2048), kIdescO, kk > 0 ? 1u : 0u);
           tc::commit(&o_full[pb]);
           const int before = cur.it;
           cur.next(p);

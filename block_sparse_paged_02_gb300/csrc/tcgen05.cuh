@@ -43,6 +43,14 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// The descriptor of the same operand `bytes` further on (a multiple of 16):
+// the start address sits in the low 14 bits as address / 16, and shared
+// addresses stay below 2^18, so the add never carries into other fields.
+// One 64-bit add per MMA instead of rebuilding the descriptor.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
 // Shared-memory matrix descriptor of an MN-major operand with the 128-byte
 // swizzle: each K index is a row of 64 consecutive MN elements (128 B); 8
 // such rows form a 1024-byte atom; atoms follow each other every 1024 B
