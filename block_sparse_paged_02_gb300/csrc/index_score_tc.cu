@@ -7,32 +7,37 @@
 // each query row and 128-token block, the max over the block's visible
 // tokens of idx_q[row] . idx_k[token].
 //
-// When a request brings >= kTcMinRows query rows, 128 rows x 128 tokens x Di
-// is a real dense tile: D = Q_tile . K_block^T runs as tcgen05.mma
-// (kind::f16, bf16 in, fp32 accumulate in TMEM), and the epilogue reduces
-// each TMEM lane (= query row) to its causal-masked max.  Integer-valued
-// index vectors keep every partial sum an exact fp32 integer, so the scores
-// equal the CUDA-core kernel's and the oracle's bit for bit.
+// When a request brings >= kTcMinRows query rows, 128 rows x 256 tokens x Di
+// is a real dense tile: D = Q_tile . [K_block0; K_block1]^T runs as
+// tcgen05.mma (kind::f16, M128 N256, bf16 in, fp32 accumulate in TMEM), and
+// the epilogue reduces each TMEM lane (= query row) to its causal-masked
+// max per block.  Integer-valued index vectors keep every partial sum an
+// exact fp32 integer, so the scores equal the CUDA-core kernel's and the
+// oracle's bit for bit.
 //
-// CTA roles (persistent grid, one CTA per SM, work = the flat list of
-// (request, 128-row tile, block) items split evenly across CTAs):
-//   warp 0  TMA producer: the K block of each item, 128-byte-swizzled
-//           tiles via cp.async.bulk.tensor into a 4-stage ring with
-//           mbarrier completion;
-//   warps 10-13 load each row tile's 128 index queries into TMEM (two
-//           buffers): the A operand, reused by every block of the tile,
-//           so the MMAs read only the K tile from shared memory (with both
-//           operands there, M128 N128 MMAs plus the tile copies saturate
-//           the shared-memory port);
-//   warp 1  allocates 512 TMEM columns (two 128-column accumulators, two
-//           query tiles); one thread of warp 1 and one of warp 14 issue the
-//           MMAs of alternate items and commit (one issuing thread left the
-//           tensor pipe idle while it waited and did its per-item
-//           bookkeeping);
-//   warps 2-9 epilogue: every item by all eight, the two warps of a TMEM
-//           lane quarter taking 64 columns each (tcgen05.ld, masked max),
-//           one of them storing the 32 rows' scores; each releases the
-//           accumulator once it holds its columns in registers.
+// Work = the flat list of (request, 128-row tile, pair of consecutive
+// blocks) items, split evenly across a persistent grid of one CTA per SM.
+// Two blocks per MMA: the issuing thread spends ~100 cycles on each
+// tcgen05.mma whatever its size, and an M128 N128 K16 step keeps the
+// tensor pipe busy for only 64, so with one block per MMA the pipe waited
+// on the issue; M128 N256 gives it 128 cycles of work per instruction.
+// CTA roles:
+//   warp 0  TMA producer: the two K blocks of each item, 128-byte-swizzled
+//           tiles via cp.async.bulk.tensor into a 4-slot ring, mbarrier
+//           completion; a slot holds one 64-dim swizzle atom of a pair
+//           (block 0's 128 rows, then block 1's: one 256-row operand), so
+//           a Di = 128 item takes two slots, and the first is refilled as
+//           soon as the MMAs of its 64 dims are done;
+//   warps 10-13 store each row tile's 128 index queries into shared memory
+//           in the same swizzled layout (two buffers): the A operand, reused
+//           by every pair of the tile;
+//   warp 1  allocates the 512 TMEM columns (two 256-column accumulators);
+//           one thread of warp 1 and one of warp 14 issue the MMAs of
+//           alternate items and commit, each owning one ring stage in two
+//           and one accumulator;
+//   warps 2-9 epilogue: warps 2-5 reduce block 0 of every item, warps 6-9
+//           block 1, each warp the 32 query rows of its TMEM lane quarter
+//           (tcgen05.ld, masked max) and storing their scores.
 // Every wait is bounded; on expiry the kernel records MSA_DEV_TIMEOUT, stops
 // issuing work and still frees its TMEM.
 #include "tcgen05.cuh"
@@ -40,91 +45,48 @@
 namespace msa {
 namespace {
 
-constexpr int kTcStages = 4;
-// threads issuing the MMAs: with two, items alternate between them, so one
-// issues while the other waits and does its per-item bookkeeping
-#ifndef MSA_TC_ISSUERS
-#define MSA_TC_ISSUERS 2
-#endif
-constexpr int kIssuers = MSA_TC_ISSUERS;
-static_assert(kIssuers == 1 || kIssuers == 2, "one or two MMA issuers");
+// two threads issue the MMAs: items alternate between them, so one issues
+// while the other waits and does its per-item bookkeeping
+constexpr int kIssuers = 2;
 // warps: copies, MMA, 2 x 4 epilogue, 4 query loaders, the second MMA issuer
-constexpr int kTcThreads = 32 * (13 + kIssuers);
+constexpr int kTcThreads = 32 * 15;
 constexpr int kIssuerWarp2 = 14;
 constexpr int kTileRows = 128;
-// epilogue: every item drained by all eight warps, two per TMEM lane quarter
-// taking 64 columns each (1), or by one group of four on alternate items (0)
-#ifndef MSA_TC_EPI_SPLIT
-#define MSA_TC_EPI_SPLIT 1
-#endif
-constexpr bool kEpiSplit = MSA_TC_EPI_SPLIT != 0;
-// 128-column fp32 accumulators in TMEM: with two issuers each owns one
-// (three shared ones, safe with the in-order epilogue, measured slower)
-constexpr int kAccBufs = kIssuers == 2 ? 2 : 3;
-constexpr uint32_t kTmemA = 128 * kAccBufs;  // then two query tiles (A operands), 64 columns each
-static_assert(kTcStages % kIssuers == 0 && kAccBufs % kIssuers == 0,
-              "each ring stage and accumulator belongs to one issuer");
-constexpr uint32_t kTmemCols = 512;
+constexpr int kPairCols = 2 * kBlock;  // accumulator columns of one item
+constexpr int kAccBufs = 2;            // one per issuer
+constexpr uint32_t kTmemCols = kAccBufs * kPairCols;
 
 template <int DI>
 struct TcCfg {
   static constexpr int kHalves = DI / 64;          // 128-byte swizzle atoms along K
-  static constexpr int kTileBytes = kTileRows * DI * 2;
-  static constexpr int kHalfBytes = kTileRows * 128;
-  static constexpr int kKSteps = DI / 16;
-  static constexpr int kACols = DI / 2;            // a query row in TMEM: bf16 pairs
-  // smem: B ring, then barriers / bookkeeping, then request prefix
+  static constexpr int kTileBytes = kTileRows * DI * 2;  // one block (or the query tile)
+  static constexpr int kHalfBytes = kTileRows * 128;     // one atom column of 128 rows
+  static constexpr int kStageBytes = 2 * kHalfBytes;     // a ring slot: one atom column of the pair's 256 rows
+  static constexpr int kStages = 4;
+  static constexpr int kAtomSteps = 4;                   // K16 steps per atom column
+  // smem: B ring, A (query) buffers, then barriers / bookkeeping, then request prefix
   static constexpr int kB = 0;
-  static constexpr int kBars = kB + kTcStages * kTileBytes;
-  // b_full / b_empty [kTcStages], a_full / a_empty [2], acc_full / acc_empty [kAccBufs]
-  static constexpr int kNumBars = 2 * kTcStages + 4 + 2 * kAccBufs;
+  static constexpr int kA = kB + kStages * kStageBytes;
+  static constexpr int kBars = kA + 2 * kTileBytes;
+  // b_full / b_empty [kStages], a_full / a_empty [2], acc_full / acc_empty [kAccBufs]
+  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAccBufs;
   static constexpr int kMisc = kBars + kNumBars * 8;
-  static constexpr int kRed = kMisc + 64;  // [2][128] floats: the split epilogue's hand-off
-  static constexpr int kPrefix = kRed + 2 * kTileRows * 4;
-  static_assert(8 + kTcStages <= 16, "misc area holds 16 ints");
+  static constexpr int kPrefix = kMisc + 64;
+  static_assert(8 + kStages <= 16, "misc area holds 16 ints");
+  // slot u = item * kHalves + h: with items alternating between the
+  // issuers, each slot is used by one issuer, in order
+  static_assert(kStages % (kIssuers * kHalves) == 0, "each ring slot belongs to one issuer");
   static size_t bytes(int num_reqs) { return 1024 + kPrefix + (size_t)(num_reqs + 1) * 4; }
 };
-
-// Max over 64 accumulator columns loaded into ra (0..31) and rb (32..63),
-// columns c <= last only when MASKED.
-template <bool MASKED>
-__device__ __forceinline__ float row_max64(const uint32_t (&ra)[32], const uint32_t (&rb)[32],
-                                           int last) {
-  float g8[8];
-#pragma unroll
-  for (int x = 0; x < 8; ++x) g8[x] = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    if (!MASKED || i <= last) g8[i & 7] = fmaxf(g8[i & 7], __uint_as_float(ra[i]));
-    if (!MASKED || 32 + i <= last) g8[i & 7] = fmaxf(g8[i & 7], __uint_as_float(rb[i]));
-  }
-  return fmaxf(fmaxf(fmaxf(g8[0], g8[1]), fmaxf(g8[2], g8[3])),
-               fmaxf(fmaxf(g8[4], g8[5]), fmaxf(g8[6], g8[7])));
-}
-
-// The two epilogue warps of one TMEM lane quarter (named barrier 1 + quarter,
-// 64 threads): AND of a predicate over both, and a plain rendezvous.
-__device__ __forceinline__ bool pair_and(bool v, int id) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, %2, 64, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void pair_sync(int id) {
-  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
-}
 
 using tc::commit;
 using tc::fence_after;
 using tc::fence_before;
-using tc::tmem_ld32;
 
-// Instruction descriptor of the score tile: M = 128 rows, N = 128 tokens.
-constexpr uint32_t kIdesc = tc::idesc_bf16(128, 128, 0);
+// Instruction descriptors of the score tile: M = 128 rows, N = 256 tokens
+// (a pair), or 128 when the tile's last item holds a single block.
+constexpr uint32_t kIdescPair = tc::idesc_bf16(128, kPairCols, 0);
+constexpr uint32_t kIdescOne = tc::idesc_bf16(128, kBlock, 0);
 
 // Max over the 128 accumulator columns of this thread's lane at ta, columns
 // c <= last only when MASKED (a block holding some row's own position);
@@ -155,10 +117,10 @@ __device__ __forceinline__ float row_max128(uint32_t ta, int last) {
 
 // ------------------------------------------------------------ work cursor
 
-// Walks the (request, row tile, block) items of the tensor-core requests in
-// order.  prefix[q] = items before request q (smem).
+// Walks the (request, row tile, block pair) items of the tensor-core
+// requests in order.  prefix[q] = items before request q (smem).
 struct Cursor {
-  int q, tile, blk, nb, ntiles, q0, qlen, ctx;
+  int q, tile, pr, np, nbk, ntiles, q0, qlen, ctx;
 
   __device__ void load_request(const msa_batch& b) {
     q0 = b.cu_seqlens_q[q];
@@ -166,9 +128,11 @@ struct Cursor {
     ctx = b.context_lens[q];
     ntiles = (qlen + kTileRows - 1) / kTileRows;
   }
-  __device__ int tile_blocks(int t) const {
+  __device__ void set_tile(int t) {
+    tile = t;
     const int last_row = min(t * kTileRows + kTileRows - 1, qlen - 1);
-    return (ctx + last_row) / kBlock + 1;
+    nbk = (ctx + last_row) / kBlock + 1;  // blocks the tile's last row sees
+    np = (nbk + 1) >> 1;
   }
   __device__ void seek(const msa_batch& b, const int* prefix, int R, int item) {
     int lo = 0, hi = R;  // largest q with prefix[q] <= item
@@ -180,27 +144,29 @@ struct Cursor {
     q = lo;
     load_request(b);
     int rem = item - prefix[q];
-    tile = 0;
-    nb = tile_blocks(0);
-    while (rem >= nb) {
-      rem -= nb;
-      ++tile;
-      nb = tile_blocks(tile);
+    set_tile(0);
+    while (rem >= np) {
+      rem -= np;
+      set_tile(tile + 1);
     }
-    blk = rem;
+    pr = rem;
   }
   __device__ void next(const msa_batch& b, const int* prefix, int R) {
-    if (++blk < nb) return;
-    blk = 0;
-    if (++tile < ntiles) {
-      nb = tile_blocks(tile);
+    if (++pr < np) return;
+    pr = 0;
+    if (tile + 1 < ntiles) {
+      set_tile(tile + 1);
       return;
     }
     do { ++q; } while (q < R - 1 && prefix[q + 1] == prefix[q]);  // skip item-less requests
     if (q >= R) return;
     load_request(b);
-    tile = 0;
-    nb = tile_blocks(0);
+    set_tile(0);
+  }
+  // page of block e (0 or 1) of the current pair; -2 when the pair has no such block
+  __device__ int page(const msa_batch& b, int e) const {
+    const int blk = 2 * pr + e;
+    return blk < nbk ? b.block_table[(long long)q * b.bt_stride + blk] : -2;
   }
 };
 
@@ -210,19 +176,22 @@ template <int DI>
 __global__ void __maxnreg__(128)
     index_score_tc_kernel(const ScoreLaunch p, const __grid_constant__ CUtensorMap kmap) {
   using C = TcCfg<DI>;
+  constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBars);
-  uint64_t* b_full = bars;                   // [kTcStages]
-  uint64_t* b_empty = bars + kTcStages;      // [kTcStages]
-  uint64_t* a_full = bars + 2 * kTcStages;   // [2]
+  uint64_t* b_full = bars;                   // [S]
+  uint64_t* b_empty = bars + S;              // [S]
+  uint64_t* a_full = bars + 2 * S;           // [2]
   uint64_t* a_empty = a_full + 2;            // [2]
   uint64_t* acc_full = a_empty + 2;          // [kAccBufs]
   uint64_t* acc_empty = acc_full + kAccBufs; // [kAccBufs]
   int* misc = reinterpret_cast<int*>(smem + C::kMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 4);
-  int* stage_valid = misc + 8;  // [kTcStages], written by the producer before arming
+  // [S] bit e = block e loaded, bit 2 = the pair has a block 1; written by
+  // the producer before arming the slot
+  int* stage_valid = misc + 8;
   int* prefix = reinterpret_cast<int*>(smem + C::kPrefix);
 
   const msa_batch& b = p.batch;
@@ -234,17 +203,17 @@ __global__ void __maxnreg__(128)
     misc[0] = !(b.cu_seqlens_q[0] == 0 && b.cu_seqlens_q[R] == b.num_rows);
     misc[1] = 0;  // timeout seen
     misc[2] = 0;  // per-request status bits
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&a_full[i], 4);  // the four query-loader warps
+      mbar_init(&a_full[i], 4);          // the four query-loader warps
       mbar_init(&a_empty[i], kIssuers);  // each issuer commits once per row tile
     }
     for (int i = 0; i < kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kEpiSplit ? 8 : 4);  // the epilogue warps draining it
+      mbar_init(&acc_empty[i], 8);  // the eight epilogue warps
     }
     fence_barrier_init();
   }
@@ -258,7 +227,7 @@ __global__ void __maxnreg__(128)
     if (!bad && ql >= kTcMinRows) {
       for (int t = 0; t * kTileRows < ql; ++t) {
         const int last_row = min(t * kTileRows + kTileRows - 1, ql - 1);
-        items += (ctx + last_row) / kBlock + 1;
+        items += ((ctx + last_row) / kBlock + 2) >> 1;
       }
     }
     prefix[q + 1] = items;
@@ -297,38 +266,42 @@ __global__ void __maxnreg__(128)
   if (n_items > 0) {
     if (warp == 0) {
       // ---------------- TMA producer warp: lanes look up 32 items at a time
-      // (request, tile, block, page id); one elected lane then arms the
+      // (request, tile, pair, two page ids); one elected lane then arms the
       // stages and issues the tile copies in order
       bool stop = false;
       for (int j0 = 0; j0 < n_items && !stop; j0 += 32) {
-        int mpage = -1;
+        int mpage0 = -1, mpage1 = -2;
         if (j0 + lane < n_items) {
           Cursor cur;
           cur.seek(b, prefix, R, i0 + j0 + lane);
-          mpage = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
+          mpage0 = cur.page(b, 0);
+          mpage1 = cur.page(b, 1);
         }
         const int cnt = min(32, n_items - j0);
         for (int jj = 0; jj < cnt; ++jj) {
           const int j = j0 + jj;
-          const int page = __shfl_sync(0xffffffffu, mpage, jj);
+          const int page0 = __shfl_sync(0xffffffffu, mpage0, jj);
+          const int page1 = __shfl_sync(0xffffffffu, mpage1, jj);
           int ok = 1;
           if (lane == 0) {
-            const int s = j % kTcStages;
-            if (ok && j >= kTcStages && !mbar_wait(&b_empty[s], ((j / kTcStages) - 1) & 1))
-              ok = 0;
-            if (ok) {
-              const bool valid = page >= 0 && page < b.num_pages;
-              stage_valid[s] = valid;
-              if (valid) {
-                mbar_arrive_expect_tx(&b_full[s], C::kTileBytes);
-                for (int h = 0; h < C::kHalves; ++h)
-                  tma_load_2d(smem + C::kB + s * C::kTileBytes + h * C::kHalfBytes, &kmap, 64 * h,
-                              page * kBlock, &b_full[s]);
+            const bool v0 = page0 >= 0 && page0 < b.num_pages;
+            const bool v1 = page1 >= 0 && page1 < b.num_pages;
+            for (int h = 0; h < C::kHalves && ok; ++h) {
+              const int u = j * C::kHalves + h, s = u % S;
+              if (u >= S && !mbar_wait(&b_empty[s], ((u / S) - 1) & 1)) {
+                ok = 0;
+                misc[1] = 1;
+                break;
+              }
+              stage_valid[s] = (v0 ? 1 : 0) | (v1 ? 2 : 0) | (page1 != -2 ? 4 : 0);
+              if (v0 || v1) {
+                uint8_t* st = smem + C::kB + s * C::kStageBytes;
+                mbar_arrive_expect_tx(&b_full[s], (v0 + v1) * C::kHalfBytes);
+                if (v0) tma_load_2d(st, &kmap, 64 * h, page0 * kBlock, &b_full[s]);
+                if (v1) tma_load_2d(st + C::kHalfBytes, &kmap, 64 * h, page1 * kBlock, &b_full[s]);
               } else {
                 mbar_arrive(&b_full[s]);  // nothing to load; the epilogue writes -inf
               }
-            } else {
-              misc[1] = 1;
             }
           }
           if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -337,12 +310,12 @@ __global__ void __maxnreg__(128)
           }
         }
       }
-    } else if ((warp == 1 || (kIssuers == 2 && warp == kIssuerWarp2)) && lane == 0) {
-      // ---------------- MMA issuer(s): D = Q_tile (TMEM) x K_block^T (shared).
-      // Issuer ii takes items j = ii mod kIssuers: ring stages and
-      // accumulators are then each used by one issuer, in order.  Both walk
-      // every row tile: each waits for its queries and commits once to its
-      // release (after its own MMAs of the tile, if any).
+    } else if ((warp == 1 || warp == kIssuerWarp2) && lane == 0) {
+      // ---------------- MMA issuers: D = Q_tile x [K_block0; K_block1]^T, both
+      // operands in shared memory.  Issuer ii takes items j = ii mod 2: ring
+      // stages and accumulators are then each used by one issuer, in order.
+      // Both walk every row tile: each waits for its queries and commits
+      // once to their release (after its own MMAs of the tile, if any).
       const int ii = warp == 1 ? 0 : 1;
       Cursor cur;
       cur.seek(b, prefix, R, i0);
@@ -359,27 +332,36 @@ __global__ void __maxnreg__(128)
           ++a_seq;
         }
         if (j % kIssuers == ii) {
-          const int s = j % kTcStages, buf = j % kAccBufs;
+          const int buf = j % kAccBufs;
           if (j >= kAccBufs && !mbar_wait(&acc_empty[buf], ((j / kAccBufs) - 1) & 1)) {
             misc[1] = 1;
             break;
           }
-          if (!mbar_wait(&b_full[s], (j / kTcStages) & 1)) {
+          const uint64_t ad = tc::desc_kmajor_sw128(smem_u32(smem + C::kA + abuf * C::kTileBytes));
+          bool stop = false;
+          for (int h = 0; h < C::kHalves; ++h) {
+            const int u = j * C::kHalves + h, s = u % S;
+            if (!mbar_wait(&b_full[s], (u / S) & 1)) {
+              stop = true;
+              break;
+            }
+            fence_after();
+            const int sv = stage_valid[s];
+            if (sv & 3) {
+              const uint64_t bd = tc::desc_kmajor_sw128(smem_u32(smem + C::kB + s * C::kStageBytes));
+              const uint32_t idesc = (sv & 4) ? kIdescPair : kIdescOne;
+#pragma unroll
+              for (int kk = 0; kk < C::kAtomSteps; ++kk)
+                tc::mma_ss(tmem + buf * kPairCols,
+                           tc::desc_advance(ad, h * C::kHalfBytes + kk * 32),
+                           tc::desc_advance(bd, kk * 32), idesc, (h | kk) ? 1u : 0u);
+            }
+            commit(&b_empty[s]);
+          }
+          if (stop) {
             misc[1] = 1;
             break;
           }
-          fence_after();
-          if (stage_valid[s]) {
-            const uint64_t bd = tc::desc_kmajor_sw128(smem_u32(smem + C::kB + s * C::kTileBytes));
-            const uint32_t a_tm = tmem + kTmemA + abuf * 64u;
-#pragma unroll
-            for (int kk = 0; kk < C::kKSteps; ++kk) {
-              const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-              tc::mma_ts(tmem + buf * 128u, a_tm + kk * 8, tc::desc_advance(bd, off), kIdesc,
-                         kk > 0 ? 1u : 0u);
-            }
-          }
-          commit(&b_empty[s]);
           commit(&acc_full[buf]);
         }
         Cursor nx = cur;
@@ -389,16 +371,17 @@ __global__ void __maxnreg__(128)
       }
     } else if (warp >= 10 && warp < 14) {
       // ---------------- query loaders: each row tile of the CTA's items into
-      // TMEM (lane = query row, column c = dims 2c, 2c+1), double-buffered;
-      // rows past the request's end are zero
+      // shared memory, double-buffered, in the 128-byte-swizzled K-major
+      // layout the MMA reads (row m's 16-byte chunk c of atom column h at
+      // h * 16 KB + m * 128 + 16 * (c ^ (m & 7))); rows past the request's
+      // end are zero
       const int quarter = warp & 3;
       const int m = quarter * 32 + lane;
-      const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
       Cursor cur;
       cur.seek(b, prefix, R, i0);
       int a_seq = 0;
       for (int j = 0; j < n_items; ++j) {
-        const bool new_tile = j == 0 || cur.blk == 0;  // a tile's items start at block 0
+        const bool new_tile = j == 0 || cur.pr == 0;  // a tile's items start at pair 0
         if (new_tile) {
           const int ab = a_seq & 1;
           if (a_seq >= 2 && !__all_sync(0xffffffffu, mbar_wait(&a_empty[ab], ((a_seq >> 1) - 1) & 1))) {
@@ -408,102 +391,38 @@ __global__ void __maxnreg__(128)
           const int row = cur.tile * kTileRows + m;
           const uint4* src = reinterpret_cast<const uint4*>(p.idx_q + (long long)(cur.q0 + row) * DI);
           const bool have = row < cur.qlen;
+          uint8_t* dst = smem + C::kA + ab * C::kTileBytes + m * 128;
 #pragma unroll
-          for (int c = 0; c < C::kACols / 16; ++c) {
-            uint32_t w[16];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const uint4 v = have ? __ldg(src + 4 * c + x) : make_uint4(0u, 0u, 0u, 0u);
-              w[4 * x] = v.x;
-              w[4 * x + 1] = v.y;
-              w[4 * x + 2] = v.z;
-              w[4 * x + 3] = v.w;
-            }
-            tc::tmem_st16(tmem + lanes + kTmemA + ab * 64u + 16 * c, w);
+          for (int c = 0; c < DI / 8; ++c) {
+            const uint4 v = have ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(dst + (c >> 3) * C::kHalfBytes + 16 * ((c & 7) ^ (m & 7))) = v;
           }
-          tc::tmem_wait_st();
-          fence_before();
+          fence_proxy_async_smem();  // generic stores before the MMA's async reads
           __syncwarp();
           if (lane == 0) mbar_arrive(&a_full[ab]);
           ++a_seq;
         }
         cur.next(b, prefix, R);
       }
-    } else if (kEpiSplit && warp >= 2 && warp < 10) {
-      // ---------------- epilogue: every item by all eight warps.  The two
-      // warps of lane quarter w % 4 (= 32 query rows) take columns 0..63 and
-      // 64..127 of the accumulator; the second hands its 32 maxima to the
-      // first through shared memory, which stores the scores.  Both decide
-      // together whether to go on (a timed-out wait ends both), so neither
-      // is left at their barrier.
-      const int half = (warp - 2) >> 2, quarter = warp & 3, bar_id = 1 + quarter;
+    } else if (warp >= 2 && warp < 10) {
+      // ---------------- epilogue: warps 2-5 reduce block 0 of every item
+      // (accumulator columns 0..127), warps 6-9 block 1 (128..255); warp w
+      // reads TMEM lanes 32 (w % 4) .. +31 = 32 query rows, each reduced to
+      // its causal-masked max.  Blocks every row of the warp sees in full
+      // skip the mask; the next item's page id is loaded while this one is
+      // reduced.
+      const int e = (warp - 2) >> 2, quarter = warp & 3;
       const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
-      float* red = reinterpret_cast<float*>(smem + C::kRed);  // maxima of the second half
       Cursor cur;
       cur.seek(b, prefix, R, i0);
-      int page = b.block_table[(long long)cur.q * b.bt_stride + cur.blk];
+      int page = cur.page(b, e);
       for (int j = 0; j < n_items; ++j) {
         const int buf = j % kAccBufs;
         Cursor nx = cur;
         int page_nx = 0;
         if (j + 1 < n_items) {
           nx.next(b, prefix, R);
-          page_nx = b.block_table[(long long)nx.q * b.bt_stride + nx.blk];
-        }
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (j / kAccBufs) & 1));
-        if (!pair_and(ok, bar_id)) {
-          misc[1] = 1;
-          break;
-        }
-        fence_after();
-        const int m = quarter * 32 + lane;
-        const int row_in_req = cur.tile * kTileRows + m;
-        const int pos = cur.ctx + row_in_req;
-        const bool page_ok = page >= 0 && page < b.num_pages;
-        const int last = pos - cur.blk * kBlock - 64 * half;  // visible columns of this half
-        const uint32_t ta = tmem + lanes + buf * 128u + 64u * half;
-        uint32_t ra[32], rb[32];
-        tc::tmem_ld32_issue(ta, ra);
-        tc::tmem_ld32_issue(ta + 32, rb);
-        tc::tmem_wait_ld(ra);
-        tc::tmem_wait_ld(rb);
-        // the columns are in registers: the accumulator is free again
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        float best = __all_sync(0xffffffffu, last >= 63) ? row_max64<false>(ra, rb, last)
-                                                         : row_max64<true>(ra, rb, last);
-        if (half == 1) red[(j & 1) * kTileRows + m] = best;
-        pair_sync(bar_id);
-        if (half == 0) {
-          best = fmaxf(best, red[(j & 1) * kTileRows + m]);
-          if (row_in_req < cur.qlen && last >= 0)
-            p.scores[(long long)(cur.q0 + row_in_req) * p.score_stride + cur.blk] =
-                page_ok ? best : -INFINITY;
-        }
-        cur = nx;
-        page = page_nx;
-      }
-    } else if (!kEpiSplit && warp >= 2 && warp < 10) {
-      // ---------------- epilogue: two groups of four warps take alternate
-      // items (accumulator j % 4); warp w reads TMEM lanes 32 (w % 4) .. +31
-      // = 32 query rows, each reduced to its causal-masked max over the 128
-      // token columns.  Blocks every row of the warp sees in full skip the
-      // mask; the next item's page id is loaded while this one is reduced.
-      const int grp = (warp - 2) >> 2, quarter = warp & 3;
-      const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
-      Cursor cur;
-      cur.seek(b, prefix, R, i0);
-      if (grp == 1 && n_items > 1) cur.next(b, prefix, R);
-      int page = grp < n_items ? b.block_table[(long long)cur.q * b.bt_stride + cur.blk] : 0;
-      for (int j = grp; j < n_items; j += 2) {
-        const int buf = j % kAccBufs;
-        Cursor nx = cur;
-        int page_nx = 0;
-        if (j + 2 < n_items) {
-          nx.next(b, prefix, R);
-          nx.next(b, prefix, R);
-          page_nx = b.block_table[(long long)nx.q * b.bt_stride + nx.blk];
+          page_nx = nx.page(b, e);
         }
         // warp-uniform decision: tcgen05.ld below needs the whole warp
         if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (j / kAccBufs) & 1))) {
@@ -511,21 +430,22 @@ __global__ void __maxnreg__(128)
           break;
         }
         fence_after();
+        const int blk = 2 * cur.pr + e;
         const int m = quarter * 32 + lane;
         const int row_in_req = cur.tile * kTileRows + m;
-        const int pos = cur.ctx + row_in_req;
-        const bool page_ok = page >= 0 && page < b.num_pages;
-        const int last = pos - cur.blk * kBlock;  // visible columns: c <= last
-        const uint32_t ta = tmem + lanes + buf * 128u;
-        const float best = __all_sync(0xffffffffu, last >= kBlock - 1)
-                               ? row_max128<false>(ta, last)
-                               : row_max128<true>(ta, last);
+        const int last = cur.ctx + row_in_req - blk * kBlock;  // visible columns: c <= last
+        float best = -INFINITY;
+        if (page != -2) {  // the pair has this block
+          const uint32_t ta = tmem + lanes + buf * kPairCols + e * kBlock;
+          best = __all_sync(0xffffffffu, last >= kBlock - 1) ? row_max128<false>(ta, last)
+                                                             : row_max128<true>(ta, last);
+        }
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        if (row_in_req < cur.qlen && last >= 0)
-          p.scores[(long long)(cur.q0 + row_in_req) * p.score_stride + cur.blk] =
-              page_ok ? best : -INFINITY;
+        if (page != -2 && row_in_req < cur.qlen && last >= 0)
+          p.scores[(long long)(cur.q0 + row_in_req) * p.score_stride + blk] =
+              (page >= 0 && page < b.num_pages) ? best : -INFINITY;
         cur = nx;
         page = page_nx;
       }
