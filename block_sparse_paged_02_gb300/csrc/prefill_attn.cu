@@ -40,9 +40,11 @@
 // lanes and warp 15's gather the chunks' query rows), warp 1 allocates TMEM
 // and one of its threads issues the S MMAs, one thread of warp 14 the P V
 // MMAs, warps 2-5 and 6-9 are two softmax groups that take alternate
-// chunks, warps 10-13 store every chunk's O (S, P and O are double-buffered
-// in TMEM: 512 columns).  Every wait is bounded; on expiry the kernel
-// records MSA_DEV_TIMEOUT, stops and still frees its TMEM.
+// chunks, warps 10-13 store every chunk's O.  TMEM (512 columns): three
+// S / P buffers (chunk j in buffer j % 3, P over S) and one O, so S of
+// chunk j + 3 waits only for P V of chunk j while two later chunks are in
+// their softmax.  Every wait is bounded; on expiry the kernel records
+// MSA_DEV_TIMEOUT, stops and still frees its TMEM.
 #include <string.h>
 
 #include "tcgen05.cuh"
@@ -69,11 +71,15 @@ constexpr int kSmK = 0;
 constexpr int kSmV = kSmK + kKvStages * kTile;
 constexpr int kSmQ = kSmV + kKvStages * kTile;
 constexpr int kSmBars = kSmQ + kQStages * kTile;
-// kv_full[2] kv_empty[2] q_full[3] q_empty[3] s_full[2] p_full[2] o_full[2] o_empty[2] kv_fill
-constexpr int kNumBars = 2 * kKvStages + 2 * kQStages + 8 + 1;
+// kv_full[2] kv_empty[2] q_full[3] q_empty[3] s_full[3] sp_free[3] p_full[3] o_full o_empty
+// kv_fill
+constexpr int kSpBufs = 3;  // S / P buffers in TMEM
+constexpr int kNumBars = 2 * kKvStages + 2 * kQStages + 3 * kSpBufs + 2 + 1;
 constexpr int kSmMisc = kSmBars + kNumBars * 8;
 constexpr int kPaSmem = kSmMisc + 64 + 1024;  // + slack for the 1024-byte alignment
-constexpr uint32_t kTmemCols = 512;           // S[2] at 0 / 128, O[2] at 256 / 384
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmS = 0;    // S / P [3]: 128 fp32 columns each (P: bf16 pairs in the first 64)
+constexpr uint32_t kTmO = 384;  // O: 128 fp32 columns
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, 128, 0);
 constexpr uint32_t kIdescO = tc::idesc_bf16(128, 128, 1);
 constexpr float kLog2e = 1.4426950408889634f;
@@ -279,6 +285,19 @@ __device__ __forceinline__ void store_o32(uint4* dst, const uint32_t (&r)[32]) {
                    pack_bf16x2(__uint_as_float(r[8 * x + 6]), __uint_as_float(r[8 * x + 7])));
 }
 
+// 32 fp32 columns as 16 bf16 pairs
+__device__ __forceinline__ void pack32(const uint32_t (&r)[32], uint32_t* pk) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+}
+
+// 16 packed pairs (32 O columns of a lane) to dims chunks 0..3 of dst
+__device__ __forceinline__ void store_pk16(uint4* dst, const uint32_t* pk) {
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+    dst[kHeadSlots * x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+}
+
 // The softmax of one TMEM lane: 128 logits from column sa, warp-collective.
 // A block that holds some row's own position counts only its first `valid`
 // tokens (MASKED); the masked code performs exactly the same arithmetic
@@ -344,10 +363,12 @@ __device__ __forceinline__ float exp32(const uint32_t (&r)[32], float scale2, fl
   return ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
 }
 
-// P of the 128 columns written back over S (P group c takes columns 16c ..
-// 16c + 15, all read already), loads in flight; returns the sum of p
+// P of the 128 columns as bf16 pairs at pa (the 32 logits of load c give
+// columns 16c .. 16c + 15; with pa = sa, P lands on columns already read),
+// loads in flight; returns the sum of p
 template <bool MASKED>
-__device__ __forceinline__ float row_exp(uint32_t sa, float scale2, float m, int valid) {
+__device__ __forceinline__ float row_exp(uint32_t sa, uint32_t pa, float scale2, float m,
+                                         int valid) {
   uint32_t ra[32], rb[32], w[16];
   float l = 0.f;
   tc::tmem_ld32_issue(sa, ra);
@@ -356,23 +377,20 @@ __device__ __forceinline__ float row_exp(uint32_t sa, float scale2, float m, int
     tc::tmem_wait_ld(ra);
     tc::tmem_ld32_issue(sa + 32 * (c + 1), rb);
     l += exp32<MASKED>(ra, scale2, m, w, 32 * c, valid);
-    tc::tmem_st16(sa + 16 * c, w);
+    tc::tmem_st16(pa + 16 * c, w);
     tc::tmem_wait_ld(rb);
     if (c + 2 < 4) tc::tmem_ld32_issue(sa + 32 * (c + 2), ra);
     l += exp32<MASKED>(rb, scale2, m, w, 32 * c + 32, valid);
-    tc::tmem_st16(sa + 16 * (c + 1), w);
+    tc::tmem_st16(pa + 16 * (c + 1), w);
   }
   return l;
 }
 
-// (max of s * scale2, sum of p) of one lane
+// max of s * scale2 over one lane's logits = |scale2| * max(sign(scale2) * s)
 template <bool MASKED>
-__device__ __forceinline__ float2 row_softmax(uint32_t sa, float scale2, int valid, bool live) {
-  // max of s * scale2 = |scale2| * max(sign(scale2) * s)
-  float m = scale2 >= 0.f ? row_max<false, MASKED>(sa, valid) * scale2
-                          : row_max<true, MASKED>(sa, valid) * -scale2;
-  if (!live) m = 0.f;
-  return make_float2(m, row_exp<MASKED>(sa, scale2, m, valid));
+__device__ __forceinline__ float row_max_scaled(uint32_t sa, float scale2, int valid) {
+  return scale2 >= 0.f ? row_max<false, MASKED>(sa, valid) * scale2
+                       : row_max<true, MASKED>(sa, valid) * -scale2;
 }
 
 // (16 warps: four share a sub-partition's 16K registers, so at most 128
@@ -390,11 +408,12 @@ __global__ void __maxnreg__(128)
   uint64_t* kv_empty = kv_full + kKvStages;
   uint64_t* q_full = kv_empty + kKvStages;
   uint64_t* q_empty = q_full + kQStages;
-  uint64_t* s_full = q_empty + kQStages;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_full = p_full + 2;
-  uint64_t* o_empty = o_full + 2;
-  uint64_t* kv_fill = o_empty + 2;
+  uint64_t* s_full = q_empty + kQStages;   // [kSpBufs]
+  uint64_t* sp_free = s_full + kSpBufs;    // [kSpBufs]
+  uint64_t* p_full = sp_free + kSpBufs;    // [kSpBufs]
+  uint64_t* o_full = p_full + kSpBufs;
+  uint64_t* o_empty = o_full + 1;
+  uint64_t* kv_fill = o_empty + 1;
   int* misc = reinterpret_cast<int*>(smem + kSmMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 4);
 
@@ -411,12 +430,13 @@ __global__ void __maxnreg__(128)
       mbar_init(&q_full[s], 2);  // the two gathering warps
       mbar_init(&q_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSpBufs; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 4);  // the four warps of a softmax group
-      mbar_init(&o_full[s], 1);
-      mbar_init(&o_empty[s], 4);  // the four O-epilogue warps
+      mbar_init(&sp_free[s], 1);
+      mbar_init(&p_full[s], 4);  // the four warps of the chunk's softmax group
     }
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 4);  // the four O-epilogue warps
     mbar_init(kv_fill, 1);
     fence_barrier_init();
   }
@@ -569,8 +589,8 @@ __global__ void __maxnreg__(128)
       }
     } else if (warp == 1) {
       // ---------------- S = Q K^T issue (one thread).  S / P of chunk j live
-      // in TMEM columns 128 (j & 1); S(j) may overwrite its buffer once P V
-      // of chunk j - 2 has completed (o_full).  (One thread issuing both
+      // in TMEM columns 128 (j % 3); S(j) may overwrite its buffer once P V
+      // of chunk j - 3 has completed (sp_free).  (One thread issuing both
       // products was the kernel's bound: ~100 cycles per MMA instruction.)
       if (lane == 0) {
         Cursor cur;
@@ -579,14 +599,14 @@ __global__ void __maxnreg__(128)
         int kv_seq = 0, cur_kvs = 0;
         bool ok = true;
         for (int j = 0; j < nj; ++j) {
-          const int buf = j & 1, qs = j % kQStages;
+          const int buf = j % kSpBufs, qs = j % kQStages;
           if (j == 0 || cur.ci == 0) {
             cur_kvs = kv_seq & 1;
             ok = mbar_wait(&kv_full[cur_kvs], (kv_seq >> 1) & 1);
             ++kv_seq;
           }
           ok = ok && mbar_wait(&q_full[qs], (j / kQStages) & 1);
-          ok = ok && (j < 2 || mbar_wait(&o_full[buf], ((j >> 1) - 1) & 1));
+          ok = ok && (j < kSpBufs || mbar_wait(&sp_free[buf], ((j / kSpBufs) - 1) & 1));
           if (!ok) break;
           tc::fence_after();
           const uint64_t qd = tc::desc_kmajor_sw128(smem_u32(smem + kSmQ + qs * kTile));
@@ -594,8 +614,8 @@ __global__ void __maxnreg__(128)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            tc::mma_ss(tmem + buf * 128, tc::desc_advance(qd, off), tc::desc_advance(kd, off),
-                       kIdescS, kk > 0 ? 1u : 0u);
+            tc::mma_ss(tmem + kTmS + buf * 128, tc::desc_advance(qd, off),
+                       tc::desc_advance(kd, off), kIdescS, kk > 0 ? 1u : 0u);
           }
           tc::commit(&q_empty[qs]);
           tc::commit(&s_full[buf]);
@@ -604,10 +624,12 @@ __global__ void __maxnreg__(128)
         if (!ok) misc[1] = 1;
       }
     } else if (warp == kPvWarp) {
-      // ---------------- O = P V issue (one thread): O of chunk i in TMEM
-      // columns 256 + 128 (i & 1), once the epilogue has read O of chunk
-      // i - 2 (o_empty); after the last chunk of an item its K / V stage is
-      // released (its scores were read before that chunk's P was written).
+      // ---------------- O = P V issue (one thread): P of chunk i from TMEM
+      // columns 128 (i % 3), O into kTmO once the epilogue has read O of
+      // chunk i - 1 (o_empty); the S / P buffer is released to the S issuer
+      // (sp_free) and O handed to the epilogue (o_full) by commits.
+      // After the last chunk of an item its K / V stage is released (its
+      // scores were read before that chunk's P was written).
       if (lane == 0) {
         Cursor cur;
         cur.n_items = n_items;
@@ -615,22 +637,23 @@ __global__ void __maxnreg__(128)
         int kv_seq = 0, cur_kvs = 0;
         bool ok = true;
         for (int i = 0; i < nj; ++i) {
-          const int pb = i & 1;
+          const int pb = i % kSpBufs;
           if (i == 0 || cur.ci == 0) {
             cur_kvs = kv_seq & 1;
             ok = mbar_wait(&kv_full[cur_kvs], (kv_seq >> 1) & 1);
             ++kv_seq;
           }
-          ok = ok && mbar_wait(&p_full[pb], (i >> 1) & 1) &&
-               (i < 2 || mbar_wait(&o_empty[pb], ((i >> 1) - 1) & 1));
+          ok = ok && mbar_wait(&p_full[pb], (i / kSpBufs) & 1) &&
+               (i < 1 || mbar_wait(o_empty, (i - 1) & 1));
           if (!ok) break;
           tc::fence_after();
           const uint64_t vd = tc::desc_mnmajor_sw128(smem_u32(smem + kSmV + cur_kvs * kTile), kHalf);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            tc::mma_ts(tmem + 256 + pb * 128, tmem + pb * 128 + kk * 8,
+            tc::mma_ts(tmem + kTmO, tmem + kTmS + pb * 128 + kk * 8,
                        tc::desc_advance(vd, kk * 2048), kIdescO, kk > 0 ? 1u : 0u);
-          tc::commit(&o_full[pb]);
+          tc::commit(&sp_free[pb]);
+          tc::commit(o_full);
           const int before = cur.it;
           cur.next(p);
           if (i == nj - 1 || cur.it != before) tc::commit(&kv_empty[cur_kvs]);
@@ -655,7 +678,7 @@ __global__ void __maxnreg__(128)
       if (grp == 1 && nj > 1) cur.next(p);
       int e = (slot < cur.rows()) ? p.pf_lists[cur.list_base() + slot] : 0;
       for (int j = grp; j < nj; j += 2) {
-        const int buf = j & 1;
+        const int buf = j % kSpBufs;
         const int r = e >> 8, si = e & 255;
         const bool live = slot < cur.rows() && head < hq && r < p.batch.num_rows && si < p.topk;
         const int pos = r + cur.rec.z;
@@ -669,26 +692,27 @@ __global__ void __maxnreg__(128)
           nx.next(p);
           e_nx = (slot < nx.rows()) ? p.pf_lists[nx.list_base() + slot] : 0;
         }
-        if (!warp_wait(&s_full[buf], (j >> 1) & 1)) {
+        if (!warp_wait(&s_full[buf], (j / kSpBufs) & 1)) {
           misc[1] = 1;
           break;
         }
         tc::fence_after();
-        const uint32_t sa = tmem + lanes + buf * 128;
+        const uint32_t sa = tmem + lanes + kTmS + buf * 128;
         // Two passes over the 128 logits, 32 columns per load with the next
         // load in flight: the max, then p = 2^(x - max) written back over S
         // as bf16 and summed.  Whole blocks (every lane of the warp sees all
         // 128 tokens) take the unrolled path; a block holding some row's own
         // position takes a compact masked loop.
-        const float2 ml = whole ? row_softmax<false>(sa, scale2, kBlock, live)
-                                : row_softmax<true>(sa, scale2, valid, live);
-        const float m = ml.x, l = ml.y;
-        const float mx = m;
+        float m = whole ? row_max_scaled<false>(sa, scale2, kBlock)
+                        : row_max_scaled<true>(sa, scale2, valid);
+        if (!live) m = 0.f;
+        const float l = whole ? row_exp<false>(sa, sa, scale2, m, kBlock)
+                              : row_exp<true>(sa, sa, scale2, m, valid);
         tc::tmem_wait_st();
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[buf]);
-        if (live) p.part_ml[((long long)r * p.topk + si) * kHeadSlots + head] = make_float2(mx, l);
+        if (live) p.part_ml[((long long)r * p.topk + si) * kHeadSlots + head] = make_float2(m, l);
         cur = nx;
         e = e_nx;
       }
@@ -705,7 +729,6 @@ __global__ void __maxnreg__(128)
       cur.seek(p, c0);
       int e = (slot < cur.rows()) ? p.pf_lists[cur.list_base() + slot] : 0;
       for (int j = 0; j < nj; ++j) {
-        const int buf = j & 1;
         const int r = e >> 8, si = e & 255;
         const bool live = slot < cur.rows() && head < hq && r < p.batch.num_rows && si < p.topk;
         Cursor nx = cur;
@@ -714,7 +737,7 @@ __global__ void __maxnreg__(128)
           nx.next(p);
           e_nx = (slot < nx.rows()) ? p.pf_lists[nx.list_base() + slot] : 0;
         }
-        if (!warp_wait(&o_full[buf], (j >> 1) & 1)) {
+        if (!warp_wait(o_full, j & 1)) {
           misc[1] = 1;
           break;
         }
@@ -723,24 +746,29 @@ __global__ void __maxnreg__(128)
                          p.part_o + ((long long)r * p.topk + si) * kHeadSlots * kHeadDim) +
                      head;
         {
-          const uint32_t oa = tmem + lanes + 256 + buf * 128;
-          uint32_t ra[32], rb[32];
+          // O leaves tensor memory in two rounds of two loads in flight (the
+          // first 64 columns packed to bf16 meanwhile), and the buffer is
+          // released before any store: P V of the next chunk waits on it
+          const uint32_t oa = tmem + lanes + kTmO;
+          uint32_t ra[32], rb[32], pk[32];
           tc::tmem_ld32_issue(oa, ra);
-#pragma unroll 1
-          for (int c = 0; c < 4; c += 2) {
-            tc::tmem_wait_ld(ra);
-            tc::tmem_ld32_issue(oa + 32 * (c + 1), rb);
-            if (live) store_o32(dst + kHeadSlots * 4 * c, ra);
-            tc::tmem_wait_ld(rb);
-            if (c + 2 < 4) {
-              tc::tmem_ld32_issue(oa + 32 * (c + 2), ra);
-            } else {
-              // every column is in registers: the O buffer is free
-              tc::fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&o_empty[buf]);
-            }
-            if (live) store_o32(dst + kHeadSlots * 4 * (c + 1), rb);
+          tc::tmem_ld32_issue(oa + 32, rb);
+          tc::tmem_wait_ld(ra);
+          tc::tmem_wait_ld(rb);
+          pack32(ra, pk);
+          pack32(rb, pk + 16);
+          tc::tmem_ld32_issue(oa + 64, ra);
+          tc::tmem_ld32_issue(oa + 96, rb);
+          tc::tmem_wait_ld(ra);
+          tc::tmem_wait_ld(rb);
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_empty);
+          if (live) {
+            store_pk16(dst, pk);
+            store_pk16(dst + kHeadSlots * 4, pk + 16);
+            store_o32(dst + kHeadSlots * 4 * 2, ra);
+            store_o32(dst + kHeadSlots * 4 * 3, rb);
           }
         }
         cur = nx;
