@@ -340,10 +340,29 @@ __global__ void __launch_bounds__(256) topk_table_kernel_multi(const TopkLaunch 
 // row and a CTA of 8 warps shares the batch checks.  Lane l holds the KPL
 // consecutive blocks l*KPL .. l*KPL+KPL-1, so lane order is block order; the
 // k-th largest key comes from the same bit-by-bit search (one warp
-// reduction per bit, no barrier) and one warp scan of the packed (== T, > T)
-// counts places the selection, as in the CTA form above.
+// reduction per bit, no barrier), or, for 8 keys a lane and k <= 32, from k
+// rounds of extraction: each lane sorts its keys once (descending), then
+// every round takes the warp's largest head (one reduction) and the lowest
+// lane holding it drops its head, the k-th value taken being T.  Either way
+// one warp scan of the packed (== T, > T) counts places the selection, as
+// in the CTA form above.
 constexpr int kWarpRows = 8;            // rows (warps) per CTA
 constexpr int kWarpTopkMax = 128;       // largest k of the warp form
+constexpr int kExtractMaxK = 32;        // largest k found by extraction
+
+// Sorts 8 keys into descending order (Batcher's odd-even merge network,
+// 19 compare-exchanges).
+__device__ __forceinline__ void sort8_desc(uint32_t (&v)[8]) {
+  constexpr int kNet[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6},
+                               {5, 7}, {1, 2}, {5, 6}, {0, 4}, {1, 5}, {2, 6}, {3, 7},
+                               {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+  for (int c = 0; c < 19; ++c) {
+    const uint32_t a = v[kNet[c][0]], b = v[kNet[c][1]];
+    v[kNet[c][0]] = max(a, b);
+    v[kNet[c][1]] = min(a, b);
+  }
+}
 
 template <int KPL>
 __global__ void __launch_bounds__(kWarpRows * 32) topk_table_kernel_warp(const TopkLaunch p) {
@@ -428,15 +447,37 @@ __global__ void __launch_bounds__(kWarpRows * 32) topk_table_kernel_warp(const T
       const int blk = KPL * lane + i;
       key[i] = blk < n ? score_key(srow[blk]) : 0u;  // 0 ranks below every candidate
     }
-    // ---- the k-th largest key T, bit by bit from the top
+    // ---- the k-th largest key T
     uint32_t T = 0;
-#pragma unroll 1
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t cand = T | (1u << bit);
-      int c = 0;
+    if (KPL == 8 && k <= kExtractMaxK) {
+      // k rounds of extraction: each lane's keys sorted, the largest head
+      // taken per round (ties: any holder; only the value matters)
+      uint32_t h[8];
 #pragma unroll
-      for (int i = 0; i < KPL; ++i) c += key[i] >= cand;
-      if (__reduce_add_sync(full, c) >= k) T = cand;
+      for (int i = 0; i < 8; ++i) h[i] = key[i % KPL];
+      sort8_desc(h);
+#pragma unroll 1
+      for (int t = 0; t < k; ++t) {
+        T = __reduce_max_sync(full, h[0]);
+        if (T == 0u) break;  // every key left is 0: so is the k-th
+        const unsigned holders = __ballot_sync(full, h[0] == T);
+        if (lane == __ffs(holders) - 1) {
+#pragma unroll
+          for (int i = 0; i < 7; ++i) h[i] = h[i + 1];
+          h[7] = 0u;
+        }
+      }
+    } else {
+      // bit by bit from the top: T takes a bit whenever at least k keys are
+      // >= the candidate
+#pragma unroll 1
+      for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = T | (1u << bit);
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) c += key[i] >= cand;
+        if (__reduce_add_sync(full, c) >= k) T = cand;
+      }
     }
     // ---- keys > T, then the lowest-indexed keys == T until k are taken
     int my_gt = 0, my_eq = 0;

@@ -282,16 +282,18 @@ def test_many_rows_single_split(msa, orc):
     check_against_oracle(orc, w, sep, fused)
 
 
-@pytest.mark.parametrize("long_seq", [20_000, 60_000, 120_000])
-def test_many_rows_warp_topk(msa, orc, long_seq):
+@pytest.mark.parametrize("long_seq,topk", [(20_000, 8), (60_000, 8), (120_000, 8),
+                                           (20_000, 32), (20_000, 48)])
+def test_many_rows_warp_topk(msa, orc, long_seq, topk):
     # >= 512 rows take the warp-per-row top-k; the longest request sets the
     # block-table width (157 / 469 / 938 blocks: 8, 16 or 32 keys per lane).
-    # Index values in {-1, 0, 1} make many blocks tie at the threshold; an
-    # empty request, a request with a page outside the pool and rows that
-    # see fewer blocks than k are in the same batch.
+    # With 8 keys a lane, k <= 32 is found by extraction and k = 48 by the
+    # bit search.  Index values in {-1, 0, 1} make many blocks tie at the
+    # threshold; an empty request, a request with a page outside the pool
+    # and rows that see fewer blocks than k are in the same batch.
     q_lens = [400, 0, 100, 6, 10, 3]
     seq = [2600, 50, 1500, long_seq, 9000, 300]
-    w = W.custom(61, q_lens=q_lens, seq_lens=seq, hq=8, di=64, idx_range=1, topk=8,
+    w = W.custom(61, q_lens=q_lens, seq_lens=seq, hq=8, di=64, idx_range=1, topk=topk,
                  kv_dtype=W.KV_BF16, with_sink=True)
     bt = w.block_table.copy()
     bt[2, 3] = w.num_pages + 1
@@ -303,6 +305,33 @@ def test_many_rows_warp_topk(msa, orc, long_seq):
         assert np.array_equal(sep[key], ref[key]), key
     assert_attn_close(sep["out"], sep["lse"], ref["out"], ref["lse"])
     check_fused(w, sep, fused, ref)
+
+
+@pytest.mark.parametrize("topk", [4, 16, 32, 48])
+def test_warp_topk_crafted_scores(msa, orc, topk):
+    # the warp-per-row top-k (>= 512 rows) on scores written directly: NaN,
+    # -inf, +inf and a few repeated values, so the k-th largest key sits in
+    # a run of ties or among NaNs (NaN ranks below -inf); rows of the second
+    # request see fewer blocks than k.  k <= 32 takes the extraction, 48 the
+    # bit search; the selection, the table and the length equal the
+    # oracle's bit for bit.
+    w = W.custom(66, q_lens=[600, 20], seq_lens=[20000, 300], hq=8, di=64, topk=topk,
+                 kv_dtype=W.KV_BF16)
+    c = msa.DeviceCase(w)
+    rng = np.random.default_rng(topk)
+    vals = np.array([np.nan, -np.inf, np.inf, 0.0, 1.0, 2.0, -1.0, 3.5], np.float32)
+    sc = vals[rng.integers(0, len(vals), size=tuple(c.scores.shape))]
+    sc[::7] = np.nan  # rows that are mostly NaN: the k-th key is a NaN's
+    sc[::7, :5] = 1.0
+    c.scores.copy_(torch.from_numpy(sc))
+    c.topk_build_table()
+    res = c.fetch()
+    ref_idx, ref_tbl, ref_len, st = orc.topk_build_table(orc.Batch.of(w), sc, topk,
+                                                         tbl_stride=c.tbl_stride)
+    assert st == 0 and res["status"] == 0
+    assert np.array_equal(res["topk_idx"], ref_idx)
+    assert np.array_equal(res["tbl"], ref_tbl)
+    assert np.array_equal(res["sparse_len"], ref_len)
 
 
 # ------------------------------------------------ block-major prefill path
