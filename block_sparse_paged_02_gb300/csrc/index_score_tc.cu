@@ -17,10 +17,10 @@
 //
 // Work = the flat list of (request, 128-row tile, pair of consecutive
 // blocks) items, split evenly across a persistent grid of one CTA per SM.
-// Two blocks per MMA: the issuing thread spends ~100 cycles on each
-// tcgen05.mma whatever its size, and an M128 N128 K16 step keeps the
-// tensor pipe busy for only 64, so with one block per MMA the pipe waited
-// on the issue; M128 N256 gives it 128 cycles of work per instruction.
+// Two blocks per MMA: with one block per MMA the issuing thread spent ~100
+// cycles on each M128 N128 K16 tcgen05.mma, a step that keeps the tensor
+// pipe busy for only 64, so the pipe waited on the issue; an M128 N256 step
+// carries 128 cycles of work per instruction.
 // CTA roles:
 //   warp 0  TMA producer: the two K blocks of each item, 128-byte-swizzled
 //           tiles via cp.async.bulk.tensor into a 4-slot ring, mbarrier
