@@ -50,7 +50,16 @@ enum { kFmaBf16 = 0, kMmaBf16 = 1, kMmaFp8 = 2 };
 #define MSA_SCORE_PRODUCERS_FP8 2
 #endif
 
-template <int DI, int HI, int KIND>
+// Shared-memory budget of the stage ring: 200 KB leaves room for the
+// request prefix of the largest batches; e4m3 pages (~18.5 KB a stage) take
+// a second build of the kernel with a 222 KB ring (12 stages instead of 10)
+// whenever the batch's prefix still fits beside it: the ring is what hides
+// the copy latency (a stage is held for a page's load plus its scoring).
+constexpr int kStageBudget = 204800;
+constexpr int kStageBudgetWide = 227328;
+constexpr size_t kMaxDynSmem = 232448;  // the opt-in limit per CTA (227 KB)
+
+template <int DI, int HI, int KIND, int BUDGET = kStageBudget>
 struct ScoreCfg {
   static constexpr int kProducers = KIND == kMmaFp8 ? MSA_SCORE_PRODUCERS_FP8 : MSA_SCORE_PRODUCERS;
   static constexpr int kElem = KIND == kMmaFp8 ? 1 : 2;
@@ -61,11 +70,11 @@ struct ScoreCfg {
   static constexpr int kRows = KIND == kMmaFp8 ? 8 / HI : kRowGroup;
   static constexpr int kQBytes = kRows * HI * DI * 2;  // query rows staged with a page
   static constexpr int kScaleBytes = KIND == kMmaFp8 ? kBlock * HI * 4 : 0;  // per-token scales
-  // stages within 200 KB (the rest holds barriers and the request prefix):
-  // 6 for 32 KB pages, 10-12 for 16 KB ones
+  // stages within the budget (the rest holds barriers and the request
+  // prefix): 6 for 32 KB pages, 10-12 for 16 KB ones
   static constexpr int kStageBytes = kPageBytes + kQBytes + kScaleBytes;
   static constexpr int kStages =
-      (204800 / kStageBytes < 12 ? 204800 / kStageBytes : 12) / kProducers * kProducers;
+      (BUDGET / kStageBytes < 12 ? BUDGET / kStageBytes : 12) / kProducers * kProducers;
   // one consumer warp per stage (a pair of warps per page measured slower:
   // more instructions without more bytes in flight)
   static constexpr int kThreads = 32 * (kProducers + kStages);
@@ -86,9 +95,9 @@ struct StageInfo {  // written by the producer before it arms the stage
   int req, blk, valid, q0, qlen, ctx, jstart, pad;
 };
 
-template <int DI, int HI, int KIND>
+template <int DI, int HI, int KIND, int BUDGET = kStageBudget>
 struct ScoreSmem {
-  using C = ScoreCfg<DI, HI, KIND>;
+  using C = ScoreCfg<DI, HI, KIND, BUDGET>;
   static constexpr size_t kPages = 0;
   static constexpr size_t kQ = kPages + (size_t)C::kStages * C::kPageBytes;
   static constexpr size_t kScale = kQ + (size_t)C::kStages * C::kQBytes;
@@ -304,11 +313,11 @@ __device__ __forceinline__ void score_page_mma(const uint8_t* page, const float*
   }
 }
 
-template <int DI, int HI, int KIND>
-__global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
+template <int DI, int HI, int KIND, int BUDGET>
+__global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND, BUDGET>::kThreads, 1)
     index_score_kernel(const ScoreLaunch p, const __grid_constant__ CUtensorMap kmap) {
-  using C = ScoreCfg<DI, HI, KIND>;
-  using S = ScoreSmem<DI, HI, KIND>;
+  using C = ScoreCfg<DI, HI, KIND, BUDGET>;
+  using S = ScoreSmem<DI, HI, KIND, BUDGET>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
   uint64_t* empty = full + C::kStages;
@@ -551,11 +560,11 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND>::kThreads, 1)
   }
 }
 
-template <int DI, int HI, int KIND>
+template <int DI, int HI, int KIND, int BUDGET = kStageBudget>
 cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
-  using C = ScoreCfg<DI, HI, KIND>;
-  const size_t smem = ScoreSmem<DI, HI, KIND>::bytes(p.batch.num_reqs);
-  auto kern = index_score_kernel<DI, HI, KIND>;
+  using C = ScoreCfg<DI, HI, KIND, BUDGET>;
+  const size_t smem = ScoreSmem<DI, HI, KIND, BUDGET>::bytes(p.batch.num_reqs);
+  auto kern = index_score_kernel<DI, HI, KIND, BUDGET>;
   CUtensorMap kmap;
   memset(&kmap, 0, sizeof(kmap));
   if constexpr (kSwizzledPages<DI, HI, KIND>) {
@@ -577,6 +586,15 @@ cudaError_t launch_cfg(const ScoreLaunch& p, cudaStream_t stream) {
 
 template <int KIND>
 cudaError_t launch_kind(const ScoreLaunch& p, cudaStream_t stream) {
+  if constexpr (KIND == kMmaFp8) {  // the wider ring when the prefix fits beside it
+    const int R = p.batch.num_reqs;
+    if (p.index_heads == 1 && p.index_dim == 128 &&
+        ScoreSmem<128, 1, KIND, kStageBudgetWide>::bytes(R) <= kMaxDynSmem)
+      return launch_cfg<128, 1, KIND, kStageBudgetWide>(p, stream);
+    if (p.index_heads == 2 && p.index_dim == 64 &&
+        ScoreSmem<64, 2, KIND, kStageBudgetWide>::bytes(R) <= kMaxDynSmem)
+      return launch_cfg<64, 2, KIND, kStageBudgetWide>(p, stream);
+  }
   if (p.index_heads == 1 && p.index_dim == 128) return launch_cfg<128, 1, KIND>(p, stream);
   if (p.index_heads == 1 && p.index_dim == 64) return launch_cfg<64, 1, KIND>(p, stream);
   if (p.index_heads == 2 && p.index_dim == 64) return launch_cfg<64, 2, KIND>(p, stream);

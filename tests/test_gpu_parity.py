@@ -242,6 +242,19 @@ def test_fp8_index_cache(msa, orc, hi, di, scaled):
     check_against_oracle(orc, w, sep, fused)  # scores included, bit for bit
 
 
+@pytest.mark.parametrize("reqs", [64, 1200])
+def test_fp8_index_ring_sizes(msa, orc, reqs):
+    # e4m3 pages of 128 dims: the 12-stage ring while the batch's request
+    # prefix fits beside it (64 requests), the 10-stage ring beyond that
+    # (1200 requests); scores, selection and attention against the oracle
+    rng = np.random.default_rng(reqs)
+    seq = [int(x) for x in rng.integers(100, 1400, size=reqs)]
+    w = W.fp8_index(W.custom(90, q_lens=[1] * reqs, seq_lens=seq, hq=8, di=128, topk=2,
+                             kv_dtype=W.KV_FP8, scale_mode=W.SCALE_SCALAR), seed=91)
+    _, sep, fused = run_steps(msa, w)
+    check_against_oracle(orc, w, sep, fused)
+
+
 def test_fp8_index_many_rows_and_garbage(msa, orc):
     # a request with >= 64 rows (no tensor-core scorer for e4m3 keys) and NaN
     # codes in every slot no row may see
