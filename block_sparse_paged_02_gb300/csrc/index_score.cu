@@ -39,8 +39,12 @@ constexpr int kRowGroup = 4;
 constexpr int kMmaMinRows = 2;
 
 // Scoring kinds: bf16 keys on CUDA-core FMAs, bf16 keys on warp MMA, OCP
-// e4m3 keys on warp MMA (fp16 operands).
-enum { kFmaBf16 = 0, kMmaBf16 = 1, kMmaFp8 = 2 };
+// e4m3 keys on warp MMA (fp16 operands), and bf16 keys on warp MMA with two
+// consumer warps per stage, each scoring half of a page's token tiles: one
+// warp takes ~4.9 K cycles for a 32 KiB page, about as long as the page's
+// copy, and a stage is held for both, so halving the scoring lets the
+// 6-page ring turn over faster.
+enum { kFmaBf16 = 0, kMmaBf16 = 1, kMmaFp8 = 2, kMmaBf16Pair = 3 };
 
 // producer warps of the score kernel (each issues every kProducers-th item)
 #ifndef MSA_SCORE_PRODUCERS
@@ -75,9 +79,11 @@ struct ScoreCfg {
   static constexpr int kStageBytes = kPageBytes + kQBytes + kScaleBytes;
   static constexpr int kStages =
       (BUDGET / kStageBytes < 12 ? BUDGET / kStageBytes : 12) / kProducers * kProducers;
-  // one consumer warp per stage (a pair of warps per page measured slower:
-  // more instructions without more bytes in flight)
-  static constexpr int kThreads = 32 * (kProducers + kStages);
+  // consumer warps per stage: one (for the FMA scorer a pair of warps per
+  // page measured slower: more instructions without more bytes in flight),
+  // two for kMmaBf16Pair
+  static constexpr int kCps = KIND == kMmaBf16Pair ? 2 : 1;
+  static constexpr int kThreads = 32 * (kProducers + kStages * kCps);
   static_assert(kStages % kProducers == 0, "every stage needs a single producer");
 };
 
@@ -95,6 +101,22 @@ struct StageInfo {  // written by the producer before it arms the stage
   int req, blk, valid, q0, qlen, ctx, jstart, pad;
 };
 
+// The two consumer warps of one stage (named barrier 1 + stage, 64 threads):
+// AND of a predicate over both, and a plain rendezvous.
+__device__ __forceinline__ bool pair_and(bool v, int id) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, 64, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
 template <int DI, int HI, int KIND, int BUDGET = kStageBudget>
 struct ScoreSmem {
   using C = ScoreCfg<DI, HI, KIND, BUDGET>;
@@ -104,7 +126,10 @@ struct ScoreSmem {
   static constexpr size_t kBars = kScale + (size_t)C::kStages * C::kScaleBytes;
   static constexpr size_t kInfo = kBars + 2 * C::kStages * sizeof(uint64_t);
   static constexpr size_t kMisc = kInfo + C::kStages * sizeof(StageInfo);
-  static constexpr size_t kPrefix = kMisc + 64;
+  // two consumers per stage: the second one's row maxima, by row-group parity
+  static constexpr size_t kRed = kMisc + 64;
+  static constexpr size_t kPrefix =
+      kRed + (C::kCps == 2 ? (size_t)C::kStages * 2 * kRowGroup * sizeof(float) : 0);
   static size_t bytes(int num_reqs) { return kPrefix + (size_t)(num_reqs + 1) * sizeof(int); }
 };
 
@@ -193,14 +218,14 @@ __device__ __forceinline__ uint2 lds64(const void* p) {
 template <int DI, int HI, bool F8, bool SWZ>
 __device__ __forceinline__ void score_page_mma(const uint8_t* page, const float* tscale,
                                                const uint8_t* q_s, int nr, int lane, int blk,
-                                               const int (&pos)[8], float (&best)[8]) {
+                                               const int (&pos)[8], float (&best)[8],
+                                               int mt0, int mt1) {
   constexpr int kK = DI / 16;                 // k-steps
   constexpr int kD4 = DI / 4;                 // dims of a lane per sub-row
   constexpr int kElem = F8 ? 1 : 2;
   constexpr int kRowB = DI * kElem;           // bytes per sub-row
   constexpr int kSpanW = kD4 * kElem / 4;     // 32-bit words of a lane's span
   constexpr int kSpanC = kSpanW / 4;          // 16-byte chunks of a lane's span
-  constexpr int kMt = kBlock * HI / 16;       // m-tiles
   const int g = lane >> 2, c = lane & 3;
   // B: column g = (query row g / HI, index head g % HI)
   uint32_t bq[kK][2];
@@ -238,7 +263,7 @@ __device__ __forceinline__ void score_page_mma(const uint8_t* page, const float*
   const bool whole = (!live[0] || lim[0] >= kBlock - 1) && (!live[1] || lim[1] >= kBlock - 1);
   float m[2] = {-INFINITY, -INFINITY};
 #pragma unroll 2
-  for (int mt = 0; mt < kMt; ++mt) {
+  for (int mt = mt0; mt < mt1; ++mt) {
     // spans of sub-rows 16mt + g and 16mt + g + 8.  Unswizzled, lanes of one
     // column group read the same bytes of rows a page row apart (bank
     // conflicts; rotating the read order per lane would need run-time
@@ -340,7 +365,7 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND, BUDGET>::kThreads, 1)
   }
   if (tid < C::kStages) {
     mbar_init(&full[tid], 1);
-    mbar_init(&empty[tid], 1);
+    mbar_init(&empty[tid], C::kCps);
   }
   fence_barrier_init();
   __syncthreads();
@@ -492,13 +517,24 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND, BUDGET>::kThreads, 1)
     return;
   }
 
-  // ---- consumers: warp kProducers + s owns stage s
-  const int st = warp - C::kProducers;
+  // ---- consumers: warps kProducers + kCps s .. + kCps - 1 own stage s; with
+  // two, warp `part` scores m-tiles [part, part + 1) * kMt / 2 of each page
+  // and the pair joins its row maxima through shared memory.  The pair
+  // decides together whether to go on (a timed-out wait ends both), so
+  // neither is left at their barrier.
+  constexpr int kCps = C::kCps;
+  constexpr int kMt = kBlock * HI / 16;  // m-tiles of a page
+  const int st = (warp - C::kProducers) / kCps, part = (warp - C::kProducers) % kCps;
+  const int bar_id = 1 + st;
+  const int mt0 = part * (kMt / kCps), mt1 = mt0 + kMt / kCps;
   const uint8_t* page = smem + S::kPages + (size_t)st * C::kPageBytes;
   uint8_t* q_s = smem + S::kQ + (size_t)st * C::kQBytes;
+  float* red = reinterpret_cast<float*>(smem + S::kRed) + st * 2 * kRowGroup;
   for (int j = st, use = 0; j < n_items; j += C::kStages, ++use) {
     // warp-uniform: the page is scored with warp shuffles
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], use & 1))) {
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&full[st], use & 1));
+    if constexpr (kCps == 2) ok = pair_and(ok, bar_id);
+    if (!ok) {
       if (lane == 0) atomicOr(p.status, MSA_DEV_TIMEOUT);
       break;
     }
@@ -506,7 +542,7 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND, BUDGET>::kThreads, 1)
     const int q0 = si.q0, qlen = si.qlen, ctx = si.ctx;
     bool wrote_q = false;
     // rows j >= jstart (ctx + j >= 128*blk) can see this block
-    for (int g0 = si.jstart; g0 < qlen; g0 += C::kRows) {
+    for (int g0 = si.jstart, grp = 0; g0 < qlen; g0 += C::kRows, ++grp) {
       const int nr = min(C::kRows, qlen - g0);
       int pos[8];
 #pragma unroll
@@ -514,14 +550,18 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND, BUDGET>::kThreads, 1)
       float best[8];
       if (si.valid) {
         if (g0 != si.jstart) {  // later row groups (requests with > 4 rows): from global
-          __syncwarp();
-          const int chunks = nr * HI * DI / 8;
-          const uint4* src = reinterpret_cast<const uint4*>(
-              p.idx_q + (long long)(q0 + g0) * HI * DI);
-          for (int c = lane; c < chunks; c += 32)
-            *reinterpret_cast<uint4*>(q_s + c * 16) = src[c];
-          __syncwarp();
-          wrote_q = true;
+          if constexpr (kCps == 2) pair_sync(bar_id);  // both have read the previous rows
+          if (part == 0) {
+            __syncwarp();
+            const int chunks = nr * HI * DI / 8;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.idx_q + (long long)(q0 + g0) * HI * DI);
+            for (int c = lane; c < chunks; c += 32)
+              *reinterpret_cast<uint4*>(q_s + c * 16) = src[c];
+            __syncwarp();
+            wrote_q = true;
+          }
+          if constexpr (kCps == 2) pair_sync(bar_id);  // the rows are there for both
         }
         if constexpr (KIND == kFmaBf16) {
           int pos4[kRowGroup];
@@ -541,17 +581,33 @@ __global__ void __launch_bounds__(ScoreCfg<DI, HI, KIND, BUDGET>::kThreads, 1)
               ? reinterpret_cast<const float*>(smem + S::kScale + (size_t)st * C::kScaleBytes)
               : nullptr;
           score_page_mma<DI, HI, KIND == kMmaFp8, kSwizzledPages<DI, HI, KIND>>(
-              page, tscale, q_s, nr, lane, si.blk, pos,
-                                                  best);
+              page, tscale, q_s, nr, lane, si.blk, pos, best, mt0, mt1);
         }
       } else {
 #pragma unroll
         for (int r = 0; r < 8; ++r) best[r] = -INFINITY;
       }
+      if constexpr (kCps == 2) {
+        // the second warp's maxima to the first (slots by row-group parity:
+        // the first has read group g's before either passes group g + 1's
+        // rendezvous)
+        float* slot = red + (grp & 1) * kRowGroup;
+        if (part == 1 && lane == 0) {
 #pragma unroll
-      for (int r = 0; r < C::kRows; ++r)
-        if (lane == r && r < nr)
-          p.scores[(long long)(q0 + g0 + r) * p.score_stride + si.blk] = best[r];
+          for (int r = 0; r < kRowGroup; ++r) slot[r] = best[r];
+        }
+        pair_sync(bar_id);
+        if (part == 0) {
+#pragma unroll
+          for (int r = 0; r < kRowGroup; ++r) best[r] = fmaxf(best[r], slot[r]);  // NaN never wins
+        }
+      }
+      if (part == 0) {
+#pragma unroll
+        for (int r = 0; r < C::kRows; ++r)
+          if (lane == r && r < nr)
+            p.scores[(long long)(q0 + g0 + r) * p.score_stride + si.blk] = best[r];
+      }
     }
     // the next bulk copy into q_s must follow this warp's own writes to it
     if (wrote_q) fence_proxy_async_smem();
@@ -609,7 +665,7 @@ cudaError_t launch_index_score(const ScoreLaunch& p, cudaStream_t stream) {
   // several rows (speculative decode) multiply the FMA work per byte, and
   // the warp MMA scorer takes them
   if (MSA_SCORE_BF16_KIND == 1 || p.batch.max_q_len >= kMmaMinRows)
-    return launch_kind<kMmaBf16>(p, stream);
+    return launch_kind<kMmaBf16Pair>(p, stream);
   return launch_kind<kFmaBf16>(p, stream);
 }
 
