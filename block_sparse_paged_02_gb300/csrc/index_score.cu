@@ -38,13 +38,13 @@ constexpr int kRowGroup = 4;
 // bf16 keys: requests of at least this many rows (max_q_len hint) -> MMA scorer
 constexpr int kMmaMinRows = 2;
 
-// Scoring kinds: bf16 keys on CUDA-core FMAs, bf16 keys on warp MMA, OCP
-// e4m3 keys on warp MMA (fp16 operands), and bf16 keys on warp MMA with two
-// consumer warps per stage, each scoring half of a page's token tiles: one
-// warp takes ~4.9 K cycles for a 32 KiB page, about as long as the page's
-// copy, and a stage is held for both, so halving the scoring lets the
-// 6-page ring turn over faster.
-enum { kFmaBf16 = 0, kMmaBf16 = 1, kMmaFp8 = 2, kMmaBf16Pair = 3 };
+// Scoring kinds: bf16 keys on CUDA-core FMAs, OCP e4m3 keys on warp MMA
+// (fp16 operands), and bf16 keys on warp MMA with two consumer warps per
+// stage, each scoring half of a page's token tiles (one warp took ~4.9 K
+// cycles for a 32 KiB page, about as long as the page's copy, and a stage
+// is held for both, so halving the scoring lets the 6-page ring turn over
+// faster).
+enum { kFmaBf16 = 0, kMmaFp8 = 2, kMmaBf16Pair = 3 };
 
 // producer warps of the score kernel (each issues every kProducers-th item)
 #ifndef MSA_SCORE_PRODUCERS
